@@ -1,0 +1,180 @@
+"""Byte layout of one cache page of one KV head, restated from the library's
+documented format (test infrastructure only; shares no code with the CUDA
+path).
+
+The pages fix the tile (128 tokens, or 64 for the finer variant: KVarN review,
+paragraph on kvarn_k4v2_g128), 4-bit keys and 2-bit values (same paragraph),
+and a paged cache (vLLM block tables). Everything below the tile is this
+library's own format. A page holds P = 16 tokens of one KV head:
+
+  K codes   8*D bytes   4-bit, token-major; within a token, four lane chunks
+                        of D/8 bytes; chunk t holds, for every 16-channel
+                        k-chunk kc, channels 16kc + {2t, 2t+1, 2t+8, 2t+9}.
+                        Word w of a chunk serves k-chunks 2w and 2w+1; its
+                        nibble n (bits 4n..4n+3) holds channel
+                        16*(2w + (n%4)//2) + 2t + 8*(n%2) + (n//4).
+  V codes   4*D bytes   2-bit; lane chunk L = 4g + t (D/8 bytes) holds
+                        channels 8nc + g for every 8-channel block nc, at
+                        tokens {2t, 2t+1, 2t+8, 2t+9}. Word w of a chunk
+                        serves blocks 4w..4w+3; the token tau = 2t + e + 8h of
+                        block nc sits at bit 2*(2*(nc%4) + h) + 16*e.
+  K a[16], K b[16], V a[16], V b[16]   fp32 row scales of the 16 tokens
+  K col     D*P/N fp32  column scales c of the page's slice of the tile
+  V col     D*P/N fp32
+The page at logical index l of a sequence carries the column scales of
+channels [(l mod N/P) * D*P/N, +D*P/N) of its tile; all words little-endian.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+P = 16  # tokens per page
+
+
+class DenseLayout:
+    def __init__(self, D: int, N: int, k_bits: int = 4, v_bits: int = 2):
+        if (k_bits, v_bits) != (4, 2):
+            raise ValueError("the page format is defined for 4-bit K and 2-bit V")
+        if N % P:
+            raise ValueError("tile must be a whole number of pages")
+        self.D, self.N = D, N
+        self.k_codes = 0
+        self.v_codes = 8 * D
+        self.k_a = 12 * D
+        self.k_b = self.k_a + 4 * P
+        self.v_a = self.k_b + 4 * P
+        self.v_b = self.v_a + 4 * P
+        self.col_per_page = D * P // N
+        self.k_col = self.v_b + 4 * P
+        self.v_col = self.k_col + 4 * self.col_per_page
+        self.page_bytes = self.v_col + 4 * self.col_per_page
+
+
+def k_code_position(D: int, tau: int, j: int):
+    """(byte offset inside the K-code region, bit shift) of token tau, channel j."""
+    kc, r = divmod(j, 16)
+    t = (r % 8) // 2
+    e = r % 2          # second element of the pair
+    h = r // 8         # upper 8 channels of the k-chunk
+    w, kp = divmod(kc, 2)
+    n = 2 * kp + h + 4 * e
+    byte = tau * (D // 2) + t * (D // 8) + 4 * w + n // 2
+    return byte, 4 * (n % 2)
+
+
+def v_code_position(D: int, tau: int, j: int):
+    """(byte offset inside the V-code region, bit shift) of token tau, channel j."""
+    nc, g = divmod(j, 8)
+    t = (tau % 8) // 2
+    e = tau % 2
+    h = tau // 8
+    L = 4 * g + t
+    w, ncl = divmod(nc, 4)
+    bit = 2 * (2 * ncl + h) + 16 * e
+    byte = L * (D // 8) + 4 * w + bit // 8
+    return byte, bit % 8
+
+
+@functools.lru_cache(maxsize=None)
+def _maps(D: int):
+    kb = np.zeros((P, D), dtype=np.int64)
+    ks = np.zeros((P, D), dtype=np.int64)
+    vb = np.zeros((P, D), dtype=np.int64)
+    vs = np.zeros((P, D), dtype=np.int64)
+    for tau in range(P):
+        for j in range(D):
+            kb[tau, j], ks[tau, j] = k_code_position(D, tau, j)
+            vb[tau, j], vs[tau, j] = v_code_position(D, tau, j)
+    return kb, ks, vb, vs
+
+
+def pack_codes(codes: np.ndarray, kind: str) -> np.ndarray:
+    """Pack a [16, D] code block of one page into its region bytes."""
+    D = codes.shape[1]
+    kb, ks, vb, vs = _maps(D)
+    byte, shift, nbytes = (kb, ks, 8 * D) if kind == "k" else (vb, vs, 4 * D)
+    out = np.zeros(nbytes, dtype=np.int64)
+    np.bitwise_or.at(out, byte.ravel(), (codes.astype(np.int64) << shift).ravel())
+    return out.astype(np.uint8)
+
+
+def unpack_codes(region: np.ndarray, D: int, kind: str) -> np.ndarray:
+    kb, ks, vb, vs = _maps(D)
+    byte, shift, mask = (kb, ks, 0xF) if kind == "k" else (vb, vs, 0x3)
+    return (region.astype(np.int64)[byte] >> shift) & mask
+
+
+def f32_bytes(x) -> np.ndarray:
+    return np.asarray(x, dtype="<f4").view(np.uint8)
+
+
+def f32_from(region: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(region).view("<f4").astype(np.float64)
+
+
+def write_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int,
+               enc_k: dict, enc_v: dict) -> None:
+    """Store the encodings of one K tile and one V tile (N tokens) into the
+    N/P physical pages ``phys_pages`` of KV head ``head``.
+
+    cache: uint8 [num_pages, Hkv, page_bytes].
+    """
+    D, N, cpp = lay.D, lay.N, lay.col_per_page
+    for p, phys in enumerate(phys_pages):
+        pg = cache[phys, head]
+        rows = slice(p * P, (p + 1) * P)
+        cols = slice(p * cpp, (p + 1) * cpp)
+        pg[lay.k_codes:lay.k_codes + 8 * D] = pack_codes(enc_k["codes"][rows], "k")
+        pg[lay.v_codes:lay.v_codes + 4 * D] = pack_codes(enc_v["codes"][rows], "v")
+        pg[lay.k_a:lay.k_a + 4 * P] = f32_bytes(enc_k["a"][rows])
+        pg[lay.k_b:lay.k_b + 4 * P] = f32_bytes(enc_k["b"][rows])
+        pg[lay.v_a:lay.v_a + 4 * P] = f32_bytes(enc_v["a"][rows])
+        pg[lay.v_b:lay.v_b + 4 * P] = f32_bytes(enc_v["b"][rows])
+        pg[lay.k_col:lay.k_col + 4 * cpp] = f32_bytes(enc_k["c"][cols])
+        pg[lay.v_col:lay.v_col + 4 * cpp] = f32_bytes(enc_v["c"][cols])
+
+
+def read_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int):
+    """Inverse of write_tile: returns (K dict, V dict) of codes [N, D] and
+    float64 copies of the stored fp32 a [N], b [N], c [D]."""
+    D, cpp = lay.D, lay.col_per_page
+    out = {}
+    for kind in ("k", "v"):
+        codes, a, b, c = [], [], [], []
+        for phys in phys_pages:
+            pg = cache[phys, head]
+            if kind == "k":
+                codes.append(unpack_codes(pg[lay.k_codes:lay.k_codes + 8 * D], D, "k"))
+                a.append(f32_from(pg[lay.k_a:lay.k_a + 4 * P]))
+                b.append(f32_from(pg[lay.k_b:lay.k_b + 4 * P]))
+                c.append(f32_from(pg[lay.k_col:lay.k_col + 4 * cpp]))
+            else:
+                codes.append(unpack_codes(pg[lay.v_codes:lay.v_codes + 4 * D], D, "v"))
+                a.append(f32_from(pg[lay.v_a:lay.v_a + 4 * P]))
+                b.append(f32_from(pg[lay.v_b:lay.v_b + 4 * P]))
+                c.append(f32_from(pg[lay.v_col:lay.v_col + 4 * cpp]))
+        out[kind] = dict(codes=np.concatenate(codes), a=np.concatenate(a),
+                         b=np.concatenate(b), c=np.concatenate(c))
+    return out["k"], out["v"]
+
+
+# --------------------------------------------------------------------------
+# MLA latent page: one shared latent of width Dl (4-bit codes, K = V) plus an
+# fp16 rope part of width R, 16 tokens per page.
+#   latent codes  8*Dl bytes   same placement as the dense K codes
+#   rope          2*R*P bytes  fp16, token-major
+#   a[16], b[16]  fp32
+#   col           Dl*P/N fp32  column-scale slice, as for the dense page
+# --------------------------------------------------------------------------
+class LatentLayout:
+    def __init__(self, Dl: int, R: int, N: int):
+        self.D, self.R, self.N = Dl, R, N
+        self.codes = 0
+        self.rope = 8 * Dl
+        self.a = self.rope + 2 * R * P
+        self.b = self.a + 4 * P
+        self.col_per_page = Dl * P // N
+        self.col = self.b + 4 * P
+        self.page_bytes = self.col + 4 * self.col_per_page

@@ -1,0 +1,181 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each case below plants one mistake in the oracle (a dropped term, a wrong sign
+or index, a swapped operand or order) by patching a function of the oracle
+package, runs the pin tests of test_oracle_codec, test_oracle_layout and
+test_oracle_attention, and expects at least one pin to fail. Everything runs
+on the CPU; nothing here touches the CUDA path.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention, codec, layout
+from tests import test_oracle_attention as ta
+from tests import test_oracle_codec as tc
+from tests import test_oracle_layout as tl
+
+PINS = [
+    (tc.test_hadamard_matches_scipy_sylvester, dict(D=128)),
+    (tc.test_hadamard_orthonormal_and_symmetric, dict(D=128)),
+    (tc.test_rotation_preserves_scores, dict(D=128)),
+    (tc.test_rotation_tiny_by_hand, {}),
+    (tc.test_sinkhorn_closed_form, {}),
+    (tc.test_normalize_reconstructs_exactly, {}),
+    (tc.test_normalize_rows_have_unit_std, dict(T=2)),
+    (tc.test_column_pass_gives_unit_column_std, {}),
+    (tc.test_normalize_columns_converge_toward_one, {}),
+    (tc.test_rtn_hand_worked_rows, {}),
+    (tc.test_rtn_range_endpoints_and_error_bound, dict(bits=4)),
+    (tc.test_reconstruction_error_shrinks_with_bits, {}),
+    (tc.test_dequantize_roundtrip_is_exact_without_rounding, {}),
+    (tl.test_page_bytes_hand_derived, {}),
+    (tl.test_write_read_tile_roundtrip, {}),
+    (ta.test_softmax_attention_matches_scipy, {}),
+    (ta.test_softmax_attention_two_tokens_by_hand, {}),
+    (ta.test_decode_equals_rotated_space_computation, {}),
+    (ta.test_tail_only_sequence_is_plain_attention, {}),
+    (ta.test_mla_decode_rope_and_shared_latent, {}),
+]
+
+
+def _pins_fail():
+    for fn, kw in PINS:
+        try:
+            fn(**kw)
+        except AssertionError:
+            return fn.__name__
+    return None
+
+
+def _hadamard_unscaled(orig):
+    return lambda D: orig(D) * np.sqrt(D)
+
+
+def _hadamard_wrong_sign(orig):
+    def H(D):
+        M = np.ones((1, 1))
+        while M.shape[0] < D:
+            M = np.block([[M, M], [-M, M]])
+        return M / np.sqrt(D)
+    return H
+
+
+def _normalize_row_first(orig):
+    def vn(Y, T):
+        Z = np.array(Y, dtype=np.float64)
+        lr, lc = np.zeros(Z.shape[0]), np.zeros(Z.shape[1])
+        for _ in range(T):
+            Z, a = codec.row_pass(Z)
+            lr += a
+            Z, b = codec.column_pass(Z)
+            lc += b
+        return Z, np.exp(lr), np.exp(lc)
+    return vn
+
+
+def _normalize_swap_scales(orig):
+    def vn(Y, T):
+        Z, r, c = orig(Y, T)
+        return Z, np.resize(c, r.size), np.resize(r, c.size)
+    return vn
+
+
+def _std_sample(orig):
+    def s(Z, axis):
+        v = np.std(Z, axis=axis, ddof=1)
+        return np.where(np.isfinite(v) & (v > 0), v, 1.0)
+    return s
+
+
+def _rtn_floor(orig):
+    def rtn(Z, bits):
+        codes, lo, delta, x = orig(Z, bits)
+        return np.clip(np.floor(x), 0, 2 ** bits - 1).astype(np.int64), lo, delta, x
+    return rtn
+
+
+def _rtn_levels_off_by_one(orig):
+    return _rtn_levels
+
+
+def _rtn_levels(Z, bits):
+    lo, hi = Z.min(1), Z.max(1)
+    delta = (hi - lo) / (2 ** bits)
+    safe = np.where(delta > 0, delta, 1.0)
+    x = (Z - lo[:, None]) / safe[:, None]
+    return np.clip(np.rint(x), 0, 2 ** bits - 1).astype(np.int64), lo, delta, x
+
+
+def _dequant_drop_b(orig):
+    return lambda codes, a, b, c: orig(codes, a, np.zeros_like(np.asarray(b, float)), c)
+
+
+def _dequant_no_unrotate(orig):
+    return lambda codes, a, b, c: codec.dequantize_rotated(codes, a, b, c)
+
+
+def _attention_no_scale(orig):
+    return lambda q, K, V, sm_scale: orig(q, K, V, 1.0)
+
+
+def _k_nibble_order(orig):
+    def pos(D, tau, j):
+        kc, r = divmod(j, 16)
+        t, e, h = (r % 8) // 2, r % 2, r // 8
+        w, kp = divmod(kc, 2)
+        n = kp + 2 * h + 4 * e
+        return tau * (D // 2) + t * (D // 8) + 4 * w + n // 2, 4 * (n % 2)
+    return pos
+
+
+def _v_pair_order(orig):
+    def pos(D, tau, j):
+        nc, g = divmod(j, 8)
+        t, e, h = (tau % 8) // 2, tau % 2, tau // 8
+        w, ncl = divmod(nc, 4)
+        bit = 2 * (2 * ncl + e) + 16 * h
+        return (4 * g + t) * (D // 8) + 4 * w + bit // 8, bit % 8
+    return pos
+
+
+def _wrong_kv_head(orig):
+    def skv(cache, lay, bt_row, seq_len, head, tail_k=None, tail_v=None):
+        return orig(cache, lay, bt_row, seq_len, (head + 1) % cache.shape[1], tail_k, tail_v)
+    return skv
+
+
+def _tail_off_by_one(orig):
+    def skv(cache, lay, bt_row, seq_len, head, tail_k=None, tail_v=None):
+        tk = None if tail_k is None else np.roll(np.asarray(tail_k), -1, axis=0)
+        return orig(cache, lay, bt_row, seq_len, head, tk, tail_v)
+    return skv
+
+
+MUTATIONS = [
+    ("hadamard without 1/sqrt(D)", codec, "hadamard", _hadamard_unscaled),
+    ("hadamard with a wrong sign", codec, "hadamard", _hadamard_wrong_sign),
+    ("row pass before column pass", codec, "variance_normalize", _normalize_row_first),
+    ("row and column scales swapped", codec, "variance_normalize", _normalize_swap_scales),
+    ("sample std instead of population std", codec, "pop_std", _std_sample),
+    ("floor instead of round-to-nearest", codec, "rtn_rows", _rtn_floor),
+    ("2^bits levels instead of 2^bits - 1", codec, "rtn_rows", _rtn_levels_off_by_one),
+    ("offset term b dropped at dequantisation", codec, "dequantize_rotated", _dequant_drop_b),
+    ("output left in the rotated basis", codec, "dequantize", _dequant_no_unrotate),
+    ("softmax scale ignored", attention, "softmax_attention", _attention_no_scale),
+    ("K nibbles in the wrong order", layout, "k_code_position", _k_nibble_order),
+    ("V token halves swapped", layout, "v_code_position", _v_pair_order),
+    ("query head mapped to the wrong KV head", attention, "sequence_kv", _wrong_kv_head),
+    ("tail read one token off", attention, "sequence_kv", _tail_off_by_one),
+]
+
+
+@pytest.mark.parametrize("label,module,name,make", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(monkeypatch, label, module, name, make):
+    assert _pins_fail() is None  # the clean oracle passes every pin
+    monkeypatch.setattr(module, name, make(getattr(module, name)))
+    layout._maps.cache_clear()
+    try:
+        caught = _pins_fail()
+    finally:
+        layout._maps.cache_clear()
+    assert caught is not None, f"no pin caught: {label}"
