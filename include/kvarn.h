@@ -1,0 +1,266 @@
+/*
+ * kvarn.h - C ABI of the GB300 (sm_103a) KVarN KV-cache codec and its
+ * decode attention.
+ *
+ * The method ("KVarN ... vLLM KV cache quantization" review, paragraph on the
+ * four quantisation stages): every fixed tile of N tokens (128, or 64 for the
+ * finer variant) of one KV head is rotated by an orthonormal Hadamard matrix
+ * across head_dim, normalised by T alternating column- and row-wise standard
+ * deviation passes with the scales kept in log space, then quantised by
+ * asymmetric round-to-nearest, 4-bit keys and 2-bit values (the
+ * kvarn_k4v2_g128 preset); the scales are folded back in when the cache is
+ * read. A tile is committed only when it is full (same review, paragraph on
+ * speculative decoding); the tokens of the partial last tile stay fp16 in a
+ * tail buffer owned by the caller. The MLA variant quantises the shared
+ * compressed latent to int4 (same review, MLA paragraph). The gmlx "KV cache
+ * quantization" page ("Which layers quantize") limits head_dim to 128, 256
+ * and 512.
+ *
+ * Conventions for every call:
+ *   - All pointers named as device pointers must be device memory of the
+ *     current device; the caller owns every buffer. The library allocates
+ *     nothing and keeps no state between calls.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *   - Argument errors are found on the host and returned at once, before any
+ *     launch. Faults found on the device (a block-table entry outside the
+ *     cache, a missing tail, a copy that never completed) set bits in the
+ *     caller's 32-bit device word `error_flags` (see KVARN_DEVERR_*); read it
+ *     with kvarn_read_error_flags. After such a fault the outputs of that
+ *     call are unspecified, but no out-of-bounds access is made.
+ *   - Device pointers must be 16-byte aligned; the cache 128-byte aligned.
+ *
+ * Rotated basis. Codes and scales are stored in the rotated basis y = x H,
+ * H the Sylvester Hadamard matrix in natural order scaled by 1/sqrt(D)
+ * (H = H^T, H H = I). Decode rotates the query once and un-rotates the
+ * output once (turbo-attn page, "How it works": scores on rotated KV equal
+ * scores on raw KV when the query is rotated by the same matrix).
+ *
+ * Dense page format (one page = P = 16 tokens of one KV head; bytes):
+ *   [0, 8D)            K codes, 4-bit, token-major. Within a token: four
+ *                      lane chunks of D/8 bytes; chunk t holds channels
+ *                      16kc + {2t, 2t+1, 2t+8, 2t+9} of every 16-channel
+ *                      k-chunk kc. Word w of a chunk serves kc = 2w, 2w+1;
+ *                      nibble n (bits 4n..4n+3) holds channel
+ *                      16(2w + (n%4)/2) + 2t + 8(n%2) + n/4.
+ *   [8D, 12D)          V codes, 2-bit. Lane chunk L = 4g + t (D/8 bytes)
+ *                      holds channels 8nc + g of every 8-channel block nc at
+ *                      tokens {2t, 2t+1, 2t+8, 2t+9}; word w serves blocks
+ *                      4w..4w+3; token tau = 2t + e + 8h of block nc sits at
+ *                      bit 2(2(nc%4) + h) + 16e of its word.
+ *   [12D, +64)         K a[16] fp32       [12D+64, +64)   K b[16] fp32
+ *   [12D+128, +64)     V a[16] fp32       [12D+192, +64)  V b[16] fp32
+ *   [12D+256, +4C)     K column scales c of this page's slice, C = D*P/N
+ *   [12D+256+4C, +4C)  V column scales of the slice
+ *   page_bytes = 12D + 256 + 8C  (1920 for D = 128, N = 128).
+ * The page at logical index l of a sequence holds the column scales of
+ * channels [(l mod N/P) * C, +C) of its tile. All words are little-endian.
+ * A dequantised rotated value is y[i, j] = c[j] * (a[i] * code[i, j] + b[i]).
+ *
+ * MLA latent page (latent width Dl = 512, rope width R, 4-bit, K = V):
+ *   [0, 8Dl)           latent codes, placed as the dense K codes
+ *   [8Dl, +2RP)        rope, fp16, token-major (stored unquantised)
+ *   then a[16], b[16] fp32, then the column-scale slice (Dl*P/N fp32)
+ *   page_bytes = 6528 for Dl = 512, R = 64, N = 128.
+ *
+ * Cache arrays: dense [num_pages][num_kv_heads][page_bytes] bytes; latent
+ * [num_pages][page_bytes]. Logical page l of sequence b is the physical page
+ * block_table[b * bt_stride + l].
+ */
+#ifndef KVARN_H_
+#define KVARN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvarn_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  KVARN_OK = 0,
+  KVARN_EINVAL = -1,       /* bad argument (null pointer, size, stride) */
+  KVARN_EUNSUPPORTED = -2, /* shape or width with no compiled variant */
+  KVARN_EALIGN = -3,       /* pointer or stride not aligned as required */
+  KVARN_ECUDA = -4,        /* a CUDA runtime call failed */
+  KVARN_EWORKSPACE = -5    /* workspace smaller than required */
+} kvarn_status;
+
+/* Bits of the device error word. */
+#define KVARN_DEVERR_PAGE_RANGE 0x1u  /* block-table entry outside [0, num_pages) */
+#define KVARN_DEVERR_NO_TAIL    0x2u  /* seq_len % N > 0 but no tail buffer */
+#define KVARN_DEVERR_TIMEOUT    0x4u  /* a bulk copy did not complete in time */
+#define KVARN_DEVERR_SEQ_LEN    0x8u  /* seq_len < 0 or above max_seq_len */
+
+typedef struct {
+  int32_t head_dim;     /* D: 128, 256 (dense) or 512 (latent) */
+  int32_t tile_tokens;  /* N: 128 or 64 (dense), 128 (latent) */
+  int32_t page_tokens;  /* P: 16 */
+  int32_t num_kv_heads; /* Hkv (1 for the latent cache) */
+  int32_t k_bits;       /* 4 */
+  int32_t v_bits;       /* 2 (dense); 0 for the latent cache (V = K codes) */
+  int32_t norm_iters;   /* T: 1..8 normalisation iterations */
+  int32_t rope_dim;     /* 0 (dense) or 64 (latent) */
+  int32_t kv_dtype;     /* 0 fp16, 1 bf16: dtype of K/V (latent), q, tails */
+  int32_t reserved;
+  int64_t num_pages;    /* physical pages in the cache */
+} kvarn_layout;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t kvarn_version(void);
+
+/* Human-readable name of a status code. */
+const char* kvarn_status_string(int32_t status);
+
+/* KVARN_OK if the layout names a compiled variant, an error code if not. */
+int32_t kvarn_layout_check(const kvarn_layout* layout);
+
+/* Bytes of one page of one KV head (1920 for D = 128, N = 128); -1 if the
+ * layout is invalid. */
+int64_t kvarn_page_bytes(const kvarn_layout* layout);
+
+/*
+ * kvarn_encode_tiles - rotate, normalise, quantise and store whole tiles.
+ *
+ * KVarN review, four-stage paragraph (the codec) and speculative-decoding
+ * paragraph (only full tiles commit). For every sequence b < num_seqs and
+ * every tile u < chunk_tokens / N, the N tokens of K and of V starting at
+ * token u*N of the chunk are encoded as logical tile tile_start[b] + u of
+ * sequence b and written to the N/P pages that the block table names.
+ *
+ *   k, v         device, kv_dtype, element (b, h, i, d) at
+ *                b*seq_stride + h*head_stride + i*D + d  (elements)
+ *   seq_stride, head_stride  in elements, multiples of 8
+ *   chunk_tokens multiple of N (0 is a no-op)
+ *   tile_start   device int32 [num_seqs]
+ *   block_table  device int32, row stride bt_stride
+ *   cache        device bytes [num_pages][Hkv][page_bytes]
+ *   error_flags  device uint32 (bits are OR-ed in; never cleared here)
+ * Pages outside the written tiles are not touched. Re-encoding the same
+ * input writes the same bytes.
+ */
+int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                           int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                           const int32_t* block_table, int32_t bt_stride,
+                           const kvarn_layout* layout, void* cache, uint32_t* error_flags,
+                           kvarn_stream_t stream);
+
+/*
+ * kvarn_decode_workspace_bytes - scratch needed by kvarn_decode (and by
+ * kvarn_decode_fp16 and kvarn_decode_mla with the same arguments): the
+ * split-K partials (running max, sum and unnormalised output per split).
+ * Returns -1 for invalid arguments.
+ */
+int64_t kvarn_decode_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_seq_len);
+
+/*
+ * kvarn_decode - one decode query per sequence over the compressed cache.
+ *
+ * out[b, h] = sum_i softmax_i(sm_scale * q[b, h] . k_i) v_i over the
+ * seq_lens[b] tokens of sequence b, where tokens [0, floor(len/N)*N) are the
+ * committed tiles, dequantised inline from the pages, and tokens
+ * [floor(len/N)*N, len) are rows 0.. of the raw tail buffer. Query head h
+ * reads KV head h / (num_q_heads / Hkv) (GQA). Split-K over tiles with a
+ * log-sum-exp merge.
+ *
+ *   q            device, kv_dtype [num_seqs][num_q_heads][D]
+ *   num_q_heads  a multiple of Hkv, with at most 8 query heads per KV head
+ *   cache        as written by kvarn_encode_tiles
+ *   seq_lens     device int32 [num_seqs], each in [0, max_seq_len]
+ *   max_seq_len  host bound on seq_lens; sizes the grid
+ *   tail_k/v     device, kv_dtype [num_seqs][Hkv][N][D], or NULL when every
+ *                seq_len is a multiple of N
+ *   out          device fp32 [num_seqs][num_q_heads][D]
+ *   lse          device fp32 [num_seqs][num_q_heads] (natural log of the
+ *                softmax denominator of the scaled scores) or NULL
+ *   workspace    device, >= kvarn_decode_workspace_bytes(...)
+ * A sequence of length 0 gives out = 0 and lse = -inf.
+ */
+int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                     const kvarn_layout* layout, const int32_t* block_table, int32_t bt_stride,
+                     const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
+                     const void* tail_v, int32_t num_seqs, float* out, float* lse,
+                     void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                     kvarn_stream_t stream);
+
+/*
+ * kvarn_fp16_page_bytes / kvarn_store_fp16 / kvarn_decode_fp16 - the same
+ * decode skeleton over an uncompressed cache (turbo-attn page, "Also a full
+ * bf16 backend": raw KV through the same kernel, so that codec and baseline
+ * differ in one variable only).
+ *
+ * fp16 page format (P = 16 tokens of one KV head, kv_dtype elements):
+ *   K: [16][D] placed per token as four lane chunks of D/4 elements, chunk t
+ *      holding channels 16kc + {2t, 2t+1, 2t+8, 2t+9} in kc order;
+ *   V: lane chunk L = 4g + t (D/4 elements) holding, for every 8-channel block
+ *      nc, channel 8nc + g at tokens {2t, 2t+1, 2t+8, 2t+9}.
+ *   page_bytes = 4 * 16 * D (K then V).
+ * kvarn_store_fp16 writes tokens [token0, token0 + count) of every sequence
+ * (token0 and count multiples of 16) into that format; no rotation, no
+ * quantisation. kvarn_decode_fp16 reads seq_lens[b] tokens from the pages
+ * (the last page may be partial) and takes the same q, out, lse, workspace
+ * and error arguments as kvarn_decode; layout->tile_tokens is ignored.
+ */
+int64_t kvarn_fp16_page_bytes(const kvarn_layout* layout);
+
+int32_t kvarn_store_fp16(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                         int32_t num_seqs, int32_t token0, int32_t count,
+                         const int32_t* block_table, int32_t bt_stride,
+                         const kvarn_layout* layout, void* cache, uint32_t* error_flags,
+                         kvarn_stream_t stream);
+
+int32_t kvarn_decode_fp16(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                          const kvarn_layout* layout, const int32_t* block_table,
+                          int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                          int32_t num_seqs, float* out, float* lse, void* workspace,
+                          int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream);
+
+/*
+ * kvarn_encode_latent - the MLA variant of kvarn_encode_tiles (KVarN review,
+ * MLA paragraph: the compressed latent quantised to int4): the four stages
+ * run on every N-token tile of the latent (width head_dim = 512) at k_bits =
+ * 4; the rope part (width rope_dim) is stored fp16 beside the codes.
+ *
+ *   latent  device bf16/fp16 (kv_dtype), element (b, i, d) at
+ *           b*seq_stride + i*Dl + d
+ *   rope    device fp16, element (b, i, r) at b*rope_seq_stride + i*R + r
+ *   cache   device bytes [num_pages][page_bytes]
+ * Other arguments as for kvarn_encode_tiles.
+ */
+int32_t kvarn_encode_latent(const void* latent, int64_t seq_stride, const void* rope,
+                            int64_t rope_seq_stride, int32_t num_seqs, int32_t chunk_tokens,
+                            const int32_t* tile_start, const int32_t* block_table,
+                            int32_t bt_stride, const kvarn_layout* layout, void* cache,
+                            uint32_t* error_flags, kvarn_stream_t stream);
+
+/*
+ * kvarn_decode_mla - absorbed-MLA decode over the latent cache: query head h
+ * scores token i as sm_scale * (q_latent[b, h] . latent_i + q_rope[b, h] .
+ * rope_i) and returns out[b, h] = sum_i p_i latent_i (width Dl).
+ *
+ *   q_latent     device kv_dtype [num_seqs][num_heads][Dl]
+ *   q_rope       device kv_dtype [num_seqs][num_heads][R]
+ *   tail_latent  device kv_dtype [num_seqs][N][Dl] or NULL
+ *   tail_rope    device fp16 [num_seqs][N][R] or NULL
+ *   out          device fp32 [num_seqs][num_heads][Dl]
+ * num_heads must be a multiple of 16 and at most 128. Other arguments as for
+ * kvarn_decode.
+ */
+int32_t kvarn_decode_mla(const void* q_latent, const void* q_rope, int32_t num_heads,
+                         float sm_scale, const void* cache, const kvarn_layout* layout,
+                         const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                         int32_t max_seq_len, const void* tail_latent, const void* tail_rope,
+                         int32_t num_seqs, float* out, float* lse, void* workspace,
+                         int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream);
+
+/* Copy the device error word to *host_out (synchronises `stream`). */
+int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,
+                               kvarn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H_ */

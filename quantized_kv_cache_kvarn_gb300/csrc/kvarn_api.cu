@@ -1,0 +1,338 @@
+// extern "C" boundary of libkvarn: argument validation on the host, then the
+// launches. Declarations and the contract of every call are in kvarn.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "../../include/kvarn.h"
+#include "kvarn_common.cuh"
+#include "kvarn_launch.h"
+
+using namespace kvarn;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int32_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ECUDA; }
+
+// Dense layout with a compiled codec variant.
+int32_t check_dense(const kvarn_layout* L) {
+  if (!L) return KVARN_EINVAL;
+  if (L->page_tokens != kPageTokens) return KVARN_EUNSUPPORTED;
+  if (L->head_dim != 128 && L->head_dim != 256) return KVARN_EUNSUPPORTED;
+  if (L->tile_tokens != 128 && L->tile_tokens != 64) return KVARN_EUNSUPPORTED;
+  if (L->k_bits != 4 || L->v_bits != 2) return KVARN_EUNSUPPORTED;
+  if (L->norm_iters < 1 || L->norm_iters > 8) return KVARN_EUNSUPPORTED;
+  if (L->rope_dim != 0) return KVARN_EINVAL;
+  if (L->kv_dtype != 0 && L->kv_dtype != 1) return KVARN_EUNSUPPORTED;
+  if (L->num_kv_heads < 1 || L->num_pages < 0) return KVARN_EINVAL;
+  return KVARN_OK;
+}
+
+int32_t check_latent(const kvarn_layout* L) {
+  if (!L) return KVARN_EINVAL;
+  if (L->page_tokens != kPageTokens || L->head_dim != 512 || L->tile_tokens != 128 ||
+      L->k_bits != 4 || L->v_bits != 0 || L->rope_dim != 64 || L->num_kv_heads != 1)
+    return KVARN_EUNSUPPORTED;
+  if (L->norm_iters < 1 || L->norm_iters > 8) return KVARN_EUNSUPPORTED;
+  if (L->kv_dtype != 0 && L->kv_dtype != 1) return KVARN_EUNSUPPORTED;
+  if (L->num_pages < 0) return KVARN_EINVAL;
+  return KVARN_OK;
+}
+
+bool is_latent(const kvarn_layout* L) { return L && L->head_dim == 512 && L->rope_dim > 0; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvarn_version(void) { return 100; }
+
+const char* kvarn_status_string(int32_t s) {
+  switch (s) {
+    case KVARN_OK: return "ok";
+    case KVARN_EINVAL: return "invalid argument";
+    case KVARN_EUNSUPPORTED: return "unsupported shape or width";
+    case KVARN_EALIGN: return "misaligned pointer or stride";
+    case KVARN_ECUDA: return "CUDA runtime error";
+    case KVARN_EWORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t kvarn_layout_check(const kvarn_layout* L) {
+  return is_latent(L) ? check_latent(L) : check_dense(L);
+}
+
+int64_t kvarn_page_bytes(const kvarn_layout* L) {
+  if (kvarn_layout_check(L) != KVARN_OK) return -1;
+  if (is_latent(L)) return LatentPage(L->head_dim, L->rope_dim, L->tile_tokens).bytes();
+  return DensePage(L->head_dim, L->tile_tokens).bytes();
+}
+
+int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                           int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                           const int32_t* block_table, int32_t bt_stride,
+                           const kvarn_layout* L, void* cache, uint32_t* error_flags,
+                           kvarn_stream_t stream) {
+  int32_t s = check_dense(L);
+  if (s != KVARN_OK) return s;
+  if (num_seqs < 0 || chunk_tokens < 0 || chunk_tokens % L->tile_tokens) return KVARN_EINVAL;
+  if (num_seqs == 0 || chunk_tokens == 0) return KVARN_OK;
+  if (!k || !v || !tile_start || !block_table || !cache || !error_flags) return KVARN_EINVAL;
+  if (seq_stride < 0 || head_stride < 0 || bt_stride < 1) return KVARN_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || seq_stride % 8 || head_stride % 8) return KVARN_EALIGN;
+  if (!aligned(cache, 128) || !aligned(error_flags, 4)) return KVARN_EALIGN;
+  EncodeParams p{};
+  p.k = k;
+  p.v = v;
+  p.seq_stride = seq_stride;
+  p.head_stride = head_stride;
+  p.num_seqs = num_seqs;
+  p.chunk_tokens = chunk_tokens;
+  p.tile_start = tile_start;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.cache = cache;
+  p.num_pages = L->num_pages;
+  p.num_kv_heads = L->num_kv_heads;
+  p.D = L->head_dim;
+  p.N = L->tile_tokens;
+  p.norm_iters = L->norm_iters;
+  p.bf16 = L->kv_dtype == 1;
+  p.err = error_flags;
+  return from_cuda(launch_encode_dense(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
+                                     int32_t max_seq_len) {
+  if (kvarn_layout_check(L) != KVARN_OK || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0)
+    return -1;
+  if (is_latent(L)) return mla_workspace_bytes(num_seqs, num_q_heads, plan_mla(num_seqs, max_seq_len));
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens, 0);
+  const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 0);
+  return std::max(dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan),
+                  dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan16));
+}
+
+static int32_t check_decode_common(const kvarn_layout* L, int32_t num_q_heads,
+                                   const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                   float* out, void* workspace, uint32_t* error_flags) {
+  if (num_seqs < 0 || max_seq_len < 0 || num_q_heads < 1) return KVARN_EINVAL;
+  if (num_seqs == 0) return KVARN_OK;
+  if (!block_table || !seq_lens || !out || !workspace || !error_flags) return KVARN_EINVAL;
+  if (num_q_heads % L->num_kv_heads) return KVARN_EINVAL;
+  if (!aligned(out, 16) || !aligned(workspace, 16)) return KVARN_EALIGN;
+  (void)bt_stride;
+  return KVARN_OK;
+}
+
+int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                     const kvarn_layout* L, const int32_t* block_table, int32_t bt_stride,
+                     const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
+                     const void* tail_v, int32_t num_seqs, float* out, float* lse,
+                     void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                     kvarn_stream_t stream) {
+  int32_t s = check_dense(L);
+  if (s != KVARN_OK) return s;
+  s = check_decode_common(L, num_q_heads, block_table, bt_stride, seq_lens, max_seq_len, num_seqs,
+                          out, workspace, error_flags);
+  if (s != KVARN_OK || num_seqs == 0) return s;
+  if (!q || !cache) return KVARN_EINVAL;
+  if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
+  const int32_t committed_pages = (max_seq_len / L->tile_tokens) * (L->tile_tokens / kPageTokens);
+  if (bt_stride < committed_pages) return KVARN_EINVAL;
+  if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
+  if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens, 0);
+  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
+    return KVARN_EWORKSPACE;
+  DecodeParams p{};
+  p.q = q;
+  p.num_q_heads = num_q_heads;
+  p.sm_scale = sm_scale;
+  p.cache = static_cast<const uint8_t*>(cache);
+  p.D = L->head_dim;
+  p.N = L->tile_tokens;
+  p.num_kv_heads = L->num_kv_heads;
+  p.num_pages = L->num_pages;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.tail_k = tail_k;
+  p.tail_v = tail_v;
+  p.num_seqs = num_seqs;
+  p.out = out;
+  p.lse = lse;
+  p.workspace = workspace;
+  p.err = error_flags;
+  p.bf16 = L->kv_dtype == 1;
+  return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t kvarn_fp16_page_bytes(const kvarn_layout* L) {
+  if (!L || (L->head_dim != 128 && L->head_dim != 256) || L->page_tokens != kPageTokens) return -1;
+  return 4LL * kPageTokens * L->head_dim;
+}
+
+int32_t kvarn_store_fp16(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                         int32_t num_seqs, int32_t token0, int32_t count,
+                         const int32_t* block_table, int32_t bt_stride, const kvarn_layout* L,
+                         void* cache, uint32_t* error_flags, kvarn_stream_t stream) {
+  if (kvarn_fp16_page_bytes(L) < 0) return KVARN_EUNSUPPORTED;
+  if (L->kv_dtype != 0) return KVARN_EUNSUPPORTED;
+  if (num_seqs < 0 || token0 < 0 || count < 0 || token0 % kPageTokens || count % kPageTokens)
+    return KVARN_EINVAL;
+  if (num_seqs == 0 || count == 0) return KVARN_OK;
+  if (!k || !v || !block_table || !cache || !error_flags || bt_stride < 1 || L->num_kv_heads < 1)
+    return KVARN_EINVAL;
+  if (!aligned(cache, 128) || !aligned(k, 4) || !aligned(v, 4)) return KVARN_EALIGN;
+  StoreFp16Params p{};
+  p.k = k;
+  p.v = v;
+  p.seq_stride = seq_stride;
+  p.head_stride = head_stride;
+  p.num_seqs = num_seqs;
+  p.token0 = token0;
+  p.count = count;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.cache = cache;
+  p.num_pages = L->num_pages;
+  p.num_kv_heads = L->num_kv_heads;
+  p.D = L->head_dim;
+  p.err = error_flags;
+  return from_cuda(launch_store_fp16(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_decode_fp16(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                          const kvarn_layout* L, const int32_t* block_table, int32_t bt_stride,
+                          const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                          float* out, float* lse, void* workspace, int64_t workspace_bytes,
+                          uint32_t* error_flags, kvarn_stream_t stream) {
+  if (kvarn_fp16_page_bytes(L) < 0 || L->kv_dtype != 0) return KVARN_EUNSUPPORTED;
+  if (L->num_kv_heads < 1 || L->num_pages < 0) return KVARN_EINVAL;
+  int32_t s = check_decode_common(L, num_q_heads, block_table, bt_stride, seq_lens, max_seq_len,
+                                  num_seqs, out, workspace, error_flags);
+  if (s != KVARN_OK || num_seqs == 0) return s;
+  if (!q || !cache) return KVARN_EINVAL;
+  if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
+  if (bt_stride < (max_seq_len + kPageTokens - 1) / kPageTokens) return KVARN_EINVAL;
+  if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 0);
+  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
+    return KVARN_EWORKSPACE;
+  DecodeParams p{};
+  p.q = q;
+  p.num_q_heads = num_q_heads;
+  p.sm_scale = sm_scale;
+  p.cache = static_cast<const uint8_t*>(cache);
+  p.D = L->head_dim;
+  p.N = 32;
+  p.num_kv_heads = L->num_kv_heads;
+  p.num_pages = L->num_pages;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.num_seqs = num_seqs;
+  p.out = out;
+  p.lse = lse;
+  p.workspace = workspace;
+  p.err = error_flags;
+  SplitPlan pl = plan;
+  pl.slots = plan.nsplit;  // no tail slot: partial pages are read directly
+  if (pl.slots == 0) pl.slots = pl.nsplit = 1;
+  return from_cuda(launch_decode_fp16(p, pl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_encode_latent(const void* latent, int64_t seq_stride, const void* rope,
+                            int64_t rope_seq_stride, int32_t num_seqs, int32_t chunk_tokens,
+                            const int32_t* tile_start, const int32_t* block_table,
+                            int32_t bt_stride, const kvarn_layout* L, void* cache,
+                            uint32_t* error_flags, kvarn_stream_t stream) {
+  int32_t s = check_latent(L);
+  if (s != KVARN_OK) return s;
+  if (num_seqs < 0 || chunk_tokens < 0 || chunk_tokens % L->tile_tokens) return KVARN_EINVAL;
+  if (num_seqs == 0 || chunk_tokens == 0) return KVARN_OK;
+  if (!latent || !rope || !tile_start || !block_table || !cache || !error_flags || bt_stride < 1)
+    return KVARN_EINVAL;
+  if (seq_stride < 0 || rope_seq_stride < 0) return KVARN_EINVAL;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || seq_stride % 8 || rope_seq_stride % 8)
+    return KVARN_EALIGN;
+  if (!aligned(cache, 128)) return KVARN_EALIGN;
+  EncodeLatentParams p{};
+  p.latent = latent;
+  p.seq_stride = seq_stride;
+  p.rope = rope;
+  p.rope_seq_stride = rope_seq_stride;
+  p.num_seqs = num_seqs;
+  p.chunk_tokens = chunk_tokens;
+  p.tile_start = tile_start;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.cache = cache;
+  p.num_pages = L->num_pages;
+  p.norm_iters = L->norm_iters;
+  p.bf16 = L->kv_dtype == 1;
+  p.err = error_flags;
+  return from_cuda(launch_encode_latent(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_decode_mla(const void* q_latent, const void* q_rope, int32_t num_heads,
+                         float sm_scale, const void* cache, const kvarn_layout* L,
+                         const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                         int32_t max_seq_len, const void* tail_latent, const void* tail_rope,
+                         int32_t num_seqs, float* out, float* lse, void* workspace,
+                         int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
+  int32_t s = check_latent(L);
+  if (s != KVARN_OK) return s;
+  s = check_decode_common(L, num_heads, block_table, bt_stride, seq_lens, max_seq_len, num_seqs, out,
+                          workspace, error_flags);
+  if (s != KVARN_OK || num_seqs == 0) return s;
+  if (!q_latent || !q_rope || !cache) return KVARN_EINVAL;
+  if (num_heads % 16 || num_heads > 128) return KVARN_EUNSUPPORTED;
+  if (bt_stride < (max_seq_len / L->tile_tokens) * (L->tile_tokens / kPageTokens)) return KVARN_EINVAL;
+  if (!aligned(q_latent, 16) || !aligned(q_rope, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
+  if ((tail_latent && !aligned(tail_latent, 16)) || (tail_rope && !aligned(tail_rope, 16)))
+    return KVARN_EALIGN;
+  const SplitPlan plan = plan_mla(num_seqs, max_seq_len);
+  if (workspace_bytes < mla_workspace_bytes(num_seqs, num_heads, plan)) return KVARN_EWORKSPACE;
+  DecodeParams p{};
+  p.q = q_latent;
+  p.q_rope = q_rope;
+  p.num_q_heads = num_heads;
+  p.sm_scale = sm_scale;
+  p.cache = static_cast<const uint8_t*>(cache);
+  p.D = 512;
+  p.N = L->tile_tokens;
+  p.num_kv_heads = 1;
+  p.num_pages = L->num_pages;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.tail_k = tail_latent;
+  p.tail_v = tail_rope;
+  p.num_seqs = num_seqs;
+  p.out = out;
+  p.lse = lse;
+  p.workspace = workspace;
+  p.err = error_flags;
+  p.bf16 = L->kv_dtype == 1;
+  return from_cuda(launch_decode_mla(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,
+                               kvarn_stream_t stream) {
+  if (!error_flags || !host_out) return KVARN_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_out, error_flags, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KVARN_ECUDA;
+  return from_cuda(cudaStreamSynchronize(st));
+}
+
+}  // extern "C"

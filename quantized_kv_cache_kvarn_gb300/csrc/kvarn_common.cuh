@@ -1,0 +1,206 @@
+// Device helpers shared by the KVarN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvarn.h"
+
+namespace kvarn {
+
+constexpr int kPageTokens = 16;
+
+// ---------------------------------------------------------------- layout
+// Byte offsets inside one dense page of one KV head (format documented in
+// kvarn.h). C = D * P / N column scales per page.
+struct DensePage {
+  int D, N;
+  __host__ __device__ constexpr DensePage(int d, int n) : D(d), N(n) {}
+  __host__ __device__ constexpr int cols() const { return D * kPageTokens / N; }
+  __host__ __device__ constexpr int k_codes() const { return 0; }
+  __host__ __device__ constexpr int v_codes() const { return 8 * D; }
+  __host__ __device__ constexpr int k_a() const { return 12 * D; }
+  __host__ __device__ constexpr int k_b() const { return 12 * D + 64; }
+  __host__ __device__ constexpr int v_a() const { return 12 * D + 128; }
+  __host__ __device__ constexpr int v_b() const { return 12 * D + 192; }
+  __host__ __device__ constexpr int k_col() const { return 12 * D + 256; }
+  __host__ __device__ constexpr int v_col() const { return 12 * D + 256 + 4 * cols(); }
+  __host__ __device__ constexpr int bytes() const { return 12 * D + 256 + 8 * cols(); }
+};
+
+// MLA latent page: codes (dense-K placement), fp16 rope, a, b, column slice.
+struct LatentPage {
+  int D, R, N;
+  __host__ __device__ constexpr LatentPage(int d, int r, int n) : D(d), R(r), N(n) {}
+  __host__ __device__ constexpr int cols() const { return D * kPageTokens / N; }
+  __host__ __device__ constexpr int codes() const { return 0; }
+  __host__ __device__ constexpr int rope() const { return 8 * D; }
+  __host__ __device__ constexpr int a() const { return 8 * D + 2 * R * kPageTokens; }
+  __host__ __device__ constexpr int b() const { return a() + 64; }
+  __host__ __device__ constexpr int col() const { return a() + 128; }
+  __host__ __device__ constexpr int bytes() const { return col() + 4 * cols(); }
+};
+
+// ------------------------------------------------------------- dtype io
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+// Eight consecutive 16-bit elements from a 16-byte aligned address.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* out) {
+  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = to_f32<T>(h[i]);
+}
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ------------------------------------------------------------ shared mem
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One-dimensional bulk copy global -> shared, completion counted in bytes on
+// the mbarrier. Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after about `limit_cycles` SM clocks and returns
+// false, so that a copy that never lands can not hang the GPU.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles = 2000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// --------------------------------------------------------------- mma
+// D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col).
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
+  return *reinterpret_cast<__half2*>(&u);
+}
+
+// Split two fp32 values into fp16 hi + lo parts (x ~ hi + lo to ~2^-22).
+__device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  __half2 h = __floats2half2_rn(x0, x1);
+  float2 hf = __half22float2(h);
+  __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = h2_as_u32(h);
+  lo = h2_as_u32(l);
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t orv) {
+  uint32_t r;
+  // (x & mask) | orv
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(orv));
+  return r;
+}
+
+// Codes to exact fp16 pairs. A 4-bit field at bits 0-3 (and 16-19) OR-ed
+// into 0x6400 (fp16 1024) is 1024 + n; one at bits 4-7 is 1024 + 16n. The
+// offsets below recentre them: 4-bit codes to n - 8, 2-bit codes to n - 2.
+// Every intermediate is an integer below 2048, so each step is exact in fp16.
+constexpr uint32_t kMagic = 0x64006400u;
+
+// One K word -> 4 half2: (kc even: b01, b23), (kc odd: b01, b23).
+__device__ __forceinline__ void dequant_k_word(uint32_t x, uint32_t* out) {
+  const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+  const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+  const __half2 o16 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
+  uint32_t y = x >> 8;
+  out[0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(x, 0x000F000Fu, kMagic)), sub));
+  out[1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(x, 0x00F000F0u, kMagic)), s16, o16));
+  out[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x000F000Fu, kMagic)), sub));
+  out[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00F000F0u, kMagic)), s16, o16));
+}
+
+// One V word -> 8 half2 in pair order p = 0..7 (fields at bits 2p, 2p + 16).
+__device__ __forceinline__ void dequant_v_word(uint32_t x, uint32_t* out) {
+  const __half2 sub = __halves2half2(__ushort_as_half(0x6402), __ushort_as_half(0x6402));  // 1026
+  const __half2 s4 = __halves2half2(__ushort_as_half(0x3400), __ushort_as_half(0x3400));   // 1/4
+  const __half2 o4 = __halves2half2(__ushort_as_half(0xDC08), __ushort_as_half(0xDC08));   // -258
+  const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+  const __half2 o16 = __halves2half2(__ushort_as_half(0xD420), __ushort_as_half(0xD420));  // -66
+  const __half2 s64 = __halves2half2(__ushort_as_half(0x2400), __ushort_as_half(0x2400));  // 1/64
+  const __half2 o64 = __halves2half2(__ushort_as_half(0xCC80), __ushort_as_half(0xCC80));  // -18
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t y = half ? (x >> 8) : x;
+    out[4 * half + 0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x00030003u, kMagic)), sub));
+    out[4 * half + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x000C000Cu, kMagic)), s4, o4));
+    out[4 * half + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00300030u, kMagic)), s16, o16));
+    out[4 * half + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00C000C0u, kMagic)), s64, o64));
+  }
+}
+
+__device__ __forceinline__ float warp_max_xor(float v, int lo, int hi) {
+  for (int o = lo; o < hi; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_xor(float v, int lo, int hi) {
+  for (int o = lo; o < hi; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace kvarn

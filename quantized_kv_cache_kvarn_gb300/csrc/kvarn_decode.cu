@@ -1,0 +1,495 @@
+// KVarN decode attention over the compressed paged cache, sm_103a.
+//
+// Paged, split-K, GQA-grouped decode that streams the packed codes and
+// scales straight from HBM and dequantises them in registers; no fp16 K or V
+// buffer is ever formed (turbo-attn page, "Inline dequant"). Scores are
+// taken in the rotated basis: the query is rotated once per CTA and the
+// output un-rotated once in the merge (turbo-attn page, "How it works").
+//
+// Kernel 1 (decode_dense_kernel): one CTA per (split, KV head, sequence);
+// each of its W warps owns every W-th tile of the split and streams it into
+// its own two-stage shared-memory ring with one-dimensional bulk copies
+// (one per page, completion counted on an mbarrier). Per tile and warp:
+//   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
+//        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
+//        half of the m16 tile free, so the split costs no extra mma);
+//   S  = q~ (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
+//        integers, made from the packed nibbles by exponent-bias arithmetic);
+//   s  = a_K * S + (b_K + 8 a_K) * sum(q~)      (row scales folded back in);
+//   online softmax in base 2;
+//   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
+//   acc = acc * alpha + c_V * (u + sum p (b_V + 2 a_V)).
+// The warps of a CTA merge in shared memory and write one partial
+// (max, sum, unnormalised output) per split. The last split slot holds the
+// fp16 tail (tokens past the last full tile, in the original basis).
+// Kernel 2 (merge_kernel): log-sum-exp merge of the partials, inverse
+// Hadamard transform of the rotated part, plus the tail part.
+#include <math.h>
+
+#include "kvarn_common.cuh"
+#include "kvarn_launch.h"
+#include "kvarn_merge.cuh"
+#include <algorithm>
+
+namespace kvarn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, int N, int W>
+struct DecShape {
+  static constexpr DensePage PG{D, N};
+  static constexpr int PPT = N / kPageTokens;
+  static constexpr int PB = PG.bytes();
+  static constexpr int TILE = PPT * PB;
+  static constexpr int NB = N / 8;
+  static constexpr int KC = D / 16;
+  static constexpr int NC = D / 8;
+  static constexpr int CPP = PG.cols();
+  static constexpr int LW = D / 32;  // words per lane chunk (K and V)
+  static constexpr int STAGES = W * 2 * TILE;
+  static constexpr int SMEM = STAGES + W * 2 * 8 + 8 * D * 4;
+  static_assert(W * 8 * (D + 2) * 4 <= STAGES, "merge scratch must fit in the stage ring");
+  static_assert(PB % 16 == 0, "pages must keep 16-byte alignment");
+};
+
+
+struct DecArgs {
+  const void* q;
+  float kappa;  // sm_scale * log2(e)
+  const uint8_t* cache;
+  int32_t Hq, Hkv, G;
+  int64_t num_pages;
+  const int32_t* bt;
+  int32_t bt_stride;
+  const int32_t* seq_lens;
+  int32_t max_seq_len;
+  const void* tail_k;
+  const void* tail_v;
+  float* ws;
+  int32_t tps, nsplit, slots;
+  uint32_t* err;
+};
+
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T* p, float* out) {
+  if constexpr (E == 4) {
+    uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = to_f32<T>(h[i]);
+  } else {
+    static_assert(E % 8 == 0, "vector width");
+#pragma unroll
+    for (int k = 0; k < E; k += 8) load8<T>(p + k, out + k);
+  }
+}
+
+__device__ __forceinline__ void write_empty(float* part, int D, int lane) {
+  if (lane == 0) {
+    part[0] = -INFINITY;
+    part[1] = 0.f;
+  }
+  for (int j = lane; j < D; j += 32) part[4 + j] = 0.f;
+}
+
+// fp16 tail over tokens [committed, len): dense attention in the original
+// basis, one warp per query head.
+template <int D, int N, typename T, int W>
+__device__ void tail_partials(const DecArgs& A, int b, int kvh, int tail, unsigned char* smem) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* sbuf = reinterpret_cast<float*>(smem) + warp * N;
+  for (int h = warp; h < A.G; h += W) {
+    const int hq = kvh * A.G + h;
+    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + hq) * A.slots + A.nsplit) * kPStride(D);
+    if (tail == 0 || A.tail_k == nullptr || A.tail_v == nullptr) {
+      if (tail > 0 && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
+      write_empty(part, D, lane);
+      continue;
+    }
+    float qv[E];
+    load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + hq) * D + lane * E, qv);
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
+    const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * N;
+    const T* tk = static_cast<const T*>(A.tail_k);
+    const T* tv = static_cast<const T*>(A.tail_v);
+    float mx = -INFINITY;
+    for (int tau = 0; tau < tail; ++tau) {
+      float kv[E];
+      load_vec<T, E>(tk + (row0 + tau) * D + lane * E, kv);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
+      dot = warp_sum_xor(dot, 1, 32);
+      if (lane == 0) sbuf[tau] = dot;
+      mx = fmaxf(mx, dot);
+    }
+    __syncwarp();
+    float l = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int tau = 0; tau < tail; ++tau) {
+      const float p = exp2f(sbuf[tau] - mx);
+      l += p;
+      float vv[E];
+      load_vec<T, E>(tv + (row0 + tau) * D + lane * E, vv);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      part[0] = mx;
+      part[1] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) part[4 + lane * E + e] = acc[e];
+  }
+}
+
+template <int D, int N, typename T, int W>
+__global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
+  using S = DecShape<D, N, W>;
+  constexpr DensePage PG{D, N};
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = A.G;
+
+  int len = A.seq_lens[b];
+  if (len < 0 || len > A.max_seq_len) {
+    if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    len = len < 0 ? 0 : A.max_seq_len;
+  }
+  const int ntiles = len / N;
+
+  if (split == A.nsplit) {
+    tail_partials<D, N, T, W>(A, b, kvh, len - ntiles * N, smem);
+    return;
+  }
+  const int t0 = split * A.tps, t1 = min(t0 + A.tps, ntiles);
+  if (t0 >= t1) {
+    for (int h = warp; h < G; h += W)
+      write_empty(A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + h) * A.slots + split) * kPStride(D),
+                  D, lane);
+    return;
+  }
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::STAGES);
+  float* qrot = reinterpret_cast<float*>(smem + S::STAGES + W * 2 * 8);
+
+  // ---- rotated, scaled query rows of the group (rows >= G are zero)
+  for (int h = warp; h < 8; h += W) {
+    constexpr int E = D / 32;
+    float v[E];
+    if (h < G) {
+      load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + kvh * G + h) * D + lane * E, v);
+      warp_fwht<E>(v);
+      const float sc = A.kappa / sqrtf(static_cast<float>(D));
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] *= sc;
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
+  }
+  if (lane == 0) {
+    mbar_init(&bars[2 * warp], 1);
+    mbar_init(&bars[2 * warp + 1], 1);
+  }
+  fence_mbar_init();
+  __syncthreads();
+
+  const int first = t0 + warp;
+  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
+  unsigned char* ring = smem + warp * 2 * S::TILE;
+  uint64_t* bar = bars + 2 * warp;
+  const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
+
+  auto issue = [&](int i) {
+    const int tile = first + i * W, st = i & 1;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&bar[st], S::TILE);
+    __syncwarp();
+    if (lane < S::PPT) {
+      int phys = bt[tile * S::PPT + lane];
+      if (phys < 0 || phys >= A.num_pages) {
+        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+        phys = 0;
+      }
+      bulk_g2s(ring + st * S::TILE + lane * S::PB,
+               A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB, S::PB, &bar[st]);
+    }
+  };
+  if (n_my > 0) issue(0);
+  if (n_my > 1) issue(1);
+
+  float m = -INFINITY, lsum = 0.f;
+  float acc[S::NC][2];
+#pragma unroll
+  for (int nc = 0; nc < S::NC; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
+
+  int i = 0;
+  for (; i < n_my; ++i) {
+    const int st = i & 1;
+    if (!mbar_wait_bounded(&bar[st], (i >> 1) & 1)) {
+      if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+      break;
+    }
+    const unsigned char* buf = ring + st * S::TILE;
+
+    // -- q~ = q' * c_K as fp16 hi/lo A fragments
+    uint32_t Aq[S::KC][4];
+    float qsum = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < S::KC; ++kc) {
+      const int ch0 = 16 * kc + 2 * t;
+      const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
+      const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
+      const unsigned char* cp = buf + (ch0 / S::CPP) * S::PB + PG.k_col();
+      const float2 c01 = *reinterpret_cast<const float2*>(cp + (ch0 % S::CPP) * 4);
+      const float2 c89 = *reinterpret_cast<const float2*>(cp + (ch0 % S::CPP) * 4 + 32);
+      const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
+      qsum += (x0 + x1) + (x8 + x9);
+      split_hi_lo(x0, x1, Aq[kc][0], Aq[kc][1]);
+      split_hi_lo(x8, x9, Aq[kc][2], Aq[kc][3]);
+    }
+    qsum = warp_sum_xor(qsum, 1, 4);
+
+    // -- S = q~ . (K codes - 8)
+    float s[S::NB][2];
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      const unsigned char* kp =
+          buf + (nb >> 1) * S::PB + ((nb & 1) * 8 + g) * (D / 2) + t * (D / 8);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q4 = 0; q4 < S::LW / 4; ++q4) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(kp + 16 * q4);
+        const uint32_t words[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int w = 4 * q4 + w4;
+          uint32_t bf[4];
+          dequant_k_word(words[w4], bf);
+          mma_f16(d, Aq[2 * w][0], Aq[2 * w][1], Aq[2 * w][2], Aq[2 * w][3], bf[0], bf[1]);
+          mma_f16(d, Aq[2 * w + 1][0], Aq[2 * w + 1][1], Aq[2 * w + 1][2], Aq[2 * w + 1][3], bf[2], bf[3]);
+        }
+      }
+      s[nb][0] = d[0] + d[2];
+      s[nb][1] = d[1] + d[3];
+    }
+
+    // -- row-scale fold and online softmax (base 2)
+    float mt = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      const unsigned char* pg = buf + (nb >> 1) * S::PB;
+      const int idx = (nb & 1) * 8 + 2 * t;
+      const float2 ka = *reinterpret_cast<const float2*>(pg + PG.k_a() + idx * 4);
+      const float2 kb = *reinterpret_cast<const float2*>(pg + PG.k_b() + idx * 4);
+      s[nb][0] = fmaf(ka.x, s[nb][0], fmaf(8.f, ka.x, kb.x) * qsum);
+      s[nb][1] = fmaf(ka.y, s[nb][1], fmaf(8.f, ka.y, kb.y) * qsum);
+      mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
+    }
+    mt = warp_max_xor(mt, 1, 4);
+    const float m_new = fmaxf(m, mt);
+    const float alpha = exp2f(m - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      s[nb][0] = exp2f(s[nb][0] - m_new);
+      s[nb][1] = exp2f(s[nb][1] - m_new);
+      psum += s[nb][0] + s[nb][1];
+    }
+    lsum = fmaf(lsum, alpha, psum);
+    m = m_new;
+
+    // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
+    uint32_t Ap[S::PPT][4];
+    float beta = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < S::PPT; ++pp) {
+      const unsigned char* pg = buf + pp * S::PB;
+      const float2 va0 = *reinterpret_cast<const float2*>(pg + PG.v_a() + (2 * t) * 4);
+      const float2 va1 = *reinterpret_cast<const float2*>(pg + PG.v_a() + (8 + 2 * t) * 4);
+      const float2 vb0 = *reinterpret_cast<const float2*>(pg + PG.v_b() + (2 * t) * 4);
+      const float2 vb1 = *reinterpret_cast<const float2*>(pg + PG.v_b() + (8 + 2 * t) * 4);
+      const float p00 = s[2 * pp][0], p01 = s[2 * pp][1], p10 = s[2 * pp + 1][0], p11 = s[2 * pp + 1][1];
+      beta = fmaf(p00, fmaf(2.f, va0.x, vb0.x), beta);
+      beta = fmaf(p01, fmaf(2.f, va0.y, vb0.y), beta);
+      beta = fmaf(p10, fmaf(2.f, va1.x, vb1.x), beta);
+      beta = fmaf(p11, fmaf(2.f, va1.y, vb1.y), beta);
+      split_hi_lo(p00 * va0.x, p01 * va0.y, Ap[pp][0], Ap[pp][1]);
+      split_hi_lo(p10 * va1.x, p11 * va1.y, Ap[pp][2], Ap[pp][3]);
+    }
+    beta = warp_sum_xor(beta, 1, 4);
+
+#pragma unroll
+    for (int half = 0; half < S::LW / 4; ++half) {
+      float u[16][4];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < S::PPT; ++pp) {
+        const uint4 vw = *reinterpret_cast<const uint4*>(buf + pp * S::PB + PG.v_codes() +
+                                                         (4 * g + t) * (D / 8) + 16 * half);
+        const uint32_t words[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          uint32_t bf[8];
+          dequant_v_word(words[w4], bf);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(u[4 * w4 + k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int nc = 16 * half + k;
+        const int ch = 8 * nc + 2 * t;
+        const float2 cv = *reinterpret_cast<const float2*>(buf + (ch / S::CPP) * S::PB + PG.v_col() +
+                                                           (ch % S::CPP) * 4);
+        acc[nc][0] = fmaf(acc[nc][0], alpha, cv.x * ((u[k][0] + u[k][2]) + beta));
+        acc[nc][1] = fmaf(acc[nc][1], alpha, cv.y * ((u[k][1] + u[k][3]) + beta));
+      }
+    }
+    if (i + 2 < n_my) issue(i + 2);
+  }
+  if (i < n_my) {  // gave up on a copy: wait (bounded) for what is still in flight
+    for (int j = i; j < min(n_my, i + 2); ++j) mbar_wait_bounded(&bar[j & 1], (j >> 1) & 1, 100000000LL);
+  }
+  lsum = warp_sum_xor(lsum, 1, 4);
+
+  // ---- merge the W warps of the CTA (scratch aliases the stage ring)
+  __syncthreads();
+  float* mrg = reinterpret_cast<float*>(smem);
+  float* mw = mrg + warp * 8 * (D + 2);
+  if (t == 0) {
+    mw[g * (D + 2)] = n_my > 0 ? m : -INFINITY;
+    mw[g * (D + 2) + 1] = n_my > 0 ? lsum : 0.f;
+  }
+#pragma unroll
+  for (int nc = 0; nc < S::NC; ++nc) {
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[nc][0];
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[nc][1];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int gg = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
+    float a = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* r = mrg + (w * 8 + gg) * (D + 2);
+        const float sc = exp2f(r[0] - M);
+        a = fmaf(r[2 + j], sc, a);
+        L = fmaf(r[1], sc, L);
+      }
+    }
+    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + gg) * A.slots + split) * kPStride(D);
+    part[4 + j] = a;
+    if (j == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+  }
+}
+
+// ------------------------------------------------------------- planning
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// Warps per CTA for a dense decode variant.
+static int dense_warps(int D) { return D == 256 ? 1 : 2; }
+
+SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
+                     int32_t /*unused*/) {
+  SplitPlan p{};
+  const int tiles = max_seq_len / N;
+  const int units = std::max(1, num_seqs * num_kv_heads);
+  const int W = 2;
+  if (tiles == 0) {
+    p.tiles_per_split = 1;
+    p.nsplit = 0;
+  } else {
+    const int target = device_sm_count() * 3 * 3;  // about three waves of three CTAs per SM
+    int want = (target + units - 1) / units;
+    const int max_split = std::max(1, (tiles + 2 * W - 1) / (2 * W));  // >= 2 tiles per warp
+    want = std::min(std::max(want, 1), max_split);
+    p.tiles_per_split = (tiles + want - 1) / want;
+    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  }
+  p.slots = p.nsplit + 1;
+  return p;
+}
+
+int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
+                              const SplitPlan& plan) {
+  return static_cast<int64_t>(num_seqs) * num_q_heads * plan.slots * kPStride(D) * 4;
+}
+
+template <int D, int N, typename T, int W>
+static cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
+  using S = DecShape<D, N, W>;
+  auto kern = decode_dense_kernel<D, N, T, W>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(A.nsplit + 1, A.Hkv, num_seqs);
+  kern<<<grid, W * 32, S::SMEM, st>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  DecArgs A{};
+  A.q = p.q;
+  A.kappa = p.sm_scale * kLog2e;
+  A.cache = p.cache;
+  A.Hq = p.num_q_heads;
+  A.Hkv = p.num_kv_heads;
+  A.G = p.num_q_heads / p.num_kv_heads;
+  A.num_pages = p.num_pages;
+  A.bt = p.block_table;
+  A.bt_stride = p.bt_stride;
+  A.seq_lens = p.seq_lens;
+  A.max_seq_len = p.max_seq_len;
+  A.tail_k = p.tail_k;
+  A.tail_v = p.tail_v;
+  A.ws = static_cast<float*>(p.workspace);
+  A.tps = plan.tiles_per_split;
+  A.nsplit = plan.nsplit;
+  A.slots = plan.slots;
+  A.err = p.err;
+  cudaError_t e = cudaErrorInvalidValue;
+#define KV_DISPATCH(DD, NN, WW)                                                       \
+  if (p.D == DD && p.N == NN)                                                         \
+    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW>(A, p.num_seqs, st)              \
+               : run_dense<DD, NN, __half, WW>(A, p.num_seqs, st);
+  KV_DISPATCH(128, 128, 2)
+  KV_DISPATCH(128, 64, 2)
+  KV_DISPATCH(256, 128, 2)
+  KV_DISPATCH(256, 64, 2)
+#undef KV_DISPATCH
+  if (e != cudaSuccess) return e;
+  const int rows = p.num_seqs * p.num_q_heads;
+  if (p.D == 128)
+    merge_kernel<128><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
+  else
+    merge_kernel<256><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace kvarn

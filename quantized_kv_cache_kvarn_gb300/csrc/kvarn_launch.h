@@ -1,0 +1,100 @@
+// Internal launch parameters shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvarn {
+
+struct EncodeParams {
+  const void* k;
+  const void* v;
+  int64_t seq_stride, head_stride;
+  int32_t num_seqs, chunk_tokens;
+  const int32_t* tile_start;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  void* cache;
+  int64_t num_pages;
+  int32_t num_kv_heads, D, N, norm_iters;
+  bool bf16;
+  uint32_t* err;
+};
+
+struct EncodeLatentParams {
+  const void* latent;
+  int64_t seq_stride;
+  const void* rope;
+  int64_t rope_seq_stride;
+  int32_t num_seqs, chunk_tokens;
+  const int32_t* tile_start;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  void* cache;
+  int64_t num_pages;
+  int32_t norm_iters;
+  bool bf16;
+  uint32_t* err;
+};
+
+struct DecodeParams {
+  const void* q;            // [B][Hq][D] (dense) or q_latent [B][H][Dl] (MLA)
+  const void* q_rope;       // MLA only
+  int32_t num_q_heads;
+  float sm_scale;
+  const uint8_t* cache;
+  int32_t D, N, num_kv_heads;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* seq_lens;
+  int32_t max_seq_len;
+  const void* tail_k;       // tail_latent for MLA
+  const void* tail_v;       // tail_rope for MLA
+  int32_t num_seqs;
+  float* out;
+  float* lse;
+  void* workspace;
+  uint32_t* err;
+  bool bf16;
+};
+
+// Split-K plan: tiles per split and the number of splits (+1 slot for the
+// tail partial). Depends only on the arguments and the device's SM count.
+struct SplitPlan {
+  int32_t tiles_per_split;
+  int32_t nsplit;   // splits over committed tiles
+  int32_t slots;    // nsplit + 1 (tail)
+};
+
+SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
+                     int32_t tokens_per_unit_min);
+int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
+                              const SplitPlan& plan);
+
+cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st);
+cudaError_t launch_encode_latent(const EncodeLatentParams& p, cudaStream_t st);
+cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
+
+struct StoreFp16Params {
+  const void* k;
+  const void* v;
+  int64_t seq_stride, head_stride;
+  int32_t num_seqs, token0, count;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  void* cache;
+  int64_t num_pages;
+  int32_t num_kv_heads, D;
+  uint32_t* err;
+};
+cudaError_t launch_store_fp16(const StoreFp16Params& p, cudaStream_t st);
+cudaError_t launch_decode_fp16(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
+
+SplitPlan plan_mla(int32_t num_seqs, int32_t max_seq_len);
+int64_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const SplitPlan& plan);
+cudaError_t launch_decode_mla(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace kvarn
