@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(128) store_fp16_kernel(StoreFp16Params p) {
   uint8_t* page = static_cast<uint8_t*>(p.cache) +
                   (static_cast<int64_t>(phys) * p.num_kv_heads + h) * (4 * kPageTokens * D);
   const int64_t base = static_cast<int64_t>(b) * p.seq_stride + static_cast<int64_t>(h) * p.head_stride +
-                       static_cast<int64_t>(pg_i) * kPageTokens * D;
+                       static_cast<int64_t>(token0) * D;
   const T* K = static_cast<const T*>(p.k) + base;
   const T* V = static_cast<const T*>(p.v) + base;
   const uint16_t* K16 = reinterpret_cast<const uint16_t*>(K);
