@@ -19,7 +19,8 @@
  * Conventions for every call:
  *   - All pointers named as device pointers must be device memory of the
  *     current device; the caller owns every buffer. The library allocates
- *     nothing and keeps no state between calls.
+ *     nothing and keeps no state between calls, except the static scratch
+ *     array of kvarn_decode_noalloc described with that call.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).
  *   - Argument errors are found on the host and returned at once, before any
  *     launch. Faults found on the device (a block-table entry outside the
@@ -254,6 +255,37 @@ int32_t kvarn_decode_mla(const void* q_latent, const void* q_rope, int32_t num_h
                          int32_t max_seq_len, const void* tail_latent, const void* tail_rope,
                          int32_t num_seqs, float* out, float* lse, void* workspace,
                          int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream);
+
+/*
+ * kvarn_decode_noalloc - kvarn_decode without a workspace argument. (The
+ * pages describing the method have no counterpart of this call; it serves
+ * callers that can not allocate device memory: a plugin that its host
+ * framework hands only input and output tensors, a process whose device
+ * memory a pool allocator owns outright, or a latency-bound path that can
+ * not afford the device synchronisation a cudaMalloc may cause.)
+ *
+ * The split-K partials live in a fixed array of KVARN_NOALLOC_SCRATCH_BYTES
+ * of static device memory inside the library, which every GPU that loads
+ * the library holds until the process exits. The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture on the device.
+ *   - Every call shares the one array per device and leaves its partials
+ *     there; calls whose kernels overlap on the GPU (two streams, two host
+ *     threads) race on it. Nothing in it needs to start at zero.
+ *   - Returns KVARN_EWORKSPACE, launching nothing, when
+ *     kvarn_decode_workspace_bytes(layout, num_seqs, num_q_heads,
+ *     max_seq_len) exceeds KVARN_NOALLOC_SCRATCH_BYTES.
+ * All other arguments, results and errors are those of kvarn_decode.
+ */
+#define KVARN_NOALLOC_SCRATCH_BYTES (16LL * 1024 * 1024)
+
+int32_t kvarn_decode_noalloc(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                             const kvarn_layout* layout, const int32_t* block_table,
+                             int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                             const void* tail_k, const void* tail_v, int32_t num_seqs, float* out,
+                             float* lse, uint32_t* error_flags, kvarn_stream_t stream);
 
 /* Copy the device error word to *host_out (synchronises `stream`). */
 int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,

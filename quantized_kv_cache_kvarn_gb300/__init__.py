@@ -67,7 +67,11 @@ _SIGS = {
     "kvarn_decode_mla": ([_P, _P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P,
                           _I64, _P, _P], _I32),
     "kvarn_read_error_flags": ([_P, _P, _P], _I32),
+    "kvarn_decode_noalloc": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _P],
+                             _I32),
 }
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 EXPORTED = tuple(_SIGS)
 
@@ -210,3 +214,16 @@ def decode_mla(q_latent, q_rope, layout: Layout, cache, block_table, seq_lens, m
                                   _ptr(out), _ptr(lse), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _ptr(err),
                                   _stream(stream)), "decode_mla")
+
+
+def decode_noalloc(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, err, sm_scale,
+                   tail_k=None, tail_v=None, lse=None, stream=None):
+    """kvarn_decode with the split-K scratch in the library's own static
+    device array (NOALLOC_SCRATCH_BYTES per device) instead of a caller
+    workspace; for callers that can not allocate device memory. Calls that
+    overlap on the GPU share that array and race."""
+    B, Hq, _ = q.shape
+    _check(lib().kvarn_decode_noalloc(_ptr(q), Hq, sm_scale, _ptr(cache), ctypes.byref(layout),
+                                      _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
+                                      max_seq_len, _ptr(tail_k), _ptr(tail_v), B, _ptr(out), _ptr(lse),
+                                      _ptr(err), _stream(stream)), "decode_noalloc")
