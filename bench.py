@@ -167,6 +167,8 @@ def run_kvarn(args):
     kv.lib()
 
     wl = W.WORKLOADS[args.workload]
+    if args.num_seqs:
+        wl = wl.with_(num_seqs=args.num_seqs)
     case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
     B, Hq, Hkv, D, L, N = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.context, wl.tile_tokens
     dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
@@ -189,6 +191,20 @@ def run_kvarn(args):
     def step():
         kv.encode_tiles(k_last, v_last, lay, last, bt, cache, err, chunk_tokens=N)
         kv.decode(case.q, lay, cache, bt, case.seq_lens, L, out, ws, err, sm)
+
+    if args.only == "decode":
+        # profiling mode: warm-up and timed launches of the decode call alone
+        for _ in range(args.warmup + args.steps):
+            kv.decode(case.q, lay, cache, bt, case.seq_lens, L, out, ws, err, sm)
+        torch.cuda.synchronize()
+        assert kv.read_error_flags(err) == 0
+        return
+    if args.only == "encode":
+        for _ in range(args.warmup + args.steps):
+            kv.encode_tiles(k_last, v_last, lay, last, bt, cache, err, chunk_tokens=N)
+        torch.cuda.synchronize()
+        assert kv.read_error_flags(err) == 0
+        return
 
     for _ in range(args.warmup):
         step()
@@ -391,6 +407,9 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling a small case)")
+    ap.add_argument("--only", choices=["decode", "encode"], default=None,
+                    help="run only warm-up + timed launches of one call, print nothing (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

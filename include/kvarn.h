@@ -37,21 +37,27 @@
  * scores on raw KV when the query is rotated by the same matrix).
  *
  * Dense page format (one page = P = 16 tokens of one KV head; bytes):
- *   [0, 8D)            K codes, 4-bit, token-major. Within a token: four
+ *   K codes, 8D bytes, 4-bit, token-major. Within a token: four
  *                      lane chunks of D/8 bytes; chunk t holds channels
  *                      16kc + {2t, 2t+1, 2t+8, 2t+9} of every 16-channel
  *                      k-chunk kc. Word w of a chunk serves kc = 2w, 2w+1;
  *                      nibble n (bits 4n..4n+3) holds channel
  *                      16(2w + (n%4)/2) + 2t + 8(n%2) + n/4.
- *   [8D, 12D)          V codes, 2-bit. Lane chunk L = 4g + t (D/8 bytes)
+ *   V codes, 4D bytes, 2-bit. Lane chunk L = 4g + t (D/8 bytes)
  *                      holds channels 8nc + g of every 8-channel block nc at
  *                      tokens {2t, 2t+1, 2t+8, 2t+9}; word w serves blocks
  *                      4w..4w+3; token tau = 2t + e + 8h of block nc sits at
  *                      bit 2(2(nc%4) + h) + 16e of its word.
- *   [12D, +64)         K a[16] fp32       [12D+64, +64)   K b[16] fp32
- *   [12D+128, +64)     V a[16] fp32       [12D+192, +64)  V b[16] fp32
- *   [12D+256, +4C)     K column scales c of this page's slice, C = D*P/N
- *   [12D+256+4C, +4C)  V column scales of the slice
+ * The page is a K part followed by a V part, each contiguous so that the
+ * decode kernel can fetch and recycle them separately:
+ *   K part, KP = 8D + 128 + 4C bytes, C = D*P/N:
+ *     [0, 8D)             K codes (above)
+ *     [8D, +64)           K a[16] fp32     [8D+64, +64)   K b[16] fp32
+ *     [8D+128, +4C)       K column scales c of this page's slice
+ *   V part, at KP:
+ *     [KP, +4D)           V codes (above)
+ *     [KP+4D, +64)        V a[16] fp32     [KP+4D+64, +64) V b[16] fp32
+ *     [KP+4D+128, +4C)    V column scales of the slice
  *   page_bytes = 12D + 256 + 8C  (1920 for D = 128, N = 128).
  * The page at logical index l of a sequence holds the column scales of
  * channels [(l mod N/P) * C, +C) of its tile. All words are little-endian.

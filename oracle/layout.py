@@ -18,9 +18,9 @@ library's own format. A page holds P = 16 tokens of one KV head:
                         tokens {2t, 2t+1, 2t+8, 2t+9}. Word w of a chunk
                         serves blocks 4w..4w+3; the token tau = 2t + e + 8h of
                         block nc sits at bit 2*(2*(nc%4) + h) + 16*e.
-  K a[16], K b[16], V a[16], V b[16]   fp32 row scales of the 16 tokens
-  K col     D*P/N fp32  column scales c of the page's slice of the tile
-  V col     D*P/N fp32
+  The page is two parts, each contiguous: the K part (K codes, then K a[16],
+  K b[16] fp32 row scales, then the K column-scale slice, D*P/N fp32), then
+  the V part (V codes, V a[16], V b[16], V column-scale slice).
 The page at logical index l of a sequence carries the column scales of
 channels [(l mod N/P) * D*P/N, +D*P/N) of its tile; all words little-endian.
 """
@@ -40,15 +40,15 @@ class DenseLayout:
         if N % P:
             raise ValueError("tile must be a whole number of pages")
         self.D, self.N = D, N
-        self.k_codes = 0
-        self.v_codes = 8 * D
-        self.k_a = 12 * D
-        self.k_b = self.k_a + 4 * P
-        self.v_a = self.k_b + 4 * P
-        self.v_b = self.v_a + 4 * P
         self.col_per_page = D * P // N
-        self.k_col = self.v_b + 4 * P
-        self.v_col = self.k_col + 4 * self.col_per_page
+        self.k_codes = 0
+        self.k_a = 8 * D
+        self.k_b = self.k_a + 4 * P
+        self.k_col = self.k_b + 4 * P
+        self.v_codes = self.k_col + 4 * self.col_per_page   # start of the V part
+        self.v_a = self.v_codes + 4 * D
+        self.v_b = self.v_a + 4 * P
+        self.v_col = self.v_b + 4 * P
         self.page_bytes = self.v_col + 4 * self.col_per_page
 
 

@@ -33,7 +33,7 @@ def sources():
 
 
 def _compile(src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *FLAGS, *os.environ.get("KVARN_EXTRA_NVCC", "").split(), "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)

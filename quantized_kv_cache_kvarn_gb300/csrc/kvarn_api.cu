@@ -110,8 +110,10 @@ int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, in
   if (kvarn_layout_check(L) != KVARN_OK || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0)
     return -1;
   if (is_latent(L)) return mla_workspace_bytes(num_seqs, num_q_heads, plan_mla(num_seqs, max_seq_len));
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens, 0);
-  const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 0);
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens,
+                                    dense_decode_warps(L->head_dim),
+                                    dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens));
+  const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
   return std::max(dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan),
                   dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan16));
 }
@@ -146,7 +148,9 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
   if (bt_stride < committed_pages) return KVARN_EINVAL;
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
   if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens, 0);
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens,
+                                    dense_decode_warps(L->head_dim),
+                                    dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens));
   if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
     return KVARN_EWORKSPACE;
   DecodeParams p{};
@@ -222,7 +226,7 @@ int32_t kvarn_decode_fp16(const void* q, int32_t num_q_heads, float sm_scale, co
   if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
   if (bt_stride < (max_seq_len + kPageTokens - 1) / kPageTokens) return KVARN_EINVAL;
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 0);
+  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
   if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
     return KVARN_EWORKSPACE;
   DecodeParams p{};

@@ -14,20 +14,23 @@ constexpr int kPageTokens = 16;
 
 // ---------------------------------------------------------------- layout
 // Byte offsets inside one dense page of one KV head (format documented in
-// kvarn.h). C = D * P / N column scales per page.
+// kvarn.h): a K part (codes, a, b, column slice) then a V part (same order).
+// C = D * P / N column scales per page.
 struct DensePage {
   int D, N;
   __host__ __device__ constexpr DensePage(int d, int n) : D(d), N(n) {}
   __host__ __device__ constexpr int cols() const { return D * kPageTokens / N; }
   __host__ __device__ constexpr int k_codes() const { return 0; }
-  __host__ __device__ constexpr int v_codes() const { return 8 * D; }
-  __host__ __device__ constexpr int k_a() const { return 12 * D; }
-  __host__ __device__ constexpr int k_b() const { return 12 * D + 64; }
-  __host__ __device__ constexpr int v_a() const { return 12 * D + 128; }
-  __host__ __device__ constexpr int v_b() const { return 12 * D + 192; }
-  __host__ __device__ constexpr int k_col() const { return 12 * D + 256; }
-  __host__ __device__ constexpr int v_col() const { return 12 * D + 256 + 4 * cols(); }
-  __host__ __device__ constexpr int bytes() const { return 12 * D + 256 + 8 * cols(); }
+  __host__ __device__ constexpr int k_a() const { return 8 * D; }
+  __host__ __device__ constexpr int k_b() const { return 8 * D + 64; }
+  __host__ __device__ constexpr int k_col() const { return 8 * D + 128; }
+  __host__ __device__ constexpr int k_part() const { return 8 * D + 128 + 4 * cols(); }
+  __host__ __device__ constexpr int v_codes() const { return k_part(); }
+  __host__ __device__ constexpr int v_a() const { return k_part() + 4 * D; }
+  __host__ __device__ constexpr int v_b() const { return k_part() + 4 * D + 64; }
+  __host__ __device__ constexpr int v_col() const { return k_part() + 4 * D + 128; }
+  __host__ __device__ constexpr int v_part() const { return 4 * D + 128 + 4 * cols(); }
+  __host__ __device__ constexpr int bytes() const { return k_part() + v_part(); }
 };
 
 // MLA latent page: codes (dense-K placement), fp16 rope, a, b, column slice.
@@ -86,6 +89,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                    smem_addr(bar)),
                "r"(bytes)
                : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (no completion tracking).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // One-dimensional bulk copy global -> shared, completion counted in bytes on
@@ -157,10 +165,11 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint3
   return r;
 }
 
-// Codes to exact fp16 pairs. A 4-bit field at bits 0-3 (and 16-19) OR-ed
-// into 0x6400 (fp16 1024) is 1024 + n; one at bits 4-7 is 1024 + 16n. The
-// offsets below recentre them: 4-bit codes to n - 8, 2-bit codes to n - 2.
-// Every intermediate is an integer below 2048, so each step is exact in fp16.
+// Codes to exact fp16 integers. A 4-bit field at bits 0-3 (and 16-19)
+// OR-ed into 0x6400 (fp16 1024) is 1024 + n; one at bits 4-7 is 1024 + 16n.
+// The offsets below recentre them: 4-bit codes to n - 8, 2-bit codes to
+// n - 2. Every intermediate is an integer below 2048, so each step is exact
+// and the mma sees ordinary normal fp16 operands.
 constexpr uint32_t kMagic = 0x64006400u;
 
 // One K word -> 4 half2: (kc even: b01, b23), (kc odd: b01, b23).
@@ -168,7 +177,7 @@ __device__ __forceinline__ void dequant_k_word(uint32_t x, uint32_t* out) {
   const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
   const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
   const __half2 o16 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
-  uint32_t y = x >> 8;
+  const uint32_t y = x >> 8;
   out[0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(x, 0x000F000Fu, kMagic)), sub));
   out[1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(x, 0x00F000F0u, kMagic)), s16, o16));
   out[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x000F000Fu, kMagic)), sub));
@@ -186,7 +195,7 @@ __device__ __forceinline__ void dequant_v_word(uint32_t x, uint32_t* out) {
   const __half2 o64 = __halves2half2(__ushort_as_half(0xCC80), __ushort_as_half(0xCC80));  // -18
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    uint32_t y = half ? (x >> 8) : x;
+    const uint32_t y = half ? (x >> 8) : x;
     out[4 * half + 0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x00030003u, kMagic)), sub));
     out[4 * half + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x000C000Cu, kMagic)), s4, o4));
     out[4 * half + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00300030u, kMagic)), s16, o16));

@@ -7,9 +7,12 @@
 // output un-rotated once in the merge (turbo-attn page, "How it works").
 //
 // Kernel 1 (decode_dense_kernel): one CTA per (split, KV head, sequence);
-// each of its W warps owns every W-th tile of the split and streams it into
-// its own two-stage shared-memory ring with one-dimensional bulk copies
-// (one per page, completion counted on an mbarrier). Per tile and warp:
+// each of its W warps owns every W-th tile of the split. A warp keeps one
+// shared-memory slot for the K parts and one for the V parts of its tile's
+// pages, filled by one-dimensional bulk copies (completion counted on an
+// mbarrier), and prefetches the pages of its next tiles into L2. The K slot
+// is refilled with the next tile while P V runs, the V slot while the next
+// Q K runs. Per tile and warp:
 //   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
 //        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
 //        half of the m16 tile free, so the split costs no extra mma);
@@ -35,23 +38,33 @@ namespace kvarn {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// CTAs per SM the 4-warp decode kernel is register-limited to (3 caps it at
+// 168 registers per thread, 2 at 255).
+#ifndef KVARN_DECODE_MIN_CTAS
+#define KVARN_DECODE_MIN_CTAS 3
+#endif
+
 template <int D, int N, int W>
 struct DecShape {
   static constexpr DensePage PG{D, N};
   static constexpr int PPT = N / kPageTokens;
   static constexpr int PB = PG.bytes();
-  static constexpr int TILE = PPT * PB;
+  static constexpr int KP = PG.k_part();
+  static constexpr int VP = PG.v_part();
+  static constexpr int KSLOT = PPT * KP;
+  static constexpr int VSLOT = PPT * VP;
+  static constexpr int WARP_SMEM = KSLOT + VSLOT;
   static constexpr int NB = N / 8;
   static constexpr int KC = D / 16;
   static constexpr int NC = D / 8;
   static constexpr int CPP = PG.cols();
   static constexpr int LW = D / 32;  // words per lane chunk (K and V)
-  static constexpr int STAGES = W * 2 * TILE;
-  static constexpr int SMEM = STAGES + W * 2 * 8 + 8 * D * 4;
-  static_assert(W * 8 * (D + 2) * 4 <= STAGES, "merge scratch must fit in the stage ring");
-  static_assert(PB % 16 == 0, "pages must keep 16-byte alignment");
+  static constexpr int RING = W * WARP_SMEM;
+  static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
+  static constexpr int PREFETCH = 2;  // tiles prefetched into L2 ahead of the K slot
+  static_assert(W * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
 };
-
 
 struct DecArgs {
   const void* q;
@@ -148,13 +161,15 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, int tail, unsign
 }
 
 template <int D, int N, typename T, int W>
-__global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
+__global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) decode_dense_kernel(DecArgs A) {
   using S = DecShape<D, N, W>;
   constexpr DensePage PG{D, N};
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  // KV head is the fastest grid axis: CTAs resident together read the same
+  // physical pages (all heads of a page are contiguous), keeping DRAM rows open
+  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int G = A.G;
 
   int len = A.seq_lens[b];
@@ -176,8 +191,63 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
     return;
   }
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::STAGES);
-  float* qrot = reinterpret_cast<float*>(smem + S::STAGES + W * 2 * 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::RING);
+  float* qrot = reinterpret_cast<float*>(smem + S::RING + W * 2 * 8);
+  int32_t* pages = reinterpret_cast<int32_t*>(smem + S::SMEM);  // this split's page ids
+  unsigned char* kslot = smem + warp * S::WARP_SMEM;
+  unsigned char* vslot = kslot + S::KSLOT;
+  uint64_t* barK = bars + 2 * warp;
+  uint64_t* barV = barK + 1;
+
+  const int first = t0 + warp;
+  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
+  const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
+
+  // the split's block-table entries, checked once, into shared memory
+  for (int e = threadIdx.x; e < (t1 - t0) * S::PPT; e += W * 32) {
+    int phys = bt[t0 * S::PPT + e];
+    if (phys < 0 || phys >= A.num_pages) {
+      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+      phys = 0;
+    }
+    pages[e] = phys;
+  }
+  __syncthreads();
+
+  // physical page `lane` of this warp's i-th tile (lanes < PPT)
+  auto page_of = [&](int i) -> const unsigned char* {
+    const int phys = pages[(first + i * W - t0) * S::PPT + lane];
+    return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB;
+  };
+  auto issue_k = [&](int i) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_of(i), S::KP, barK);
+  };
+  auto issue_v = [&](int i) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
+  };
+  auto prefetch = [&](int i) {
+    if (lane < S::PPT) prefetch_l2(page_of(i), S::PB);
+  };
+
+  if (lane == 0) {
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
+  }
+  fence_mbar_init();
+  __syncwarp();
+  if (n_my > 0) {
+    issue_k(0);
+    issue_v(0);
+  }
+  for (int j = 1; j <= S::PREFETCH && j < n_my; ++j) prefetch(j);
 
   // ---- rotated, scaled query rows of the group (rows >= G are zero)
   for (int h = warp; h < 8; h += W) {
@@ -196,37 +266,7 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
 #pragma unroll
     for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
   }
-  if (lane == 0) {
-    mbar_init(&bars[2 * warp], 1);
-    mbar_init(&bars[2 * warp + 1], 1);
-  }
-  fence_mbar_init();
   __syncthreads();
-
-  const int first = t0 + warp;
-  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
-  unsigned char* ring = smem + warp * 2 * S::TILE;
-  uint64_t* bar = bars + 2 * warp;
-  const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
-
-  auto issue = [&](int i) {
-    const int tile = first + i * W, st = i & 1;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(&bar[st], S::TILE);
-    __syncwarp();
-    if (lane < S::PPT) {
-      int phys = bt[tile * S::PPT + lane];
-      if (phys < 0 || phys >= A.num_pages) {
-        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
-        phys = 0;
-      }
-      bulk_g2s(ring + st * S::TILE + lane * S::PB,
-               A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB, S::PB, &bar[st]);
-    }
-  };
-  if (n_my > 0) issue(0);
-  if (n_my > 1) issue(1);
 
   float m = -INFINITY, lsum = 0.f;
   float acc[S::NC][2];
@@ -234,13 +274,13 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
   for (int nc = 0; nc < S::NC; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
 
   int i = 0;
+  bool timed_out = false;
   for (; i < n_my; ++i) {
-    const int st = i & 1;
-    if (!mbar_wait_bounded(&bar[st], (i >> 1) & 1)) {
-      if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+    const uint32_t par = i & 1;
+    if (!mbar_wait_bounded(barK, par)) {
+      timed_out = true;
       break;
     }
-    const unsigned char* buf = ring + st * S::TILE;
 
     // -- q~ = q' * c_K as fp16 hi/lo A fragments
     uint32_t Aq[S::KC][4];
@@ -250,9 +290,9 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
       const int ch0 = 16 * kc + 2 * t;
       const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
       const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
-      const unsigned char* cp = buf + (ch0 / S::CPP) * S::PB + PG.k_col();
-      const float2 c01 = *reinterpret_cast<const float2*>(cp + (ch0 % S::CPP) * 4);
-      const float2 c89 = *reinterpret_cast<const float2*>(cp + (ch0 % S::CPP) * 4 + 32);
+      const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * 4;
+      const float2 c01 = *reinterpret_cast<const float2*>(cp);
+      const float2 c89 = *reinterpret_cast<const float2*>(cp + 32);
       const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
       qsum += (x0 + x1) + (x8 + x9);
       split_hi_lo(x0, x1, Aq[kc][0], Aq[kc][1]);
@@ -260,35 +300,48 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
     }
     qsum = warp_sum_xor(qsum, 1, 4);
 
-    // -- S = q~ . (K codes - 8)
+    // -- S = q~ . (K codes - 8); four 8-token blocks at a time so that four
+    //    independent accumulator chains hide the mma latency
     float s[S::NB][2];
 #pragma unroll
-    for (int nb = 0; nb < S::NB; ++nb) {
-      const unsigned char* kp =
-          buf + (nb >> 1) * S::PB + ((nb & 1) * 8 + g) * (D / 2) + t * (D / 8);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int nb0 = 0; nb0 < S::NB; nb0 += 4) {
+      float d[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
 #pragma unroll
       for (int q4 = 0; q4 < S::LW / 4; ++q4) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(kp + 16 * q4);
-        const uint32_t words[4] = {kw.x, kw.y, kw.z, kw.w};
+        uint4 kw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int nb = nb0 + j;
+          kw[j] = *reinterpret_cast<const uint4*>(kslot + (nb >> 1) * S::KP + ((nb & 1) * 8 + g) * (D / 2) +
+                                                  t * (D / 8) + 16 * q4);
+        }
 #pragma unroll
         for (int w4 = 0; w4 < 4; ++w4) {
           const int w = 4 * q4 + w4;
-          uint32_t bf[4];
-          dequant_k_word(words[w4], bf);
-          mma_f16(d, Aq[2 * w][0], Aq[2 * w][1], Aq[2 * w][2], Aq[2 * w][3], bf[0], bf[1]);
-          mma_f16(d, Aq[2 * w + 1][0], Aq[2 * w + 1][1], Aq[2 * w + 1][2], Aq[2 * w + 1][3], bf[2], bf[3]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t word = w4 == 0 ? kw[j].x : w4 == 1 ? kw[j].y : w4 == 2 ? kw[j].z : kw[j].w;
+            uint32_t bf[4];
+            dequant_k_word(word, bf);
+            mma_f16(d[j], Aq[2 * w][0], Aq[2 * w][1], Aq[2 * w][2], Aq[2 * w][3], bf[0], bf[1]);
+            mma_f16(d[j], Aq[2 * w + 1][0], Aq[2 * w + 1][1], Aq[2 * w + 1][2], Aq[2 * w + 1][3], bf[2], bf[3]);
+          }
         }
       }
-      s[nb][0] = d[0] + d[2];
-      s[nb][1] = d[1] + d[3];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s[nb0 + j][0] = d[j][0] + d[j][2];
+        s[nb0 + j][1] = d[j][1] + d[j][3];
+      }
     }
 
     // -- row-scale fold and online softmax (base 2)
     float mt = -INFINITY;
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
-      const unsigned char* pg = buf + (nb >> 1) * S::PB;
+      const unsigned char* pg = kslot + (nb >> 1) * S::KP;
       const int idx = (nb & 1) * 8 + 2 * t;
       const float2 ka = *reinterpret_cast<const float2*>(pg + PG.k_a() + idx * 4);
       const float2 kb = *reinterpret_cast<const float2*>(pg + PG.k_b() + idx * 4);
@@ -309,16 +362,25 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
     lsum = fmaf(lsum, alpha, psum);
     m = m_new;
 
+    // the K slot is free: start the next tile's K part, prefetch further
+    if (i + 1 < n_my) issue_k(i + 1);
+    if (i + 1 + S::PREFETCH < n_my) prefetch(i + 1 + S::PREFETCH);
+
+    if (!mbar_wait_bounded(barV, par)) {
+      timed_out = true;
+      break;
+    }
+
     // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
     uint32_t Ap[S::PPT][4];
     float beta = 0.f;
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
-      const unsigned char* pg = buf + pp * S::PB;
-      const float2 va0 = *reinterpret_cast<const float2*>(pg + PG.v_a() + (2 * t) * 4);
-      const float2 va1 = *reinterpret_cast<const float2*>(pg + PG.v_a() + (8 + 2 * t) * 4);
-      const float2 vb0 = *reinterpret_cast<const float2*>(pg + PG.v_b() + (2 * t) * 4);
-      const float2 vb1 = *reinterpret_cast<const float2*>(pg + PG.v_b() + (8 + 2 * t) * 4);
+      const unsigned char* pg = vslot + pp * S::VP;
+      const float2 va0 = *reinterpret_cast<const float2*>(pg + PG.v_a() - S::KP + (2 * t) * 4);
+      const float2 va1 = *reinterpret_cast<const float2*>(pg + PG.v_a() - S::KP + (8 + 2 * t) * 4);
+      const float2 vb0 = *reinterpret_cast<const float2*>(pg + PG.v_b() - S::KP + (2 * t) * 4);
+      const float2 vb1 = *reinterpret_cast<const float2*>(pg + PG.v_b() - S::KP + (8 + 2 * t) * 4);
       const float p00 = s[2 * pp][0], p01 = s[2 * pp][1], p10 = s[2 * pp + 1][0], p11 = s[2 * pp + 1][1];
       beta = fmaf(p00, fmaf(2.f, va0.x, vb0.x), beta);
       beta = fmaf(p01, fmaf(2.f, va0.y, vb0.y), beta);
@@ -330,42 +392,50 @@ __global__ void __launch_bounds__(W * 32) decode_dense_kernel(DecArgs A) {
     beta = warp_sum_xor(beta, 1, 4);
 
 #pragma unroll
-    for (int half = 0; half < S::LW / 4; ++half) {
-      float u[16][4];
+    for (int nc = 0; nc < S::NC; ++nc) {
+      acc[nc][0] *= alpha;
+      acc[nc][1] *= alpha;
+    }
+    // channel blocks in groups of eight (two words of the lane chunk)
 #pragma unroll
-      for (int k = 0; k < 16; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
+    for (int hq = 0; hq < S::LW / 2; ++hq) {
+      float u[8][4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
 #pragma unroll
       for (int pp = 0; pp < S::PPT; ++pp) {
-        const uint4 vw = *reinterpret_cast<const uint4*>(buf + pp * S::PB + PG.v_codes() +
-                                                         (4 * g + t) * (D / 8) + 16 * half);
-        const uint32_t words[4] = {vw.x, vw.y, vw.z, vw.w};
+        const uint2 vw = *reinterpret_cast<const uint2*>(vslot + pp * S::VP + (4 * g + t) * (D / 8) + 8 * hq);
+        uint32_t bf[8];
+        dequant_v_word(vw.x, bf);
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          uint32_t bf[8];
-          dequant_v_word(words[w4], bf);
+        for (int k = 0; k < 4; ++k)
+          mma_f16(u[k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
+        dequant_v_word(vw.y, bf);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f16(u[4 * w4 + k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
-        }
+        for (int k = 0; k < 4; ++k)
+          mma_f16(u[4 + k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
       }
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int nc = 16 * half + k;
+      for (int k = 0; k < 8; ++k) {
+        const int nc = 8 * hq + k;
         const int ch = 8 * nc + 2 * t;
-        const float2 cv = *reinterpret_cast<const float2*>(buf + (ch / S::CPP) * S::PB + PG.v_col() +
-                                                           (ch % S::CPP) * 4);
-        acc[nc][0] = fmaf(acc[nc][0], alpha, cv.x * ((u[k][0] + u[k][2]) + beta));
-        acc[nc][1] = fmaf(acc[nc][1], alpha, cv.y * ((u[k][1] + u[k][3]) + beta));
+        const float2 cv = *reinterpret_cast<const float2*>(vslot + (ch / S::CPP) * S::VP + PG.v_col() -
+                                                           S::KP + (ch % S::CPP) * 4);
+        acc[nc][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[nc][0]);
+        acc[nc][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[nc][1]);
       }
     }
-    if (i + 2 < n_my) issue(i + 2);
+    if (i + 1 < n_my) issue_v(i + 1);
   }
-  if (i < n_my) {  // gave up on a copy: wait (bounded) for what is still in flight
-    for (int j = i; j < min(n_my, i + 2); ++j) mbar_wait_bounded(&bar[j & 1], (j >> 1) & 1, 100000000LL);
+  if (timed_out) {
+    if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+    // wait (bounded) for the copies this warp still has in flight
+    mbar_wait_bounded(barK, i & 1, 100000000LL);
+    mbar_wait_bounded(barV, i & 1, 100000000LL);
   }
   lsum = warp_sum_xor(lsum, 1, 4);
 
-  // ---- merge the W warps of the CTA (scratch aliases the stage ring)
+  // ---- merge the W warps of the CTA (scratch aliases the slots)
   __syncthreads();
   float* mrg = reinterpret_cast<float*>(smem);
   float* mw = mrg + warp * 8 * (D + 2);
@@ -412,28 +482,64 @@ int device_sm_count() {
   return n;
 }
 
-// Warps per CTA for a dense decode variant.
-static int dense_warps(int D) { return D == 256 ? 1 : 2; }
-
 SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
-                     int32_t /*unused*/) {
+                     int32_t warps, int32_t ctas_per_sm) {
   SplitPlan p{};
   const int tiles = max_seq_len / N;
   const int units = std::max(1, num_seqs * num_kv_heads);
-  const int W = 2;
   if (tiles == 0) {
     p.tiles_per_split = 1;
     p.nsplit = 0;
   } else {
-    const int target = device_sm_count() * 3 * 3;  // about three waves of three CTAs per SM
-    int want = (target + units - 1) / units;
-    const int max_split = std::max(1, (tiles + 2 * W - 1) / (2 * W));  // >= 2 tiles per warp
-    want = std::min(std::max(want, 1), max_split);
-    p.tiles_per_split = (tiles + want - 1) / want;
+    // Split count whose CTA count fills whole waves best (resident CTAs per
+    // SM times the SM count), keeping at least 4 tiles per warp; ties go to
+    // fewer splits (fewer partials to merge).
+    const double slots = static_cast<double>(device_sm_count()) * ctas_per_sm;
+    const int max_split = std::max(1, tiles / (4 * warps));
+    int best = 1;
+    double best_eff = 0.0;
+    for (int n = 1; n <= max_split; ++n) {
+      const double waves = units * static_cast<double>(n) / slots;
+      const double eff = waves / std::ceil(waves);
+      if (eff > best_eff + 0.02) {
+        best_eff = eff;
+        best = n;
+      }
+    }
+    p.tiles_per_split = (tiles + best - 1) / best;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
   }
   p.slots = p.nsplit + 1;
   return p;
+}
+
+int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
+
+template <int D, int N, typename T, int W>
+static int resident_ctas() {
+  using S = DecShape<D, N, W>;
+  auto kern = decode_dense_kernel<D, N, T, W>;
+  const int smem = S::SMEM + 48 * S::PPT * 4;  // with a typical split's page ids
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, smem) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
+// CTAs of the compressed decode kernel that fit on one SM at once (same for
+// fp16 and bf16 queries, which share the register and smem footprint).
+int dense_decode_ctas_per_sm(int32_t D, int32_t N) {
+  static int cache[2][2] = {{0, 0}, {0, 0}};
+  const int di = D == 256, ni = N == 64;
+  if (!cache[di][ni]) {
+    if (D == 128 && N == 128) cache[di][ni] = resident_ctas<128, 128, __half, 4>();
+    else if (D == 128) cache[di][ni] = resident_ctas<128, 64, __half, 4>();
+    else if (N == 128) cache[di][ni] = resident_ctas<256, 128, __half, 2>();
+    else cache[di][ni] = resident_ctas<256, 64, __half, 2>();
+  }
+  return cache[di][ni];
 }
 
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
@@ -445,10 +551,11 @@ template <int D, int N, typename T, int W>
 static cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
   using S = DecShape<D, N, W>;
   auto kern = decode_dense_kernel<D, N, T, W>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  const int smem = S::SMEM + A.tps * S::PPT * 4;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(A.nsplit + 1, A.Hkv, num_seqs);
-  kern<<<grid, W * 32, S::SMEM, st>>>(A);
+  dim3 grid(A.Hkv, A.nsplit + 1, num_seqs);
+  kern<<<grid, W * 32, smem, st>>>(A);
   return cudaGetLastError();
 }
 
@@ -478,8 +585,8 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   if (p.D == DD && p.N == NN)                                                         \
     e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW>(A, p.num_seqs, st)              \
                : run_dense<DD, NN, __half, WW>(A, p.num_seqs, st);
-  KV_DISPATCH(128, 128, 2)
-  KV_DISPATCH(128, 64, 2)
+  KV_DISPATCH(128, 128, 4)
+  KV_DISPATCH(128, 64, 4)
   KV_DISPATCH(256, 128, 2)
   KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH

@@ -68,7 +68,9 @@ struct SplitPlan {
 };
 
 SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
-                     int32_t tokens_per_unit_min);
+                     int32_t warps, int32_t ctas_per_sm);
+int dense_decode_warps(int32_t D);
+int dense_decode_ctas_per_sm(int32_t D, int32_t N);
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
                               const SplitPlan& plan);
 
