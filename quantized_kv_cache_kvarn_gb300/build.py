@@ -32,8 +32,14 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+# The aarch64 ptxas of CUDA 13.0.88 crashes (SIGSEGV) on the MLA decode kernel
+# at -O2 and above; the x86 one does not. Both hosts use the same level.
+PER_FILE = {"kvarn_mla.cu": ["-Xptxas", "-O1"]}
+
+
 def _compile(src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc(), *ARCH, *FLAGS, *os.environ.get("KVARN_EXTRA_NVCC", "").split(), "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *FLAGS, *PER_FILE.get(os.path.basename(src), []),
+           *os.environ.get("KVARN_EXTRA_NVCC", "").split(), "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
