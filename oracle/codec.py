@@ -17,7 +17,9 @@ notes):
   * One normalisation iteration is a column pass then a row pass. A pass
     divides by the population standard deviation (ddof=0) about the mean and
     adds log(sigma) to the running log-scale; scales leave log space once, at
-    the end. A sigma that is zero or not finite is replaced by 1.
+    the end. A vector that is numerically constant - sigma <= 2^-20 |mean|,
+    which covers sigma = 0 and the rounding residue of an exactly constant
+    vector - or whose sigma is not finite keeps sigma = 1.
   * Quantisation is per token row of the normalised tile: lo = min, hi = max,
     delta = (hi - lo) / (2^bits - 1), code = clamp(rint((z - lo) / delta)),
     rint being round-half-to-even. A row with hi == lo gets delta = 0 and all
@@ -52,10 +54,15 @@ def rotate(X: np.ndarray) -> np.ndarray:
     return X @ hadamard(X.shape[-1])
 
 
+CONSTANT_REL = 2.0 ** -20
+
+
 def pop_std(Z: np.ndarray, axis: int) -> np.ndarray:
-    """Population standard deviation along ``axis``; zero or non-finite -> 1."""
+    """Population standard deviation along ``axis``; 1 for a numerically
+    constant vector (std <= 2^-20 |mean|) or a non-finite std."""
     s = np.std(Z, axis=axis, ddof=0)
-    return np.where(np.isfinite(s) & (s > 0), s, 1.0)
+    mu = np.abs(np.mean(Z, axis=axis))
+    return np.where(np.isfinite(s) & (s > CONSTANT_REL * mu), s, 1.0)
 
 
 def column_pass(Z: np.ndarray):

@@ -105,10 +105,12 @@ __device__ __forceinline__ void column_sum(float (&s)[16], float* red, float* co
   }
 }
 
-// Pop std -> 1 where it is zero or not finite.
-__device__ __forceinline__ float safe_sigma(float var) {
-  float s = sqrtf(var);
-  return (s > 0.f && isfinite(s)) ? s : 1.f;
+// Population std; 1 for a numerically constant vector (std <= 2^-20 |mean|,
+// which covers the rounding residue of an exactly constant one) or a
+// non-finite std.
+__device__ __forceinline__ float safe_sigma(float var, float mean) {
+  const float s = sqrtf(var);
+  return (isfinite(s) && s > 9.5367431640625e-07f * fabsf(mean)) ? s : 1.f;
 }
 
 template <int D, int N, int CS, int BITS, int KIND, typename T>
@@ -139,8 +141,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     load8<T>(p + 8, x[i] + 8);
   }
 
-  // ---- Hadamard: 4 in-register stages, then lane butterflies (unscaled;
-  // the 1/sqrt(D) factor folds into the column scales at the end)
+  // ---- Hadamard: 4 in-register stages, then lane butterflies, then 1/sqrt(D)
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
 #pragma unroll
@@ -163,6 +164,14 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
         float p = __shfl_xor_sync(0xffffffffu, x[i][e], d);
         x[i][e] = upper ? p - x[i][e] : x[i][e] + p;
       }
+  }
+
+  {
+    const float rsd = 1.f / sqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= rsd;
   }
 
   // ---- variance normalisation, T iterations of (column pass, row pass)
@@ -199,7 +208,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     column_sum<D, N, CS>(s, red, colbuf, colpart);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float sig = safe_sigma(s[e] * invN);
+      const float sig = safe_sigma(s[e] * invN, mean[e]);
       logc[e] += logf(sig);
       const float inv = 1.f / sig;
 #pragma unroll
@@ -220,7 +229,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
         v = fmaf(dv, dv, v);
       }
       v = warp_sum_xor(v, 1, S::TPR);
-      const float sig = safe_sigma(v * invD);
+      const float sig = safe_sigma(v * invD, m);
       logr[i] += logf(sig);
       const float inv = 1.f / sig;
 #pragma unroll
@@ -261,9 +270,8 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     }
   }
   if (warp == 0 && rsub == 0) {
-    const float rsd = rsqrtf(static_cast<float>(D));
 #pragma unroll
-    for (int e = 0; e < 16; ++e) colC[seg * 16 + e] = expf(logc[e]) * rsd;
+    for (int e = 0; e < 16; ++e) colC[seg * 16 + e] = expf(logc[e]);
   }
   __syncthreads();
 

@@ -8,7 +8,8 @@ Tolerances (from the problem statement of this codec):
     normalisation passes, about twenty roundings of quantities up to a few
     times the row's std; with delta >= range/15 that moves x by at most
     ~2e-5 code units. CODE_BAND = 2^-13 (1.2e-4) leaves a 5x margin;
-  * scales a, b, c to relative 1e-5;
+  * scales a, b, c to relative 1e-5 (b relative to the larger of |b| and
+    the row range |a| (2^bits - 1), its natural scale);
   * attention output to max abs 2e-3 (fp32 accumulation).
 """
 from __future__ import annotations
@@ -42,9 +43,17 @@ def compare_tile(gpu: dict, ref: dict, bits: int, stats: dict):
         stats["max_dist"] = max(stats["max_dist"], float(dist.max()))
     stats["mismatch"] += int(mism.sum())
     stats["codes"] += mism.size
-    for key, rows in (("a", None), ("b", None), ("c", None)):
+    qmax = (1 << bits) - 1
+    ref_a = ref["a"].astype(np.float32).astype(np.float64)
+    for key in ("a", "b", "c"):
         g, r = gpu[key], ref[key].astype(np.float32).astype(np.float64)
-        rel = np.abs(g - r) / np.maximum(np.abs(r), 1e-30)
+        denom = np.abs(r)
+        if key == "b":
+            # the row offset lives on the row's quantisation grid: its scale is
+            # the row range |a| (2^bits - 1), which also covers an offset that
+            # is zero up to rounding (a constant row after rotation)
+            denom = np.maximum(denom, np.abs(ref_a) * qmax)
+        rel = np.abs(g - r) / np.maximum(denom, 1e-30)
         stats["scale_rel"] = max(stats["scale_rel"], float(rel.max()))
 
 

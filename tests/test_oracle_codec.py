@@ -142,6 +142,20 @@ def test_normalize_scale_equivariance():
     np.testing.assert_allclose(np.outer(r2, c2), 8.0 * np.outer(r1, c1), rtol=1e-12)
 
 
+def test_normalize_constant_vectors_keep_unit_scale():
+    """A constant column (any value) and a constant row are left unscaled;
+    the rounding residue of the mean does not count as spread."""
+    rng = np.random.default_rng(13)
+    Y = rng.standard_normal((128, 64))
+    Y[:, 5] = 0.1 * 3 + 1e-3          # constant column, value not exact in binary
+    Z, ls = codec.column_pass(Y)
+    assert ls[5] == 0.0 and np.all(Z[:, 5] == Y[:, 5])
+    R = np.tile(np.array([[7.3]]), (4, 32))
+    Zr, lr = codec.row_pass(R)
+    np.testing.assert_array_equal(lr, 0.0)
+    np.testing.assert_array_equal(Zr, R)
+
+
 def test_normalize_zero_column_stays_finite():
     Y = np.random.default_rng(9).standard_normal((16, 8))
     Y[:, 3] = 0.0
