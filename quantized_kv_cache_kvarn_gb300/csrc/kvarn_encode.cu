@@ -2,16 +2,18 @@
 //
 // KVarN review ("KVarN ... vLLM KV cache quantization"), four-stage
 // paragraph: rotate each tile by an orthonormal Hadamard matrix across the
-// channels, run T alternating column/row standard-deviation normalisations
-// with the scales in log space, then asymmetric round-to-nearest with the
-// scales folded into the stored row offsets. One CTA (or a cluster of two
-// for head_dim 512) owns one N x D tile and keeps it in registers: every
-// thread holds a 16-channel segment of N/32 token rows. The Hadamard
-// transform runs as four in-register butterfly stages and log2(D/16) lane
-// shuffles; column statistics reduce through shared memory (and the peer
-// CTA's shared memory in a cluster); row statistics reduce with shuffles.
-// Codes are staged in shared memory as bytes and then packed into the page
-// format that the decode kernel reads as mma fragments.
+// channels, run T alternating column/row standard-deviation normalisations,
+// then asymmetric round-to-nearest with the scales folded into the stored
+// row offsets. One CTA (or a cluster of two for head_dim 512) owns one N x D
+// tile and keeps it in registers: every thread holds a 16-channel segment of
+// N/32 token rows. The Hadamard transform runs as four in-register butterfly
+// stages and log2(D/16) lane shuffles. Column statistics reduce through
+// shared memory (and the peer CTA's shared memory in a cluster) and are
+// finished once per channel by thread `channel`, which broadcasts the result;
+// row statistics reduce with shuffles. The scales accumulate as products of
+// the per-pass standard deviations (the exponential of the summed logs, up
+// to rounding). Codes are packed in registers straight into the page's word
+// order, staged in shared memory and written out in 16-byte stores.
 #include <cooperative_groups.h>
 
 #include "kvarn_common.cuh"
@@ -31,12 +33,20 @@ struct EncShape {
   static constexpr int NW = NT / 32;          // warps
   static constexpr int ROWS = N / CS;         // rows owned by this CTA
   static constexpr int RPT = N / 32;          // rows per thread
+  static constexpr int PPC = ROWS / kPageTokens;  // pages per CTA
   static_assert(ROWS == RPT * NW * RPW, "tile rows must cover the CTA");
+  static_assert(NT >= D, "one thread per channel finishes the column statistics");
   static constexpr int RED_BYTES = NW * D * 4;
-  static constexpr int CODE_BYTES = ROWS * D;
+  static constexpr int CODE_BYTES = ROWS * D / 2;  // packed K words or V staging bytes
   static constexpr int SCRATCH = RED_BYTES > CODE_BYTES ? RED_BYTES : CODE_BYTES;
-  // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][D] (cluster)
-  static constexpr int SMEM = SCRATCH + 4 * D + 8 * ROWS + 4 * D + 8 * D;
+  // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][D] | pages[PPC]
+  static constexpr int OFF_COLBUF = SCRATCH;
+  static constexpr int OFF_ROWA = OFF_COLBUF + 4 * D;
+  static constexpr int OFF_ROWB = OFF_ROWA + 4 * ROWS;
+  static constexpr int OFF_COLC = OFF_ROWB + 4 * ROWS;
+  static constexpr int OFF_COLPART = OFF_COLC + 4 * D;
+  static constexpr int OFF_PAGES = OFF_COLPART + 8 * D;
+  static constexpr int SMEM = OFF_PAGES + 8 * PPC;
 };
 
 struct EncodeArgs {
@@ -44,6 +54,7 @@ struct EncodeArgs {
   const __half* rope;      // latent only
   int64_t seq_stride, head_stride, rope_seq_stride;
   int32_t chunk_tiles;
+  int32_t num_seqs;
   const int32_t* tile_start;
   const int32_t* block_table;
   int32_t bt_stride;
@@ -57,15 +68,18 @@ struct EncodeArgs {
 };
 
 // Column statistic: every thread passes its 16 per-channel partial sums over
-// its rows; returns the full sums over the tile (all CS CTAs) for its 16
-// channels.
+// its rows. Returns, in thread tid < D, the sum over the whole tile (both
+// CTAs of a cluster) for channel tid; other threads get 0. colpart is the
+// buffer of this statistic (callers alternate two), so that one cluster
+// barrier per statistic keeps a fast CTA from overwriting a partial that its
+// peer has not read yet.
 template <int D, int N, int CS>
-__device__ __forceinline__ void column_sum(float (&s)[16], float* red, float* colbuf,
-                                           float* colpart) {
+__device__ __forceinline__ float column_total(float (&s)[16], float* red, float* colpart) {
   using S = EncShape<D, N, CS>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, seg = lane % S::TPR;
 #pragma unroll
   for (int e = 0; e < 16; ++e)
+#pragma unroll
     for (int o = S::TPR; o < 32; o <<= 1) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
   if (lane < S::TPR) {
     float4* dst = reinterpret_cast<float4*>(red + warp * D + seg * 16);
@@ -73,35 +87,32 @@ __device__ __forceinline__ void column_sum(float (&s)[16], float* red, float* co
     for (int e = 0; e < 4; ++e) dst[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
   }
   __syncthreads();
+  float t = 0.f;
   if (threadIdx.x < D) {
-    float t = 0.f;
 #pragma unroll 8
     for (int w = 0; w < S::NW; ++w) t += red[w * D + threadIdx.x];
-    if constexpr (CS == 1) {
-      colbuf[threadIdx.x] = t;
-    } else {
-      colpart[threadIdx.x] = t;
-    }
   }
-  if constexpr (CS == 1) {
-    __syncthreads();
-  } else {
+  if constexpr (CS > 1) {
     cg::cluster_group cl = cg::this_cluster();
+    if (threadIdx.x < D) colpart[threadIdx.x] = t;
     cl.sync();
     if (threadIdx.x < D) {
-      float own = colpart[threadIdx.x];
-      float* peer = cl.map_shared_rank(colpart, cl.block_rank() ^ 1);
-      float other = peer[threadIdx.x];
+      const float other = cl.map_shared_rank(colpart, cl.block_rank() ^ 1)[threadIdx.x];
       // both CTAs add in rank order, so they hold bit-identical sums
-      colbuf[threadIdx.x] = cl.block_rank() == 0 ? own + other : other + own;
+      t = cl.block_rank() == 0 ? t + other : other + t;
     }
-    cl.sync();
   }
+  return t;
+}
+
+// Reads the 16 broadcast per-channel values of this thread's segment.
+template <int D>
+__device__ __forceinline__ void read_segment(float (&v)[16], const float* colbuf, int seg) {
   const float4* src = reinterpret_cast<const float4*>(colbuf + seg * 16);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    float4 v = src[e];
-    s[4 * e] = v.x; s[4 * e + 1] = v.y; s[4 * e + 2] = v.z; s[4 * e + 3] = v.w;
+    const float4 f = src[e];
+    v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
   }
 }
 
@@ -113,23 +124,35 @@ __device__ __forceinline__ float safe_sigma(float var, float mean) {
   return (isfinite(s) && s > 9.5367431640625e-07f * fabsf(mean)) ? s : 1.f;
 }
 
+// 4-bit page order (K and the MLA latent): in a page, the 32-bit word
+// tau * (D/8) + t * (D/32) + w of token tau holds, at nibbles 0,1,4,5, the
+// codes of channels 2t, 2t+8, 2t+1, 2t+9 of 16-channel segment 2w and, at
+// nibbles 2,3,6,7, the same channels of segment 2w+1 (the B-fragment order
+// of an m16n8k16 mma). `P` holds the row's 16 codes of one segment as bytes;
+// returns this segment's nibbles of word t, placed for segment parity `s`.
+__device__ __forceinline__ uint32_t k_word_part(const uint32_t (&P)[4], int t, int s) {
+  const uint32_t v = __byte_perm(P[t >> 1], P[2 + (t >> 1)], (t & 1) ? 0x7362 : 0x5140);
+  return ((v | (v >> 4)) & 0x00FF00FFu) << (8 * s);
+}
+
 template <int D, int N, int CS, int BITS, int KIND, typename T>
 __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __restrict__ src,
-                                            int b, int head, int u, int which,
-                                            unsigned char* smem) {
+                                            int b, int head, int u, unsigned char* smem) {
   using S = EncShape<D, N, CS>;
+  constexpr bool IS_V = KIND == 0 && BITS == 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int seg = lane % S::TPR, rsub = lane / S::TPR;
   int crank = 0;
   if constexpr (CS > 1) crank = static_cast<int>(cg::this_cluster().block_rank());
 
   float* red = reinterpret_cast<float*>(smem);
-  unsigned char* codes = smem;  // aliases red once the statistics are done
-  float* colbuf = reinterpret_cast<float*>(smem + S::SCRATCH);
-  float* rowA = colbuf + D;
-  float* rowB = rowA + S::ROWS;
-  float* colC = rowB + S::ROWS;
-  float* colpart = colC + D;
+  unsigned char* stage = smem;  // aliases red once the statistics are done
+  float* colbuf = reinterpret_cast<float*>(smem + S::OFF_COLBUF);
+  float* rowA = reinterpret_cast<float*>(smem + S::OFF_ROWA);
+  float* rowB = reinterpret_cast<float*>(smem + S::OFF_ROWB);
+  float* colC = reinterpret_cast<float*>(smem + S::OFF_COLC);
+  float* colpart = reinterpret_cast<float*>(smem + S::OFF_COLPART);
+  uint8_t** pages = reinterpret_cast<uint8_t**>(smem + S::OFF_PAGES);
 
   // ---- load: row r_local(i) = i*32 + warp*RPW + rsub (within this CTA's rows)
   float x[S::RPT][16];
@@ -139,6 +162,20 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     const T* p = src + static_cast<int64_t>(r) * D + seg * 16;
     load8<T>(p, x[i]);
     load8<T>(p + 8, x[i] + 8);
+  }
+
+  // ---- page addresses of this CTA's rows (read by the stores at the end)
+  constexpr int PPT = N / kPageTokens;  // pages per tile
+  if (tid < S::PPC) {
+    const int64_t lp = (static_cast<int64_t>(A.tile_start[b]) + u) * PPT + crank * S::PPC + tid;
+    uint8_t* pg = nullptr;
+    const int32_t phys =
+        (lp >= 0 && lp < A.bt_stride) ? A.block_table[static_cast<int64_t>(b) * A.bt_stride + lp] : -1;
+    if (phys >= 0 && phys < A.num_pages)
+      pg = A.cache + (static_cast<int64_t>(phys) * A.num_kv_heads + head) * A.page_bytes;
+    else
+      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+    pages[tid] = pg;
   }
 
   // ---- Hadamard: 4 in-register stages, then lane butterflies, then 1/sqrt(D)
@@ -156,16 +193,13 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   }
 #pragma unroll
   for (int d = 1; d < S::TPR; d <<= 1) {
-    const bool upper = lane & d;
+    // lower lane: x + partner; upper lane: partner - x  (one FFMA either way)
+    const float sgn = (lane & d) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float p = __shfl_xor_sync(0xffffffffu, x[i][e], d);
-        x[i][e] = upper ? p - x[i][e] : x[i][e] + p;
-      }
+      for (int e = 0; e < 16; ++e) x[i][e] = fmaf(sgn, x[i][e], __shfl_xor_sync(0xffffffffu, x[i][e], d));
   }
-
   {
     const float rsd = 1.f / sqrtf(static_cast<float>(D));
 #pragma unroll
@@ -175,15 +209,16 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   }
 
   // ---- variance normalisation, T iterations of (column pass, row pass)
-  float logc[16], logr[S::RPT];
+  float cscale = 1.f;  // column scale of channel tid (tid < D)
+  float rscale[S::RPT];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) logc[e] = 0.f;
-#pragma unroll
-  for (int i = 0; i < S::RPT; ++i) logr[i] = 0.f;
+  for (int i = 0; i < S::RPT; ++i) rscale[i] = 1.f;
   const float invN = 1.f / N, invD = 1.f / D;
 
+#pragma unroll 1
   for (int it = 0; it < A.norm_iters; ++it) {
     float s[16];
+    // column means
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       float t = 0.f;
@@ -191,29 +226,36 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       for (int i = 0; i < S::RPT; ++i) t += x[i][e];
       s[e] = t;
     }
-    column_sum<D, N, CS>(s, red, colbuf, colpart);
+    const float cmean = column_total<D, N, CS>(s, red, colpart) * invN;
+    if (tid < D) colbuf[tid] = cmean;
+    __syncthreads();
     float mean[16];
+    read_segment<D>(mean, colbuf, seg);
+    // column variances about the mean
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      mean[e] = s[e] * invN;
       float t = 0.f;
 #pragma unroll
       for (int i = 0; i < S::RPT; ++i) {
-        float dv = x[i][e] - mean[e];
+        const float dv = x[i][e] - mean[e];
         t = fmaf(dv, dv, t);
       }
       s[e] = t;
     }
-    __syncthreads();  // red is reused
-    column_sum<D, N, CS>(s, red, colbuf, colpart);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float sig = safe_sigma(s[e] * invN, mean[e]);
-      logc[e] += logf(sig);
-      const float inv = 1.f / sig;
-#pragma unroll
-      for (int i = 0; i < S::RPT; ++i) x[i][e] *= inv;
+    const float cvar = column_total<D, N, CS>(s, red, colpart + D) * invN;
+    __syncthreads();  // every thread has read the means out of colbuf
+    if (tid < D) {
+      const float sig = safe_sigma(cvar, cmean);
+      cscale *= sig;
+      colbuf[tid] = 1.f / sig;
     }
+    __syncthreads();
+    float inv[16];
+    read_segment<D>(inv, colbuf, seg);
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= inv[e];
     // row pass: a row lives in TPR consecutive lanes
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i) {
@@ -225,21 +267,22 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       float v = 0.f;
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        float dv = x[i][e] - m;
+        const float dv = x[i][e] - m;
         v = fmaf(dv, dv, v);
       }
       v = warp_sum_xor(v, 1, S::TPR);
       const float sig = safe_sigma(v * invD, m);
-      logr[i] += logf(sig);
-      const float inv = 1.f / sig;
+      rscale[i] *= sig;
+      const float ri = 1.f / sig;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] *= inv;
+      for (int e = 0; e < 16; ++e) x[i][e] *= ri;
     }
-    __syncthreads();
+    __syncthreads();  // colbuf is rewritten by the next iteration
   }
 
-  // ---- asymmetric RTN per row
+  // ---- asymmetric RTN per row; codes packed into page word order in `stage`
   constexpr int QMAX = (1 << BITS) - 1;
+  const int s_par = seg & 1, w_pair = seg >> 1;
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
     float lo = x[i][0], hi = x[i][0];
@@ -248,106 +291,77 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       lo = fminf(lo, x[i][e]);
       hi = fmaxf(hi, x[i][e]);
     }
+#pragma unroll
     for (int o = 1; o < S::TPR; o <<= 1) {
       lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
     const float delta = (hi - lo) / static_cast<float>(QMAX);
-    const float inv = delta > 0.f ? 1.f / delta : 0.f;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    const float rinv = delta > 0.f ? 1.f / delta : 0.f;
+    uint32_t P[4];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      int q = __float2int_rn((x[i][e] - lo) * inv);
-      q = min(max(q, 0), QMAX);
-      w[e >> 2] |= static_cast<uint32_t>(q) << (8 * (e & 3));
+    for (int k = 0; k < 4; ++k) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // x - lo lies in [0, hi - lo], so the rounded quotient lies in
+        // [0, QMAX]; the unsigned conversion saturates and min() only
+        // guards non-finite input
+        const uint32_t q = min(__float2uint_rn((x[i][4 * k + e] - lo) * rinv), static_cast<uint32_t>(QMAX));
+        word |= q << (8 * e);
+      }
+      P[k] = word;
     }
     const int r = i * (S::NW * S::RPW) + warp * S::RPW + rsub;  // local row
-    *reinterpret_cast<uint4*>(codes + r * D + seg * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    const int pg = r / kPageTokens, tau = r % kPageTokens;
+    if constexpr (!IS_V) {
+      // each lane pair shares words; the even lane writes t = 0, 1, the odd lane t = 2, 3
+      uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D + tau * (D / 8) + w_pair;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t lo_t = k_word_part(P, j, s_par), hi_t = k_word_part(P, 2 + j, s_par);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, s_par ? lo_t : hi_t, 1);
+        img[(2 * s_par + j) * (D / 32)] = (s_par ? hi_t : lo_t) | other;
+      }
+    } else {
+      // 2-bit V page order: word (4g + t) * (D/32) + w holds, for tokens
+      // 2t + e + 8h and channels 32w + g + 8j, the code at bit 4j + 2h + 16e.
+      // The thread's byte for group g (codes of channels g and g + 8 of its
+      // segment, nibble-spaced) is staged at byte 4h + 2e + s of that word's
+      // 8-byte slot; the copy-out folds the h = 1 half in with a 2-bit shift.
+      const uint32_t Wa = P[0] | (P[2] << 4), Wb = P[1] | (P[3] << 4);
+      const int h = tau >> 3, e = tau & 1, t = (tau & 7) >> 1;
+      unsigned char* base = stage + (pg * D + t * (D / 32) + w_pair) * 8 + 4 * h + 2 * e + s_par;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        base[g * 4 * (D / 32) * 8] = static_cast<unsigned char>((g < 4 ? Wa : Wb) >> (8 * (g & 3)));
+    }
     if (seg == 0) {
-      const float rr = expf(logr[i]);
-      rowA[r] = rr * (delta > 0.f ? delta : 0.f);
-      rowB[r] = rr * lo;
+      rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
+      rowB[r] = rscale[i] * lo;
     }
   }
-  if (warp == 0 && rsub == 0) {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) colC[seg * 16 + e] = expf(logc[e]);
-  }
+  if (tid < D) colC[tid] = cscale;
   __syncthreads();
 
-  // ---- page addresses of this CTA's rows
-  constexpr int PPT = N / kPageTokens;            // pages per tile
-  constexpr int PPC = PPT / CS;                   // pages per CTA
-  const int64_t lt = static_cast<int64_t>(A.tile_start[b]) + u;
-  const int32_t* bt = A.block_table + static_cast<int64_t>(b) * A.bt_stride;
-
-  auto page_ptr = [&](int p_local) -> uint8_t* {
-    const int64_t lp = lt * PPT + crank * PPC + p_local;
-    const int32_t phys = bt[lp];
-    if (phys < 0 || phys >= A.num_pages) return nullptr;
-    return A.cache + (static_cast<int64_t>(phys) * A.num_kv_heads + head) * A.page_bytes;
-  };
-
-  // ---- pack codes
-  if constexpr (BITS == 4) {
-    // dense K or latent: per page 2D words; a thread builds 4 words (16 B)
-    constexpr int CHUNKS = PPC * 2 * D / 4;
-    for (int c = tid; c < CHUNKS; c += S::NT) {
-      const int W0 = c * 4;
-      const int p = W0 / (2 * D), win0 = W0 % (2 * D);
-      uint8_t* pg = page_ptr(p);
-      if (!pg) {
-        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
-        continue;
-      }
-      uint32_t out[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int win = win0 + k;
-        const int tau = win / (D / 8), rem = win % (D / 8);
-        const int t = rem / (D / 32), w = rem % (D / 32);
-        const unsigned char* row = codes + (p * kPageTokens + tau) * D;
-        uint32_t word = 0;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          const int ch = 16 * (2 * w + ((n & 3) >> 1)) + 2 * t + 8 * (n & 1) + (n >> 2);
-          word |= static_cast<uint32_t>(row[ch]) << (4 * n);
-        }
-        out[k] = word;
-      }
-      *reinterpret_cast<uint4*>(pg + 4 * win0) = make_uint4(out[0], out[1], out[2], out[3]);
+  // ---- codes: 16-byte stores of the staged page words
+  if constexpr (!IS_V) {
+    constexpr int CPP = 2 * D / 4;  // 16-byte chunks per page
+    const uint4* img = reinterpret_cast<const uint4*>(stage);
+    for (int c = tid; c < S::PPC * CPP; c += S::NT) {
+      uint8_t* pg = pages[c / CPP];
+      if (pg) reinterpret_cast<uint4*>(pg)[c % CPP] = img[c];
     }
   } else {
-    // dense V: per page D words
-    constexpr int CHUNKS = PPC * D / 4;
+    constexpr int CPP = D / 4;
     const int base = DensePage(D, N).v_codes();
-    for (int c = tid; c < CHUNKS; c += S::NT) {
-      const int W0 = c * 4;
-      const int p = W0 / D, win0 = W0 % D;
-      uint8_t* pg = page_ptr(p);
-      if (!pg) {
-        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
-        continue;
-      }
-      uint32_t out[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int win = win0 + k;
-        const int L = win / (D / 32), w = win % (D / 32);
-        const int g = L >> 2, t = L & 3;
-        uint32_t word = 0;
-#pragma unroll
-        for (int pp = 0; pp < 8; ++pp)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int nc = 4 * w + (pp >> 1), h = pp & 1;
-            const int tau = 2 * t + e + 8 * h;
-            const int ch = 8 * nc + g;
-            word |= static_cast<uint32_t>(codes[(p * kPageTokens + tau) * D + ch]) << (2 * pp + 16 * e);
-          }
-        out[k] = word;
-      }
-      *reinterpret_cast<uint4*>(pg + base + 4 * win0) = make_uint4(out[0], out[1], out[2], out[3]);
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
+    for (int c = tid; c < S::PPC * CPP; c += S::NT) {
+      uint8_t* pg = pages[c / CPP];
+      if (!pg) continue;
+      const uint4 a = st[2 * c], bb = st[2 * c + 1];
+      reinterpret_cast<uint4*>(pg + base)[c % CPP] =
+          make_uint4(a.x | (a.y << 2), a.z | (a.w << 2), bb.x | (bb.y << 2), bb.z | (bb.w << 2));
     }
   }
 
@@ -358,12 +372,12 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     off_a = L.a(); off_b = L.b(); off_c = L.col();
   } else {
     constexpr DensePage P(D, N);
-    off_a = which ? P.v_a() : P.k_a();
-    off_b = which ? P.v_b() : P.k_b();
-    off_c = which ? P.v_col() : P.k_col();
+    off_a = IS_V ? P.v_a() : P.k_a();
+    off_b = IS_V ? P.v_b() : P.k_b();
+    off_c = IS_V ? P.v_col() : P.k_col();
   }
   if (tid < S::ROWS) {
-    uint8_t* pg = page_ptr(tid / kPageTokens);
+    uint8_t* pg = pages[tid / kPageTokens];
     if (pg) {
       reinterpret_cast<float*>(pg + off_a)[tid % kPageTokens] = rowA[tid];
       reinterpret_cast<float*>(pg + off_b)[tid % kPageTokens] = rowB[tid];
@@ -371,9 +385,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   }
   {
     constexpr int C = D * kPageTokens / N;  // column scales per page
-    for (int j = tid; j < PPC * C; j += S::NT) {
-      uint8_t* pg = page_ptr(j / C);
-      if (pg) reinterpret_cast<float*>(pg + off_c)[j % C] = colC[(crank * PPC) * C + j];
+    for (int j = tid; j < S::PPC * C; j += S::NT) {
+      uint8_t* pg = pages[j / C];
+      if (pg) reinterpret_cast<float*>(pg + off_c)[j % C] = colC[(crank * S::PPC) * C + j];
     }
   }
   if constexpr (KIND == 1) {
@@ -381,9 +395,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     constexpr LatentPage L(D, 64, N);
     const int R = A.rope_dim;
     const int vec_per_page = kPageTokens * R * 2 / 16;
-    for (int c = tid; c < PPC * vec_per_page; c += S::NT) {
+    for (int c = tid; c < S::PPC * vec_per_page; c += S::NT) {
       const int p = c / vec_per_page, k = c % vec_per_page;
-      uint8_t* pg = page_ptr(p);
+      uint8_t* pg = pages[p];
       if (!pg) continue;
       const int row = crank * S::ROWS + p * kPageTokens;  // first token of the page in the tile
       const uint8_t* s = reinterpret_cast<const uint8_t*>(
@@ -393,17 +407,20 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   }
 }
 
+// K (4-bit) and V (2-bit) tiles share one launch: blockIdx.z < num_seqs
+// encodes K, the rest V, so that the K half of a large grid runs before the
+// V half and an SM mostly runs one of the two code paths.
 template <int D, int N, typename T>
 __global__ void __launch_bounds__(2 * D) encode_dense_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int u = blockIdx.x >> 1, which = blockIdx.x & 1;
-  const int head = blockIdx.y, b = blockIdx.z;
-  const T* src = static_cast<const T*>(A.x[which]) + static_cast<int64_t>(b) * A.seq_stride +
-                 static_cast<int64_t>(head) * A.head_stride + static_cast<int64_t>(u) * N * D;
-  if (which == 0)
-    encode_tile<D, N, 1, 4, 0, T>(A, src, b, head, u, 0, smem);
+  const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
+  const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);
+  const int64_t off = static_cast<int64_t>(b) * A.seq_stride + static_cast<int64_t>(head) * A.head_stride +
+                      static_cast<int64_t>(u) * N * D;
+  if (is_v)
+    encode_tile<D, N, 1, 2, 0, T>(A, static_cast<const T*>(A.x[1]) + off, b, head, u, smem);
   else
-    encode_tile<D, N, 1, 2, 0, T>(A, src, b, head, u, 1, smem);
+    encode_tile<D, N, 1, 4, 0, T>(A, static_cast<const T*>(A.x[0]) + off, b, head, u, smem);
 }
 
 template <typename T>
@@ -413,17 +430,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
   const int u = blockIdx.x >> 1, b = blockIdx.y;
   const T* src = static_cast<const T*>(A.x[0]) + static_cast<int64_t>(b) * A.seq_stride +
                  static_cast<int64_t>(u) * 128 * 512;
-  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, 0, smem);
+  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, smem);
 }
 
 // ------------------------------------------------------------- launchers
 template <int D, int N, typename T>
-static cudaError_t launch_dense(const EncodeArgs& A, int num_seqs, cudaStream_t st) {
+static cudaError_t launch_dense(const EncodeArgs& A, cudaStream_t st) {
   constexpr int smem = EncShape<D, N, 1>::SMEM;
   auto kern = encode_dense_kernel<D, N, T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(2 * A.chunk_tiles, A.num_kv_heads, num_seqs);
+  dim3 grid(A.chunk_tiles, A.num_kv_heads, 2 * A.num_seqs);
   kern<<<grid, 2 * D, smem, st>>>(A);
   return cudaGetLastError();
 }
@@ -444,11 +461,12 @@ cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st) {
   A.page_bytes = DensePage(p.D, p.N).bytes();
   A.norm_iters = p.norm_iters;
   A.err = p.err;
+  A.num_seqs = p.num_seqs;
   if (A.chunk_tiles == 0 || p.num_seqs == 0) return cudaSuccess;
 #define KV_DISPATCH(DD, NN)                                                              \
   if (p.D == DD && p.N == NN)                                                            \
-    return p.bf16 ? launch_dense<DD, NN, __nv_bfloat16>(A, p.num_seqs, st)               \
-                  : launch_dense<DD, NN, __half>(A, p.num_seqs, st);
+    return p.bf16 ? launch_dense<DD, NN, __nv_bfloat16>(A, st)               \
+                  : launch_dense<DD, NN, __half>(A, st);
   KV_DISPATCH(128, 128)
   KV_DISPATCH(128, 64)
   KV_DISPATCH(256, 128)
@@ -474,6 +492,7 @@ cudaError_t launch_encode_latent(const EncodeLatentParams& p, cudaStream_t st) {
   A.norm_iters = p.norm_iters;
   A.rope_dim = 64;
   A.err = p.err;
+  A.num_seqs = p.num_seqs;
   if (A.chunk_tiles == 0 || p.num_seqs == 0) return cudaSuccess;
   constexpr int smem = EncShape<512, 128, 2>::SMEM;
   auto kern = p.bf16 ? encode_latent_kernel<__nv_bfloat16> : encode_latent_kernel<__half>;
