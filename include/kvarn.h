@@ -43,10 +43,11 @@
  *                      k-chunk kc. Word w of a chunk serves kc = 2w, 2w+1;
  *                      nibble n (bits 4n..4n+3) holds channel
  *                      16(2w + (n%4)/2) + 2t + 8(n%2) + n/4.
- *   V codes, 4D bytes, 2-bit, channel-major. Word j holds channel j
- *                      of the page's 16 tokens: token tau sits at bit
- *                      2(tau/2) + 16(tau%2), even tokens in the low half-word
- *                      and odd tokens in the high one.
+ *   V codes, 4D bytes, 2-bit. Lane chunk L = 4g + t (D/8 bytes)
+ *                      holds channels 8nc + g of every 8-channel block nc at
+ *                      tokens {2t, 2t+1, 2t+8, 2t+9}; word w serves blocks
+ *                      4w..4w+3; token tau = 2t + e + 8h of block nc sits at
+ *                      bit 2(2(nc%4) + h) + 16e of its word.
  * The page is a K part followed by a V part, each contiguous so that the
  * decode kernel can fetch and recycle them separately:
  *   K part, KP = 8D + 128 + 4C bytes, C = D*P/N:

@@ -13,10 +13,11 @@ library's own format. A page holds P = 16 tokens of one KV head:
                         Word w of a chunk serves k-chunks 2w and 2w+1; its
                         nibble n (bits 4n..4n+3) holds channel
                         16*(2w + (n%4)//2) + 2t + 8*(n%2) + (n//4).
-  V codes   4*D bytes   2-bit, channel-major: word j (bytes 4j..4j+3) holds
-                        channel j of the page's 16 tokens; token tau sits at
-                        bit 2*(tau//2) + 16*(tau%2) (even tokens in the low
-                        half-word, odd tokens in the high half-word).
+  V codes   4*D bytes   2-bit; lane chunk L = 4g + t (D/8 bytes) holds
+                        channels 8nc + g for every 8-channel block nc, at
+                        tokens {2t, 2t+1, 2t+8, 2t+9}. Word w of a chunk
+                        serves blocks 4w..4w+3; the token tau = 2t + e + 8h of
+                        block nc sits at bit 2*(2*(nc%4) + h) + 16*e.
   The page is two parts, each contiguous: the K part (K codes, then K a[16],
   K b[16] fp32 row scales, then the K column-scale slice, D*P/N fp32), then
   the V part (V codes, V a[16], V b[16], V column-scale slice).
@@ -65,8 +66,15 @@ def k_code_position(D: int, tau: int, j: int):
 
 def v_code_position(D: int, tau: int, j: int):
     """(byte offset inside the V-code region, bit shift) of token tau, channel j."""
-    bit = 2 * (tau // 2) + 16 * (tau % 2)
-    return 4 * j + bit // 8, bit % 8
+    nc, g = divmod(j, 8)
+    t = (tau % 8) // 2
+    e = tau % 2
+    h = tau // 8
+    L = 4 * g + t
+    w, ncl = divmod(nc, 4)
+    bit = 2 * (2 * ncl + h) + 16 * e
+    byte = L * (D // 8) + 4 * w + bit // 8
+    return byte, bit % 8
 
 
 @functools.lru_cache(maxsize=None)

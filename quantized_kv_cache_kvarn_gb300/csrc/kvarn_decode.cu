@@ -1,33 +1,30 @@
 // KVarN decode attention over the compressed paged cache, sm_103a.
 //
 // Paged, split-K, GQA-grouped decode that streams the packed codes and
-// scales straight from HBM and dequantises them on chip; no fp16 K or V
-// buffer is ever formed in memory (turbo-attn page, "Inline dequant").
-// Scores are taken in the rotated basis: the query is rotated once per CTA
-// and the output un-rotated once in the merge (turbo-attn page, "How it
-// works").
+// scales straight from HBM and dequantises them in registers; no fp16 K or V
+// buffer is ever formed (turbo-attn page, "Inline dequant"). Scores are
+// taken in the rotated basis: the query is rotated once per CTA and the
+// output un-rotated once in the merge (turbo-attn page, "How it works").
 //
-// Kernel 1 (decode_dense_kernel): one CTA per (KV head, split, sequence),
-// one thread per channel (D threads). The split's tiles stream through a
-// two-stage shared-memory ring filled by one-dimensional bulk copies (one
-// per page, completion counted on an mbarrier) with the pages further
-// ahead prefetched into L2. Per tile, on the fifth-generation tensor cores:
-//   Q K:  thread i turns token i's packed K codes into exact fp16 integers
-//         (code - 8) and stores them in tensor memory: A = K~ [128 tokens x
-//         D]. q~ = (kappa q H) * c_K, split into fp16 hi + lo rows, is the
-//         shared-memory B operand [16 x D] (rows 0-7 hi, 8-15 lo of the
-//         G <= 8 heads of the group); S^T = K~ q~^T lands in tensor memory;
-//   s  = a_K * (S_hi + S_lo) + (b_K + 8 a_K) * sum(q~)  (row scales folded);
-//   online softmax in base 2, rescaling only when a running maximum rises;
-//   P V:  thread j turns channel j's V codes into fp16 (code - 2) in tensor
-//         memory: A = V~^T [D x tokens]; the weights p * a_V (hi + lo) are
-//         the B operand, so U^T = V~^T (p a_V)^T; a second product against
-//         an all-ones A block gives beta = sum_i p_i (b_V + 2 a_V) for every
-//         lane without a cross-thread reduction;
-//   acc_j = acc_j * alpha + c_V[j] * (U_j + beta)    (thread j, all heads).
-// The CTA writes one partial (max, sum, unnormalised output) per split and
-// head; the last split slot holds the fp16 tail (tokens past the last full
-// tile, in the original basis).
+// Kernel 1 (decode_dense_kernel): one CTA per (split, KV head, sequence);
+// each of its W warps owns every W-th tile of the split. A warp keeps one
+// shared-memory slot for the K parts and one for the V parts of its tile's
+// pages, filled by one-dimensional bulk copies (completion counted on an
+// mbarrier), and prefetches the pages of its next tiles into L2. The K slot
+// is refilled with the next tile while P V runs, the V slot while the next
+// Q K runs. Per tile and warp:
+//   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
+//        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
+//        half of the m16 tile free, so the split costs no extra mma);
+//   S  = q~ (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
+//        integers, made from the packed nibbles by exponent-bias arithmetic);
+//   s  = a_K * S + (b_K + 8 a_K) * sum(q~)      (row scales folded back in);
+//   online softmax in base 2;
+//   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
+//   acc = acc * alpha + c_V * (u + sum p (b_V + 2 a_V)).
+// The warps of a CTA merge in shared memory and write one partial
+// (max, sum, unnormalised output) per split. The last split slot holds the
+// fp16 tail (tokens past the last full tile, in the original basis).
 // Kernel 2 (merge_kernel): log-sum-exp merge of the partials, inverse
 // Hadamard transform of the rotated part, plus the tail part.
 #include <math.h>
@@ -35,51 +32,38 @@
 #include "kvarn_common.cuh"
 #include "kvarn_launch.h"
 #include "kvarn_merge.cuh"
-#include "kvarn_tc.cuh"
 #include <algorithm>
 
 namespace kvarn {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+// CTAs per SM the 4-warp decode kernel is register-limited to (3 caps it at
+// 168 registers per thread, 2 at 255).
+#ifndef KVARN_DECODE_MIN_CTAS
+#define KVARN_DECODE_MIN_CTAS 3
+#endif
 
-template <int D, int N>
+template <int D, int N, int W>
 struct DecShape {
   static constexpr DensePage PG{D, N};
-  static constexpr int NT = D;                 // one thread per channel
-  static constexpr int NWARP = NT / 32;
-  static constexpr int PPT = N / kPageTokens;  // pages per tile
+  static constexpr int PPT = N / kPageTokens;
   static constexpr int PB = PG.bytes();
-  static constexpr int TILE = PPT * PB;        // staged bytes per tile
-  static constexpr int STAGES = 2;
-  static constexpr int CPP = PG.cols();        // column scales per page
-  static constexpr int DB = D / 128;           // 128-channel blocks of V~^T
-  static constexpr int HPT = 8 / DB;           // heads per thread in the softmax
-  // tensor-memory columns
-  static constexpr int TM_A = 0;               // A operand (K~ or V~^T): D/2 columns
-  static constexpr int TM_S = D / 2;           // S^T, 16 columns
-  static constexpr int TM_U = TM_S + 16;       // U^T, 16 per channel block
-  static constexpr int TM_B = TM_U + 16 * DB;  // beta, 16
-  static constexpr int TM_ONE = TM_B + 16;     // all-ones A block, 8 (K = 16)
-  static constexpr int TM_COLS = TM_ONE + 8 <= 128 ? 128 : 256;
-  // shared memory
-  static constexpr int OFF_BP = align_up(STAGES * TILE, 1024);  // B of P V: [16 x N] f16, MN-major
-  static constexpr int OFF_BQ = OFF_BP + align_up(32 * N, 1024);  // B of Q K [16 x D], K-major; then beta weights
-  static constexpr int BQ_BYTES = align_up(32 * (D > N ? D : N), 1024);
-  static constexpr int OFF_QSUM = OFF_BQ + BQ_BYTES;  // [8] f32
-  static constexpr int OFF_TMAX = OFF_QSUM + 32;      // [NWARP][8] f32
-  static constexpr int OFF_FLAG = OFF_TMAX + NWARP * 32;  // [NWARP] u32
-  static constexpr int OFF_BAR = align_up(OFF_FLAG + NWARP * 4, 16);  // STAGES + 2 mbarriers
-  static constexpr int OFF_TMEM = OFF_BAR + 8 * (STAGES + 2);
-  static constexpr int OFF_PAGES = align_up(OFF_TMEM + 4, 16);  // the split's page ids
-  // at least this much shared memory, so that no more CTAs share an SM than
-  // its 512 tensor-memory columns hold
-  static constexpr int SMEM_FLOOR = 228 * 1024 / (512 / TM_COLS + 1) + 1024;
-  static constexpr uint32_t IDESC_K = idesc_f16(128, 16, false);
-  static constexpr uint32_t IDESC_MN = idesc_f16(128, 16, true);
-  static_assert(TM_ONE + 8 <= TM_COLS, "tensor-memory plan");
-  static_assert(TILE % 16 == 0 && PB % 16 == 0, "bulk copies keep 16-byte alignment");
+  static constexpr int KP = PG.k_part();
+  static constexpr int VP = PG.v_part();
+  static constexpr int KSLOT = PPT * KP;
+  static constexpr int VSLOT = PPT * VP;
+  static constexpr int WARP_SMEM = KSLOT + VSLOT;
+  static constexpr int NB = N / 8;
+  static constexpr int KC = D / 16;
+  static constexpr int NC = D / 8;
+  static constexpr int CPP = PG.cols();
+  static constexpr int LW = D / 32;  // words per lane chunk (K and V)
+  static constexpr int RING = W * WARP_SMEM;
+  static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
+  static constexpr int PREFETCH = 2;  // tiles prefetched into L2 ahead of the K slot
+  static_assert(W * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
 };
 
 struct DecArgs {
@@ -176,66 +160,51 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, int tail, unsign
   }
 }
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Warp maximum of a float through the integer reduction unit: the map
-// below is monotone on IEEE floats and its own inverse.
-__device__ __forceinline__ float warp_max_redux(float v) {
-  int k = __float_as_int(v);
-  k = k >= 0 ? k : (k ^ 0x7FFFFFFF);
-  k = __reduce_max_sync(0xffffffffu, k);
-  return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF));
-}
-
-template <int D, int N, typename T>
-__global__ void __launch_bounds__(D, (D == 128 ? 4 : 2)) decode_dense_kernel(DecArgs A) {
-  using S = DecShape<D, N>;
+template <int D, int N, typename T, int W>
+__global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) decode_dense_kernel(DecArgs A) {
+  using S = DecShape<D, N, W>;
   constexpr DensePage PG{D, N};
-  extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // token role: token tid % 128; kh = channel half (K~) and head group
-  // (softmax) for D = 256, always 0 for D = 128
-  const int tok = tid & 127, kh = DecShape<D, N>::DB == 1 ? 0 : (tid >> 7);
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  // KV head is the fastest grid axis: CTAs resident together read the same
+  // physical pages (all heads of a page are contiguous), keeping DRAM rows open
   const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int G = A.G;
 
   int len = A.seq_lens[b];
   if (len < 0 || len > A.max_seq_len) {
-    if (tid == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
     len = len < 0 ? 0 : A.max_seq_len;
   }
   const int ntiles = len / N;
+
   if (split == A.nsplit) {
-    tail_partials<D, N, T, S::NWARP>(A, b, kvh, len - ntiles * N, smem);
+    tail_partials<D, N, T, W>(A, b, kvh, len - ntiles * N, smem);
     return;
   }
   const int t0 = split * A.tps, t1 = min(t0 + A.tps, ntiles);
   if (t0 >= t1) {
-    for (int h = warp; h < G; h += S::NWARP)
+    for (int h = warp; h < G; h += W)
       write_empty(A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + h) * A.slots + split) * kPStride(D),
                   D, lane);
     return;
   }
-  const int nt = t1 - t0;
 
-  unsigned char* bp = smem + S::OFF_BP;
-  unsigned char* bq = smem + S::OFF_BQ;
-  float* qsum = reinterpret_cast<float*>(smem + S::OFF_QSUM);
-  float* tmax = reinterpret_cast<float*>(smem + S::OFF_TMAX);
-  uint32_t* flag = reinterpret_cast<uint32_t*>(smem + S::OFF_FLAG);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
-  uint64_t* barQ = bars + S::STAGES;
-  uint64_t* barP = barQ + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TMEM);
-  int32_t* pages = reinterpret_cast<int32_t*>(smem + S::OFF_PAGES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::RING);
+  float* qrot = reinterpret_cast<float*>(smem + S::RING + W * 2 * 8);
+  int32_t* pages = reinterpret_cast<int32_t*>(smem + S::SMEM);  // this split's page ids
+  unsigned char* kslot = smem + warp * S::WARP_SMEM;
+  unsigned char* vslot = kslot + S::KSLOT;
+  uint64_t* barK = bars + 2 * warp;
+  uint64_t* barV = barK + 1;
+
+  const int first = t0 + warp;
+  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
   const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
 
   // the split's block-table entries, checked once, into shared memory
-  for (int e = tid; e < nt * S::PPT; e += S::NT) {
+  for (int e = threadIdx.x; e < (t1 - t0) * S::PPT; e += W * 32) {
     int phys = bt[t0 * S::PPT + e];
     if (phys < 0 || phys >= A.num_pages) {
       set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
@@ -243,353 +212,265 @@ __global__ void __launch_bounds__(D, (D == 128 ? 4 : 2)) decode_dense_kernel(Dec
     }
     pages[e] = phys;
   }
-  if (tid == 0) {
-    for (int s = 0; s < S::STAGES + 2; ++s) mbar_init(bars + s, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc<S::TM_COLS>(tslot);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-  const uint32_t tq = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // this warp's lane quarter
 
-  auto page_src = [&](int i, int p) -> const unsigned char* {
-    return A.cache + (static_cast<int64_t>(pages[i * S::PPT + p]) * A.Hkv + kvh) * S::PB;
+  // physical page `lane` of this warp's i-th tile (lanes < PPT)
+  auto page_of = [&](int i) -> const unsigned char* {
+    const int phys = pages[(first + i * W - t0) * S::PPT + lane];
+    return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB;
   };
-  auto issue = [&](int i) {  // thread 0: tile i of the split into stage i % STAGES
-    uint64_t* bar = bars + i % S::STAGES;
-    unsigned char* dst = smem + (i % S::STAGES) * S::TILE;
+  auto issue_k = [&](int i) {
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, S::TILE);
-    for (int p = 0; p < S::PPT; ++p) bulk_g2s(dst + p * S::PB, page_src(i, p), S::PB, bar);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_of(i), S::KP, barK);
+  };
+  auto issue_v = [&](int i) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
   };
   auto prefetch = [&](int i) {
-    for (int p = 0; p < S::PPT; ++p) prefetch_l2(page_src(i, p), S::PB);
+    if (lane < S::PPT) prefetch_l2(page_of(i), S::PB);
   };
-  int issued = min(S::STAGES, nt);  // tiles whose copies have been started (uniform)
-  if (tid == 0) {
-    for (int i = 0; i < issued; ++i) issue(i);
-    if (S::STAGES < nt) prefetch(S::STAGES);
-  }
 
-  // ---- rotated, scaled query rows (fp32, staged in the B_q area), then
-  //      each thread keeps the 8 channels of its q~ role in registers
-  {
-    float* qrot = reinterpret_cast<float*>(bq);
-    constexpr int E = D / 32;
-    for (int h = warp; h < 8; h += S::NWARP) {
-      float v[E];
-      if (h < G) {
-        load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + kvh * G + h) * D + lane * E, v);
-        warp_fwht<E>(v);
-        const float sc = A.kappa / sqrtf(static_cast<float>(D));
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] *= sc;
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
-    }
+  if (lane == 0) {
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
   }
-  // the all-ones A block (fp16 1.0 pairs), once
-  if (warp < 4) {
-    uint32_t ones[8];
+  fence_mbar_init();
+  __syncwarp();
+  if (n_my > 0) {
+    issue_k(0);
+    issue_v(0);
+  }
+  for (int j = 1; j <= S::PREFETCH && j < n_my; ++j) prefetch(j);
+
+  // ---- rotated, scaled query rows of the group (rows >= G are zero)
+  for (int h = warp; h < 8; h += W) {
+    constexpr int E = D / 32;
+    float v[E];
+    if (h < G) {
+      load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + kvh * G + h) * D + lane * E, v);
+      warp_fwht<E>(v);
+      const float sc = A.kappa / sqrtf(static_cast<float>(D));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ones[j] = 0x3C003C00u;
-    tmem_st8(tq + S::TM_ONE, ones);
-    tmem_wait_st();
+      for (int e = 0; e < E; ++e) v[e] *= sc;
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
   }
   __syncthreads();
-  const int qh = tid / (D / 8), qc = tid % (D / 8);  // q~ role: head row, 8-channel chunk
-  float qf[8];
-  {
-    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<float*>(bq) + qh * D + 8 * qc);
-    const float4 u0 = src[0], u1 = src[1];
-    qf[0] = u0.x; qf[1] = u0.y; qf[2] = u0.z; qf[3] = u0.w;
-    qf[4] = u1.x; qf[5] = u1.y; qf[6] = u1.z; qf[7] = u1.w;
-  }
-  __syncthreads();  // B_q area free
 
-  float m[8], alpha[8], lpart[S::HPT], acc[8];
+  float m = -INFINITY, lsum = 0.f;
+  float acc[S::NC][2];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) m[h] = -INFINITY, acc[h] = 0.f, alpha[h] = 1.f;
-#pragma unroll
-  for (int j = 0; j < S::HPT; ++j) lpart[j] = 0.f;
+  for (int nc = 0; nc < S::NC; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
 
   int i = 0;
-  int to = 0;
-  for (; i < nt; ++i) {
-    const int st = i % S::STAGES;
-    if (!mbar_wait_bounded(bars + st, (i / S::STAGES) & 1)) to = 1;
-    to = __any_sync(0xffffffffu, to);  // warp-uniform: warp-collective TMEM moves follow
-    const unsigned char* tile = smem + st * S::TILE;
+  bool timed_out = false;
+  for (; i < n_my; ++i) {
+    const uint32_t par = i & 1;
+    if (!mbar_wait_bounded(barK, par)) {
+      timed_out = true;
+      break;
+    }
 
-    // -- (a) K~ rows into tensor memory; q~ into the B operand
-    if (tok < N && !to) {
-      const unsigned char* kp = tile + (tok / kPageTokens) * S::PB + (tok % kPageTokens) * (D / 2) + 16 * kh;
-      uint4 kw[4];
+    // -- q~ = q' * c_K as fp16 hi/lo A fragments
+    uint32_t Aq[S::KC][4];
+    float qsum = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) kw[t] = *reinterpret_cast<const uint4*>(kp + t * (D / 8));
+    for (int kc = 0; kc < S::KC; ++kc) {
+      const int ch0 = 16 * kc + 2 * t;
+      const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
+      const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
+      const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * 4;
+      const float2 c01 = *reinterpret_cast<const float2*>(cp);
+      const float2 c89 = *reinterpret_cast<const float2*>(cp + 32);
+      const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
+      qsum += (x0 + x1) + (x8 + x9);
+      split_hi_lo(x0, x1, Aq[kc][0], Aq[kc][1]);
+      split_hi_lo(x8, x9, Aq[kc][2], Aq[kc][3]);
+    }
+    qsum = warp_sum_xor(qsum, 1, 4);
+
+    // -- S = q~ . (K codes - 8); four 8-token blocks at a time so that four
+    //    independent accumulator chains hide the mma latency
+    float s[S::NB][2];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
+    for (int nb0 = 0; nb0 < S::NB; nb0 += 4) {
+      float d[4][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
+      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < 2; ++ww) {
-            const int w4 = 2 * half + ww;
-            const uint32_t word = w4 == 0 ? kw[t].x : w4 == 1 ? kw[t].y : w4 == 2 ? kw[t].z : kw[t].w;
+      for (int q4 = 0; q4 < S::LW / 4; ++q4) {
+        uint4 kw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int nb = nb0 + j;
+          kw[j] = *reinterpret_cast<const uint4*>(kslot + (nb >> 1) * S::KP + ((nb & 1) * 8 + g) * (D / 2) +
+                                                  t * (D / 8) + 16 * q4);
+        }
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int w = 4 * q4 + w4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t word = w4 == 0 ? kw[j].x : w4 == 1 ? kw[j].y : w4 == 2 ? kw[j].z : kw[j].w;
             uint32_t bf[4];
             dequant_k_word(word, bf);
-            // channel pairs 16 ww + t (+4, +8, +12) of this 64-channel half
-            r[16 * ww + t] = bf[0];
-            r[16 * ww + t + 4] = bf[1];
-            r[16 * ww + t + 8] = bf[2];
-            r[16 * ww + t + 12] = bf[3];
+            mma_f16(d[j], Aq[2 * w][0], Aq[2 * w][1], Aq[2 * w][2], Aq[2 * w][3], bf[0], bf[1]);
+            mma_f16(d[j], Aq[2 * w + 1][0], Aq[2 * w + 1][1], Aq[2 * w + 1][2], Aq[2 * w + 1][3], bf[2], bf[3]);
           }
-        tmem_st32(tq + S::TM_A + 64 * kh + 32 * half, r);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s[nb0 + j][0] = d[j][0] + d[j][2];
+        s[nb0 + j][1] = d[j][1] + d[j][3];
       }
     }
-    if (!to) {
-      const float* cp = reinterpret_cast<const float*>(tile + ((8 * qc) / S::CPP) * S::PB + PG.k_col() +
-                                                       ((8 * qc) % S::CPP) * 4);
-      const float4 c0 = reinterpret_cast<const float4*>(cp)[0], c1 = reinterpret_cast<const float4*>(cp)[1];
-      const float x[8] = {qf[0] * c0.x, qf[1] * c0.y, qf[2] * c0.z, qf[3] * c0.w,
-                          qf[4] * c1.x, qf[5] * c1.y, qf[6] * c1.z, qf[7] * c1.w};
-      uint32_t hi[4], lo[4];
+
+    // -- row-scale fold and online softmax (base 2)
+    float mt = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split_hi_lo(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
-      // K-major [16 x D]: row n at (n % 8) 16 + (n / 8) 16D, k-chunk at 128 (k / 8)
-      *reinterpret_cast<uint4*>(bq + qh * 16 + qc * 128) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(bq + 16 * D + qh * 16 + qc * 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      float qs = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
-      qs = warp_sum_xor(qs, 1, D / 8);
-      if (qc == 0) qsum[qh] = qs;
+    for (int nb = 0; nb < S::NB; ++nb) {
+      const unsigned char* pg = kslot + (nb >> 1) * S::KP;
+      const int idx = (nb & 1) * 8 + 2 * t;
+      const float2 ka = *reinterpret_cast<const float2*>(pg + PG.k_a() + idx * 4);
+      const float2 kb = *reinterpret_cast<const float2*>(pg + PG.k_b() + idx * 4);
+      s[nb][0] = fmaf(ka.x, s[nb][0], fmaf(8.f, ka.x, kb.x) * qsum);
+      s[nb][1] = fmaf(ka.y, s[nb][1], fmaf(8.f, ka.y, kb.y) * qsum);
+      mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
     }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(to)) {
-      to = 1;
+    mt = warp_max_xor(mt, 1, 4);
+    const float m_new = fmaxf(m, mt);
+    const float alpha = exp2f(m - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      s[nb][0] = exp2f(s[nb][0] - m_new);
+      s[nb][1] = exp2f(s[nb][1] - m_new);
+      psum += s[nb][0] + s[nb][1];
+    }
+    lsum = fmaf(lsum, alpha, psum);
+    m = m_new;
+
+    // the K slot is free: start the next tile's K part, prefetch further
+    if (i + 1 < n_my) issue_k(i + 1);
+    if (i + 1 + S::PREFETCH < n_my) prefetch(i + 1 + S::PREFETCH);
+
+    if (!mbar_wait_bounded(barV, par)) {
+      timed_out = true;
       break;
     }
 
-    // -- (b) S^T = K~ q~^T
-    if (tid == 0) {
-      tc_fence_after();
+    // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
+    uint32_t Ap[S::PPT][4];
+    float beta = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        umma_ts(tbase + S::TM_S, tbase + S::TM_A + 8 * kk,
-                smem_desc(tc_smem(bq) + 256 * kk, 128, 16 * D), S::IDESC_K, kk > 0);
-      umma_commit(barQ);
+    for (int pp = 0; pp < S::PPT; ++pp) {
+      const unsigned char* pg = vslot + pp * S::VP;
+      const float2 va0 = *reinterpret_cast<const float2*>(pg + PG.v_a() - S::KP + (2 * t) * 4);
+      const float2 va1 = *reinterpret_cast<const float2*>(pg + PG.v_a() - S::KP + (8 + 2 * t) * 4);
+      const float2 vb0 = *reinterpret_cast<const float2*>(pg + PG.v_b() - S::KP + (2 * t) * 4);
+      const float2 vb1 = *reinterpret_cast<const float2*>(pg + PG.v_b() - S::KP + (8 + 2 * t) * 4);
+      const float p00 = s[2 * pp][0], p01 = s[2 * pp][1], p10 = s[2 * pp + 1][0], p11 = s[2 * pp + 1][1];
+      beta = fmaf(p00, fmaf(2.f, va0.x, vb0.x), beta);
+      beta = fmaf(p01, fmaf(2.f, va0.y, vb0.y), beta);
+      beta = fmaf(p10, fmaf(2.f, va1.x, vb1.x), beta);
+      beta = fmaf(p11, fmaf(2.f, va1.y, vb1.y), beta);
+      split_hi_lo(p00 * va0.x, p01 * va0.y, Ap[pp][0], Ap[pp][1]);
+      split_hi_lo(p10 * va1.x, p11 * va1.y, Ap[pp][2], Ap[pp][3]);
     }
-    if (!mbar_wait_bounded(barQ, i & 1)) to = 1;
-    to = __any_sync(0xffffffffu, to);
-    tc_fence_after();
+    beta = warp_sum_xor(beta, 1, 4);
 
-    // -- (c) scores, running maximum, weights
-    float sc[S::HPT];
-    float over = -INFINITY;
-    const bool has_tok = tok < N;
-    const unsigned char* kpg = tile + (tok / kPageTokens) * S::PB;
-    if (has_tok) {  // warp-uniform
-      uint32_t sr[16];
-      tmem_ld16(tq + S::TM_S, sr);
-      const float ka = reinterpret_cast<const float*>(kpg + PG.k_a())[tok % kPageTokens];
-      const float kb = reinterpret_cast<const float*>(kpg + PG.k_b())[tok % kPageTokens];
-      const float kb8 = fmaf(8.f, ka, kb);
-      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < S::HPT; ++j) {
-        const int h = kh * S::HPT + j;
-        const float shi = kh ? __uint_as_float(sr[S::HPT + j]) : __uint_as_float(sr[j]);
-        const float slo = kh ? __uint_as_float(sr[S::HPT + j + 8]) : __uint_as_float(sr[j + 8]);
-        const float mh = kh ? m[S::HPT + j] : m[j];
-        sc[j] = fmaf(ka, shi + slo, kb8 * qsum[h]);
-        over = fmaxf(over, sc[j] - mh);
-      }
+    for (int nc = 0; nc < S::NC; ++nc) {
+      acc[nc][0] *= alpha;
+      acc[nc][1] *= alpha;
     }
-    const uint32_t any = __any_sync(0xffffffffu, over > 0.f);
-    if (lane == 0) flag[warp] = any;
-    __syncthreads();
-    uint32_t rescale = 0;
+    // channel blocks in groups of eight (two words of the lane chunk)
 #pragma unroll
-    for (int w = 0; w < S::NWARP; ++w) rescale |= flag[w];
-    if (rescale) {  // CTA-uniform: a running maximum rises
+    for (int hq = 0; hq < S::LW / 2; ++hq) {
+      float u[8][4];
 #pragma unroll
-      for (int j = 0; j < S::HPT; ++j) {
-        const float v = warp_max_redux(has_tok ? sc[j] : -INFINITY);
-        if (lane == 0) tmax[warp * 8 + j] = v;
-      }
-      __syncthreads();
+      for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const int grp = h / S::HPT, j = h % S::HPT;  // warps 4 grp .. 4 grp + 3 hold head h
-        float mt = m[h];
+      for (int pp = 0; pp < S::PPT; ++pp) {
+        const uint2 vw = *reinterpret_cast<const uint2*>(vslot + pp * S::VP + (4 * g + t) * (D / 8) + 8 * hq);
+        uint32_t bf[8];
+        dequant_v_word(vw.x, bf);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mt = fmaxf(mt, tmax[(4 * grp + w) * 8 + j]);
-        alpha[h] = fast_exp2(m[h] - mt);
-        m[h] = mt;
+        for (int k = 0; k < 4; ++k)
+          mma_f16(u[k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
+        dequant_v_word(vw.y, bf);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16(u[4 + k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
       }
 #pragma unroll
-      for (int j = 0; j < S::HPT; ++j) lpart[j] *= kh ? alpha[S::HPT + j] : alpha[j];
-    }
-    if (has_tok) {
-      const unsigned char* vpg = kpg + PG.k_part();
-      const float va = reinterpret_cast<const float*>(vpg + PG.v_a() - PG.k_part())[tok % kPageTokens];
-      const float vb = reinterpret_cast<const float*>(vpg + PG.v_b() - PG.k_part())[tok % kPageTokens];
-      const float vb2 = fmaf(2.f, va, vb);
-      float pa[S::HPT], pb[S::HPT];
-#pragma unroll
-      for (int j = 0; j < S::HPT; ++j) {
-        const float p = fast_exp2(sc[j] - (kh ? m[S::HPT + j] : m[j]));
-        lpart[j] += p;
-        pa[j] = p * va;
-        pb[j] = p * vb2;
-      }
-      // MN-major [16 x N]: token k at (k % 8) 16 + (k / 8) 128, head row n at
-      // (n % 8) 2 + (n / 8) 16N
-      const int o = (tok % 8) * 16 + (tok / 8) * 128 + kh * (2 * S::HPT);
-      if constexpr (S::HPT == 8) {
-        uint32_t h0[4], l0[4], h1[4], l1[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          split_hi_lo(pa[2 * e], pa[2 * e + 1], h0[e], l0[e]);
-          split_hi_lo(pb[2 * e], pb[2 * e + 1], h1[e], l1[e]);
-        }
-        *reinterpret_cast<uint4*>(bp + o) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-        *reinterpret_cast<uint4*>(bp + 16 * N + o) = make_uint4(l0[0], l0[1], l0[2], l0[3]);
-        *reinterpret_cast<uint4*>(bq + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-        *reinterpret_cast<uint4*>(bq + 16 * N + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-      } else {
-        uint32_t h0[2], l0[2], h1[2], l1[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          split_hi_lo(pa[2 * e], pa[2 * e + 1], h0[e], l0[e]);
-          split_hi_lo(pb[2 * e], pb[2 * e + 1], h1[e], l1[e]);
-        }
-        *reinterpret_cast<uint2*>(bp + o) = make_uint2(h0[0], h0[1]);
-        *reinterpret_cast<uint2*>(bp + 16 * N + o) = make_uint2(l0[0], l0[1]);
-        *reinterpret_cast<uint2*>(bq + o) = make_uint2(h1[0], h1[1]);
-        *reinterpret_cast<uint2*>(bq + 16 * N + o) = make_uint2(l1[0], l1[1]);
+      for (int k = 0; k < 8; ++k) {
+        const int nc = 8 * hq + k;
+        const int ch = 8 * nc + 2 * t;
+        const float2 cv = *reinterpret_cast<const float2*>(vslot + (ch / S::CPP) * S::VP + PG.v_col() -
+                                                           S::KP + (ch % S::CPP) * 4);
+        acc[nc][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[nc][0]);
+        acc[nc][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[nc][1]);
       }
     }
-
-    // -- (d) V~^T rows (channel tid) into tensor memory
-    float cv;
-    {
-      const int d = tid;
-      cv = reinterpret_cast<const float*>(tile + (d / S::CPP) * S::PB + PG.v_col())[d % S::CPP];
-      constexpr int GROUPS = (S::PPT + 3) / 4;  // 4 pages = 32 columns per store
-#pragma unroll
-      for (int gi = 0; gi < GROUPS; ++gi) {
-        uint32_t r[32];
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const uint32_t word =
-              reinterpret_cast<const uint32_t*>(tile + (4 * gi + pp) * S::PB + PG.v_codes())[d];
-          uint32_t vf[8];
-          dequant_v_word(word, vf);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) r[8 * pp + q] = vf[q];
-        }
-        tmem_st32(tq + S::TM_A + (d >> 7) * (N / 2) + 32 * gi, r);
-      }
-    }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(to)) {
-      to = 1;
-      break;
-    }
-    // the stage is consumed: refill it with tile i + STAGES
-    if (i + S::STAGES < nt) {
-      if (tid == 0) {
-        issue(i + S::STAGES);
-        if (i + S::STAGES + 1 < nt) prefetch(i + S::STAGES + 1);
-      }
-      issued = i + S::STAGES + 1;
-    }
-
-    // -- (e) U^T = V~^T (p a_V)^T per channel block, beta = 1 (p (b_V + 2 a_V))^T
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int db = 0; db < S::DB; ++db)
-#pragma unroll
-        for (int kk = 0; kk < N / 16; ++kk)
-          umma_ts(tbase + S::TM_U + 16 * db, tbase + S::TM_A + db * (N / 2) + 8 * kk,
-                  smem_desc(tc_smem(bp) + 256 * kk, 128, 16 * N), S::IDESC_MN, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < N / 16; ++kk)
-        umma_ts(tbase + S::TM_B, tbase + S::TM_ONE, smem_desc(tc_smem(bq) + 256 * kk, 128, 16 * N),
-                S::IDESC_MN, kk > 0);
-      umma_commit(barP);
-    }
-    if (!mbar_wait_bounded(barP, i & 1)) to = 1;
-    to = __any_sync(0xffffffffu, to);
-    tc_fence_after();
-
-    // -- (f) accumulate (thread = channel, all heads)
-    {
-      uint32_t u[16], be[16];
-      tmem_ld16(tq + S::TM_U + 16 * kh, u);
-      tmem_ld16(tq + S::TM_B, be);
-      tmem_wait_ld();
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float t = (__uint_as_float(u[h]) + __uint_as_float(u[h + 8])) +
-                        (__uint_as_float(be[h]) + __uint_as_float(be[h + 8]));
-        acc[h] = fmaf(acc[h], alpha[h], cv * t);
-      }
-    }
-    if (rescale) {
-#pragma unroll
-      for (int h = 0; h < 8; ++h) alpha[h] = 1.f;
-    }
-    tc_fence_before();
+    if (i + 1 < n_my) issue_v(i + 1);
   }
-
-  if (to) {
-    if (tid == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
-    // let the copies and products this CTA started finish before its
-    // shared and tensor memory go away
-    for (int j = i; j < issued; ++j) mbar_wait_bounded(bars + j % S::STAGES, (j / S::STAGES) & 1, 100000000LL);
-    mbar_wait_bounded(barQ, i & 1, 100000000LL);
-    mbar_wait_bounded(barP, i & 1, 100000000LL);
+  if (timed_out) {
+    if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+    // wait (bounded) for the copies this warp still has in flight
+    mbar_wait_bounded(barK, i & 1, 100000000LL);
+    mbar_wait_bounded(barV, i & 1, 100000000LL);
   }
+  lsum = warp_sum_xor(lsum, 1, 4);
 
-  // ---- per-head sums of the weights: warp sums, then across the warps of
-  //      the head's group
+  // ---- merge the W warps of the CTA (scratch aliases the slots)
   __syncthreads();
-  float* lred = tmax;  // [NWARP][8]
+  float* mrg = reinterpret_cast<float*>(smem);
+  float* mw = mrg + warp * 8 * (D + 2);
+  if (t == 0) {
+    mw[g * (D + 2)] = n_my > 0 ? m : -INFINITY;
+    mw[g * (D + 2) + 1] = n_my > 0 ? lsum : 0.f;
+  }
 #pragma unroll
-  for (int j = 0; j < S::HPT; ++j) {
-    const float v = warp_sum_xor(lpart[j], 1, 32);
-    if (lane == 0) lred[warp * 8 + j] = v;
+  for (int nc = 0; nc < S::NC; ++nc) {
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[nc][0];
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[nc][1];
   }
   __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+    const int gg = idx / D, j = idx % D;
+    float M = -INFINITY;
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    if (h >= G) break;
-    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + h) * A.slots + split) * kPStride(D);
-    part[4 + tid] = to ? 0.f : acc[h];
-    if (tid == 0) {
-      const int grp = h / S::HPT, j = h % S::HPT;
-      float l = 0.f;
-      for (int w = 0; w < 4; ++w) l += lred[(4 * grp + w) * 8 + j];
-      part[0] = to ? -INFINITY : m[h];
-      part[1] = to ? 0.f : l;
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
+    float a = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* r = mrg + (w * 8 + gg) * (D + 2);
+        const float sc = exp2f(r[0] - M);
+        a = fmaf(r[2 + j], sc, a);
+        L = fmaf(r[1], sc, L);
+      }
+    }
+    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + gg) * A.slots + split) * kPStride(D);
+    part[4 + j] = a;
+    if (j == 0) {
+      part[0] = M;
+      part[1] = L;
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc<S::TM_COLS>(tbase);
 }
 
 // ------------------------------------------------------------- planning
@@ -611,8 +492,7 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
     p.nsplit = 0;
   } else {
     // Split count whose CTA count fills whole waves best (resident CTAs per
-    // SM times the SM count), keeping at least 4 tiles per concurrently
-    // processed tile slot of a CTA (`warps`); ties go to
+    // SM times the SM count), keeping at least 4 tiles per warp; ties go to
     // fewer splits (fewer partials to merge).
     const double slots = static_cast<double>(device_sm_count()) * ctas_per_sm;
     const int max_split = std::max(1, tiles / (4 * warps));
@@ -633,28 +513,49 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
   return p;
 }
 
-// Tiles a CTA of the compressed decode works on at once (the whole CTA
-// cooperates on one tile).
-int dense_decode_warps(int32_t) { return 1; }
+int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 
-// CTAs of the compressed decode kernel resident on one SM: bounded by the
-// 512 tensor-memory columns (128 per CTA for head_dim 128, 256 for 256).
-int dense_decode_ctas_per_sm(int32_t D, int32_t) { return D == 256 ? 2 : 4; }
+template <int D, int N, typename T, int W>
+static int resident_ctas() {
+  using S = DecShape<D, N, W>;
+  auto kern = decode_dense_kernel<D, N, T, W>;
+  const int smem = S::SMEM + 48 * S::PPT * 4;  // with a typical split's page ids
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, smem) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
+// CTAs of the compressed decode kernel that fit on one SM at once (same for
+// fp16 and bf16 queries, which share the register and smem footprint).
+int dense_decode_ctas_per_sm(int32_t D, int32_t N) {
+  static int cache[2][2] = {{0, 0}, {0, 0}};
+  const int di = D == 256, ni = N == 64;
+  if (!cache[di][ni]) {
+    if (D == 128 && N == 128) cache[di][ni] = resident_ctas<128, 128, __half, 4>();
+    else if (D == 128) cache[di][ni] = resident_ctas<128, 64, __half, 4>();
+    else if (N == 128) cache[di][ni] = resident_ctas<256, 128, __half, 2>();
+    else cache[di][ni] = resident_ctas<256, 64, __half, 2>();
+  }
+  return cache[di][ni];
+}
 
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
                               const SplitPlan& plan) {
   return static_cast<int64_t>(num_seqs) * num_q_heads * plan.slots * kPStride(D) * 4;
 }
 
-template <int D, int N, typename T>
+template <int D, int N, typename T, int W>
 static cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
-  using S = DecShape<D, N>;
-  auto kern = decode_dense_kernel<D, N, T>;
-  const int smem = std::max(S::OFF_PAGES + A.tps * S::PPT * 4, S::SMEM_FLOOR);
+  using S = DecShape<D, N, W>;
+  auto kern = decode_dense_kernel<D, N, T, W>;
+  const int smem = S::SMEM + A.tps * S::PPT * 4;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(A.Hkv, A.nsplit + 1, num_seqs);
-  kern<<<grid, S::NT, smem, st>>>(A);
+  kern<<<grid, W * 32, smem, st>>>(A);
   return cudaGetLastError();
 }
 
@@ -680,14 +581,14 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   A.slots = plan.slots;
   A.err = p.err;
   cudaError_t e = cudaErrorInvalidValue;
-#define KV_DISPATCH(DD, NN)                                                            \
-  if (p.D == DD && p.N == NN)                                                          \
-    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16>(A, p.num_seqs, st)                   \
-               : run_dense<DD, NN, __half>(A, p.num_seqs, st);
-  KV_DISPATCH(128, 128)
-  KV_DISPATCH(128, 64)
-  KV_DISPATCH(256, 128)
-  KV_DISPATCH(256, 64)
+#define KV_DISPATCH(DD, NN, WW)                                                       \
+  if (p.D == DD && p.N == NN)                                                         \
+    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW>(A, p.num_seqs, st)              \
+               : run_dense<DD, NN, __half, WW>(A, p.num_seqs, st);
+  KV_DISPATCH(128, 128, 4)
+  KV_DISPATCH(128, 64, 4)
+  KV_DISPATCH(256, 128, 2)
+  KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * p.num_q_heads;

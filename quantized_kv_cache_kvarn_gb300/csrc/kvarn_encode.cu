@@ -37,7 +37,7 @@ struct EncShape {
   static_assert(ROWS == RPT * NW * RPW, "tile rows must cover the CTA");
   static_assert(NT >= D, "one thread per channel finishes the column statistics");
   static constexpr int RED_BYTES = NW * D * 4;
-  static constexpr int CODE_BYTES = ROWS * D;  // packed K words (half of it) or V code bytes
+  static constexpr int CODE_BYTES = ROWS * D / 2;  // packed K words or V staging bytes
   static constexpr int SCRATCH = RED_BYTES > CODE_BYTES ? RED_BYTES : CODE_BYTES;
   // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][D] | pages[PPC]
   static constexpr int OFF_COLBUF = SCRATCH;
@@ -324,8 +324,17 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
         img[(2 * s_par + j) * (D / 32)] = (s_par ? hi_t : lo_t) | other;
       }
     } else {
-      // V: one code per byte, token-major, packed into channel words below
-      *reinterpret_cast<uint4*>(stage + r * D + seg * 16) = make_uint4(P[0], P[1], P[2], P[3]);
+      // 2-bit V page order: word (4g + t) * (D/32) + w holds, for tokens
+      // 2t + e + 8h and channels 32w + g + 8j, the code at bit 4j + 2h + 16e.
+      // The thread's byte for group g (codes of channels g and g + 8 of its
+      // segment, nibble-spaced) is staged at byte 4h + 2e + s of that word's
+      // 8-byte slot; the copy-out folds the h = 1 half in with a 2-bit shift.
+      const uint32_t Wa = P[0] | (P[2] << 4), Wb = P[1] | (P[3] << 4);
+      const int h = tau >> 3, e = tau & 1, t = (tau & 7) >> 1;
+      unsigned char* base = stage + (pg * D + t * (D / 32) + w_pair) * 8 + 4 * h + 2 * e + s_par;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        base[g * 4 * (D / 32) * 8] = static_cast<unsigned char>((g < 4 ? Wa : Wb) >> (8 * (g & 3)));
     }
     if (seg == 0) {
       rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
@@ -344,32 +353,15 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       if (pg) reinterpret_cast<uint4*>(pg)[c % CPP] = img[c];
     }
   } else {
-    // 2-bit channel-major page order: word j holds channel j, token tau at bit
-    // 2(tau/2) + 16(tau%2). A thread packs four channels of one page from the
-    // sixteen 32-bit rows (one code byte per channel) of the page's tokens:
-    // byte lane c of E0 collects tokens 0, 2, 4, 6 of channel c at bits
-    // 0, 2, 4, 6 (codes are below 4, so byte lanes never carry), E1 tokens
-    // 8..14, O0 and O1 the odd tokens; a byte permute assembles each word.
     constexpr int CPP = D / 4;
     const int base = DensePage(D, N).v_codes();
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
     for (int c = tid; c < S::PPC * CPP; c += S::NT) {
       uint8_t* pg = pages[c / CPP];
       if (!pg) continue;
-      const unsigned char* col = stage + (c / CPP) * kPageTokens * D + 4 * (c % CPP);
-      uint32_t R[16];
-#pragma unroll
-      for (int tau = 0; tau < 16; ++tau) R[tau] = *reinterpret_cast<const uint32_t*>(col + tau * D);
-      const uint32_t E0 = R[0] + (R[2] << 2) + (R[4] << 4) + (R[6] << 6);
-      const uint32_t E1 = R[8] + (R[10] << 2) + (R[12] << 4) + (R[14] << 6);
-      const uint32_t O0 = R[1] + (R[3] << 2) + (R[5] << 4) + (R[7] << 6);
-      const uint32_t O1 = R[9] + (R[11] << 2) + (R[13] << 4) + (R[15] << 6);
-      uint32_t w[4];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t sel = ch | ((4 + ch) << 4);
-        w[ch] = __byte_perm(__byte_perm(E0, E1, sel), __byte_perm(O0, O1, sel), 0x5410);
-      }
-      reinterpret_cast<uint4*>(pg + base)[c % CPP] = make_uint4(w[0], w[1], w[2], w[3]);
+      const uint4 a = st[2 * c], bb = st[2 * c + 1];
+      reinterpret_cast<uint4*>(pg + base)[c % CPP] =
+          make_uint4(a.x | (a.y << 2), a.z | (a.w << 2), bb.x | (bb.y << 2), bb.z | (bb.w << 2));
     }
   }
 

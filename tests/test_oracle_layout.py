@@ -25,7 +25,7 @@ def test_page_bytes_hand_derived():
     D = 128
     tau, j = np.meshgrid(np.arange(16), np.arange(D), indexing="ij")
     kc = (j + j // 16 + 3 * tau) % 16
-    vc = (j + tau + tau // 4) % 4
+    vc = (3 * j + tau + j // 8) % 4
     kb = layout.pack_codes(kc, "k")
     vb = layout.pack_codes(vc, "v")
     assert kb.size == 1024 and vb.size == 512

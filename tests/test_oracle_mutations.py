@@ -130,8 +130,11 @@ def _k_nibble_order(orig):
 
 def _v_pair_order(orig):
     def pos(D, tau, j):
-        bit = 2 * (tau // 2) + 16 * (1 - tau % 2)   # odd tokens in the low half-word
-        return 4 * j + bit // 8, bit % 8
+        nc, g = divmod(j, 8)
+        t, e, h = (tau % 8) // 2, tau % 2, tau // 8
+        w, ncl = divmod(nc, 4)
+        bit = 2 * (2 * ncl + e) + 16 * h
+        return (4 * g + t) * (D // 8) + 4 * w + bit // 8, bit % 8
     return pos
 
 
