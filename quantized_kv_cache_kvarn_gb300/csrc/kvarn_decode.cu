@@ -351,12 +351,12 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     }
     mt = warp_max_xor(mt, 1, 4);
     const float m_new = fmaxf(m, mt);
-    const float alpha = exp2f(m - m_new);
+    const float alpha = fast_exp2(m - m_new);
     float psum = 0.f;
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
-      s[nb][0] = exp2f(s[nb][0] - m_new);
-      s[nb][1] = exp2f(s[nb][1] - m_new);
+      s[nb][0] = fast_exp2(s[nb][0] - m_new);
+      s[nb][1] = fast_exp2(s[nb][1] - m_new);
       psum += s[nb][0] + s[nb][1];
     }
     lsum = fmaf(lsum, alpha, psum);
