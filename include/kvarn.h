@@ -64,7 +64,10 @@
  * A dequantised rotated value is y[i, j] = c[j] * (a[i] * code[i, j] + b[i]).
  *
  * MLA latent page (latent width Dl = 512, rope width R, 4-bit, K = V):
- *   [0, 8Dl)           latent codes, placed as the dense K codes
+ *   [0, 8Dl)           latent codes: the dense K words of a token row
+ *                      (above, with D = Dl), whose 16-byte units (unit
+ *                      4t + q holds words 4q..4q+3 of lane chunk t) sit at
+ *                      unit (4q + t) XOR 4(tau%2) of the row
  *   [8Dl, +2RP)        rope, fp16, token-major (stored unquantised)
  *   then a[16], b[16] fp32, then the column-scale slice (Dl*P/N fp32)
  *   page_bytes = 6528 for Dl = 512, R = 64, N = 128.

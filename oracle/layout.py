@@ -77,32 +77,51 @@ def v_code_position(D: int, tau: int, j: int):
     return byte, bit % 8
 
 
+def latent_code_position(D: int, tau: int, j: int):
+    """(byte offset inside the latent-code region, bit shift) of token tau,
+    channel j. Same nibble and word content as the dense K placement, but
+    the 16-byte units of a token row (unit 4t + q of the K placement holds
+    words 4q..4q+3 of lane chunk t) are stored at unit (4q + t) XOR 4*(tau%2):
+    lane chunks interleaved, odd tokens shifted by four units."""
+    byte, shift = k_code_position(D, tau, j)
+    r = byte - tau * (D // 2)
+    t, rem = divmod(r, D // 8)
+    q, within = divmod(rem, 16)
+    unit = (4 * q + t) ^ (4 * (tau % 2))
+    return tau * (D // 2) + 16 * unit + within, shift
+
+
 @functools.lru_cache(maxsize=None)
 def _maps(D: int):
-    kb = np.zeros((P, D), dtype=np.int64)
-    ks = np.zeros((P, D), dtype=np.int64)
-    vb = np.zeros((P, D), dtype=np.int64)
-    vs = np.zeros((P, D), dtype=np.int64)
-    for tau in range(P):
-        for j in range(D):
-            kb[tau, j], ks[tau, j] = k_code_position(D, tau, j)
-            vb[tau, j], vs[tau, j] = v_code_position(D, tau, j)
-    return kb, ks, vb, vs
+    pos = {"k": k_code_position, "v": v_code_position, "latent": latent_code_position}
+    out = {}
+    for kind, f in pos.items():
+        if kind == "latent" and D // 32 < 8:
+            continue  # the latent order needs at least 8 units per token row
+        byte = np.zeros((P, D), dtype=np.int64)
+        shift = np.zeros((P, D), dtype=np.int64)
+        for tau in range(P):
+            for j in range(D):
+                byte[tau, j], shift[tau, j] = f(D, tau, j)
+        out[kind] = (byte, shift)
+    return out
+
+
+_WIDTH = {"k": (4, 8), "latent": (4, 8), "v": (2, 4)}   # bits, bytes per channel of a page
 
 
 def pack_codes(codes: np.ndarray, kind: str) -> np.ndarray:
     """Pack a [16, D] code block of one page into its region bytes."""
     D = codes.shape[1]
-    kb, ks, vb, vs = _maps(D)
-    byte, shift, nbytes = (kb, ks, 8 * D) if kind == "k" else (vb, vs, 4 * D)
-    out = np.zeros(nbytes, dtype=np.int64)
+    byte, shift = _maps(D)[kind]
+    out = np.zeros(_WIDTH[kind][1] * D, dtype=np.int64)
     np.bitwise_or.at(out, byte.ravel(), (codes.astype(np.int64) << shift).ravel())
     return out.astype(np.uint8)
 
 
 def unpack_codes(region: np.ndarray, D: int, kind: str) -> np.ndarray:
-    kb, ks, vb, vs = _maps(D)
-    byte, shift, mask = (kb, ks, 0xF) if kind == "k" else (vb, vs, 0x3)
+    byte, shift = _maps(D)[kind]
+    mask = (1 << _WIDTH[kind][0]) - 1
     return (region.astype(np.int64)[byte] >> shift) & mask
 
 
@@ -163,7 +182,8 @@ def read_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int):
 # --------------------------------------------------------------------------
 # MLA latent page: one shared latent of width Dl (4-bit codes, K = V) plus an
 # fp16 rope part of width R, 16 tokens per page.
-#   latent codes  8*Dl bytes   same placement as the dense K codes
+#   latent codes  8*Dl bytes   the dense K content, 16-byte units reordered
+#                              (latent_code_position)
 #   rope          2*R*P bytes  fp16, token-major
 #   a[16], b[16]  fp32
 #   col           Dl*P/N fp32  column-scale slice, as for the dense page

@@ -24,7 +24,7 @@ def write_tile(cache, lay: layout.LatentLayout, phys_pages, enc: dict, rope) -> 
     for p, phys in enumerate(phys_pages):
         pg = cache[phys]
         rows = slice(p * P, (p + 1) * P)
-        pg[lay.codes:lay.codes + 8 * Dl] = layout.pack_codes(enc["codes"][rows], "k")
+        pg[lay.codes:lay.codes + 8 * Dl] = layout.pack_codes(enc["codes"][rows], "latent")
         pg[lay.rope:lay.rope + 2 * R * P] = np.ascontiguousarray(rope16[rows]).view(np.uint8).ravel()
         pg[lay.a:lay.a + 4 * P] = layout.f32_bytes(enc["a"][rows])
         pg[lay.b:lay.b + 4 * P] = layout.f32_bytes(enc["b"][rows])
@@ -37,7 +37,7 @@ def read_tile(cache, lay: layout.LatentLayout, phys_pages):
     codes, a, b, c, rope = [], [], [], [], []
     for phys in phys_pages:
         pg = cache[phys]
-        codes.append(layout.unpack_codes(pg[lay.codes:lay.codes + 8 * Dl], Dl, "k"))
+        codes.append(layout.unpack_codes(pg[lay.codes:lay.codes + 8 * Dl], Dl, "latent"))
         rope.append(np.ascontiguousarray(pg[lay.rope:lay.rope + 2 * R * P]).view(np.float16)
                     .reshape(P, R).astype(np.float64))
         a.append(layout.f32_from(pg[lay.a:lay.a + 4 * P]))

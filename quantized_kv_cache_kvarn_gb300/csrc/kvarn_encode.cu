@@ -316,12 +316,18 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     const int pg = r / kPageTokens, tau = r % kPageTokens;
     if constexpr (!IS_V) {
       // each lane pair shares words; the even lane writes t = 0, 1, the odd lane t = 2, 3
-      uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D + tau * (D / 8) + w_pair;
+      uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D + tau * (D / 8);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t lo_t = k_word_part(P, j, s_par), hi_t = k_word_part(P, 2 + j, s_par);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, s_par ? lo_t : hi_t, 1);
-        img[(2 * s_par + j) * (D / 32)] = (s_par ? hi_t : lo_t) | other;
+        const int t = 2 * s_par + j;
+        int word;
+        if constexpr (KIND == 1)  // latent: 16-byte units 4q + t, XOR 4 on odd tokens
+          word = 4 * ((4 * (w_pair >> 2) + t) ^ (4 * (tau & 1))) + (w_pair & 3);
+        else
+          word = t * (D / 32) + w_pair;
+        img[word] = (s_par ? hi_t : lo_t) | other;
       }
     } else {
       // 2-bit V page order: word (4g + t) * (D/32) + w holds, for tokens

@@ -51,16 +51,17 @@ constexpr int kMlaPStride = kDl + 4;
 constexpr float kLog2eM = 1.4426950408889634f;
 
 // shared-memory map
-constexpr int kOffStage = 0;                                   // tile pages
-constexpr int kOffQ = kOffStage + kTile;                       // q' [16][512] fp32
+constexpr int kStages = 2;
+constexpr int kOffStage = 0;                                   // tile pages, two stages
+constexpr int kOffQ = kOffStage + kStages * kTile;             // q' [16][512] fp32
 constexpr int kOffAhi = kOffQ + kHeads * kDl * 4;              // A hi [16][kLDA] f16
 constexpr int kOffAlo = kOffAhi + kHeads * kLDA * 2;           // A lo
 constexpr int kOffP = kOffAlo + kHeads * kLDA * 2;             // P hi [16][kLDP] f16
 constexpr int kOffPlo = kOffP + kHeads * kLDP * 2;             // P lo
 constexpr int kOffRed = kOffPlo + kHeads * kLDP * 2;           // [8 warps][16] floats x 2
 constexpr int kOffQsum = kOffRed + 2 * kWarps * kHeads * 4;    // [16]
-constexpr int kOffBar = kOffQsum + kHeads * 4;                 // mbarrier
-constexpr int kOffPages = kOffBar + 16;                        // page ids
+constexpr int kOffBar = kOffQsum + kHeads * 4;                 // mbarriers, one per stage
+constexpr int kOffPages = kOffBar + 8 * kStages;               // page ids
 constexpr int kSmemBase = kOffPages;
 static_assert(kOffAhi % 16 == 0 && kOffP % 16 == 0 && kOffPlo % 16 == 0 && kOffBar % 8 == 0, "alignment");
 
@@ -179,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
     return;
   }
 
-  unsigned char* stage = smem + kOffStage;
   float* qrot = reinterpret_cast<float*>(smem + kOffQ);
   __half* Ahi = reinterpret_cast<__half*>(smem + kOffAhi);
   __half* Alo = reinterpret_cast<__half*>(smem + kOffAlo);
@@ -199,23 +199,29 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
     }
     pages[e] = phys;
   }
-  if (tid == 0) mbar_init(bar, 1);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
+  }
   fence_mbar_init();
   __syncthreads();
 
+  // tile `tile` of the split lives in stage (tile - t0) % 2
+  auto stage_of = [&](int tile) -> unsigned char* { return smem + kOffStage + ((tile - t0) & 1) * kTile; };
   auto issue = [&](int tile) {  // warp 0
+    uint64_t* sb = bar + ((tile - t0) & 1);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
+    if (lane == 0) mbar_arrive_expect_tx(sb, kTile);
     __syncwarp();
     if (lane < kPPT)
-      bulk_g2s(stage + lane * kPB, A.cache + static_cast<int64_t>(pages[(tile - t0) * kPPT + lane]) * kPB,
-               kPB, bar);
+      bulk_g2s(stage_of(tile) + lane * kPB,
+               A.cache + static_cast<int64_t>(pages[(tile - t0) * kPPT + lane]) * kPB, kPB, sb);
   };
   if (warp == 0) {
     issue(t0);
-    if (t0 + 1 < t1 && lane < kPPT)
-      prefetch_l2(A.cache + static_cast<int64_t>(pages[kPPT + lane]) * kPB, kPB);
+    if (t0 + 1 < t1) issue(t0 + 1);
+    if (t0 + 2 < t1 && lane < kPPT)
+      prefetch_l2(A.cache + static_cast<int64_t>(pages[2 * kPPT + lane]) * kPB, kPB);
   }
 
   // ---- rotated, scaled latent query rows (q'), rope query planes (once)
@@ -246,15 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
   int timed_out = 0;
 
   for (int tile = t0; tile < t1; ++tile) {
-    const uint32_t par = (tile - t0) & 1;
-    if (!mbar_wait_bounded(bar, par)) timed_out = true;
+    const uint32_t par = ((tile - t0) >> 1) & 1;
+    uint64_t* sbar = bar + ((tile - t0) & 1);
+    unsigned char* stage = stage_of(tile);
+    if (!mbar_wait_bounded(sbar, par)) timed_out = true;
     // -- A planes: q~ = q' * c, hi and lo, and the per-head sum of q~
     {
-      const int hl = tid >> 4, j0 = (tid & 15) * 32;  // 16 threads per head, 32 channels each
+      // 16 threads per head; thread r takes channel pairs 2r + 32i, so that
+      // neighbouring threads touch neighbouring words
+      const int hl = tid >> 4, j0 = (tid & 15) * 2;
       float s = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        const int j = j0 + e;
+        const int j = j0 + 16 * e;
         const float2 c = *reinterpret_cast<const float2*>(stage + (j / 64) * kPB + kPG.col() + (j % 64) * 4);
         const float2 q = *reinterpret_cast<const float2*>(qrot + hl * kDl + j);
         const float x0 = q.x * c.x, x1 = q.y * c.y;
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
       uint4 kw[2];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
-        kw[j] = *reinterpret_cast<const uint4*>(pg + (j * 8 + g) * (kDl / 2) + t * (kDl / 8) + 16 * q4);
+        kw[j] = *reinterpret_cast<const uint4*>(pg + (j * 8 + g) * (kDl / 2) + 16 * ((4 * q4 + t) ^ (4 * (g & 1))));
 #pragma unroll
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t bf[2][4];
@@ -406,8 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
       ldsm_x4(aq, prow_lo + 16 * pp);
       const unsigned char* cp = stage + pp * kPB;
       // codes of page tokens g and 8+g, channels 16kc..16kc+15 for kc = 4 warp .. 4 warp + 3
-      const uint2 w0 = *reinterpret_cast<const uint2*>(cp + g * (kDl / 2) + t * (kDl / 8) + 8 * warp);
-      const uint2 w1 = *reinterpret_cast<const uint2*>(cp + (8 + g) * (kDl / 2) + t * (kDl / 8) + 8 * warp);
+      // latent unit order: unit 4q + t at (4q + t) XOR 4 (tau % 2); this
+      // warp's words 2 warp, 2 warp + 1 are unit q = warp / 2, bytes 8 (warp % 2)
+      const int uo = 16 * ((4 * (warp >> 1) + t) ^ (4 * (g & 1))) + 8 * (warp & 1);
+      const uint2 w0 = *reinterpret_cast<const uint2*>(cp + g * (kDl / 2) + uo);
+      const uint2 w1 = *reinterpret_cast<const uint2*>(cp + (8 + g) * (kDl / 2) + uo);
 #pragma unroll
       for (int wi = 0; wi < 2; ++wi) {
         uint32_t f0[4], f1[4];
@@ -440,13 +453,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
     // the whole CTA (uniformly) after waiting a bounded time for it
     if (__syncthreads_or(timed_out)) {
       if (tid == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
-      mbar_wait_bounded(bar, par, 100000000LL);
+      // the copies still in flight: this tile's stage and the next one's
+      mbar_wait_bounded(sbar, par, 100000000LL);
+      if (tile + 1 < t1) mbar_wait_bounded(bar + ((tile + 1 - t0) & 1), ((tile + 1 - t0) >> 1) & 1, 100000000LL);
       break;
     }
-    if (warp == 0 && tile + 1 < t1) {
-      issue(tile + 1);
-      if (tile + 2 < t1 && lane < kPPT)
-        prefetch_l2(A.cache + static_cast<int64_t>(pages[(tile + 2 - t0) * kPPT + lane]) * kPB, kPB);
+    // this stage is free: refill it with tile + 2
+    if (warp == 0 && tile + 2 < t1) {
+      issue(tile + 2);
+      if (tile + 3 < t1 && lane < kPPT)
+        prefetch_l2(A.cache + static_cast<int64_t>(pages[(tile + 3 - t0) * kPPT + lane]) * kPB, kPB);
     }
   }
 

@@ -36,20 +36,35 @@ def test_page_bytes_hand_derived():
 
 @pytest.mark.parametrize("D", [128, 256, 512])
 def test_code_positions_are_a_bijection(D):
-    for kind, nbytes, width in (("k", 8 * D, 4), ("v", 4 * D, 2)):
+    kinds = [("k", 8 * D, 4), ("v", 4 * D, 2)] + ([("latent", 8 * D, 4)] if D >= 256 else [])
+    fn = {"k": layout.k_code_position, "v": layout.v_code_position, "latent": layout.latent_code_position}
+    for kind, nbytes, width in kinds:
         seen = set()
         for tau in range(16):
             for j in range(D):
-                pos = (layout.k_code_position if kind == "k" else layout.v_code_position)(D, tau, j)
+                pos = fn[kind](D, tau, j)
                 assert 0 <= pos[0] < nbytes and pos[1] % width == 0
                 seen.add(pos)
         assert len(seen) == 16 * D
 
 
+def test_latent_code_positions_hand_derived():
+    """Latent width 512: token 0 keeps the K placement's unit order with the
+    lane chunks interleaved; token 1 is shifted by four units (64 bytes).
+    Channel 0 is lane chunk 0, word 0, nibble 0; channel 1 nibble 4 (byte 2);
+    channel 8 nibble 1 (shift 4); channel 2 lane chunk 1 (unit 1); channel
+    130 lane chunk 1, word 4 (unit 4 * 1 + 1 = 5)."""
+    cases = {(0, 0): (0, 0), (1, 0): (256 + 64, 0), (0, 1): (2, 0), (1, 1): (256 + 66, 0),
+             (0, 8): (0, 4), (1, 8): (256 + 64, 4), (0, 2): (16, 0), (1, 2): (256 + 80, 0),
+             (0, 130): (80, 0), (1, 130): (256 + 16, 0)}
+    for (tau, j), want in cases.items():
+        assert layout.latent_code_position(512, tau, j) == want, (tau, j)
+
+
 @pytest.mark.parametrize("D", [128, 256, 512])
 def test_pack_unpack_roundtrip(D):
     rng = np.random.default_rng(D)
-    for kind, q in (("k", 16), ("v", 4)):
+    for kind, q in (("k", 16), ("v", 4)) + ((("latent", 16),) if D >= 256 else ()):
         codes = rng.integers(0, q, (16, D))
         np.testing.assert_array_equal(layout.unpack_codes(layout.pack_codes(codes, kind), D, kind), codes)
 
