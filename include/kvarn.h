@@ -37,17 +37,20 @@
  * scores on raw KV when the query is rotated by the same matrix).
  *
  * Dense page format (one page = P = 16 tokens of one KV head; bytes):
- *   K codes, 8D bytes, 4-bit, token-major. Within a token: four
- *                      lane chunks of D/8 bytes; chunk t holds channels
- *                      16kc + {2t, 2t+1, 2t+8, 2t+9} of every 16-channel
- *                      k-chunk kc. Word w of a chunk serves kc = 2w, 2w+1;
- *                      nibble n (bits 4n..4n+3) holds channel
- *                      16(2w + (n%4)/2) + 2t + 8(n%2) + n/4.
- *   V codes, 4D bytes, 2-bit. Lane chunk L = 4g + t (D/8 bytes)
- *                      holds channels 8nc + g of every 8-channel block nc at
- *                      tokens {2t, 2t+1, 2t+8, 2t+9}; word w serves blocks
- *                      4w..4w+3; token tau = 2t + e + 8h of block nc sits at
- *                      bit 2(2(nc%4) + h) + 16e of its word.
+ *   K codes, 8D bytes, 4-bit. Lane L = 4g + t (g in 0..7, t in 0..3)
+ *                      owns one 32-bit word per 16-channel k-chunk kc; its
+ *                      byte m = h + 2e holds channel 16kc + 2t + e + 8h of
+ *                      token g in the low nibble and of token 8 + g in the
+ *                      high nibble. The word of (kc, L) sits at byte
+ *                      16(32(kc/4) + L) + 4(kc%4): 16-byte units of four
+ *                      k-chunks, the 32 lanes' units contiguous.
+ *   V codes, 4D bytes, 2-bit. Lane L = 4g + t owns one word per four
+ *                      8-channel blocks nc = 4w + c; channel 8nc + g of
+ *                      token 2t + e + 8h sits at bit 2c + 8h + 16e. Word w of
+ *                      lane L sits at byte 8(32(w/2) + L) + 4(w%2).
+ *   Every code field of one tensor-core operand thus sits at one bit
+ *   position of its 16-bit half, so masking it out yields an exact fp16
+ *   subnormal operand (code times a power of two).
  * The page is a K part followed by a V part, each contiguous so that the
  * decode kernel can fetch and recycle them separately:
  *   K part, KP = 8D + 128 + 4C bytes, C = D*P/N:
@@ -64,10 +67,14 @@
  * A dequantised rotated value is y[i, j] = c[j] * (a[i] * code[i, j] + b[i]).
  *
  * MLA latent page (latent width Dl = 512, rope width R, 4-bit, K = V):
- *   [0, 8Dl)           latent codes: the dense K words of a token row
- *                      (above, with D = Dl), whose 16-byte units (unit
- *                      4t + q holds words 4q..4q+3 of lane chunk t) sit at
- *                      unit (4q + t) XOR 4(tau%2) of the row
+ *   [0, 8Dl)           latent codes, token-major rows of Dl/2 bytes. A row
+ *                      is four lane chunks of Dl/8 bytes; chunk t holds, per
+ *                      16-channel k-chunk kc, channels 16kc + {2t, 2t+1,
+ *                      2t+8, 2t+9}; its word w serves kc = 2w, 2w+1 and
+ *                      nibble n of the word holds channel
+ *                      16(2w + (n%4)/2) + 2t + 8(n%2) + n/4. The row's
+ *                      16-byte units (unit 4t + q holds words 4q..4q+3 of
+ *                      chunk t) sit at unit (4q + t) XOR 4(tau%2).
  *   [8Dl, +2RP)        rope, fp16, token-major (stored unquantised)
  *   then a[16], b[16] fp32, then the column-scale slice (Dl*P/N fp32)
  *   page_bytes = 6528 for Dl = 512, R = 64, N = 128.

@@ -7,17 +7,18 @@ paragraph on kvarn_k4v2_g128), 4-bit keys and 2-bit values (same paragraph),
 and a paged cache (vLLM block tables). Everything below the tile is this
 library's own format. A page holds P = 16 tokens of one KV head:
 
-  K codes   8*D bytes   4-bit, token-major; within a token, four lane chunks
-                        of D/8 bytes; chunk t holds, for every 16-channel
-                        k-chunk kc, channels 16kc + {2t, 2t+1, 2t+8, 2t+9}.
-                        Word w of a chunk serves k-chunks 2w and 2w+1; its
-                        nibble n (bits 4n..4n+3) holds channel
-                        16*(2w + (n%4)//2) + 2t + 8*(n%2) + (n//4).
-  V codes   4*D bytes   2-bit; lane chunk L = 4g + t (D/8 bytes) holds
-                        channels 8nc + g for every 8-channel block nc, at
-                        tokens {2t, 2t+1, 2t+8, 2t+9}. Word w of a chunk
-                        serves blocks 4w..4w+3; the token tau = 2t + e + 8h of
-                        block nc sits at bit 2*(2*(nc%4) + h) + 16*e.
+  K codes   8*D bytes   4-bit. Lane L = 4g + t (g, t in 0..7, 0..3) owns,
+                        for every 16-channel k-chunk kc, one 32-bit word;
+                        its byte m (m = h + 2e) holds channel
+                        16kc + 2t + e + 8h of token g in the low nibble and
+                        of token 8 + g in the high nibble. Words are stored
+                        as 16-byte units of four k-chunks: the word of
+                        (kc, L) sits at byte 16*(32*(kc//4) + L) + 4*(kc%4).
+  V codes   4*D bytes   2-bit. Lane L = 4g + t owns, for every four 8-channel
+                        blocks nc = 4w + c, one 32-bit word; channel 8nc + g
+                        of token 2t + e + 8h sits at bit 2c + 8h + 16e.
+                        Words are stored as 8-byte units of two: the word w
+                        of lane L sits at byte 8*(32*(w//2) + L) + 4*(w%2).
   The page is two parts, each contiguous: the K part (K codes, then K a[16],
   K b[16] fp32 row scales, then the K column-scale slice, D*P/N fp32), then
   the V part (V codes, V a[16], V b[16], V column-scale slice).
@@ -55,35 +56,46 @@ class DenseLayout:
 def k_code_position(D: int, tau: int, j: int):
     """(byte offset inside the K-code region, bit shift) of token tau, channel j."""
     kc, r = divmod(j, 16)
+    t, e, h = (r % 8) // 2, r % 2, r // 8
+    g, upper = tau % 8, tau // 8
+    lane = 4 * g + t
+    word = 16 * (32 * (kc // 4) + lane) + 4 * (kc % 4)
+    return word + h + 2 * e, 4 * upper
+
+
+def v_code_position(D: int, tau: int, j: int):
+    """(byte offset inside the V-code region, bit shift) of token tau, channel j."""
+    nc, g = divmod(j, 8)
+    t, e, h = (tau % 8) // 2, tau % 2, tau // 8
+    w, c = divmod(nc, 4)
+    lane = 4 * g + t
+    bit = 2 * c + 8 * h + 16 * e
+    return 8 * (32 * (w // 2) + lane) + 4 * (w % 2) + bit // 8, bit % 8
+
+
+def _latent_word_position(D: int, tau: int, j: int):
+    """Word content of the latent page before its 16-byte units are
+    reordered: token-major rows of D/2 bytes made of four lane chunks of D/8
+    bytes; chunk t holds, for every 16-channel k-chunk kc, channels
+    16kc + {2t, 2t+1, 2t+8, 2t+9}; word w of a chunk serves kc = 2w, 2w+1 and
+    its nibble n holds channel 16(2w + (n%4)//2) + 2t + 8(n%2) + n//4."""
+    kc, r = divmod(j, 16)
     t = (r % 8) // 2
-    e = r % 2          # second element of the pair
-    h = r // 8         # upper 8 channels of the k-chunk
+    e = r % 2
+    h = r // 8
     w, kp = divmod(kc, 2)
     n = 2 * kp + h + 4 * e
     byte = tau * (D // 2) + t * (D // 8) + 4 * w + n // 2
     return byte, 4 * (n % 2)
 
 
-def v_code_position(D: int, tau: int, j: int):
-    """(byte offset inside the V-code region, bit shift) of token tau, channel j."""
-    nc, g = divmod(j, 8)
-    t = (tau % 8) // 2
-    e = tau % 2
-    h = tau // 8
-    L = 4 * g + t
-    w, ncl = divmod(nc, 4)
-    bit = 2 * (2 * ncl + h) + 16 * e
-    byte = L * (D // 8) + 4 * w + bit // 8
-    return byte, bit % 8
-
-
 def latent_code_position(D: int, tau: int, j: int):
     """(byte offset inside the latent-code region, bit shift) of token tau,
-    channel j. Same nibble and word content as the dense K placement, but
-    the 16-byte units of a token row (unit 4t + q of the K placement holds
-    words 4q..4q+3 of lane chunk t) are stored at unit (4q + t) XOR 4*(tau%2):
-    lane chunks interleaved, odd tokens shifted by four units."""
-    byte, shift = k_code_position(D, tau, j)
+    channel j. The word content of _latent_word_position, with the 16-byte
+    units of a token row (unit 4t + q holds words 4q..4q+3 of lane chunk t)
+    stored at unit (4q + t) XOR 4*(tau%2): lane chunks interleaved, odd
+    tokens shifted by four units."""
+    byte, shift = _latent_word_position(D, tau, j)
     r = byte - tau * (D // 2)
     t, rem = divmod(r, D // 8)
     q, within = divmod(rem, 16)
@@ -182,7 +194,7 @@ def read_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int):
 # --------------------------------------------------------------------------
 # MLA latent page: one shared latent of width Dl (4-bit codes, K = V) plus an
 # fp16 rope part of width R, 16 tokens per page.
-#   latent codes  8*Dl bytes   the dense K content, 16-byte units reordered
+#   latent codes  8*Dl bytes   latent word content, 16-byte units reordered
 #                              (latent_code_position)
 #   rope          2*R*P bytes  fp16, token-major
 #   a[16], b[16]  fp32

@@ -179,7 +179,10 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint3
 // OR-ed into 0x6400 (fp16 1024) is 1024 + n; one at bits 4-7 is 1024 + 16n.
 // The offsets below recentre them: 4-bit codes to n - 8, 2-bit codes to
 // n - 2. Every intermediate is an integer below 2048, so each step is exact
-// and the mma sees ordinary normal fp16 operands.
+// and the mma sees ordinary normal fp16 operands. (Masked fields used
+// directly as fp16 subnormals would save the recentring, but the tensor
+// cores align a sum of such products as if the subnormal were 2^-14, which
+// drops about 10 - p bits of a field at bit p from the sum.)
 constexpr uint32_t kMagic = 0x64006400u;
 
 // One K word -> 4 half2: (kc even: b01, b23), (kc odd: b01, b23).
@@ -194,7 +197,8 @@ __device__ __forceinline__ void dequant_k_word(uint32_t x, uint32_t* out) {
   out[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00F000F0u, kMagic)), s16, o16));
 }
 
-// One V word -> 8 half2 in pair order p = 0..7 (fields at bits 2p, 2p + 16).
+// One V word -> 8 half2: fields at bits 2c, 2c + 16 (c = 0..3) as
+// out[c], then the same fields of x >> 8 as out[4 + c].
 __device__ __forceinline__ void dequant_v_word(uint32_t x, uint32_t* out) {
   const __half2 sub = __halves2half2(__ushort_as_half(0x6402), __ushort_as_half(0x6402));  // 1026
   const __half2 s4 = __halves2half2(__ushort_as_half(0x3400), __ushort_as_half(0x3400));   // 1/4

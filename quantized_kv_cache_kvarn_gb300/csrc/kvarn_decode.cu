@@ -16,8 +16,11 @@
 //   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
 //        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
 //        half of the m16 tile free, so the split costs no extra mma);
-//   S  = q~ (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
-//        integers, made from the packed nibbles by exponent-bias arithmetic);
+//   S  = q~ . (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
+//        integers, made from the packed nibbles by exponent-bias arithmetic;
+//        recentred codes keep every running sum near the size of its result,
+//        which the tensor cores need: they round a sum relative to its
+//        largest term);
 //   s  = a_K * S + (b_K + 8 a_K) * sum(q~)      (row scales folded back in);
 //   online softmax in base 2;
 //   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
@@ -58,7 +61,8 @@ struct DecShape {
   static constexpr int KC = D / 16;
   static constexpr int NC = D / 8;
   static constexpr int CPP = PG.cols();
-  static constexpr int LW = D / 32;  // words per lane chunk (K and V)
+  static constexpr int KCH = D / 64;  // 16-byte K units per lane and page (four k-chunks each)
+  static constexpr int VHC = D / 64;  // 8-byte V units per lane and page (eight channel blocks each)
   static constexpr int RING = W * WARP_SMEM;
   static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
   static constexpr int PREFETCH = 2;  // tiles prefetched into L2 ahead of the K slot
@@ -300,41 +304,44 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     }
     qsum = warp_sum_xor(qsum, 1, 4);
 
-    // -- S = q~ . (K codes - 8); four 8-token blocks at a time so that four
-    //    independent accumulator chains hide the mma latency
+    // -- S = q~ . (K codes - 8), two pages (four 8-token blocks) at a time so
+    //    that four independent accumulator chains hide the mma latency.
+    //    Tokens 0-7 of a page are the low nibbles of the words, tokens 8-15
+    //    the high nibbles.
     float s[S::NB][2];
 #pragma unroll
-    for (int nb0 = 0; nb0 < S::NB; nb0 += 4) {
-      float d[4][4];
+    for (int p0 = 0; p0 < S::PPT; p0 += 2) {
+      float d[2][2][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+      for (int pi = 0; pi < 2; ++pi)
 #pragma unroll
-      for (int q4 = 0; q4 < S::LW / 4; ++q4) {
-        uint4 kw[4];
+        for (int e = 0; e < 2; ++e) d[pi][e][0] = d[pi][e][1] = d[pi][e][2] = d[pi][e][3] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int nb = nb0 + j;
-          kw[j] = *reinterpret_cast<const uint4*>(kslot + (nb >> 1) * S::KP + ((nb & 1) * 8 + g) * (D / 2) +
-                                                  t * (D / 8) + 16 * q4);
-        }
+      for (int ch = 0; ch < S::KCH; ++ch) {
+        uint4 kw[2];
+#pragma unroll
+        for (int pi = 0; pi < 2; ++pi)
+          kw[pi] = *reinterpret_cast<const uint4*>(kslot + (p0 + pi) * S::KP + (ch * 32 + lane) * 16);
 #pragma unroll
         for (int w4 = 0; w4 < 4; ++w4) {
-          const int w = 4 * q4 + w4;
+          const int kc = 4 * ch + w4;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t word = w4 == 0 ? kw[j].x : w4 == 1 ? kw[j].y : w4 == 2 ? kw[j].z : kw[j].w;
-            uint32_t bf[4];
-            dequant_k_word(word, bf);
-            mma_f16(d[j], Aq[2 * w][0], Aq[2 * w][1], Aq[2 * w][2], Aq[2 * w][3], bf[0], bf[1]);
-            mma_f16(d[j], Aq[2 * w + 1][0], Aq[2 * w + 1][1], Aq[2 * w + 1][2], Aq[2 * w + 1][3], bf[2], bf[3]);
+          for (int pi = 0; pi < 2; ++pi) {
+            const uint32_t x = w4 == 0 ? kw[pi].x : w4 == 1 ? kw[pi].y : w4 == 2 ? kw[pi].z : kw[pi].w;
+            uint32_t bf[4];  // (low nibbles, high nibbles) of x, then of x >> 8
+            dequant_k_word(x, bf);
+            mma_f16(d[pi][0], Aq[kc][0], Aq[kc][1], Aq[kc][2], Aq[kc][3], bf[0], bf[2]);
+            mma_f16(d[pi][1], Aq[kc][0], Aq[kc][1], Aq[kc][2], Aq[kc][3], bf[1], bf[3]);
           }
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        s[nb0 + j][0] = d[j][0] + d[j][2];
-        s[nb0 + j][1] = d[j][1] + d[j][3];
-      }
+      for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          s[2 * (p0 + pi) + e][0] = d[pi][e][0] + d[pi][e][2];
+          s[2 * (p0 + pi) + e][1] = d[pi][e][1] + d[pi][e][3];
+        }
     }
 
     // -- row-scale fold and online softmax (base 2)
@@ -396,24 +403,24 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
       acc[nc][0] *= alpha;
       acc[nc][1] *= alpha;
     }
-    // channel blocks in groups of eight (two words of the lane chunk)
+    // channel blocks in groups of eight (one 8-byte unit of the lane's
+    // words; block 4w + c has its fields at bit 2c of each byte)
 #pragma unroll
-    for (int hq = 0; hq < S::LW / 2; ++hq) {
+    for (int hq = 0; hq < S::VHC; ++hq) {
       float u[8][4];
 #pragma unroll
       for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
 #pragma unroll
       for (int pp = 0; pp < S::PPT; ++pp) {
-        const uint2 vw = *reinterpret_cast<const uint2*>(vslot + pp * S::VP + (4 * g + t) * (D / 8) + 8 * hq);
-        uint32_t bf[8];
-        dequant_v_word(vw.x, bf);
+        const uint2 vw = *reinterpret_cast<const uint2*>(vslot + pp * S::VP + (hq * 32 + lane) * 8);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_f16(u[k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
-        dequant_v_word(vw.y, bf);
+        for (int wi = 0; wi < 2; ++wi) {
+          uint32_t bf[8];  // field classes 0-3 of x, then of x >> 8
+          dequant_v_word(wi ? vw.y : vw.x, bf);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_f16(u[4 + k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[2 * k], bf[2 * k + 1]);
+          for (int c = 0; c < 4; ++c)
+            mma_f16(u[4 * wi + c], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], bf[c], bf[4 + c]);
+        }
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {

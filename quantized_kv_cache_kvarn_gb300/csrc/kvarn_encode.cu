@@ -124,7 +124,7 @@ __device__ __forceinline__ float safe_sigma(float var, float mean) {
   return (isfinite(s) && s > 9.5367431640625e-07f * fabsf(mean)) ? s : 1.f;
 }
 
-// 4-bit page order (K and the MLA latent): in a page, the 32-bit word
+// Latent page word order (before the 16-byte unit swizzle): the 32-bit word
 // tau * (D/8) + t * (D/32) + w of token tau holds, at nibbles 0,1,4,5, the
 // codes of channels 2t, 2t+8, 2t+1, 2t+9 of 16-channel segment 2w and, at
 // nibbles 2,3,6,7, the same channels of segment 2w+1 (the B-fragment order
@@ -154,11 +154,22 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   float* colpart = reinterpret_cast<float*>(smem + S::OFF_COLPART);
   uint8_t** pages = reinterpret_cast<uint8_t**>(smem + S::OFF_PAGES);
 
-  // ---- load: row r_local(i) = i*32 + warp*RPW + rsub (within this CTA's rows)
+  // ---- load. Dense tiles: thread group j = warp*RPW + rsub (0..31) holds
+  // tokens j%8 and j%8 + 8 of RPT/2 pages, so that the two tokens sharing a
+  // packed byte of the dense page are in one thread. Latent tiles: row
+  // i*32 + j of this CTA's rows.
   float x[S::RPT][16];
+  auto local_row = [&](int i) -> int {
+    const int j = warp * S::RPW + rsub;
+    if constexpr (KIND == 0)
+      return kPageTokens * ((S::RPT / 2) * (j >> 3) + (i >> 1)) + (j & 7) + 8 * (i & 1);
+    else
+      return i * (S::NW * S::RPW) + j;
+  };
+  static_assert(KIND != 0 || (S::NW * S::RPW == 32 && S::RPT % 2 == 0), "dense row pairing");
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
-    const int r = crank * S::ROWS + i * (S::NW * S::RPW) + warp * S::RPW + rsub;
+    const int r = crank * S::ROWS + local_row(i);
     const T* p = src + static_cast<int64_t>(r) * D + seg * 16;
     load8<T>(p, x[i]);
     load8<T>(p + 8, x[i] + 8);
@@ -280,9 +291,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     __syncthreads();  // colbuf is rewritten by the next iteration
   }
 
-  // ---- asymmetric RTN per row; codes packed into page word order in `stage`
+  // ---- asymmetric RTN per row: codes as bytes, Pc[i][k] byte e = channel 4k + e
   constexpr int QMAX = (1 << BITS) - 1;
-  const int s_par = seg & 1, w_pair = seg >> 1;
+  uint32_t Pc[S::RPT][4];
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
     float lo = x[i][0], hi = x[i][0];
@@ -298,7 +309,6 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     }
     const float delta = (hi - lo) / static_cast<float>(QMAX);
     const float rinv = delta > 0.f ? 1.f / delta : 0.f;
-    uint32_t P[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint32_t word = 0;
@@ -310,64 +320,88 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
         const uint32_t q = min(__float2uint_rn((x[i][4 * k + e] - lo) * rinv), static_cast<uint32_t>(QMAX));
         word |= q << (8 * e);
       }
-      P[k] = word;
+      Pc[i][k] = word;
     }
-    const int r = i * (S::NW * S::RPW) + warp * S::RPW + rsub;  // local row
-    const int pg = r / kPageTokens, tau = r % kPageTokens;
-    if constexpr (!IS_V) {
+    if (seg == 0) {
+      const int r = local_row(i);
+      rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
+      rowB[r] = rscale[i] * lo;
+    }
+  }
+
+  // ---- codes packed into the page's word order in `stage`
+  const int s_par = seg & 1, w_pair = seg >> 1;
+  if constexpr (KIND == 1) {
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i) {
+      const int r = local_row(i);
+      const int pg = r / kPageTokens, tau = r % kPageTokens;
       // each lane pair shares words; the even lane writes t = 0, 1, the odd lane t = 2, 3
       uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D + tau * (D / 8);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const uint32_t lo_t = k_word_part(P, j, s_par), hi_t = k_word_part(P, 2 + j, s_par);
+        const uint32_t lo_t = k_word_part(Pc[i], j, s_par), hi_t = k_word_part(Pc[i], 2 + j, s_par);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, s_par ? lo_t : hi_t, 1);
         const int t = 2 * s_par + j;
-        int word;
-        if constexpr (KIND == 1)  // latent: 16-byte units 4q + t, XOR 4 on odd tokens
-          word = 4 * ((4 * (w_pair >> 2) + t) ^ (4 * (tau & 1))) + (w_pair & 3);
-        else
-          word = t * (D / 32) + w_pair;
+        // 16-byte units 4q + t, XOR 4 on odd tokens
+        const int word = 4 * ((4 * (w_pair >> 2) + t) ^ (4 * (tau & 1))) + (w_pair & 3);
         img[word] = (s_par ? hi_t : lo_t) | other;
       }
-    } else {
-      // 2-bit V page order: word (4g + t) * (D/32) + w holds, for tokens
-      // 2t + e + 8h and channels 32w + g + 8j, the code at bit 4j + 2h + 16e.
-      // The thread's byte for group g (codes of channels g and g + 8 of its
-      // segment, nibble-spaced) is staged at byte 4h + 2e + s of that word's
-      // 8-byte slot; the copy-out folds the h = 1 half in with a 2-bit shift.
-      const uint32_t Wa = P[0] | (P[2] << 4), Wb = P[1] | (P[3] << 4);
-      const int h = tau >> 3, e = tau & 1, t = (tau & 7) >> 1;
-      unsigned char* base = stage + (pg * D + t * (D / 32) + w_pair) * 8 + 4 * h + 2 * e + s_par;
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        base[g * 4 * (D / 32) * 8] = static_cast<unsigned char>((g < 4 ? Wa : Wb) >> (8 * (g & 3)));
     }
-    if (seg == 0) {
-      rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
-      rowB[r] = rscale[i] * lo;
+  } else {
+    const int j = warp * S::RPW + rsub, g = j & 7;
+#pragma unroll
+    for (int ip = 0; ip < S::RPT / 2; ++ip) {
+      const int pg = (S::RPT / 2) * (j >> 3) + ip;
+      const uint32_t* P0 = Pc[2 * ip];      // token g of the page
+      const uint32_t* P1 = Pc[2 * ip + 1];  // token g + 8
+      if constexpr (!IS_V) {
+        // 4-bit: word (kc = seg, lane 4g + t) bytes = channels 2t, 2t+8,
+        // 2t+1, 2t+9; token g in the low nibble, token g + 8 in the high one
+        uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+          const uint32_t w0 = __byte_perm(P0[t >> 1], P0[2 + (t >> 1)], sel);
+          const uint32_t w1 = __byte_perm(P1[t >> 1], P1[2 + (t >> 1)], sel);
+          img[((seg >> 2) * 32 + 4 * g + t) * 4 + (seg & 3)] = w0 | (w1 << 4);
+        }
+      } else {
+        // 2-bit: channel 16 seg + g' (block 2 seg) and 16 seg + 8 + g' (block
+        // 2 seg + 1) of this token land at bits 2c, c = 2 (seg % 2) + {0, 1},
+        // of byte h + 2e of word (w = seg / 2, lane 4 g' + t); this thread's
+        // two tokens are h = 0 and h = 1. Byte g' of A/B: channel g' | g'+8 << 2.
+        uint32_t A0 = P0[0] | (P0[2] << 2), B0 = P0[1] | (P0[3] << 2);
+        uint32_t A1 = P1[0] | (P1[2] << 2), B1 = P1[1] | (P1[3] << 2);
+        const uint32_t oA0 = __shfl_xor_sync(0xffffffffu, A0, 1), oB0 = __shfl_xor_sync(0xffffffffu, B0, 1);
+        const uint32_t oA1 = __shfl_xor_sync(0xffffffffu, A1, 1), oB1 = __shfl_xor_sync(0xffffffffu, B1, 1);
+        if (s_par == 0) {
+          A0 |= oA0 << 4; B0 |= oB0 << 4; A1 |= oA1 << 4; B1 |= oB1 << 4;
+          const int tau = g, t = tau >> 1, e = tau & 1, w = w_pair;
+          uint16_t* img = reinterpret_cast<uint16_t*>(stage) + pg * 2 * D;
+          // halfword of channel g' = (byte of token g, byte of token g + 8)
+          const uint32_t hw[4] = {__byte_perm(A0, A1, 0x5140), __byte_perm(A0, A1, 0x7362),
+                                  __byte_perm(B0, B1, 0x5140), __byte_perm(B0, B1, 0x7362)};
+#pragma unroll
+          for (int gg = 0; gg < 8; ++gg) {
+            const int word = ((w >> 1) * 32 + 4 * gg + t) * 2 + (w & 1);
+            img[2 * word + e] = static_cast<uint16_t>(hw[gg >> 1] >> (16 * (gg & 1)));
+          }
+        }
+      }
     }
   }
   if (tid < D) colC[tid] = cscale;
   __syncthreads();
 
   // ---- codes: 16-byte stores of the staged page words
-  if constexpr (!IS_V) {
-    constexpr int CPP = 2 * D / 4;  // 16-byte chunks per page
+  {
+    constexpr int CPP = (IS_V ? 4 : 8) * D / 16;  // 16-byte chunks per page
+    const int base = IS_V ? DensePage(D, N).v_codes() : 0;
     const uint4* img = reinterpret_cast<const uint4*>(stage);
     for (int c = tid; c < S::PPC * CPP; c += S::NT) {
       uint8_t* pg = pages[c / CPP];
-      if (pg) reinterpret_cast<uint4*>(pg)[c % CPP] = img[c];
-    }
-  } else {
-    constexpr int CPP = D / 4;
-    const int base = DensePage(D, N).v_codes();
-    const uint4* st = reinterpret_cast<const uint4*>(stage);
-    for (int c = tid; c < S::PPC * CPP; c += S::NT) {
-      uint8_t* pg = pages[c / CPP];
-      if (!pg) continue;
-      const uint4 a = st[2 * c], bb = st[2 * c + 1];
-      reinterpret_cast<uint4*>(pg + base)[c % CPP] =
-          make_uint4(a.x | (a.y << 2), a.z | (a.w << 2), bb.x | (bb.y << 2), bb.z | (bb.w << 2));
+      if (pg) reinterpret_cast<uint4*>(pg + base)[c % CPP] = img[c];
     }
   }
 

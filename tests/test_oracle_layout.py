@@ -25,7 +25,8 @@ def test_page_bytes_hand_derived():
     D = 128
     tau, j = np.meshgrid(np.arange(16), np.arange(D), indexing="ij")
     kc = (j + j // 16 + 3 * tau) % 16
-    vc = (3 * j + tau + j // 8) % 4
+    nc = j // 8
+    vc = (j % 8 + nc * (nc + 1) // 2 + tau) % 4
     kb = layout.pack_codes(kc, "k")
     vb = layout.pack_codes(vc, "v")
     assert kb.size == 1024 and vb.size == 512

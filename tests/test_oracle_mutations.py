@@ -119,22 +119,23 @@ def _attention_no_scale(orig):
 
 
 def _k_nibble_order(orig):
+    # the pair element and the upper-eight flag trade places in the byte index
     def pos(D, tau, j):
         kc, r = divmod(j, 16)
         t, e, h = (r % 8) // 2, r % 2, r // 8
-        w, kp = divmod(kc, 2)
-        n = kp + 2 * h + 4 * e
-        return tau * (D // 2) + t * (D // 8) + 4 * w + n // 2, 4 * (n % 2)
+        lane = 4 * (tau % 8) + t
+        return 16 * (32 * (kc // 4) + lane) + 4 * (kc % 4) + e + 2 * h, 4 * (tau // 8)
     return pos
 
 
 def _v_pair_order(orig):
+    # tokens 8 apart and tokens 1 apart trade their bit offsets
     def pos(D, tau, j):
         nc, g = divmod(j, 8)
         t, e, h = (tau % 8) // 2, tau % 2, tau // 8
-        w, ncl = divmod(nc, 4)
-        bit = 2 * (2 * ncl + e) + 16 * h
-        return (4 * g + t) * (D // 8) + 4 * w + bit // 8, bit % 8
+        w, c = divmod(nc, 4)
+        bit = 2 * c + 8 * e + 16 * h
+        return 8 * (32 * (w // 2) + 4 * g + t) + 4 * (w % 2) + bit // 8, bit % 8
     return pos
 
 
