@@ -10,7 +10,8 @@
 // each of its W warps owns every W-th tile of the split. A warp keeps one
 // shared-memory slot for the K parts and one for the V parts of its tile's
 // pages, filled by one-dimensional bulk copies (completion counted on an
-// mbarrier), and prefetches the pages of its next tiles into L2. The K slot
+// mbarrier); an L2 prefetch of later tiles measured slower (its lines were
+// partly evicted and read twice) and is not used. The K slot
 // is refilled with the next tile while P V runs, the V slot while the next
 // Q K runs. Per tile and warp:
 //   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
@@ -65,7 +66,6 @@ struct DecShape {
   static constexpr int VHC = D / 64;  // 8-byte V units per lane and page (eight channel blocks each)
   static constexpr int RING = W * WARP_SMEM;
   static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
-  static constexpr int PREFETCH = 2;  // tiles prefetched into L2 ahead of the K slot
   static_assert(W * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
 };
@@ -237,9 +237,6 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     __syncwarp();
     if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
   };
-  auto prefetch = [&](int i) {
-    if (lane < S::PPT) prefetch_l2(page_of(i), S::PB);
-  };
 
   if (lane == 0) {
     mbar_init(barK, 1);
@@ -251,7 +248,6 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     issue_k(0);
     issue_v(0);
   }
-  for (int j = 1; j <= S::PREFETCH && j < n_my; ++j) prefetch(j);
 
   // ---- rotated, scaled query rows of the group (rows >= G are zero)
   for (int h = warp; h < 8; h += W) {
@@ -369,9 +365,8 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     lsum = fmaf(lsum, alpha, psum);
     m = m_new;
 
-    // the K slot is free: start the next tile's K part, prefetch further
+    // the K slot is free: start the next tile's K part
     if (i + 1 < n_my) issue_k(i + 1);
-    if (i + 1 + S::PREFETCH < n_my) prefetch(i + 1 + S::PREFETCH);
 
     if (!mbar_wait_bounded(barV, par)) {
       timed_out = true;
