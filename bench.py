@@ -9,7 +9,7 @@ with 128-token tiles; its step commits the tile the newest token just filled
 in every (sequence, KV head). Other workloads (--workload):
   toy     1 sequence, 1024 tokens: commit the last tile, decode
   g64     64-token tiles, lengths 2K-32K, fp16 tails: re-commit the last full
-          tile of every sequence, decode with the tails
+          tile of every sequence (one call), decode with the tails
   hybrid  head_dim 256, 65536 tokens: encode the 4096-token prefill chunk
           (tiles 480..511), decode
   mla     64 sequences x 128 heads on a 512-wide int4 latent + fp16 rope:
@@ -39,7 +39,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn packed-KV GB/s (% of HBM peak), tokens/s; encode tokens/s"
 WORKLOAD = "dense32b"
-DECODE_SOURCES = ["kvarn_decode.cu", "kvarn_common.cuh", "kvarn_merge.cuh"]
+DECODE_SOURCES = {"dense": ["kvarn_decode.cu", "kvarn_common.cuh", "kvarn_merge.cuh"],
+                  "mla": ["kvarn_mla.cu", "kvarn_common.cuh", "kvarn_merge.cuh"]}
 
 
 def _peaks():
@@ -51,9 +52,19 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def decode_source_digest():
+def _tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s), burst: the decode is timed alone.
+    fp16 has the same nominal dense rate as bf16."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def decode_source_digest(kind="dense"):
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
+    for f in DECODE_SOURCES[kind]:
         with open(os.path.join(ROOT, "quantized_kv_cache_kvarn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -240,17 +251,22 @@ class DenseHarness:
             self.commit.append((case.k[:, :, (T - 1) * N:], case.v[:, :, (T - 1) * N:], ts, case.block_table, N))
             self.encode_tokens = B * N
         else:
-            # variable lengths: every sequence's last full tile is re-committed,
-            # one call per sequence
+            # variable lengths: every sequence's last full tile is re-committed
+            # in one call, from a [B, Hkv, N, D] buffer of those tiles' raw
+            # tokens (where a serving engine keeps the tile that just filled);
+            # a sequence without a full tile gets tile_start -1 (skipped)
+            ts, src_k, src_v = [], [], []
             for b, L in enumerate(lens):
                 T = L // N
                 if T > 1:
                     kv.encode_tiles(case.k[b:b + 1], case.v[b:b + 1], self.lay, zeros1, case.block_table[b:b + 1],
                                     self.cache, self.err, chunk_tokens=(T - 1) * N)
-                if T:
-                    ts = torch.full((1,), T - 1, dtype=torch.int32, device=dev)
-                    self.commit.append((case.k[b:b + 1, :, (T - 1) * N:], case.v[b:b + 1, :, (T - 1) * N:], ts,
-                                        case.block_table[b:b + 1], N))
+                ts.append(T - 1 if T else -1)
+                c0 = max(T - 1, 0) * N
+                src_k.append(case.k[b:b + 1, :, c0:c0 + N])
+                src_v.append(case.v[b:b + 1, :, c0:c0 + N])
+            ck, cv = torch.cat(src_k).contiguous(), torch.cat(src_v).contiguous()
+            self.commit.append((ck, cv, torch.tensor(ts, dtype=torch.int32, device=dev), case.block_table, N))
             self.encode_tokens = sum(1 for L in lens if L // N) * N
         # fp16 tails of the partial last tiles
         self.tail_k = self.tail_v = None
@@ -561,7 +577,8 @@ def run_kvarn(args):
         with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as fh:
             tr = json.load(fh)
         entry = tr.get(wl.name)
-        if entry and entry.get("source_digest") == decode_source_digest() and not args.num_seqs:
+        kind = "mla" if wl.rope_dim else "dense"
+        if entry and entry.get("source_digest") == decode_source_digest(kind) and not args.num_seqs:
             traffic = entry.get("bytes_per_launch")
     except Exception:
         pass
@@ -579,6 +596,23 @@ def run_kvarn(args):
                          f"float64 oracle on {cores} single-threaded host processes",
                "decode_tokens_per_s": round(frac * B / wall, 4)}
 
+    kernel_desc = "decode call (split kernel + merge kernel), CUDA events on its stream"
+    if wl.rope_dim:
+        # MLA: tensor-bound. Algorithmic flops = 2 per multiply-add of the
+        # scores (latent + rope width) and of the output (latent width) for
+        # every (sequence, head, token); the kernel issues twice that on the
+        # tensor cores (fp16 hi + lo operands).
+        flops = 2.0 * sum(H.lens) * wl.num_q_heads * (2 * wl.head_dim + wl.rope_dim)
+        tpk, tpk_kind = _tensor_peak()
+        tf = flops / (dec_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s",
+                    "frac": round(tf / tpk, 4), "traffic": traffic, "kernel": kernel_desc,
+                    "peak_kind": tpk_kind, "flops_per_launch": flops,
+                    "hbm_gbs": round(dec_gbs, 2), "hbm_frac": round(dec_gbs / peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+                    "frac": round(dec_gbs / peak, 4), "traffic": traffic, "kernel": kernel_desc,
+                    "peak_kind": peak_kind, "bytes_per_launch": H.packed}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -594,10 +628,7 @@ def run_kvarn(args):
         "commit_ms": round(enc_ms, 5), "commit_tokens": H.encode_tokens,
         "encode_tokens_per_s": round(encode_tok_s, 1), "encode_full_context_ms": round(enc_full_ms, 4),
         "fp16_kv_decode": fp16,
-        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "kernel": "decode call (split kernel + merge kernel), CUDA events on its stream",
-                     "peak_kind": peak_kind},
+        "roofline": roofline,
         "e2e": {"value": round(world * H.packed / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": H.launches * args.steps,

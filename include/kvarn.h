@@ -150,7 +150,9 @@ int64_t kvarn_page_bytes(const kvarn_layout* layout);
  *                b*seq_stride + h*head_stride + i*D + d  (elements)
  *   seq_stride, head_stride  in elements, multiples of 8
  *   chunk_tokens multiple of N (0 is a no-op)
- *   tile_start   device int32 [num_seqs]
+ *   tile_start   device int32 [num_seqs]; a negative entry skips sequence b
+ *                (nothing of it is read or written), so that one call can
+ *                commit the tiles that filled in some sequences of a batch
  *   block_table  device int32, row stride bt_stride
  *   cache        device bytes [num_pages][Hkv][page_bytes]
  *   error_flags  device uint32 (bits are OR-ed in; never cleared here)
@@ -201,6 +203,46 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
                      const void* tail_v, int32_t num_seqs, float* out, float* lse,
                      void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
                      kvarn_stream_t stream);
+
+/*
+ * kvarn_decode_verify - speculative-decoding verification: num_queries query
+ * tokens per sequence, causal among themselves, over the compressed cache.
+ *
+ * KVarN review, speculative-decoding paragraph: a block is committed only
+ * once all its tokens are accepted; gmlx page, "Speed and speculative
+ * decoding": a batch verifies up to 4 tokens per row. Sequence b holds
+ * L = seq_lens[b] tokens, the last Q = num_queries of them under
+ * verification; query token j (0 <= j < Q) is token L - Q + j and attends to
+ * tokens [0, L - Q + 1 + j). Tokens up to the first query token are
+ * accepted, so the committed tiles are [0, C), C = floor((L - Q + 1)/N)*N,
+ * read from the pages, and tokens [C, L) are rows 0.. of the raw tail
+ * buffer (at most N + Q - 2 of them). With Q = 1 this is kvarn_decode.
+ *
+ *   q              device, kv_dtype [num_seqs][Q][num_q_heads][D]
+ *   num_queries    1 .. KVARN_MAX_VERIFY_QUERIES
+ *   tail_k/v       device, kv_dtype [num_seqs][Hkv][tail_capacity][D], or
+ *                  NULL when no query sees a token past C
+ *   tail_capacity  rows per (sequence, KV head), >= N + Q - 2, <= 4096
+ *   out            device fp32 [num_seqs][Q][num_q_heads][D]
+ *   lse            device fp32 [num_seqs][Q][num_q_heads] or NULL
+ *   workspace      device, >= kvarn_decode_verify_workspace_bytes(...)
+ * Other arguments as for kvarn_decode. A query token that sees no token
+ * gives out = 0 and lse = -inf. (query head, query token) pairs share the
+ * tensor-core row tile in groups of eight, so up to 8 / (num_q_heads / Hkv)
+ * query tokens cost the compute of one.
+ */
+#define KVARN_MAX_VERIFY_QUERIES 8
+
+int64_t kvarn_decode_verify_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t num_queries,
+                                            int32_t max_seq_len);
+
+int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
+                            const void* cache, const kvarn_layout* layout, const int32_t* block_table,
+                            int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                            const void* tail_k, const void* tail_v, int32_t tail_capacity,
+                            int32_t num_seqs, float* out, float* lse, void* workspace,
+                            int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream);
 
 /*
  * kvarn_fp16_page_bytes / kvarn_store_fp16 / kvarn_decode_fp16 - the same

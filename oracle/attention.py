@@ -89,6 +89,63 @@ def decode(q, cache, lay: layout.DenseLayout, block_table, seq_lens, sm_scale,
     return out, lse
 
 
+def verify_committed(L: int, Q: int, N: int) -> int:
+    """Committed tokens of a sequence of L tokens whose last Q are under
+    verification: the whole tiles of the accepted tokens [0, L - Q + 1)."""
+    return (max(0, L - Q + 1) // N) * N
+
+
+def verify_visible(L: int, Q: int, j: int) -> int:
+    """Tokens seen by query token j (token L - Q + j): [0, L - Q + 1 + j)."""
+    return max(0, L - Q + 1 + j)
+
+
+def decode_verify(q, cache, lay: layout.DenseLayout, block_table, seq_lens, sm_scale,
+                  tail_k=None, tail_v=None, rows=None):
+    """Speculative verification: Q query tokens per sequence, causal among
+    themselves (gmlx page, "Speed and speculative decoding": a batch
+    verifies several tokens per row; KVarN review, speculative-decoding
+    paragraph: a block commits only once all its tokens are accepted).
+
+    Sequence b holds L = seq_lens[b] tokens, the last Q under verification;
+    query token j is token L - Q + j and attends to tokens [0, L - Q + 1 + j).
+    The accepted tokens [0, L - Q + 1) fill the committed tiles
+    [0, C), C = floor((L - Q + 1) / N) * N, read from the pages; tokens
+    [C, L) are rows 0.. of the raw tail buffer.
+
+    q [B, Q, Hq, D]; tail_k/v [B, Hkv, capacity, D]; rows = [(b, j, h), ...]
+    or None for all. Returns (out [B, Q, Hq, D], lse [B, Q, Hq]); a query that
+    sees no token gives out = 0 and lse = -inf, unlisted rows NaN.
+    """
+    q = np.asarray(q, np.float64)
+    B, Q, Hq, D = q.shape
+    Hkv = cache.shape[1]
+    G = Hq // Hkv
+    N = lay.N
+    out = np.full((B, Q, Hq, D), np.nan)
+    lse = np.full((B, Q, Hq), np.nan)
+    todo = rows if rows is not None else [(b, j, h) for b in range(B) for j in range(Q) for h in range(Hq)]
+    kv_cache = {}
+    for b, j, h in todo:
+        L = int(seq_lens[b])
+        kvh = h // G
+        key = (b, kvh)
+        if key not in kv_cache:
+            C = verify_committed(L, Q, N)
+            K, V = sequence_kv(cache, lay, block_table[b], C, kvh)
+            if L > C:
+                K = np.concatenate([K, np.asarray(tail_k[b, kvh], np.float64)[:L - C]])
+                V = np.concatenate([V, np.asarray(tail_v[b, kvh], np.float64)[:L - C]])
+            kv_cache[key] = (K, V)
+        K, V = kv_cache[key]
+        vis = verify_visible(L, Q, j)
+        if vis == 0:
+            out[b, j, h], lse[b, j, h] = 0.0, -np.inf
+            continue
+        out[b, j, h], lse[b, j, h] = softmax_attention(q[b, j, h], K[:vis], V[:vis], sm_scale)
+    return out, lse
+
+
 def encode_into_cache(cache, lay: layout.DenseLayout, k, v, block_table, tile_start,
                       bits=(4, 2), T=2):
     """Encode every full tile of a chunk and store it.

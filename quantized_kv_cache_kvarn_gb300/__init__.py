@@ -59,6 +59,9 @@ _SIGS = {
     "kvarn_decode_workspace_bytes": ([_LP, _I32, _I32, _I32], _I64),
     "kvarn_decode": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _I64,
                       _P, _P], _I32),
+    "kvarn_decode_verify_workspace_bytes": ([_LP, _I32, _I32, _I32, _I32], _I64),
+    "kvarn_decode_verify": ([_P, _I32, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P,
+                             _P, _I64, _P, _P], _I32),
     "kvarn_fp16_page_bytes": ([_LP], _I64),
     "kvarn_store_fp16": ([_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _I32, _LP, _P, _P, _P], _I32),
     "kvarn_decode_fp16": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _I32, _P, _P, _P, _I64, _P,
@@ -170,6 +173,27 @@ def decode(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, wo
                               _ptr(tail_k), _ptr(tail_v), B, _ptr(out), _ptr(lse), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(err),
                               _stream(stream)), "decode")
+
+
+def decode_verify_workspace_bytes(layout: Layout, num_seqs: int, num_q_heads: int, num_queries: int,
+                                  max_seq_len: int) -> int:
+    n = lib().kvarn_decode_verify_workspace_bytes(ctypes.byref(layout), num_seqs, num_q_heads, num_queries,
+                                                  max_seq_len)
+    if n < 0:
+        raise ValueError("invalid arguments for kvarn_decode_verify_workspace_bytes")
+    return n
+
+
+def decode_verify(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, workspace, err,
+                  sm_scale, tail_k=None, tail_v=None, lse=None, stream=None):
+    """q: [B, Q, Hq, D]; tail_k/v: [B, Hkv, capacity, D]; out: [B, Q, Hq, D]."""
+    B, Q, Hq, _ = q.shape
+    cap = tail_k.shape[2] if tail_k is not None else layout.tile_tokens + Q - 2
+    _check(lib().kvarn_decode_verify(_ptr(q), Hq, Q, sm_scale, _ptr(cache), ctypes.byref(layout),
+                                     _ptr(block_table), block_table.stride(0), _ptr(seq_lens), max_seq_len,
+                                     _ptr(tail_k), _ptr(tail_v), max(cap, 1), B, _ptr(out), _ptr(lse),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+                                     _stream(stream)), "decode_verify")
 
 
 def alloc_fp16_cache(layout: Layout, device=None) -> torch.Tensor:

@@ -105,17 +105,34 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
   return from_cuda(launch_encode_dense(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static SplitPlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_queries, int32_t max_seq_len) {
+  const int32_t G = num_q_heads / L->num_kv_heads;
+  return plan_dense(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len, L->tile_tokens,
+                    dense_decode_warps(L->head_dim), dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens));
+}
+
 int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
                                      int32_t max_seq_len) {
   if (kvarn_layout_check(L) != KVARN_OK || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0)
     return -1;
   if (is_latent(L)) return mla_workspace_bytes(num_seqs, num_q_heads, plan_mla(num_seqs, max_seq_len));
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens,
-                                    dense_decode_warps(L->head_dim),
-                                    dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens));
+  if (num_q_heads % L->num_kv_heads) return -1;
+  const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, 1, max_seq_len);
   const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
   return std::max(dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan),
                   dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan16));
+}
+
+int64_t kvarn_decode_verify_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t num_queries, int32_t max_seq_len) {
+  if (kvarn_layout_check(L) != KVARN_OK || is_latent(L) || num_seqs < 0 || num_q_heads < 1 ||
+      max_seq_len < 0 || num_queries < 1 || num_queries > KVARN_MAX_VERIFY_QUERIES ||
+      num_q_heads % L->num_kv_heads)
+    return -1;
+  const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries,
+                                    std::max(0, max_seq_len - num_queries + 1));
+  return dense_workspace_bytes(num_seqs, num_q_heads * num_queries, L->head_dim, plan);
 }
 
 static int32_t check_decode_common(const kvarn_layout* L, int32_t num_q_heads,
@@ -131,12 +148,12 @@ static int32_t check_decode_common(const kvarn_layout* L, int32_t num_q_heads,
   return KVARN_OK;
 }
 
-int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
-                     const kvarn_layout* L, const int32_t* block_table, int32_t bt_stride,
-                     const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
-                     const void* tail_v, int32_t num_seqs, float* out, float* lse,
-                     void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
-                     kvarn_stream_t stream) {
+static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
+                                   const void* cache, const kvarn_layout* L, const int32_t* block_table,
+                                   int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                                   const void* tail_k, const void* tail_v, int32_t tail_cap,
+                                   int32_t num_seqs, float* out, float* lse, void* workspace,
+                                   int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
   int32_t s = check_dense(L);
   if (s != KVARN_OK) return s;
   s = check_decode_common(L, num_q_heads, block_table, bt_stride, seq_lens, max_seq_len, num_seqs,
@@ -144,14 +161,14 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
   if (s != KVARN_OK || num_seqs == 0) return s;
   if (!q || !cache) return KVARN_EINVAL;
   if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
-  const int32_t committed_pages = (max_seq_len / L->tile_tokens) * (L->tile_tokens / kPageTokens);
+  // committed tiles: those filled by the accepted tokens [0, len - Q + 1)
+  const int32_t accepted = std::max(0, max_seq_len - num_queries + 1);
+  const int32_t committed_pages = (accepted / L->tile_tokens) * (L->tile_tokens / kPageTokens);
   if (bt_stride < committed_pages) return KVARN_EINVAL;
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
   if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len, L->tile_tokens,
-                                    dense_decode_warps(L->head_dim),
-                                    dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens));
-  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
+  const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries, accepted);
+  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads * num_queries, L->head_dim, plan))
     return KVARN_EWORKSPACE;
   DecodeParams p{};
   p.q = q;
@@ -174,7 +191,36 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
   p.workspace = workspace;
   p.err = error_flags;
   p.bf16 = L->kv_dtype == 1;
+  p.num_queries = num_queries;
+  p.tail_cap = tail_cap;
   return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                     const kvarn_layout* L, const int32_t* block_table, int32_t bt_stride,
+                     const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
+                     const void* tail_v, int32_t num_seqs, float* out, float* lse,
+                     void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                     kvarn_stream_t stream) {
+  if (!L) return KVARN_EINVAL;
+  return decode_dense_common(q, num_q_heads, 1, sm_scale, cache, L, block_table, bt_stride, seq_lens,
+                             max_seq_len, tail_k, tail_v, L->tile_tokens, num_seqs, out, lse, workspace,
+                             workspace_bytes, error_flags, stream);
+}
+
+int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
+                            const void* cache, const kvarn_layout* L, const int32_t* block_table,
+                            int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                            const void* tail_k, const void* tail_v, int32_t tail_capacity,
+                            int32_t num_seqs, float* out, float* lse, void* workspace,
+                            int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
+  if (!L) return KVARN_EINVAL;
+  if (num_queries < 1 || num_queries > KVARN_MAX_VERIFY_QUERIES) return KVARN_EUNSUPPORTED;
+  if (tail_capacity < L->tile_tokens + num_queries - 2 || tail_capacity < 1 || tail_capacity > 4096)
+    return KVARN_EINVAL;
+  return decode_dense_common(q, num_q_heads, num_queries, sm_scale, cache, L, block_table, bt_stride,
+                             seq_lens, max_seq_len, tail_k, tail_v, tail_capacity, num_seqs, out, lse,
+                             workspace, workspace_bytes, error_flags, stream);
 }
 
 int64_t kvarn_fp16_page_bytes(const kvarn_layout* L) {

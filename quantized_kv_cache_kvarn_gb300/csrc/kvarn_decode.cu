@@ -71,10 +71,12 @@ struct DecShape {
 };
 
 struct DecArgs {
-  const void* q;
-  float kappa;  // sm_scale * log2(e)
+  const void* q;  // [B][Q][Hq][D]
+  float kappa;    // sm_scale * log2(e)
   const uint8_t* cache;
   int32_t Hq, Hkv, G;
+  int32_t Q;         // query tokens per sequence (speculative verify: the last Q tokens)
+  int32_t tail_cap;  // tail rows per (sequence, KV head)
   int64_t num_pages;
   const int32_t* bt;
   int32_t bt_stride;
@@ -109,52 +111,66 @@ __device__ __forceinline__ void write_empty(float* part, int D, int lane) {
   for (int j = lane; j < D; j += 32) part[4 + j] = 0.f;
 }
 
-// fp16 tail over tokens [committed, len): dense attention in the original
-// basis, one warp per query head.
+// Rows of a CTA: up to eight (query head, query token) pairs, pair p = 8 rg + r
+// with head p % G and query token p / G, so that one mma row tile serves G Q
+// <= 8 pairs at the cost of one.
+struct RowMap {
+  int rg, n;  // row group, rows used in it
+  __device__ RowMap(const DecArgs& A, int rg_) : rg(rg_), n(min(8, A.G * A.Q - 8 * rg_)) {}
+  __device__ int head(const DecArgs& A, int r) const { return (8 * rg + r) % A.G; }
+  __device__ int query(const DecArgs& A, int r) const { return (8 * rg + r) / A.G; }
+};
+
+// Partial slot of (sequence b, query token j, query head hq).
+__device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j, int hq, int slot) {
+  return A.ws + (static_cast<int64_t>((b * A.Q + j) * A.Hq + hq) * A.slots + slot) * kPStride(D);
+}
+
+// Tokens visible to query token j of a sequence of len tokens (causal among
+// the Q tokens under verification), and the committed prefix shared by all.
+__device__ __forceinline__ int visible_len(int len, int Q, int j) { return max(0, len - Q + 1 + j); }
+
+// Raw tail over tokens [committed, visible): dense attention in the original
+// basis, one warp per row, one pass with a running maximum (no per-token
+// buffer, so the tail length is bounded only by its buffer).
 template <int D, int N, typename T, int W>
-__device__ void tail_partials(const DecArgs& A, int b, int kvh, int tail, unsigned char* smem) {
+__device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int committed) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float* sbuf = reinterpret_cast<float*>(smem) + warp * N;
-  for (int h = warp; h < A.G; h += W) {
-    const int hq = kvh * A.G + h;
-    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + hq) * A.slots + A.nsplit) * kPStride(D);
-    if (tail == 0 || A.tail_k == nullptr || A.tail_v == nullptr) {
+  for (int r = warp; r < R.n; r += W) {
+    const int j = R.query(A, r), hq = kvh * A.G + R.head(A, r);
+    const int tail = visible_len(len, A.Q, j) - committed;
+    float* part = part_of(A, D, b, j, hq, A.nsplit);
+    if (tail <= 0 || A.tail_k == nullptr || A.tail_v == nullptr) {
       if (tail > 0 && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
       write_empty(part, D, lane);
       continue;
     }
     float qv[E];
-    load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + hq) * D + lane * E, qv);
+    load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, qv);
 #pragma unroll
     for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
-    const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * N;
+    const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
     const T* tk = static_cast<const T*>(A.tail_k);
     const T* tv = static_cast<const T*>(A.tail_v);
-    float mx = -INFINITY;
-    for (int tau = 0; tau < tail; ++tau) {
-      float kv[E];
-      load_vec<T, E>(tk + (row0 + tau) * D + lane * E, kv);
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
-      dot = warp_sum_xor(dot, 1, 32);
-      if (lane == 0) sbuf[tau] = dot;
-      mx = fmaxf(mx, dot);
-    }
-    __syncwarp();
-    float l = 0.f, acc[E];
+    float mx = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     for (int tau = 0; tau < tail; ++tau) {
-      const float p = exp2f(sbuf[tau] - mx);
-      l += p;
-      float vv[E];
+      float kv[E], vv[E];
+      load_vec<T, E>(tk + (row0 + tau) * D + lane * E, kv);
       load_vec<T, E>(tv + (row0 + tau) * D + lane * E, vv);
+      float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[e], acc[e]);
+      for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
+      dot = warp_sum_xor(dot, 1, 32);  // identical in every lane
+      const float mn = fmaxf(mx, dot);
+      const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
+      l = fmaf(l, sc, p);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], sc, p * vv[e]);
+      mx = mn;
     }
-    __syncwarp();
     if (lane == 0) {
       part[0] = mx;
       part[1] = l;
@@ -173,25 +189,26 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
   const int g = lane >> 2, t = lane & 3;
   // KV head is the fastest grid axis: CTAs resident together read the same
   // physical pages (all heads of a page are contiguous), keeping DRAM rows open
-  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-  const int G = A.G;
+  const int kvh = blockIdx.x % A.Hkv, split = blockIdx.y, b = blockIdx.z;
+  const RowMap R(A, blockIdx.x / A.Hkv);
 
   int len = A.seq_lens[b];
   if (len < 0 || len > A.max_seq_len) {
     if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
     len = len < 0 ? 0 : A.max_seq_len;
   }
-  const int ntiles = len / N;
+  // only tokens up to the first query token are accepted, so only the tiles
+  // they fill are committed (read from the compressed pages)
+  const int ntiles = visible_len(len, A.Q, 0) / N;
 
   if (split == A.nsplit) {
-    tail_partials<D, N, T, W>(A, b, kvh, len - ntiles * N, smem);
+    tail_partials<D, N, T, W>(A, b, kvh, R, len, ntiles * N);
     return;
   }
   const int t0 = split * A.tps, t1 = min(t0 + A.tps, ntiles);
   if (t0 >= t1) {
-    for (int h = warp; h < G; h += W)
-      write_empty(A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + h) * A.slots + split) * kPStride(D),
-                  D, lane);
+    for (int r = warp; r < R.n; r += W)
+      write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), split), D, lane);
     return;
   }
 
@@ -249,12 +266,13 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     issue_v(0);
   }
 
-  // ---- rotated, scaled query rows of the group (rows >= G are zero)
+  // ---- rotated, scaled query rows of the row group (unused rows are zero)
   for (int h = warp; h < 8; h += W) {
     constexpr int E = D / 32;
     float v[E];
-    if (h < G) {
-      load_vec<T, E>(static_cast<const T*>(A.q) + static_cast<int64_t>(b * A.Hq + kvh * G + h) * D + lane * E, v);
+    if (h < R.n) {
+      const int hq = kvh * A.G + R.head(A, h), j = R.query(A, h);
+      load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, v);
       warp_fwht<E>(v);
       const float sc = A.kappa / sqrtf(static_cast<float>(D));
 #pragma unroll
@@ -451,7 +469,7 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[nc][1];
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+  for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
     const int gg = idx / D, j = idx % D;
     float M = -INFINITY;
 #pragma unroll
@@ -466,7 +484,7 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
         L = fmaf(r[1], sc, L);
       }
     }
-    float* part = A.ws + (static_cast<int64_t>(b * A.Hq + kvh * G + gg) * A.slots + split) * kPStride(D);
+    float* part = part_of(A, D, b, R.query(A, gg), kvh * A.G + R.head(A, gg), split);
     part[4 + j] = a;
     if (j == 0) {
       part[0] = M;
@@ -556,7 +574,7 @@ static cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
   const int smem = S::SMEM + A.tps * S::PPT * 4;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(A.Hkv, A.nsplit + 1, num_seqs);
+  dim3 grid(A.Hkv * row_groups(A.G, A.Q), A.nsplit + 1, num_seqs);
   kern<<<grid, W * 32, smem, st>>>(A);
   return cudaGetLastError();
 }
@@ -570,6 +588,8 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   A.Hq = p.num_q_heads;
   A.Hkv = p.num_kv_heads;
   A.G = p.num_q_heads / p.num_kv_heads;
+  A.Q = p.num_queries > 0 ? p.num_queries : 1;
+  A.tail_cap = p.tail_cap > 0 ? p.tail_cap : p.N;
   A.num_pages = p.num_pages;
   A.bt = p.block_table;
   A.bt_stride = p.bt_stride;
@@ -593,7 +613,7 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH
   if (e != cudaSuccess) return e;
-  const int rows = p.num_seqs * p.num_q_heads;
+  const int rows = p.num_seqs * A.Q * p.num_q_heads;
   if (p.D == 128)
     merge_kernel<128><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
   else

@@ -455,6 +455,7 @@ __global__ void __launch_bounds__(2 * D) encode_dense_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
   const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);
+  if (A.tile_start[b] < 0) return;  // nothing to commit for this sequence (uniform per CTA)
   const int64_t off = static_cast<int64_t>(b) * A.seq_stride + static_cast<int64_t>(head) * A.head_stride +
                       static_cast<int64_t>(u) * N * D;
   if (is_v)
@@ -468,6 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
     encode_latent_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int u = blockIdx.x >> 1, b = blockIdx.y;
+  if (A.tile_start[b] < 0) return;  // uniform over the cluster: both CTAs share b
   const T* src = static_cast<const T*>(A.x[0]) + static_cast<int64_t>(b) * A.seq_stride +
                  static_cast<int64_t>(u) * 128 * 512;
   encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, smem);

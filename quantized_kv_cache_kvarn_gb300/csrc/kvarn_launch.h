@@ -57,7 +57,12 @@ struct DecodeParams {
   void* workspace;
   uint32_t* err;
   bool bf16;
+  int32_t num_queries;  // dense: query tokens per sequence (0 or 1: plain decode)
+  int32_t tail_cap;     // dense: tail rows per (sequence, KV head) (0: N)
 };
+
+// (query head, query token) row groups of eight per KV head.
+inline int32_t row_groups(int32_t G, int32_t Q) { return (G * Q + 7) / 8; }
 
 // Split-K plan: tiles per split and the number of splits (+1 slot for the
 // tail partial). Depends only on the arguments and the device's SM count.

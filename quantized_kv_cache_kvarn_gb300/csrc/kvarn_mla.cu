@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
       mn0 = fmaxf(mn0, red[w * kHeads + g]);
       mn1 = fmaxf(mn1, red[w * kHeads + g + 8]);
     }
-    const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+    const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
     m[0] = mn0;
     m[1] = mn1;
     // -- weights p * a (fp16 A operand of P V) and the offset sums
@@ -370,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
       const int idx = j * 8 + 2 * t;
       const float2 ka = *reinterpret_cast<const float2*>(pg + kPG.a() + idx * 4);
       const float2 kb = *reinterpret_cast<const float2*>(pg + kPG.b() + idx * 4);
-      const float p0 = exp2f(s[j][0] - mn0), p1 = exp2f(s[j][1] - mn0);
-      const float p2 = exp2f(s[j][2] - mn1), p3 = exp2f(s[j][3] - mn1);
+      const float p0 = fast_exp2(s[j][0] - mn0), p1 = fast_exp2(s[j][1] - mn0);
+      const float p2 = fast_exp2(s[j][2] - mn1), p3 = fast_exp2(s[j][3] - mn1);
       ps0 += p0 + p1;
       ps1 += p2 + p3;
       const float b0 = fmaf(8.f, ka.x, kb.x), b1 = fmaf(8.f, ka.y, kb.y);
@@ -508,19 +508,20 @@ SplitPlan plan_mla(int32_t num_seqs, int32_t max_seq_len) {
     p.nsplit = 0;
   } else {
     // CTAs of 16 heads: 8 per (sequence, split) at 128 heads; one CTA per SM
+    // Every split writes a 512-float partial per head that the merge reads
+    // back, so take the fewest splits whose wave efficiency is within 0.05
+    // of the best one.
     const double slots = device_sm_count();
     const int units = std::max(1, num_seqs) * 8;
     const int max_split = std::max(1, tiles / 2);
-    int best = 1;
-    double best_eff = 0.0;
-    for (int n = 1; n <= max_split; ++n) {
+    auto eff_of = [&](int n) {
       const double waves = units * static_cast<double>(n) / slots;
-      const double eff = waves / std::ceil(waves);
-      if (eff > best_eff + 0.02) {
-        best_eff = eff;
-        best = n;
-      }
-    }
+      return waves / std::ceil(waves);
+    };
+    double top = 0.0;
+    for (int n = 1; n <= max_split; ++n) top = std::max(top, eff_of(n));
+    int best = 1;
+    while (best < max_split && eff_of(best) < top - 0.05) ++best;
     p.tiles_per_split = (tiles + best - 1) / best;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
   }

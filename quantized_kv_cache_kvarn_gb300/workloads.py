@@ -184,6 +184,14 @@ def make_dense(wl: Workload, device="cpu", seed: Optional[int] = None) -> DenseC
     return DenseCase(wl, out[0], out[1], q, seq_lens, bt, num_pages)
 
 
+def verify_queries(wl: Workload, num_queries: int, device="cpu", seed: Optional[int] = None) -> torch.Tensor:
+    """Query rows of the tokens under speculative verification: [B, Q, Hq, D]
+    N(0,1) in the workload's dtype."""
+    g = _gen(device, (wl.seed if seed is None else seed) + 104729)
+    return torch.randn((wl.num_seqs, num_queries, wl.num_q_heads, wl.head_dim), generator=g,
+                       device=device).to(TORCH_DTYPE[wl.dtype])
+
+
 def make_latent(wl: Workload, device="cpu", seed: Optional[int] = None) -> LatentCase:
     g = _gen(device, wl.seed if seed is None else seed)
     B, L, Dl, R = wl.num_seqs, wl.context, wl.head_dim, wl.rope_dim

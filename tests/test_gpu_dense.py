@@ -77,6 +77,31 @@ def test_encode_is_idempotent_and_touches_only_its_pages():
         assert int(cache1[unused].abs().sum()) == 0
 
 
+def test_negative_tile_start_skips_the_sequence():
+    """One commit call for a batch in which only some sequences filled a
+    tile: a negative tile_start leaves that sequence's pages untouched and
+    the others get exactly the bytes of a call without it."""
+    wl, case = _case("dense_small")
+    dev = "cuda"
+    lay = kv.dense_layout(wl.head_dim, wl.tile_tokens, wl.num_kv_heads, case.num_pages)
+    N = wl.tile_tokens
+    bt = case.block_table.to(dev)
+    k, v = case.k[:, :, N:2 * N].contiguous().to(dev), case.v[:, :, N:2 * N].contiguous().to(dev)
+    both = kv.alloc_cache(lay, dev)
+    err = kv.new_error_word(dev)
+    kv.encode_tiles(k, v, lay, torch.tensor([1, 1], dtype=torch.int32, device=dev), bt, both, err, chunk_tokens=N)
+    only1 = kv.alloc_cache(lay, dev)
+    kv.encode_tiles(k, v, lay, torch.tensor([-1, 1], dtype=torch.int32, device=dev), bt, only1, err, chunk_tokens=N)
+    torch.cuda.synchronize()
+    assert kv.read_error_flags(err) == 0
+    ppt = N // 16
+    pages0 = case.block_table[0, ppt:2 * ppt].tolist()
+    pages1 = case.block_table[1, ppt:2 * ppt].tolist()
+    assert int(only1[pages0].abs().sum()) == 0
+    assert torch.equal(only1[pages1], both[pages1])
+    assert int(both[pages0].abs().sum()) > 0
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_decode_on_oracle_pages_matches_oracle(name):
     wl, case = _case(name)

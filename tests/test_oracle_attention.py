@@ -187,3 +187,103 @@ def test_mla_decode_rope_and_shared_latent():
         s = sm * K @ np.concatenate([ql[0, h], qr[0, h]])
         np.testing.assert_allclose(out[0, h], scipy.special.softmax(s) @ latent_hat, rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(lse[0, h], scipy.special.logsumexp(s), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- verify
+def _verify_case(lens, Q, B=None, Hkv=2, G=2, D=128, N=64, seed=3):
+    """Cache with the accepted tiles committed and the rest in a raw tail of
+    N + Q - 2 rows, built from the commit rule's definition."""
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    lay = layout.DenseLayout(D, N)
+    Lmax = max(lens)
+    k = rng.standard_normal((B, Hkv, Lmax, D))
+    v = rng.standard_normal((B, Hkv, Lmax, D))
+    k[..., 9] *= 15
+    q = rng.standard_normal((B, Q, Hkv * G, D))
+    ppt = N // 16
+    C = [(max(0, L - Q + 1) // N) * N for L in lens]
+    num_pages = sum(c // N for c in C) * ppt + 2
+    bt = np.full((B, Lmax // 16 + 2), -1)
+    off = 0
+    for b in range(B):
+        n = C[b] // N * ppt
+        bt[b, :n] = np.arange(off, off + n)[::-1]
+        off += n
+    cache = np.zeros((num_pages, Hkv, lay.page_bytes), np.uint8)
+    for b in range(B):
+        if C[b]:
+            attention.encode_into_cache(cache, lay, k[b:b + 1, :, :C[b]], v[b:b + 1, :, :C[b]], bt[b:b + 1], [0])
+    cap = N + Q - 2
+    tk = np.full((B, Hkv, cap, D), np.nan)
+    tv = np.full((B, Hkv, cap, D), np.nan)
+    for b, L in enumerate(lens):
+        tk[b, :, :L - C[b]] = k[b, :, C[b]:L]
+        tv[b, :, :L - C[b]] = v[b, :, C[b]:L]
+    return dict(lay=lay, k=k, v=v, q=q, bt=bt, cache=cache, lens=np.array(lens), tk=tk, tv=tv, C=C, G=G)
+
+
+def test_verify_with_one_query_is_decode():
+    c = _verify_case([200, 64, 130], Q=1)
+    out, lse = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
+    ref, rlse = attention.decode(c["q"][:, 0], c["cache"], c["lay"], c["bt"], c["lens"], 0.1,
+                                 c["tk"][:, :, :64], c["tv"][:, :, :64])
+    np.testing.assert_array_equal(out[:, 0], ref)
+    np.testing.assert_array_equal(lse[:, 0], rlse)
+
+
+def test_verify_without_committed_tiles_is_causal_softmax():
+    """Nothing committed (L - Q + 1 < N): query j is plain softmax attention
+    over the raw tokens 0 .. L - Q + j, by scipy."""
+    L, Q = 40, 4
+    c = _verify_case([L], Q)
+    assert c["C"] == [0]
+    out, lse = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.07, c["tk"], c["tv"])
+    for j in range(Q):
+        for h in range(4):
+            K, V = c["k"][0, h // 2, :L - Q + 1 + j], c["v"][0, h // 2, :L - Q + 1 + j]
+            s = 0.07 * K @ c["q"][0, j, h]
+            np.testing.assert_allclose(out[0, j, h], scipy.special.softmax(s) @ V, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(lse[0, j, h], scipy.special.logsumexp(s), rtol=1e-12)
+
+
+def test_verify_is_causal():
+    """Changing the last token under verification changes only the last
+    query token's output."""
+    L, Q = 150, 3
+    c = _verify_case([L], Q)
+    a, _ = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
+    tk, tv = c["tk"].copy(), c["tv"].copy()
+    last = L - 1 - c["C"][0]
+    tk[0, :, last] *= -3.0
+    tv[0, :, last] += 5.0
+    b, _ = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, tk, tv)
+    np.testing.assert_array_equal(a[0, :Q - 1], b[0, :Q - 1])
+    assert np.abs(a[0, Q - 1] - b[0, Q - 1]).max() > 1e-3
+
+
+def test_verify_keeps_a_tile_filled_by_drafts_raw():
+    """The tokens under verification complete a tile (L - Q + 1 < 2N <= L):
+    that tile is not committed, so every query reads its tokens raw; query 0
+    equals plain decode at length L - Q + 1, whose commit point is the same."""
+    N, Q = 64, 4
+    L = 2 * N + 1  # accepted: 2N - 2 tokens, one committed tile
+    c = _verify_case([L], Q, N=N)
+    assert c["C"] == [N]
+    out, _ = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
+    ref, _ = attention.decode(c["q"][:, 0], c["cache"], c["lay"], c["bt"], np.array([L - Q + 1]), 0.1,
+                              c["tk"][:, :, :N], c["tv"][:, :, :N])
+    np.testing.assert_allclose(out[:, 0], ref, rtol=1e-12, atol=1e-13)
+    # the last query: dequantised first tile, then 2N + 1 - N = N + 1 raw tokens
+    K0, V0 = attention.sequence_kv(c["cache"], c["lay"], c["bt"][0], N, 0)
+    K = np.concatenate([K0, c["k"][0, 0, N:L]])
+    V = np.concatenate([V0, c["v"][0, 0, N:L]])
+    s = 0.1 * K @ c["q"][0, Q - 1, 0]
+    np.testing.assert_allclose(out[0, Q - 1, 0], scipy.special.softmax(s) @ V, rtol=1e-10, atol=1e-12)
+
+
+def test_verify_queries_before_the_first_token_see_nothing():
+    c = _verify_case([2], Q=4)
+    out, lse = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
+    assert (out[0, :2] == 0).all() and np.isneginf(lse[0, :2]).all()
+    assert np.isfinite(lse[0, 2:]).all()

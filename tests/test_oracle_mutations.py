@@ -35,6 +35,8 @@ PINS = [
     (ta.test_decode_equals_rotated_space_computation, {}),
     (ta.test_tail_only_sequence_is_plain_attention, {}),
     (ta.test_mla_decode_rope_and_shared_latent, {}),
+    (ta.test_verify_without_committed_tiles_is_causal_softmax, {}),
+    (ta.test_verify_keeps_a_tile_filled_by_drafts_raw, {}),
 ]
 
 
@@ -152,6 +154,14 @@ def _tail_off_by_one(orig):
     return skv
 
 
+def _commit_from_full_length(orig):
+    return lambda L, Q, N: (L // N) * N
+
+
+def _visible_off_by_one(orig):
+    return lambda L, Q, j: max(0, L - Q + j)
+
+
 MUTATIONS = [
     ("hadamard without 1/sqrt(D)", codec, "hadamard", _hadamard_unscaled),
     ("hadamard with a wrong sign", codec, "hadamard", _hadamard_wrong_sign),
@@ -167,6 +177,8 @@ MUTATIONS = [
     ("V token halves swapped", layout, "v_code_position", _v_pair_order),
     ("query head mapped to the wrong KV head", attention, "sequence_kv", _wrong_kv_head),
     ("tail read one token off", attention, "sequence_kv", _tail_off_by_one),
+    ("verify commits tiles the drafts filled", attention, "verify_committed", _commit_from_full_length),
+    ("verify query sees one token too few", attention, "verify_visible", _visible_off_by_one),
 ]
 
 
