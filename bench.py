@@ -158,6 +158,28 @@ def _oracle_unit(args):
             layout.write_tile(cache, lay, list(range((tiles - 1) * ppt, tiles * ppt)), 0, ek, ev)
         attention.decode(q[None], cache, lay, bt, [L], sm, tk, tv)
         return time.perf_counter() - t0
+    if kind == "verify":
+        _, k, v, q, sm, N, L, Q = args
+        lay = layout.DenseLayout(k.shape[-1], N)
+        C = attention.verify_committed(L, Q, N)
+        tiles = C // N
+        ppt = N // 16
+        cache = np.zeros((max(1, tiles) * ppt, 1, lay.page_bytes), np.uint8)
+        bt = np.arange(max(1, tiles) * ppt)[None, :]
+        if tiles > 1:
+            attention.encode_into_cache(cache, lay, k[None, None, :(tiles - 1) * N],
+                                        v[None, None, :(tiles - 1) * N], bt, [0])
+        tk = np.zeros((1, 1, N + Q - 2, k.shape[-1]))
+        tv = np.zeros_like(tk)
+        tk[0, 0, :L - C] = k[C:L]
+        tv[0, 0, :L - C] = v[C:L]
+        t0 = time.perf_counter()
+        if tiles:
+            ek = codec.encode_tile(k[(tiles - 1) * N:tiles * N], 4, 2)
+            ev = codec.encode_tile(v[(tiles - 1) * N:tiles * N], 2, 2)
+            layout.write_tile(cache, lay, list(range((tiles - 1) * ppt, tiles * ppt)), 0, ek, ev)
+        attention.decode_verify(q[None], cache, lay, bt, [L], sm, tk, tv)
+        return time.perf_counter() - t0
     _, lat, rope, ql, qr, sm, L = args
     lay = layout.LatentLayout(512, 64, 128)
     tiles = L // 128
@@ -186,7 +208,7 @@ def oracle_time(pool, cores, work):
     return sum(pool.map(_oracle_unit, work)) / cores
 
 
-def oracle_work(wl, case, n):
+def oracle_work(wl, case, n, queries=1, qv=None):
     """Host float64 inputs of n sampled units of the step, and the fraction
     of the whole step they are."""
     if wl.rope_dim:
@@ -208,9 +230,13 @@ def oracle_work(wl, case, n):
     work = []
     for b, h in pick:
         L = int(case.seq_lens[b])
-        work.append(("dense", case.k[b, h, :L].double().cpu().numpy(), case.v[b, h, :L].double().cpu().numpy(),
-                     case.q[b, h * G:(h + 1) * G].double().cpu().numpy(), 1 / math.sqrt(wl.head_dim),
-                     wl.tile_tokens, L))
+        k, v = case.k[b, h, :L].double().cpu().numpy(), case.v[b, h, :L].double().cpu().numpy()
+        if queries > 1:
+            work.append(("verify", k, v, qv[b, :, h * G:(h + 1) * G].double().cpu().numpy(),
+                         1 / math.sqrt(wl.head_dim), wl.tile_tokens, L, queries))
+        else:
+            work.append(("dense", k, v, case.q[b, h * G:(h + 1) * G].double().cpu().numpy(),
+                         1 / math.sqrt(wl.head_dim), wl.tile_tokens, L))
     return work, len(pick) / len(units)
 
 
@@ -372,6 +398,86 @@ class DenseHarness:
         return run, h2d, d2h
 
 
+class VerifyHarness(DenseHarness):
+    """Dense workloads under speculative verification: the last Q tokens of
+    every sequence are under verification. A step commits one accepted tile
+    per (sequence, KV head) and runs one kvarn_decode_verify over Q query
+    tokens per sequence; only the tiles of accepted tokens are read from the
+    pages, the rest (up to N + Q - 2 tokens) from the raw tail."""
+
+    def __init__(self, kv, W, wl, dev, rank, Q):
+        import torch
+        self.kv, self.wl, self.dev, self.Q = kv, wl, dev, Q
+        self.case = case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
+        B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
+        self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
+        self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters)
+        self.cache = kv.alloc_cache(self.lay, dev)
+        self.err = kv.new_error_word(dev)
+        lens = case.seq_lens.cpu().tolist()
+        self.lens, self.Lmax = lens, max(lens)
+        committed = [(max(0, L - Q + 1) // N) * N for L in lens]
+        z1 = torch.zeros(1, dtype=torch.int32, device=dev)
+        ts, src_k, src_v = [], [], []
+        for b, C in enumerate(committed):
+            T = C // N
+            if T > 1:
+                kv.encode_tiles(case.k[b:b + 1], case.v[b:b + 1], self.lay, z1, case.block_table[b:b + 1],
+                                self.cache, self.err, chunk_tokens=(T - 1) * N)
+            ts.append(T - 1 if T else -1)
+            c0 = max(T - 1, 0) * N
+            src_k.append(case.k[b:b + 1, :, c0:c0 + N])
+            src_v.append(case.v[b:b + 1, :, c0:c0 + N])
+        self.commit = [(torch.cat(src_k).contiguous(), torch.cat(src_v).contiguous(),
+                        torch.tensor(ts, dtype=torch.int32, device=dev), case.block_table, N)]
+        self.encode_tokens = sum(1 for C in committed if C) * N
+        cap = N + Q - 2
+        self.tail_k = torch.zeros((B, Hkv, cap, D), dtype=case.k.dtype, device=dev)
+        self.tail_v = torch.zeros_like(self.tail_k)
+        for b, (L, C) in enumerate(zip(lens, committed)):
+            self.tail_k[b, :, :L - C] = case.k[b, :, C:L]
+            self.tail_v[b, :, :L - C] = case.v[b, :, C:L]
+        self.qv = W.verify_queries(wl, Q, device=dev, seed=wl.seed + 7919 * rank)
+        self.out = torch.empty((B, Q, wl.num_q_heads, D), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(kv.decode_verify_workspace_bytes(self.lay, B, wl.num_q_heads, Q, self.Lmax),
+                              dtype=torch.uint8, device=dev)
+        self.sm = W.default_sm_scale(wl)
+        pb = kv.page_bytes(self.lay)
+        self.packed = sum(Hkv * (C * pb // 16 + (L - C) * D * 2 * 2) for L, C in zip(lens, committed))
+        self.launches = 3
+        self.tokens_per_step = B * Q
+
+    def decode(self, q=None, lens=None):
+        c = self.case
+        self.kv.decode_verify(self.qv if q is None else q, self.lay, self.cache, c.block_table,
+                              c.seq_lens if lens is None else lens, self.Lmax, self.out, self.ws, self.err,
+                              self.sm, self.tail_k, self.tail_v)
+
+    def full_encode(self):
+        return DenseHarness.full_encode(self)
+
+    def fp16_decode_setup(self):
+        return None
+
+    def e2e_setup(self):
+        """Per step from pinned host memory: the Q query rows and the lengths;
+        the Q outputs go back."""
+        import torch
+        q_h = self.qv.cpu().pin_memory()
+        lens_h = self.case.seq_lens.cpu().pin_memory()
+        out_h = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        q_d = torch.empty_like(self.qv)
+        lens_d = torch.empty_like(self.case.seq_lens)
+
+        def run():
+            q_d.copy_(q_h, non_blocking=True)
+            lens_d.copy_(lens_h, non_blocking=True)
+            self.encode()
+            self.decode(q_d, lens_d)
+            out_h.copy_(self.out, non_blocking=True)
+        return run, q_h.numel() * q_h.element_size() + lens_h.numel() * 4, out_h.numel() * 4
+
+
 class LatentHarness:
     """The MLA workload: latent cache, the step's commit, MLA decode."""
 
@@ -465,7 +571,12 @@ def run_kvarn(args):
     wl = W.WORKLOADS[args.workload]
     if args.num_seqs:
         wl = wl.with_(num_seqs=args.num_seqs)
-    H = (LatentHarness if wl.rope_dim else DenseHarness)(kv, W, wl, dev, rank)
+    if args.queries > 1:
+        if wl.rope_dim:
+            raise SystemExit("--queries applies to the dense workloads")
+        H = VerifyHarness(kv, W, wl, dev, rank, args.queries)
+    else:
+        H = (LatentHarness if wl.rope_dim else DenseHarness)(kv, W, wl, dev, rank)
     stream = torch.cuda.current_stream()
     B = wl.num_seqs
 
@@ -586,7 +697,7 @@ def run_kvarn(args):
     cpu = None
     if world == 1 and not args.no_cpu:
         n = max(4, min(16, os.cpu_count() or 4))
-        work, frac = oracle_work(wl, H.case, n)
+        work, frac = oracle_work(wl, H.case, n, args.queries, getattr(H, "qv", None))
         pool, cores = oracle_pool(len(work))
         with pool:
             wall = oracle_time(pool, cores, work)
@@ -594,7 +705,7 @@ def run_kvarn(args):
         cpu = {"value": round(frac * H.packed / wall / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{len(work)} {unit} units of one step ({frac:.4f} of it): commit and decode, "
                          f"float64 oracle on {cores} single-threaded host processes",
-               "decode_tokens_per_s": round(frac * B / wall, 4)}
+               "decode_tokens_per_s": round(frac * B * args.queries / wall, 4)}
 
     kernel_desc = "decode call (split kernel + merge kernel), CUDA events on its stream"
     if wl.rope_dim:
@@ -619,11 +730,13 @@ def run_kvarn(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (codes u4/u2; fp16 hi/lo mma operands)", "data": "synthetic",
         "config": {"workload": _workload_desc(wl),
-                   "step": ("encode the 4096-token prefill chunk, then decode 1 token per seq" if wl.encode_chunk
+                   "step": (f"commit one accepted tile per (seq, KV head), then verify {args.queries} tokens "
+                            f"per seq (kvarn_decode_verify)" if args.queries > 1 else
+                            "encode the 4096-token prefill chunk, then decode 1 token per seq" if wl.encode_chunk
                             else "commit one tile per (seq, KV head), then decode 1 token per seq"),
                    "l2": f"inputs larger than L2 ({H.packed / 1e6:.0f} MB of packed KV read per step)",
                    "parallelism": f"dp{world} (independent batches per GPU)"},
-        "decode_tokens_per_s": round(world * B / (ms_step * 1e-3), 1),
+        "decode_tokens_per_s": round(world * B * args.queries / (ms_step * 1e-3), 1),
         "decode_gbs": round(dec_gbs, 2), "decode_ms": round(dec_ms, 5),
         "commit_ms": round(enc_ms, 5), "commit_tokens": H.encode_tokens,
         "encode_tokens_per_s": round(encode_tok_s, 1), "encode_full_context_ms": round(enc_full_ms, 4),
@@ -688,6 +801,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=["toy", "dense32b", "g64", "hybrid", "mla"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling a small case)")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query tokens per sequence under speculative verification (dense workloads)")
     ap.add_argument("--only", choices=["decode", "encode"], default=None,
                     help="run only warm-up + timed launches of one call, print nothing (for ncu)")
     args = ap.parse_args()
