@@ -106,7 +106,7 @@ typedef enum {
 
 /* Bits of the device error word. */
 #define KVARN_DEVERR_PAGE_RANGE 0x1u  /* block-table entry outside [0, num_pages) */
-#define KVARN_DEVERR_NO_TAIL    0x2u  /* seq_len % N > 0 but no tail buffer */
+#define KVARN_DEVERR_NO_TAIL    0x2u  /* a raw record (tail or sink) is needed but its buffer is NULL */
 #define KVARN_DEVERR_TIMEOUT    0x4u  /* a bulk copy did not complete in time */
 #define KVARN_DEVERR_SEQ_LEN    0x8u  /* seq_len < 0 or above max_seq_len */
 
@@ -222,7 +222,7 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
  *   num_queries    1 .. KVARN_MAX_VERIFY_QUERIES
  *   tail_k/v       device, kv_dtype [num_seqs][Hkv][tail_capacity][D], or
  *                  NULL when no query sees a token past C
- *   tail_capacity  rows per (sequence, KV head), >= N + Q - 2, <= 4096
+ *   tail_capacity  rows per (sequence, KV head), >= N + Q - 2
  *   out            device fp32 [num_seqs][Q][num_q_heads][D]
  *   lse            device fp32 [num_seqs][Q][num_q_heads] or NULL
  *   workspace      device, >= kvarn_decode_verify_workspace_bytes(...)
@@ -243,6 +243,39 @@ int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_quer
                             const void* tail_k, const void* tail_v, int32_t tail_capacity,
                             int32_t num_seqs, float* out, float* lse, void* workspace,
                             int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream);
+
+/*
+ * kvarn_decode_window - kvarn_decode_verify with raw sink and recent records
+ * (gmlx page, "The two schemes": the first tokens and the newest tokens of a
+ * sequence stay fp16 while the records between them are quantised).
+ *
+ * Sequence b of L = seq_lens[b] tokens, the last Q = num_queries under
+ * verification (Q = 1: plain decode): tokens [0, min(S, L)), S =
+ * sink_tokens, are rows of the raw sink buffer; the whole tiles [S, C),
+ * C = max(S, floor((L - Q + 1 - R) / N) * N), R = recent_tokens, are read
+ * from the pages (logical tile t holds tokens [tN, tN + N); tiles below
+ * S / N are never read); tokens [C, L) are rows 0.. of the raw tail buffer
+ * (at most R + N + Q - 2 of them). Query token j sees [0, L - Q + 1 + j).
+ * With S = R = 0 this is kvarn_decode_verify.
+ *
+ *   sink_tokens    a multiple of N (0: no sink)
+ *   sink_k/v       device, kv_dtype [num_seqs][Hkv][sink_tokens][D], or NULL
+ *                  when sink_tokens = 0
+ *   recent_tokens  >= 0
+ *   tail_capacity  rows per (sequence, KV head) of tail_k/v, >= R + N + Q - 2
+ *   workspace      >= kvarn_decode_verify_workspace_bytes(...) with the same
+ *                  num_seqs, num_q_heads, num_queries and max_seq_len
+ * Other arguments as for kvarn_decode_verify. A missing sink or tail buffer
+ * that a row needs sets KVARN_DEVERR_NO_TAIL.
+ */
+int32_t kvarn_decode_window(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
+                            const void* cache, const kvarn_layout* layout, const int32_t* block_table,
+                            int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                            int32_t sink_tokens, const void* sink_k, const void* sink_v,
+                            int32_t recent_tokens, const void* tail_k, const void* tail_v,
+                            int32_t tail_capacity, int32_t num_seqs, float* out, float* lse,
+                            void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                            kvarn_stream_t stream);
 
 /*
  * kvarn_fp16_page_bytes / kvarn_store_fp16 / kvarn_decode_fp16 - the same

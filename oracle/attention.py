@@ -146,6 +146,66 @@ def decode_verify(q, cache, lay: layout.DenseLayout, block_table, seq_lens, sm_s
     return out, lse
 
 
+def window_committed(L: int, Q: int, N: int, sink: int, recent: int) -> int:
+    """End of the compressed tiles under the raw-record policy of the gmlx
+    page ("The two schemes": the first tokens and the newest tokens stay
+    fp16): tiles start after the `sink` raw tokens and end before the newest
+    `recent` accepted tokens, in whole tiles; never before the sink."""
+    return max(sink, (max(0, L - Q + 1 - recent) // N) * N)
+
+
+def decode_window(q, cache, lay: layout.DenseLayout, block_table, seq_lens, sm_scale, sink, recent,
+                  sink_k=None, sink_v=None, tail_k=None, tail_v=None, rows=None):
+    """Verification decode (decode_verify) with raw sink and recent records.
+
+    Sequence b of L tokens, the last Q under verification: tokens
+    [0, min(sink, L)) are rows of the raw sink buffer, the whole tiles
+    [sink, C), C = window_committed(L, Q, N, sink, recent), come from the
+    pages (logical tile t holds tokens [tN, tN + N)), and tokens [C, L) are
+    rows 0.. of the raw tail buffer. Query token j sees [0, L - Q + 1 + j).
+
+    sink_k/v [B, Hkv, sink, D]; tail_k/v [B, Hkv, capacity, D]. Returns
+    (out [B, Q, Hq, D], lse [B, Q, Hq]).
+    """
+    q = np.asarray(q, np.float64)
+    B, Q, Hq, D = q.shape
+    Hkv = cache.shape[1]
+    G = Hq // Hkv
+    N = lay.N
+    ppt = N // layout.P
+    out = np.full((B, Q, Hq, D), np.nan)
+    lse = np.full((B, Q, Hq), np.nan)
+    todo = rows if rows is not None else [(b, j, h) for b in range(B) for j in range(Q) for h in range(Hq)]
+    kv_cache = {}
+    for b, j, h in todo:
+        L = int(seq_lens[b])
+        kvh = h // G
+        key = (b, kvh)
+        if key not in kv_cache:
+            C = window_committed(L, Q, N, sink, recent)
+            Ks, Vs = [], []
+            if min(sink, L):
+                Ks.append(np.asarray(sink_k[b, kvh], np.float64)[:min(sink, L)])
+                Vs.append(np.asarray(sink_v[b, kvh], np.float64)[:min(sink, L)])
+            for t in range(sink // N, C // N):
+                pages = [int(block_table[b][t * ppt + p]) for p in range(ppt)]
+                ek, ev = layout.read_tile(cache, lay, pages, kvh)
+                Ks.append(codec.dequantize(ek["codes"], ek["a"], ek["b"], ek["c"]))
+                Vs.append(codec.dequantize(ev["codes"], ev["a"], ev["b"], ev["c"]))
+            if L > C:
+                Ks.append(np.asarray(tail_k[b, kvh], np.float64)[:L - C])
+                Vs.append(np.asarray(tail_v[b, kvh], np.float64)[:L - C])
+            kv_cache[key] = (np.concatenate(Ks) if Ks else np.zeros((0, D)),
+                             np.concatenate(Vs) if Vs else np.zeros((0, D)))
+        K, V = kv_cache[key]
+        vis = verify_visible(L, Q, j)
+        if vis == 0:
+            out[b, j, h], lse[b, j, h] = 0.0, -np.inf
+            continue
+        out[b, j, h], lse[b, j, h] = softmax_attention(q[b, j, h], K[:vis], V[:vis], sm_scale)
+    return out, lse
+
+
 def encode_into_cache(cache, lay: layout.DenseLayout, k, v, block_table, tile_start,
                       bits=(4, 2), T=2):
     """Encode every full tile of a chunk and store it.

@@ -62,6 +62,8 @@ _SIGS = {
     "kvarn_decode_verify_workspace_bytes": ([_LP, _I32, _I32, _I32, _I32], _I64),
     "kvarn_decode_verify": ([_P, _I32, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P,
                              _P, _I64, _P, _P], _I32),
+    "kvarn_decode_window": ([_P, _I32, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _I32, _P, _P, _I32, _P, _P,
+                             _I32, _I32, _P, _P, _P, _I64, _P, _P], _I32),
     "kvarn_fp16_page_bytes": ([_LP], _I64),
     "kvarn_store_fp16": ([_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _I32, _LP, _P, _P, _P], _I32),
     "kvarn_decode_fp16": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _I32, _P, _P, _P, _I64, _P,
@@ -194,6 +196,22 @@ def decode_verify(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, 
                                      _ptr(tail_k), _ptr(tail_v), max(cap, 1), B, _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
                                      _stream(stream)), "decode_verify")
+
+
+def decode_window(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, workspace, err,
+                  sm_scale, sink_k=None, sink_v=None, recent_tokens=0, tail_k=None, tail_v=None, lse=None,
+                  stream=None):
+    """q: [B, Q, Hq, D]; sink_k/v: [B, Hkv, S, D] (S a multiple of N) or None;
+    tail_k/v: [B, Hkv, capacity, D]; out: [B, Q, Hq, D]."""
+    B, Q, Hq, _ = q.shape
+    S = sink_k.shape[2] if sink_k is not None else 0
+    cap = tail_k.shape[2] if tail_k is not None else recent_tokens + layout.tile_tokens + Q - 2
+    _check(lib().kvarn_decode_window(_ptr(q), Hq, Q, sm_scale, _ptr(cache), ctypes.byref(layout),
+                                     _ptr(block_table), block_table.stride(0), _ptr(seq_lens), max_seq_len, S,
+                                     _ptr(sink_k), _ptr(sink_v), recent_tokens, _ptr(tail_k), _ptr(tail_v),
+                                     max(cap, 1), B, _ptr(out), _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
+           "decode_window")
 
 
 def alloc_fp16_cache(layout: Layout, device=None) -> torch.Tensor:

@@ -152,8 +152,10 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
                                    const void* cache, const kvarn_layout* L, const int32_t* block_table,
                                    int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
                                    const void* tail_k, const void* tail_v, int32_t tail_cap,
-                                   int32_t num_seqs, float* out, float* lse, void* workspace,
-                                   int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
+                                   int32_t sink_tokens, const void* sink_k, const void* sink_v,
+                                   int32_t recent_tokens, int32_t num_seqs, float* out, float* lse,
+                                   void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                                   kvarn_stream_t stream) {
   int32_t s = check_dense(L);
   if (s != KVARN_OK) return s;
   s = check_decode_common(L, num_q_heads, block_table, bt_stride, seq_lens, max_seq_len, num_seqs,
@@ -161,12 +163,16 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   if (s != KVARN_OK || num_seqs == 0) return s;
   if (!q || !cache) return KVARN_EINVAL;
   if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
-  // committed tiles: those filled by the accepted tokens [0, len - Q + 1)
+  // committed tiles: those filled by the accepted tokens [0, len - Q + 1),
+  // less the newest recent_tokens, never before the sink
   const int32_t accepted = std::max(0, max_seq_len - num_queries + 1);
-  const int32_t committed_pages = (accepted / L->tile_tokens) * (L->tile_tokens / kPageTokens);
+  const int32_t end = std::max(sink_tokens, (std::max(0, accepted - recent_tokens) / L->tile_tokens) *
+                                                L->tile_tokens);
+  const int32_t committed_pages = end > sink_tokens ? end / kPageTokens : 0;
   if (bt_stride < committed_pages) return KVARN_EINVAL;
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
   if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
+  if ((sink_k && !aligned(sink_k, 16)) || (sink_v && !aligned(sink_v, 16))) return KVARN_EALIGN;
   const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries, accepted);
   if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads * num_queries, L->head_dim, plan))
     return KVARN_EWORKSPACE;
@@ -193,6 +199,10 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   p.bf16 = L->kv_dtype == 1;
   p.num_queries = num_queries;
   p.tail_cap = tail_cap;
+  p.sink_tokens = sink_tokens;
+  p.sink_k = sink_k;
+  p.sink_v = sink_v;
+  p.recent_tokens = recent_tokens;
   return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -204,8 +214,8 @@ int32_t kvarn_decode(const void* q, int32_t num_q_heads, float sm_scale, const v
                      kvarn_stream_t stream) {
   if (!L) return KVARN_EINVAL;
   return decode_dense_common(q, num_q_heads, 1, sm_scale, cache, L, block_table, bt_stride, seq_lens,
-                             max_seq_len, tail_k, tail_v, L->tile_tokens, num_seqs, out, lse, workspace,
-                             workspace_bytes, error_flags, stream);
+                             max_seq_len, tail_k, tail_v, L->tile_tokens, 0, nullptr, nullptr, 0, num_seqs,
+                             out, lse, workspace, workspace_bytes, error_flags, stream);
 }
 
 int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
@@ -216,11 +226,31 @@ int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_quer
                             int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
   if (!L) return KVARN_EINVAL;
   if (num_queries < 1 || num_queries > KVARN_MAX_VERIFY_QUERIES) return KVARN_EUNSUPPORTED;
-  if (tail_capacity < L->tile_tokens + num_queries - 2 || tail_capacity < 1 || tail_capacity > 4096)
+  if (tail_capacity < L->tile_tokens + num_queries - 2 || tail_capacity < 1) return KVARN_EINVAL;
+  return decode_dense_common(q, num_q_heads, num_queries, sm_scale, cache, L, block_table, bt_stride,
+                             seq_lens, max_seq_len, tail_k, tail_v, tail_capacity, 0, nullptr, nullptr, 0,
+                             num_seqs, out, lse, workspace, workspace_bytes, error_flags, stream);
+}
+
+int32_t kvarn_decode_window(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
+                            const void* cache, const kvarn_layout* L, const int32_t* block_table,
+                            int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,
+                            int32_t sink_tokens, const void* sink_k, const void* sink_v,
+                            int32_t recent_tokens, const void* tail_k, const void* tail_v,
+                            int32_t tail_capacity, int32_t num_seqs, float* out, float* lse,
+                            void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                            kvarn_stream_t stream) {
+  if (!L) return KVARN_EINVAL;
+  if (num_queries < 1 || num_queries > KVARN_MAX_VERIFY_QUERIES) return KVARN_EUNSUPPORTED;
+  if (L->tile_tokens < 1 || sink_tokens < 0 || sink_tokens % L->tile_tokens || recent_tokens < 0)
+    return KVARN_EINVAL;
+  if (tail_capacity < 1 || static_cast<int64_t>(tail_capacity) <
+                               static_cast<int64_t>(recent_tokens) + L->tile_tokens + num_queries - 2)
     return KVARN_EINVAL;
   return decode_dense_common(q, num_q_heads, num_queries, sm_scale, cache, L, block_table, bt_stride,
-                             seq_lens, max_seq_len, tail_k, tail_v, tail_capacity, num_seqs, out, lse,
-                             workspace, workspace_bytes, error_flags, stream);
+                             seq_lens, max_seq_len, tail_k, tail_v, tail_capacity, sink_tokens, sink_k,
+                             sink_v, recent_tokens, num_seqs, out, lse, workspace, workspace_bytes,
+                             error_flags, stream);
 }
 
 int64_t kvarn_fp16_page_bytes(const kvarn_layout* L) {

@@ -75,8 +75,12 @@ struct DecArgs {
   float kappa;    // sm_scale * log2(e)
   const uint8_t* cache;
   int32_t Hq, Hkv, G;
-  int32_t Q;         // query tokens per sequence (speculative verify: the last Q tokens)
-  int32_t tail_cap;  // tail rows per (sequence, KV head)
+  int32_t Q;           // query tokens per sequence (speculative verify: the last Q tokens)
+  int32_t tail_cap;    // tail rows per (sequence, KV head)
+  int32_t sink_tiles;  // raw sink records: tokens [0, sink_tiles N) are rows of sink_k / sink_v
+  int32_t recent;      // raw recent records: the newest `recent` accepted tokens stay in the tail
+  const void* sink_k;
+  const void* sink_v;
   int64_t num_pages;
   const int32_t* bt;
   int32_t bt_stride;
@@ -130,19 +134,46 @@ __device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j,
 // the Q tokens under verification), and the committed prefix shared by all.
 __device__ __forceinline__ int visible_len(int len, int Q, int j) { return max(0, len - Q + 1 + j); }
 
-// Raw tail over tokens [committed, visible): dense attention in the original
-// basis, one warp per row, one pass with a running maximum (no per-token
-// buffer, so the tail length is bounded only by its buffer).
+// Raw records of a row: the sink rows [0, min(sink, visible)) and the tail rows
+// for tokens [committed, visible); dense attention in the original basis, one
+// warp per row, one pass with a running maximum (no per-token buffer, so the
+// record lengths are bounded only by their buffers).
+template <int D, typename T>
+__device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count, const float* qv, float& mx,
+                                            float& l, float* acc) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  for (int tau = 0; tau < count; ++tau) {
+    float kv[E], vv[E];
+    load_vec<T, E>(kp + static_cast<int64_t>(tau) * D + lane * E, kv);
+    load_vec<T, E>(vp + static_cast<int64_t>(tau) * D + lane * E, vv);
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
+    dot = warp_sum_xor(dot, 1, 32);  // identical in every lane
+    const float mn = fmaxf(mx, dot);
+    const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
+    l = fmaf(l, sc, p);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], sc, p * vv[e]);
+    mx = mn;
+  }
+}
+
 template <int D, int N, typename T, int W>
-__device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int committed) {
+__device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int sink,
+                              int committed) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int r = warp; r < R.n; r += W) {
     const int j = R.query(A, r), hq = kvh * A.G + R.head(A, r);
-    const int tail = visible_len(len, A.Q, j) - committed;
+    const int vis = visible_len(len, A.Q, j);
+    const int n_sink = min(sink, vis), n_tail = vis - committed;
     float* part = part_of(A, D, b, j, hq, A.nsplit);
-    if (tail <= 0 || A.tail_k == nullptr || A.tail_v == nullptr) {
-      if (tail > 0 && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
+    const bool miss = (n_tail > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
+                      (n_sink > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
+    if ((n_tail <= 0 && n_sink <= 0) || miss) {
+      if (miss && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
       write_empty(part, D, lane);
       continue;
     }
@@ -150,26 +181,18 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
     load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, qv);
 #pragma unroll
     for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
-    const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
-    const T* tk = static_cast<const T*>(A.tail_k);
-    const T* tv = static_cast<const T*>(A.tail_v);
     float mx = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int tau = 0; tau < tail; ++tau) {
-      float kv[E], vv[E];
-      load_vec<T, E>(tk + (row0 + tau) * D + lane * E, kv);
-      load_vec<T, E>(tv + (row0 + tau) * D + lane * E, vv);
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
-      dot = warp_sum_xor(dot, 1, 32);  // identical in every lane
-      const float mn = fmaxf(mx, dot);
-      const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
-      l = fmaf(l, sc, p);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], sc, p * vv[e]);
-      mx = mn;
+    if (n_sink > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
+      raw_segment<D, T>(static_cast<const T*>(A.sink_k) + row0 * D, static_cast<const T*>(A.sink_v) + row0 * D,
+                        n_sink, qv, mx, l, acc);
+    }
+    if (n_tail > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
+      raw_segment<D, T>(static_cast<const T*>(A.tail_k) + row0 * D, static_cast<const T*>(A.tail_v) + row0 * D,
+                        n_tail, qv, mx, l, acc);
     }
     if (lane == 0) {
       part[0] = mx;
@@ -197,15 +220,19 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
     len = len < 0 ? 0 : A.max_seq_len;
   }
-  // only tokens up to the first query token are accepted, so only the tiles
-  // they fill are committed (read from the compressed pages)
-  const int ntiles = visible_len(len, A.Q, 0) / N;
+  // Only tokens up to the first query token are accepted, so only the tiles
+  // they fill can be committed; of those, the raw sink records come first and
+  // the newest `recent` accepted tokens stay raw. Compressed: tiles
+  // [sink_tiles, end).
+  const int sink = A.sink_tiles * N;
+  const int committed = max(sink, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
+  const int end = committed / N;
 
   if (split == A.nsplit) {
-    tail_partials<D, N, T, W>(A, b, kvh, R, len, ntiles * N);
+    tail_partials<D, N, T, W>(A, b, kvh, R, len, sink, committed);
     return;
   }
-  const int t0 = split * A.tps, t1 = min(t0 + A.tps, ntiles);
+  const int t0 = A.sink_tiles + split * A.tps, t1 = min(t0 + A.tps, end);
   if (t0 >= t1) {
     for (int r = warp; r < R.n; r += W)
       write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), split), D, lane);
@@ -590,6 +617,10 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   A.G = p.num_q_heads / p.num_kv_heads;
   A.Q = p.num_queries > 0 ? p.num_queries : 1;
   A.tail_cap = p.tail_cap > 0 ? p.tail_cap : p.N;
+  A.sink_tiles = p.sink_tokens / p.N;
+  A.recent = p.recent_tokens;
+  A.sink_k = p.sink_k;
+  A.sink_v = p.sink_v;
   A.num_pages = p.num_pages;
   A.bt = p.block_table;
   A.bt_stride = p.bt_stride;

@@ -59,6 +59,10 @@ struct DecodeParams {
   bool bf16;
   int32_t num_queries;  // dense: query tokens per sequence (0 or 1: plain decode)
   int32_t tail_cap;     // dense: tail rows per (sequence, KV head) (0: N)
+  int32_t sink_tokens;  // dense: raw sink records (a multiple of N; 0: none)
+  int32_t recent_tokens;  // dense: newest accepted tokens kept raw (0: none)
+  const void* sink_k;   // dense: [B][Hkv][sink_tokens][D]
+  const void* sink_v;
 };
 
 // (query head, query token) row groups of eight per KV head.

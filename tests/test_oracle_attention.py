@@ -287,3 +287,84 @@ def test_verify_queries_before_the_first_token_see_nothing():
     out, lse = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
     assert (out[0, :2] == 0).all() and np.isneginf(lse[0, :2]).all()
     assert np.isfinite(lse[0, 2:]).all()
+
+
+# ------------------------------------------------------- sink + recent records
+def test_window_commit_points_by_hand():
+    """(L, Q, N, sink, recent) -> end of the compressed tiles, worked by hand:
+    accepted = L - Q + 1; whole tiles of [0, accepted - recent); not before
+    the sink."""
+    cases = [((1000, 1, 128, 128, 256), 640),   # 744 -> 5 tiles
+             ((300, 1, 128, 128, 256), 128),    # 44 -> 0 tiles, clamped to the sink
+             ((100, 1, 128, 128, 256), 128),    # shorter than the sink
+             ((2050, 4, 64, 128, 1024), 960),   # 2047 - 1024 = 1023 -> 15 whole tiles of 64
+             ((1151, 1, 128, 0, 1024), 0),      # 127 -> 0
+             ((1152, 1, 128, 0, 1024), 128),    # 128 -> 1 tile
+             ((1154, 3, 128, 0, 1024), 128)]    # accepted 1152 -> 128 -> 1 tile
+    for args, want in cases:
+        assert attention.window_committed(*args) == want, (args, want)
+
+
+def test_window_without_records_is_verify():
+    c = _verify_case([200, 64, 130], Q=2)
+    a, la = attention.decode_verify(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, c["tk"], c["tv"])
+    b, lb = attention.decode_window(c["q"], c["cache"], c["lay"], c["bt"], c["lens"], 0.1, 0, 0,
+                                    tail_k=c["tk"], tail_v=c["tv"])
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
+
+
+def test_window_all_raw_is_causal_softmax():
+    """L - Q + 1 <= sink + recent: every token is raw (sink rows, then tail
+    rows from the sink's end); scipy softmax over the causally visible ones."""
+    rng = np.random.default_rng(11)
+    N, S, R, Q, D, L = 64, 64, 100, 2, 128, 150
+    lay = layout.DenseLayout(D, N)
+    k, v = rng.standard_normal((L, D)), rng.standard_normal((L, D))
+    k[:, 3] *= 30  # an outlier channel stays exact in the raw records
+    q = rng.standard_normal((1, Q, 2, D))
+    assert attention.window_committed(L, Q, N, S, R) == S
+    sk, sv = k[None, None, :S], v[None, None, :S]
+    cap = R + N + Q - 2
+    tk = np.zeros((1, 1, cap, D)); tv = np.zeros((1, 1, cap, D))
+    tk[0, 0, :L - S], tv[0, 0, :L - S] = k[S:], v[S:]
+    cache = np.zeros((1, 1, lay.page_bytes), np.uint8)
+    out, lse = attention.decode_window(q, cache, lay, np.zeros((1, 8), int), np.array([L]), 0.09, S, R,
+                                       sk, sv, tk, tv)
+    for j in range(Q):
+        for h in range(2):
+            vis = L - Q + 1 + j
+            s = 0.09 * k[:vis] @ q[0, j, h]
+            np.testing.assert_allclose(out[0, j, h], scipy.special.softmax(s) @ v[:vis], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(lse[0, j, h], scipy.special.logsumexp(s), rtol=1e-12)
+
+
+def test_window_reads_the_sink_raw_and_the_middle_from_pages():
+    """Sink of one tile, one compressed tile, a raw tail: the output moves
+    with a change to the raw sink row and not with a change to the tokens of
+    the sink tile in the pages' source (they are never read)."""
+    rng = np.random.default_rng(12)
+    N, S, R, Q, D = 64, 64, 70, 1, 128
+    L = 200  # accepted 200 - 70 = 130 -> 2 tiles -> C = 128: tile 1 compressed, tail [128, 200)
+    lay = layout.DenseLayout(D, N)
+    assert attention.window_committed(L, Q, N, S, R) == 128
+    k, v = rng.standard_normal((L, D)), rng.standard_normal((L, D))
+    q = rng.standard_normal((1, Q, 2, D))
+    bt = np.arange(8)[None, :]
+    cache = np.zeros((8, 1, lay.page_bytes), np.uint8)
+    attention.encode_into_cache(cache, lay, k[None, None, :2 * N], v[None, None, :2 * N], bt, [0])
+    sk, sv = k[None, None, :S].copy(), v[None, None, :S].copy()
+    tk = np.zeros((1, 1, R + N + Q - 2, D)); tv = np.zeros_like(tk)
+    tk[0, 0, :L - 128], tv[0, 0, :L - 128] = k[128:], v[128:]
+    a, _ = attention.decode_window(q, cache, lay, bt, np.array([L]), 0.1, S, R, sk, sv, tk, tv)
+    cache2 = cache.copy()
+    cache2[bt[0, :4]] = 0  # the pages of tile 0 are not read under a one-tile sink
+    b, _ = attention.decode_window(q, cache2, lay, bt, np.array([L]), 0.1, S, R, sk, sv, tk, tv)
+    np.testing.assert_array_equal(a, b)
+    sv2 = sv.copy(); sv2[0, 0, 5] += 4.0
+    c, _ = attention.decode_window(q, cache, lay, bt, np.array([L]), 0.1, S, R, sk, sv2, tk, tv)
+    assert np.abs(c - a).max() > 1e-4
+    cache3 = cache.copy()
+    cache3[bt[0, 4:8]] = 0  # the compressed tile 1 is read
+    d, _ = attention.decode_window(q, cache3, lay, bt, np.array([L]), 0.1, S, R, sk, sv, tk, tv)
+    assert np.abs(d - a).max() > 1e-4

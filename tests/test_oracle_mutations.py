@@ -37,6 +37,8 @@ PINS = [
     (ta.test_mla_decode_rope_and_shared_latent, {}),
     (ta.test_verify_without_committed_tiles_is_causal_softmax, {}),
     (ta.test_verify_keeps_a_tile_filled_by_drafts_raw, {}),
+    (ta.test_window_commit_points_by_hand, {}),
+    (ta.test_window_all_raw_is_causal_softmax, {}),
 ]
 
 
@@ -162,6 +164,10 @@ def _visible_off_by_one(orig):
     return lambda L, Q, j: max(0, L - Q + j)
 
 
+def _recent_ignored(orig):
+    return lambda L, Q, N, sink, recent: orig(L, Q, N, sink, 0)
+
+
 MUTATIONS = [
     ("hadamard without 1/sqrt(D)", codec, "hadamard", _hadamard_unscaled),
     ("hadamard with a wrong sign", codec, "hadamard", _hadamard_wrong_sign),
@@ -179,6 +185,7 @@ MUTATIONS = [
     ("tail read one token off", attention, "sequence_kv", _tail_off_by_one),
     ("verify commits tiles the drafts filled", attention, "verify_committed", _commit_from_full_length),
     ("verify query sees one token too few", attention, "verify_visible", _visible_off_by_one),
+    ("recent raw records ignored", attention, "window_committed", _recent_ignored),
 ]
 
 
