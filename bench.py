@@ -399,15 +399,16 @@ class DenseHarness:
 
 
 class VerifyHarness(DenseHarness):
-    """Dense workloads under speculative verification: the last Q tokens of
-    every sequence are under verification. A step commits one accepted tile
-    per (sequence, KV head) and runs one kvarn_decode_verify over Q query
-    tokens per sequence; only the tiles of accepted tokens are read from the
-    pages, the rest (up to N + Q - 2 tokens) from the raw tail."""
+    """Dense workloads under speculative verification and/or raw records: the
+    last Q tokens of every sequence are under verification, the first S
+    tokens and the newest R accepted tokens stay raw (S = R = 0: plain
+    commit rule). A step commits one compressed tile per (sequence, KV head)
+    and runs one kvarn_decode_window (kvarn_decode_verify when S = R = 0)
+    over Q query tokens per sequence."""
 
-    def __init__(self, kv, W, wl, dev, rank, Q):
+    def __init__(self, kv, W, wl, dev, rank, Q, S=0, R=0):
         import torch
-        self.kv, self.wl, self.dev, self.Q = kv, wl, dev, Q
+        self.kv, self.wl, self.dev, self.Q, self.S, self.R = kv, wl, dev, Q, S, R
         self.case = case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
         B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
@@ -416,22 +417,27 @@ class VerifyHarness(DenseHarness):
         self.err = kv.new_error_word(dev)
         lens = case.seq_lens.cpu().tolist()
         self.lens, self.Lmax = lens, max(lens)
-        committed = [(max(0, L - Q + 1) // N) * N for L in lens]
-        z1 = torch.zeros(1, dtype=torch.int32, device=dev)
+        committed = [max(S, (max(0, L - Q + 1 - R) // N) * N) for L in lens]
         ts, src_k, src_v = [], [], []
         for b, C in enumerate(committed):
             T = C // N
-            if T > 1:
-                kv.encode_tiles(case.k[b:b + 1], case.v[b:b + 1], self.lay, z1, case.block_table[b:b + 1],
-                                self.cache, self.err, chunk_tokens=(T - 1) * N)
-            ts.append(T - 1 if T else -1)
+            T0 = S // N  # first compressed tile
+            if T - 1 > T0:
+                kv.encode_tiles(case.k[b:b + 1, :, S:], case.v[b:b + 1, :, S:], self.lay,
+                                torch.full((1,), T0, dtype=torch.int32, device=dev), case.block_table[b:b + 1],
+                                self.cache, self.err, chunk_tokens=(T - 1 - T0) * N)
+            ts.append(T - 1 if T > T0 else -1)
             c0 = max(T - 1, 0) * N
             src_k.append(case.k[b:b + 1, :, c0:c0 + N])
             src_v.append(case.v[b:b + 1, :, c0:c0 + N])
         self.commit = [(torch.cat(src_k).contiguous(), torch.cat(src_v).contiguous(),
                         torch.tensor(ts, dtype=torch.int32, device=dev), case.block_table, N)]
-        self.encode_tokens = sum(1 for C in committed if C) * N
-        cap = N + Q - 2
+        self.encode_tokens = sum(1 for C in committed if C > S) * N
+        cap = R + N + Q - 2
+        self.sink_k = self.sink_v = None
+        if S:
+            self.sink_k = case.k[:, :, :S].contiguous()
+            self.sink_v = case.v[:, :, :S].contiguous()
         self.tail_k = torch.zeros((B, Hkv, cap, D), dtype=case.k.dtype, device=dev)
         self.tail_v = torch.zeros_like(self.tail_k)
         for b, (L, C) in enumerate(zip(lens, committed)):
@@ -439,19 +445,24 @@ class VerifyHarness(DenseHarness):
             self.tail_v[b, :, :L - C] = case.v[b, :, C:L]
         self.qv = W.verify_queries(wl, Q, device=dev, seed=wl.seed + 7919 * rank)
         self.out = torch.empty((B, Q, wl.num_q_heads, D), dtype=torch.float32, device=dev)
-        self.ws = torch.empty(kv.decode_verify_workspace_bytes(self.lay, B, wl.num_q_heads, Q, self.Lmax),
+        self.ws = torch.empty(kv.decode_window_workspace_bytes(self.lay, B, wl.num_q_heads, Q, self.Lmax, S, R),
                               dtype=torch.uint8, device=dev)
         self.sm = W.default_sm_scale(wl)
         pb = kv.page_bytes(self.lay)
-        self.packed = sum(Hkv * (C * pb // 16 + (L - C) * D * 2 * 2) for L, C in zip(lens, committed))
+        self.packed = sum(Hkv * ((C - S) * pb // 16 + (min(S, L) + L - C) * D * 2 * 2)
+                          for L, C in zip(lens, committed))
         self.launches = 3
         self.tokens_per_step = B * Q
 
     def decode(self, q=None, lens=None):
         c = self.case
-        self.kv.decode_verify(self.qv if q is None else q, self.lay, self.cache, c.block_table,
-                              c.seq_lens if lens is None else lens, self.Lmax, self.out, self.ws, self.err,
-                              self.sm, self.tail_k, self.tail_v)
+        args = (self.qv if q is None else q, self.lay, self.cache, c.block_table,
+                c.seq_lens if lens is None else lens, self.Lmax, self.out, self.ws, self.err, self.sm)
+        if self.S or self.R:
+            self.kv.decode_window(*args, sink_k=self.sink_k, sink_v=self.sink_v, recent_tokens=self.R,
+                                  tail_k=self.tail_k, tail_v=self.tail_v)
+        else:
+            self.kv.decode_verify(*args, self.tail_k, self.tail_v)
 
     def full_encode(self):
         return DenseHarness.full_encode(self)
@@ -571,10 +582,10 @@ def run_kvarn(args):
     wl = W.WORKLOADS[args.workload]
     if args.num_seqs:
         wl = wl.with_(num_seqs=args.num_seqs)
-    if args.queries > 1:
+    if args.queries > 1 or args.sink or args.recent:
         if wl.rope_dim:
-            raise SystemExit("--queries applies to the dense workloads")
-        H = VerifyHarness(kv, W, wl, dev, rank, args.queries)
+            raise SystemExit("--queries, --sink and --recent apply to the dense workloads")
+        H = VerifyHarness(kv, W, wl, dev, rank, args.queries, args.sink, args.recent)
     else:
         H = (LatentHarness if wl.rope_dim else DenseHarness)(kv, W, wl, dev, rank)
     stream = torch.cuda.current_stream()
@@ -695,7 +706,7 @@ def run_kvarn(args):
         pass
 
     cpu = None
-    if world == 1 and not args.no_cpu:
+    if world == 1 and not args.no_cpu and not (args.sink or args.recent):
         n = max(4, min(16, os.cpu_count() or 4))
         work, frac = oracle_work(wl, H.case, n, args.queries, getattr(H, "qv", None))
         pool, cores = oracle_pool(len(work))
@@ -730,7 +741,10 @@ def run_kvarn(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (codes u4/u2; fp16 hi/lo mma operands)", "data": "synthetic",
         "config": {"workload": _workload_desc(wl),
-                   "step": (f"commit one accepted tile per (seq, KV head), then verify {args.queries} tokens "
+                   "step": (f"commit one compressed tile per (seq, KV head), then {args.queries} query token(s) "
+                            f"per seq, raw sink {args.sink} + recent {args.recent} (kvarn_decode_window)"
+                            if args.sink or args.recent else
+                            f"commit one accepted tile per (seq, KV head), then verify {args.queries} tokens "
                             f"per seq (kvarn_decode_verify)" if args.queries > 1 else
                             "encode the 4096-token prefill chunk, then decode 1 token per seq" if wl.encode_chunk
                             else "commit one tile per (seq, KV head), then decode 1 token per seq"),
@@ -803,6 +817,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling a small case)")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per sequence under speculative verification (dense workloads)")
+    ap.add_argument("--sink", type=int, default=0, help="raw sink tokens (a multiple of the tile)")
+    ap.add_argument("--recent", type=int, default=0, help="newest accepted tokens kept raw")
     ap.add_argument("--only", choices=["decode", "encode"], default=None,
                     help="run only warm-up + timed launches of one call, print nothing (for ncu)")
     args = ap.parse_args()

@@ -263,11 +263,18 @@ int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_quer
  *                  when sink_tokens = 0
  *   recent_tokens  >= 0
  *   tail_capacity  rows per (sequence, KV head) of tail_k/v, >= R + N + Q - 2
- *   workspace      >= kvarn_decode_verify_workspace_bytes(...) with the same
- *                  num_seqs, num_q_heads, num_queries and max_seq_len
+ *   workspace      >= kvarn_decode_window_workspace_bytes(...) with the same
+ *                  num_seqs, num_q_heads, num_queries, max_seq_len,
+ *                  sink_tokens and recent_tokens
  * Other arguments as for kvarn_decode_verify. A missing sink or tail buffer
- * that a row needs sets KVARN_DEVERR_NO_TAIL.
+ * that a row needs sets KVARN_DEVERR_NO_TAIL. The raw records are read in
+ * splits of 128 tokens, in parallel with the splits over the pages.
  */
+int64_t kvarn_decode_window_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t num_queries,
+                                            int32_t max_seq_len, int32_t sink_tokens,
+                                            int32_t recent_tokens);
+
 int32_t kvarn_decode_window(const void* q, int32_t num_q_heads, int32_t num_queries, float sm_scale,
                             const void* cache, const kvarn_layout* layout, const int32_t* block_table,
                             int32_t bt_stride, const int32_t* seq_lens, int32_t max_seq_len,

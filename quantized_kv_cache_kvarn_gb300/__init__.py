@@ -62,6 +62,7 @@ _SIGS = {
     "kvarn_decode_verify_workspace_bytes": ([_LP, _I32, _I32, _I32, _I32], _I64),
     "kvarn_decode_verify": ([_P, _I32, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P,
                              _P, _I64, _P, _P], _I32),
+    "kvarn_decode_window_workspace_bytes": ([_LP, _I32, _I32, _I32, _I32, _I32, _I32], _I64),
     "kvarn_decode_window": ([_P, _I32, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _I32, _P, _P, _I32, _P, _P,
                              _I32, _I32, _P, _P, _P, _I64, _P, _P], _I32),
     "kvarn_fp16_page_bytes": ([_LP], _I64),
@@ -196,6 +197,15 @@ def decode_verify(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, 
                                      _ptr(tail_k), _ptr(tail_v), max(cap, 1), B, _ptr(out), _ptr(lse),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
                                      _stream(stream)), "decode_verify")
+
+
+def decode_window_workspace_bytes(layout: Layout, num_seqs: int, num_q_heads: int, num_queries: int,
+                                  max_seq_len: int, sink_tokens: int, recent_tokens: int) -> int:
+    n = lib().kvarn_decode_window_workspace_bytes(ctypes.byref(layout), num_seqs, num_q_heads, num_queries,
+                                                  max_seq_len, sink_tokens, recent_tokens)
+    if n < 0:
+        raise ValueError("invalid arguments for kvarn_decode_window_workspace_bytes")
+    return n
 
 
 def decode_window(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, workspace, err,

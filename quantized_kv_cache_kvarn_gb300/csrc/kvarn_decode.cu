@@ -142,15 +142,50 @@ template <int D, typename T>
 __device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count, const float* qv, float& mx,
                                             float& l, float* acc) {
   constexpr int E = D / 32;
+  constexpr int U = D == 128 ? 8 : 4;  // tokens in flight per step
   const int lane = threadIdx.x & 31;
-  for (int tau = 0; tau < count; ++tau) {
+  int tau = 0;
+  for (; tau + U <= count; tau += U) {
+    float kv[U][E], vv[U][E], dot[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      load_vec<T, E>(kp + static_cast<int64_t>(tau + u) * D + lane * E, kv[u]);
+      load_vec<T, E>(vp + static_cast<int64_t>(tau + u) * D + lane * E, vv[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      dot[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot[u] = fmaf(qv[e], kv[u][e], dot[u]);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < U; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], o);  // same in every lane
+    float mn = mx;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mn = fmaxf(mn, dot[u]);
+    const float sc = exp2f(mx - mn);
+    l *= sc;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float p = exp2f(dot[u] - mn);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[u][e], acc[e]);
+    }
+    mx = mn;
+  }
+  for (; tau < count; ++tau) {
     float kv[E], vv[E];
     load_vec<T, E>(kp + static_cast<int64_t>(tau) * D + lane * E, kv);
     load_vec<T, E>(vp + static_cast<int64_t>(tau) * D + lane * E, vv);
     float dot = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
-    dot = warp_sum_xor(dot, 1, 32);  // identical in every lane
+    dot = warp_sum_xor(dot, 1, 32);
     const float mn = fmaxf(mx, dot);
     const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
     l = fmaf(l, sc, p);
@@ -160,19 +195,23 @@ __device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count,
   }
 }
 
+// Raw split `chunk` covers raw tokens [chunk * kRawChunk, +kRawChunk) of the
+// row's raw list: its sink rows, then its tail rows.
 template <int D, int N, typename T, int W>
 __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int sink,
-                              int committed) {
+                              int committed, int chunk) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int r = warp; r < R.n; r += W) {
     const int j = R.query(A, r), hq = kvh * A.G + R.head(A, r);
     const int vis = visible_len(len, A.Q, j);
-    const int n_sink = min(sink, vis), n_tail = vis - committed;
-    float* part = part_of(A, D, b, j, hq, A.nsplit);
-    const bool miss = (n_tail > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
-                      (n_sink > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
-    if ((n_tail <= 0 && n_sink <= 0) || miss) {
+    const int n_sink = min(sink, vis), n_tail = max(0, vis - committed);
+    const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
+    const int s_cnt = max(0, min(c1, n_sink) - c0), t0 = max(c0, n_sink) - n_sink, t_cnt = max(0, c1 - max(c0, n_sink));
+    float* part = part_of(A, D, b, j, hq, A.nsplit + chunk);
+    const bool miss = (t_cnt > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
+                      (s_cnt > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
+    if ((t_cnt <= 0 && s_cnt <= 0) || miss) {
       if (miss && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
       write_empty(part, D, lane);
       continue;
@@ -184,15 +223,15 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
     float mx = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    if (n_sink > 0) {
-      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
+    if (s_cnt > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N) + c0;
       raw_segment<D, T>(static_cast<const T*>(A.sink_k) + row0 * D, static_cast<const T*>(A.sink_v) + row0 * D,
-                        n_sink, qv, mx, l, acc);
+                        s_cnt, qv, mx, l, acc);
     }
-    if (n_tail > 0) {
-      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
+    if (t_cnt > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap + t0;
       raw_segment<D, T>(static_cast<const T*>(A.tail_k) + row0 * D, static_cast<const T*>(A.tail_v) + row0 * D,
-                        n_tail, qv, mx, l, acc);
+                        t_cnt, qv, mx, l, acc);
     }
     if (lane == 0) {
       part[0] = mx;
@@ -228,8 +267,8 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
   const int committed = max(sink, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
   const int end = committed / N;
 
-  if (split == A.nsplit) {
-    tail_partials<D, N, T, W>(A, b, kvh, R, len, sink, committed);
+  if (split >= A.nsplit) {
+    tail_partials<D, N, T, W>(A, b, kvh, R, len, sink, committed, split - A.nsplit);
     return;
   }
   const int t0 = A.sink_tiles + split * A.tps, t1 = min(t0 + A.tps, end);
@@ -556,6 +595,7 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
     p.tiles_per_split = (tiles + best - 1) / best;
     p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
   }
+  p.raw_splits = 1;
   p.slots = p.nsplit + 1;
   return p;
 }
@@ -601,7 +641,7 @@ static cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
   const int smem = S::SMEM + A.tps * S::PPT * 4;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(A.Hkv * row_groups(A.G, A.Q), A.nsplit + 1, num_seqs);
+  dim3 grid(A.Hkv * row_groups(A.G, A.Q), A.slots, num_seqs);
   kern<<<grid, W * 32, smem, st>>>(A);
   return cudaGetLastError();
 }

@@ -72,9 +72,19 @@ inline int32_t row_groups(int32_t G, int32_t Q) { return (G * Q + 7) / 8; }
 // tail partial). Depends only on the arguments and the device's SM count.
 struct SplitPlan {
   int32_t tiles_per_split;
-  int32_t nsplit;   // splits over committed tiles
-  int32_t slots;    // nsplit + 1 (tail)
+  int32_t nsplit;      // splits over committed tiles
+  int32_t raw_splits;  // splits over the raw records (chunks of kRawChunk tokens; at least 1)
+  int32_t slots;       // nsplit + raw_splits
 };
+
+constexpr int32_t kRawChunk = 128;  // raw (sink and tail) tokens per split
+
+// The plan with enough raw splits for up to raw_max raw tokens per row.
+inline SplitPlan with_raw_chunks(SplitPlan p, int32_t raw_max) {
+  p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
+  p.slots = p.nsplit + p.raw_splits;
+  return p;
+}
 
 SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
                      int32_t warps, int32_t ctas_per_sm);

@@ -78,7 +78,7 @@ def _run(wl, Q, S, R, lens, bt, cache, sink_k, sink_v, tail_k, tail_v, q, sm, wi
     Lmax = int(lens.max())
     out = torch.empty((B, Q, Hq, D), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty(kv.decode_verify_workspace_bytes(lay, B, Hq, Q, Lmax), dtype=torch.uint8, device=dev)
+    ws = torch.empty(kv.decode_window_workspace_bytes(lay, B, Hq, Q, Lmax, S, R), dtype=torch.uint8, device=dev)
     err = kv.new_error_word(dev)
     args = (q.to(dev), lay, torch.from_numpy(cache).to(dev), torch.from_numpy(bt).to(dev),
             torch.from_numpy(lens).to(dev), Lmax, out, ws, err, sm)
