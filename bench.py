@@ -312,7 +312,32 @@ class DenseHarness:
         self.packed = sum(Hkv * ((L // N) * N * pb // 16 + (L % N) * D * 2 * 2) for L in lens)
         self.launches = len(self.commit) + 2
 
+    def use_append(self):
+        """The step's commit as kvarn_append of each sequence's newest token
+        (position len - 1): it completes the last tile in uniform-length
+        workloads, which the same launch encodes; the raw tail holds the
+        tile's other tokens."""
+        import torch
+        c, N = self.case, self.wl.tile_tokens
+        B, Hkv, D = self.wl.num_seqs, self.wl.num_kv_heads, self.wl.head_dim
+        self.ap_tail_k = torch.zeros((B, Hkv, N, D), dtype=c.k.dtype, device=self.dev)
+        self.ap_tail_v = torch.zeros_like(self.ap_tail_k)
+        for b, L in enumerate(self.lens):
+            c0 = ((L - 1) // N) * N
+            self.ap_tail_k[b, :, :L - 1 - c0] = c.k[b, :, c0:L - 1]
+            self.ap_tail_v[b, :, :L - 1 - c0] = c.v[b, :, c0:L - 1]
+        pos = torch.tensor([L - 1 for L in self.lens], device=self.dev)
+        ar = torch.arange(B, device=self.dev)
+        self.ap_k = c.k[ar, :, pos].contiguous()
+        self.ap_v = c.v[ar, :, pos].contiguous()
+        self.appending = True
+        self.encode_tokens = sum(1 for L in self.lens if L % N == 0) * N
+
     def encode(self):
+        if getattr(self, "appending", False):
+            self.kv.append(self.ap_k, self.ap_v, self.case.seq_lens, self.Lmax, self.ap_tail_k, self.ap_tail_v,
+                           self.case.block_table, self.lay, self.cache, self.err)
+            return
         for k, v, ts, bt, C in self.commit:
             self.kv.encode_tiles(k, v, self.lay, ts, bt, self.cache, self.err, chunk_tokens=C)
 
@@ -588,6 +613,10 @@ def run_kvarn(args):
         H = VerifyHarness(kv, W, wl, dev, rank, args.queries, args.sink, args.recent)
     else:
         H = (LatentHarness if wl.rope_dim else DenseHarness)(kv, W, wl, dev, rank)
+    if args.append:
+        if wl.rope_dim or args.queries > 1 or args.sink or args.recent or wl.encode_chunk:
+            raise SystemExit("--append applies to the plain dense step")
+        H.use_append()
     stream = torch.cuda.current_stream()
     B = wl.num_seqs
 
@@ -746,6 +775,8 @@ def run_kvarn(args):
                             if args.sink or args.recent else
                             f"commit one accepted tile per (seq, KV head), then verify {args.queries} tokens "
                             f"per seq (kvarn_decode_verify)" if args.queries > 1 else
+                            "kvarn_append of the newest token (commits the tile it fills), then decode 1 token per seq"
+                            if args.append else
                             "encode the 4096-token prefill chunk, then decode 1 token per seq" if wl.encode_chunk
                             else "commit one tile per (seq, KV head), then decode 1 token per seq"),
                    "l2": f"inputs larger than L2 ({H.packed / 1e6:.0f} MB of packed KV read per step)",
@@ -817,6 +848,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling a small case)")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per sequence under speculative verification (dense workloads)")
+    ap.add_argument("--append", action="store_true",
+                    help="commit through kvarn_append of the newest token (fused append + commit)")
     ap.add_argument("--sink", type=int, default=0, help="raw sink tokens (a multiple of the tile)")
     ap.add_argument("--recent", type=int, default=0, help="newest accepted tokens kept raw")
     ap.add_argument("--only", choices=["decode", "encode"], default=None,

@@ -166,6 +166,32 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
                            kvarn_stream_t stream);
 
 /*
+ * kvarn_append - fused append and commit: one launch per decode step for the
+ * whole batch (turbo-attn page, "Compress-on-the-wire": the new token is
+ * encoded and written to the packed cache in one kernel; KVarN review,
+ * speculative-decoding paragraph: a tile is committed once it is full).
+ *
+ * For every sequence b with L = seq_lens[b] > 0, the token at position L - 1
+ * of every KV head is k / v [b][h]. If L is not a multiple of N, it is stored
+ * as row (L - 1) % N of the raw tail. If it is, it completes logical tile
+ * L/N - 1, whose other N - 1 tokens are rows 0..N-2 of the tail: the tile is
+ * rotated, normalised, quantised and written to its pages exactly as
+ * kvarn_encode_tiles would, and the tail holds no token afterwards. A
+ * sequence with L = 0 is skipped. The decision is taken on the device, so a
+ * captured CUDA graph of the step serves every length.
+ *
+ *   k, v         device, kv_dtype [num_seqs][Hkv][D]
+ *   seq_lens     device int32 [num_seqs], lengths including the new token,
+ *                each <= max_seq_len (else KVARN_DEVERR_SEQ_LEN, skipped)
+ *   tail_k/v     device, kv_dtype [num_seqs][Hkv][N][D] (read and written)
+ *   block_table, bt_stride, layout, cache, error_flags: as kvarn_encode_tiles
+ */
+int32_t kvarn_append(const void* k, const void* v, const int32_t* seq_lens, int32_t max_seq_len,
+                     void* tail_k, void* tail_v, int32_t num_seqs, const int32_t* block_table,
+                     int32_t bt_stride, const kvarn_layout* layout, void* cache, uint32_t* error_flags,
+                     kvarn_stream_t stream);
+
+/*
  * kvarn_decode_workspace_bytes - scratch needed by kvarn_decode (and by
  * kvarn_decode_fp16 and kvarn_decode_mla with the same arguments): the
  * split-K partials (running max, sum and unnormalised output per split).

@@ -56,6 +56,7 @@ _SIGS = {
     "kvarn_layout_check": ([_LP], _I32),
     "kvarn_page_bytes": ([_LP], _I64),
     "kvarn_encode_tiles": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P, _I32, _LP, _P, _P, _P], _I32),
+    "kvarn_append": ([_P, _P, _P, _I32, _P, _P, _I32, _P, _I32, _LP, _P, _P, _P], _I32),
     "kvarn_decode_workspace_bytes": ([_LP, _I32, _I32, _I32], _I64),
     "kvarn_decode": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _I64,
                       _P, _P], _I32),
@@ -166,6 +167,14 @@ def encode_tiles(k, v, layout: Layout, tile_start, block_table, cache, err, chun
     _check(lib().kvarn_encode_tiles(_ptr(k), _ptr(v), k.stride(0), k.stride(1), B, C, _ptr(tile_start),
                                     _ptr(block_table), block_table.stride(0), ctypes.byref(layout),
                                     _ptr(cache), _ptr(err), _stream(stream)), "encode_tiles")
+
+
+def append(k, v, seq_lens, max_seq_len, tail_k, tail_v, block_table, layout: Layout, cache, err, stream=None):
+    """k, v: [B, Hkv, D] newest tokens; tail_k/v: [B, Hkv, N, D]."""
+    assert k.is_contiguous() and v.is_contiguous() and tail_k.is_contiguous() and tail_v.is_contiguous()
+    _check(lib().kvarn_append(_ptr(k), _ptr(v), _ptr(seq_lens), max_seq_len, _ptr(tail_k), _ptr(tail_v),
+                              k.shape[0], _ptr(block_table), block_table.stride(0), ctypes.byref(layout),
+                              _ptr(cache), _ptr(err), _stream(stream)), "append")
 
 
 def decode(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, workspace, err,

@@ -124,6 +124,40 @@ static int32_t raw_bound(const kvarn_layout* L, int32_t max_seq_len, int32_t num
   return static_cast<int32_t>(std::min<int64_t>(std::max(0, max_seq_len), std::max<int64_t>(0, r)));
 }
 
+int32_t kvarn_append(const void* k, const void* v, const int32_t* seq_lens, int32_t max_seq_len,
+                     void* tail_k, void* tail_v, int32_t num_seqs, const int32_t* block_table,
+                     int32_t bt_stride, const kvarn_layout* L, void* cache, uint32_t* error_flags,
+                     kvarn_stream_t stream) {
+  int32_t s = check_dense(L);
+  if (s != KVARN_OK) return s;
+  if (num_seqs < 0 || max_seq_len < 0) return KVARN_EINVAL;
+  if (num_seqs == 0) return KVARN_OK;
+  if (!k || !v || !seq_lens || !tail_k || !tail_v || !block_table || !cache || !error_flags || bt_stride < 1)
+    return KVARN_EINVAL;
+  if (bt_stride < (max_seq_len / L->tile_tokens) * (L->tile_tokens / kPageTokens)) return KVARN_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(tail_k, 16) || !aligned(tail_v, 16)) return KVARN_EALIGN;
+  if (!aligned(cache, 128) || !aligned(error_flags, 4)) return KVARN_EALIGN;
+  AppendParams p{};
+  p.k = k;
+  p.v = v;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.tail_k = tail_k;
+  p.tail_v = tail_v;
+  p.num_seqs = num_seqs;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.cache = cache;
+  p.num_pages = L->num_pages;
+  p.num_kv_heads = L->num_kv_heads;
+  p.D = L->head_dim;
+  p.N = L->tile_tokens;
+  p.norm_iters = L->norm_iters;
+  p.bf16 = L->kv_dtype == 1;
+  p.err = error_flags;
+  return from_cuda(launch_append_commit(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
                                      int32_t max_seq_len) {
   if (kvarn_layout_check(L) != KVARN_OK || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0)

@@ -135,9 +135,14 @@ __device__ __forceinline__ uint32_t k_word_part(const uint32_t (&P)[4], int t, i
   return ((v | (v >> 4)) & 0x00FF00FFu) << (8 * s);
 }
 
+// Encodes rows [0, N) of `src` as logical tile `tile` of sequence b (u: the
+// tile's index in the chunk, for the latent rope rows). With last_row set,
+// row N - 1 comes from last_row instead of src (the newest token, appended
+// in the same launch).
 template <int D, int N, int CS, int BITS, int KIND, typename T>
 __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __restrict__ src,
-                                            int b, int head, int u, unsigned char* smem) {
+                                            int b, int head, int u, int64_t tile, const T* last_row,
+                                            unsigned char* smem) {
   using S = EncShape<D, N, CS>;
   constexpr bool IS_V = KIND == 0 && BITS == 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -170,7 +175,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
     const int r = crank * S::ROWS + local_row(i);
-    const T* p = src + static_cast<int64_t>(r) * D + seg * 16;
+    const T* p = (last_row != nullptr && r == N - 1) ? last_row + seg * 16 : src + static_cast<int64_t>(r) * D + seg * 16;
     load8<T>(p, x[i]);
     load8<T>(p + 8, x[i] + 8);
   }
@@ -178,7 +183,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   // ---- page addresses of this CTA's rows (read by the stores at the end)
   constexpr int PPT = N / kPageTokens;  // pages per tile
   if (tid < S::PPC) {
-    const int64_t lp = (static_cast<int64_t>(A.tile_start[b]) + u) * PPT + crank * S::PPC + tid;
+    const int64_t lp = tile * PPT + crank * S::PPC + tid;
     uint8_t* pg = nullptr;
     const int32_t phys =
         (lp >= 0 && lp < A.bt_stride) ? A.block_table[static_cast<int64_t>(b) * A.bt_stride + lp] : -1;
@@ -459,9 +464,11 @@ __global__ void __launch_bounds__(2 * D) encode_dense_kernel(EncodeArgs A) {
   const int64_t off = static_cast<int64_t>(b) * A.seq_stride + static_cast<int64_t>(head) * A.head_stride +
                       static_cast<int64_t>(u) * N * D;
   if (is_v)
-    encode_tile<D, N, 1, 2, 0, T>(A, static_cast<const T*>(A.x[1]) + off, b, head, u, smem);
+    encode_tile<D, N, 1, 2, 0, T>(A, static_cast<const T*>(A.x[1]) + off, b, head, u, A.tile_start[b] + u,
+                                  nullptr, smem);
   else
-    encode_tile<D, N, 1, 4, 0, T>(A, static_cast<const T*>(A.x[0]) + off, b, head, u, smem);
+    encode_tile<D, N, 1, 4, 0, T>(A, static_cast<const T*>(A.x[0]) + off, b, head, u, A.tile_start[b] + u,
+                                  nullptr, smem);
 }
 
 template <typename T>
@@ -472,7 +479,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
   if (A.tile_start[b] < 0) return;  // uniform over the cluster: both CTAs share b
   const T* src = static_cast<const T*>(A.x[0]) + static_cast<int64_t>(b) * A.seq_stride +
                  static_cast<int64_t>(u) * 128 * 512;
-  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, smem);
+  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, A.tile_start[b] + u, nullptr, smem);
+}
+
+// Fused append + commit (one launch per decode step): x[0] / x[1] hold each
+// (sequence, KV head)'s newest K / V token, at position seq_lens[b] - 1. A
+// token that does not complete a tile goes to its row of the raw tail; one
+// that does completes the tile in the tail's rows 0..N-2 and the tile is
+// encoded straight into its pages (the tail then holds nothing). The tail
+// rows read here were written by earlier launches.
+template <int D, int N, typename T>
+__global__ void __launch_bounds__(2 * D) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
+                                                              int32_t max_seq_len, T* tail_k, T* tail_v) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const bool is_v = blockIdx.z == 1;
+  const int head = blockIdx.x, b = blockIdx.y;
+  const int L = seq_lens[b];
+  if (L <= 0 || L > max_seq_len) {  // nothing appended (0) or an invalid length
+    if (L != 0 && threadIdx.x == 0 && !is_v && head == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    return;
+  }
+  const int64_t hs = static_cast<int64_t>(b) * A.num_kv_heads + head;
+  const T* tok = static_cast<const T*>(A.x[is_v]) + hs * D;
+  T* tail = (is_v ? tail_v : tail_k) + hs * N * D;
+  if (L % N != 0) {
+    const int row = (L - 1) % N;
+    for (int i = threadIdx.x; i < D / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(tail + static_cast<int64_t>(row) * D)[i] = reinterpret_cast<const uint4*>(tok)[i];
+    return;
+  }
+  if (is_v)
+    encode_tile<D, N, 1, 2, 0, T>(A, tail, b, head, 0, L / N - 1, tok, smem);
+  else
+    encode_tile<D, N, 1, 4, 0, T>(A, tail, b, head, 0, L / N - 1, tok, smem);
 }
 
 // ------------------------------------------------------------- launchers
@@ -509,6 +548,44 @@ cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st) {
   if (p.D == DD && p.N == NN)                                                            \
     return p.bf16 ? launch_dense<DD, NN, __nv_bfloat16>(A, st)               \
                   : launch_dense<DD, NN, __half>(A, st);
+  KV_DISPATCH(128, 128)
+  KV_DISPATCH(128, 64)
+  KV_DISPATCH(256, 128)
+  KV_DISPATCH(256, 64)
+#undef KV_DISPATCH
+  return cudaErrorInvalidValue;
+}
+
+template <int D, int N, typename T>
+static cudaError_t launch_append(const EncodeArgs& A, const AppendParams& p, cudaStream_t st) {
+  constexpr int smem = EncShape<D, N, 1>::SMEM;
+  auto kern = append_commit_kernel<D, N, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(A.num_kv_heads, p.num_seqs, 2);
+  kern<<<grid, 2 * D, smem, st>>>(A, p.seq_lens, p.max_seq_len, static_cast<T*>(p.tail_k),
+                                  static_cast<T*>(p.tail_v));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_commit(const AppendParams& p, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  EncodeArgs A{};
+  A.x[0] = p.k;
+  A.x[1] = p.v;
+  A.block_table = p.block_table;
+  A.bt_stride = p.bt_stride;
+  A.cache = static_cast<uint8_t*>(p.cache);
+  A.num_pages = p.num_pages;
+  A.num_kv_heads = p.num_kv_heads;
+  A.page_bytes = DensePage(p.D, p.N).bytes();
+  A.norm_iters = p.norm_iters;
+  A.err = p.err;
+  A.num_seqs = p.num_seqs;
+#define KV_DISPATCH(DD, NN)                                                              \
+  if (p.D == DD && p.N == NN)                                                            \
+    return p.bf16 ? launch_append<DD, NN, __nv_bfloat16>(A, p, st)                      \
+                  : launch_append<DD, NN, __half>(A, p, st);
   KV_DISPATCH(128, 128)
   KV_DISPATCH(128, 64)
   KV_DISPATCH(256, 128)

@@ -21,6 +21,24 @@ struct EncodeParams {
   uint32_t* err;
 };
 
+struct AppendParams {
+  const void* k;  // newest token per (sequence, KV head): [B][Hkv][D]
+  const void* v;
+  const int32_t* seq_lens;  // lengths including the newest token
+  int32_t max_seq_len;
+  void* tail_k;  // [B][Hkv][N][D]
+  void* tail_v;
+  int32_t num_seqs;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  void* cache;
+  int64_t num_pages;
+  int32_t num_kv_heads, D, N, norm_iters;
+  bool bf16;
+  uint32_t* err;
+};
+cudaError_t launch_append_commit(const AppendParams& p, cudaStream_t st);
+
 struct EncodeLatentParams {
   const void* latent;
   int64_t seq_stride;
