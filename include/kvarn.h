@@ -51,6 +51,23 @@
  *   Every code field of one tensor-core operand thus sits at one bit
  *   position of its 16-bit half, so masking it out yields an exact fp16
  *   subnormal operand (code times a power of two).
+ * Other widths (gmlx page, "The two schemes": kvarn widths 2, 3, 4, 5, 6, 8
+ * for keys and values): with head_dim 128 and fp16 scales, k_bits = v_bits =
+ * b in {2, 3, 4, 5, 6, 8} (and the preset's 4 and 2 with fp16 scales). A
+ * b-bit code is stored as planes, 2: [2], 3: [2, 1], 4: [4], 5: [4, 1],
+ * 6: [4, 2], 8: [4, 4] (code = plane0 + 2^w0 plane1), each plane region
+ * (2*D*w bytes per page, in order) placed by one rule for width w in
+ * {1, 2, 4} of which the K codes and V codes above are the w = 4 and w = 2
+ * cases: lane L = 4g + t owns words of 8/w fragments; fragment f has its
+ * first operand register at bits w*f, 16 + w*f and its second at 8 + w*f,
+ * 24 + w*f. K: fragment 2kc + e (tokens 8e + g), channel 16kc + 2t + e' + 8h
+ * at bit w*f + 8h + 16e'; words in units of U = min(4, D*w/64): word i of
+ * lane L at byte 4U(32(i/U) + L) + 4(i%U). V: fragment nc, channel 8nc + g of
+ * token 2t + e' + 8h at bit w*f + 8h + 16e'; words in units of w: word i of
+ * lane L at byte 4w(32(i/w) + L) + 4(i%w). With fp16 scales a, b and the
+ * column slice are 2-byte values; each part is padded to 16 bytes. At 6 bits
+ * a page of D = 128, N = 128 takes 3264 bytes, 40% of fp16.
+ *
  * The page is a K part followed by a V part, each contiguous so that the
  * decode kernel can fetch and recycle them separately:
  *   K part, KP = 8D + 128 + 4C bytes, C = D*P/N:
@@ -115,12 +132,12 @@ typedef struct {
   int32_t tile_tokens;  /* N: 128 or 64 (dense), 128 (latent) */
   int32_t page_tokens;  /* P: 16 */
   int32_t num_kv_heads; /* Hkv (1 for the latent cache) */
-  int32_t k_bits;       /* 4 */
-  int32_t v_bits;       /* 2 (dense); 0 for the latent cache (V = K codes) */
+  int32_t k_bits;       /* 4 (the k4v2 preset); see below for other widths */
+  int32_t v_bits;       /* 2 (the preset); 0 for the latent cache (V = K codes) */
   int32_t norm_iters;   /* T: 1..8 normalisation iterations */
   int32_t rope_dim;     /* 0 (dense) or 64 (latent) */
   int32_t kv_dtype;     /* 0 fp16, 1 bf16: dtype of K/V (latent), q, tails */
-  int32_t reserved;
+  int32_t scale_dtype;  /* 0: fp32 scales a, b, c; 1: fp16 scales (dense only) */
   int64_t num_pages;    /* physical pages in the cache */
 } kvarn_layout;
 

@@ -207,7 +207,7 @@ def decode_window(q, cache, lay: layout.DenseLayout, block_table, seq_lens, sm_s
 
 
 def encode_into_cache(cache, lay: layout.DenseLayout, k, v, block_table, tile_start,
-                      bits=(4, 2), T=2):
+                      bits=None, T=2):
     """Encode every full tile of a chunk and store it.
 
     k, v [B, Hkv, C, D] values of the chunk (C a multiple of N); tile_start[b]
@@ -217,6 +217,7 @@ def encode_into_cache(cache, lay: layout.DenseLayout, k, v, block_table, tile_st
     v = np.asarray(v, np.float64)
     B, Hkv, C, D = k.shape
     N = lay.N
+    bits = (lay.k_bits, lay.v_bits) if bits is None else bits
     ppt = N // layout.P
     for b in range(B):
         for t in range(C // N):

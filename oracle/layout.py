@@ -24,6 +24,25 @@ library's own format. A page holds P = 16 tokens of one KV head:
   the V part (V codes, V a[16], V b[16], V column-scale slice).
 The page at logical index l of a sequence carries the column scales of
 channels [(l mod N/P) * D*P/N, +D*P/N) of its tile; all words little-endian.
+
+Other widths (gmlx page, "The two schemes": kvarn widths 2, 3, 4, 5, 6 and 8,
+separate for keys and values). A b-bit code is stored as one or two planes,
+b = 2: [2], 3: [2, 1], 4: [4], 5: [4, 1], 6: [4, 2], 8: [4, 4], the code
+being plane0 + 2^w0 plane1; each plane region (2*D*w bytes per page, the
+planes in order) follows one rule for a plane of width w in {1, 2, 4}: lane
+L = 4g + t owns words of 8/w fragments each; fragment f of a word has its
+first operand register at bits w*f (low half) and 16 + w*f (high half), its
+second at 8 + w*f and 24 + w*f.
+  K plane: fragment 2*kc + e (k-chunk kc, token block e: tokens 8e + g);
+           channel 16kc + 2t + e' + 8h at bit w*f + 8h + 16e'. Words go in
+           units of U = min(4, D*w/64) words: word i of lane L at byte
+           4U*(32*(i//U) + L) + 4*(i%U).
+  V plane: fragment nc (8-channel block); channel 8nc + g of token
+           2t + e' + 8h at bit w*f + 8h + 16e'. Words go in units of w
+           words (eight blocks): word i of lane L at 4w*(32*(i//w) + L) +
+           4*(i%w).
+The 4-bit K and 2-bit V placements above are the w = 4 and w = 2 cases. The
+scales are fp32 ("S32") or fp16 ("S16"): a[16], b[16], col as 2-byte values.
 """
 from __future__ import annotations
 
@@ -34,23 +53,31 @@ import numpy as np
 P = 16  # tokens per page
 
 
+PLANES = {2: (2,), 3: (2, 1), 4: (4,), 5: (4, 1), 6: (4, 2), 8: (4, 4)}
+
+
+def _align16(x: int) -> int:
+    return (x + 15) // 16 * 16
+
+
 class DenseLayout:
-    def __init__(self, D: int, N: int, k_bits: int = 4, v_bits: int = 2):
-        if (k_bits, v_bits) != (4, 2):
-            raise ValueError("the page format is defined for 4-bit K and 2-bit V")
+    def __init__(self, D: int, N: int, k_bits: int = 4, v_bits: int = 2, scale_bytes: int = 4):
+        if k_bits not in PLANES or v_bits not in PLANES or scale_bytes not in (2, 4):
+            raise ValueError("widths 2, 3, 4, 5, 6, 8 and fp32 or fp16 scales")
         if N % P:
             raise ValueError("tile must be a whole number of pages")
-        self.D, self.N = D, N
+        self.D, self.N, self.k_bits, self.v_bits, self.sb = D, N, k_bits, v_bits, scale_bytes
+        sb = scale_bytes
         self.col_per_page = D * P // N
         self.k_codes = 0
-        self.k_a = 8 * D
-        self.k_b = self.k_a + 4 * P
-        self.k_col = self.k_b + 4 * P
-        self.v_codes = self.k_col + 4 * self.col_per_page   # start of the V part
-        self.v_a = self.v_codes + 4 * D
-        self.v_b = self.v_a + 4 * P
-        self.v_col = self.v_b + 4 * P
-        self.page_bytes = self.v_col + 4 * self.col_per_page
+        self.k_a = 2 * D * k_bits
+        self.k_b = self.k_a + sb * P
+        self.k_col = self.k_b + sb * P
+        self.v_codes = _align16(self.k_col + sb * self.col_per_page)   # start of the V part
+        self.v_a = self.v_codes + 2 * D * v_bits
+        self.v_b = self.v_a + sb * P
+        self.v_col = self.v_b + sb * P
+        self.page_bytes = _align16(self.v_col + sb * self.col_per_page)
 
 
 def k_code_position(D: int, tau: int, j: int):
@@ -71,6 +98,30 @@ def v_code_position(D: int, tau: int, j: int):
     lane = 4 * g + t
     bit = 2 * c + 8 * h + 16 * e
     return 8 * (32 * (w // 2) + lane) + 4 * (w % 2) + bit // 8, bit % 8
+
+
+def k_plane_position(D: int, tau: int, j: int, w: int):
+    """(byte, bit shift) of token tau, channel j inside a K plane of width w."""
+    F = 8 // w
+    kc, r = divmod(j, 16)
+    t, ep, h = (r % 8) // 2, r % 2, r // 8
+    g, e = tau % 8, tau // 8
+    lane = 4 * g + t
+    word, f = divmod(2 * kc + e, F)
+    U = min(4, D * w // 64)
+    bit = w * f + 8 * h + 16 * ep
+    return 4 * U * (32 * (word // U) + lane) + 4 * (word % U) + bit // 8, bit % 8
+
+
+def v_plane_position(D: int, tau: int, j: int, w: int):
+    """(byte, bit shift) of token tau, channel j inside a V plane of width w."""
+    F = 8 // w
+    nc, g = divmod(j, 8)
+    t, ep, h = (tau % 8) // 2, tau % 2, tau // 8
+    lane = 4 * g + t
+    word, f = divmod(nc, F)
+    bit = w * f + 8 * h + 16 * ep
+    return 4 * w * (32 * (word // w) + lane) + 4 * (word % w) + bit // 8, bit % 8
 
 
 def _latent_word_position(D: int, tau: int, j: int):
@@ -106,6 +157,9 @@ def latent_code_position(D: int, tau: int, j: int):
 @functools.lru_cache(maxsize=None)
 def _maps(D: int):
     pos = {"k": k_code_position, "v": v_code_position, "latent": latent_code_position}
+    for w in (1, 2, 4):
+        pos[f"k{w}"] = functools.partial(k_plane_position, w=w)
+        pos[f"v{w}"] = functools.partial(v_plane_position, w=w)
     out = {}
     for kind, f in pos.items():
         if kind == "latent" and D // 32 < 8:
@@ -119,7 +173,8 @@ def _maps(D: int):
     return out
 
 
-_WIDTH = {"k": (4, 8), "latent": (4, 8), "v": (2, 4)}   # bits, bytes per channel of a page
+_WIDTH = {"k": (4, 8), "latent": (4, 8), "v": (2, 4),   # bits, bytes per channel of a page
+          "k1": (1, 2), "k2": (2, 4), "k4": (4, 8), "v1": (1, 2), "v2": (2, 4), "v4": (4, 8)}
 
 
 def pack_codes(codes: np.ndarray, kind: str) -> np.ndarray:
@@ -137,12 +192,43 @@ def unpack_codes(region: np.ndarray, D: int, kind: str) -> np.ndarray:
     return (region.astype(np.int64)[byte] >> shift) & mask
 
 
+def pack_planes(codes: np.ndarray, bits: int, side: str) -> np.ndarray:
+    """A [16, D] block of `bits`-bit codes of K (side "k") or V ("v") as its
+    plane regions in order. The K4 / V2 planes are the "k" / "v" kinds."""
+    out, rest = [], codes.astype(np.int64)
+    for w in PLANES[bits]:
+        plane = rest & ((1 << w) - 1)
+        rest = rest >> w
+        kind = {("k", 4): "k", ("v", 2): "v"}.get((side, w), f"{side}{w}")
+        out.append(pack_codes(plane, kind))
+    return np.concatenate(out)
+
+
+def unpack_planes(region: np.ndarray, D: int, bits: int, side: str) -> np.ndarray:
+    codes, off, shift = 0, 0, 0
+    for w in PLANES[bits]:
+        kind = {("k", 4): "k", ("v", 2): "v"}.get((side, w), f"{side}{w}")
+        n = 2 * D * w
+        codes = codes + (unpack_codes(region[off:off + n], D, kind) << shift)
+        off += n
+        shift += w
+    return codes
+
+
 def f32_bytes(x) -> np.ndarray:
     return np.asarray(x, dtype="<f4").view(np.uint8)
 
 
 def f32_from(region: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(region).view("<f4").astype(np.float64)
+
+
+def scale_bytes(x, sb: int) -> np.ndarray:
+    return np.asarray(x, dtype="<f4" if sb == 4 else "<f2").view(np.uint8)
+
+
+def scale_from(region: np.ndarray, sb: int) -> np.ndarray:
+    return np.ascontiguousarray(region).view("<f4" if sb == 4 else "<f2").astype(np.float64)
 
 
 def write_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int,
@@ -152,40 +238,36 @@ def write_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int,
 
     cache: uint8 [num_pages, Hkv, page_bytes].
     """
-    D, N, cpp = lay.D, lay.N, lay.col_per_page
+    D, N, cpp, sb = lay.D, lay.N, lay.col_per_page, lay.sb
     for p, phys in enumerate(phys_pages):
         pg = cache[phys, head]
         rows = slice(p * P, (p + 1) * P)
         cols = slice(p * cpp, (p + 1) * cpp)
-        pg[lay.k_codes:lay.k_codes + 8 * D] = pack_codes(enc_k["codes"][rows], "k")
-        pg[lay.v_codes:lay.v_codes + 4 * D] = pack_codes(enc_v["codes"][rows], "v")
-        pg[lay.k_a:lay.k_a + 4 * P] = f32_bytes(enc_k["a"][rows])
-        pg[lay.k_b:lay.k_b + 4 * P] = f32_bytes(enc_k["b"][rows])
-        pg[lay.v_a:lay.v_a + 4 * P] = f32_bytes(enc_v["a"][rows])
-        pg[lay.v_b:lay.v_b + 4 * P] = f32_bytes(enc_v["b"][rows])
-        pg[lay.k_col:lay.k_col + 4 * cpp] = f32_bytes(enc_k["c"][cols])
-        pg[lay.v_col:lay.v_col + 4 * cpp] = f32_bytes(enc_v["c"][cols])
+        pg[lay.k_codes:lay.k_codes + 2 * D * lay.k_bits] = pack_planes(enc_k["codes"][rows], lay.k_bits, "k")
+        pg[lay.v_codes:lay.v_codes + 2 * D * lay.v_bits] = pack_planes(enc_v["codes"][rows], lay.v_bits, "v")
+        pg[lay.k_a:lay.k_a + sb * P] = scale_bytes(enc_k["a"][rows], sb)
+        pg[lay.k_b:lay.k_b + sb * P] = scale_bytes(enc_k["b"][rows], sb)
+        pg[lay.v_a:lay.v_a + sb * P] = scale_bytes(enc_v["a"][rows], sb)
+        pg[lay.v_b:lay.v_b + sb * P] = scale_bytes(enc_v["b"][rows], sb)
+        pg[lay.k_col:lay.k_col + sb * cpp] = scale_bytes(enc_k["c"][cols], sb)
+        pg[lay.v_col:lay.v_col + sb * cpp] = scale_bytes(enc_v["c"][cols], sb)
 
 
 def read_tile(cache: np.ndarray, lay: DenseLayout, phys_pages, head: int):
     """Inverse of write_tile: returns (K dict, V dict) of codes [N, D] and
-    float64 copies of the stored fp32 a [N], b [N], c [D]."""
-    D, cpp = lay.D, lay.col_per_page
+    float64 copies of the stored a [N], b [N], c [D] (fp32 or fp16)."""
+    D, cpp, sb = lay.D, lay.col_per_page, lay.sb
     out = {}
     for kind in ("k", "v"):
         codes, a, b, c = [], [], [], []
+        base, bits = (lay.k_codes, lay.k_bits) if kind == "k" else (lay.v_codes, lay.v_bits)
+        oa, ob, oc = (lay.k_a, lay.k_b, lay.k_col) if kind == "k" else (lay.v_a, lay.v_b, lay.v_col)
         for phys in phys_pages:
             pg = cache[phys, head]
-            if kind == "k":
-                codes.append(unpack_codes(pg[lay.k_codes:lay.k_codes + 8 * D], D, "k"))
-                a.append(f32_from(pg[lay.k_a:lay.k_a + 4 * P]))
-                b.append(f32_from(pg[lay.k_b:lay.k_b + 4 * P]))
-                c.append(f32_from(pg[lay.k_col:lay.k_col + 4 * cpp]))
-            else:
-                codes.append(unpack_codes(pg[lay.v_codes:lay.v_codes + 4 * D], D, "v"))
-                a.append(f32_from(pg[lay.v_a:lay.v_a + 4 * P]))
-                b.append(f32_from(pg[lay.v_b:lay.v_b + 4 * P]))
-                c.append(f32_from(pg[lay.v_col:lay.v_col + 4 * cpp]))
+            codes.append(unpack_planes(pg[base:base + 2 * D * bits], D, bits, kind))
+            a.append(scale_from(pg[oa:oa + sb * P], sb))
+            b.append(scale_from(pg[ob:ob + sb * P], sb))
+            c.append(scale_from(pg[oc:oc + sb * cpp], sb))
         out[kind] = dict(codes=np.concatenate(codes), a=np.concatenate(a),
                          b=np.concatenate(b), c=np.concatenate(c))
     return out["k"], out["v"]

@@ -31,14 +31,14 @@ class Layout(ctypes.Structure):
                 ("page_tokens", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32),
                 ("norm_iters", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("scale_dtype", ctypes.c_int32),
                 ("num_pages", ctypes.c_int64)]
 
 
 def dense_layout(head_dim, tile_tokens, num_kv_heads, num_pages, kv_dtype=FP16, norm_iters=2,
-                 k_bits=4, v_bits=2) -> Layout:
+                 k_bits=4, v_bits=2, fp16_scales=False) -> Layout:
     return Layout(head_dim, tile_tokens, 16, num_kv_heads, k_bits, v_bits, norm_iters, 0,
-                  kv_dtype, 0, num_pages)
+                  kv_dtype, 1 if fp16_scales else 0, num_pages)
 
 
 def latent_layout(num_pages, kv_dtype=BF16, norm_iters=2) -> Layout:

@@ -22,7 +22,9 @@ int32_t check_dense(const kvarn_layout* L) {
   if (L->page_tokens != kPageTokens) return KVARN_EUNSUPPORTED;
   if (L->head_dim != 128 && L->head_dim != 256) return KVARN_EUNSUPPORTED;
   if (L->tile_tokens != 128 && L->tile_tokens != 64) return KVARN_EUNSUPPORTED;
-  if (L->k_bits != 4 || L->v_bits != 2) return KVARN_EUNSUPPORTED;
+  if (L->scale_dtype != 0 && L->scale_dtype != 1) return KVARN_EUNSUPPORTED;
+  if (!widths_supported(L->head_dim, L->k_bits, L->v_bits, L->scale_dtype == 1 ? 2 : 4))
+    return KVARN_EUNSUPPORTED;
   if (L->norm_iters < 1 || L->norm_iters > 8) return KVARN_EUNSUPPORTED;
   if (L->rope_dim != 0) return KVARN_EINVAL;
   if (L->kv_dtype != 0 && L->kv_dtype != 1) return KVARN_EUNSUPPORTED;
@@ -68,7 +70,13 @@ int32_t kvarn_layout_check(const kvarn_layout* L) {
 int64_t kvarn_page_bytes(const kvarn_layout* L) {
   if (kvarn_layout_check(L) != KVARN_OK) return -1;
   if (is_latent(L)) return LatentPage(L->head_dim, L->rope_dim, L->tile_tokens).bytes();
-  return DensePage(L->head_dim, L->tile_tokens).bytes();
+  return DensePage(L->head_dim, L->tile_tokens, L->k_bits, L->v_bits, L->scale_dtype == 1 ? 2 : 4).bytes();
+}
+
+// The k4v2 preset with fp32 scales: the page format of the append, fp16
+// bypass and no-allocation paths.
+static bool is_preset(const kvarn_layout* L) {
+  return L->k_bits == 4 && L->v_bits == 2 && L->scale_dtype == 0;
 }
 
 int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
@@ -102,6 +110,9 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
   p.norm_iters = L->norm_iters;
   p.bf16 = L->kv_dtype == 1;
   p.err = error_flags;
+  p.k_bits = L->k_bits;
+  p.v_bits = L->v_bits;
+  p.scale_bytes = L->scale_dtype == 1 ? 2 : 4;
   return from_cuda(launch_encode_dense(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -130,6 +141,7 @@ int32_t kvarn_append(const void* k, const void* v, const int32_t* seq_lens, int3
                      kvarn_stream_t stream) {
   int32_t s = check_dense(L);
   if (s != KVARN_OK) return s;
+  if (!is_preset(L)) return KVARN_EUNSUPPORTED;
   if (num_seqs < 0 || max_seq_len < 0) return KVARN_EINVAL;
   if (num_seqs == 0) return KVARN_OK;
   if (!k || !v || !seq_lens || !tail_k || !tail_v || !block_table || !cache || !error_flags || bt_stride < 1)
@@ -257,6 +269,9 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   p.sink_k = sink_k;
   p.sink_v = sink_v;
   p.recent_tokens = recent_tokens;
+  p.k_bits = L->k_bits;
+  p.v_bits = L->v_bits;
+  p.scale_bytes = L->scale_dtype == 1 ? 2 : 4;
   return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 

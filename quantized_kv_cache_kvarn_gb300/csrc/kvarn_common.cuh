@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/kvarn.h"
 
 namespace kvarn {
@@ -15,23 +17,32 @@ constexpr int kPageTokens = 16;
 // ---------------------------------------------------------------- layout
 // Byte offsets inside one dense page of one KV head (format documented in
 // kvarn.h): a K part (codes, a, b, column slice) then a V part (same order).
-// C = D * P / N column scales per page.
+// KB / VB: code widths; SB: bytes per scale (4: fp32, 2: fp16). C = D*P/N
+// column scales per page; parts start and end on 16-byte boundaries.
+constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+
 struct DensePage {
-  int D, N;
-  __host__ __device__ constexpr DensePage(int d, int n) : D(d), N(n) {}
+  int D, N, KB, VB, SB;
+  __host__ __device__ constexpr DensePage(int d, int n, int kb = 4, int vb = 2, int sb = 4)
+      : D(d), N(n), KB(kb), VB(vb), SB(sb) {}
   __host__ __device__ constexpr int cols() const { return D * kPageTokens / N; }
   __host__ __device__ constexpr int k_codes() const { return 0; }
-  __host__ __device__ constexpr int k_a() const { return 8 * D; }
-  __host__ __device__ constexpr int k_b() const { return 8 * D + 64; }
-  __host__ __device__ constexpr int k_col() const { return 8 * D + 128; }
-  __host__ __device__ constexpr int k_part() const { return 8 * D + 128 + 4 * cols(); }
+  __host__ __device__ constexpr int k_a() const { return 2 * D * KB; }
+  __host__ __device__ constexpr int k_b() const { return k_a() + SB * kPageTokens; }
+  __host__ __device__ constexpr int k_col() const { return k_b() + SB * kPageTokens; }
+  __host__ __device__ constexpr int k_part() const { return align16(k_col() + SB * cols()); }
   __host__ __device__ constexpr int v_codes() const { return k_part(); }
-  __host__ __device__ constexpr int v_a() const { return k_part() + 4 * D; }
-  __host__ __device__ constexpr int v_b() const { return k_part() + 4 * D + 64; }
-  __host__ __device__ constexpr int v_col() const { return k_part() + 4 * D + 128; }
-  __host__ __device__ constexpr int v_part() const { return 4 * D + 128 + 4 * cols(); }
+  __host__ __device__ constexpr int v_a() const { return k_part() + 2 * D * VB; }
+  __host__ __device__ constexpr int v_b() const { return v_a() + SB * kPageTokens; }
+  __host__ __device__ constexpr int v_col() const { return v_b() + SB * kPageTokens; }
+  __host__ __device__ constexpr int v_part() const { return align16(2 * D * VB + 2 * SB * kPageTokens + SB * cols()); }
   __host__ __device__ constexpr int bytes() const { return k_part() + v_part(); }
 };
+
+// Code planes of a b-bit code (low plane first): 2: [2], 3: [2, 1], 4: [4],
+// 5: [4, 1], 6: [4, 2], 8: [4, 4]; the code is plane0 + 2^w0 plane1.
+__host__ __device__ constexpr int plane_w0(int b) { return b == 2 || b == 3 ? 2 : 4; }
+__host__ __device__ constexpr int plane_w1(int b) { return b == 3 || b == 5 ? 1 : b == 6 ? 2 : b == 8 ? 4 : 0; }
 
 // MLA latent page: codes (dense-K placement), fp16 rope, a, b, column slice.
 struct LatentPage {
@@ -215,6 +226,91 @@ __device__ __forceinline__ void dequant_v_word(uint32_t x, uint32_t* out) {
     out[4 * half + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00300030u, kMagic)), s16, o16));
     out[4 * half + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00C000C0u, kMagic)), s64, o64));
   }
+}
+
+// fp16 bit patterns of small integers (|n| < 2048) and of powers of two,
+// for compile-time operand constants.
+__host__ __device__ constexpr unsigned short fp16_int(int n) {
+  const unsigned short sgn = n < 0 ? 0x8000u : 0u;
+  const int a = n < 0 ? -n : n;
+  int e = 0;
+  while ((2 << e) <= a) ++e;
+  return a == 0 ? sgn : static_cast<unsigned short>(sgn | ((e + 15) << 10) | ((a - (1 << e)) << (10 - e)));
+}
+__host__ __device__ constexpr unsigned short fp16_pow2(int e) { return static_cast<unsigned short>((e + 15) << 10); }
+
+__device__ __forceinline__ __half2 h2_bits(unsigned short b) {
+  return __halves2half2(__ushort_as_half(b), __ushort_as_half(b));
+}
+
+// The W-bit fields at bits P and P + 16 of x (P + W <= 8) as the exact fp16
+// pair (n - C): OR-ed into fp16 1024 a field is 1024 + 2^P n; scaling by
+// 2^-P and subtracting 1024 / 2^P + C leaves n - C. Every intermediate is an
+// integer below 2048 times a power of two, so each step is exact.
+template <int W, int P, int C>
+__device__ __forceinline__ uint32_t field_h2(uint32_t x) {
+  constexpr uint32_t m = ((1u << W) - 1u) << P;
+  const __half2 v = u32_as_h2(lop3_and_or(x, m | (m << 16), kMagic));
+  if constexpr (P == 0)
+    return h2_as_u32(__hsub2(v, h2_bits(fp16_int(1024 + C))));
+  else
+    return h2_as_u32(__hfma2(v, h2_bits(fp16_pow2(-P)), h2_bits(fp16_int(-((1024 >> P) + C)))));
+}
+
+// Operand pair (b0, b1) of fragment slot F_ of a code-plane word pair: b0
+// from the word, b1 from the word >> 8 (see the page format).
+template <int W, int SLOT, int C>
+__device__ __forceinline__ void plane_pair(uint32_t x, uint32_t& b0, uint32_t& b1) {
+  b0 = field_h2<W, W * SLOT, C>(x);
+  b1 = field_h2<W, W * SLOT, C>(x >> 8);
+}
+
+// Operand pair of a B-bit code (one or two planes) as exact fp16 (n - 2^(B-1)).
+// x0 / x1: the words of plane 0 / plane 1 holding the fragment; S0 / S1 its
+// slots in them.
+template <int B, int S0, int S1>
+__device__ __forceinline__ void code_pair(uint32_t x0, uint32_t x1, uint32_t& b0, uint32_t& b1) {
+  constexpr int W0 = plane_w0(B), W1 = plane_w1(B);
+  if constexpr (W1 == 0) {
+    plane_pair<W0, S0, (1 << (B - 1))>(x0, b0, b1);
+  } else {
+    uint32_t l0, l1, h0, h1;
+    plane_pair<W0, S0, 0>(x0, l0, l1);
+    plane_pair<W1, S1, (1 << (B - 1 - W0))>(x1, h0, h1);
+    const __half2 sc = h2_bits(fp16_pow2(W0));
+    b0 = h2_as_u32(__hfma2(u32_as_h2(h0), sc, u32_as_h2(l0)));
+    b1 = h2_as_u32(__hfma2(u32_as_h2(h1), sc, u32_as_h2(l1)));
+  }
+}
+
+// Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E).
+template <int B, int E, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (B < E) {
+    f(std::integral_constant<int, B>{});
+    static_for<B + 1, E>(f);
+  }
+}
+
+// NW consecutive 32-bit words from shared memory (NW = 1, 2 or 4, aligned).
+template <int NW>
+__device__ __forceinline__ void load_words(const unsigned char* p, uint32_t (&out)[NW]) {
+  if constexpr (NW == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+  } else if constexpr (NW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    out[0] = v.x; out[1] = v.y;
+  } else {
+    out[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
+
+// Two consecutive scale values (fp32 or fp16 in the page) as float2.
+template <int SB>
+__device__ __forceinline__ float2 load_scale2(const unsigned char* p) {
+  if constexpr (SB == 4) return *reinterpret_cast<const float2*>(p);
+  else return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
 __device__ __forceinline__ float warp_max_xor(float v, int lo, int hi) {

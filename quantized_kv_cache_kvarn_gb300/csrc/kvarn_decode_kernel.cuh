@@ -1,0 +1,620 @@
+// KVarN decode attention over the compressed paged cache, sm_103a.
+//
+// Paged, split-K, GQA-grouped decode that streams the packed codes and
+// scales straight from HBM and dequantises them in registers; no fp16 K or V
+// buffer is ever formed (turbo-attn page, "Inline dequant"). Scores are
+// taken in the rotated basis: the query is rotated once per CTA and the
+// output un-rotated once in the merge (turbo-attn page, "How it works").
+//
+// Kernel 1 (decode_dense_kernel): one CTA per (split, KV head, sequence);
+// each of its W warps owns every W-th tile of the split. A warp keeps one
+// shared-memory slot for the K parts and one for the V parts of its tile's
+// pages, filled by one-dimensional bulk copies (completion counted on an
+// mbarrier); an L2 prefetch of later tiles measured slower (its lines were
+// partly evicted and read twice) and is not used. The K slot
+// is refilled with the next tile while P V runs, the V slot while the next
+// Q K runs. Per tile and warp:
+//   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
+//        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
+//        half of the m16 tile free, so the split costs no extra mma);
+//   S  = q~ . (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
+//        integers, made from the packed nibbles by exponent-bias arithmetic;
+//        recentred codes keep every running sum near the size of its result,
+//        which the tensor cores need: they round a sum relative to its
+//        largest term);
+//   s  = a_K * S + (b_K + 8 a_K) * sum(q~)      (row scales folded back in);
+//   online softmax in base 2;
+//   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
+//   acc = acc * alpha + c_V * (u + sum p (b_V + 2 a_V)).
+// The warps of a CTA merge in shared memory and write one partial
+// (max, sum, unnormalised output) per split. The last split slot holds the
+// fp16 tail (tokens past the last full tile, in the original basis).
+// Kernel 2 (merge_kernel): log-sum-exp merge of the partials, inverse
+// Hadamard transform of the rotated part, plus the tail part.
+#pragma once
+
+#include <math.h>
+
+#include <algorithm>
+
+#include "kvarn_common.cuh"
+#include "kvarn_launch.h"
+#include "kvarn_merge.cuh"
+
+namespace kvarn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// CTAs per SM the 4-warp decode kernel is register-limited to (3 caps it at
+// 168 registers per thread, 2 at 255).
+#ifndef KVARN_DECODE_MIN_CTAS
+#define KVARN_DECODE_MIN_CTAS 3
+#endif
+
+template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4>
+struct DecShape {
+  static constexpr DensePage PG{D, N, KB, VB, SB};
+  static constexpr int PPT = N / kPageTokens;
+  static constexpr int PB = PG.bytes();
+  static constexpr int KP = PG.k_part();
+  static constexpr int VP = PG.v_part();
+  static constexpr int KSLOT = PPT * KP;
+  static constexpr int VSLOT = PPT * VP;
+  static constexpr int WARP_SMEM = KSLOT + VSLOT;
+  static constexpr int NB = N / 8;
+  static constexpr int KC = D / 16;
+  static constexpr int NC = D / 8;
+  static constexpr int CPP = PG.cols();
+  static constexpr int KCH = D / 64;  // groups of four k-chunks (eight K fragments) per page
+  static constexpr int VHC = D / 64;  // groups of eight channel blocks (eight V fragments) per page
+  // code planes (width, fragments per word, words per unit, region offset)
+  static constexpr int KW0 = plane_w0(KB), KW1 = plane_w1(KB), VW0 = plane_w0(VB), VW1 = plane_w1(VB);
+  static constexpr int KF0 = 8 / KW0, KF1 = KW1 ? 8 / KW1 : 8, VF0 = 8 / VW0, VF1 = VW1 ? 8 / VW1 : 8;
+  static constexpr int KU0 = D * KW0 / 64 < 4 ? D * KW0 / 64 : 4;
+  static constexpr int KU1 = KW1 ? (D * KW1 / 64 < 4 ? D * KW1 / 64 : 4) : 1;
+  static constexpr int KR1 = 2 * D * KW0, VR1 = 2 * D * VW0;
+  static constexpr float KCENTER = static_cast<float>(1 << (KB - 1)), VCENTER = static_cast<float>(1 << (VB - 1));
+  static constexpr int RING = W * WARP_SMEM;
+  static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
+  static_assert(W * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
+};
+
+struct DecArgs {
+  const void* q;  // [B][Q][Hq][D]
+  float kappa;    // sm_scale * log2(e)
+  const uint8_t* cache;
+  int32_t Hq, Hkv, G;
+  int32_t Q;           // query tokens per sequence (speculative verify: the last Q tokens)
+  int32_t tail_cap;    // tail rows per (sequence, KV head)
+  int32_t sink_tiles;  // raw sink records: tokens [0, sink_tiles N) are rows of sink_k / sink_v
+  int32_t recent;      // raw recent records: the newest `recent` accepted tokens stay in the tail
+  const void* sink_k;
+  const void* sink_v;
+  int64_t num_pages;
+  const int32_t* bt;
+  int32_t bt_stride;
+  const int32_t* seq_lens;
+  int32_t max_seq_len;
+  const void* tail_k;
+  const void* tail_v;
+  float* ws;
+  int32_t tps, nsplit, slots;
+  uint32_t* err;
+};
+
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T* p, float* out) {
+  if constexpr (E == 4) {
+    uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = to_f32<T>(h[i]);
+  } else {
+    static_assert(E % 8 == 0, "vector width");
+#pragma unroll
+    for (int k = 0; k < E; k += 8) load8<T>(p + k, out + k);
+  }
+}
+
+__device__ __forceinline__ void write_empty(float* part, int D, int lane) {
+  if (lane == 0) {
+    part[0] = -INFINITY;
+    part[1] = 0.f;
+  }
+  for (int j = lane; j < D; j += 32) part[4 + j] = 0.f;
+}
+
+// Rows of a CTA: up to eight (query head, query token) pairs, pair p = 8 rg + r
+// with head p % G and query token p / G, so that one mma row tile serves G Q
+// <= 8 pairs at the cost of one.
+struct RowMap {
+  int rg, n;  // row group, rows used in it
+  __device__ RowMap(const DecArgs& A, int rg_) : rg(rg_), n(min(8, A.G * A.Q - 8 * rg_)) {}
+  __device__ int head(const DecArgs& A, int r) const { return (8 * rg + r) % A.G; }
+  __device__ int query(const DecArgs& A, int r) const { return (8 * rg + r) / A.G; }
+};
+
+// Partial slot of (sequence b, query token j, query head hq).
+__device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j, int hq, int slot) {
+  return A.ws + (static_cast<int64_t>((b * A.Q + j) * A.Hq + hq) * A.slots + slot) * kPStride(D);
+}
+
+// Tokens visible to query token j of a sequence of len tokens (causal among
+// the Q tokens under verification), and the committed prefix shared by all.
+__device__ __forceinline__ int visible_len(int len, int Q, int j) { return max(0, len - Q + 1 + j); }
+
+// Raw records of a row: the sink rows [0, min(sink, visible)) and the tail rows
+// for tokens [committed, visible); dense attention in the original basis, one
+// warp per row, one pass with a running maximum (no per-token buffer, so the
+// record lengths are bounded only by their buffers).
+template <int D, typename T>
+__device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count, const float* qv, float& mx,
+                                            float& l, float* acc) {
+  constexpr int E = D / 32;
+  constexpr int U = D == 128 ? 8 : 4;  // tokens in flight per step
+  const int lane = threadIdx.x & 31;
+  int tau = 0;
+  for (; tau + U <= count; tau += U) {
+    float kv[U][E], vv[U][E], dot[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      load_vec<T, E>(kp + static_cast<int64_t>(tau + u) * D + lane * E, kv[u]);
+      load_vec<T, E>(vp + static_cast<int64_t>(tau + u) * D + lane * E, vv[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      dot[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot[u] = fmaf(qv[e], kv[u][e], dot[u]);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < U; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], o);  // same in every lane
+    float mn = mx;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mn = fmaxf(mn, dot[u]);
+    const float sc = exp2f(mx - mn);
+    l *= sc;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float p = exp2f(dot[u] - mn);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[u][e], acc[e]);
+    }
+    mx = mn;
+  }
+  for (; tau < count; ++tau) {
+    float kv[E], vv[E];
+    load_vec<T, E>(kp + static_cast<int64_t>(tau) * D + lane * E, kv);
+    load_vec<T, E>(vp + static_cast<int64_t>(tau) * D + lane * E, vv);
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
+    dot = warp_sum_xor(dot, 1, 32);
+    const float mn = fmaxf(mx, dot);
+    const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
+    l = fmaf(l, sc, p);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], sc, p * vv[e]);
+    mx = mn;
+  }
+}
+
+// Raw split `chunk` covers raw tokens [chunk * kRawChunk, +kRawChunk) of the
+// row's raw list: its sink rows, then its tail rows.
+template <int D, int N, typename T, int W>
+__device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int sink,
+                              int committed, int chunk) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int r = warp; r < R.n; r += W) {
+    const int j = R.query(A, r), hq = kvh * A.G + R.head(A, r);
+    const int vis = visible_len(len, A.Q, j);
+    const int n_sink = min(sink, vis), n_tail = max(0, vis - committed);
+    const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
+    const int s_cnt = max(0, min(c1, n_sink) - c0), t0 = max(c0, n_sink) - n_sink, t_cnt = max(0, c1 - max(c0, n_sink));
+    float* part = part_of(A, D, b, j, hq, A.nsplit + chunk);
+    const bool miss = (t_cnt > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
+                      (s_cnt > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
+    if ((t_cnt <= 0 && s_cnt <= 0) || miss) {
+      if (miss && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
+      write_empty(part, D, lane);
+      continue;
+    }
+    float qv[E];
+    load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, qv);
+#pragma unroll
+    for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
+    float mx = -INFINITY, l = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (s_cnt > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N) + c0;
+      raw_segment<D, T>(static_cast<const T*>(A.sink_k) + row0 * D, static_cast<const T*>(A.sink_v) + row0 * D,
+                        s_cnt, qv, mx, l, acc);
+    }
+    if (t_cnt > 0) {
+      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap + t0;
+      raw_segment<D, T>(static_cast<const T*>(A.tail_k) + row0 * D, static_cast<const T*>(A.tail_v) + row0 * D,
+                        t_cnt, qv, mx, l, acc);
+    }
+    if (lane == 0) {
+      part[0] = mx;
+      part[1] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) part[4 + lane * E + e] = acc[e];
+  }
+}
+
+template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
+__global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) decode_dense_kernel(DecArgs A) {
+  using S = DecShape<D, N, W, KB, VB, SB>;
+  constexpr DensePage PG = S::PG;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  // KV head is the fastest grid axis: CTAs resident together read the same
+  // physical pages (all heads of a page are contiguous), keeping DRAM rows open
+  const int kvh = blockIdx.x % A.Hkv, split = blockIdx.y, b = blockIdx.z;
+  const RowMap R(A, blockIdx.x / A.Hkv);
+
+  int len = A.seq_lens[b];
+  if (len < 0 || len > A.max_seq_len) {
+    if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    len = len < 0 ? 0 : A.max_seq_len;
+  }
+  // Only tokens up to the first query token are accepted, so only the tiles
+  // they fill can be committed; of those, the raw sink records come first and
+  // the newest `recent` accepted tokens stay raw. Compressed: tiles
+  // [sink_tiles, end).
+  const int sink = A.sink_tiles * N;
+  const int committed = max(sink, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
+  const int end = committed / N;
+
+  if (split >= A.nsplit) {
+    tail_partials<D, N, T, W>(A, b, kvh, R, len, sink, committed, split - A.nsplit);
+    return;
+  }
+  const int t0 = A.sink_tiles + split * A.tps, t1 = min(t0 + A.tps, end);
+  if (t0 >= t1) {
+    for (int r = warp; r < R.n; r += W)
+      write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), split), D, lane);
+    return;
+  }
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::RING);
+  float* qrot = reinterpret_cast<float*>(smem + S::RING + W * 2 * 8);
+  int32_t* pages = reinterpret_cast<int32_t*>(smem + S::SMEM);  // this split's page ids
+  unsigned char* kslot = smem + warp * S::WARP_SMEM;
+  unsigned char* vslot = kslot + S::KSLOT;
+  uint64_t* barK = bars + 2 * warp;
+  uint64_t* barV = barK + 1;
+
+  const int first = t0 + warp;
+  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
+  const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
+
+  // the split's block-table entries, checked once, into shared memory
+  for (int e = threadIdx.x; e < (t1 - t0) * S::PPT; e += W * 32) {
+    int phys = bt[t0 * S::PPT + e];
+    if (phys < 0 || phys >= A.num_pages) {
+      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+      phys = 0;
+    }
+    pages[e] = phys;
+  }
+  __syncthreads();
+
+  // physical page `lane` of this warp's i-th tile (lanes < PPT)
+  auto page_of = [&](int i) -> const unsigned char* {
+    const int phys = pages[(first + i * W - t0) * S::PPT + lane];
+    return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB;
+  };
+  auto issue_k = [&](int i) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_of(i), S::KP, barK);
+  };
+  auto issue_v = [&](int i) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
+    __syncwarp();
+    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
+  };
+
+  if (lane == 0) {
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
+  }
+  fence_mbar_init();
+  __syncwarp();
+  if (n_my > 0) {
+    issue_k(0);
+    issue_v(0);
+  }
+
+  // ---- rotated, scaled query rows of the row group (unused rows are zero)
+  for (int h = warp; h < 8; h += W) {
+    constexpr int E = D / 32;
+    float v[E];
+    if (h < R.n) {
+      const int hq = kvh * A.G + R.head(A, h), j = R.query(A, h);
+      load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, v);
+      warp_fwht<E>(v);
+      const float sc = A.kappa / sqrtf(static_cast<float>(D));
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] *= sc;
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
+  }
+  __syncthreads();
+
+  float m = -INFINITY, lsum = 0.f;
+  float acc[S::NC][2];
+#pragma unroll
+  for (int nc = 0; nc < S::NC; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
+
+  int i = 0;
+  bool timed_out = false;
+  for (; i < n_my; ++i) {
+    const uint32_t par = i & 1;
+    if (!mbar_wait_bounded(barK, par)) {
+      timed_out = true;
+      break;
+    }
+
+    // -- q~ = q' * c_K as fp16 hi/lo A fragments
+    uint32_t Aq[S::KC][4];
+    float qsum = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < S::KC; ++kc) {
+      const int ch0 = 16 * kc + 2 * t;
+      const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
+      const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
+      const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * SB;
+      const float2 c01 = load_scale2<SB>(cp);
+      const float2 c89 = load_scale2<SB>(cp + 8 * SB);
+      const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
+      qsum += (x0 + x1) + (x8 + x9);
+      split_hi_lo(x0, x1, Aq[kc][0], Aq[kc][1]);
+      split_hi_lo(x8, x9, Aq[kc][2], Aq[kc][3]);
+    }
+    qsum = warp_sum_xor(qsum, 1, 4);
+
+    // -- S = q~ . (K codes - 2^(KB-1)), two pages (four 8-token blocks) at a
+    //    time so that four independent accumulator chains hide the mma
+    //    latency. Per group of four k-chunks a lane's fragments (2 kc + e,
+    //    e the token block) are KW consecutive words of each code plane.
+    float s[S::NB][2];
+#pragma unroll
+    for (int p0 = 0; p0 < S::PPT; p0 += 2) {
+      float d[2][2][4];
+#pragma unroll
+      for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) d[pi][e][0] = d[pi][e][1] = d[pi][e][2] = d[pi][e][3] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < S::KCH; ++ch) {
+        uint32_t x0[2][S::KW0], x1[2][S::KW1 ? S::KW1 : 1];
+#pragma unroll
+        for (int pi = 0; pi < 2; ++pi) {
+          const unsigned char* pg = kslot + (p0 + pi) * S::KP;
+          load_words<S::KW0>(pg + 4 * S::KU0 * (32 * ((ch * S::KW0) / S::KU0) + lane) + 4 * ((ch * S::KW0) % S::KU0),
+                             x0[pi]);
+          if constexpr (S::KW1 != 0)
+            load_words<S::KW1>(pg + S::KR1 + 4 * S::KU1 * (32 * ((ch * S::KW1) / S::KU1) + lane) +
+                                   4 * ((ch * S::KW1) % S::KU1),
+                               x1[pi]);
+        }
+        static_for<0, 8>([&](auto fgc) {
+          constexpr int fg = decltype(fgc)::value;  // fragment 2 w4 + e of the group
+          const int kc = 4 * ch + fg / 2;
+#pragma unroll
+          for (int pi = 0; pi < 2; ++pi) {
+            uint32_t b0, b1;
+            code_pair<KB, fg % S::KF0, fg % S::KF1>(x0[pi][fg / S::KF0], x1[pi][(fg / S::KF1) % (S::KW1 ? S::KW1 : 1)],
+                                                    b0, b1);
+            mma_f16(d[pi][fg % 2], Aq[kc][0], Aq[kc][1], Aq[kc][2], Aq[kc][3], b0, b1);
+          }
+        });
+      }
+#pragma unroll
+      for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          s[2 * (p0 + pi) + e][0] = d[pi][e][0] + d[pi][e][2];
+          s[2 * (p0 + pi) + e][1] = d[pi][e][1] + d[pi][e][3];
+        }
+    }
+
+    // -- row-scale fold and online softmax (base 2)
+    float mt = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      const unsigned char* pg = kslot + (nb >> 1) * S::KP;
+      const int idx = (nb & 1) * 8 + 2 * t;
+      const float2 ka = load_scale2<SB>(pg + PG.k_a() + idx * SB);
+      const float2 kb = load_scale2<SB>(pg + PG.k_b() + idx * SB);
+      s[nb][0] = fmaf(ka.x, s[nb][0], fmaf(S::KCENTER, ka.x, kb.x) * qsum);
+      s[nb][1] = fmaf(ka.y, s[nb][1], fmaf(S::KCENTER, ka.y, kb.y) * qsum);
+      mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
+    }
+    mt = warp_max_xor(mt, 1, 4);
+    const float m_new = fmaxf(m, mt);
+    const float alpha = fast_exp2(m - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) {
+      s[nb][0] = fast_exp2(s[nb][0] - m_new);
+      s[nb][1] = fast_exp2(s[nb][1] - m_new);
+      psum += s[nb][0] + s[nb][1];
+    }
+    lsum = fmaf(lsum, alpha, psum);
+    m = m_new;
+
+    // the K slot is free: start the next tile's K part
+    if (i + 1 < n_my) issue_k(i + 1);
+
+    if (!mbar_wait_bounded(barV, par)) {
+      timed_out = true;
+      break;
+    }
+
+    // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
+    uint32_t Ap[S::PPT][4];
+    float beta = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < S::PPT; ++pp) {
+      const unsigned char* pg = vslot + pp * S::VP;
+      const float2 va0 = load_scale2<SB>(pg + PG.v_a() - S::KP + (2 * t) * SB);
+      const float2 va1 = load_scale2<SB>(pg + PG.v_a() - S::KP + (8 + 2 * t) * SB);
+      const float2 vb0 = load_scale2<SB>(pg + PG.v_b() - S::KP + (2 * t) * SB);
+      const float2 vb1 = load_scale2<SB>(pg + PG.v_b() - S::KP + (8 + 2 * t) * SB);
+      const float p00 = s[2 * pp][0], p01 = s[2 * pp][1], p10 = s[2 * pp + 1][0], p11 = s[2 * pp + 1][1];
+      beta = fmaf(p00, fmaf(S::VCENTER, va0.x, vb0.x), beta);
+      beta = fmaf(p01, fmaf(S::VCENTER, va0.y, vb0.y), beta);
+      beta = fmaf(p10, fmaf(S::VCENTER, va1.x, vb1.x), beta);
+      beta = fmaf(p11, fmaf(S::VCENTER, va1.y, vb1.y), beta);
+      split_hi_lo(p00 * va0.x, p01 * va0.y, Ap[pp][0], Ap[pp][1]);
+      split_hi_lo(p10 * va1.x, p11 * va1.y, Ap[pp][2], Ap[pp][3]);
+    }
+    beta = warp_sum_xor(beta, 1, 4);
+
+#pragma unroll
+    for (int nc = 0; nc < S::NC; ++nc) {
+      acc[nc][0] *= alpha;
+      acc[nc][1] *= alpha;
+    }
+    // channel blocks in groups of eight: the group's fragments are one
+    // unit (VW consecutive words) of each code plane
+#pragma unroll
+    for (int hq = 0; hq < S::VHC; ++hq) {
+      float u[8][4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < S::PPT; ++pp) {
+        uint32_t x0[S::VW0], x1[S::VW1 ? S::VW1 : 1];
+        load_words<S::VW0>(vslot + pp * S::VP + 4 * S::VW0 * (32 * hq + lane), x0);
+        if constexpr (S::VW1 != 0) load_words<S::VW1>(vslot + pp * S::VP + S::VR1 + 4 * S::VW1 * (32 * hq + lane), x1);
+        static_for<0, 8>([&](auto kc_) {
+          constexpr int k = decltype(kc_)::value;
+          uint32_t b0, b1;
+          code_pair<VB, k % S::VF0, k % S::VF1>(x0[k / S::VF0], x1[(k / S::VF1) % (S::VW1 ? S::VW1 : 1)], b0, b1);
+          mma_f16(u[k], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], b0, b1);
+        });
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int nc = 8 * hq + k;
+        const int ch = 8 * nc + 2 * t;
+        const float2 cv = load_scale2<SB>(vslot + (ch / S::CPP) * S::VP + PG.v_col() - S::KP + (ch % S::CPP) * SB);
+        acc[nc][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[nc][0]);
+        acc[nc][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[nc][1]);
+      }
+    }
+    if (i + 1 < n_my) issue_v(i + 1);
+  }
+  if (timed_out) {
+    if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+    // wait (bounded) for the copies this warp still has in flight
+    mbar_wait_bounded(barK, i & 1, 100000000LL);
+    mbar_wait_bounded(barV, i & 1, 100000000LL);
+  }
+  lsum = warp_sum_xor(lsum, 1, 4);
+
+  // ---- merge the W warps of the CTA (scratch aliases the slots)
+  __syncthreads();
+  float* mrg = reinterpret_cast<float*>(smem);
+  float* mw = mrg + warp * 8 * (D + 2);
+  if (t == 0) {
+    mw[g * (D + 2)] = n_my > 0 ? m : -INFINITY;
+    mw[g * (D + 2) + 1] = n_my > 0 ? lsum : 0.f;
+  }
+#pragma unroll
+  for (int nc = 0; nc < S::NC; ++nc) {
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[nc][0];
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[nc][1];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
+    const int gg = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
+    float a = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* r = mrg + (w * 8 + gg) * (D + 2);
+        const float sc = exp2f(r[0] - M);
+        a = fmaf(r[2 + j], sc, a);
+        L = fmaf(r[1], sc, L);
+      }
+    }
+    float* part = part_of(A, D, b, R.query(A, gg), kvh * A.G + R.head(A, gg), split);
+    part[4 + j] = a;
+    if (j == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+  }
+}
+
+template <int D, int N, typename T, int W, int KB, int VB, int SB>
+cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
+  using S = DecShape<D, N, W, KB, VB, SB>;
+  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
+  const int smem = S::SMEM + A.tps * S::PPT * 4;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(A.Hkv * row_groups(A.G, A.Q), A.slots, num_seqs);
+  kern<<<grid, W * 32, smem, st>>>(A);
+  return cudaGetLastError();
+}
+
+// The decode kernels of one (K width, V width, scale bytes) combination;
+// each combination is compiled in its own translation unit.
+template <int KB, int VB, int SB>
+cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int num_seqs, cudaStream_t st);
+
+#define KVARN_DECLARE_WIDTHS(KB, VB, SB)                                                             \
+  template <>                                                                                       \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int num_seqs, \
+                                           cudaStream_t st);
+KVARN_DECLARE_WIDTHS(4, 2, 2)
+KVARN_DECLARE_WIDTHS(2, 2, 2)
+KVARN_DECLARE_WIDTHS(3, 3, 2)
+KVARN_DECLARE_WIDTHS(4, 4, 2)
+KVARN_DECLARE_WIDTHS(5, 5, 2)
+KVARN_DECLARE_WIDTHS(6, 6, 2)
+KVARN_DECLARE_WIDTHS(8, 8, 2)
+#undef KVARN_DECLARE_WIDTHS
+
+#define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \
+  template <>                                                                                           \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int num_seqs,     \
+                                           cudaStream_t st) {                                           \
+    if (D == 128 && N == 128)                                                                           \
+      return bf16 ? run_dense<128, 128, __nv_bfloat16, 4, KB, VB, SB>(A, num_seqs, st)                 \
+                  : run_dense<128, 128, __half, 4, KB, VB, SB>(A, num_seqs, st);                        \
+    if (D == 128 && N == 64)                                                                            \
+      return bf16 ? run_dense<128, 64, __nv_bfloat16, 4, KB, VB, SB>(A, num_seqs, st)                  \
+                  : run_dense<128, 64, __half, 4, KB, VB, SB>(A, num_seqs, st);                         \
+    return cudaErrorInvalidValue;                                                                       \
+  }
+
+}  // namespace kvarn

@@ -1,0 +1,606 @@
+// KVarN tile encoder for sm_103a.
+//
+// KVarN review ("KVarN ... vLLM KV cache quantization"), four-stage
+// paragraph: rotate each tile by an orthonormal Hadamard matrix across the
+// channels, run T alternating column/row standard-deviation normalisations,
+// then asymmetric round-to-nearest with the scales folded into the stored
+// row offsets. One CTA (or a cluster of two for head_dim 512) owns one N x D
+// tile and keeps it in registers: every thread holds a 16-channel segment of
+// N/32 token rows. The Hadamard transform runs as four in-register butterfly
+// stages and log2(D/16) lane shuffles. Column statistics reduce through
+// shared memory (and the peer CTA's shared memory in a cluster) and are
+// finished once per channel by thread `channel`, which broadcasts the result;
+// row statistics reduce with shuffles. The scales accumulate as products of
+// the per-pass standard deviations (the exponential of the summed logs, up
+// to rounding). Codes are packed in registers straight into the page's word
+// order, staged in shared memory and written out in 16-byte stores.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "kvarn_common.cuh"
+#include "kvarn_launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace kvarn {
+
+// Cluster size 2 splits the tile's rows over two CTAs (head_dim 512, where a
+// whole 128 x 512 fp32 tile would not fit one CTA's registers).
+template <int D, int N, int CS, bool GEN = false>
+struct EncShape {
+  static constexpr int NT = 2 * D / CS;       // threads per CTA
+  static constexpr int TPR = D / 16;          // threads per token row
+  static constexpr int RPW = 32 / TPR;        // rows per warp and pass
+  static constexpr int NW = NT / 32;          // warps
+  static constexpr int ROWS = N / CS;         // rows owned by this CTA
+  static constexpr int RPT = N / 32;          // rows per thread
+  static constexpr int PPC = ROWS / kPageTokens;  // pages per CTA
+  static_assert(ROWS == RPT * NW * RPW, "tile rows must cover the CTA");
+  static_assert(NT >= D, "one thread per channel finishes the column statistics");
+  static constexpr int RED_BYTES = NW * D * 4;
+  // packed words (4-bit K / 2-bit V); the generic path stages one byte per
+  // code plus the packed image of up to 8 bits per code
+  static constexpr int CODE_BYTES = GEN ? 2 * ROWS * D : ROWS * D / 2;
+  static constexpr int SCRATCH = RED_BYTES > CODE_BYTES ? RED_BYTES : CODE_BYTES;
+  // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][D] | pages[PPC]
+  static constexpr int OFF_COLBUF = SCRATCH;
+  static constexpr int OFF_ROWA = OFF_COLBUF + 4 * D;
+  static constexpr int OFF_ROWB = OFF_ROWA + 4 * ROWS;
+  static constexpr int OFF_COLC = OFF_ROWB + 4 * ROWS;
+  static constexpr int OFF_COLPART = OFF_COLC + 4 * D;
+  static constexpr int OFF_PAGES = OFF_COLPART + 8 * D;
+  static constexpr int SMEM = OFF_PAGES + 8 * PPC;
+};
+
+struct EncodeArgs {
+  const void* x[2];        // K, V (dense) or latent (x[0])
+  const __half* rope;      // latent only
+  int64_t seq_stride, head_stride, rope_seq_stride;
+  int32_t chunk_tiles;
+  int32_t num_seqs;
+  const int32_t* tile_start;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  uint8_t* cache;
+  int64_t num_pages;
+  int32_t num_kv_heads;
+  int32_t page_bytes;
+  int32_t norm_iters;
+  int32_t rope_dim;
+  uint32_t* err;
+};
+
+// Column statistic: every thread passes its 16 per-channel partial sums over
+// its rows. Returns, in thread tid < D, the sum over the whole tile (both
+// CTAs of a cluster) for channel tid; other threads get 0. colpart is the
+// buffer of this statistic (callers alternate two), so that one cluster
+// barrier per statistic keeps a fast CTA from overwriting a partial that its
+// peer has not read yet.
+template <int D, int N, int CS>
+__device__ __forceinline__ float column_total(float (&s)[16], float* red, float* colpart) {
+  using S = EncShape<D, N, CS>;  // the statistics part of the shape does not depend on GEN
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, seg = lane % S::TPR;
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+#pragma unroll
+    for (int o = S::TPR; o < 32; o <<= 1) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
+  if (lane < S::TPR) {
+    float4* dst = reinterpret_cast<float4*>(red + warp * D + seg * 16);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
+  }
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x < D) {
+#pragma unroll 8
+    for (int w = 0; w < S::NW; ++w) t += red[w * D + threadIdx.x];
+  }
+  if constexpr (CS > 1) {
+    cg::cluster_group cl = cg::this_cluster();
+    if (threadIdx.x < D) colpart[threadIdx.x] = t;
+    cl.sync();
+    if (threadIdx.x < D) {
+      const float other = cl.map_shared_rank(colpart, cl.block_rank() ^ 1)[threadIdx.x];
+      // both CTAs add in rank order, so they hold bit-identical sums
+      t = cl.block_rank() == 0 ? t + other : other + t;
+    }
+  }
+  return t;
+}
+
+// Reads the 16 broadcast per-channel values of this thread's segment.
+template <int D>
+__device__ __forceinline__ void read_segment(float (&v)[16], const float* colbuf, int seg) {
+  const float4* src = reinterpret_cast<const float4*>(colbuf + seg * 16);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 f = src[e];
+    v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
+  }
+}
+
+// Population std; 1 for a numerically constant vector (std <= 2^-20 |mean|,
+// which covers the rounding residue of an exactly constant one) or a
+// non-finite std.
+__device__ __forceinline__ float safe_sigma(float var, float mean) {
+  const float s = sqrtf(var);
+  return (isfinite(s) && s > 9.5367431640625e-07f * fabsf(mean)) ? s : 1.f;
+}
+
+// Latent page word order (before the 16-byte unit swizzle): the 32-bit word
+// tau * (D/8) + t * (D/32) + w of token tau holds, at nibbles 0,1,4,5, the
+// codes of channels 2t, 2t+8, 2t+1, 2t+9 of 16-channel segment 2w and, at
+// nibbles 2,3,6,7, the same channels of segment 2w+1 (the B-fragment order
+// of an m16n8k16 mma). `P` holds the row's 16 codes of one segment as bytes;
+// returns this segment's nibbles of word t, placed for segment parity `s`.
+__device__ __forceinline__ uint32_t k_word_part(const uint32_t (&P)[4], int t, int s) {
+  const uint32_t v = __byte_perm(P[t >> 1], P[2 + (t >> 1)], (t & 1) ? 0x7362 : 0x5140);
+  return ((v | (v >> 4)) & 0x00FF00FFu) << (8 * s);
+}
+
+// Encodes rows [0, N) of `src` as logical tile `tile` of sequence b (u: the
+// tile's index in the chunk, for the latent rope rows). With last_row set,
+// row N - 1 comes from last_row instead of src (the newest token, appended
+// in the same launch).
+// KIND 0: a dense tile, SIDE_V selecting its V (else K) part of pages of code
+// widths KB, VB and SB-byte scales; KIND 1: a latent tile (4-bit, fp32).
+template <int D, int N, int CS, int BITS, int KIND, typename T, bool SIDE_V = false, int KB = 4, int VB = 2,
+          int SB = 4>
+__device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __restrict__ src,
+                                            int b, int head, int u, int64_t tile, const T* last_row,
+                                            unsigned char* smem) {
+  constexpr bool IS_V = KIND == 0 && SIDE_V;
+  // the 4-bit K and 2-bit V placements pack in registers; other widths take
+  // the generic plane path
+  constexpr bool GEN = KIND == 0 && !(SIDE_V ? BITS == 2 : BITS == 4);
+  using S = EncShape<D, N, CS, GEN>;
+  constexpr DensePage PGE{D, N, KB, VB, SB};
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seg = lane % S::TPR, rsub = lane / S::TPR;
+  int crank = 0;
+  if constexpr (CS > 1) crank = static_cast<int>(cg::this_cluster().block_rank());
+
+  float* red = reinterpret_cast<float*>(smem);
+  unsigned char* stage = smem;  // aliases red once the statistics are done
+  float* colbuf = reinterpret_cast<float*>(smem + S::OFF_COLBUF);
+  float* rowA = reinterpret_cast<float*>(smem + S::OFF_ROWA);
+  float* rowB = reinterpret_cast<float*>(smem + S::OFF_ROWB);
+  float* colC = reinterpret_cast<float*>(smem + S::OFF_COLC);
+  float* colpart = reinterpret_cast<float*>(smem + S::OFF_COLPART);
+  uint8_t** pages = reinterpret_cast<uint8_t**>(smem + S::OFF_PAGES);
+
+  // ---- load. Dense tiles: thread group j = warp*RPW + rsub (0..31) holds
+  // tokens j%8 and j%8 + 8 of RPT/2 pages, so that the two tokens sharing a
+  // packed byte of the dense page are in one thread. Latent tiles: row
+  // i*32 + j of this CTA's rows.
+  float x[S::RPT][16];
+  auto local_row = [&](int i) -> int {
+    const int j = warp * S::RPW + rsub;
+    if constexpr (KIND == 0)
+      return kPageTokens * ((S::RPT / 2) * (j >> 3) + (i >> 1)) + (j & 7) + 8 * (i & 1);
+    else
+      return i * (S::NW * S::RPW) + j;
+  };
+  static_assert(KIND != 0 || (S::NW * S::RPW == 32 && S::RPT % 2 == 0), "dense row pairing");
+#pragma unroll
+  for (int i = 0; i < S::RPT; ++i) {
+    const int r = crank * S::ROWS + local_row(i);
+    const T* p = (last_row != nullptr && r == N - 1) ? last_row + seg * 16 : src + static_cast<int64_t>(r) * D + seg * 16;
+    load8<T>(p, x[i]);
+    load8<T>(p + 8, x[i] + 8);
+  }
+
+  // ---- page addresses of this CTA's rows (read by the stores at the end)
+  constexpr int PPT = N / kPageTokens;  // pages per tile
+  if (tid < S::PPC) {
+    const int64_t lp = tile * PPT + crank * S::PPC + tid;
+    uint8_t* pg = nullptr;
+    const int32_t phys =
+        (lp >= 0 && lp < A.bt_stride) ? A.block_table[static_cast<int64_t>(b) * A.bt_stride + lp] : -1;
+    if (phys >= 0 && phys < A.num_pages)
+      pg = A.cache + (static_cast<int64_t>(phys) * A.num_kv_heads + head) * A.page_bytes;
+    else
+      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+    pages[tid] = pg;
+  }
+
+  // ---- Hadamard: 4 in-register stages, then lane butterflies, then 1/sqrt(D)
+#pragma unroll
+  for (int i = 0; i < S::RPT; ++i) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (!(e & h)) {
+          float a = x[i][e], c = x[i][e + h];
+          x[i][e] = a + c;
+          x[i][e + h] = a - c;
+        }
+  }
+#pragma unroll
+  for (int d = 1; d < S::TPR; d <<= 1) {
+    // lower lane: x + partner; upper lane: partner - x  (one FFMA either way)
+    const float sgn = (lane & d) ? -1.f : 1.f;
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] = fmaf(sgn, x[i][e], __shfl_xor_sync(0xffffffffu, x[i][e], d));
+  }
+  {
+    const float rsd = 1.f / sqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= rsd;
+  }
+
+  // ---- variance normalisation, T iterations of (column pass, row pass)
+  float cscale = 1.f;  // column scale of channel tid (tid < D)
+  float rscale[S::RPT];
+#pragma unroll
+  for (int i = 0; i < S::RPT; ++i) rscale[i] = 1.f;
+  const float invN = 1.f / N, invD = 1.f / D;
+
+#pragma unroll 1
+  for (int it = 0; it < A.norm_iters; ++it) {
+    float s[16];
+    // column means
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < S::RPT; ++i) t += x[i][e];
+      s[e] = t;
+    }
+    const float cmean = column_total<D, N, CS>(s, red, colpart) * invN;
+    if (tid < D) colbuf[tid] = cmean;
+    __syncthreads();
+    float mean[16];
+    read_segment<D>(mean, colbuf, seg);
+    // column variances about the mean
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < S::RPT; ++i) {
+        const float dv = x[i][e] - mean[e];
+        t = fmaf(dv, dv, t);
+      }
+      s[e] = t;
+    }
+    const float cvar = column_total<D, N, CS>(s, red, colpart + D) * invN;
+    __syncthreads();  // every thread has read the means out of colbuf
+    if (tid < D) {
+      const float sig = safe_sigma(cvar, cmean);
+      cscale *= sig;
+      colbuf[tid] = 1.f / sig;
+    }
+    __syncthreads();
+    float inv[16];
+    read_segment<D>(inv, colbuf, seg);
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= inv[e];
+    // row pass: a row lives in TPR consecutive lanes
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i) {
+      float t = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) t += x[i][e];
+      t = warp_sum_xor(t, 1, S::TPR);
+      const float m = t * invD;
+      float v = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float dv = x[i][e] - m;
+        v = fmaf(dv, dv, v);
+      }
+      v = warp_sum_xor(v, 1, S::TPR);
+      const float sig = safe_sigma(v * invD, m);
+      rscale[i] *= sig;
+      const float ri = 1.f / sig;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= ri;
+    }
+    __syncthreads();  // colbuf is rewritten by the next iteration
+  }
+
+  // ---- asymmetric RTN per row: codes as bytes, Pc[i][k] byte e = channel 4k + e
+  constexpr int QMAX = (1 << BITS) - 1;
+  uint32_t Pc[S::RPT][4];
+#pragma unroll
+  for (int i = 0; i < S::RPT; ++i) {
+    float lo = x[i][0], hi = x[i][0];
+#pragma unroll
+    for (int e = 1; e < 16; ++e) {
+      lo = fminf(lo, x[i][e]);
+      hi = fmaxf(hi, x[i][e]);
+    }
+#pragma unroll
+    for (int o = 1; o < S::TPR; o <<= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const float delta = (hi - lo) / static_cast<float>(QMAX);
+    const float rinv = delta > 0.f ? 1.f / delta : 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // x - lo lies in [0, hi - lo], so the rounded quotient lies in
+        // [0, QMAX]; the unsigned conversion saturates and min() only
+        // guards non-finite input
+        const uint32_t q = min(__float2uint_rn((x[i][4 * k + e] - lo) * rinv), static_cast<uint32_t>(QMAX));
+        word |= q << (8 * e);
+      }
+      Pc[i][k] = word;
+    }
+    if (seg == 0) {
+      const int r = local_row(i);
+      rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
+      rowB[r] = rscale[i] * lo;
+    }
+  }
+
+  // ---- codes packed into the page's word order in `stage`
+  const int s_par = seg & 1, w_pair = seg >> 1;
+  if constexpr (KIND == 1) {
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i) {
+      const int r = local_row(i);
+      const int pg = r / kPageTokens, tau = r % kPageTokens;
+      // each lane pair shares words; the even lane writes t = 0, 1, the odd lane t = 2, 3
+      uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D + tau * (D / 8);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t lo_t = k_word_part(Pc[i], j, s_par), hi_t = k_word_part(Pc[i], 2 + j, s_par);
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, s_par ? lo_t : hi_t, 1);
+        const int t = 2 * s_par + j;
+        // 16-byte units 4q + t, XOR 4 on odd tokens
+        const int word = 4 * ((4 * (w_pair >> 2) + t) ^ (4 * (tau & 1))) + (w_pair & 3);
+        img[word] = (s_par ? hi_t : lo_t) | other;
+      }
+    }
+  } else if constexpr (GEN) {
+    // stage the codes as bytes [ROWS][D], then build every plane word
+    unsigned char* cb = stage;
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+      *reinterpret_cast<uint4*>(cb + local_row(i) * D + seg * 16) = make_uint4(Pc[i][0], Pc[i][1], Pc[i][2], Pc[i][3]);
+    __syncthreads();
+    constexpr int W0 = plane_w0(BITS), W1 = plane_w1(BITS);
+    constexpr int WPP = D * BITS / 2;  // 32-bit words of codes per page
+    uint32_t* img = reinterpret_cast<uint32_t*>(stage + S::ROWS * D);
+    for (int ws = tid; ws < S::PPC * WPP; ws += S::NT) {
+      const int pg = ws / WPP, rem = ws % WPP;
+      const bool p1 = rem >= D * W0 / 2;
+      const int w = p1 ? W1 : W0, shift = p1 ? W0 : 0, wi = p1 ? rem - D * W0 / 2 : rem;
+      const int U = IS_V ? w : min(4, D * w / 64);
+      const int L = (wi % (32 * U)) / U, i = (wi / (32 * U)) * U + wi % U;
+      const int g = L >> 2, t = L & 3, F = 8 / w;
+      uint32_t word = 0;
+      for (int f = 0; f < F; ++f) {
+        const int fg = i * F + f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ep = 0; ep < 2; ++ep) {
+            const int ch = IS_V ? 8 * fg + g : 16 * (fg >> 1) + 2 * t + ep + 8 * h;
+            const int tok = IS_V ? 2 * t + ep + 8 * h : 8 * (fg & 1) + g;
+            const uint32_t field = (cb[(pg * kPageTokens + tok) * D + ch] >> shift) & ((1u << w) - 1u);
+            word |= field << (w * f + 8 * h + 16 * ep);
+          }
+      }
+      img[ws] = word;
+    }
+  } else {
+    const int j = warp * S::RPW + rsub, g = j & 7;
+#pragma unroll
+    for (int ip = 0; ip < S::RPT / 2; ++ip) {
+      const int pg = (S::RPT / 2) * (j >> 3) + ip;
+      const uint32_t* P0 = Pc[2 * ip];      // token g of the page
+      const uint32_t* P1 = Pc[2 * ip + 1];  // token g + 8
+      if constexpr (!IS_V) {
+        // 4-bit: word (kc = seg, lane 4g + t) bytes = channels 2t, 2t+8,
+        // 2t+1, 2t+9; token g in the low nibble, token g + 8 in the high one
+        uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+          const uint32_t w0 = __byte_perm(P0[t >> 1], P0[2 + (t >> 1)], sel);
+          const uint32_t w1 = __byte_perm(P1[t >> 1], P1[2 + (t >> 1)], sel);
+          img[((seg >> 2) * 32 + 4 * g + t) * 4 + (seg & 3)] = w0 | (w1 << 4);
+        }
+      } else {
+        // 2-bit: channel 16 seg + g' (block 2 seg) and 16 seg + 8 + g' (block
+        // 2 seg + 1) of this token land at bits 2c, c = 2 (seg % 2) + {0, 1},
+        // of byte h + 2e of word (w = seg / 2, lane 4 g' + t); this thread's
+        // two tokens are h = 0 and h = 1. Byte g' of A/B: channel g' | g'+8 << 2.
+        uint32_t A0 = P0[0] | (P0[2] << 2), B0 = P0[1] | (P0[3] << 2);
+        uint32_t A1 = P1[0] | (P1[2] << 2), B1 = P1[1] | (P1[3] << 2);
+        const uint32_t oA0 = __shfl_xor_sync(0xffffffffu, A0, 1), oB0 = __shfl_xor_sync(0xffffffffu, B0, 1);
+        const uint32_t oA1 = __shfl_xor_sync(0xffffffffu, A1, 1), oB1 = __shfl_xor_sync(0xffffffffu, B1, 1);
+        if (s_par == 0) {
+          A0 |= oA0 << 4; B0 |= oB0 << 4; A1 |= oA1 << 4; B1 |= oB1 << 4;
+          const int tau = g, t = tau >> 1, e = tau & 1, w = w_pair;
+          uint16_t* img = reinterpret_cast<uint16_t*>(stage) + pg * 2 * D;
+          // halfword of channel g' = (byte of token g, byte of token g + 8)
+          const uint32_t hw[4] = {__byte_perm(A0, A1, 0x5140), __byte_perm(A0, A1, 0x7362),
+                                  __byte_perm(B0, B1, 0x5140), __byte_perm(B0, B1, 0x7362)};
+#pragma unroll
+          for (int gg = 0; gg < 8; ++gg) {
+            const int word = ((w >> 1) * 32 + 4 * gg + t) * 2 + (w & 1);
+            img[2 * word + e] = static_cast<uint16_t>(hw[gg >> 1] >> (16 * (gg & 1)));
+          }
+        }
+      }
+    }
+  }
+  if (tid < D) colC[tid] = cscale;
+  __syncthreads();
+
+  // ---- codes: 16-byte stores of the staged page words
+  {
+    constexpr int CPP = 2 * D * BITS / 16;  // 16-byte chunks per page
+    const int base = IS_V ? PGE.v_codes() : 0;
+    const uint4* img = reinterpret_cast<const uint4*>(stage + (GEN ? S::ROWS * D : 0));
+    for (int c = tid; c < S::PPC * CPP; c += S::NT) {
+      uint8_t* pg = pages[c / CPP];
+      if (pg) reinterpret_cast<uint4*>(pg + base)[c % CPP] = img[c];
+    }
+  }
+
+  // ---- scales
+  int off_a, off_b, off_c;
+  if constexpr (KIND == 1) {
+    constexpr LatentPage L(D, 64, N);
+    off_a = L.a(); off_b = L.b(); off_c = L.col();
+  } else {
+    off_a = IS_V ? PGE.v_a() : PGE.k_a();
+    off_b = IS_V ? PGE.v_b() : PGE.k_b();
+    off_c = IS_V ? PGE.v_col() : PGE.k_col();
+  }
+  auto put = [&](uint8_t* at, int idx, float x) {
+    if constexpr (SB == 4) reinterpret_cast<float*>(at)[idx] = x;
+    else reinterpret_cast<__half*>(at)[idx] = __float2half_rn(x);
+  };
+  if (tid < S::ROWS) {
+    uint8_t* pg = pages[tid / kPageTokens];
+    if (pg) {
+      put(pg + off_a, tid % kPageTokens, rowA[tid]);
+      put(pg + off_b, tid % kPageTokens, rowB[tid]);
+    }
+  }
+  {
+    constexpr int C = D * kPageTokens / N;  // column scales per page
+    for (int j = tid; j < S::PPC * C; j += S::NT) {
+      uint8_t* pg = pages[j / C];
+      if (pg) put(pg + off_c, j % C, colC[(crank * S::PPC) * C + j]);
+    }
+  }
+  if constexpr (KIND == 1) {
+    // rope rows, fp16, copied as is
+    constexpr LatentPage L(D, 64, N);
+    const int R = A.rope_dim;
+    const int vec_per_page = kPageTokens * R * 2 / 16;
+    for (int c = tid; c < S::PPC * vec_per_page; c += S::NT) {
+      const int p = c / vec_per_page, k = c % vec_per_page;
+      uint8_t* pg = pages[p];
+      if (!pg) continue;
+      const int row = crank * S::ROWS + p * kPageTokens;  // first token of the page in the tile
+      const uint8_t* s = reinterpret_cast<const uint8_t*>(
+          A.rope + static_cast<int64_t>(b) * A.rope_seq_stride + (static_cast<int64_t>(u) * N + row) * R);
+      reinterpret_cast<uint4*>(pg + L.rope())[k] = __ldg(reinterpret_cast<const uint4*>(s) + k);
+    }
+  }
+}
+
+// K (4-bit) and V (2-bit) tiles share one launch: blockIdx.z < num_seqs
+// encodes K, the rest V, so that the K half of a large grid runs before the
+// V half and an SM mostly runs one of the two code paths.
+template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
+__global__ void __launch_bounds__(2 * D) encode_dense_kernel(EncodeArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
+  const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);
+  if (A.tile_start[b] < 0) return;  // nothing to commit for this sequence (uniform per CTA)
+  const int64_t off = static_cast<int64_t>(b) * A.seq_stride + static_cast<int64_t>(head) * A.head_stride +
+                      static_cast<int64_t>(u) * N * D;
+  if (is_v)
+    encode_tile<D, N, 1, VB, 0, T, true, KB, VB, SB>(A, static_cast<const T*>(A.x[1]) + off, b, head, u,
+                                                     A.tile_start[b] + u, nullptr, smem);
+  else
+    encode_tile<D, N, 1, KB, 0, T, false, KB, VB, SB>(A, static_cast<const T*>(A.x[0]) + off, b, head, u,
+                                                      A.tile_start[b] + u, nullptr, smem);
+}
+
+template <typename T>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
+    encode_latent_kernel(EncodeArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int u = blockIdx.x >> 1, b = blockIdx.y;
+  if (A.tile_start[b] < 0) return;  // uniform over the cluster: both CTAs share b
+  const T* src = static_cast<const T*>(A.x[0]) + static_cast<int64_t>(b) * A.seq_stride +
+                 static_cast<int64_t>(u) * 128 * 512;
+  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, A.tile_start[b] + u, nullptr, smem);
+}
+
+// Fused append + commit (one launch per decode step): x[0] / x[1] hold each
+// (sequence, KV head)'s newest K / V token, at position seq_lens[b] - 1. A
+// token that does not complete a tile goes to its row of the raw tail; one
+// that does completes the tile in the tail's rows 0..N-2 and the tile is
+// encoded straight into its pages (the tail then holds nothing). The tail
+// rows read here were written by earlier launches.
+template <int D, int N, typename T>
+__global__ void __launch_bounds__(2 * D) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
+                                                              int32_t max_seq_len, T* tail_k, T* tail_v) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const bool is_v = blockIdx.z == 1;
+  const int head = blockIdx.x, b = blockIdx.y;
+  const int L = seq_lens[b];
+  if (L <= 0 || L > max_seq_len) {  // nothing appended (0) or an invalid length
+    if (L != 0 && threadIdx.x == 0 && !is_v && head == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    return;
+  }
+  const int64_t hs = static_cast<int64_t>(b) * A.num_kv_heads + head;
+  const T* tok = static_cast<const T*>(A.x[is_v]) + hs * D;
+  T* tail = (is_v ? tail_v : tail_k) + hs * N * D;
+  if (L % N != 0) {
+    const int row = (L - 1) % N;
+    for (int i = threadIdx.x; i < D / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(tail + static_cast<int64_t>(row) * D)[i] = reinterpret_cast<const uint4*>(tok)[i];
+    return;
+  }
+  if (is_v)
+    encode_tile<D, N, 1, 2, 0, T, true>(A, tail, b, head, 0, L / N - 1, tok, smem);
+  else
+    encode_tile<D, N, 1, 4, 0, T, false>(A, tail, b, head, 0, L / N - 1, tok, smem);
+}
+
+// ------------------------------------------------------------- launchers
+template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
+cudaError_t launch_dense(const EncodeArgs& A, cudaStream_t st) {
+  constexpr bool gen = !(KB == 4 && VB == 2);
+  constexpr int smem = gen ? EncShape<D, N, 1, true>::SMEM : EncShape<D, N, 1>::SMEM;
+  auto kern = encode_dense_kernel<D, N, T, KB, VB, SB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(A.chunk_tiles, A.num_kv_heads, 2 * A.num_seqs);
+  kern<<<grid, 2 * D, smem, st>>>(A);
+  return cudaGetLastError();
+}
+
+// The dense encode kernels of one (K width, V width, scale bytes)
+// combination (head_dim 128); each combination compiles in its own
+// translation unit.
+template <int KB, int VB, int SB>
+cudaError_t launch_encode_widths(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+
+#define KVARN_DECLARE_ENC_WIDTHS(KB, VB, SB) \
+  template <>                                \
+  cudaError_t launch_encode_widths<KB, VB, SB>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+KVARN_DECLARE_ENC_WIDTHS(4, 2, 2)
+KVARN_DECLARE_ENC_WIDTHS(2, 2, 2)
+KVARN_DECLARE_ENC_WIDTHS(3, 3, 2)
+KVARN_DECLARE_ENC_WIDTHS(4, 4, 2)
+KVARN_DECLARE_ENC_WIDTHS(5, 5, 2)
+KVARN_DECLARE_ENC_WIDTHS(6, 6, 2)
+KVARN_DECLARE_ENC_WIDTHS(8, 8, 2)
+#undef KVARN_DECLARE_ENC_WIDTHS
+
+#define KVARN_ENCODE_WIDTHS(KB, VB, SB)                                                                \
+  template <>                                                                                          \
+  cudaError_t launch_encode_widths<KB, VB, SB>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st) { \
+    if (N == 128)                                                                                      \
+      return bf16 ? launch_dense<128, 128, __nv_bfloat16, KB, VB, SB>(A, st)                          \
+                  : launch_dense<128, 128, __half, KB, VB, SB>(A, st);                                 \
+    if (N == 64)                                                                                       \
+      return bf16 ? launch_dense<128, 64, __nv_bfloat16, KB, VB, SB>(A, st)                           \
+                  : launch_dense<128, 64, __half, KB, VB, SB>(A, st);                                  \
+    return cudaErrorInvalidValue;                                                                      \
+  }
+
+}  // namespace kvarn

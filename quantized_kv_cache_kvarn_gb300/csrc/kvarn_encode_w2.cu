@@ -1,0 +1,6 @@
+// Encode kernels for code widths K2 / V2 with fp16 scales (head_dim 128).
+#include "kvarn_encode_kernel.cuh"
+
+namespace kvarn {
+KVARN_ENCODE_WIDTHS(2, 2, 2)
+}  // namespace kvarn

@@ -19,7 +19,16 @@ struct EncodeParams {
   int32_t num_kv_heads, D, N, norm_iters;
   bool bf16;
   uint32_t* err;
+  int32_t k_bits, v_bits, scale_bytes;  // 4, 2, 4 for the k4v2 preset with fp32 scales
 };
+
+// Code widths and scale sizes with compiled kernels: (4, 2) with fp32 or
+// fp16 scales for every head_dim and tile; (b, b), b in {2, 3, 4, 5, 6, 8},
+// with fp16 scales for head_dim 128.
+inline bool widths_supported(int32_t D, int32_t kb, int32_t vb, int32_t sb) {
+  if (kb == 4 && vb == 2) return sb == 4 || sb == 2;
+  return D == 128 && sb == 2 && kb == vb && (kb == 2 || kb == 3 || kb == 4 || kb == 5 || kb == 6 || kb == 8);
+}
 
 struct AppendParams {
   const void* k;  // newest token per (sequence, KV head): [B][Hkv][D]
@@ -81,6 +90,7 @@ struct DecodeParams {
   int32_t recent_tokens;  // dense: newest accepted tokens kept raw (0: none)
   const void* sink_k;   // dense: [B][Hkv][sink_tokens][D]
   const void* sink_v;
+  int32_t k_bits, v_bits, scale_bytes;  // dense code widths and scale size (0: the k4v2 preset, fp32)
 };
 
 // (query head, query token) row groups of eight per KV head.

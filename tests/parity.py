@@ -9,7 +9,10 @@ Tolerances (from the problem statement of this codec):
     times the row's std; with delta >= range/15 that moves x by at most
     ~2e-5 code units. CODE_BAND = 2^-13 (1.2e-4) leaves a 5x margin;
   * scales a, b, c to relative 1e-5 (b relative to the larger of |b| and
-    the row range |a| (2^bits - 1), its natural scale);
+    the row range |a| (2^bits - 1), its natural scale); with fp16 scales in
+    the page, one fp16 step (relative 2^-10): the GPU rounds its fp32 value,
+    the oracle its float64 one, and the two may fall either side of a
+    rounding point;
   * attention output to max abs 2e-3 (fp32 accumulation).
 """
 from __future__ import annotations
@@ -28,7 +31,7 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def compare_tile(gpu: dict, ref: dict, bits: int, stats: dict):
+def compare_tile(gpu: dict, ref: dict, bits: int, stats: dict, sb: int = 4):
     """gpu: codes/a/b/c read back from the GPU pages; ref: oracle encode_tile."""
     mism = gpu["codes"] != ref["codes"]
     if mism.any():
@@ -44,9 +47,10 @@ def compare_tile(gpu: dict, ref: dict, bits: int, stats: dict):
     stats["mismatch"] += int(mism.sum())
     stats["codes"] += mism.size
     qmax = (1 << bits) - 1
-    ref_a = ref["a"].astype(np.float32).astype(np.float64)
+    dt = np.float32 if sb == 4 else np.float16
+    ref_a = ref["a"].astype(dt).astype(np.float64)
     for key in ("a", "b", "c"):
-        g, r = gpu[key], ref[key].astype(np.float32).astype(np.float64)
+        g, r = gpu[key], ref[key].astype(dt).astype(np.float64)
         denom = np.abs(r)
         if key == "b":
             # the row offset lives on the row's quantisation grid: its scale is
@@ -54,6 +58,8 @@ def compare_tile(gpu: dict, ref: dict, bits: int, stats: dict):
             # is zero up to rounding (a constant row after rotation)
             denom = np.maximum(denom, np.abs(ref_a) * qmax)
         rel = np.abs(g - r) / np.maximum(denom, 1e-30)
+        if sb == 2:
+            rel = rel * SCALE_RTOL / 2.0 ** -10  # one fp16 step maps onto the fp32 tolerance
         stats["scale_rel"] = max(stats["scale_rel"], float(rel.max()))
 
 
@@ -61,11 +67,11 @@ def new_stats():
     return dict(mismatch=0, codes=0, within_1ulp=0, max_dist=0.0, scale_rel=0.0)
 
 
-def check_dense_pages(cache_gpu: np.ndarray, k, v, bt, lens, N, D, heads=None, T=2):
+def check_dense_pages(cache_gpu: np.ndarray, k, v, bt, lens, N, D, heads=None, T=2, kb=4, vb=2, sb=4):
     """Compare every committed tile of the listed (b, kvh) pairs (all when
     None) of a GPU-written dense cache with the oracle's encoding of the same
     inputs. k, v: float64 [B, Hkv, L, D]."""
-    lay = layout.DenseLayout(D, N)
+    lay = layout.DenseLayout(D, N, kb, vb, sb)
     B, Hkv = k.shape[:2]
     ppt = N // 16
     stats_k, stats_v = new_stats(), new_stats()
@@ -74,18 +80,18 @@ def check_dense_pages(cache_gpu: np.ndarray, k, v, bt, lens, N, D, heads=None, T
         for t in range(int(lens[b]) // N):
             pages = [int(bt[b][t * ppt + p]) for p in range(ppt)]
             gk, gv = layout.read_tile(cache_gpu, lay, pages, h)
-            rk = codec.encode_tile(k[b, h, t * N:(t + 1) * N], 4, T)
-            rv = codec.encode_tile(v[b, h, t * N:(t + 1) * N], 2, T)
-            compare_tile(gk, rk, 4, stats_k)
-            compare_tile(gv, rv, 2, stats_v)
+            rk = codec.encode_tile(k[b, h, t * N:(t + 1) * N], kb, T)
+            rv = codec.encode_tile(v[b, h, t * N:(t + 1) * N], vb, T)
+            compare_tile(gk, rk, kb, stats_k, sb)
+            compare_tile(gv, rv, vb, stats_v, sb)
     for st in (stats_k, stats_v):
         assert st["scale_rel"] <= SCALE_RTOL, st
         assert st["mismatch"] <= max(4, 1e-3 * st["codes"]), st
     return stats_k, stats_v
 
 
-def oracle_dense_cache(k, v, bt, lens, N, D, num_pages, T=2):
-    lay = layout.DenseLayout(D, N)
+def oracle_dense_cache(k, v, bt, lens, N, D, num_pages, T=2, kb=4, vb=2, sb=4):
+    lay = layout.DenseLayout(D, N, kb, vb, sb)
     B, Hkv = k.shape[:2]
     cache = np.zeros((num_pages, Hkv, lay.page_bytes), np.uint8)
     for b in range(B):

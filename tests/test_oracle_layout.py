@@ -111,3 +111,85 @@ def test_write_read_tile_roundtrip():
         np.testing.assert_array_equal(got["codes"], enc["codes"])
         for key in "abc":
             np.testing.assert_array_equal(got[key], enc[key].astype(np.float32).astype(np.float64))
+
+
+# ------------------------------------------------ other widths (code planes)
+def test_plane_positions_hand_derived():
+    """D = 128. K plane: lane 4g + t, fragment 2kc + e, 8/w fragments per word,
+    units of min(4, 2w) words; V plane: fragment nc, units of w words; bit
+    w*f + 8h + 16e' (see the layout module)."""
+    cases = {
+        # (side, w, tau, j): (byte, shift)
+        ("k", 1, 0, 0): (0, 0),
+        ("k", 1, 9, 0): (32, 1),      # g1 t0 -> lane 4, e1 -> fragment 1 of word 0; units of 2 words (8 B)
+        ("k", 1, 0, 112): (4, 6),     # kc7 -> fragment 14 = word 1, slot 6
+        ("k", 1, 7, 127): (255, 6),   # lane 31, fragment 14, h1 e'1 -> bit 30
+        ("k", 2, 8, 0): (0, 2),       # e1 -> slot 1
+        ("k", 2, 0, 16): (0, 4),      # kc1 -> slot 2
+        ("k", 2, 0, 32): (4, 0),      # kc2 -> word 1
+        ("k", 2, 15, 127): (511, 6),  # lane 31, fragment 15 = word 3 slot 3, bit 30
+        ("v", 1, 0, 8): (0, 1),       # block 1 -> slot 1
+        ("v", 1, 8, 0): (1, 0),       # h1 -> bit 8
+        ("v", 1, 1, 0): (2, 0),       # e'1 -> bit 16
+        ("v", 1, 2, 3): (52, 0),      # t1 g3 -> lane 13, 4-byte units
+        ("v", 1, 15, 127): (255, 7),  # block 15 = word 1 slot 7, lane 31, bit 31
+        ("v", 4, 0, 8): (0, 4),       # block 1 -> slot 1
+        ("v", 4, 0, 16): (4, 0),      # block 2 -> word 1
+        ("v", 4, 15, 127): (1023, 4),  # block 15 = word 7 = word 3 of unit 1, lane 31, bit 28
+    }
+    for (side, w, tau, j), want in cases.items():
+        f = layout.k_plane_position if side == "k" else layout.v_plane_position
+        assert f(128, tau, j, w) == want, (side, w, tau, j, f(128, tau, j, w), want)
+    # the 4-bit K and 2-bit V placements are the w = 4 and w = 2 cases
+    for tau in range(16):
+        for j in range(128):
+            assert layout.k_plane_position(128, tau, j, 4) == layout.k_code_position(128, tau, j)
+            assert layout.v_plane_position(128, tau, j, 2) == layout.v_code_position(128, tau, j)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("side,w", [("k", 1), ("k", 2), ("v", 1), ("v", 4)])
+def test_plane_positions_are_a_bijection(D, side, w):
+    f = layout.k_plane_position if side == "k" else layout.v_plane_position
+    seen = set()
+    for tau in range(16):
+        for j in range(D):
+            byte, sh = f(D, tau, j, w)
+            assert 0 <= byte < 2 * D * w and sh % w == 0 and sh + w <= 8
+            seen.add((byte, sh))
+    assert len(seen) == 16 * D
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+def test_planes_roundtrip(bits):
+    rng = np.random.default_rng(bits)
+    for side in ("k", "v"):
+        codes = rng.integers(0, 2 ** bits, (16, 128))
+        region = layout.pack_planes(codes, bits, side)
+        assert region.size == 2 * 128 * bits
+        np.testing.assert_array_equal(layout.unpack_planes(region, 128, bits, side), codes)
+
+
+def test_six_bit_fp16_scale_record_is_about_40_percent_of_fp16():
+    """gmlx page, "The two schemes": at 6 bits a record takes about 40% of
+    the memory of fp16. Here: K and V at 6 bits with fp16 scales."""
+    lay = layout.DenseLayout(128, 128, 6, 6, scale_bytes=2)
+    per_token = lay.page_bytes / 16
+    assert lay.page_bytes == 3264
+    assert abs(per_token / (2 * 2 * 128) - 0.40) < 0.01
+
+
+@pytest.mark.parametrize("kb,vb,sb", [(6, 6, 2), (3, 3, 2), (8, 8, 2), (4, 2, 2), (5, 5, 4)])
+def test_write_read_tile_roundtrip_other_widths(kb, vb, sb):
+    lay = layout.DenseLayout(128, 64, kb, vb, scale_bytes=sb)
+    rng = np.random.default_rng(kb * 10 + vb)
+    cache = np.zeros((8, 1, lay.page_bytes), np.uint8)
+    enc_k = dict(codes=rng.integers(0, 2 ** kb, (64, 128)), a=rng.random(64), b=-rng.random(64), c=rng.random(128))
+    enc_v = dict(codes=rng.integers(0, 2 ** vb, (64, 128)), a=rng.random(64), b=-rng.random(64), c=rng.random(128))
+    layout.write_tile(cache, lay, [5, 1, 7, 2], 0, enc_k, enc_v)
+    k, v = layout.read_tile(cache, lay, [5, 1, 7, 2], 0)
+    dt = np.float32 if sb == 4 else np.float16
+    for enc, got in ((enc_k, k), (enc_v, v)):
+        np.testing.assert_array_equal(got["codes"], enc["codes"])
+        for key in "abc":
+            np.testing.assert_array_equal(got[key], enc[key].astype(dt).astype(np.float64))

@@ -30,6 +30,7 @@ PINS = [
     (tc.test_dequantize_roundtrip_is_exact_without_rounding, {}),
     (tl.test_page_bytes_hand_derived, {}),
     (tl.test_write_read_tile_roundtrip, {}),
+    (tl.test_plane_positions_hand_derived, {}),
     (ta.test_softmax_attention_matches_scipy, {}),
     (ta.test_softmax_attention_two_tokens_by_hand, {}),
     (ta.test_decode_equals_rotated_space_computation, {}),
@@ -164,6 +165,19 @@ def _visible_off_by_one(orig):
     return lambda L, Q, j: max(0, L - Q + j)
 
 
+def _plane_halves_swapped(orig):
+    # the pair element and the second-register flag trade bit offsets
+    def pos(D, tau, j, w):
+        F = 8 // w
+        kc, r = divmod(j, 16)
+        t, ep, h = (r % 8) // 2, r % 2, r // 8
+        word, f = divmod(2 * kc + tau // 8, F)
+        U = min(4, D * w // 64)
+        bit = w * f + 16 * h + 8 * ep
+        return 4 * U * (32 * (word // U) + 4 * (tau % 8) + t) + 4 * (word % U) + bit // 8, bit % 8
+    return pos
+
+
 def _recent_ignored(orig):
     return lambda L, Q, N, sink, recent: orig(L, Q, N, sink, 0)
 
@@ -186,6 +200,7 @@ MUTATIONS = [
     ("verify commits tiles the drafts filled", attention, "verify_committed", _commit_from_full_length),
     ("verify query sees one token too few", attention, "verify_visible", _visible_off_by_one),
     ("recent raw records ignored", attention, "window_committed", _recent_ignored),
+    ("plane register halves swapped", layout, "k_plane_position", _plane_halves_swapped),
 ]
 
 
