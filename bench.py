@@ -137,8 +137,8 @@ def _oracle_unit(args):
     from oracle import attention, codec, layout, mla
     kind = args[0]
     if kind == "dense":
-        _, k, v, q, sm, N, L = args
-        lay = layout.DenseLayout(k.shape[-1], N)
+        _, k, v, q, sm, N, L, kb, vb, sb = args
+        lay = layout.DenseLayout(k.shape[-1], N, kb, vb, sb)
         tiles = L // N
         ppt = N // 16
         cache = np.zeros((max(1, tiles) * ppt, 1, lay.page_bytes), np.uint8)
@@ -153,8 +153,8 @@ def _oracle_unit(args):
         tv[0, 0, :tail] = v[tiles * N:L]
         t0 = time.perf_counter()
         if tiles:
-            ek = codec.encode_tile(k[(tiles - 1) * N:tiles * N], 4, 2)
-            ev = codec.encode_tile(v[(tiles - 1) * N:tiles * N], 2, 2)
+            ek = codec.encode_tile(k[(tiles - 1) * N:tiles * N], kb, 2)
+            ev = codec.encode_tile(v[(tiles - 1) * N:tiles * N], vb, 2)
             layout.write_tile(cache, lay, list(range((tiles - 1) * ppt, tiles * ppt)), 0, ek, ev)
         attention.decode(q[None], cache, lay, bt, [L], sm, tk, tv)
         return time.perf_counter() - t0
@@ -208,7 +208,7 @@ def oracle_time(pool, cores, work):
     return sum(pool.map(_oracle_unit, work)) / cores
 
 
-def oracle_work(wl, case, n, queries=1, qv=None):
+def oracle_work(wl, case, n, queries=1, qv=None, widths=(4, 2, 4)):
     """Host float64 inputs of n sampled units of the step, and the fraction
     of the whole step they are."""
     if wl.rope_dim:
@@ -236,7 +236,7 @@ def oracle_work(wl, case, n, queries=1, qv=None):
                          1 / math.sqrt(wl.head_dim), wl.tile_tokens, L, queries))
         else:
             work.append(("dense", k, v, case.q[b, h * G:(h + 1) * G].double().cpu().numpy(),
-                         1 / math.sqrt(wl.head_dim), wl.tile_tokens, L))
+                         1 / math.sqrt(wl.head_dim), wl.tile_tokens, L) + tuple(widths))
     return work, len(pick) / len(units)
 
 
@@ -244,13 +244,14 @@ def oracle_work(wl, case, n, queries=1, qv=None):
 class DenseHarness:
     """Dense (GQA) workloads: the cache, the step's commit and the decode."""
 
-    def __init__(self, kv, W, wl, dev, rank):
+    def __init__(self, kv, W, wl, dev, rank, widths=(4, 2, 4)):
         import torch
         self.kv, self.wl, self.dev = kv, wl, dev
         self.case = case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
         B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
-        self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters)
+        self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters, k_bits=widths[0],
+                                   v_bits=widths[1], fp16_scales=widths[2] == 2)
         self.cache = kv.alloc_cache(self.lay, dev)
         self.err = kv.new_error_word(dev)
         lens = case.seq_lens.cpu().tolist()
@@ -607,12 +608,19 @@ def run_kvarn(args):
     wl = W.WORKLOADS[args.workload]
     if args.num_seqs:
         wl = wl.with_(num_seqs=args.num_seqs)
+    widths = (args.kbits, args.vbits, 2 if args.fp16_scales else 4)
+    if widths != (4, 2, 4):
+        if wl.rope_dim or args.queries > 1 or args.sink or args.recent or args.append:
+            raise SystemExit("--kbits/--vbits/--fp16-scales apply to the plain dense step")
+        wl = wl.with_(k_bits=args.kbits, v_bits=args.vbits)
     if args.queries > 1 or args.sink or args.recent:
         if wl.rope_dim:
             raise SystemExit("--queries, --sink and --recent apply to the dense workloads")
         H = VerifyHarness(kv, W, wl, dev, rank, args.queries, args.sink, args.recent)
+    elif wl.rope_dim:
+        H = LatentHarness(kv, W, wl, dev, rank)
     else:
-        H = (LatentHarness if wl.rope_dim else DenseHarness)(kv, W, wl, dev, rank)
+        H = DenseHarness(kv, W, wl, dev, rank, widths)
     if args.append:
         if wl.rope_dim or args.queries > 1 or args.sink or args.recent or wl.encode_chunk:
             raise SystemExit("--append applies to the plain dense step")
@@ -737,7 +745,7 @@ def run_kvarn(args):
     cpu = None
     if world == 1 and not args.no_cpu and not (args.sink or args.recent):
         n = max(4, min(16, os.cpu_count() or 4))
-        work, frac = oracle_work(wl, H.case, n, args.queries, getattr(H, "qv", None))
+        work, frac = oracle_work(wl, H.case, n, args.queries, getattr(H, "qv", None), widths)
         pool, cores = oracle_pool(len(work))
         with pool:
             wall = oracle_time(pool, cores, work)
@@ -768,8 +776,9 @@ def run_kvarn(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 (codes u4/u2; fp16 hi/lo mma operands)", "data": "synthetic",
-        "config": {"workload": _workload_desc(wl),
+        "dtype": (f"f32 (codes u{args.kbits}/u{args.vbits}, {'fp16' if args.fp16_scales else 'fp32'} scales; "
+                  f"fp16 hi/lo mma operands)"), "data": "synthetic",
+        "config": {"workload": _workload_desc(wl) + (" fp16-scales" if args.fp16_scales else ""),
                    "step": (f"commit one compressed tile per (seq, KV head), then {args.queries} query token(s) "
                             f"per seq, raw sink {args.sink} + recent {args.recent} (kvarn_decode_window)"
                             if args.sink or args.recent else
@@ -829,7 +838,7 @@ def run_reference(args):
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": _workload_desc(wl),
+            "config": {"workload": _workload_desc(wl) + (" fp16-scales" if args.fp16_scales else ""),
                        "step": "commit one tile per (seq, KV head), then decode 1 token per seq"},
             "cpu_baseline": {"value": round(val, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"{len(work)} of {units_total} units per step, scaled to the whole step"},
@@ -848,6 +857,9 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=0, help="override the batch (profiling a small case)")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per sequence under speculative verification (dense workloads)")
+    ap.add_argument("--kbits", type=int, default=4, help="key code width (2, 3, 4, 5, 6, 8)")
+    ap.add_argument("--vbits", type=int, default=2, help="value code width (2, 3, 4, 5, 6, 8)")
+    ap.add_argument("--fp16-scales", action="store_true", help="fp16 scales in the page (else fp32)")
     ap.add_argument("--append", action="store_true",
                     help="commit through kvarn_append of the newest token (fused append + commit)")
     ap.add_argument("--sink", type=int, default=0, help="raw sink tokens (a multiple of the tile)")
