@@ -51,8 +51,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 #define KVARN_DECODE_MIN_CTAS 3
 #endif
 
+// HV warps share a tile (HV = 2 at head_dim 256: each warp owns half of the
+// channels of Q K and of P V, and the pair adds its partial scores).
+template <int D> constexpr int halves_for() { return D == 256 ? 2 : 1; }
+
 template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4>
 struct DecShape {
+  static constexpr int HV = halves_for<D>();
+  static constexpr int UNITS = W / HV;  // tiles in flight per CTA
   static constexpr DensePage PG{D, N, KB, VB, SB};
   static constexpr int PPT = N / kPageTokens;
   static constexpr int PB = PG.bytes();
@@ -74,9 +80,13 @@ struct DecShape {
   static constexpr int KU1 = KW1 ? (D * KW1 / 64 < 4 ? D * KW1 / 64 : 4) : 1;
   static constexpr int KR1 = 2 * D * KW0, VR1 = 2 * D * VW0;
   static constexpr float KCENTER = static_cast<float>(1 << (KB - 1)), VCENTER = static_cast<float>(1 << (VB - 1));
-  static constexpr int RING = W * WARP_SMEM;
-  static constexpr int SMEM = RING + W * 2 * 8 + 8 * D * 4;
-  static_assert(W * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  static constexpr int RING = UNITS * WARP_SMEM;
+  static constexpr int XS = 2 * (N / 8) + 2;  // exchanged per lane: partial scores, two timeout flags
+  static constexpr int XBUF = HV == 2 ? UNITS * 2 * 32 * XS * 4 : 0;
+  static constexpr int OFF_BARS = RING, OFF_QROT = RING + UNITS * 2 * 8, OFF_XBUF = OFF_QROT + 8 * D * 4;
+  static constexpr int SMEM = OFF_XBUF + XBUF;
+  static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
 };
 
@@ -252,8 +262,12 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
   }
 }
 
+// Resident CTAs per SM the kernel is compiled for: 3 x 4 warps at head_dim
+// 128 (168 registers); 5 x 2 warps at 256 (a warp pair, up to 204 registers).
+template <int D, int W> constexpr int decode_min_ctas() { return W == 4 ? KVARN_DECODE_MIN_CTAS : D == 256 ? 5 : 1; }
+
 template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
-__global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) decode_dense_kernel(DecArgs A) {
+__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(DecArgs A) {
   using S = DecShape<D, N, W, KB, VB, SB>;
   constexpr DensePage PG = S::PG;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -288,17 +302,30 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     return;
   }
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::RING);
-  float* qrot = reinterpret_cast<float*>(smem + S::RING + W * 2 * 8);
+  constexpr int HV = S::HV, UNITS = S::UNITS;
+  const int half = HV == 2 ? (warp & 1) : 0, unit = warp / HV;
+  const bool leader = half == 0;  // issues its unit's copies
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
+  float* qrot = reinterpret_cast<float*>(smem + S::OFF_QROT);
+  float* xbuf = reinterpret_cast<float*>(smem + S::OFF_XBUF);
   int32_t* pages = reinterpret_cast<int32_t*>(smem + S::SMEM);  // this split's page ids
-  unsigned char* kslot = smem + warp * S::WARP_SMEM;
+  unsigned char* kslot = smem + unit * S::WARP_SMEM;
   unsigned char* vslot = kslot + S::KSLOT;
-  uint64_t* barK = bars + 2 * warp;
+  uint64_t* barK = bars + 2 * unit;
   uint64_t* barV = barK + 1;
+  // the two warps of a unit meet at named barrier 1 + unit
+  auto pair_sync = [&]() {
+    if constexpr (HV == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
+  };
 
-  const int first = t0 + warp;
-  const int n_my = first < t1 ? (t1 - first + W - 1) / W : 0;
+  const int first = t0 + unit;
+  const int n_my = first < t1 ? (t1 - first + UNITS - 1) / UNITS : 0;
   const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
+  if (leader && lane == 0) {
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
+  }
+  fence_mbar_init();
 
   // the split's block-table entries, checked once, into shared memory
   for (int e = threadIdx.x; e < (t1 - t0) * S::PPT; e += W * 32) {
@@ -311,12 +338,14 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
   }
   __syncthreads();
 
-  // physical page `lane` of this warp's i-th tile (lanes < PPT)
+  // physical page `lane` of this unit's i-th tile (lanes < PPT)
   auto page_of = [&](int i) -> const unsigned char* {
-    const int phys = pages[(first + i * W - t0) * S::PPT + lane];
+    const int phys = pages[(first + i * UNITS - t0) * S::PPT + lane];
     return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB;
   };
+  int k_iss = 0, v_iss = 0;  // copies this warp started (the leader's count)
   auto issue_k = [&](int i) {
+    ++k_iss;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
@@ -324,6 +353,7 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_of(i), S::KP, barK);
   };
   auto issue_v = [&](int i) {
+    ++v_iss;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
@@ -331,13 +361,7 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
   };
 
-  if (lane == 0) {
-    mbar_init(barK, 1);
-    mbar_init(barV, 1);
-  }
-  fence_mbar_init();
-  __syncwarp();
-  if (n_my > 0) {
+  if (leader && n_my > 0) {
     issue_k(0);
     issue_v(0);
   }
@@ -362,25 +386,34 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
   }
   __syncthreads();
 
+  constexpr int KCW = S::KC / HV, NCW = S::NC / HV;  // this warp's k-chunks and channel blocks
   float m = -INFINITY, lsum = 0.f;
-  float acc[S::NC][2];
+  float acc[NCW][2];
 #pragma unroll
-  for (int nc = 0; nc < S::NC; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
+  for (int nc = 0; nc < NCW; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
+  float* xmine = xbuf + (unit * 2 + half) * 32 * S::XS;
+  const float* xother = xbuf + (unit * 2 + (half ^ 1)) * 32 * S::XS;
 
   int i = 0;
   bool timed_out = false;
   for (; i < n_my; ++i) {
     const uint32_t par = i & 1;
-    if (!mbar_wait_bounded(barK, par)) {
-      timed_out = true;
-      break;
+    // a warp of a pair that gives up on a copy tells its partner at the next
+    // pair barrier and both leave together
+    bool late = !mbar_wait_bounded(barK, par);
+    if constexpr (HV == 1) {
+      if (late) {
+        timed_out = true;
+        break;
+      }
     }
 
-    // -- q~ = q' * c_K as fp16 hi/lo A fragments
-    uint32_t Aq[S::KC][4];
+    // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels)
+    uint32_t Aq[KCW][4];
     float qsum = 0.f;
 #pragma unroll
-    for (int kc = 0; kc < S::KC; ++kc) {
+    for (int kcl = 0; kcl < KCW; ++kcl) {
+      const int kc = half * KCW + kcl;
       const int ch0 = 16 * kc + 2 * t;
       const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
       const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
@@ -389,8 +422,8 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
       const float2 c89 = load_scale2<SB>(cp + 8 * SB);
       const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
       qsum += (x0 + x1) + (x8 + x9);
-      split_hi_lo(x0, x1, Aq[kc][0], Aq[kc][1]);
-      split_hi_lo(x8, x9, Aq[kc][2], Aq[kc][3]);
+      split_hi_lo(x0, x1, Aq[kcl][0], Aq[kcl][1]);
+      split_hi_lo(x8, x9, Aq[kcl][2], Aq[kcl][3]);
     }
     qsum = warp_sum_xor(qsum, 1, 4);
 
@@ -407,7 +440,8 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
 #pragma unroll
         for (int e = 0; e < 2; ++e) d[pi][e][0] = d[pi][e][1] = d[pi][e][2] = d[pi][e][3] = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < S::KCH; ++ch) {
+      for (int chl = 0; chl < S::KCH / HV; ++chl) {
+        const int ch = half * (S::KCH / HV) + chl;
         uint32_t x0[2][S::KW0], x1[2][S::KW1 ? S::KW1 : 1];
 #pragma unroll
         for (int pi = 0; pi < 2; ++pi) {
@@ -421,7 +455,7 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
         }
         static_for<0, 8>([&](auto fgc) {
           constexpr int fg = decltype(fgc)::value;  // fragment 2 w4 + e of the group
-          const int kc = 4 * ch + fg / 2;
+          const int kc = 4 * chl + fg / 2;          // this warp's k-chunk
 #pragma unroll
           for (int pi = 0; pi < 2; ++pi) {
             uint32_t b0, b1;
@@ -440,8 +474,10 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
         }
     }
 
-    // -- row-scale fold and online softmax (base 2)
-    float mt = -INFINITY;
+    // -- row-scale fold (linear, so a warp of a pair folds its partial
+    //    scores with its own sum of q~ and the pair adds them in a fixed
+    //    order, leaving both with the same scores), then the online softmax
+    //    in base 2. The K slot is read for the last time here.
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
       const unsigned char* pg = kslot + (nb >> 1) * S::KP;
@@ -450,8 +486,31 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
       const float2 kb = load_scale2<SB>(pg + PG.k_b() + idx * SB);
       s[nb][0] = fmaf(ka.x, s[nb][0], fmaf(S::KCENTER, ka.x, kb.x) * qsum);
       s[nb][1] = fmaf(ka.y, s[nb][1], fmaf(S::KCENTER, ka.y, kb.y) * qsum);
-      mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
     }
+    if constexpr (HV == 2) {
+#pragma unroll
+      for (int nb = 0; nb < S::NB; ++nb) {
+        xmine[(2 * nb) * 32 + lane] = s[nb][0];
+        xmine[(2 * nb + 1) * 32 + lane] = s[nb][1];
+      }
+      xmine[(S::XS - 2) * 32 + lane] = late ? 1.f : 0.f;
+      pair_sync();
+      late = late || xother[(S::XS - 2) * 32 + lane] != 0.f;
+      late = __any_sync(0xffffffffu, late);
+#pragma unroll
+      for (int nb = 0; nb < S::NB; ++nb) {
+        const float o0 = xother[(2 * nb) * 32 + lane], o1 = xother[(2 * nb + 1) * 32 + lane];
+        s[nb][0] = half ? o0 + s[nb][0] : s[nb][0] + o0;
+        s[nb][1] = half ? o1 + s[nb][1] : s[nb][1] + o1;
+      }
+      if (late) {
+        timed_out = true;
+        break;
+      }
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < S::NB; ++nb) mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
     mt = warp_max_xor(mt, 1, 4);
     const float m_new = fmaxf(m, mt);
     const float alpha = fast_exp2(m - m_new);
@@ -466,11 +525,14 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     m = m_new;
 
     // the K slot is free: start the next tile's K part
-    if (i + 1 < n_my) issue_k(i + 1);
+    if (leader && i + 1 < n_my) issue_k(i + 1);
 
-    if (!mbar_wait_bounded(barV, par)) {
-      timed_out = true;
-      break;
+    late = !mbar_wait_bounded(barV, par);
+    if constexpr (HV == 1) {
+      if (late) {
+        timed_out = true;
+        break;
+      }
     }
 
     // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
@@ -494,14 +556,15 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
     beta = warp_sum_xor(beta, 1, 4);
 
 #pragma unroll
-    for (int nc = 0; nc < S::NC; ++nc) {
+    for (int nc = 0; nc < NCW; ++nc) {
       acc[nc][0] *= alpha;
       acc[nc][1] *= alpha;
     }
     // channel blocks in groups of eight: the group's fragments are one
     // unit (VW consecutive words) of each code plane
 #pragma unroll
-    for (int hq = 0; hq < S::VHC; ++hq) {
+    for (int hql = 0; hql < S::VHC / HV; ++hql) {
+      const int hq = half * (S::VHC / HV) + hql;
       float u[8][4];
 #pragma unroll
       for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
@@ -519,46 +582,56 @@ __global__ void __launch_bounds__(W * 32, (W == 4 ? KVARN_DECODE_MIN_CTAS : 1)) 
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int nc = 8 * hq + k;
+        const int nc = 8 * hq + k, ncl = 8 * hql + k;
         const int ch = 8 * nc + 2 * t;
         const float2 cv = load_scale2<SB>(vslot + (ch / S::CPP) * S::VP + PG.v_col() - S::KP + (ch % S::CPP) * SB);
-        acc[nc][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[nc][0]);
-        acc[nc][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[nc][1]);
+        acc[ncl][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[ncl][0]);
+        acc[ncl][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[ncl][1]);
       }
     }
-    if (i + 1 < n_my) issue_v(i + 1);
+    if constexpr (HV == 2) {  // both warps are done with the V slot
+      xmine[(S::XS - 1) * 32 + lane] = late ? 1.f : 0.f;
+      pair_sync();
+      late = __any_sync(0xffffffffu, late || xother[(S::XS - 1) * 32 + lane] != 0.f);
+      if (late) {
+        timed_out = true;
+        break;
+      }
+    }
+    if (leader && i + 1 < n_my) issue_v(i + 1);
   }
-  if (timed_out) {
+  if (timed_out && leader) {
     if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
-    // wait (bounded) for the copies this warp still has in flight
-    mbar_wait_bounded(barK, i & 1, 100000000LL);
-    mbar_wait_bounded(barV, i & 1, 100000000LL);
+    // wait (bounded) for the last copy of each slot this warp started
+    if (k_iss > 0) mbar_wait_bounded(barK, (k_iss - 1) & 1, 100000000LL);
+    if (v_iss > 0) mbar_wait_bounded(barV, (v_iss - 1) & 1, 100000000LL);
   }
   lsum = warp_sum_xor(lsum, 1, 4);
 
-  // ---- merge the W warps of the CTA (scratch aliases the slots)
+  // ---- merge the units of the CTA (scratch aliases the slots)
   __syncthreads();
   float* mrg = reinterpret_cast<float*>(smem);
-  float* mw = mrg + warp * 8 * (D + 2);
-  if (t == 0) {
+  float* mw = mrg + unit * 8 * (D + 2);
+  if (t == 0 && leader) {
     mw[g * (D + 2)] = n_my > 0 ? m : -INFINITY;
     mw[g * (D + 2) + 1] = n_my > 0 ? lsum : 0.f;
   }
 #pragma unroll
-  for (int nc = 0; nc < S::NC; ++nc) {
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[nc][0];
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[nc][1];
+  for (int ncl = 0; ncl < NCW; ++ncl) {
+    const int nc = half * NCW + ncl;
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[ncl][0];
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[ncl][1];
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
     const int gg = idx / D, j = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
+    for (int w = 0; w < UNITS; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
     float a = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
+      for (int w = 0; w < UNITS; ++w) {
         const float* r = mrg + (w * 8 + gg) * (D + 2);
         const float sc = exp2f(r[0] - M);
         a = fmaf(r[2 + j], sc, a);
