@@ -179,6 +179,20 @@ __device__ __forceinline__ void split_hi_lo(float x0, float x1, uint32_t& hi, ui
   lo = h2_as_u32(l);
 }
 
+// Pairs of fp32 values: one packed instruction for both (sm_100 and later).
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// split_hi_lo of a pair held as float2 (x - hi is exact, as above).
+__device__ __forceinline__ void split_hi_lo2(float2 x, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __float22half2_rn(x);
+  const float2 r = __ffma2_rn(__half22float2(h), f2(-1.f), x);
+  hi = h2_as_u32(h);
+  lo = h2_as_u32(__float22half2_rn(r));
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t orv) {
   uint32_t r;
   // (x & mask) | orv

@@ -134,11 +134,8 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   }
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * A.Q * p.num_q_heads;
-  if (p.D == 128)
-    merge_kernel<128><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
-  else
-    merge_kernel<256><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
-  return cudaGetLastError();
+  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st)
+                    : launch_merge<256>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st);
 }
 
 }  // namespace kvarn

@@ -145,6 +145,12 @@ struct RowMap {
   __device__ int query(const DecArgs& A, int r) const { return (8 * rg + r) / A.G; }
 };
 
+// The rotated, scaled query rows in shared memory, in mma fragment order:
+// for k-chunk kc, row g and lane column t the four channels 16 kc + 2 t,
+// +1, +8, +9 are one 16-byte word, and a warp's 32 words for one k-chunk are
+// contiguous (one conflict-free 128-bit load per lane).
+__device__ __forceinline__ int q_frag(int kc, int g, int t) { return ((kc * 8 + g) * 4 + t) * 4; }
+
 // Partial slot of (sequence b, query token j, query head hq).
 __device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j, int hq, int slot) {
   return A.ws + (static_cast<int64_t>((b * A.Q + j) * A.Hq + hq) * A.slots + slot) * kPStride(D);
@@ -271,6 +277,7 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   using S = DecShape<D, N, W, KB, VB, SB>;
   constexpr DensePage PG = S::PG;
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   // KV head is the fastest grid axis: CTAs resident together read the same
@@ -382,15 +389,18 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
       for (int e = 0; e < E; ++e) v[e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) qrot[h * D + lane * E + e] = v[e];
+    for (int e = 0; e < E; ++e) {
+      const int ch = lane * E + e, w = ch % 16;
+      qrot[q_frag(ch / 16, h, (w % 8) / 2) + (w % 2) + 2 * (w / 8)] = v[e];
+    }
   }
   __syncthreads();
 
   constexpr int KCW = S::KC / HV, NCW = S::NC / HV;  // this warp's k-chunks and channel blocks
   float m = -INFINITY, lsum = 0.f;
-  float acc[NCW][2];
+  float2 acc[NCW];
 #pragma unroll
-  for (int nc = 0; nc < NCW; ++nc) acc[nc][0] = acc[nc][1] = 0.f;
+  for (int nc = 0; nc < NCW; ++nc) acc[nc] = f2(0.f);
   float* xmine = xbuf + (unit * 2 + half) * 32 * S::XS;
   const float* xother = xbuf + (unit * 2 + (half ^ 1)) * 32 * S::XS;
 
@@ -410,28 +420,26 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
 
     // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels)
     uint32_t Aq[KCW][4];
-    float qsum = 0.f;
+    float2 qs2 = f2(0.f);
 #pragma unroll
     for (int kcl = 0; kcl < KCW; ++kcl) {
       const int kc = half * KCW + kcl;
       const int ch0 = 16 * kc + 2 * t;
-      const float2 q01 = *reinterpret_cast<const float2*>(qrot + g * D + ch0);
-      const float2 q89 = *reinterpret_cast<const float2*>(qrot + g * D + ch0 + 8);
+      const float4 qv = *reinterpret_cast<const float4*>(qrot + q_frag(kc, g, t));
       const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * SB;
-      const float2 c01 = load_scale2<SB>(cp);
-      const float2 c89 = load_scale2<SB>(cp + 8 * SB);
-      const float x0 = q01.x * c01.x, x1 = q01.y * c01.y, x8 = q89.x * c89.x, x9 = q89.y * c89.y;
-      qsum += (x0 + x1) + (x8 + x9);
-      split_hi_lo(x0, x1, Aq[kcl][0], Aq[kcl][1]);
-      split_hi_lo(x8, x9, Aq[kcl][2], Aq[kcl][3]);
+      const float2 x01 = f2mul(make_float2(qv.x, qv.y), load_scale2<SB>(cp));
+      const float2 x89 = f2mul(make_float2(qv.z, qv.w), load_scale2<SB>(cp + 8 * SB));
+      qs2 = f2add(qs2, f2add(x01, x89));
+      split_hi_lo2(x01, Aq[kcl][0], Aq[kcl][1]);
+      split_hi_lo2(x89, Aq[kcl][2], Aq[kcl][3]);
     }
-    qsum = warp_sum_xor(qsum, 1, 4);
+    const float2 qsum = f2(warp_sum_xor(qs2.x + qs2.y, 1, 4));
 
     // -- S = q~ . (K codes - 2^(KB-1)), two pages (four 8-token blocks) at a
     //    time so that four independent accumulator chains hide the mma
     //    latency. Per group of four k-chunks a lane's fragments (2 kc + e,
     //    e the token block) are KW consecutive words of each code plane.
-    float s[S::NB][2];
+    float2 s[S::NB];
 #pragma unroll
     for (int p0 = 0; p0 < S::PPT; p0 += 2) {
       float d[2][2][4];
@@ -468,10 +476,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
 #pragma unroll
       for (int pi = 0; pi < 2; ++pi)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          s[2 * (p0 + pi) + e][0] = d[pi][e][0] + d[pi][e][2];
-          s[2 * (p0 + pi) + e][1] = d[pi][e][1] + d[pi][e][3];
-        }
+        for (int e = 0; e < 2; ++e)
+          s[2 * (p0 + pi) + e] = f2add(make_float2(d[pi][e][0], d[pi][e][1]), make_float2(d[pi][e][2], d[pi][e][3]));
     }
 
     // -- row-scale fold (linear, so a warp of a pair folds its partial
@@ -484,14 +490,13 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
       const int idx = (nb & 1) * 8 + 2 * t;
       const float2 ka = load_scale2<SB>(pg + PG.k_a() + idx * SB);
       const float2 kb = load_scale2<SB>(pg + PG.k_b() + idx * SB);
-      s[nb][0] = fmaf(ka.x, s[nb][0], fmaf(S::KCENTER, ka.x, kb.x) * qsum);
-      s[nb][1] = fmaf(ka.y, s[nb][1], fmaf(S::KCENTER, ka.y, kb.y) * qsum);
+      s[nb] = f2fma(ka, s[nb], f2mul(f2fma(f2(S::KCENTER), ka, kb), qsum));
     }
     if constexpr (HV == 2) {
 #pragma unroll
       for (int nb = 0; nb < S::NB; ++nb) {
-        xmine[(2 * nb) * 32 + lane] = s[nb][0];
-        xmine[(2 * nb + 1) * 32 + lane] = s[nb][1];
+        xmine[(2 * nb) * 32 + lane] = s[nb].x;
+        xmine[(2 * nb + 1) * 32 + lane] = s[nb].y;
       }
       xmine[(S::XS - 2) * 32 + lane] = late ? 1.f : 0.f;
       pair_sync();
@@ -499,9 +504,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
       late = __any_sync(0xffffffffu, late);
 #pragma unroll
       for (int nb = 0; nb < S::NB; ++nb) {
-        const float o0 = xother[(2 * nb) * 32 + lane], o1 = xother[(2 * nb + 1) * 32 + lane];
-        s[nb][0] = half ? o0 + s[nb][0] : s[nb][0] + o0;
-        s[nb][1] = half ? o1 + s[nb][1] : s[nb][1] + o1;
+        const float2 o = make_float2(xother[(2 * nb) * 32 + lane], xother[(2 * nb + 1) * 32 + lane]);
+        s[nb] = half ? f2add(o, s[nb]) : f2add(s[nb], o);
       }
       if (late) {
         timed_out = true;
@@ -510,18 +514,18 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
     }
     float mt = -INFINITY;
 #pragma unroll
-    for (int nb = 0; nb < S::NB; ++nb) mt = fmaxf(mt, fmaxf(s[nb][0], s[nb][1]));
+    for (int nb = 0; nb < S::NB; ++nb) mt = fmaxf(mt, fmaxf(s[nb].x, s[nb].y));
     mt = warp_max_xor(mt, 1, 4);
     const float m_new = fmaxf(m, mt);
     const float alpha = fast_exp2(m - m_new);
-    float psum = 0.f;
+    float2 ps2 = f2(0.f);
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
-      s[nb][0] = fast_exp2(s[nb][0] - m_new);
-      s[nb][1] = fast_exp2(s[nb][1] - m_new);
-      psum += s[nb][0] + s[nb][1];
+      const float2 z = f2add(s[nb], f2(-m_new));
+      s[nb] = make_float2(fast_exp2(z.x), fast_exp2(z.y));
+      ps2 = f2add(ps2, s[nb]);
     }
-    lsum = fmaf(lsum, alpha, psum);
+    lsum = fmaf(lsum, alpha, ps2.x + ps2.y);
     m = m_new;
 
     // the K slot is free: start the next tile's K part
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
 
     // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
     uint32_t Ap[S::PPT][4];
-    float beta = 0.f;
+    float2 be2 = f2(0.f);
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
       const unsigned char* pg = vslot + pp * S::VP;
@@ -545,21 +549,15 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
       const float2 va1 = load_scale2<SB>(pg + PG.v_a() - S::KP + (8 + 2 * t) * SB);
       const float2 vb0 = load_scale2<SB>(pg + PG.v_b() - S::KP + (2 * t) * SB);
       const float2 vb1 = load_scale2<SB>(pg + PG.v_b() - S::KP + (8 + 2 * t) * SB);
-      const float p00 = s[2 * pp][0], p01 = s[2 * pp][1], p10 = s[2 * pp + 1][0], p11 = s[2 * pp + 1][1];
-      beta = fmaf(p00, fmaf(S::VCENTER, va0.x, vb0.x), beta);
-      beta = fmaf(p01, fmaf(S::VCENTER, va0.y, vb0.y), beta);
-      beta = fmaf(p10, fmaf(S::VCENTER, va1.x, vb1.x), beta);
-      beta = fmaf(p11, fmaf(S::VCENTER, va1.y, vb1.y), beta);
-      split_hi_lo(p00 * va0.x, p01 * va0.y, Ap[pp][0], Ap[pp][1]);
-      split_hi_lo(p10 * va1.x, p11 * va1.y, Ap[pp][2], Ap[pp][3]);
+      be2 = f2fma(s[2 * pp], f2fma(f2(S::VCENTER), va0, vb0), be2);
+      be2 = f2fma(s[2 * pp + 1], f2fma(f2(S::VCENTER), va1, vb1), be2);
+      split_hi_lo2(f2mul(s[2 * pp], va0), Ap[pp][0], Ap[pp][1]);
+      split_hi_lo2(f2mul(s[2 * pp + 1], va1), Ap[pp][2], Ap[pp][3]);
     }
-    beta = warp_sum_xor(beta, 1, 4);
+    const float2 beta = f2(warp_sum_xor(be2.x + be2.y, 1, 4));
 
 #pragma unroll
-    for (int nc = 0; nc < NCW; ++nc) {
-      acc[nc][0] *= alpha;
-      acc[nc][1] *= alpha;
-    }
+    for (int nc = 0; nc < NCW; ++nc) acc[nc] = f2mul(acc[nc], f2(alpha));
     // channel blocks in groups of eight: the group's fragments are one
     // unit (VW consecutive words) of each code plane
 #pragma unroll
@@ -585,8 +583,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
         const int nc = 8 * hq + k, ncl = 8 * hql + k;
         const int ch = 8 * nc + 2 * t;
         const float2 cv = load_scale2<SB>(vslot + (ch / S::CPP) * S::VP + PG.v_col() - S::KP + (ch % S::CPP) * SB);
-        acc[ncl][0] = fmaf(cv.x, (u[k][0] + u[k][2]) + beta, acc[ncl][0]);
-        acc[ncl][1] = fmaf(cv.y, (u[k][1] + u[k][3]) + beta, acc[ncl][1]);
+        const float2 uk = f2add(make_float2(u[k][0], u[k][1]), make_float2(u[k][2], u[k][3]));
+        acc[ncl] = f2fma(cv, f2add(uk, beta), acc[ncl]);
       }
     }
     if constexpr (HV == 2) {  // both warps are done with the V slot
@@ -619,8 +617,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
 #pragma unroll
   for (int ncl = 0; ncl < NCW; ++ncl) {
     const int nc = half * NCW + ncl;
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[ncl][0];
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[ncl][1];
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[ncl].x;
+    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[ncl].y;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(64) decode_fp16_kernel(F16Args A) {
   using S = F16Shape<D>;
   constexpr int W = S::W;
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -351,11 +352,8 @@ cudaError_t launch_decode_fp16(const DecodeParams& p, const SplitPlan& plan, cud
   else if (p.D == 256) e = run_fp16<256>(A, p.num_seqs, st);
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * p.num_q_heads;
-  if (p.D == 128)
-    merge_kernel<128><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, 0, p.out, p.lse);
-  else
-    merge_kernel<256><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, 0, p.out, p.lse);
-  return cudaGetLastError();
+  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, 0, p.out, p.lse, st)
+                    : launch_merge<256>(A.ws, A.slots, rows, 0, p.out, p.lse, st);
 }
 
 }  // namespace kvarn

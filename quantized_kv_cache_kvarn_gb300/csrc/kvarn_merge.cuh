@@ -35,20 +35,58 @@ __device__ __forceinline__ void warp_fwht(float* v) {
   }
 }
 
+// ------------------------------------------------- programmatic launch
+// The split kernels let the merge kernel be scheduled while their last CTAs
+// still run; the merge waits for their completion (and memory flush) before
+// it reads a partial.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ merge
+// dst = sum over slots [s0, s1) of exp2(m_s - M) * (this lane's part of the
+// slot vector); every lane reads the slot maxima (one broadcast load each),
+// and several slot vectors are in flight at once.
+template <int E>
+__device__ __forceinline__ void accumulate_slots(const float* P, int stride, int s0, int s1, float M,
+                                                 float (&dst)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = 0.f;
+#pragma unroll 4
+  for (int s = s0; s < s1; ++s) {
+    const float* p = P + static_cast<int64_t>(s) * stride;
+    const float w = exp2f(p[0] - M);
+    p += 4 + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + e);
+      dst[e] = fmaf(v.x, w, dst[e]);
+      dst[e + 1] = fmaf(v.y, w, dst[e + 1]);
+      dst[e + 2] = fmaf(v.z, w, dst[e + 2]);
+      dst[e + 3] = fmaf(v.w, w, dst[e + 3]);
+    }
+  }
+}
+
 // One warp per (sequence, query head): LSE merge of all slots, inverse
-// Hadamard of the rotated part (slots < nsplit), plus the tail slot.
+// Hadamard of the rotated part (slots < rotated_slots), plus the raw slots.
+// The lanes read the slot maxima and sums in parallel (lane s: slots s,
+// s + 32, ...).
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws, int slots,
                                                     int rows, int rotated_slots, float* out,
                                                     float* lse) {
   constexpr int E = D / 32;
+  pdl_wait_primary();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= rows) return;
   const float* P = ws + static_cast<int64_t>(row) * slots * kPStride(D);
   float M = -INFINITY;
-  for (int s = 0; s < slots; ++s) M = fmaxf(M, P[s * kPStride(D)]);
+  for (int s = lane; s < slots; s += 32) M = fmaxf(M, P[s * kPStride(D)]);
+  M = warp_max_xor(M, 1, 32);
   float* o = out + static_cast<int64_t>(row) * D + lane * E;
   if (M == -INFINITY) {
 #pragma unroll
@@ -57,28 +95,35 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws
     return;
   }
   float L = 0.f, rot[E], tl[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) rot[e] = tl[e] = 0.f;
-  for (int s = 0; s < slots; ++s) {
-    const float* p = P + s * kPStride(D);
-    const float w = exp2f(p[0] - M);
-    L = fmaf(p[1], w, L);
-    float* dst = s < rotated_slots ? rot : tl;
-#pragma unroll
-    for (int e = 0; e < E; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(p + 4 + lane * E + e);
-      dst[e] = fmaf(v.x, w, dst[e]);
-      dst[e + 1] = fmaf(v.y, w, dst[e + 1]);
-      dst[e + 2] = fmaf(v.z, w, dst[e + 2]);
-      dst[e + 3] = fmaf(v.w, w, dst[e + 3]);
-    }
-  }
+  for (int s = lane; s < slots; s += 32) L = fmaf(P[s * kPStride(D) + 1], exp2f(P[s * kPStride(D)] - M), L);
+  accumulate_slots<E>(P, kPStride(D), 0, rotated_slots, M, rot);
+  accumulate_slots<E>(P, kPStride(D), rotated_slots, slots, M, tl);
+  L = warp_sum_xor(L, 1, 32);
   const float invL = 1.f / L;
   warp_fwht<E>(rot);
   const float sc = invL / sqrtf(static_cast<float>(D));
 #pragma unroll
   for (int e = 0; e < E; ++e) o[e] = fmaf(rot[e], sc, tl[e] * invL);
   if (lse && lane == 0) lse[row] = (M + log2f(L)) * kLn2;
+}
+
+// Launches the merge as a programmatic dependent of the kernel before it on
+// the stream.
+template <int D>
+cudaError_t launch_merge(const float* ws, int slots, int rows, int rotated_slots, float* out, float* lse,
+                         cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, ws, slots, rows, rotated_slots, out, lse);
 }
 
 }  // namespace kvarn

@@ -155,6 +155,7 @@ __device__ void mla_tail(const MlaArgs& A, int b, int hg, int tail, unsigned cha
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(MlaArgs A) {
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int hg = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
@@ -562,8 +563,7 @@ cudaError_t launch_decode_mla(const DecodeParams& p, const SplitPlan& plan, cuda
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * p.num_q_heads;
-  merge_kernel<512><<<(rows + 3) / 4, 128, 0, st>>>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse);
-  return cudaGetLastError();
+  return launch_merge<512>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st);
 }
 
 }  // namespace kvarn
