@@ -211,8 +211,10 @@ int32_t kvarn_append(const void* k, const void* v, const int32_t* seq_lens, int3
 /*
  * kvarn_decode_workspace_bytes - scratch needed by kvarn_decode (and by
  * kvarn_decode_fp16 and kvarn_decode_mla with the same arguments): the
- * split-K partials (running max, sum and unnormalised output per split).
- * Returns -1 for invalid arguments.
+ * split-K partials (running max, sum and unnormalised output per split)
+ * and, for the compressed decode, one partial count per output row. The
+ * call writes every part of it that it reads; nothing needs to start at
+ * zero. Returns -1 for invalid arguments.
  */
 int64_t kvarn_decode_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
                                      int32_t num_q_heads, int32_t max_seq_len);
@@ -225,7 +227,9 @@ int64_t kvarn_decode_workspace_bytes(const kvarn_layout* layout, int32_t num_seq
  * committed tiles, dequantised inline from the pages, and tokens
  * [floor(len/N)*N, len) are rows 0.. of the raw tail buffer. Query head h
  * reads KV head h / (num_q_heads / Hkv) (GQA). Split-K over tiles with a
- * log-sum-exp merge.
+ * log-sum-exp merge: the committed tiles of all (sequence, KV head) pairs
+ * form one list that persistent CTAs share in equal contiguous ranges
+ * (stream-K), so the work per CTA does not depend on how the lengths vary.
  *
  *   q            device, kv_dtype [num_seqs][num_q_heads][D]
  *   num_q_heads  a multiple of Hkv, with at most 8 query heads per KV head

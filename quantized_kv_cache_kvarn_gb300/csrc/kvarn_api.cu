@@ -118,13 +118,16 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
 
 // max_seq_len here: the accepted length bound (sizes the tile splits); raw_max:
 // raw (sink + tail) tokens a row may see (sizes the raw splits).
-static SplitPlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
+static DensePlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
                             int32_t num_queries, int32_t max_seq_len, int32_t raw_max) {
   const int32_t G = num_q_heads / L->num_kv_heads;
-  return with_raw_chunks(
-      plan_dense(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len, L->tile_tokens,
-                 dense_decode_warps(L->head_dim), dense_decode_ctas_per_sm(L->head_dim, L->tile_tokens)),
-      raw_max);
+  return plan_dense_stream(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len / L->tile_tokens,
+                           L->head_dim, L->tile_tokens, raw_max);
+}
+
+static int64_t dense_ws(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads, int32_t num_queries,
+                        const DensePlan& plan) {
+  return dense_stream_workspace_bytes(static_cast<int64_t>(num_seqs) * num_q_heads * num_queries, L->head_dim, plan);
 }
 
 // Raw tokens a row can see: at most the sequence, and at most the sink, the
@@ -176,9 +179,9 @@ int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, in
     return -1;
   if (is_latent(L)) return mla_workspace_bytes(num_seqs, num_q_heads, plan_mla(num_seqs, max_seq_len));
   if (num_q_heads % L->num_kv_heads) return -1;
-  const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, 1, max_seq_len, raw_bound(L, max_seq_len, 1, 0, 0));
+  const DensePlan plan = dense_plan(L, num_seqs, num_q_heads, 1, max_seq_len, raw_bound(L, max_seq_len, 1, 0, 0));
   const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
-  return std::max(dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan),
+  return std::max(dense_ws(L, num_seqs, num_q_heads, 1, plan),
                   dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan16));
 }
 
@@ -189,10 +192,10 @@ int64_t kvarn_decode_window_workspace_bytes(const kvarn_layout* L, int32_t num_s
       max_seq_len < 0 || num_queries < 1 || num_queries > KVARN_MAX_VERIFY_QUERIES ||
       num_q_heads % L->num_kv_heads || sink_tokens < 0 || recent_tokens < 0)
     return -1;
-  const SplitPlan plan =
+  const DensePlan plan =
       dense_plan(L, num_seqs, num_q_heads, num_queries, std::max(0, max_seq_len - num_queries + 1),
                  raw_bound(L, max_seq_len, num_queries, sink_tokens, recent_tokens));
-  return dense_workspace_bytes(num_seqs, num_q_heads * num_queries, L->head_dim, plan);
+  return dense_ws(L, num_seqs, num_q_heads, num_queries, plan);
 }
 
 int64_t kvarn_decode_verify_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
@@ -238,10 +241,9 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
   if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
   if ((sink_k && !aligned(sink_k, 16)) || (sink_v && !aligned(sink_v, 16))) return KVARN_EALIGN;
-  const SplitPlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries, accepted,
+  const DensePlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries, accepted,
                                     raw_bound(L, max_seq_len, num_queries, sink_tokens, recent_tokens));
-  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads * num_queries, L->head_dim, plan))
-    return KVARN_EWORKSPACE;
+  if (workspace_bytes < dense_ws(L, num_seqs, num_q_heads, num_queries, plan)) return KVARN_EWORKSPACE;
   DecodeParams p{};
   p.q = q;
   p.num_q_heads = num_q_heads;

@@ -48,11 +48,31 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
 
 int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 
+DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
+                            int32_t raw_max) {
+  DensePlan p{};
+  const int units_per_cta = dense_decode_warps(D) / (D == 256 ? 2 : 1);  // tiles a CTA has in flight
+  p.min_tiles = 4 * units_per_cta;
+  p.tile_slots = max_tiles > 0 ? 1 + (max_tiles - 1 + p.min_tiles - 1) / p.min_tiles : 0;
+  p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
+  p.slots = p.tile_slots + p.raw_splits;
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N);
+  const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
+  const int64_t tile_ctas = (units * std::max(0, max_tiles) + p.min_tiles - 1) / p.min_tiles;
+  const int64_t raw_items = units * p.raw_splits;
+  p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min(resident, std::max(tile_ctas, raw_items))));
+  return p;
+}
+
+int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& plan) {
+  return rows * plan.slots * kPStride(D) * 4 + (rows * 4 + 15) / 16 * 16;
+}
+
 template <int D, int N, typename T, int W>
 static int resident_ctas() {
   using S = DecShape<D, N, W>;
   auto kern = decode_dense_kernel<D, N, T, W, 4, 2, 4>;
-  const int smem = S::SMEM + 48 * S::PPT * 4;  // with a typical split's page ids
+  const int smem = S::SMEM;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 1;
   int n = 0;
@@ -80,7 +100,7 @@ int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
   return static_cast<int64_t>(num_seqs) * num_q_heads * plan.slots * kPStride(D) * 4;
 }
 
-cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st) {
+cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   DecArgs A{};
   A.q = p.q;
@@ -103,8 +123,13 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   A.tail_k = p.tail_k;
   A.tail_v = p.tail_v;
   A.ws = static_cast<float*>(p.workspace);
-  A.tps = plan.tiles_per_split;
-  A.nsplit = plan.nsplit;
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * A.Q * p.num_q_heads;
+  A.counts = reinterpret_cast<int32_t*>(A.ws + rows * plan.slots * kPStride(p.D));
+  A.num_seqs = p.num_seqs;
+  A.X = p.num_kv_heads * row_groups(A.G, A.Q);
+  A.min_tiles = plan.min_tiles;
+  A.tile_slots = plan.tile_slots;
+  A.raw_splits = plan.raw_splits;
   A.slots = plan.slots;
   A.err = p.err;
   cudaError_t e = cudaErrorInvalidValue;
@@ -112,30 +137,29 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cu
   if (kb == 4 && vb == 2 && sb == 4) {
 #define KV_DISPATCH(DD, NN, WW)                                                              \
   if (p.D == DD && p.N == NN)                                                                \
-    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW, 4, 2, 4>(A, p.num_seqs, st)            \
-               : run_dense<DD, NN, __half, WW, 4, 2, 4>(A, p.num_seqs, st);
+    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW, 4, 2, 4>(A, plan.ctas, st)             \
+               : run_dense<DD, NN, __half, WW, 4, 2, 4>(A, plan.ctas, st);
     KV_DISPATCH(128, 128, 4)
     KV_DISPATCH(128, 64, 4)
     KV_DISPATCH(256, 128, 2)
     KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH
   } else if (kb == 4 && vb == 2 && sb == 2) {
-    e = run_dense_widths<4, 2, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st);
+    e = run_dense_widths<4, 2, 2>(A, p.D, p.N, p.bf16, plan.ctas, st);
   } else if (kb == vb && sb == 2) {
     switch (kb) {
-      case 2: e = run_dense_widths<2, 2, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
-      case 3: e = run_dense_widths<3, 3, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
-      case 4: e = run_dense_widths<4, 4, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
-      case 5: e = run_dense_widths<5, 5, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
-      case 6: e = run_dense_widths<6, 6, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
-      case 8: e = run_dense_widths<8, 8, 2>(A, p.D, p.N, p.bf16, p.num_seqs, st); break;
+      case 2: e = run_dense_widths<2, 2, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      case 3: e = run_dense_widths<3, 3, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      case 4: e = run_dense_widths<4, 4, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      case 5: e = run_dense_widths<5, 5, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      case 6: e = run_dense_widths<6, 6, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      case 8: e = run_dense_widths<8, 8, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
       default: break;
     }
   }
   if (e != cudaSuccess) return e;
-  const int rows = p.num_seqs * A.Q * p.num_q_heads;
-  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st)
-                    : launch_merge<256>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st);
+  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, A.counts, 0, A.tile_slots, p.out, p.lse, st)
+                    : launch_merge<256>(A.ws, A.slots, rows, A.counts, 0, A.tile_slots, p.out, p.lse, st);
 }
 
 }  // namespace kvarn

@@ -6,8 +6,12 @@
 // taken in the rotated basis: the query is rotated once per CTA and the
 // output un-rotated once in the merge (turbo-attn page, "How it works").
 //
-// Kernel 1 (decode_dense_kernel): one CTA per (split, KV head, sequence);
-// each of its W warps owns every W-th tile of the split. A warp keeps one
+// Kernel 1 (decode_dense_kernel): persistent CTAs, each taking an equal
+// contiguous range of the flattened list of committed tiles of all
+// (sequence, KV head, row group) units (stream-K) and writing one partial
+// per unit its range touches; a segment's tiles go round-robin to the W
+// warps (warp pairs at head_dim 256). The CTAs also take the raw-record
+// chunks (sink and tail rows) round-robin, before their tiles. A warp keeps one
 // shared-memory slot for the K parts and one for the V parts of its tile's
 // pages, filled by one-dimensional bulk copies (completion counted on an
 // mbarrier); an L2 prefetch of later tiles measured slower (its lines were
@@ -27,8 +31,9 @@
 //   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
 //   acc = acc * alpha + c_V * (u + sum p (b_V + 2 a_V)).
 // The warps of a CTA merge in shared memory and write one partial
-// (max, sum, unnormalised output) per split. The last split slot holds the
-// fp16 tail (tokens past the last full tile, in the original basis).
+// (max, sum, unnormalised output) per segment; the raw partials (original
+// basis) sit in the slots after the tile partials, and each row's count of
+// tile partials is written beside them.
 // Kernel 2 (merge_kernel): log-sum-exp merge of the partials, inverse
 // Hadamard transform of the rotated part, plus the tail part.
 #pragma once
@@ -109,7 +114,13 @@ struct DecArgs {
   const void* tail_k;
   const void* tail_v;
   float* ws;
-  int32_t tps, nsplit, slots;
+  int32_t* counts;     // per output row: tile partial slots written for it (slots [0, count))
+  int32_t num_seqs;
+  int32_t X;           // work units per sequence: KV heads x row groups
+  int32_t min_tiles;   // fewest compressed tiles a CTA takes (bounds the slots a unit needs)
+  int32_t tile_slots;  // partial slots reserved for compressed tiles; raw slots follow them
+  int32_t raw_splits;  // raw slots (chunks of kRawChunk raw tokens)
+  int32_t slots;       // tile_slots + raw_splits
   uint32_t* err;
 };
 
@@ -234,7 +245,7 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
     const int n_sink = min(sink, vis), n_tail = max(0, vis - committed);
     const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
     const int s_cnt = max(0, min(c1, n_sink) - c0), t0 = max(c0, n_sink) - n_sink, t_cnt = max(0, c1 - max(c0, n_sink));
-    float* part = part_of(A, D, b, j, hq, A.nsplit + chunk);
+    float* part = part_of(A, D, b, j, hq, A.tile_slots + chunk);
     const bool miss = (t_cnt > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
                       (s_cnt > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
     if ((t_cnt <= 0 && s_cnt <= 0) || miss) {
@@ -272,42 +283,113 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
 // 128 (168 registers); 5 x 2 warps at 256 (a warp pair, up to 204 registers).
 template <int D, int W> constexpr int decode_min_ctas() { return W == 4 ? KVARN_DECODE_MIN_CTAS : D == 256 ? 5 : 1; }
 
-template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
-__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(DecArgs A) {
-  using S = DecShape<D, N, W, KB, VB, SB>;
-  constexpr DensePage PG = S::PG;
-  extern __shared__ __align__(128) unsigned char smem[];
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  // KV head is the fastest grid axis: CTAs resident together read the same
-  // physical pages (all heads of a page are contiguous), keeping DRAM rows open
-  const int kvh = blockIdx.x % A.Hkv, split = blockIdx.y, b = blockIdx.z;
-  const RowMap R(A, blockIdx.x / A.Hkv);
+// ---------------------------------------------------------- work mapping
+// The compressed tiles of all (sequence, unit) pairs form one flattened
+// list: sequence-major, then unit x = row group * Hkv + KV head, then tile.
+// CTA c of C takes the contiguous range [c T / C, (c + 1) T / C) of the T
+// tiles (stream-K), so every CTA gets the same number of tiles to within one
+// whatever the sequence lengths; a unit cut by range ends gets one partial
+// per CTA, merged afterwards.
 
+// Length of sequence b, checked against max_seq_len (flagged and clamped).
+__device__ __forceinline__ int checked_len(const DecArgs& A, int b) {
   int len = A.seq_lens[b];
   if (len < 0 || len > A.max_seq_len) {
-    if (threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_SEQ_LEN);
+    set_error(A.err, KVARN_DEVERR_SEQ_LEN);
     len = len < 0 ? 0 : A.max_seq_len;
   }
-  // Only tokens up to the first query token are accepted, so only the tiles
-  // they fill can be committed; of those, the raw sink records come first and
-  // the newest `recent` accepted tokens stay raw. Compressed: tiles
-  // [sink_tiles, end).
-  const int sink = A.sink_tiles * N;
-  const int committed = max(sink, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
-  const int end = committed / N;
+  return len;
+}
 
-  if (split >= A.nsplit) {
-    tail_partials<D, N, T, W>(A, b, kvh, R, len, sink, committed, split - A.nsplit);
-    return;
+// First token past the committed tiles: only tokens up to the first query
+// token are accepted, so only the tiles they fill can be committed; of those,
+// the raw sink records come first and the newest `recent` accepted tokens
+// stay raw. Compressed tiles are [sink_tiles, committed / N).
+__device__ __forceinline__ int committed_end(const DecArgs& A, int N, int len) {
+  return max(A.sink_tiles * N, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
+}
+
+__device__ __forceinline__ int seq_tiles(const DecArgs& A, int N, int b) {
+  return committed_end(A, N, checked_len(A, b)) / N - A.sink_tiles;
+}
+
+// Inclusive warp prefix sum.
+__device__ __forceinline__ int64_t warp_incl_scan(int64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
   }
-  const int t0 = A.sink_tiles + split * A.tps, t1 = min(t0 + A.tps, end);
-  if (t0 >= t1) {
-    for (int r = warp; r < R.n; r += W)
-      write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), split), D, lane);
-    return;
+  return v;
+}
+
+// Flattened tiles of sequences [0, b_end) (every lane of the warp returns it).
+__device__ __forceinline__ int64_t tiles_before(const DecArgs& A, int N, int b_end) {
+  const int lane = threadIdx.x & 31;
+  int64_t base = 0;
+  for (int b0 = 0; b0 < b_end; b0 += 32) {
+    const int bb = b0 + lane;
+    const int64_t n = bb < b_end ? static_cast<int64_t>(seq_tiles(A, N, bb)) * A.X : 0;
+    base += __shfl_sync(0xffffffffu, warp_incl_scan(n), 31);
   }
+  return base;
+}
+
+struct TilePos {
+  int b, x, tile, n;  // sequence, unit, tile within the unit's compressed tiles, the unit's tiles
+  int64_t u0;         // the unit's first flattened tile
+};
+
+// Position of flattened tile `cur` (< the total); warp-cooperative.
+__device__ __forceinline__ TilePos locate_tile(const DecArgs& A, int N, int64_t cur) {
+  const int lane = threadIdx.x & 31;
+  int64_t base = 0;
+  TilePos P{-1, 0, 0, 0, 0};
+  for (int b0 = 0; b0 < A.num_seqs; b0 += 32) {
+    const int bb = b0 + lane;
+    const int n = bb < A.num_seqs ? seq_tiles(A, N, bb) : 0;
+    const int64_t incl = warp_incl_scan(static_cast<int64_t>(n) * A.X);
+    const unsigned hit = __ballot_sync(0xffffffffu, base + incl > cur);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      P.b = b0 + l;
+      P.n = __shfl_sync(0xffffffffu, n, l);
+      const int64_t before = base + __shfl_sync(0xffffffffu, incl, l) - static_cast<int64_t>(P.n) * A.X;
+      const int64_t within = cur - before;
+      P.x = static_cast<int>(within / P.n);
+      P.tile = static_cast<int>(within % P.n);
+      P.u0 = before + static_cast<int64_t>(P.x) * P.n;
+      return P;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return P;
+}
+
+// The CTA whose range holds flattened tile t.
+__device__ __forceinline__ int cta_of_tile(int64_t t, int C, int64_t total) {
+  return static_cast<int>(((t + 1) * C - 1) / total);
+}
+
+// ------------------------------------------------------------ one segment
+// Tiles [t0, t1) of unit x of sequence b: rotated query rows, the tile loop
+// of every warp, the merge of the CTA's warps, and the partial into `slot`.
+// ph: this warp's mbarrier bookkeeping, which persists across segments:
+// K and V slot phases waited (bits 0 and 8) and copies started (bits 16 and
+// 24), each counted mod 256 (only parities are read). `dead`: a copy timed
+// out earlier; the segment then only writes empty partials. Returns false
+// when a copy timed out (in this segment or before).
+template <int D, int N, typename T, int W, int KB, int VB, int SB>
+__device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* smem, int b, int x, int t0, int t1,
+                                              int slot, uint32_t& ph,
+                                              bool dead) {
+  using S = DecShape<D, N, W, KB, VB, SB>;
+  constexpr DensePage PG = S::PG;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int kvh = x % A.Hkv;
+  const RowMap R(A, x / A.Hkv);
 
   constexpr int HV = S::HV, UNITS = S::UNITS;
   const int half = HV == 2 ? (warp & 1) : 0, unit = warp / HV;
@@ -315,62 +397,53 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
   float* qrot = reinterpret_cast<float*>(smem + S::OFF_QROT);
   float* xbuf = reinterpret_cast<float*>(smem + S::OFF_XBUF);
-  int32_t* pages = reinterpret_cast<int32_t*>(smem + S::SMEM);  // this split's page ids
   unsigned char* kslot = smem + unit * S::WARP_SMEM;
   unsigned char* vslot = kslot + S::KSLOT;
   uint64_t* barK = bars + 2 * unit;
   uint64_t* barV = barK + 1;
   // the two warps of a unit meet at named barrier 1 + unit
   auto pair_sync = [&]() {
-    if constexpr (HV == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
+    if constexpr (HV == 2 && UNITS == 1) asm volatile("bar.sync 1, 64;" ::: "memory");
+    else if constexpr (HV == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
   };
 
   const int first = t0 + unit;
-  const int n_my = first < t1 ? (t1 - first + UNITS - 1) / UNITS : 0;
+  const int n_my = !dead && first < t1 ? (t1 - first + UNITS - 1) / UNITS : 0;
   const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
-  if (leader && lane == 0) {
-    mbar_init(barK, 1);
-    mbar_init(barV, 1);
-  }
-  fence_mbar_init();
-
-  // the split's block-table entries, checked once, into shared memory
-  for (int e = threadIdx.x; e < (t1 - t0) * S::PPT; e += W * 32) {
-    int phys = bt[t0 * S::PPT + e];
-    if (phys < 0 || phys >= A.num_pages) {
-      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
-      phys = 0;
+  // physical page `lane` (lanes < PPT) of this unit's i-th tile, checked
+  auto page_id = [&](int i) -> int {
+    int phys = 0;
+    if (lane < S::PPT) {
+      phys = bt[(first + i * UNITS) * S::PPT + lane];
+      if (phys < 0 || phys >= A.num_pages) {
+        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+        phys = 0;
+      }
     }
-    pages[e] = phys;
-  }
-  __syncthreads();
-
-  // physical page `lane` of this unit's i-th tile (lanes < PPT)
-  auto page_of = [&](int i) -> const unsigned char* {
-    const int phys = pages[(first + i * UNITS - t0) * S::PPT + lane];
-    return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB;
+    return phys;
   };
-  int k_iss = 0, v_iss = 0;  // copies this warp started (the leader's count)
-  auto issue_k = [&](int i) {
-    ++k_iss;
+  auto page_at = [&](int phys) { return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB; };
+  auto issue_k = [&](int phys) {
+    ph += 1u << 16;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
     __syncwarp();
-    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_of(i), S::KP, barK);
+    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_at(phys), S::KP, barK);
   };
-  auto issue_v = [&](int i) {
-    ++v_iss;
+  auto issue_v = [&](int phys) {
+    ph += 1u << 24;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
     __syncwarp();
-    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_of(i) + S::KP, S::VP, barV);
+    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_at(phys) + S::KP, S::VP, barV);
   };
 
   if (leader && n_my > 0) {
-    issue_k(0);
-    issue_v(0);
+    const int phys = page_id(0);
+    issue_k(phys);
+    issue_v(phys);
   }
 
   // ---- rotated, scaled query rows of the row group (unused rows are zero)
@@ -404,20 +477,20 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   float* xmine = xbuf + (unit * 2 + half) * 32 * S::XS;
   const float* xother = xbuf + (unit * 2 + (half ^ 1)) * 32 * S::XS;
 
-  int i = 0;
   bool timed_out = false;
-  for (; i < n_my; ++i) {
-    const uint32_t par = i & 1;
+  for (int i = 0; i < n_my; ++i) {
+    // the next tile's page ids, loaded a tile ahead of their copies
+    const int phys_next = leader && i + 1 < n_my ? page_id(i + 1) : 0;
     // a warp of a pair that gives up on a copy tells its partner at the next
     // pair barrier and both leave together
-    bool late = !mbar_wait_bounded(barK, par);
+    bool late = !mbar_wait_bounded(barK, ph & 1);
+    ph += 1u;
     if constexpr (HV == 1) {
       if (late) {
         timed_out = true;
         break;
       }
     }
-
     // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels)
     uint32_t Aq[KCW][4];
     float2 qs2 = f2(0.f);
@@ -529,9 +602,10 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
     m = m_new;
 
     // the K slot is free: start the next tile's K part
-    if (leader && i + 1 < n_my) issue_k(i + 1);
+    if (leader && i + 1 < n_my) issue_k(phys_next);
 
-    late = !mbar_wait_bounded(barV, par);
+    late = !mbar_wait_bounded(barV, (ph >> 8) & 1);
+    ph += 1u << 8;
     if constexpr (HV == 1) {
       if (late) {
         timed_out = true;
@@ -596,18 +670,20 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
         break;
       }
     }
-    if (leader && i + 1 < n_my) issue_v(i + 1);
+    if (leader && i + 1 < n_my) issue_v(phys_next);
   }
   if (timed_out && leader) {
     if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
-    // wait (bounded) for the last copy of each slot this warp started
-    if (k_iss > 0) mbar_wait_bounded(barK, (k_iss - 1) & 1, 100000000LL);
-    if (v_iss > 0) mbar_wait_bounded(barV, (v_iss - 1) & 1, 100000000LL);
+    // wait (bounded) for the last copy of each slot this warp started (a
+    // parity whose phase precedes the barrier's first completes at once); no
+    // copy is started after a time-out
+    mbar_wait_bounded(barK, ((ph >> 16) - 1) & 1, 100000000LL);
+    mbar_wait_bounded(barV, ((ph >> 24) - 1) & 1, 100000000LL);
   }
   lsum = warp_sum_xor(lsum, 1, 4);
 
   // ---- merge the units of the CTA (scratch aliases the slots)
-  __syncthreads();
+  const bool any_late = __syncthreads_or(timed_out);
   float* mrg = reinterpret_cast<float*>(smem);
   float* mw = mrg + unit * 8 * (D + 2);
   if (t == 0 && leader) {
@@ -636,35 +712,111 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
         L = fmaf(r[1], sc, L);
       }
     }
-    float* part = part_of(A, D, b, R.query(A, gg), kvh * A.G + R.head(A, gg), split);
+    float* part = part_of(A, D, b, R.query(A, gg), kvh * A.G + R.head(A, gg), slot);
     part[4 + j] = a;
     if (j == 0) {
       part[0] = M;
       part[1] = L;
     }
   }
+  // the scratch is read before the next segment's copies land in the slots
+  __syncthreads();
+  return !any_late;
+}
+
+template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
+__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(DecArgs A) {
+  using S = DecShape<D, N, W, KB, VB, SB>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
+    if (warp % S::HV == 0 && lane == 0) {
+      mbar_init(bars + 2 * (warp / S::HV), 1);
+      mbar_init(bars + 2 * (warp / S::HV) + 1, 1);
+    }
+    fence_mbar_init();
+  }
+
+  // ---- raw records: items r = blockIdx.x, + gridDim.x, ... of (sequence,
+  //      unit, raw chunk)
+  const int64_t units = static_cast<int64_t>(A.num_seqs) * A.X;
+  for (int64_t r = blockIdx.x; r < units * A.raw_splits; r += gridDim.x) {
+    const int chunk = static_cast<int>(r % A.raw_splits);
+    const int64_t u = r / A.raw_splits;
+    const int b = static_cast<int>(u / A.X), x = static_cast<int>(u % A.X);
+    const int len = checked_len(A, b);
+    tail_partials<D, N, T, W>(A, b, x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N,
+                              committed_end(A, N, len), chunk);
+  }
+
+  const int64_t total = tiles_before(A, N, A.num_seqs);
+  const int64_t by_tiles = total / A.min_tiles > 1 ? total / A.min_tiles : 1;
+  const int C = static_cast<int>(by_tiles < gridDim.x ? by_tiles : gridDim.x);
+
+  // ---- tile-partial counts of units u = blockIdx.x, + gridDim.x, ...
+  if (warp == 0) {
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+      const int b = static_cast<int>(u / A.X), x = static_cast<int>(u % A.X);
+      const int n = seq_tiles(A, N, b);
+      int count = 0;
+      if (n > 0) {
+        const int64_t u0 = tiles_before(A, N, b) + static_cast<int64_t>(x) * n;
+        count = cta_of_tile(u0 + n - 1, C, total) - cta_of_tile(u0, C, total) + 1;
+      }
+      const RowMap R(A, x / A.Hkv);
+      if (lane < R.n)
+        A.counts[(b * A.Q + R.query(A, lane)) * A.Hq + (x % A.Hkv) * A.G + R.head(A, lane)] = count;
+    }
+  }
+  __syncthreads();  // mbarrier initialisation visible to every warp
+  if (total == 0 || static_cast<int>(blockIdx.x) >= C) return;
+
+  // ---- this CTA's tiles, one segment per unit they touch. The position is
+  //      kept in shared memory (no register holds it across a segment),
+  //      double-buffered: the next position is written to the entry nobody
+  //      reads in this pass, and read after the segment's closing barrier.
+  __shared__ int64_t pos[3];  // current tile (two entries), end of the range
+  if (threadIdx.x == 0) {
+    pos[0] = blockIdx.x * total / C;
+    pos[2] = (blockIdx.x + 1) * total / C;
+  }
+  __syncthreads();
+  uint32_t ph = 0;
+  bool dead = false;
+  for (int k = 0;; k ^= 1) {
+    const int64_t cur = pos[k], stop = pos[2];
+    if (cur >= stop) break;
+    const TilePos P = locate_tile(A, N, cur);
+    if (P.b < 0) break;  // unreachable: cur < total
+    const int64_t seg_end = min(stop, P.u0 + P.n);
+    const int slot = static_cast<int>(blockIdx.x) - cta_of_tile(P.u0, C, total);
+    const int t0 = A.sink_tiles + P.tile;
+    const int t1 = t0 + static_cast<int>(seg_end - cur);
+    if (threadIdx.x == 0) pos[k ^ 1] = seg_end;
+    dead = !dense_segment<D, N, T, W, KB, VB, SB>(A, smem, P.b, P.x, t0, t1, slot, ph, dead) || dead;
+  }
 }
 
 template <int D, int N, typename T, int W, int KB, int VB, int SB>
-cudaError_t run_dense(const DecArgs& A, int num_seqs, cudaStream_t st) {
+cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
   using S = DecShape<D, N, W, KB, VB, SB>;
   auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
-  const int smem = S::SMEM + A.tps * S::PPT * 4;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(A.Hkv * row_groups(A.G, A.Q), A.slots, num_seqs);
-  kern<<<grid, W * 32, smem, st>>>(A);
+  kern<<<ctas, W * 32, S::SMEM, st>>>(A);
   return cudaGetLastError();
 }
 
 // The decode kernels of one (K width, V width, scale bytes) combination;
 // each combination is compiled in its own translation unit.
 template <int KB, int VB, int SB>
-cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int num_seqs, cudaStream_t st);
+cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int ctas, cudaStream_t st);
 
 #define KVARN_DECLARE_WIDTHS(KB, VB, SB)                                                             \
   template <>                                                                                       \
-  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int num_seqs, \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas, \
                                            cudaStream_t st);
 KVARN_DECLARE_WIDTHS(4, 2, 2)
 KVARN_DECLARE_WIDTHS(2, 2, 2)
@@ -677,14 +829,14 @@ KVARN_DECLARE_WIDTHS(8, 8, 2)
 
 #define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \
   template <>                                                                                           \
-  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int num_seqs,     \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas,         \
                                            cudaStream_t st) {                                           \
     if (D == 128 && N == 128)                                                                           \
-      return bf16 ? run_dense<128, 128, __nv_bfloat16, 4, KB, VB, SB>(A, num_seqs, st)                 \
-                  : run_dense<128, 128, __half, 4, KB, VB, SB>(A, num_seqs, st);                        \
+      return bf16 ? run_dense<128, 128, __nv_bfloat16, 4, KB, VB, SB>(A, ctas, st)                 \
+                  : run_dense<128, 128, __half, 4, KB, VB, SB>(A, ctas, st);                        \
     if (D == 128 && N == 64)                                                                            \
-      return bf16 ? run_dense<128, 64, __nv_bfloat16, 4, KB, VB, SB>(A, num_seqs, st)                  \
-                  : run_dense<128, 64, __half, 4, KB, VB, SB>(A, num_seqs, st);                         \
+      return bf16 ? run_dense<128, 64, __nv_bfloat16, 4, KB, VB, SB>(A, ctas, st)                  \
+                  : run_dense<128, 64, __half, 4, KB, VB, SB>(A, ctas, st);                         \
     return cudaErrorInvalidValue;                                                                       \
   }
 

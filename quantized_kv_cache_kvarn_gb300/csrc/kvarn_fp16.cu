@@ -352,8 +352,8 @@ cudaError_t launch_decode_fp16(const DecodeParams& p, const SplitPlan& plan, cud
   else if (p.D == 256) e = run_fp16<256>(A, p.num_seqs, st);
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * p.num_q_heads;
-  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, 0, p.out, p.lse, st)
-                    : launch_merge<256>(A.ws, A.slots, rows, 0, p.out, p.lse, st);
+  return p.D == 128 ? launch_merge<128>(A.ws, A.slots, rows, nullptr, 0, 0, p.out, p.lse, st)
+                    : launch_merge<256>(A.ws, A.slots, rows, nullptr, 0, 0, p.out, p.lse, st);
 }
 
 }  // namespace kvarn

@@ -116,6 +116,25 @@ inline SplitPlan with_raw_chunks(SplitPlan p, int32_t raw_max) {
 
 SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
                      int32_t warps, int32_t ctas_per_sm);
+
+// Plan of the compressed decode: `ctas` persistent CTAs share the flattened
+// list of compressed tiles (stream-K), each taking at least `min_tiles` of
+// them, so a unit of n tiles writes at most 1 + ceil((n - 1) / min_tiles)
+// tile partials; raw partials (kRawChunk raw tokens each) follow them.
+struct DensePlan {
+  int32_t ctas;
+  int32_t min_tiles;
+  int32_t tile_slots;  // partial slots per row reserved for tiles
+  int32_t raw_splits;
+  int32_t slots;       // tile_slots + raw_splits
+};
+
+// units_per_seq: KV heads x row groups; max_tiles: compressed tiles a unit
+// can hold; raw_max: raw tokens a row can see.
+DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
+                            int32_t raw_max);
+// Partials of `rows` output rows, then one int32 tile-partial count per row.
+int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& plan);
 int dense_decode_warps(int32_t D);
 int dense_decode_ctas_per_sm(int32_t D, int32_t N);
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
@@ -123,7 +142,7 @@ int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
 
 cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_encode_latent(const EncodeLatentParams& p, cudaStream_t st);
-cudaError_t launch_decode_dense(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
+cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cudaStream_t st);
 
 struct StoreFp16Params {
   const void* k;

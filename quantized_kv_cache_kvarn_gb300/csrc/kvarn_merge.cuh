@@ -70,22 +70,25 @@ __device__ __forceinline__ void accumulate_slots(const float* P, int stride, int
   }
 }
 
-// One warp per (sequence, query head): LSE merge of all slots, inverse
-// Hadamard of the rotated part (slots < rotated_slots), plus the raw slots.
-// The lanes read the slot maxima and sums in parallel (lane s: slots s,
-// s + 32, ...).
+// One warp per (sequence, query head): LSE merge of the row's partials, the
+// rotated ones (slots [0, counts[row]), or [0, rotated_slots) without
+// counts) through the inverse Hadamard transform, plus the raw ones (slots
+// [raw_begin, slots)). The lanes read the slot maxima and sums in parallel.
 template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws, int slots,
-                                                    int rows, int rotated_slots, float* out,
-                                                    float* lse) {
+__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws, int slots, int rows,
+                                                    const int32_t* __restrict__ counts, int rotated_slots,
+                                                    int raw_begin, float* out, float* lse) {
   constexpr int E = D / 32;
   pdl_wait_primary();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= rows) return;
+  const int rot_end = counts ? min(counts[row], raw_begin) : rotated_slots;
+  auto used = [&](int s) { return s < rot_end || s >= raw_begin; };
   const float* P = ws + static_cast<int64_t>(row) * slots * kPStride(D);
   float M = -INFINITY;
-  for (int s = lane; s < slots; s += 32) M = fmaxf(M, P[s * kPStride(D)]);
+  for (int s = lane; s < slots; s += 32)
+    if (used(s)) M = fmaxf(M, P[s * kPStride(D)]);
   M = warp_max_xor(M, 1, 32);
   float* o = out + static_cast<int64_t>(row) * D + lane * E;
   if (M == -INFINITY) {
@@ -95,9 +98,10 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws
     return;
   }
   float L = 0.f, rot[E], tl[E];
-  for (int s = lane; s < slots; s += 32) L = fmaf(P[s * kPStride(D) + 1], exp2f(P[s * kPStride(D)] - M), L);
-  accumulate_slots<E>(P, kPStride(D), 0, rotated_slots, M, rot);
-  accumulate_slots<E>(P, kPStride(D), rotated_slots, slots, M, tl);
+  for (int s = lane; s < slots; s += 32)
+    if (used(s)) L = fmaf(P[s * kPStride(D) + 1], exp2f(P[s * kPStride(D)] - M), L);
+  accumulate_slots<E>(P, kPStride(D), 0, rot_end, M, rot);
+  accumulate_slots<E>(P, kPStride(D), raw_begin, slots, M, tl);
   L = warp_sum_xor(L, 1, 32);
   const float invL = 1.f / L;
   warp_fwht<E>(rot);
@@ -110,8 +114,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws
 // Launches the merge as a programmatic dependent of the kernel before it on
 // the stream.
 template <int D>
-cudaError_t launch_merge(const float* ws, int slots, int rows, int rotated_slots, float* out, float* lse,
-                         cudaStream_t st) {
+cudaError_t launch_merge(const float* ws, int slots, int rows, const int32_t* counts, int rotated_slots,
+                         int raw_begin, float* out, float* lse, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((rows + 3) / 4);
@@ -123,7 +127,7 @@ cudaError_t launch_merge(const float* ws, int slots, int rows, int rotated_slots
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, ws, slots, rows, rotated_slots, out, lse);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, ws, slots, rows, counts, rotated_slots, raw_begin, out, lse);
 }
 
 }  // namespace kvarn

@@ -563,7 +563,7 @@ cudaError_t launch_decode_mla(const DecodeParams& p, const SplitPlan& plan, cuda
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = p.num_seqs * p.num_q_heads;
-  return launch_merge<512>(A.ws, A.slots, rows, A.nsplit, p.out, p.lse, st);
+  return launch_merge<512>(A.ws, A.slots, rows, nullptr, A.nsplit, A.nsplit, p.out, p.lse, st);
 }
 
 }  // namespace kvarn
