@@ -51,14 +51,18 @@ int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
                             int32_t raw_max) {
   DensePlan p{};
-  const int units_per_cta = dense_decode_warps(D) / (D == 256 ? 2 : 1);  // tiles a CTA has in flight
-  p.min_tiles = 4 * units_per_cta;
+  // tiles a CTA has in flight: one per warp, one per warp pair at head_dim 256
+  const int in_flight = D == 256 ? dense_decode_warps(D) / 2 : dense_decode_warps(D);
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N);
+  const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
+  const int64_t most = units * std::max(0, max_tiles);
+  // four tiles in flight per CTA slot at least, fewer (down to one round)
+  // when the whole batch is too small to fill the GPU
+  p.min_tiles = static_cast<int32_t>(std::max<int64_t>(in_flight, std::min<int64_t>(4 * in_flight, most / resident)));
   p.tile_slots = max_tiles > 0 ? 1 + (max_tiles - 1 + p.min_tiles - 1) / p.min_tiles : 0;
   p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
   p.slots = p.tile_slots + p.raw_splits;
-  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N);
-  const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
-  const int64_t tile_ctas = (units * std::max(0, max_tiles) + p.min_tiles - 1) / p.min_tiles;
+  const int64_t tile_ctas = (most + p.min_tiles - 1) / p.min_tiles;
   const int64_t raw_items = units * p.raw_splits;
   p.ctas = static_cast<int32_t>(std::max<int64_t>(1, std::min(resident, std::max(tile_ctas, raw_items))));
   return p;

@@ -191,6 +191,45 @@ def test_decode_edge_lengths():
     assert np.abs(o[1:] - ref[1:]).max() <= parity.OUT_ATOL
 
 
+def test_decode_many_ragged_sequences():
+    """More sequences than a warp scans at once (the CTAs locate their tiles
+    with warp-wide scans over 32 sequences at a time), lengths from empty to
+    five tiles with and without tails: every CTA range of the flattened tile
+    list crosses unit boundaries, so units get one to several partials."""
+    B, Hq, Hkv, N, Lmax = 70, 8, 2, 128, 640
+    wl = W.WORKLOADS["dense32b"].with_(num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv, context=Lmax)
+    case = W.make_dense(wl, device="cpu")
+    rng = np.random.default_rng(7)
+    lens = rng.integers(0, Lmax + 1, size=B).astype(np.int32)
+    lens[:6] = [0, N, 2 * N, 5 * N, 1, N - 1]
+    lens[40:44] = 0
+    k, v = parity.f64(case.k), parity.f64(case.v)
+    bt = case.block_table.numpy()
+    ocache = parity.oracle_dense_cache(k, v, bt, lens, N, 128, case.num_pages)
+    tk, tv = parity.tails(k, lens, N), parity.tails(v, lens, N)
+    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(128, N), bt, lens, 0.1, tk, tv)
+    dev = "cuda"
+    lay = kv.dense_layout(128, N, Hkv, case.num_pages)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(kv.decode_workspace_bytes(lay, B, Hq, Lmax), dtype=torch.uint8, device=dev)
+    err = kv.new_error_word(dev)
+    for _ in range(2):  # the second call reuses a workspace full of the first call's partials
+        kv.decode(case.q.to(dev), lay, torch.from_numpy(ocache).to(dev), case.block_table.to(dev),
+                  torch.from_numpy(lens).to(dev), Lmax, out, ws, err, 0.1,
+                  torch.from_numpy(tk).half().to(dev), torch.from_numpy(tv).half().to(dev), lse=lse)
+        torch.cuda.synchronize()
+        assert kv.read_error_flags(err) == 0
+        o, l = parity.f64(out), parity.f64(lse)
+        empty = lens == 0
+        assert (o[empty] == 0).all() and np.isneginf(l[empty]).all()
+        diff = np.abs(o[~empty] - ref[~empty]).max()
+        print(f"\nmany_ragged: max |out - oracle| = {diff:.3e}, "
+              f"max |lse - oracle| = {np.abs(l[~empty] - ref_lse[~empty]).max():.3e}")
+        assert diff <= parity.OUT_ATOL
+        assert np.abs(l[~empty] - ref_lse[~empty]).max() <= 1e-4
+
+
 def test_device_errors_are_flagged_not_faulted():
     """A block-table entry outside the cache and a missing tail set bits of the
     error word; the kernel reads a valid page instead and finishes."""
