@@ -39,18 +39,21 @@
  * Dense page format (one page = P = 16 tokens of one KV head; bytes):
  *   K codes, 8D bytes, 4-bit. Lane L = 4g + t (g in 0..7, t in 0..3)
  *                      owns one 32-bit word per 16-channel k-chunk kc; its
- *                      byte m = h + 2e holds channel 16kc + 2t + e + 8h of
+ *                      byte m = e + 2h holds channel 16kc + 2t + e + 8h of
  *                      token g in the low nibble and of token 8 + g in the
  *                      high nibble. The word of (kc, L) sits at byte
  *                      16(32(kc/4) + L) + 4(kc%4): 16-byte units of four
  *                      k-chunks, the 32 lanes' units contiguous.
  *   V codes, 4D bytes, 2-bit. Lane L = 4g + t owns one word per four
- *                      8-channel blocks nc = 4w + c; channel 8nc + g of
- *                      token 2t + e + 8h sits at bit 2c + 8h + 16e. Word w of
- *                      lane L sits at byte 8(32(w/2) + L) + 4(w%2).
- *   Every code field of one tensor-core operand thus sits at one bit
- *   position of its 16-bit half, so masking it out yields an exact fp16
- *   subnormal operand (code times a power of two).
+ *                      8-channel blocks nc = 4w + c; byte c of the word is
+ *                      channel 8nc + g, its token 2t + e + 8h at bit 2h + 4e
+ *                      of the byte. Word w of lane L sits at byte
+ *                      8(32(w/2) + L) + 4(w%2).
+ *   One mask of a K word leaves four codes in the low 4 bits of its bytes,
+ *   which the hardware e2m3 -> fp16 conversion turns into exact operands
+ *   (code / 8), two per instruction; one mask of a V word leaves eight codes
+ *   as the low 2 bits of nibbles, which the e2m1 -> fp16 conversion turns
+ *   into exact operands (code / 2), two per instruction.
  * Other widths (gmlx page, "The two schemes": kvarn widths 2, 3, 4, 5, 6, 8
  * for keys and values): with head_dim 128 and fp16 scales, k_bits = v_bits =
  * b in {2, 3, 4, 5, 6, 8} (and the preset's 4 and 2 with fp16 scales). A
@@ -58,12 +61,13 @@
  * 6: [4, 2], 8: [4, 4] (code = plane0 + 2^w0 plane1), each plane region
  * (2*D*w bytes per page, in order) placed by one rule for width w in
  * {1, 2, 4} of which the K codes and V codes above are the w = 4 and w = 2
- * cases: lane L = 4g + t owns words of 8/w fragments; fragment f has its
- * first operand register at bits w*f, 16 + w*f and its second at 8 + w*f,
- * 24 + w*f. K: fragment 2kc + e (tokens 8e + g), channel 16kc + 2t + e' + 8h
- * at bit w*f + 8h + 16e'; words in units of U = min(4, D*w/64): word i of
- * lane L at byte 4U(32(i/U) + L) + 4(i%U). V: fragment nc, channel 8nc + g of
- * token 2t + e' + 8h at bit w*f + 8h + 16e'; words in units of w: word i of
+ * cases: lane L = 4g + t owns words of 8/w fragments; fragment f holds two
+ * operand registers h = 0, 1 of two elements e' = 0, 1, element (h, e') at
+ * bit 4f + 8e' + 16h (w = 4), 8f + 2h + 4e' (w = 2) or f + 8h + 16e'
+ * (w = 1). K: fragment 2kc + e (tokens 8e + g), element (h, e') channel
+ * 16kc + 2t + e' + 8h; words in units of U = min(4, D*w/64): word i of
+ * lane L at byte 4U(32(i/U) + L) + 4(i%U). V: fragment nc, element (h, e')
+ * channel 8nc + g of token 2t + e' + 8h; words in units of w: word i of
  * lane L at byte 4w(32(i/w) + L) + 4(i%w). With fp16 scales a, b and the
  * column slice are 2-byte values; each part is padded to 16 bytes. At 6 bits
  * a page of D = 128, N = 128 takes 3264 bytes, 40% of fp16.

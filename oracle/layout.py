@@ -9,14 +9,15 @@ library's own format. A page holds P = 16 tokens of one KV head:
 
   K codes   8*D bytes   4-bit. Lane L = 4g + t (g, t in 0..7, 0..3) owns,
                         for every 16-channel k-chunk kc, one 32-bit word;
-                        its byte m (m = h + 2e) holds channel
+                        its byte m = e + 2h holds channel
                         16kc + 2t + e + 8h of token g in the low nibble and
                         of token 8 + g in the high nibble. Words are stored
                         as 16-byte units of four k-chunks: the word of
                         (kc, L) sits at byte 16*(32*(kc//4) + L) + 4*(kc%4).
   V codes   4*D bytes   2-bit. Lane L = 4g + t owns, for every four 8-channel
-                        blocks nc = 4w + c, one 32-bit word; channel 8nc + g
-                        of token 2t + e + 8h sits at bit 2c + 8h + 16e.
+                        blocks nc = 4w + c, one 32-bit word whose byte c is
+                        channel 8nc + g; token 2t + e + 8h of that channel
+                        sits at bit 2h + 4e of the byte.
                         Words are stored as 8-byte units of two: the word w
                         of lane L sits at byte 8*(32*(w//2) + L) + 4*(w%2).
   The page is two parts, each contiguous: the K part (K codes, then K a[16],
@@ -30,15 +31,18 @@ separate for keys and values). A b-bit code is stored as one or two planes,
 b = 2: [2], 3: [2, 1], 4: [4], 5: [4, 1], 6: [4, 2], 8: [4, 4], the code
 being plane0 + 2^w0 plane1; each plane region (2*D*w bytes per page, the
 planes in order) follows one rule for a plane of width w in {1, 2, 4}: lane
-L = 4g + t owns words of 8/w fragments each; fragment f of a word has its
-first operand register at bits w*f (low half) and 16 + w*f (high half), its
-second at 8 + w*f and 24 + w*f.
+L = 4g + t owns words of 8/w fragments each;
+fragment f of a word holds two operand registers h = 0, 1 of two elements
+e' = 0, 1 each, element (h, e') at bit
+    w = 4:  4f + 8e' + 16h   (register h = half-word h, element = byte)
+    w = 2:  8f + 2h + 4e'    (fragment = byte f)
+    w = 1:  f + 8h + 16e'.
   K plane: fragment 2*kc + e (k-chunk kc, token block e: tokens 8e + g);
-           channel 16kc + 2t + e' + 8h at bit w*f + 8h + 16e'. Words go in
+           element (h, e') is channel 16kc + 2t + e' + 8h. Words go in
            units of U = min(4, D*w/64) words: word i of lane L at byte
            4U*(32*(i//U) + L) + 4*(i%U).
-  V plane: fragment nc (8-channel block); channel 8nc + g of token
-           2t + e' + 8h at bit w*f + 8h + 16e'. Words go in units of w
+  V plane: fragment nc (8-channel block); element (h, e') is channel
+           8nc + g of token 2t + e' + 8h. Words go in units of w
            words (eight blocks): word i of lane L at 4w*(32*(i//w) + L) +
            4*(i%w).
 The 4-bit K and 2-bit V placements above are the w = 4 and w = 2 cases. The
@@ -87,7 +91,7 @@ def k_code_position(D: int, tau: int, j: int):
     g, upper = tau % 8, tau // 8
     lane = 4 * g + t
     word = 16 * (32 * (kc // 4) + lane) + 4 * (kc % 4)
-    return word + h + 2 * e, 4 * upper
+    return word + e + 2 * h, 4 * upper
 
 
 def v_code_position(D: int, tau: int, j: int):
@@ -96,8 +100,17 @@ def v_code_position(D: int, tau: int, j: int):
     t, e, h = (tau % 8) // 2, tau % 2, tau // 8
     w, c = divmod(nc, 4)
     lane = 4 * g + t
-    bit = 2 * c + 8 * h + 16 * e
+    bit = 8 * c + 2 * h + 4 * e
     return 8 * (32 * (w // 2) + lane) + 4 * (w % 2) + bit // 8, bit % 8
+
+
+def plane_bit(w: int, f: int, h: int, ep: int) -> int:
+    """Bit of element (h, e') of fragment f in a plane word of width w."""
+    if w == 4:
+        return 4 * f + 8 * ep + 16 * h
+    if w == 2:
+        return 8 * f + 2 * h + 4 * ep
+    return f + 8 * h + 16 * ep
 
 
 def k_plane_position(D: int, tau: int, j: int, w: int):
@@ -109,7 +122,7 @@ def k_plane_position(D: int, tau: int, j: int, w: int):
     lane = 4 * g + t
     word, f = divmod(2 * kc + e, F)
     U = min(4, D * w // 64)
-    bit = w * f + 8 * h + 16 * ep
+    bit = plane_bit(w, f, h, ep)
     return 4 * U * (32 * (word // U) + lane) + 4 * (word % U) + bit // 8, bit % 8
 
 
@@ -120,7 +133,7 @@ def v_plane_position(D: int, tau: int, j: int, w: int):
     t, ep, h = (tau % 8) // 2, tau % 2, tau // 8
     lane = 4 * g + t
     word, f = divmod(nc, F)
-    bit = w * f + 8 * h + 16 * ep
+    bit = plane_bit(w, f, h, ep)
     return 4 * w * (32 * (word // w) + lane) + 4 * (word % w) + bit // 8, bit % 8
 
 

@@ -200,11 +200,11 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint3
   return r;
 }
 
-// Codes to exact fp16 integers. A 4-bit field at bits 0-3 (and 16-19)
-// OR-ed into 0x6400 (fp16 1024) is 1024 + n; one at bits 4-7 is 1024 + 16n.
-// The offsets below recentre them: 4-bit codes to n - 8, 2-bit codes to
-// n - 2. Every intermediate is an integer below 2048, so each step is exact
-// and the mma sees ordinary normal fp16 operands. (Masked fields used
+// Codes to exact fp16 integers (the MLA latent words and the 1-bit planes).
+// A 4-bit field at bits 0-3 (and 16-19) OR-ed into 0x6400 (fp16 1024) is
+// 1024 + n; one at bits 4-7 is 1024 + 16n. The offsets below recentre them:
+// 4-bit codes to n - 8. Every intermediate is an integer below 2048, so each
+// step is exact and the mma sees ordinary normal fp16 operands. (Masked fields used
 // directly as fp16 subnormals would save the recentring, but the tensor
 // cores align a sum of such products as if the subnormal were 2^-14, which
 // drops about 10 - p bits of a field at bit p from the sum.)
@@ -220,26 +220,6 @@ __device__ __forceinline__ void dequant_k_word(uint32_t x, uint32_t* out) {
   out[1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(x, 0x00F000F0u, kMagic)), s16, o16));
   out[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x000F000Fu, kMagic)), sub));
   out[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00F000F0u, kMagic)), s16, o16));
-}
-
-// One V word -> 8 half2: fields at bits 2c, 2c + 16 (c = 0..3) as
-// out[c], then the same fields of x >> 8 as out[4 + c].
-__device__ __forceinline__ void dequant_v_word(uint32_t x, uint32_t* out) {
-  const __half2 sub = __halves2half2(__ushort_as_half(0x6402), __ushort_as_half(0x6402));  // 1026
-  const __half2 s4 = __halves2half2(__ushort_as_half(0x3400), __ushort_as_half(0x3400));   // 1/4
-  const __half2 o4 = __halves2half2(__ushort_as_half(0xDC08), __ushort_as_half(0xDC08));   // -258
-  const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
-  const __half2 o16 = __halves2half2(__ushort_as_half(0xD420), __ushort_as_half(0xD420));  // -66
-  const __half2 s64 = __halves2half2(__ushort_as_half(0x2400), __ushort_as_half(0x2400));  // 1/64
-  const __half2 o64 = __halves2half2(__ushort_as_half(0xCC80), __ushort_as_half(0xCC80));  // -18
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const uint32_t y = half ? (x >> 8) : x;
-    out[4 * half + 0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(y, 0x00030003u, kMagic)), sub));
-    out[4 * half + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x000C000Cu, kMagic)), s4, o4));
-    out[4 * half + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00300030u, kMagic)), s16, o16));
-    out[4 * half + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(y, 0x00C000C0u, kMagic)), s64, o64));
-  }
 }
 
 // fp16 bit patterns of small integers (|n| < 2048) and of powers of two,
@@ -271,29 +251,103 @@ __device__ __forceinline__ uint32_t field_h2(uint32_t x) {
     return h2_as_u32(__hfma2(v, h2_bits(fp16_pow2(-P)), h2_bits(fp16_int(-((1024 >> P) + C)))));
 }
 
-// Operand pair (b0, b1) of fragment slot F_ of a code-plane word pair: b0
-// from the word, b1 from the word >> 8 (see the page format).
-template <int W, int SLOT, int C>
-__device__ __forceinline__ void plane_pair(uint32_t x, uint32_t& b0, uint32_t& b1) {
-  b0 = field_h2<W, W * SLOT, C>(x);
-  b1 = field_h2<W, W * SLOT, C>(x >> 8);
+// ---- code planes to tensor-core operands (page format in include/kvarn.h)
+// Blackwell converts a pair of 6-bit e2m3 values (one per byte of a 16-bit
+// half-word, bits 6-7 of each byte ignored) or of 4-bit e2m1 values (the two
+// nibbles of a byte) to an fp16 pair in one instruction. With the sign and
+// the upper exponent bit clear both formats are linear in their low bits: a
+// 4-bit field n is the e2m3 value n / 8 (n < 8 subnormal m/8, n >= 8 the
+// normal 1 + m/8) and a 2-bit field n the e2m1 value n / 2. Both are exact
+// normal fp16 numbers, so a plane word becomes operands with one mask per
+// four (4-bit) or eight (2-bit) registers and one conversion per register.
+__device__ __forceinline__ uint32_t e2m3x2_lo(uint32_t x) {  // bytes 0, 1 -> fp16 pair
+  uint32_t r;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e2m3x2 %0, l; }" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t e2m3x2_hi(uint32_t x) {  // bytes 2, 3 -> fp16 pair
+  uint32_t r;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e2m3x2 %0, h; }" : "=r"(r) : "r"(x));
+  return r;
+}
+template <int BYTE>  // the two nibbles of byte BYTE -> fp16 pair (low nibble in the low half)
+__device__ __forceinline__ uint32_t e2m1x2_byte(uint32_t x) {
+  uint32_t r;
+  if constexpr (BYTE == 0)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, a; }" : "=r"(r) : "r"(x));
+  else if constexpr (BYTE == 1)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(r) : "r"(x));
+  else if constexpr (BYTE == 2)
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, c; }" : "=r"(r) : "r"(x));
+  else
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %1; cvt.rn.f16x2.e2m1x2 %0, d; }" : "=r"(r) : "r"(x));
+  return r;
 }
 
-// Operand pair of a B-bit code (one or two planes) as exact fp16 (n - 2^(B-1)).
-// x0 / x1: the words of plane 0 / plane 1 holding the fragment; S0 / S1 its
-// slots in them.
+// Bit of element (h, e') (operand register h, its half e') of fragment f in
+// a plane word of width w (page format in include/kvarn.h).
+__host__ __device__ constexpr int plane_bit(int w, int f, int h, int ep) {
+  return w == 4 ? 4 * f + 8 * ep + 16 * h : w == 2 ? 8 * f + 2 * h + 4 * ep : f + 8 * h + 16 * ep;
+}
+
+// Scale of a plane's operand values: a w-bit field n becomes plane_kappa(w) * n.
+__host__ __device__ constexpr float plane_kappa(int w) { return w == 4 ? 0.125f : w == 2 ? 0.5f : 1.f; }
+// Operand value of a b-bit code n: code_kappa(b) * (n - code_center(b)).
+// One-plane codes (2 and 4 bits) are used as they are; two-plane codes are
+// recentred on 2^(b-1), which keeps the products of the wide codes near the
+// size of the sums they feed.
+__host__ __device__ constexpr float code_kappa(int b) { return plane_kappa(plane_w0(b)); }
+__host__ __device__ constexpr int code_center(int b) { return plane_w1(b) == 0 ? 0 : 1 << (b - 1); }
+
+// Operand pair (b0, b1) of fragment SLOT of a plane word of width W. Width 4:
+// fragment SLOT is the low (0) or high (1) nibble of every byte, b0 the low
+// half-word, b1 the high one, values n / 8. Width 2: fragment SLOT is byte
+// SLOT, its bits 0-1 and 4-5 b0, bits 2-3 and 6-7 b1, values n / 2. Width 1:
+// the fields at bits SLOT and SLOT + 16 form b0, those of the word >> 8 form
+// b1, values n - C.
+template <int W, int SLOT, int C = 0>
+__device__ __forceinline__ void plane_pair(uint32_t x, uint32_t& b0, uint32_t& b1) {
+  if constexpr (W == 4) {
+    const uint32_t m = (SLOT ? (x >> 4) : x) & 0x0F0F0F0Fu;
+    b0 = e2m3x2_lo(m);
+    b1 = e2m3x2_hi(m);
+  } else if constexpr (W == 2) {
+    b0 = e2m1x2_byte<SLOT>(x & 0x33333333u);
+    b1 = e2m1x2_byte<SLOT>((x >> 2) & 0x33333333u);
+  } else {
+    b0 = field_h2<W, W * SLOT, C>(x);
+    b1 = field_h2<W, W * SLOT, C>(x >> 8);
+  }
+}
+
+// Operand pair of a B-bit code (one or two planes) as exact fp16
+// code_kappa(B) * (n - code_center(B)). x0 / x1: the words of plane 0 /
+// plane 1 holding the fragment; S0 / S1 its slots in them. Two planes
+// combine as kappa0 n0 + 2^W0 kappa0 (n1 - 2^(B-1-W0)): a 1-bit plane takes
+// its offset in its own conversion, a 2- or 4-bit plane (value kappa1 n1)
+// after the combination. Every value is a multiple of kappa0 of magnitude
+// at most 2^(B-1) kappa0 <= 16, exact in fp16.
 template <int B, int S0, int S1>
 __device__ __forceinline__ void code_pair(uint32_t x0, uint32_t x1, uint32_t& b0, uint32_t& b1) {
   constexpr int W0 = plane_w0(B), W1 = plane_w1(B);
   if constexpr (W1 == 0) {
-    plane_pair<W0, S0, (1 << (B - 1))>(x0, b0, b1);
+    plane_pair<W0, S0>(x0, b0, b1);
   } else {
     uint32_t l0, l1, h0, h1;
-    plane_pair<W0, S0, 0>(x0, l0, l1);
-    plane_pair<W1, S1, (1 << (B - 1 - W0))>(x1, h0, h1);
-    const __half2 sc = h2_bits(fp16_pow2(W0));
-    b0 = h2_as_u32(__hfma2(u32_as_h2(h0), sc, u32_as_h2(l0)));
-    b1 = h2_as_u32(__hfma2(u32_as_h2(h1), sc, u32_as_h2(l1)));
+    plane_pair<W0, S0>(x0, l0, l1);
+    constexpr int LOG2_K0 = W0 == 4 ? -3 : -1;
+    if constexpr (W1 == 1) {
+      plane_pair<1, S1, (1 << (B - 1 - W0))>(x1, h0, h1);
+      const __half2 sc = h2_bits(fp16_pow2(W0 + LOG2_K0));
+      b0 = h2_as_u32(__hfma2(u32_as_h2(h0), sc, u32_as_h2(l0)));
+      b1 = h2_as_u32(__hfma2(u32_as_h2(h1), sc, u32_as_h2(l1)));
+    } else {
+      plane_pair<W1, S1>(x1, h0, h1);
+      const __half2 sc = h2_bits(fp16_pow2(W0 + LOG2_K0 - (W1 == 4 ? -3 : -1)));
+      const __half2 ctr = h2_bits(fp16_pow2(B - 1 + LOG2_K0));
+      b0 = h2_as_u32(__hsub2(__hfma2(u32_as_h2(h0), sc, u32_as_h2(l0)), ctr));
+      b1 = h2_as_u32(__hsub2(__hfma2(u32_as_h2(h1), sc, u32_as_h2(l1)), ctr));
+    }
   }
 }
 

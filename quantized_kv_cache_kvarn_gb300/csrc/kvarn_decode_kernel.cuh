@@ -21,15 +21,13 @@
 //   q~ = (kappa q H) * c_K, split into fp16 hi + lo rows of the mma A tile
 //        (rows 0-7 hi, 8-15 lo: the G <= 8 query heads of the group leave
 //        half of the m16 tile free, so the split costs no extra mma);
-//   S  = q~ . (K codes - 8)^T with mma.sync m16n8k16 (K codes as exact fp16
-//        integers, made from the packed nibbles by exponent-bias arithmetic;
-//        recentred codes keep every running sum near the size of its result,
-//        which the tensor cores need: they round a sum relative to its
-//        largest term);
-//   s  = a_K * S + (b_K + 8 a_K) * sum(q~)      (row scales folded back in);
+//   S  = q~ . (K codes / 8)^T with mma.sync m16n8k16 (the codes as exact fp16
+//        multiples of 1/8, one hardware e2m3 -> fp16 conversion per operand
+//        register after one mask per four registers);
+//   s  = 8 a_K * S + b_K * sum(q~)              (row scales folded back in);
 //   online softmax in base 2;
-//   u  = (p * a_V)(V codes - 2) with the same hi/lo A tile;
-//   acc = acc * alpha + c_V * (u + sum p (b_V + 2 a_V)).
+//   u  = (p * a_V)(V codes / 2) with the same hi/lo A tile (e2m1 -> fp16);
+//   acc = acc * alpha + c_V * (2 u + sum p b_V).
 // The warps of a CTA merge in shared memory and write one partial
 // (max, sum, unnormalised output) per segment; the raw partials (original
 // basis) sit in the slots after the tile partials, and each row's count of
@@ -84,7 +82,9 @@ struct DecShape {
   static constexpr int KU0 = D * KW0 / 64 < 4 ? D * KW0 / 64 : 4;
   static constexpr int KU1 = KW1 ? (D * KW1 / 64 < 4 ? D * KW1 / 64 : 4) : 1;
   static constexpr int KR1 = 2 * D * KW0, VR1 = 2 * D * VW0;
-  static constexpr float KCENTER = static_cast<float>(1 << (KB - 1)), VCENTER = static_cast<float>(1 << (VB - 1));
+  // operand values are code_kappa(bits) * (code - code_center(bits))
+  static constexpr float KINV = 1.f / code_kappa(KB), VINV = 1.f / code_kappa(VB);
+  static constexpr float KCENTER = static_cast<float>(code_center(KB)), VCENTER = static_cast<float>(code_center(VB));
   static constexpr int RING = UNITS * WARP_SMEM;
   static constexpr int XS = 2 * (N / 8) + 2;  // exchanged per lane: partial scores, two timeout flags
   static constexpr int XBUF = HV == 2 ? UNITS * 2 * 32 * XS * 4 : 0;
@@ -280,8 +280,14 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
 }
 
 // Resident CTAs per SM the kernel is compiled for: 3 x 4 warps at head_dim
-// 128 (168 registers); 5 x 2 warps at 256 (a warp pair, up to 204 registers).
-template <int D, int W> constexpr int decode_min_ctas() { return W == 4 ? KVARN_DECODE_MIN_CTAS : D == 256 ? 5 : 1; }
+// 128 (168 registers); 4 x 2 warps at 256 (a warp pair, up to 255 registers:
+// at 5 CTAs the pair's 204 registers spill).
+#ifndef KVARN_DECODE_MIN_CTAS_256
+#define KVARN_DECODE_MIN_CTAS_256 4
+#endif
+template <int D, int W> constexpr int decode_min_ctas() {
+  return W == 4 ? KVARN_DECODE_MIN_CTAS : D == 256 ? KVARN_DECODE_MIN_CTAS_256 : 1;
+}
 
 // ---------------------------------------------------------- work mapping
 // The compressed tiles of all (sequence, unit) pairs form one flattened
@@ -563,7 +569,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const int idx = (nb & 1) * 8 + 2 * t;
       const float2 ka = load_scale2<SB>(pg + PG.k_a() + idx * SB);
       const float2 kb = load_scale2<SB>(pg + PG.k_b() + idx * SB);
-      s[nb] = f2fma(ka, s[nb], f2mul(f2fma(f2(S::KCENTER), ka, kb), qsum));
+      const float2 kb_c = S::KCENTER != 0.f ? f2fma(f2(S::KCENTER), ka, kb) : kb;
+      s[nb] = f2fma(f2mul(ka, f2(S::KINV)), s[nb], f2mul(kb_c, qsum));
     }
     if constexpr (HV == 2) {
 #pragma unroll
@@ -623,8 +630,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const float2 va1 = load_scale2<SB>(pg + PG.v_a() - S::KP + (8 + 2 * t) * SB);
       const float2 vb0 = load_scale2<SB>(pg + PG.v_b() - S::KP + (2 * t) * SB);
       const float2 vb1 = load_scale2<SB>(pg + PG.v_b() - S::KP + (8 + 2 * t) * SB);
-      be2 = f2fma(s[2 * pp], f2fma(f2(S::VCENTER), va0, vb0), be2);
-      be2 = f2fma(s[2 * pp + 1], f2fma(f2(S::VCENTER), va1, vb1), be2);
+      be2 = f2fma(s[2 * pp], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va0, vb0) : vb0, be2);
+      be2 = f2fma(s[2 * pp + 1], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va1, vb1) : vb1, be2);
       split_hi_lo2(f2mul(s[2 * pp], va0), Ap[pp][0], Ap[pp][1]);
       split_hi_lo2(f2mul(s[2 * pp + 1], va1), Ap[pp][2], Ap[pp][3]);
     }
@@ -658,7 +665,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         const int ch = 8 * nc + 2 * t;
         const float2 cv = load_scale2<SB>(vslot + (ch / S::CPP) * S::VP + PG.v_col() - S::KP + (ch % S::CPP) * SB);
         const float2 uk = f2add(make_float2(u[k][0], u[k][1]), make_float2(u[k][2], u[k][3]));
-        acc[ncl] = f2fma(cv, f2add(uk, beta), acc[ncl]);
+        acc[ncl] = f2fma(cv, f2fma(uk, f2(S::VINV), beta), acc[ncl]);
       }
     }
     if constexpr (HV == 2) {  // both warps are done with the V slot

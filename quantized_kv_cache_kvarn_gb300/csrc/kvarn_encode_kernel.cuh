@@ -391,7 +391,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
             const int ch = IS_V ? 8 * fg + g : 16 * (fg >> 1) + 2 * t + ep + 8 * h;
             const int tok = IS_V ? 2 * t + ep + 8 * h : 8 * (fg & 1) + g;
             const uint32_t field = (cb[(pg * kPageTokens + tok) * D + ch] >> shift) & ((1u << w) - 1u);
-            word |= field << (w * f + 8 * h + 16 * ep);
+            word |= field << plane_bit(w, f, h, ep);
           }
       }
       img[ws] = word;
@@ -404,37 +404,39 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       const uint32_t* P0 = Pc[2 * ip];      // token g of the page
       const uint32_t* P1 = Pc[2 * ip + 1];  // token g + 8
       if constexpr (!IS_V) {
-        // 4-bit: word (kc = seg, lane 4g + t) bytes = channels 2t, 2t+8,
-        // 2t+1, 2t+9; token g in the low nibble, token g + 8 in the high one
+        // 4-bit: word (kc = seg, lane 4g + t) bytes = channels 2t, 2t+1,
+        // 2t+8, 2t+9; token g in the low nibble, token g + 8 in the high one
         uint32_t* img = reinterpret_cast<uint32_t*>(stage) + pg * 2 * D;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+          const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;
           const uint32_t w0 = __byte_perm(P0[t >> 1], P0[2 + (t >> 1)], sel);
           const uint32_t w1 = __byte_perm(P1[t >> 1], P1[2 + (t >> 1)], sel);
           img[((seg >> 2) * 32 + 4 * g + t) * 4 + (seg & 3)] = w0 | (w1 << 4);
         }
       } else {
-        // 2-bit: channel 16 seg + g' (block 2 seg) and 16 seg + 8 + g' (block
-        // 2 seg + 1) of this token land at bits 2c, c = 2 (seg % 2) + {0, 1},
-        // of byte h + 2e of word (w = seg / 2, lane 4 g' + t); this thread's
-        // two tokens are h = 0 and h = 1. Byte g' of A/B: channel g' | g'+8 << 2.
-        uint32_t A0 = P0[0] | (P0[2] << 2), B0 = P0[1] | (P0[3] << 2);
-        uint32_t A1 = P1[0] | (P1[2] << 2), B1 = P1[1] | (P1[3] << 2);
-        const uint32_t oA0 = __shfl_xor_sync(0xffffffffu, A0, 1), oB0 = __shfl_xor_sync(0xffffffffu, B0, 1);
-        const uint32_t oA1 = __shfl_xor_sync(0xffffffffu, A1, 1), oB1 = __shfl_xor_sync(0xffffffffu, B1, 1);
-        if (s_par == 0) {
-          A0 |= oA0 << 4; B0 |= oB0 << 4; A1 |= oA1 << 4; B1 |= oB1 << 4;
-          const int tau = g, t = tau >> 1, e = tau & 1, w = w_pair;
-          uint16_t* img = reinterpret_cast<uint16_t*>(stage) + pg * 2 * D;
-          // halfword of channel g' = (byte of token g, byte of token g + 8)
-          const uint32_t hw[4] = {__byte_perm(A0, A1, 0x5140), __byte_perm(A0, A1, 0x7362),
-                                  __byte_perm(B0, B1, 0x5140), __byte_perm(B0, B1, 0x7362)};
+        // 2-bit: byte c of word (lane 4g' + t, w) is channel 8(4w + c) + g'
+        // with tokens 2t, 2t + 8, 2t + 1, 2t + 9 at bits 0, 2, 4, 6. This
+        // thread holds tokens g and g + 8 of channels 16 seg + 0..15; the
+        // thread of token g ^ 1 (lane ^ TPR) holds the other two, so the
+        // pair exchanges its half-bytes and each writes four half-words:
+        // channels g' and 8 + g' (blocks 2 seg and 2 seg + 1) of lane
+        // 4g' + g/2, word seg/2, half-word seg % 2.
+        uint32_t Z[4];
 #pragma unroll
-          for (int gg = 0; gg < 8; ++gg) {
-            const int word = ((w >> 1) * 32 + 4 * gg + t) * 2 + (w & 1);
-            img[2 * word + e] = static_cast<uint16_t>(hw[gg >> 1] >> (16 * (gg & 1)));
-          }
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a = P0[k] | (P1[k] << 2);
+          const uint32_t o = __shfl_xor_sync(0xffffffffu, a, S::TPR);
+          Z[k] = (g & 1) ? (o | (a << 4)) : (a | (o << 4));
+        }
+        uint16_t* img = reinterpret_cast<uint16_t*>(stage) + pg * 2 * D;
+        const int t = g >> 1, wi = seg >> 1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int gp = 4 * (g & 1) + q;  // g' = 0..3 from the even thread, 4..7 from the odd one
+          const uint32_t hw = __byte_perm(Z[gp >> 2], Z[2 + (gp >> 2)], q | ((4 + q) << 4));
+          const int word = 2 * (32 * (wi >> 1) + 4 * gp + t) + (wi & 1);
+          img[2 * word + (seg & 1)] = static_cast<uint16_t>(hw);
         }
       }
     }

@@ -116,18 +116,24 @@ def test_write_read_tile_roundtrip():
 # ------------------------------------------------ other widths (code planes)
 def test_plane_positions_hand_derived():
     """D = 128. K plane: lane 4g + t, fragment 2kc + e, 8/w fragments per word,
-    units of min(4, 2w) words; V plane: fragment nc, units of w words; bit
-    w*f + 8h + 16e' (see the layout module)."""
+    units of min(4, 2w) words; V plane: fragment nc, units of w words; element
+    (h, e') of fragment f at bit 4f + 8e' + 16h (w = 4), 8f + 2h + 4e' (w = 2),
+    f + 8h + 16e' (w = 1) (see the layout module)."""
     cases = {
         # (side, w, tau, j): (byte, shift)
         ("k", 1, 0, 0): (0, 0),
         ("k", 1, 9, 0): (32, 1),      # g1 t0 -> lane 4, e1 -> fragment 1 of word 0; units of 2 words (8 B)
         ("k", 1, 0, 112): (4, 6),     # kc7 -> fragment 14 = word 1, slot 6
         ("k", 1, 7, 127): (255, 6),   # lane 31, fragment 14, h1 e'1 -> bit 30
-        ("k", 2, 8, 0): (0, 2),       # e1 -> slot 1
-        ("k", 2, 0, 16): (0, 4),      # kc1 -> slot 2
+        ("k", 2, 8, 0): (1, 0),       # e1 -> fragment 1 = byte 1
+        ("k", 2, 0, 16): (2, 0),      # kc1 -> fragment 2 = byte 2
         ("k", 2, 0, 32): (4, 0),      # kc2 -> word 1
-        ("k", 2, 15, 127): (511, 6),  # lane 31, fragment 15 = word 3 slot 3, bit 30
+        ("k", 2, 0, 8): (0, 2),       # h1 -> bit 2
+        ("k", 2, 0, 1): (0, 4),       # e'1 -> bit 4
+        ("k", 2, 15, 127): (511, 6),  # lane 31, fragment 15 = word 3 byte 3, h1 e'1 -> bit 30
+        ("k", 4, 0, 1): (1, 0),       # e'1 -> byte 1
+        ("k", 4, 0, 8): (2, 0),       # h1 -> half-word 1
+        ("k", 4, 8, 0): (0, 4),       # e1 -> fragment 1, the high nibble
         ("v", 1, 0, 8): (0, 1),       # block 1 -> slot 1
         ("v", 1, 8, 0): (1, 0),       # h1 -> bit 8
         ("v", 1, 1, 0): (2, 0),       # e'1 -> bit 16
@@ -136,6 +142,8 @@ def test_plane_positions_hand_derived():
         ("v", 4, 0, 8): (0, 4),       # block 1 -> slot 1
         ("v", 4, 0, 16): (4, 0),      # block 2 -> word 1
         ("v", 4, 15, 127): (1023, 4),  # block 15 = word 7 = word 3 of unit 1, lane 31, bit 28
+        ("v", 4, 1, 0): (1, 0),       # token 1: e'1 -> byte 1
+        ("v", 4, 8, 0): (2, 0),       # token 8: h1 -> half-word 1
     }
     for (side, w, tau, j), want in cases.items():
         f = layout.k_plane_position if side == "k" else layout.v_plane_position

@@ -129,7 +129,7 @@ def _k_nibble_order(orig):
         kc, r = divmod(j, 16)
         t, e, h = (r % 8) // 2, r % 2, r // 8
         lane = 4 * (tau % 8) + t
-        return 16 * (32 * (kc // 4) + lane) + 4 * (kc % 4) + e + 2 * h, 4 * (tau // 8)
+        return 16 * (32 * (kc // 4) + lane) + 4 * (kc % 4) + h + 2 * e, 4 * (tau // 8)
     return pos
 
 
@@ -139,7 +139,7 @@ def _v_pair_order(orig):
         nc, g = divmod(j, 8)
         t, e, h = (tau % 8) // 2, tau % 2, tau // 8
         w, c = divmod(nc, 4)
-        bit = 2 * c + 8 * e + 16 * h
+        bit = 8 * c + 4 * h + 2 * e
         return 8 * (32 * (w // 2) + 4 * g + t) + 4 * (w % 2) + bit // 8, bit % 8
     return pos
 
@@ -173,7 +173,7 @@ def _plane_halves_swapped(orig):
         t, ep, h = (r % 8) // 2, r % 2, r // 8
         word, f = divmod(2 * kc + tau // 8, F)
         U = min(4, D * w // 64)
-        bit = w * f + 16 * h + 8 * ep
+        bit = layout.plane_bit(w, f, ep, h)
         return 4 * U * (32 * (word // U) + 4 * (tau % 8) + t) + 4 * (word % U) + bit // 8, bit % 8
     return pos
 
