@@ -118,6 +118,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared by this thread (load/store
+// pipe; no bulk-copy unit involved).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (counts toward the phase: the barrier expects one per thread).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // The waiting thread may be suspended (it issues nothing) until the phase
 // completes or about 20 us pass.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -349,6 +364,17 @@ __device__ __forceinline__ void code_pair(uint32_t x0, uint32_t x1, uint32_t& b0
       b1 = h2_as_u32(__hsub2(__hfma2(u32_as_h2(h1), sc, u32_as_h2(l1)), ctr));
     }
   }
+}
+
+// Pairwise (tree) reduction of a register array in place: log2(N)
+// dependent steps instead of N - 1. Returns a[0].
+template <int N, typename T, typename Op>
+__device__ __forceinline__ T tree_reduce(T (&a)[N], Op op) {
+#pragma unroll
+  for (int w = 1; w < N; w *= 2)
+#pragma unroll
+    for (int i = 0; i + w < N; i += 2 * w) a[i] = op(a[i], a[i + w]);
+  return a[0];
 }
 
 // Compile-time loop: f(std::integral_constant<int, I>) for I in [B, E).

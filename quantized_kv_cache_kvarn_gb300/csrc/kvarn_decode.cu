@@ -57,8 +57,10 @@ DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max
   const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
   const int64_t most = units * std::max(0, max_tiles);
   // four tiles in flight per CTA slot at least, fewer (down to one round)
-  // when the whole batch is too small to fill the GPU
-  p.min_tiles = static_cast<int32_t>(std::max<int64_t>(in_flight, std::min<int64_t>(4 * in_flight, most / resident)));
+  // when the whole batch is too small to fill the GPU; a multiple of the
+  // tiles in flight, the granularity of the CTA ranges
+  const int64_t want = std::max<int64_t>(in_flight, std::min<int64_t>(4 * in_flight, most / resident));
+  p.min_tiles = static_cast<int32_t>((want + in_flight - 1) / in_flight * in_flight);
   p.tile_slots = max_tiles > 0 ? 1 + (max_tiles - 1 + p.min_tiles - 1) / p.min_tiles : 0;
   p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
   p.slots = p.tile_slots + p.raw_splits;

@@ -373,9 +373,19 @@ __device__ __forceinline__ TilePos locate_tile(const DecArgs& A, int N, int64_t 
   return P;
 }
 
+// CTA ranges are cut on multiples of g tiles (the tiles a CTA has in
+// flight), so that a segment inside a range splits evenly over the warps
+// whenever the unit lengths are multiples of g: with T tiles in G =
+// ceil(T / g) groups, CTA c takes groups [c G / C, (c + 1) G / C).
+__device__ __forceinline__ int64_t cta_range_start(int c, int C, int64_t total, int g) {
+  const int64_t G = (total + g - 1) / g;
+  return min(total, static_cast<int64_t>(g) * (c * G / C));
+}
+
 // The CTA whose range holds flattened tile t.
-__device__ __forceinline__ int cta_of_tile(int64_t t, int C, int64_t total) {
-  return static_cast<int>(((t + 1) * C - 1) / total);
+__device__ __forceinline__ int cta_of_tile(int64_t t, int C, int64_t total, int g) {
+  const int64_t G = (total + g - 1) / g;
+  return static_cast<int>(((t / g + 1) * C - 1) / G);
 }
 
 // ------------------------------------------------------------ one segment
@@ -399,7 +409,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 
   constexpr int HV = S::HV, UNITS = S::UNITS;
   const int half = HV == 2 ? (warp & 1) : 0, unit = warp / HV;
-  const bool leader = half == 0;  // issues its unit's copies
+  const bool leader = half == 0;  // writes the unit's results
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
   float* qrot = reinterpret_cast<float*>(smem + S::OFF_QROT);
   float* xbuf = reinterpret_cast<float*>(smem + S::OFF_XBUF);
@@ -416,38 +426,46 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   const int first = t0 + unit;
   const int n_my = !dead && first < t1 ? (t1 - first + UNITS - 1) / UNITS : 0;
   const int32_t* bt = A.bt + static_cast<int64_t>(b) * A.bt_stride;
-  // physical page `lane` (lanes < PPT) of this unit's i-th tile, checked
-  auto page_id = [&](int i) -> int {
-    int phys = 0;
-    if (lane < S::PPT) {
-      phys = bt[(first + i * UNITS) * S::PPT + lane];
-      if (phys < 0 || phys >= A.num_pages) {
-        set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
-        phys = 0;
-      }
+  // physical page `lane` (lanes < PPT) of this unit's i-th tile; the load is
+  // issued a tile ahead and checked only where the copy needs it, so that
+  // no instruction waits on it early
+  auto page_load = [&](int i) -> int { return lane < S::PPT ? bt[(first + i * UNITS) * S::PPT + lane] : 0; };
+  auto page_check = [&](int phys) -> int {
+    if (phys < 0 || phys >= A.num_pages) {
+      set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
+      phys = 0;
     }
     return phys;
   };
   auto page_at = [&](int phys) { return A.cache + (static_cast<int64_t>(phys) * A.Hkv + kvh) * S::PB; };
+  // The unit's HV warps copy the tile's page parts into the slot 16 bytes a
+  // thread at a time (cp.async on the load/store pipe: sixteen bulk copies
+  // a tile serialised on the SM's copy unit cost a sixth of the tile loop);
+  // each thread then arrives on the slot's barrier once its copies land.
+  // Page p's physical id sits in lane p (page ids are read by lanes < PPT).
+  auto issue_part = [&](int phys, unsigned char* slot, int part_off, int part_bytes, uint64_t* bar) {
+    __syncwarp();  // every lane's reads of the slot precede the copies
+    const int tid = half * 32 + lane;
+#pragma unroll
+    for (int p = 0; p < S::PPT; ++p) {
+      const unsigned char* src = page_at(__shfl_sync(0xffffffffu, phys, p)) + part_off;
+      unsigned char* dst = slot + p * part_bytes;
+#pragma unroll
+      for (int c = tid; c < part_bytes / 16; c += 32 * HV) cp_async16(dst + 16 * c, src + 16 * c);
+    }
+    cp_async_arrive(bar);
+  };
   auto issue_k = [&](int phys) {
     ph += 1u << 16;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(barK, S::KSLOT);
-    __syncwarp();
-    if (lane < S::PPT) bulk_g2s(kslot + lane * S::KP, page_at(phys), S::KP, barK);
+    issue_part(phys, kslot, 0, S::KP, barK);
   };
   auto issue_v = [&](int phys) {
     ph += 1u << 24;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(barV, S::VSLOT);
-    __syncwarp();
-    if (lane < S::PPT) bulk_g2s(vslot + lane * S::VP, page_at(phys) + S::KP, S::VP, barV);
+    issue_part(phys, vslot, S::KP, S::VP, barV);
   };
 
-  if (leader && n_my > 0) {
-    const int phys = page_id(0);
+  if (n_my > 0) {
+    const int phys = page_check(page_load(0));
     issue_k(phys);
     issue_v(phys);
   }
@@ -486,7 +504,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   bool timed_out = false;
   for (int i = 0; i < n_my; ++i) {
     // the next tile's page ids, loaded a tile ahead of their copies
-    const int phys_next = leader && i + 1 < n_my ? page_id(i + 1) : 0;
+    int phys_next = i + 1 < n_my ? page_load(i + 1) : 0;
     // a warp of a pair that gives up on a copy tells its partner at the next
     // pair barrier and both leave together
     bool late = !mbar_wait_bounded(barK, ph & 1);
@@ -499,7 +517,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     }
     // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels)
     uint32_t Aq[KCW][4];
-    float2 qs2 = f2(0.f);
+    float2 qs2[KCW];
 #pragma unroll
     for (int kcl = 0; kcl < KCW; ++kcl) {
       const int kc = half * KCW + kcl;
@@ -508,13 +526,14 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * SB;
       const float2 x01 = f2mul(make_float2(qv.x, qv.y), load_scale2<SB>(cp));
       const float2 x89 = f2mul(make_float2(qv.z, qv.w), load_scale2<SB>(cp + 8 * SB));
-      qs2 = f2add(qs2, f2add(x01, x89));
+      qs2[kcl] = f2add(x01, x89);
       split_hi_lo2(x01, Aq[kcl][0], Aq[kcl][1]);
       split_hi_lo2(x89, Aq[kcl][2], Aq[kcl][3]);
     }
-    const float2 qsum = f2(warp_sum_xor(qs2.x + qs2.y, 1, 4));
+    const float2 q2 = tree_reduce(qs2, [](float2 a, float2 b) { return f2add(a, b); });
+    const float2 qsum = f2(warp_sum_xor(q2.x + q2.y, 1, 4));
 
-    // -- S = q~ . (K codes - 2^(KB-1)), two pages (four 8-token blocks) at a
+    // -- S = q~ . (kappa_K codes)^T, two pages (four 8-token blocks) at a
     //    time so that four independent accumulator chains hide the mma
     //    latency. Per group of four k-chunks a lane's fragments (2 kc + e,
     //    e the token block) are KW consecutive words of each code plane.
@@ -592,24 +611,29 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         break;
       }
     }
-    float mt = -INFINITY;
+    float mts[S::NB];
 #pragma unroll
-    for (int nb = 0; nb < S::NB; ++nb) mt = fmaxf(mt, fmaxf(s[nb].x, s[nb].y));
+    for (int nb = 0; nb < S::NB; ++nb) mts[nb] = fmaxf(s[nb].x, s[nb].y);
+    float mt = tree_reduce(mts, [](float a, float b) { return fmaxf(a, b); });
     mt = warp_max_xor(mt, 1, 4);
     const float m_new = fmaxf(m, mt);
     const float alpha = fast_exp2(m - m_new);
-    float2 ps2 = f2(0.f);
+    float2 ps2[S::NB];
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
       const float2 z = f2add(s[nb], f2(-m_new));
       s[nb] = make_float2(fast_exp2(z.x), fast_exp2(z.y));
-      ps2 = f2add(ps2, s[nb]);
+      ps2[nb] = s[nb];
     }
-    lsum = fmaf(lsum, alpha, ps2.x + ps2.y);
+    const float2 pt = tree_reduce(ps2, [](float2 a, float2 b) { return f2add(a, b); });
+    lsum = fmaf(lsum, alpha, pt.x + pt.y);
     m = m_new;
 
     // the K slot is free: start the next tile's K part
-    if (leader && i + 1 < n_my) issue_k(phys_next);
+    if (i + 1 < n_my) {
+      phys_next = page_check(phys_next);
+      issue_k(phys_next);
+    }
 
     late = !mbar_wait_bounded(barV, (ph >> 8) & 1);
     ph += 1u << 8;
@@ -622,7 +646,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 
     // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
     uint32_t Ap[S::PPT][4];
-    float2 be2 = f2(0.f);
+    float2 be2[S::PPT];
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
       const unsigned char* pg = vslot + pp * S::VP;
@@ -630,12 +654,13 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const float2 va1 = load_scale2<SB>(pg + PG.v_a() - S::KP + (8 + 2 * t) * SB);
       const float2 vb0 = load_scale2<SB>(pg + PG.v_b() - S::KP + (2 * t) * SB);
       const float2 vb1 = load_scale2<SB>(pg + PG.v_b() - S::KP + (8 + 2 * t) * SB);
-      be2 = f2fma(s[2 * pp], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va0, vb0) : vb0, be2);
-      be2 = f2fma(s[2 * pp + 1], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va1, vb1) : vb1, be2);
+      be2[pp] = f2fma(s[2 * pp], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va0, vb0) : vb0,
+                      f2mul(s[2 * pp + 1], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va1, vb1) : vb1));
       split_hi_lo2(f2mul(s[2 * pp], va0), Ap[pp][0], Ap[pp][1]);
       split_hi_lo2(f2mul(s[2 * pp + 1], va1), Ap[pp][2], Ap[pp][3]);
     }
-    const float2 beta = f2(warp_sum_xor(be2.x + be2.y, 1, 4));
+    const float2 bt2 = tree_reduce(be2, [](float2 a, float2 b) { return f2add(a, b); });
+    const float2 beta = f2(warp_sum_xor(bt2.x + bt2.y, 1, 4));
 
 #pragma unroll
     for (int nc = 0; nc < NCW; ++nc) acc[nc] = f2mul(acc[nc], f2(alpha));
@@ -677,10 +702,11 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         break;
       }
     }
-    if (leader && i + 1 < n_my) issue_v(phys_next);
+    if (i + 1 < n_my) issue_v(phys_next);
   }
-  if (timed_out && leader) {
-    if (lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+  if (timed_out) {
+    if (leader && lane == 0) set_error(A.err, KVARN_DEVERR_TIMEOUT);
+    cp_async_wait_all();  // this thread's copies have landed (a hardware wait, like a load's)
     // wait (bounded) for the last copy of each slot this warp started (a
     // parity whose phase precedes the barrier's first completes at once); no
     // copy is started after a time-out
@@ -740,8 +766,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
     if (warp % S::HV == 0 && lane == 0) {
-      mbar_init(bars + 2 * (warp / S::HV), 1);
-      mbar_init(bars + 2 * (warp / S::HV) + 1, 1);
+      mbar_init(bars + 2 * (warp / S::HV), 32 * S::HV);  // one arrival per copying thread
+      mbar_init(bars + 2 * (warp / S::HV) + 1, 32 * S::HV);
     }
     fence_mbar_init();
   }
@@ -770,7 +796,7 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
       int count = 0;
       if (n > 0) {
         const int64_t u0 = tiles_before(A, N, b) + static_cast<int64_t>(x) * n;
-        count = cta_of_tile(u0 + n - 1, C, total) - cta_of_tile(u0, C, total) + 1;
+        count = cta_of_tile(u0 + n - 1, C, total, S::UNITS) - cta_of_tile(u0, C, total, S::UNITS) + 1;
       }
       const RowMap R(A, x / A.Hkv);
       if (lane < R.n)
@@ -786,8 +812,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   //      reads in this pass, and read after the segment's closing barrier.
   __shared__ int64_t pos[3];  // current tile (two entries), end of the range
   if (threadIdx.x == 0) {
-    pos[0] = blockIdx.x * total / C;
-    pos[2] = (blockIdx.x + 1) * total / C;
+    pos[0] = cta_range_start(blockIdx.x, C, total, S::UNITS);
+    pos[2] = cta_range_start(blockIdx.x + 1, C, total, S::UNITS);
   }
   __syncthreads();
   uint32_t ph = 0;
@@ -798,7 +824,7 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
     const TilePos P = locate_tile(A, N, cur);
     if (P.b < 0) break;  // unreachable: cur < total
     const int64_t seg_end = min(stop, P.u0 + P.n);
-    const int slot = static_cast<int>(blockIdx.x) - cta_of_tile(P.u0, C, total);
+    const int slot = static_cast<int>(blockIdx.x) - cta_of_tile(P.u0, C, total, S::UNITS);
     const int t0 = A.sink_tiles + P.tile;
     const int t1 = t0 + static_cast<int>(seg_end - cur);
     if (threadIdx.x == 0) pos[k ^ 1] = seg_end;
