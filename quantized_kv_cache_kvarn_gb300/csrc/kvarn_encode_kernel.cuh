@@ -38,18 +38,18 @@ struct EncShape {
   static constexpr int PPC = ROWS / kPageTokens;  // pages per CTA
   static_assert(ROWS == RPT * NW * RPW, "tile rows must cover the CTA");
   static_assert(NT >= D, "one thread per channel finishes the column statistics");
-  static constexpr int RED_BYTES = NW * D * 4;
+  static constexpr int RED_BYTES = NW * D * 8;  // (mean, M2) per warp and channel
   // packed words (4-bit K / 2-bit V); the generic path stages one byte per
   // code plus the packed image of up to 8 bits per code
   static constexpr int CODE_BYTES = GEN ? 2 * ROWS * D : ROWS * D / 2;
   static constexpr int SCRATCH = RED_BYTES > CODE_BYTES ? RED_BYTES : CODE_BYTES;
-  // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][D] | pages[PPC]
+  // scratch | colbuf[D] | rowA[ROWS] | rowB[ROWS] | colC[D] | colpart[2][2][D] | pages[PPC]
   static constexpr int OFF_COLBUF = SCRATCH;
   static constexpr int OFF_ROWA = OFF_COLBUF + 4 * D;
   static constexpr int OFF_ROWB = OFF_ROWA + 4 * ROWS;
   static constexpr int OFF_COLC = OFF_ROWB + 4 * ROWS;
   static constexpr int OFF_COLPART = OFF_COLC + 4 * D;
-  static constexpr int OFF_PAGES = OFF_COLPART + 8 * D;
+  static constexpr int OFF_PAGES = OFF_COLPART + 16 * D;
   static constexpr int SMEM = OFF_PAGES + 8 * PPC;
 };
 
@@ -71,42 +71,72 @@ struct EncodeArgs {
   uint32_t* err;
 };
 
-// Column statistic: every thread passes its 16 per-channel partial sums over
-// its rows. Returns, in thread tid < D, the sum over the whole tile (both
-// CTAs of a cluster) for channel tid; other threads get 0. colpart is the
-// buffer of this statistic (callers alternate two), so that one cluster
-// barrier per statistic keeps a fast CTA from overwriting a partial that its
-// peer has not read yet.
+// Merge of two (mean, M2) summaries of n values each (Chan, Golub and
+// LeVeque's pairwise update of the sum of squared deviations): the mean of
+// 2n values and their M2. Written symmetrically in a and b, so that the two
+// lanes of a butterfly (or the two CTAs of a cluster) hold bit-identical
+// results.
+__device__ __forceinline__ float2 merge_moments(float2 a, float2 b, float n) {
+  const float d = b.x - a.x;
+  return make_float2(0.5f * (a.x + b.x), (a.y + b.y) + 0.5f * n * d * d);
+}
+
+// Column moments in one reduction: every thread passes, per channel of its
+// segment, the mean and M2 of its RPT rows. Returns, in thread tid < D, the
+// population mean and variance over the whole tile (both CTAs of a cluster)
+// of channel tid; other threads get (0, 0). colpart (2 x D floats) is this
+// statistic's cluster exchange buffer (callers alternate two).
 template <int D, int N, int CS>
-__device__ __forceinline__ float column_total(float (&s)[16], float* red, float* colpart) {
-  using S = EncShape<D, N, CS>;  // the statistics part of the shape does not depend on GEN
+__device__ __forceinline__ float2 column_moments(float2 (&mo)[16], float* red, float* colpart) {
+  using S = EncShape<D, N, CS>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, seg = lane % S::TPR;
+  float n = static_cast<float>(S::RPT);
 #pragma unroll
-  for (int e = 0; e < 16; ++e)
+  for (int o = S::TPR; o < 32; o <<= 1) {
 #pragma unroll
-    for (int o = S::TPR; o < 32; o <<= 1) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
+    for (int e = 0; e < 16; ++e) {
+      const float2 b = make_float2(__shfl_xor_sync(0xffffffffu, mo[e].x, o), __shfl_xor_sync(0xffffffffu, mo[e].y, o));
+      mo[e] = merge_moments(mo[e], b, n);
+    }
+    n *= 2.f;
+  }
   if (lane < S::TPR) {
-    float4* dst = reinterpret_cast<float4*>(red + warp * D + seg * 16);
+    float4* dm = reinterpret_cast<float4*>(red + warp * D + seg * 16);
+    float4* dv = reinterpret_cast<float4*>(red + (S::NW + warp) * D + seg * 16);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dst[e] = make_float4(s[4 * e], s[4 * e + 1], s[4 * e + 2], s[4 * e + 3]);
+    for (int e = 0; e < 4; ++e) {
+      dm[e] = make_float4(mo[4 * e].x, mo[4 * e + 1].x, mo[4 * e + 2].x, mo[4 * e + 3].x);
+      dv[e] = make_float4(mo[4 * e].y, mo[4 * e + 1].y, mo[4 * e + 2].y, mo[4 * e + 3].y);
+    }
   }
   __syncthreads();
-  float t = 0.f;
+  float2 t = make_float2(0.f, 0.f);
   if (threadIdx.x < D) {
-#pragma unroll 8
-    for (int w = 0; w < S::NW; ++w) t += red[w * D + threadIdx.x];
+    float2 w[S::NW];
+#pragma unroll
+    for (int i = 0; i < S::NW; ++i) w[i] = make_float2(red[i * D + threadIdx.x], red[(S::NW + i) * D + threadIdx.x]);
+    float nw = static_cast<float>(S::RPT * S::RPW);  // rows per warp
+#pragma unroll
+    for (int st = 1; st < S::NW; st *= 2) {
+#pragma unroll
+      for (int i = 0; i + st < S::NW; i += 2 * st) w[i] = merge_moments(w[i], w[i + st], nw);
+      nw *= 2.f;
+    }
+    t = w[0];
   }
   if constexpr (CS > 1) {
     cg::cluster_group cl = cg::this_cluster();
-    if (threadIdx.x < D) colpart[threadIdx.x] = t;
+    if (threadIdx.x < D) {
+      colpart[threadIdx.x] = t.x;
+      colpart[D + threadIdx.x] = t.y;
+    }
     cl.sync();
     if (threadIdx.x < D) {
-      const float other = cl.map_shared_rank(colpart, cl.block_rank() ^ 1)[threadIdx.x];
-      // both CTAs add in rank order, so they hold bit-identical sums
-      t = cl.block_rank() == 0 ? t + other : other + t;
+      const float* o = cl.map_shared_rank(colpart, cl.block_rank() ^ 1);
+      t = merge_moments(t, make_float2(o[threadIdx.x], o[D + threadIdx.x]), static_cast<float>(S::ROWS));
     }
   }
-  return t;
+  return make_float2(t.x, t.y * (1.f / N));
 }
 
 // Reads the 16 broadcast per-channel values of this thread's segment.
@@ -240,39 +270,30 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   float rscale[S::RPT];
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) rscale[i] = 1.f;
-  const float invN = 1.f / N, invD = 1.f / D;
+  const float invD = 1.f / D;
 
 #pragma unroll 1
   for (int it = 0; it < A.norm_iters; ++it) {
-    float s[16];
-    // column means
+    // column pass: mean and M2 of this thread's rows per channel, merged
+    // over the tile in one reduction
+    float2 mo[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       float t = 0.f;
 #pragma unroll
       for (int i = 0; i < S::RPT; ++i) t += x[i][e];
-      s[e] = t;
-    }
-    const float cmean = column_total<D, N, CS>(s, red, colpart) * invN;
-    if (tid < D) colbuf[tid] = cmean;
-    __syncthreads();
-    float mean[16];
-    read_segment<D>(mean, colbuf, seg);
-    // column variances about the mean
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float t = 0.f;
+      const float m = t * (1.f / S::RPT);
+      float v = 0.f;
 #pragma unroll
       for (int i = 0; i < S::RPT; ++i) {
-        const float dv = x[i][e] - mean[e];
-        t = fmaf(dv, dv, t);
+        const float dv = x[i][e] - m;
+        v = fmaf(dv, dv, v);
       }
-      s[e] = t;
+      mo[e] = make_float2(m, v);
     }
-    const float cvar = column_total<D, N, CS>(s, red, colpart + D) * invN;
-    __syncthreads();  // every thread has read the means out of colbuf
+    const float2 cm = column_moments<D, N, CS>(mo, red, colpart + (it & 1) * 2 * D);
     if (tid < D) {
-      const float sig = safe_sigma(cvar, cmean);
+      const float sig = safe_sigma(cm.y, cm.x);
       cscale *= sig;
       colbuf[tid] = 1.f / sig;
     }
@@ -283,28 +304,34 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     for (int i = 0; i < S::RPT; ++i)
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[i][e] *= inv[e];
-    // row pass: a row lives in TPR consecutive lanes
+    // row pass: a row lives in TPR consecutive lanes; mean and M2 of the
+    // lane's 16 channels, merged over the row's lanes
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i) {
       float t = 0.f;
 #pragma unroll
       for (int e = 0; e < 16; ++e) t += x[i][e];
-      t = warp_sum_xor(t, 1, S::TPR);
-      const float m = t * invD;
+      const float m0 = t * (1.f / 16.f);
       float v = 0.f;
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float dv = x[i][e] - m;
+        const float dv = x[i][e] - m0;
         v = fmaf(dv, dv, v);
       }
-      v = warp_sum_xor(v, 1, S::TPR);
-      const float sig = safe_sigma(v * invD, m);
+      float2 r = make_float2(m0, v);
+      float n = 16.f;
+#pragma unroll
+      for (int o = 1; o < S::TPR; o <<= 1) {
+        r = merge_moments(r, make_float2(__shfl_xor_sync(0xffffffffu, r.x, o), __shfl_xor_sync(0xffffffffu, r.y, o)), n);
+        n *= 2.f;
+      }
+      const float sig = safe_sigma(r.y * invD, r.x);
       rscale[i] *= sig;
       const float ri = 1.f / sig;
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[i][e] *= ri;
     }
-    __syncthreads();  // colbuf is rewritten by the next iteration
+    // colbuf is rewritten next only after the next column reduction's barrier
   }
 
   // ---- asymmetric RTN per row: codes as bytes, Pc[i][k] byte e = channel 4k + e
