@@ -122,7 +122,8 @@ static DensePlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num
                             int32_t num_queries, int32_t max_seq_len, int32_t raw_max) {
   const int32_t G = num_q_heads / L->num_kv_heads;
   return plan_dense_stream(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len / L->tile_tokens,
-                           L->head_dim, L->tile_tokens, raw_max);
+                           L->head_dim, L->tile_tokens, raw_max, L->k_bits ? L->k_bits : 4, L->v_bits ? L->v_bits : 2,
+                           L->scale_dtype == 1 ? 2 : 4);
 }
 
 static int64_t dense_ws(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads, int32_t num_queries,

@@ -49,11 +49,11 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
 int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
-                            int32_t raw_max) {
+                            int32_t raw_max, int32_t kb, int32_t vb, int32_t sb) {
   DensePlan p{};
   // tiles a CTA has in flight: one per warp, one per warp pair at head_dim 256
   const int in_flight = D == 256 ? dense_decode_warps(D) / 2 : dense_decode_warps(D);
-  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N);
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N, kb, vb, sb);
   const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
   const int64_t most = units * std::max(0, max_tiles);
   // four tiles in flight per CTA slot at least, fewer (down to one round)
@@ -74,31 +74,37 @@ int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& p
   return rows * plan.slots * kPStride(D) * 4 + (rows * 4 + 15) / 16 * 16;
 }
 
-template <int D, int N, typename T, int W>
-static int resident_ctas() {
-  using S = DecShape<D, N, W>;
-  auto kern = decode_dense_kernel<D, N, T, W, 4, 2, 4>;
-  const int smem = S::SMEM;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, smem) != cudaSuccess || n < 1)
-    return 1;
-  return n;
-}
-
-// CTAs of the compressed decode kernel that fit on one SM at once (same for
-// fp16 and bf16 queries, which share the register and smem footprint).
-int dense_decode_ctas_per_sm(int32_t D, int32_t N) {
-  static int cache[2][2] = {{0, 0}, {0, 0}};
-  const int di = D == 256, ni = N == 64;
-  if (!cache[di][ni]) {
-    if (D == 128 && N == 128) cache[di][ni] = resident_ctas<128, 128, __half, 4>();
-    else if (D == 128) cache[di][ni] = resident_ctas<128, 64, __half, 4>();
-    else if (N == 128) cache[di][ni] = resident_ctas<256, 128, __half, 2>();
-    else cache[di][ni] = resident_ctas<256, 64, __half, 2>();
+// CTAs of the compressed decode kernel of these widths that fit on one SM at
+// once (same for fp16 and bf16 queries, which share the register and smem
+// footprint); computed once per combination.
+int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32_t sb) {
+  static int cache[2][2][9][9][2] = {};
+  const int di = D == 256, ni = N == 64, si = sb == 2;
+  if (kb < 0 || kb > 8 || vb < 0 || vb > 8) return 1;
+  int& c = cache[di][ni][kb][vb][si];
+  if (!c) {
+    if (kb == 4 && vb == 2 && sb == 4) {
+      if (D == 128 && N == 128) c = resident_dense<128, 128, __half, 4, 4, 2, 4>();
+      else if (D == 128) c = resident_dense<128, 64, __half, 4, 4, 2, 4>();
+      else if (N == 128) c = resident_dense<256, 128, __half, 2, 4, 2, 4>();
+      else c = resident_dense<256, 64, __half, 2, 4, 2, 4>();
+    } else if (kb == 4 && vb == 2) {
+      c = resident_widths<4, 2, 2>(D, N);
+    } else if (kb == vb) {
+      switch (kb) {
+        case 2: c = resident_widths<2, 2, 2>(D, N); break;
+        case 3: c = resident_widths<3, 3, 2>(D, N); break;
+        case 4: c = resident_widths<4, 4, 2>(D, N); break;
+        case 5: c = resident_widths<5, 5, 2>(D, N); break;
+        case 6: c = resident_widths<6, 6, 2>(D, N); break;
+        case 8: c = resident_widths<8, 8, 2>(D, N); break;
+        default: c = 1; break;
+      }
+    } else {
+      c = 1;
+    }
   }
-  return cache[di][ni];
+  return c;
 }
 
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,

@@ -842,15 +842,41 @@ cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The decode kernels of one (K width, V width, scale bytes) combination;
-// each combination is compiled in its own translation unit.
+// CTAs of one decode kernel resident per SM (registers and shared memory).
+template <int D, int N, typename T, int W, int KB, int VB, int SB>
+int resident_dense() {
+  using S = DecShape<D, N, W, KB, VB, SB>;
+  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM) != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, S::SMEM) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+// Warps per CTA of the head_dim-128 decode of these widths: 4, or 2 where a
+// 4-warp CTA's page slots would take more than half an SM's shared memory
+// (8-bit codes at 128-token tiles: 137 KB, one CTA of 4 warps per SM; 2-warp
+// CTAs fit three to an SM).
+template <int D, int N, int KB, int VB, int SB>
+constexpr int width_warps() {
+  return DecShape<D, N, 4, KB, VB, SB>::SMEM > 116 * 1024 ? 2 : 4;
+}
+
+// The decode kernels of one (K width, V width, scale bytes) combination and
+// their residency (which sizes the persistent grid: the page parts of wider
+// codes take more shared memory); each combination is compiled in its own
+// translation unit.
 template <int KB, int VB, int SB>
 cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int ctas, cudaStream_t st);
+template <int KB, int VB, int SB>
+int resident_widths(int D, int N);
 
 #define KVARN_DECLARE_WIDTHS(KB, VB, SB)                                                             \
   template <>                                                                                       \
   cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas, \
-                                           cudaStream_t st);
+                                           cudaStream_t st);                                        \
+  template <>                                                                                       \
+  int resident_widths<KB, VB, SB>(int D, int N);
 KVARN_DECLARE_WIDTHS(4, 2, 2)
 KVARN_DECLARE_WIDTHS(2, 2, 2)
 KVARN_DECLARE_WIDTHS(3, 3, 2)
@@ -864,13 +890,20 @@ KVARN_DECLARE_WIDTHS(8, 8, 2)
   template <>                                                                                           \
   cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas,         \
                                            cudaStream_t st) {                                           \
+    constexpr int W1 = width_warps<128, 128, KB, VB, SB>(), W2 = width_warps<128, 64, KB, VB, SB>();    \
     if (D == 128 && N == 128)                                                                           \
-      return bf16 ? run_dense<128, 128, __nv_bfloat16, 4, KB, VB, SB>(A, ctas, st)                 \
-                  : run_dense<128, 128, __half, 4, KB, VB, SB>(A, ctas, st);                        \
+      return bf16 ? run_dense<128, 128, __nv_bfloat16, W1, KB, VB, SB>(A, ctas, st)                \
+                  : run_dense<128, 128, __half, W1, KB, VB, SB>(A, ctas, st);                       \
     if (D == 128 && N == 64)                                                                            \
-      return bf16 ? run_dense<128, 64, __nv_bfloat16, 4, KB, VB, SB>(A, ctas, st)                  \
-                  : run_dense<128, 64, __half, 4, KB, VB, SB>(A, ctas, st);                         \
+      return bf16 ? run_dense<128, 64, __nv_bfloat16, W2, KB, VB, SB>(A, ctas, st)                 \
+                  : run_dense<128, 64, __half, W2, KB, VB, SB>(A, ctas, st);                        \
     return cudaErrorInvalidValue;                                                                       \
+  }                                                                                                     \
+  template <>                                                                                           \
+  int resident_widths<KB, VB, SB>(int D, int N) {                                                       \
+    if (D == 128 && N == 128) return resident_dense<128, 128, __half, width_warps<128, 128, KB, VB, SB>(), KB, VB, SB>(); \
+    if (D == 128 && N == 64) return resident_dense<128, 64, __half, width_warps<128, 64, KB, VB, SB>(), KB, VB, SB>();   \
+    return 1;                                                                                           \
   }
 
 }  // namespace kvarn

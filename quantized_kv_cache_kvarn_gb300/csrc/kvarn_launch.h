@@ -132,11 +132,11 @@ struct DensePlan {
 // units_per_seq: KV heads x row groups; max_tiles: compressed tiles a unit
 // can hold; raw_max: raw tokens a row can see.
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
-                            int32_t raw_max);
+                            int32_t raw_max, int32_t kb = 4, int32_t vb = 2, int32_t sb = 4);
 // Partials of `rows` output rows, then one int32 tile-partial count per row.
 int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& plan);
 int dense_decode_warps(int32_t D);
-int dense_decode_ctas_per_sm(int32_t D, int32_t N);
+int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb = 4, int32_t vb = 2, int32_t sb = 4);
 int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
                               const SplitPlan& plan);
 
