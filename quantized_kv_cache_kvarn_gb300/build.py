@@ -32,9 +32,8 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-# The aarch64 ptxas of CUDA 13.0.88 crashes (SIGSEGV) on the MLA decode kernel
-# at -O2 and above; the x86 one does not. Both hosts use the same level.
-PER_FILE = {"kvarn_mla.cu": ["-Xptxas", "-O1"]}
+# Per-file extra flags (none at present).
+PER_FILE: dict = {}
 
 
 def _compile(src: str, obj: str, verbose: bool) -> str:
