@@ -204,7 +204,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   // tokens j%8 and j%8 + 8 of RPT/2 pages, so that the two tokens sharing a
   // packed byte of the dense page are in one thread. Latent tiles: row
   // i*32 + j of this CTA's rows.
-  float x[S::RPT][16];
+  // channel pairs (2e, 2e + 1) of the thread's 16 channels, so that the
+  // arithmetic below runs as packed fp32 pair instructions
+  float2 xp[S::RPT][8];
   auto local_row = [&](int i) -> int {
     const int j = warp * S::RPW + rsub;
     if constexpr (KIND == 0)
@@ -217,8 +219,11 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   for (int i = 0; i < S::RPT; ++i) {
     const int r = crank * S::ROWS + local_row(i);
     const T* p = (last_row != nullptr && r == N - 1) ? last_row + seg * 16 : src + static_cast<int64_t>(r) * D + seg * 16;
-    load8<T>(p, x[i]);
-    load8<T>(p + 8, x[i] + 8);
+    float v[16];
+    load8<T>(p, v);
+    load8<T>(p + 8, v + 8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xp[i][e] = make_float2(v[2 * e], v[2 * e + 1]);
   }
 
   // ---- page addresses of this CTA's rows (read by the stores at the end)
@@ -239,30 +244,39 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
+    for (int e = 0; e < 8; ++e) {  // stage 1: within a pair
+      const float a = xp[i][e].x, c = xp[i][e].y;
+      xp[i][e] = make_float2(a + c, a - c);
+    }
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
+    for (int h = 1; h < 8; h <<= 1)  // stages 2, 4, 8: between pairs
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
         if (!(e & h)) {
-          float a = x[i][e], c = x[i][e + h];
-          x[i][e] = a + c;
-          x[i][e + h] = a - c;
+          const float2 a = xp[i][e], c = xp[i][e + h];
+          xp[i][e] = f2add(a, c);
+          xp[i][e + h] = f2fma(c, f2(-1.f), a);
         }
   }
 #pragma unroll
   for (int d = 1; d < S::TPR; d <<= 1) {
     // lower lane: x + partner; upper lane: partner - x  (one FFMA either way)
-    const float sgn = (lane & d) ? -1.f : 1.f;
+    const float2 sgn = f2((lane & d) ? -1.f : 1.f);
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] = fmaf(sgn, x[i][e], __shfl_xor_sync(0xffffffffu, x[i][e], d));
+      for (int e = 0; e < 8; ++e) {
+        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, xp[i][e].x, d),
+                                     __shfl_xor_sync(0xffffffffu, xp[i][e].y, d));
+        xp[i][e] = f2fma(sgn, xp[i][e], o);
+      }
   }
   {
-    const float rsd = 1.f / sqrtf(static_cast<float>(D));
+    const float2 rsd = f2(1.f / sqrtf(static_cast<float>(D)));
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] *= rsd;
+      for (int e = 0; e < 8; ++e) xp[i][e] = f2mul(xp[i][e], rsd);
   }
 
   // ---- variance normalisation, T iterations of (column pass, row pass)
@@ -278,18 +292,19 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     // over the tile in one reduction
     float2 mo[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float t = 0.f;
+    for (int e = 0; e < 8; ++e) {
+      float2 t = xp[0][e];
 #pragma unroll
-      for (int i = 0; i < S::RPT; ++i) t += x[i][e];
-      const float m = t * (1.f / S::RPT);
-      float v = 0.f;
+      for (int i = 1; i < S::RPT; ++i) t = f2add(t, xp[i][e]);
+      const float2 m = f2mul(t, f2(1.f / S::RPT)), nm = f2mul(m, f2(-1.f));
+      float2 v = f2(0.f);
 #pragma unroll
       for (int i = 0; i < S::RPT; ++i) {
-        const float dv = x[i][e] - m;
-        v = fmaf(dv, dv, v);
+        const float2 dv = f2add(xp[i][e], nm);
+        v = f2fma(dv, dv, v);
       }
-      mo[e] = make_float2(m, v);
+      mo[2 * e] = make_float2(m.x, v.x);
+      mo[2 * e + 1] = make_float2(m.y, v.y);
     }
     const float2 cm = column_moments<D, N, CS>(mo, red, colpart + (it & 1) * 2 * D);
     if (tid < D) {
@@ -298,27 +313,38 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       colbuf[tid] = 1.f / sig;
     }
     __syncthreads();
-    float inv[16];
-    read_segment<D>(inv, colbuf, seg);
+    float2 inv[8];
+    {
+      const float4* src = reinterpret_cast<const float4*>(colbuf + seg * 16);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 f = src[e];
+        inv[2 * e] = make_float2(f.x, f.y);
+        inv[2 * e + 1] = make_float2(f.z, f.w);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] *= inv[e];
+      for (int e = 0; e < 8; ++e) xp[i][e] = f2mul(xp[i][e], inv[e]);
     // row pass: a row lives in TPR consecutive lanes; mean and M2 of the
     // lane's 16 channels, merged over the row's lanes
 #pragma unroll
     for (int i = 0; i < S::RPT; ++i) {
-      float t = 0.f;
+      float2 ts[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) t += x[i][e];
-      const float m0 = t * (1.f / 16.f);
-      float v = 0.f;
+      for (int e = 0; e < 8; ++e) ts[e] = xp[i][e];
+      const float2 tt = tree_reduce(ts, [](float2 u, float2 w) { return f2add(u, w); });
+      const float m0 = (tt.x + tt.y) * (1.f / 16.f);
+      const float2 nm = f2(-m0);
+      float2 vs[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float dv = x[i][e] - m0;
-        v = fmaf(dv, dv, v);
+      for (int e = 0; e < 8; ++e) {
+        const float2 dv = f2add(xp[i][e], nm);
+        vs[e] = f2mul(dv, dv);
       }
-      float2 r = make_float2(m0, v);
+      const float2 vt = tree_reduce(vs, [](float2 u, float2 w) { return f2add(u, w); });
+      float2 r = make_float2(m0, vt.x + vt.y);
       float n = 16.f;
 #pragma unroll
       for (int o = 1; o < S::TPR; o <<= 1) {
@@ -327,9 +353,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       }
       const float sig = safe_sigma(r.y * invD, r.x);
       rscale[i] *= sig;
-      const float ri = 1.f / sig;
+      const float2 ri = f2(1.f / sig);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] *= ri;
+      for (int e = 0; e < 8; ++e) xp[i][e] = f2mul(xp[i][e], ri);
     }
     // colbuf is rewritten next only after the next column reduction's barrier
   }
@@ -339,11 +365,11 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
   uint32_t Pc[S::RPT][4];
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
-    float lo = x[i][0], hi = x[i][0];
+    float lo = fminf(xp[i][0].x, xp[i][0].y), hi = fmaxf(xp[i][0].x, xp[i][0].y);
 #pragma unroll
-    for (int e = 1; e < 16; ++e) {
-      lo = fminf(lo, x[i][e]);
-      hi = fmaxf(hi, x[i][e]);
+    for (int e = 1; e < 8; ++e) {
+      lo = fminf(lo, fminf(xp[i][e].x, xp[i][e].y));
+      hi = fmaxf(hi, fmaxf(xp[i][e].x, xp[i][e].y));
     }
 #pragma unroll
     for (int o = 1; o < S::TPR; o <<= 1) {
@@ -352,16 +378,19 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     }
     const float delta = (hi - lo) / static_cast<float>(QMAX);
     const float rinv = delta > 0.f ? 1.f / delta : 0.f;
+    const float2 nlo = f2(-lo), rv = f2(rinv);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint32_t word = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 2; ++e) {
         // x - lo lies in [0, hi - lo], so the rounded quotient lies in
         // [0, QMAX]; the unsigned conversion saturates and min() only
         // guards non-finite input
-        const uint32_t q = min(__float2uint_rn((x[i][4 * k + e] - lo) * rinv), static_cast<uint32_t>(QMAX));
-        word |= q << (8 * e);
+        const float2 z = f2mul(f2add(xp[i][2 * k + e], nlo), rv);
+        const uint32_t q0 = min(__float2uint_rn(z.x), static_cast<uint32_t>(QMAX));
+        const uint32_t q1 = min(__float2uint_rn(z.y), static_cast<uint32_t>(QMAX));
+        word |= (q0 << (16 * e)) | (q1 << (16 * e + 8));
       }
       Pc[i][k] = word;
     }
@@ -531,7 +560,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 // encodes K, the rest V, so that the K half of a large grid runs before the
 // V half and an SM mostly runs one of the two code paths.
 template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
-__global__ void __launch_bounds__(2 * D) encode_dense_kernel(EncodeArgs A) {
+__global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) encode_dense_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
   const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);
@@ -564,7 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
 // encoded straight into its pages (the tail then holds nothing). The tail
 // rows read here were written by earlier launches.
 template <int D, int N, typename T>
-__global__ void __launch_bounds__(2 * D) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
+__global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
                                                               int32_t max_seq_len, T* tail_k, T* tail_v) {
   extern __shared__ __align__(16) unsigned char smem[];
   const bool is_v = blockIdx.z == 1;
