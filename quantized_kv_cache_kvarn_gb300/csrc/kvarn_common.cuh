@@ -39,6 +39,15 @@ struct DensePage {
   __host__ __device__ constexpr int bytes() const { return k_part() + v_part(); }
 };
 
+// Dense decode shapes whose page parts are staged by TMA gathers of four
+// pages (a 2-D tensor map over the cache with 8-byte elements and one row per
+// (page, KV head): both parts at most 256 elements wide, whole groups of four
+// pages per tile, one warp per tile).
+__host__ __device__ constexpr bool dense_gather(int D, int N, int KB, int VB, int SB) {
+  return D == 128 && DensePage(D, N, KB, VB, SB).k_part() <= 2048 && DensePage(D, N, KB, VB, SB).v_part() <= 2048 &&
+         (N / kPageTokens) % 4 == 0;
+}
+
 // Code planes of a b-bit code (low plane first): 2: [2], 3: [2, 1], 4: [4],
 // 5: [4, 1], 6: [4, 2], 8: [4, 4]; the code is plane0 + 2^w0 plane1.
 __host__ __device__ constexpr int plane_w0(int b) { return b == 2 || b == 3 ? 2 : 4; }
@@ -132,6 +141,17 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 
 // Waits until every cp.async this thread issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// TMA gather of four rows (x .. x + box - 1 of rows y0..y3) of a 2-D tensor
+// map into shared memory, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_addr(bar))
+      : "memory");
+}
 
 // The waiting thread may be suspended (it issues nothing) until the phase
 // completes or about 20 us pass.

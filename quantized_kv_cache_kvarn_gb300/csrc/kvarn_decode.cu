@@ -1,6 +1,8 @@
 // KVarN decode attention: split planning and launch (kernels in
 // kvarn_decode_kernel.cuh; the k4v2 preset with fp32 scales is instantiated
 // here, every other code width in its own kvarn_decode_w*.cu).
+#include <cudaTypedefs.h>
+
 #include "kvarn_decode_kernel.cuh"
 
 namespace kvarn {
@@ -112,9 +114,50 @@ int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
   return static_cast<int64_t>(num_seqs) * num_q_heads * plan.slots * kPStride(D) * 4;
 }
 
+// cuTensorMapEncodeTiled of the driver, found once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The cache as rows of 8-byte elements, one row per (page, KV head); the box
+// is one row high and `box_bytes` wide (a page's K or V part).
+static cudaError_t cache_tensor_map(CUtensorMap* map, const void* cache, int64_t rows, int page_bytes,
+                                    int box_bytes) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(page_bytes / 8), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(page_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / 8), 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(cache), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   DecArgs A{};
+  {
+    const int kb = p.k_bits ? p.k_bits : 4, vb = p.v_bits ? p.v_bits : 2, sb = p.scale_bytes ? p.scale_bytes : 4;
+    if (dense_gather(p.D, p.N, kb, vb, sb)) {
+      const DensePage pg(p.D, p.N, kb, vb, sb);
+      const int64_t rows = static_cast<int64_t>(p.num_pages) * p.num_kv_heads;
+      cudaError_t e = cache_tensor_map(&A.tmk, p.cache, rows, pg.bytes(), pg.k_part());
+      if (e == cudaSuccess) e = cache_tensor_map(&A.tmv, p.cache, rows, pg.bytes(), pg.v_part());
+      if (e != cudaSuccess) return e;
+    }
+  }
   A.q = p.q;
   A.kappa = p.sm_scale * kLog2e;
   A.cache = p.cache;

@@ -36,6 +36,7 @@
 // Hadamard transform of the rotated part, plus the tail part.
 #pragma once
 
+#include <cuda.h>
 #include <math.h>
 
 #include <algorithm>
@@ -93,9 +94,16 @@ struct DecShape {
   static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
+  static constexpr bool GATHER = HV == 1 && dense_gather(D, N, KB, VB, SB);
+  static_assert(!GATHER || ((4 * KP) % 128 == 0 && (4 * VP) % 128 == 0 && KSLOT % 128 == 0 && WARP_SMEM % 128 == 0),
+                "gather destinations stay 128-byte aligned");
 };
 
 struct DecArgs {
+  // 2-D tensor maps over the cache (one row per (page, KV head), 8-byte
+  // elements) with boxes of a page's K part and of its V part: the TMA
+  // gathers of the shapes dense_gather() selects (unused otherwise)
+  CUtensorMap tmk, tmv;
   const void* q;  // [B][Q][Hq][D]
   float kappa;    // sm_scale * log2(e)
   const uint8_t* cache;
@@ -443,25 +451,41 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   // a tile serialised on the SM's copy unit cost a sixth of the tile loop);
   // each thread then arrives on the slot's barrier once its copies land.
   // Page p's physical id sits in lane p (page ids are read by lanes < PPT).
-  auto issue_part = [&](int phys, unsigned char* slot, int part_off, int part_bytes, uint64_t* bar) {
-    __syncwarp();  // every lane's reads of the slot precede the copies
-    const int tid = half * 32 + lane;
+  auto issue_part = [&](int phys, unsigned char* slot, int part_off, int part_bytes, uint64_t* bar, const CUtensorMap* tm) {
+    if constexpr (S::GATHER) {
+      // one TMA gather per four pages, from lane 0 (rows phys * Hkv + kvh)
+      fence_proxy_async_smem();  // the warp's reads of the slot precede the async writes
+      int row[S::PPT];
 #pragma unroll
-    for (int p = 0; p < S::PPT; ++p) {
-      const unsigned char* src = page_at(__shfl_sync(0xffffffffu, phys, p)) + part_off;
-      unsigned char* dst = slot + p * part_bytes;
+      for (int p = 0; p < S::PPT; ++p) row[p] = __shfl_sync(0xffffffffu, phys, p) * A.Hkv + kvh;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, S::PPT * part_bytes);
 #pragma unroll
-      for (int c = tid; c < part_bytes / 16; c += 32 * HV) cp_async16(dst + 16 * c, src + 16 * c);
+        for (int q4 = 0; q4 < S::PPT / 4; ++q4)
+          tma_gather4(slot + 4 * q4 * part_bytes, tm, part_off / 8, row[4 * q4], row[4 * q4 + 1], row[4 * q4 + 2],
+                      row[4 * q4 + 3], bar);
+      }
+    } else {
+      __syncwarp();  // every lane's reads of the slot precede the copies
+      const int tid = half * 32 + lane;
+#pragma unroll
+      for (int p = 0; p < S::PPT; ++p) {
+        const unsigned char* src = page_at(__shfl_sync(0xffffffffu, phys, p)) + part_off;
+        unsigned char* dst = slot + p * part_bytes;
+#pragma unroll
+        for (int c = tid; c < part_bytes / 16; c += 32 * HV) cp_async16(dst + 16 * c, src + 16 * c);
+      }
+      cp_async_arrive(bar);
     }
-    cp_async_arrive(bar);
   };
   auto issue_k = [&](int phys) {
     ph += 1u << 16;
-    issue_part(phys, kslot, 0, S::KP, barK);
+    issue_part(phys, kslot, 0, S::KP, barK, &A.tmk);
   };
   auto issue_v = [&](int phys) {
     ph += 1u << 24;
-    issue_part(phys, vslot, S::KP, S::VP, barV);
+    issue_part(phys, vslot, S::KP, S::VP, barV, &A.tmv);
   };
 
   if (n_my > 0) {
@@ -758,7 +782,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 }
 
 template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
-__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(DecArgs A) {
+__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(const __grid_constant__ DecArgs A) {
   using S = DecShape<D, N, W, KB, VB, SB>;
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
@@ -766,8 +790,9 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
   {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
     if (warp % S::HV == 0 && lane == 0) {
-      mbar_init(bars + 2 * (warp / S::HV), 32 * S::HV);  // one arrival per copying thread
-      mbar_init(bars + 2 * (warp / S::HV) + 1, 32 * S::HV);
+      // one arrival per copying thread (cp.async), or lane 0's (TMA gathers)
+      mbar_init(bars + 2 * (warp / S::HV), S::GATHER ? 1 : 32 * S::HV);
+      mbar_init(bars + 2 * (warp / S::HV) + 1, S::GATHER ? 1 : 32 * S::HV);
     }
     fence_mbar_init();
   }
