@@ -40,12 +40,23 @@ struct DensePage {
 };
 
 // Dense decode shapes whose page parts are staged by TMA gathers of four
-// pages (a 2-D tensor map over the cache with 8-byte elements and one row per
-// (page, KV head): both parts at most 256 elements wide, whole groups of four
-// pages per tile, one warp per tile).
+// pages: a 2-D tensor map over the cache with 8-byte elements and one row per
+// (page, KV head), boxes one row high and at most 256 elements (2048 bytes)
+// wide. A part wider than that is gathered as two boxes split where its
+// codes' first half ends (gather_split), so that four pages' first boxes lie
+// together and then their second boxes.
+__host__ __device__ constexpr int gather_split(int part, int codes_bytes) {
+  return part <= 2048 ? part : codes_bytes / 2;
+}
+__host__ __device__ constexpr bool gather_part_ok(int part, int codes_bytes) {
+  return gather_split(part, codes_bytes) <= 2048 && part - gather_split(part, codes_bytes) <= 2048 &&
+         gather_split(part, codes_bytes) % 16 == 0 && (4 * part) % 128 == 0 &&
+         (4 * gather_split(part, codes_bytes)) % 128 == 0;
+}
 __host__ __device__ constexpr bool dense_gather(int D, int N, int KB, int VB, int SB) {
-  return D == 128 && DensePage(D, N, KB, VB, SB).k_part() <= 2048 && DensePage(D, N, KB, VB, SB).v_part() <= 2048 &&
-         (N / kPageTokens) % 4 == 0;
+  return (D == 128 || D == 256) && (N / kPageTokens) % 4 == 0 &&
+         gather_part_ok(DensePage(D, N, KB, VB, SB).k_part(), 2 * D * KB) &&
+         gather_part_ok(DensePage(D, N, KB, VB, SB).v_part(), 2 * D * VB);
 }
 
 // Code planes of a b-bit code (low plane first): 2: [2], 3: [2, 1], 4: [4],

@@ -130,7 +130,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The cache as rows of 8-byte elements, one row per (page, KV head); the box
-// is one row high and `box_bytes` wide (a page's K or V part).
+// is one row high and `box_bytes` wide (a page's K or V part, or one of its
+// two pieces).
 static cudaError_t cache_tensor_map(CUtensorMap* map, const void* cache, int64_t rows, int page_bytes,
                                     int box_bytes) {
   auto enc = tensor_map_encoder();
@@ -153,8 +154,15 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
     if (dense_gather(p.D, p.N, kb, vb, sb)) {
       const DensePage pg(p.D, p.N, kb, vb, sb);
       const int64_t rows = static_cast<int64_t>(p.num_pages) * p.num_kv_heads;
-      cudaError_t e = cache_tensor_map(&A.tmk, p.cache, rows, pg.bytes(), pg.k_part());
-      if (e == cudaSuccess) e = cache_tensor_map(&A.tmv, p.cache, rows, pg.bytes(), pg.v_part());
+      // a part wider than one box is gathered as two (split where its
+      // codes' first half ends); the second map is unused otherwise
+      const int ks = gather_split(pg.k_part(), 2 * p.D * kb), vs = gather_split(pg.v_part(), 2 * p.D * vb);
+      cudaError_t e = cache_tensor_map(&A.tmk, p.cache, rows, pg.bytes(), ks);
+      if (e == cudaSuccess) e = cache_tensor_map(&A.tmv, p.cache, rows, pg.bytes(), vs);
+      if (e == cudaSuccess && ks < pg.k_part())
+        e = cache_tensor_map(&A.tmk2, p.cache, rows, pg.bytes(), pg.k_part() - ks);
+      if (e == cudaSuccess && vs < pg.v_part())
+        e = cache_tensor_map(&A.tmv2, p.cache, rows, pg.bytes(), pg.v_part() - vs);
       if (e != cudaSuccess) return e;
     }
   }

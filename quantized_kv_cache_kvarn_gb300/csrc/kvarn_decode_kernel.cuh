@@ -94,16 +94,18 @@ struct DecShape {
   static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
-  static constexpr bool GATHER = HV == 1 && dense_gather(D, N, KB, VB, SB);
-  static_assert(!GATHER || ((4 * KP) % 128 == 0 && (4 * VP) % 128 == 0 && KSLOT % 128 == 0 && WARP_SMEM % 128 == 0),
-                "gather destinations stay 128-byte aligned");
+  static constexpr bool GATHER = dense_gather(D, N, KB, VB, SB);
+  // first-box widths of the K and V parts (the whole part unless split)
+  static constexpr int KS = GATHER ? gather_split(KP, 2 * D * KB) : KP;
+  static constexpr int VS = GATHER ? gather_split(VP, 2 * D * VB) : VP;
+  static_assert(!GATHER || (KSLOT % 128 == 0 && WARP_SMEM % 128 == 0), "gather destinations stay 128-byte aligned");
 };
 
 struct DecArgs {
   // 2-D tensor maps over the cache (one row per (page, KV head), 8-byte
   // elements) with boxes of a page's K part and of its V part: the TMA
   // gathers of the shapes dense_gather() selects (unused otherwise)
-  CUtensorMap tmk, tmv;
+  CUtensorMap tmk, tmk2, tmv, tmv2;  // second boxes of split parts
   const void* q;  // [B][Q][Hq][D]
   float kappa;    // sm_scale * log2(e)
   const uint8_t* cache;
@@ -451,20 +453,38 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   // a tile serialised on the SM's copy unit cost a sixth of the tile loop);
   // each thread then arrives on the slot's barrier once its copies land.
   // Page p's physical id sits in lane p (page ids are read by lanes < PPT).
-  auto issue_part = [&](int phys, unsigned char* slot, int part_off, int part_bytes, uint64_t* bar, const CUtensorMap* tm) {
+  // Byte `off` of page p's part (part size P, first box Sp) in its slot: per
+  // group of four pages, the four first boxes, then the four second boxes.
+  auto part_at = [](const unsigned char* slot, int p, int off, int P, int Sp) -> const unsigned char* {
     if constexpr (S::GATHER) {
-      // one TMA gather per four pages, from lane 0 (rows phys * Hkv + kvh)
+      const unsigned char* grp = slot + (p / 4) * 4 * P;
+      return off < Sp ? grp + (p % 4) * Sp + off : grp + 4 * Sp + (p % 4) * (P - Sp) + (off - Sp);
+    } else {
+      return slot + p * P + off;
+    }
+  };
+  auto kp = [&](int p, int off) { return part_at(kslot, p, off, S::KP, S::KS); };
+  auto vp = [&](int p, int off) { return part_at(vslot, p, off, S::VP, S::VS); };
+  auto issue_part = [&](int phys, unsigned char* slot, int part_off, int part_bytes, int box1, uint64_t* bar,
+                        const CUtensorMap* tm, const CUtensorMap* tm2) {
+    if constexpr (S::GATHER) {
+      // one TMA gather per four pages (two for a split part), from the
+      // unit's lane 0 (rows phys * Hkv + kvh)
       fence_proxy_async_smem();  // the warp's reads of the slot precede the async writes
       int row[S::PPT];
 #pragma unroll
       for (int p = 0; p < S::PPT; ++p) row[p] = __shfl_sync(0xffffffffu, phys, p) * A.Hkv + kvh;
       __syncwarp();
-      if (lane == 0) {
+      if (leader && lane == 0) {
         mbar_arrive_expect_tx(bar, S::PPT * part_bytes);
 #pragma unroll
-        for (int q4 = 0; q4 < S::PPT / 4; ++q4)
-          tma_gather4(slot + 4 * q4 * part_bytes, tm, part_off / 8, row[4 * q4], row[4 * q4 + 1], row[4 * q4 + 2],
-                      row[4 * q4 + 3], bar);
+        for (int q4 = 0; q4 < S::PPT / 4; ++q4) {
+          unsigned char* dst = slot + 4 * q4 * part_bytes;
+          tma_gather4(dst, tm, part_off / 8, row[4 * q4], row[4 * q4 + 1], row[4 * q4 + 2], row[4 * q4 + 3], bar);
+          if (box1 < part_bytes)
+            tma_gather4(dst + 4 * box1, tm2, (part_off + box1) / 8, row[4 * q4], row[4 * q4 + 1], row[4 * q4 + 2],
+                        row[4 * q4 + 3], bar);
+        }
       }
     } else {
       __syncwarp();  // every lane's reads of the slot precede the copies
@@ -481,11 +501,11 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   };
   auto issue_k = [&](int phys) {
     ph += 1u << 16;
-    issue_part(phys, kslot, 0, S::KP, barK, &A.tmk);
+    issue_part(phys, kslot, 0, S::KP, S::KS, barK, &A.tmk, &A.tmk2);
   };
   auto issue_v = [&](int phys) {
     ph += 1u << 24;
-    issue_part(phys, vslot, S::KP, S::VP, barV, &A.tmv);
+    issue_part(phys, vslot, S::KP, S::VP, S::VS, barV, &A.tmv, &A.tmv2);
   };
 
   if (n_my > 0) {
@@ -547,7 +567,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const int kc = half * KCW + kcl;
       const int ch0 = 16 * kc + 2 * t;
       const float4 qv = *reinterpret_cast<const float4*>(qrot + q_frag(kc, g, t));
-      const unsigned char* cp = kslot + (ch0 / S::CPP) * S::KP + PG.k_col() + (ch0 % S::CPP) * SB;
+      const unsigned char* cp = kp(ch0 / S::CPP, PG.k_col() + (ch0 % S::CPP) * SB);
       const float2 x01 = f2mul(make_float2(qv.x, qv.y), load_scale2<SB>(cp));
       const float2 x89 = f2mul(make_float2(qv.z, qv.w), load_scale2<SB>(cp + 8 * SB));
       qs2[kcl] = f2add(x01, x89);
@@ -575,12 +595,11 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         uint32_t x0[2][S::KW0], x1[2][S::KW1 ? S::KW1 : 1];
 #pragma unroll
         for (int pi = 0; pi < 2; ++pi) {
-          const unsigned char* pg = kslot + (p0 + pi) * S::KP;
-          load_words<S::KW0>(pg + 4 * S::KU0 * (32 * ((ch * S::KW0) / S::KU0) + lane) + 4 * ((ch * S::KW0) % S::KU0),
+          load_words<S::KW0>(kp(p0 + pi, 4 * S::KU0 * (32 * ((ch * S::KW0) / S::KU0) + lane) + 4 * ((ch * S::KW0) % S::KU0)),
                              x0[pi]);
           if constexpr (S::KW1 != 0)
-            load_words<S::KW1>(pg + S::KR1 + 4 * S::KU1 * (32 * ((ch * S::KW1) / S::KU1) + lane) +
-                                   4 * ((ch * S::KW1) % S::KU1),
+            load_words<S::KW1>(kp(p0 + pi, S::KR1 + 4 * S::KU1 * (32 * ((ch * S::KW1) / S::KU1) + lane) +
+                                               4 * ((ch * S::KW1) % S::KU1)),
                                x1[pi]);
         }
         static_for<0, 8>([&](auto fgc) {
@@ -608,10 +627,9 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     //    in base 2. The K slot is read for the last time here.
 #pragma unroll
     for (int nb = 0; nb < S::NB; ++nb) {
-      const unsigned char* pg = kslot + (nb >> 1) * S::KP;
       const int idx = (nb & 1) * 8 + 2 * t;
-      const float2 ka = load_scale2<SB>(pg + PG.k_a() + idx * SB);
-      const float2 kb = load_scale2<SB>(pg + PG.k_b() + idx * SB);
+      const float2 ka = load_scale2<SB>(kp(nb >> 1, PG.k_a() + idx * SB));
+      const float2 kb = load_scale2<SB>(kp(nb >> 1, PG.k_b() + idx * SB));
       const float2 kb_c = S::KCENTER != 0.f ? f2fma(f2(S::KCENTER), ka, kb) : kb;
       s[nb] = f2fma(f2mul(ka, f2(S::KINV)), s[nb], f2mul(kb_c, qsum));
     }
@@ -673,11 +691,10 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     float2 be2[S::PPT];
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
-      const unsigned char* pg = vslot + pp * S::VP;
-      const float2 va0 = load_scale2<SB>(pg + PG.v_a() - S::KP + (2 * t) * SB);
-      const float2 va1 = load_scale2<SB>(pg + PG.v_a() - S::KP + (8 + 2 * t) * SB);
-      const float2 vb0 = load_scale2<SB>(pg + PG.v_b() - S::KP + (2 * t) * SB);
-      const float2 vb1 = load_scale2<SB>(pg + PG.v_b() - S::KP + (8 + 2 * t) * SB);
+      const float2 va0 = load_scale2<SB>(vp(pp, PG.v_a() - S::KP + (2 * t) * SB));
+      const float2 va1 = load_scale2<SB>(vp(pp, PG.v_a() - S::KP + (8 + 2 * t) * SB));
+      const float2 vb0 = load_scale2<SB>(vp(pp, PG.v_b() - S::KP + (2 * t) * SB));
+      const float2 vb1 = load_scale2<SB>(vp(pp, PG.v_b() - S::KP + (8 + 2 * t) * SB));
       be2[pp] = f2fma(s[2 * pp], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va0, vb0) : vb0,
                       f2mul(s[2 * pp + 1], S::VCENTER != 0.f ? f2fma(f2(S::VCENTER), va1, vb1) : vb1));
       split_hi_lo2(f2mul(s[2 * pp], va0), Ap[pp][0], Ap[pp][1]);
@@ -699,8 +716,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 #pragma unroll
       for (int pp = 0; pp < S::PPT; ++pp) {
         uint32_t x0[S::VW0], x1[S::VW1 ? S::VW1 : 1];
-        load_words<S::VW0>(vslot + pp * S::VP + 4 * S::VW0 * (32 * hq + lane), x0);
-        if constexpr (S::VW1 != 0) load_words<S::VW1>(vslot + pp * S::VP + S::VR1 + 4 * S::VW1 * (32 * hq + lane), x1);
+        load_words<S::VW0>(vp(pp, 4 * S::VW0 * (32 * hq + lane)), x0);
+        if constexpr (S::VW1 != 0) load_words<S::VW1>(vp(pp, S::VR1 + 4 * S::VW1 * (32 * hq + lane)), x1);
         static_for<0, 8>([&](auto kc_) {
           constexpr int k = decltype(kc_)::value;
           uint32_t b0, b1;
@@ -712,7 +729,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       for (int k = 0; k < 8; ++k) {
         const int nc = 8 * hq + k, ncl = 8 * hql + k;
         const int ch = 8 * nc + 2 * t;
-        const float2 cv = load_scale2<SB>(vslot + (ch / S::CPP) * S::VP + PG.v_col() - S::KP + (ch % S::CPP) * SB);
+        const float2 cv = load_scale2<SB>(vp(ch / S::CPP, PG.v_col() - S::KP + (ch % S::CPP) * SB));
         const float2 uk = f2add(make_float2(u[k][0], u[k][1]), make_float2(u[k][2], u[k][3]));
         acc[ncl] = f2fma(cv, f2fma(uk, f2(S::VINV), beta), acc[ncl]);
       }
