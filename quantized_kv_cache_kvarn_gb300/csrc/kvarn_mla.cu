@@ -569,6 +569,17 @@ __device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -658,6 +669,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
   // Bounded wait, uniform over the warp; gives up (and tells every role to)
   // after about a second or once another warp has given up.
   auto wait = [&](int bar, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test(bars + bar, parity))) return true;
     bool ok = true;
     const long long start = clock64();
     while (!mbar_probe(bars + bar, parity)) {
@@ -717,9 +729,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
     load_q(1, qb);
     for (int i = 0; i < n; ++i) {
       const int par = i & 1;
-      // the previous tile's P V is done (P, which aliases the ring, and
-      // this half's code blocks are free) and this tile's pages have landed
-      if (i > 0 && !wait(BAR_OFULL, (i - 1) & 1)) break;
+      // this tile's pages have landed (its scales go to the meta buffer of
+      // tile i - 2, long free)
       if (!wait(BAR_RAW, i & 1)) break;
       float* meta = reinterpret_cast<float*>(sm + kOffMeta + par * kMeta);
       {  // column scales (page q of the tile holds channels [64 q, +64)), row scales
@@ -735,6 +746,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
       }
       mbar_arrive_plain(bars + BAR_PSYNC);
       if (!wait(BAR_PSYNC, 0)) break;  // phase 2i
+      // the previous tile's P V is done: P, which aliases the ring, and this
+      // half's code blocks are free
+      if (i > 0 && !wait(BAR_OFULL, (i - 1) & 1)) break;
       float wk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       // chunk c: wait for its ring stage, build A (and B) into it, publish it
       auto chunk = [&](int c, const float4 (&q)[8]) -> bool {
@@ -761,11 +775,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int r = 16 * pw + 2 * k + (pl >> 4);
-            const float x0 = q[k].x * cv.x, x1 = q[k].y * cv.y, x2 = q[k].z * cv.z, x3 = q[k].w * cv.w;
-            wk[k] += (x0 + x1) + (x2 + x3);
+            const float2 x01 = f2mul(make_float2(q[k].x, q[k].y), make_float2(cv.x, cv.y));
+            const float2 x23 = f2mul(make_float2(q[k].z, q[k].w), make_float2(cv.z, cv.w));
+            const float2 xs = f2add(x01, x23);
+            wk[k] += xs.x + xs.y;
             uint32_t h0, l0, h1, l1;
-            split_hi_lo(x0, x1, h0, l0);
-            split_hi_lo(x2, x3, h1, l1);
+            split_hi_lo2(x01, h0, l0);
+            split_hi_lo2(x23, h1, l1);
             const uint32_t off = sw128_unit(r, piece >> 1) + 8 * (piece & 1);
             *reinterpret_cast<uint2*>(st + off) = make_uint2(h0, h1);
             *reinterpret_cast<uint2*>(st + kBlk + off) = make_uint2(l0, l1);
