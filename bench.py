@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attn packed-KV GB/s (% of HBM peak), tokens/s; encode tokens/s"
 WORKLOAD = "dense32b"
 DECODE_SOURCES = {"dense": ["kvarn_decode.cu", "kvarn_decode_kernel.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"],
-                  "mla": ["kvarn_mla.cu", "kvarn_common.cuh", "kvarn_merge.cuh"]}
+                  "mla": ["kvarn_mla.cu", "kvarn_tcgen05.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"]}
 
 
 def _peaks():
