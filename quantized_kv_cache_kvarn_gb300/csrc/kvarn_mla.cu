@@ -541,9 +541,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
       tc_fence_before();
       mbar_arrive_plain(bars + BAR_TFREE);
     }
-    if (ok && m < A.H) {
-      float* part = A.ws + (static_cast<int64_t>(b * A.H + m) * A.slots + split) * kMlaPStride;
-      if (half == 0) {
+    if (ok) {  // warp-uniform: every lane takes part in the tensor-memory loads
+      const bool row = m < A.H;
+      float* part = A.ws + (static_cast<int64_t>(b * A.H + (row ? m : 0)) * A.slots + split) * kMlaPStride;
+      if (row && half == 0) {
         part[0] = m_run;
         part[1] = l_run;
       }
@@ -553,10 +554,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
         uint32_t oa[32];
         tc_ld32(tl + 256 + 32 * q, oa);
         tc_wait_ld();
+        if (row) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(pa + 32 * q + e) = make_float4(
-              __uint_as_float(oa[e]), __uint_as_float(oa[e + 1]), __uint_as_float(oa[e + 2]), __uint_as_float(oa[e + 3]));
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(pa + 32 * q + e) =
+                make_float4(__uint_as_float(oa[e]), __uint_as_float(oa[e + 1]), __uint_as_float(oa[e + 2]),
+                            __uint_as_float(oa[e + 3]));
+        }
       }
     }
   }

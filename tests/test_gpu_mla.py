@@ -105,3 +105,69 @@ def test_decode_mla_on_oracle_pages(lens):
           f"max |lse - oracle| = {np.abs(parity.f64(lse) - ref_lse).max():.3e}")
     assert diff <= parity.OUT_ATOL
     np.testing.assert_allclose(parity.f64(lse), ref_lse, atol=1e-4, rtol=0)
+
+
+def test_decode_mla_fp16_queries_many_splits():
+    """fp16 queries and tails, all 128 heads, one 4096 + 60-token sequence: the
+    split plan cuts the 32 tiles over several CTA pairs (a short last split),
+    whose partials the merge combines with the tail's."""
+    wl, case = _case(num_seqs=1, heads=128, context=4156)
+    olay = layout.LatentLayout(512, 64, 128)
+    lat, rope = parity.f64(case.latent), parity.f64(case.rope)
+    bt, sl = case.block_table.numpy(), case.seq_lens.numpy()
+    ocache = np.zeros((case.num_pages, olay.page_bytes), np.uint8)
+    mla.encode_into_cache(ocache, olay, lat[:, :4096], rope[:, :4096], bt, [0])
+    tl = np.zeros((1, 128, 512))
+    tr = np.zeros((1, 128, 64))
+    tl[0, :60], tr[0, :60] = lat[0, 4096:4156], rope[0, 4096:4156]
+    ql = case.q_latent.to(torch.float16)
+    qr = case.q_rope.to(torch.float16)
+    sm = W.default_sm_scale(wl)
+    ref, ref_lse = mla.decode(parity.f64(ql), parity.f64(qr), ocache, olay, bt, sl, sm, tl, tr)
+
+    dev = "cuda"
+    lay = kv.latent_layout(case.num_pages, kv.FP16)
+    out = torch.empty((1, 128, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(kv.decode_workspace_bytes(lay, 1, 128, 4156), dtype=torch.uint8, device=dev)
+    err = kv.new_error_word(dev)
+    kv.decode_mla(ql.to(dev), qr.to(dev), lay, torch.from_numpy(ocache).to(dev), case.block_table.to(dev),
+                  torch.from_numpy(sl).to(dev), 4156, out, ws, err, sm,
+                  torch.from_numpy(tl).half().to(dev), torch.from_numpy(tr).half().to(dev), lse=lse)
+    torch.cuda.synchronize()
+    assert kv.read_error_flags(err) == 0
+    diff = np.abs(parity.f64(out) - ref).max()
+    print(f"\nmla decode fp16, 32 tiles + 60: max |out - oracle| = {diff:.3e}")
+    assert diff <= parity.OUT_ATOL
+    np.testing.assert_allclose(parity.f64(lse), ref_lse, atol=1e-4, rtol=0)
+
+
+@pytest.mark.parametrize("heads", [16, 48])
+def test_decode_mla_head_counts_inside_a_warp(heads):
+    """Head counts whose last row falls inside a warp of the tensor-memory
+    lanes (16, 48): the padded rows take part in the tensor-memory loads and
+    write nothing."""
+    wl, case = _case(num_seqs=1, heads=heads, context=300)
+    olay = layout.LatentLayout(512, 64, 128)
+    lat, rope = parity.f64(case.latent), parity.f64(case.rope)
+    bt, sl = case.block_table.numpy(), case.seq_lens.numpy()
+    ocache = np.zeros((case.num_pages, olay.page_bytes), np.uint8)
+    mla.encode_into_cache(ocache, olay, lat[:, :256], rope[:, :256], bt, [0])
+    tl = np.zeros((1, 128, 512))
+    tr = np.zeros((1, 128, 64))
+    tl[0, :44], tr[0, :44] = lat[0, 256:300], rope[0, 256:300]
+    sm = W.default_sm_scale(wl)
+    ref, _ = mla.decode(parity.f64(case.q_latent), parity.f64(case.q_rope), ocache, olay, bt, sl, sm, tl, tr)
+    dev = "cuda"
+    lay = kv.latent_layout(case.num_pages, kv.BF16)
+    out = torch.empty((1, heads, 512), dtype=torch.float32, device=dev)
+    ws = torch.empty(kv.decode_workspace_bytes(lay, 1, heads, 300), dtype=torch.uint8, device=dev)
+    err = kv.new_error_word(dev)
+    kv.decode_mla(case.q_latent.to(dev), case.q_rope.to(dev), lay, torch.from_numpy(ocache).to(dev),
+                  case.block_table.to(dev), torch.from_numpy(sl).to(dev), 300, out, ws, err, sm,
+                  torch.from_numpy(tl).to(torch.bfloat16).to(dev), torch.from_numpy(tr).half().to(dev))
+    torch.cuda.synchronize()
+    assert kv.read_error_flags(err) == 0
+    diff = np.abs(parity.f64(out) - ref).max()
+    print(f"\nmla decode {heads} heads: max |out - oracle| = {diff:.3e}")
+    assert diff <= parity.OUT_ATOL
