@@ -90,16 +90,12 @@ int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32
       else if (D == 128) c = resident_dense<128, 64, __half, 4, 4, 2, 4>();
       else if (N == 128) c = resident_dense<256, 128, __half, 2, 4, 2, 4>();
       else c = resident_dense<256, 64, __half, 2, 4, 2, 4>();
-    } else if (kb == 4 && vb == 2) {
-      c = resident_widths<4, 2, 2>(D, N);
-    } else if (kb == vb) {
-      switch (kb) {
-        case 2: c = resident_widths<2, 2, 2>(D, N); break;
-        case 3: c = resident_widths<3, 3, 2>(D, N); break;
-        case 4: c = resident_widths<4, 4, 2>(D, N); break;
-        case 5: c = resident_widths<5, 5, 2>(D, N); break;
-        case 6: c = resident_widths<6, 6, 2>(D, N); break;
-        case 8: c = resident_widths<8, 8, 2>(D, N); break;
+    } else if (D == 128 && sb == 2) {
+      switch (16 * kb + vb) {
+#define KVARN_RES_CASE(K, V) \
+  case 16 * K + V: c = resident_widths<K, V, 2>(D, N); break;
+        KVARN_WIDTH_PAIRS(KVARN_RES_CASE)
+#undef KVARN_RES_CASE
         default: c = 1; break;
       }
     } else {
@@ -207,16 +203,12 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
     KV_DISPATCH(256, 128, 2)
     KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH
-  } else if (kb == 4 && vb == 2 && sb == 2) {
-    e = run_dense_widths<4, 2, 2>(A, p.D, p.N, p.bf16, plan.ctas, st);
-  } else if (kb == vb && sb == 2) {
-    switch (kb) {
-      case 2: e = run_dense_widths<2, 2, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
-      case 3: e = run_dense_widths<3, 3, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
-      case 4: e = run_dense_widths<4, 4, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
-      case 5: e = run_dense_widths<5, 5, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
-      case 6: e = run_dense_widths<6, 6, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
-      case 8: e = run_dense_widths<8, 8, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+  } else if (sb == 2) {
+    switch (16 * kb + vb) {
+#define KVARN_RUN_CASE(K, V) \
+  case 16 * K + V: e = run_dense_widths<K, V, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      KVARN_WIDTH_PAIRS(KVARN_RUN_CASE)
+#undef KVARN_RUN_CASE
       default: break;
     }
   }

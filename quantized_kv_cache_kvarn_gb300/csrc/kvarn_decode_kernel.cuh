@@ -913,19 +913,13 @@ cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int ctas
 template <int KB, int VB, int SB>
 int resident_widths(int D, int N);
 
-#define KVARN_DECLARE_WIDTHS(KB, VB, SB)                                                             \
+#define KVARN_DECLARE_WIDTHS(KB, VB)                                                                 \
   template <>                                                                                       \
-  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas, \
-                                           cudaStream_t st);                                        \
+  cudaError_t run_dense_widths<KB, VB, 2>(const DecArgs& A, int D, int N, bool bf16, int ctas,     \
+                                          cudaStream_t st);                                         \
   template <>                                                                                       \
-  int resident_widths<KB, VB, SB>(int D, int N);
-KVARN_DECLARE_WIDTHS(4, 2, 2)
-KVARN_DECLARE_WIDTHS(2, 2, 2)
-KVARN_DECLARE_WIDTHS(3, 3, 2)
-KVARN_DECLARE_WIDTHS(4, 4, 2)
-KVARN_DECLARE_WIDTHS(5, 5, 2)
-KVARN_DECLARE_WIDTHS(6, 6, 2)
-KVARN_DECLARE_WIDTHS(8, 8, 2)
+  int resident_widths<KB, VB, 2>(int D, int N);
+KVARN_WIDTH_PAIRS(KVARN_DECLARE_WIDTHS)
 #undef KVARN_DECLARE_WIDTHS
 
 #define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \

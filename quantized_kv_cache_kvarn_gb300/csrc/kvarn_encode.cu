@@ -13,15 +13,11 @@ static cudaError_t launch_dense_w(const EncodeArgs& A, const EncodeParams& p, cu
   if (kb == 4 && vb == 2 && sb == 4)
     return p.bf16 ? launch_dense<D, N, __nv_bfloat16>(A, st) : launch_dense<D, N, __half>(A, st);
   if (D != 128 || sb != 2) return cudaErrorInvalidValue;
-  if (kb == 4 && vb == 2) return launch_encode_widths<4, 2, 2>(A, N, p.bf16, st);
-  if (kb != vb) return cudaErrorInvalidValue;
-  switch (kb) {
-    case 2: return launch_encode_widths<2, 2, 2>(A, N, p.bf16, st);
-    case 3: return launch_encode_widths<3, 3, 2>(A, N, p.bf16, st);
-    case 4: return launch_encode_widths<4, 4, 2>(A, N, p.bf16, st);
-    case 5: return launch_encode_widths<5, 5, 2>(A, N, p.bf16, st);
-    case 6: return launch_encode_widths<6, 6, 2>(A, N, p.bf16, st);
-    case 8: return launch_encode_widths<8, 8, 2>(A, N, p.bf16, st);
+  switch (16 * kb + vb) {
+#define KVARN_ENC_CASE(K, V) \
+  case 16 * K + V: return launch_encode_widths<K, V, 2>(A, N, p.bf16, st);
+    KVARN_WIDTH_PAIRS(KVARN_ENC_CASE)
+#undef KVARN_ENC_CASE
     default: return cudaErrorInvalidValue;
   }
 }

@@ -637,16 +637,10 @@ cudaError_t launch_dense(const EncodeArgs& A, cudaStream_t st) {
 template <int KB, int VB, int SB>
 cudaError_t launch_encode_widths(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
 
-#define KVARN_DECLARE_ENC_WIDTHS(KB, VB, SB) \
-  template <>                                \
-  cudaError_t launch_encode_widths<KB, VB, SB>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
-KVARN_DECLARE_ENC_WIDTHS(4, 2, 2)
-KVARN_DECLARE_ENC_WIDTHS(2, 2, 2)
-KVARN_DECLARE_ENC_WIDTHS(3, 3, 2)
-KVARN_DECLARE_ENC_WIDTHS(4, 4, 2)
-KVARN_DECLARE_ENC_WIDTHS(5, 5, 2)
-KVARN_DECLARE_ENC_WIDTHS(6, 6, 2)
-KVARN_DECLARE_ENC_WIDTHS(8, 8, 2)
+#define KVARN_DECLARE_ENC_WIDTHS(KB, VB) \
+  template <>                            \
+  cudaError_t launch_encode_widths<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+KVARN_WIDTH_PAIRS(KVARN_DECLARE_ENC_WIDTHS)
 #undef KVARN_DECLARE_ENC_WIDTHS
 
 #define KVARN_ENCODE_WIDTHS(KB, VB, SB)                                                                \

@@ -22,13 +22,22 @@ struct EncodeParams {
   int32_t k_bits, v_bits, scale_bytes;  // 4, 2, 4 for the k4v2 preset with fp32 scales
 };
 
-// Code widths and scale sizes with compiled kernels: (4, 2) with fp32 or
-// fp16 scales for every head_dim and tile; (b, b), b in {2, 3, 4, 5, 6, 8},
-// with fp16 scales for head_dim 128.
+// Code widths and scale sizes with compiled kernels: (4, 2) with fp32 scales
+// for every head_dim and tile; with fp16 scales, every pair of a key width
+// and a value width from {2, 3, 4, 5, 6, 8} for head_dim 128 (the gmlx page
+// sets the two widths separately).
+inline bool width_compiled(int32_t b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 inline bool widths_supported(int32_t D, int32_t kb, int32_t vb, int32_t sb) {
-  if (kb == 4 && vb == 2) return sb == 4 || sb == 2;
-  return D == 128 && sb == 2 && kb == vb && (kb == 2 || kb == 3 || kb == 4 || kb == 5 || kb == 6 || kb == 8);
+  if (kb == 4 && vb == 2 && sb == 4) return true;
+  return D == 128 && sb == 2 && width_compiled(kb) && width_compiled(vb);
 }
+
+// X(KB, VB) for every compiled (key width, value width) pair with fp16
+// scales; the key used by the dispatch switches is 16 KB + VB.
+#define KVARN_WIDTH_ROW(X, K) X(K, 2) X(K, 3) X(K, 4) X(K, 5) X(K, 6) X(K, 8)
+#define KVARN_WIDTH_PAIRS(X)                                                         \
+  KVARN_WIDTH_ROW(X, 2) KVARN_WIDTH_ROW(X, 3) KVARN_WIDTH_ROW(X, 4) KVARN_WIDTH_ROW(X, 5) \
+  KVARN_WIDTH_ROW(X, 6) KVARN_WIDTH_ROW(X, 8)
 
 struct AppendParams {
   const void* k;  // newest token per (sequence, KV head): [B][Hkv][D]

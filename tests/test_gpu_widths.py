@@ -1,5 +1,6 @@
 """GPU parity of the other code widths (gmlx page, "The two schemes": kvarn
-widths 2, 3, 4, 5, 6 and 8) with fp16 scales, through the C ABI: the pages the
+widths 2, 3, 4, 5, 6 and 8, set separately for keys and values) with fp16
+scales, through the C ABI: the pages the
 GPU encoder writes against the oracle's encoding, and the GPU decode of pages
 the oracle wrote against the oracle's decode."""
 import numpy as np
@@ -14,6 +15,10 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 WIDTHS = [(2, 2, 128), (3, 3, 128), (4, 4, 64), (5, 5, 128), (6, 6, 128), (6, 6, 64), (8, 8, 128), (4, 2, 128)]
+# separate key and value widths (gmlx page, GMLX_KVARN_BITS): every width on
+# each side at least once, both tile sizes
+WIDTHS += [(8, 4, 128), (6, 4, 64), (4, 6, 128), (3, 2, 128), (2, 5, 64), (5, 3, 128), (8, 6, 128), (2, 8, 64),
+           (6, 2, 128)]
 
 
 @pytest.fixture(scope="module", autouse=True)
