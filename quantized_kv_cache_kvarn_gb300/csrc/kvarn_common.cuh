@@ -454,4 +454,15 @@ __device__ __forceinline__ float warp_sum_xor(float v, int lo, int hi) {
   return v;
 }
 
+// ------------------------------------------------- programmatic launch
+// A kernel that calls pdl_launch_dependents lets the next kernel on its
+// stream, if that one is launched as a programmatic dependent, be scheduled
+// while it still runs; the dependent calls pdl_wait_primary before it reads
+// anything, which returns once the kernel before it has completed and its
+// memory operations are visible. Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace kvarn

@@ -813,6 +813,10 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
     }
     fence_mbar_init();
   }
+  // launched as a programmatic dependent of the kernel before it (a commit,
+  // or whatever wrote the queries, lengths or tails): nothing in global
+  // memory is read before that kernel has completed
+  pdl_wait_primary();
 
   // ---- raw records: items r = blockIdx.x, + gridDim.x, ... of (sequence,
   //      unit, raw chunk)
@@ -880,8 +884,20 @@ cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
   auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<ctas, W * 32, S::SMEM, st>>>(A);
-  return cudaGetLastError();
+  // a programmatic dependent of the kernel before it on the stream: the
+  // grid is scheduled while that kernel's last CTAs run and waits for its
+  // completion before the first global read
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(W * 32);
+  cfg.dynamicSmemBytes = S::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, A);
 }
 
 // CTAs of one decode kernel resident per SM (registers and shared memory).

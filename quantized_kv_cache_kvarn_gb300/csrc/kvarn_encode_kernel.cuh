@@ -562,6 +562,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) encode_dense_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
+  // the decode launched after a commit may be scheduled once every CTA here
+  // has started; it waits for this grid's completion before it reads
+  pdl_launch_dependents();
   const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
   const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);
   if (A.tile_start[b] < 0) return;  // nothing to commit for this sequence (uniform per CTA)
@@ -596,6 +599,7 @@ template <int D, int N, typename T>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
                                                               int32_t max_seq_len, T* tail_k, T* tail_v) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_launch_dependents();
   const bool is_v = blockIdx.z == 1;
   const int head = blockIdx.x, b = blockIdx.y;
   const int L = seq_lens[b];

@@ -35,15 +35,6 @@ __device__ __forceinline__ void warp_fwht(float* v) {
   }
 }
 
-// ------------------------------------------------- programmatic launch
-// The split kernels let the merge kernel be scheduled while their last CTAs
-// still run; the merge waits for their completion (and memory flush) before
-// it reads a partial.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // ------------------------------------------------------------------ merge
 // dst = sum over slots [s0, s1) of exp2(m_s - M) * (this lane's part of the
 // slot vector); every lane reads the slot maxima (one broadcast load each),
