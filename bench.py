@@ -750,7 +750,10 @@ def run_kvarn(args):
             tr = json.load(fh)
         entry = tr.get(wl.name)
         kind = "mla" if wl.rope_dim else "dense"
-        if entry and entry.get("source_digest") == decode_source_digest(kind) and not args.num_seqs:
+        # the capture is of the workload's own decode: the preset widths, one
+        # query token, no raw records (the append step decodes the same pages)
+        same = widths == (4, 2, 4) and args.queries == 1 and not (args.sink or args.recent)
+        if entry and entry.get("source_digest") == decode_source_digest(kind) and not args.num_seqs and same:
             traffic = entry.get("bytes_per_launch")
     except Exception:
         pass
