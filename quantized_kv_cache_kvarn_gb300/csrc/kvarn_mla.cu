@@ -636,22 +636,27 @@ SplitPlan plan_mla(int32_t num_seqs, int32_t max_seq_len) {
     p.tiles_per_split = 1;
     p.nsplit = 0;
   } else {
-    // Two CTAs per (sequence, split), one CTA per SM. Every split writes a
-    // 512-float partial per head that the merge reads back, so take the
-    // fewest splits whose wave efficiency is within 0.05 of the best one.
-    const double slots = device_sm_count();
-    const int units = std::max(1, num_seqs) * 2;
+    // Two CTAs per (sequence, split), one CTA per SM, so SMs / 2 splits run
+    // at once. A split of t tiles costs about t + 1/2 tile times (its
+    // prologue and the 512-float partial per head that it writes and the
+    // merge reads back); with S = num_seqs * ceil(tiles / t) equal splits the
+    // call takes ceil(S / (SMs / 2)) such rounds. Take the split length of
+    // the fewest rounds x cost, the longer one on a tie.
+    const int pairs = std::max(1, device_sm_count() / 2);
     const int max_split = std::max(1, tiles / 2);
-    auto eff_of = [&](int n) {
-      const double waves = units * static_cast<double>(n) / slots;
-      return waves / std::ceil(waves);
-    };
-    double top = 0.0;
-    for (int n = 1; n <= max_split; ++n) top = std::max(top, eff_of(n));
-    int best = 1;
-    while (best < max_split && eff_of(best) < top - 0.05) ++best;
-    p.tiles_per_split = (tiles + best - 1) / best;
-    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    double best_cost = 0.0;
+    int best_tps = tiles;
+    for (int n = 1; n <= max_split; ++n) {
+      const int tps = (tiles + n - 1) / n;
+      const int64_t items = static_cast<int64_t>(std::max(1, num_seqs)) * ((tiles + tps - 1) / tps);
+      const double cost = static_cast<double>((items + pairs - 1) / pairs) * (tps + 0.5);
+      if (n == 1 || cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_tps = tps;
+      }
+    }
+    p.tiles_per_split = best_tps;
+    p.nsplit = (tiles + best_tps - 1) / best_tps;
   }
   p.slots = p.nsplit + 1;
   return p;
