@@ -98,6 +98,14 @@ int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32
 #undef KVARN_RES_CASE
         default: c = 1; break;
       }
+    } else if (D == 256 && sb == 2) {
+      switch (16 * kb + vb) {
+#define KVARN_RES_CASE(K, V) \
+  case 16 * K + V: c = resident_widths256<K, V, 2>(N); break;
+        KVARN_WIDTH_PAIRS_256(KVARN_RES_CASE)
+#undef KVARN_RES_CASE
+        default: c = 1; break;
+      }
     } else {
       c = 1;
     }
@@ -203,6 +211,14 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
     KV_DISPATCH(256, 128, 2)
     KV_DISPATCH(256, 64, 2)
 #undef KV_DISPATCH
+  } else if (sb == 2 && p.D == 256) {
+    switch (16 * kb + vb) {
+#define KVARN_RUN_CASE(K, V) \
+  case 16 * K + V: e = run_dense_widths256<K, V, 2>(A, p.N, p.bf16, plan.ctas, st); break;
+      KVARN_WIDTH_PAIRS_256(KVARN_RUN_CASE)
+#undef KVARN_RUN_CASE
+      default: break;
+    }
   } else if (sb == 2) {
     switch (16 * kb + vb) {
 #define KVARN_RUN_CASE(K, V) \

@@ -938,6 +938,20 @@ int resident_widths(int D, int N);
 KVARN_WIDTH_PAIRS(KVARN_DECLARE_WIDTHS)
 #undef KVARN_DECLARE_WIDTHS
 
+// The same at head_dim 256 (warp pairs share a tile).
+template <int KB, int VB, int SB>
+cudaError_t run_dense_widths256(const DecArgs& A, int N, bool bf16, int ctas, cudaStream_t st);
+template <int KB, int VB, int SB>
+int resident_widths256(int N);
+
+#define KVARN_DECLARE_WIDTHS_256(KB, VB)                                                           \
+  template <>                                                                                     \
+  cudaError_t run_dense_widths256<KB, VB, 2>(const DecArgs& A, int N, bool bf16, int ctas, cudaStream_t st); \
+  template <>                                                                                     \
+  int resident_widths256<KB, VB, 2>(int N);
+KVARN_WIDTH_PAIRS_256(KVARN_DECLARE_WIDTHS_256)
+#undef KVARN_DECLARE_WIDTHS_256
+
 #define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \
   template <>                                                                                           \
   cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas,         \
@@ -956,6 +970,23 @@ KVARN_WIDTH_PAIRS(KVARN_DECLARE_WIDTHS)
     if (D == 128 && N == 128) return resident_dense<128, 128, __half, width_warps<128, 128, KB, VB, SB>(), KB, VB, SB>(); \
     if (D == 128 && N == 64) return resident_dense<128, 64, __half, width_warps<128, 64, KB, VB, SB>(), KB, VB, SB>();   \
     return 1;                                                                                           \
+  }
+
+#define KVARN_DECODE_WIDTHS_256(KB, VB)                                                                \
+  template <>                                                                                          \
+  cudaError_t run_dense_widths256<KB, VB, 2>(const DecArgs& A, int N, bool bf16, int ctas, cudaStream_t st) { \
+    if (N == 128)                                                                                      \
+      return bf16 ? run_dense<256, 128, __nv_bfloat16, 2, KB, VB, 2>(A, ctas, st)                     \
+                  : run_dense<256, 128, __half, 2, KB, VB, 2>(A, ctas, st);                            \
+    if (N == 64)                                                                                       \
+      return bf16 ? run_dense<256, 64, __nv_bfloat16, 2, KB, VB, 2>(A, ctas, st)                      \
+                  : run_dense<256, 64, __half, 2, KB, VB, 2>(A, ctas, st);                             \
+    return cudaErrorInvalidValue;                                                                      \
+  }                                                                                                    \
+  template <>                                                                                          \
+  int resident_widths256<KB, VB, 2>(int N) {                                                           \
+    return N == 128 ? resident_dense<256, 128, __half, 2, KB, VB, 2>()                                 \
+                    : resident_dense<256, 64, __half, 2, KB, VB, 2>();                                 \
   }
 
 }  // namespace kvarn

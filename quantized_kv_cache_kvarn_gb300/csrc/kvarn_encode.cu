@@ -12,7 +12,17 @@ static cudaError_t launch_dense_w(const EncodeArgs& A, const EncodeParams& p, cu
   const int kb = p.k_bits, vb = p.v_bits, sb = p.scale_bytes;
   if (kb == 4 && vb == 2 && sb == 4)
     return p.bf16 ? launch_dense<D, N, __nv_bfloat16>(A, st) : launch_dense<D, N, __half>(A, st);
-  if (D != 128 || sb != 2) return cudaErrorInvalidValue;
+  if (sb != 2) return cudaErrorInvalidValue;
+  if constexpr (D == 256) {
+    switch (16 * kb + vb) {
+#define KVARN_ENC_CASE(K, V) \
+  case 16 * K + V: return launch_encode_widths256<K, V, 2>(A, N, p.bf16, st);
+      KVARN_WIDTH_PAIRS_256(KVARN_ENC_CASE)
+#undef KVARN_ENC_CASE
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (D != 128) return cudaErrorInvalidValue;
   switch (16 * kb + vb) {
 #define KVARN_ENC_CASE(K, V) \
   case 16 * K + V: return launch_encode_widths<K, V, 2>(A, N, p.bf16, st);

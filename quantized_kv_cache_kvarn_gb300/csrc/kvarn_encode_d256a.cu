@@ -1,0 +1,9 @@
+// Encode kernels at head_dim 256 with fp16 scales for the width pairs K2V2, K3V3, K4V2, K4V4.
+#include "kvarn_encode_kernel.cuh"
+
+namespace kvarn {
+KVARN_ENCODE_WIDTHS_256(2, 2)
+KVARN_ENCODE_WIDTHS_256(3, 3)
+KVARN_ENCODE_WIDTHS_256(4, 2)
+KVARN_ENCODE_WIDTHS_256(4, 4)
+}  // namespace kvarn

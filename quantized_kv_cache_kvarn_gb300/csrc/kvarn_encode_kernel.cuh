@@ -645,6 +645,13 @@ cudaError_t launch_encode_widths(const EncodeArgs& A, int N, bool bf16, cudaStre
   template <>                            \
   cudaError_t launch_encode_widths<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
 KVARN_WIDTH_PAIRS(KVARN_DECLARE_ENC_WIDTHS)
+template <int KB, int VB, int SB>
+cudaError_t launch_encode_widths256(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+#define KVARN_DECLARE_ENC_WIDTHS_256(KB, VB) \
+  template <>                                \
+  cudaError_t launch_encode_widths256<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+KVARN_WIDTH_PAIRS_256(KVARN_DECLARE_ENC_WIDTHS_256)
+#undef KVARN_DECLARE_ENC_WIDTHS_256
 #undef KVARN_DECLARE_ENC_WIDTHS
 
 #define KVARN_ENCODE_WIDTHS(KB, VB, SB)                                                                \
@@ -657,6 +664,18 @@ KVARN_WIDTH_PAIRS(KVARN_DECLARE_ENC_WIDTHS)
       return bf16 ? launch_dense<128, 64, __nv_bfloat16, KB, VB, SB>(A, st)                           \
                   : launch_dense<128, 64, __half, KB, VB, SB>(A, st);                                  \
     return cudaErrorInvalidValue;                                                                      \
+  }
+
+#define KVARN_ENCODE_WIDTHS_256(KB, VB)                                                                 \
+  template <>                                                                                         \
+  cudaError_t launch_encode_widths256<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st) { \
+    if (N == 128)                                                                                     \
+      return bf16 ? launch_dense<256, 128, __nv_bfloat16, KB, VB, 2>(A, st)                          \
+                  : launch_dense<256, 128, __half, KB, VB, 2>(A, st);                                 \
+    if (N == 64)                                                                                      \
+      return bf16 ? launch_dense<256, 64, __nv_bfloat16, KB, VB, 2>(A, st)                           \
+                  : launch_dense<256, 64, __half, KB, VB, 2>(A, st);                                  \
+    return cudaErrorInvalidValue;                                                                     \
   }
 
 }  // namespace kvarn

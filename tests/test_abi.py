@@ -60,14 +60,16 @@ def test_layout_rejections(L, field, value, code):
 @pytest.mark.parametrize("vb", [2, 3, 4, 5, 6, 8])
 def test_width_pairs_with_fp16_scales(L, kb, vb):
     """Keys and values take their widths separately (gmlx page, "The two
-    schemes"): every pair is accepted at head_dim 128 with fp16 scales, and
-    the page is the K part then the V part at their own widths."""
+    schemes"): every pair is accepted at head_dim 128 with fp16 scales (equal
+    widths and k4v2 at 256), and the page is the K part then the V part at
+    their own widths."""
     lay = kv.dense_layout(128, 128, 8, 10, k_bits=kb, v_bits=vb, fp16_scales=True)
     assert L.kvarn_layout_check(ctypes.byref(lay)) == 0
     from oracle import layout
     assert kv.page_bytes(lay) == layout.DenseLayout(128, 128, kb, vb, 2).page_bytes
     wide = kv.dense_layout(256, 128, 4, 10, k_bits=kb, v_bits=vb, fp16_scales=True)
-    assert L.kvarn_layout_check(ctypes.byref(wide)) == -2
+    # head_dim 256 carries equal widths and the k4v2 pair
+    assert L.kvarn_layout_check(ctypes.byref(wide)) == (0 if kb == vb or (kb, vb) == (4, 2) else -2)
 
 
 @pytest.mark.parametrize("kb,vb", [(7, 4), (4, 7), (1, 2), (6, 0)])

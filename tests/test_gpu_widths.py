@@ -1,6 +1,6 @@
 """GPU parity of the other code widths (gmlx page, "The two schemes": kvarn
 widths 2, 3, 4, 5, 6 and 8, set separately for keys and values) with fp16
-scales, through the C ABI: the pages the
+scales at head_dim 128 and 256, through the C ABI: the pages the
 GPU encoder writes against the oracle's encoding, and the GPU decode of pages
 the oracle wrote against the oracle's decode."""
 import numpy as np
@@ -19,6 +19,10 @@ WIDTHS = [(2, 2, 128), (3, 3, 128), (4, 4, 64), (5, 5, 128), (6, 6, 128), (6, 6,
 # each side at least once, both tile sizes
 WIDTHS += [(8, 4, 128), (6, 4, 64), (4, 6, 128), (3, 2, 128), (2, 5, 64), (5, 3, 128), (8, 6, 128), (2, 8, 64),
            (6, 2, 128)]
+WIDTHS = [w + (128,) for w in WIDTHS]
+# head_dim 256 (warp pairs share a tile; 8-bit parts wider than one gather box)
+WIDTHS += [(2, 2, 64, 256), (3, 3, 128, 256), (4, 2, 128, 256), (4, 4, 64, 256), (5, 5, 128, 256), (6, 6, 128, 256),
+           (6, 6, 64, 256), (8, 8, 128, 256)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -28,18 +32,18 @@ def built():
     kv.lib()
 
 
-def _case(N):
+def _case(N, D=128):
     wl = W.WORKLOADS["dense32b"].with_(num_seqs=2, num_q_heads=8, num_kv_heads=2, context=2 * N + 37,
-                                       tile_tokens=N)
+                                       tile_tokens=N, head_dim=D)
     return wl, W.make_dense(wl, device="cpu")
 
 
-@pytest.mark.parametrize("kb,vb,N", WIDTHS)
-def test_encode_matches_oracle(kb, vb, N):
-    wl, case = _case(N)
+@pytest.mark.parametrize("kb,vb,N,D", WIDTHS)
+def test_encode_matches_oracle(kb, vb, N, D):
+    wl, case = _case(N, D)
     dev = "cuda"
-    lay = kv.dense_layout(128, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
-    assert kv.page_bytes(lay) == layout.DenseLayout(128, N, kb, vb, 2).page_bytes
+    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
+    assert kv.page_bytes(lay) == layout.DenseLayout(D, N, kb, vb, 2).page_bytes
     cache = kv.alloc_cache(lay, dev)
     err = kv.new_error_word(dev)
     T = int(case.seq_lens[0]) // N
@@ -48,26 +52,26 @@ def test_encode_matches_oracle(kb, vb, N):
     torch.cuda.synchronize()
     assert kv.read_error_flags(err) == 0
     st_k, st_v = parity.check_dense_pages(cache.cpu().numpy(), parity.f64(case.k), parity.f64(case.v),
-                                          case.block_table.numpy(), case.seq_lens.numpy(), N, 128,
+                                          case.block_table.numpy(), case.seq_lens.numpy(), N, D,
                                           kb=kb, vb=vb, sb=2)
-    print(f"\nK{kb}V{vb} N{N}: K codes {st_k['mismatch']}/{st_k['codes']} differ, V {st_v['mismatch']}/"
+    print(f"\nK{kb}V{vb} N{N} D{D}: K codes {st_k['mismatch']}/{st_k['codes']} differ, V {st_v['mismatch']}/"
           f"{st_v['codes']}")
 
 
-@pytest.mark.parametrize("kb,vb,N", WIDTHS)
-def test_decode_on_oracle_pages_matches_oracle(kb, vb, N):
-    wl, case = _case(N)
+@pytest.mark.parametrize("kb,vb,N,D", WIDTHS)
+def test_decode_on_oracle_pages_matches_oracle(kb, vb, N, D):
+    wl, case = _case(N, D)
     k, v = parity.f64(case.k), parity.f64(case.v)
     bt, lens = case.block_table.numpy(), case.seq_lens.numpy()
-    ocache = parity.oracle_dense_cache(k, v, bt, lens, N, 128, case.num_pages, kb=kb, vb=vb, sb=2)
+    ocache = parity.oracle_dense_cache(k, v, bt, lens, N, D, case.num_pages, kb=kb, vb=vb, sb=2)
     tk, tv = parity.tails(k, lens, N), parity.tails(v, lens, N)
     sm = W.default_sm_scale(wl)
-    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(128, N, kb, vb, 2), bt, lens,
+    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(D, N, kb, vb, 2), bt, lens,
                                     sm, tk, tv)
     dev = "cuda"
-    lay = kv.dense_layout(128, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
+    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
     Lmax = int(lens.max())
-    out = torch.empty((wl.num_seqs, wl.num_q_heads, 128), dtype=torch.float32, device=dev)
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, D), dtype=torch.float32, device=dev)
     lse = torch.empty((wl.num_seqs, wl.num_q_heads), dtype=torch.float32, device=dev)
     ws = torch.empty(kv.decode_workspace_bytes(lay, wl.num_seqs, wl.num_q_heads, Lmax), dtype=torch.uint8,
                      device=dev)
@@ -78,6 +82,6 @@ def test_decode_on_oracle_pages_matches_oracle(kb, vb, N):
     torch.cuda.synchronize()
     assert kv.read_error_flags(err) == 0
     diff = np.abs(parity.f64(out) - ref).max()
-    print(f"\nK{kb}V{vb} N{N}: max |out - oracle| = {diff:.3e}")
+    print(f"\nK{kb}V{vb} N{N} D{D}: max |out - oracle| = {diff:.3e}")
     assert diff <= parity.OUT_ATOL
     np.testing.assert_allclose(parity.f64(lse), ref_lse, atol=1e-4, rtol=0)
