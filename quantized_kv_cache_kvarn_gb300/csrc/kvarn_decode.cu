@@ -1,7 +1,10 @@
 // KVarN decode attention: split planning and launch (kernels in
 // kvarn_decode_kernel.cuh; the k4v2 preset with fp32 scales is instantiated
-// here, every other code width in its own kvarn_decode_w*.cu).
+// here, the other code widths in kvarn_decode_k*{lo,hi}.cu and
+// kvarn_decode_d256{a,b}.cu).
 #include <cudaTypedefs.h>
+
+#include <atomic>
 
 #include "kvarn_decode_kernel.cuh"
 
@@ -80,11 +83,15 @@ int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& p
 // once (same for fp16 and bf16 queries, which share the register and smem
 // footprint); computed once per combination.
 int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32_t sb) {
-  static int cache[2][2][9][9][2] = {};
+  // one entry per combination, filled by whichever host thread asks first
+  // (threads racing on an empty entry compute the same value)
+  static std::atomic<int> cache[2][2][9][9][2] = {};
   const int di = D == 256, ni = N == 64, si = sb == 2;
   if (kb < 0 || kb > 8 || vb < 0 || vb > 8) return 1;
-  int& c = cache[di][ni][kb][vb][si];
-  if (!c) {
+  const int known = cache[di][ni][kb][vb][si].load(std::memory_order_relaxed);
+  if (known) return known;
+  int c = 0;
+  {
     if (kb == 4 && vb == 2 && sb == 4) {
       if (D == 128 && N == 128) c = resident_dense<128, 128, __half, 4, 4, 2, 4>();
       else if (D == 128) c = resident_dense<128, 64, __half, 4, 4, 2, 4>();
@@ -110,6 +117,7 @@ int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32
       c = 1;
     }
   }
+  cache[di][ni][kb][vb][si].store(c, std::memory_order_relaxed);
   return c;
 }
 
@@ -120,16 +128,15 @@ int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
 
 // cuTensorMapEncodeTiled of the driver, found once through the runtime.
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // a function-local static: initialised once, thread-safe
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 

@@ -1,6 +1,7 @@
 // KVarN tile encoder: launchers (kernels in kvarn_encode_kernel.cuh; the
 // k4v2 preset with fp32 scales, the latent and the append kernels are
-// instantiated here, other code widths in kvarn_encode_w*.cu).
+// instantiated here, other code widths in kvarn_encode_k*{lo,hi}.cu and
+// kvarn_encode_d256{a,b}.cu).
 #include "kvarn_encode_kernel.cuh"
 
 namespace kvarn {
