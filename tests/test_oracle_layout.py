@@ -187,13 +187,26 @@ def test_six_bit_fp16_scale_record_is_about_40_percent_of_fp16():
     assert abs(per_token / (2 * 2 * 128) - 0.40) < 0.01
 
 
-@pytest.mark.parametrize("kb,vb,sb", [(6, 6, 2), (3, 3, 2), (8, 8, 2), (4, 2, 2), (5, 5, 4)])
-def test_write_read_tile_roundtrip_other_widths(kb, vb, sb):
-    lay = layout.DenseLayout(128, 64, kb, vb, scale_bytes=sb)
-    rng = np.random.default_rng(kb * 10 + vb)
+@pytest.mark.parametrize("D,N,kb,vb,expected", [(128, 128, 8, 4, 3264), (256, 64, 2, 6, 4480)])
+def test_mixed_width_page_bytes_hand_derived(D, N, kb, vb, expected):
+    """Keys and values at their own widths (gmlx page, GMLX_KVARN_BITS), fp16
+    scales. By hand, K8V4 at D 128, N 128: K part 2*128*8 codes + 2*16*2 of
+    a, b + 128*16/128*2 of column slice = 2048 + 64 + 32 = 2144, V part
+    1024 + 64 + 32 = 1120, 3264 in all (the same as K6V6: the code bits per
+    token are equal). K2V6 at D 256, N 64: 1024 + 64 + 128 = 1216 and
+    3072 + 64 + 128 = 3264, 4480 in all."""
+    assert layout.DenseLayout(D, N, kb, vb, scale_bytes=2).page_bytes == expected
+
+
+@pytest.mark.parametrize("D,kb,vb,sb", [(128, 6, 6, 2), (128, 3, 3, 2), (128, 8, 8, 2), (128, 4, 2, 2), (128, 5, 5, 4),
+                                        (128, 8, 4, 2), (128, 2, 6, 2), (128, 5, 3, 2), (256, 6, 6, 2),
+                                        (256, 3, 8, 2)])
+def test_write_read_tile_roundtrip_other_widths(D, kb, vb, sb):
+    lay = layout.DenseLayout(D, 64, kb, vb, scale_bytes=sb)
+    rng = np.random.default_rng(kb * 10 + vb + D)
     cache = np.zeros((8, 1, lay.page_bytes), np.uint8)
-    enc_k = dict(codes=rng.integers(0, 2 ** kb, (64, 128)), a=rng.random(64), b=-rng.random(64), c=rng.random(128))
-    enc_v = dict(codes=rng.integers(0, 2 ** vb, (64, 128)), a=rng.random(64), b=-rng.random(64), c=rng.random(128))
+    enc_k = dict(codes=rng.integers(0, 2 ** kb, (64, D)), a=rng.random(64), b=-rng.random(64), c=rng.random(D))
+    enc_v = dict(codes=rng.integers(0, 2 ** vb, (64, D)), a=rng.random(64), b=-rng.random(64), c=rng.random(D))
     layout.write_tile(cache, lay, [5, 1, 7, 2], 0, enc_k, enc_v)
     k, v = layout.read_tile(cache, lay, [5, 1, 7, 2], 0)
     dt = np.float32 if sb == 4 else np.float16
