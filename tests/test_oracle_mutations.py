@@ -31,6 +31,7 @@ PINS = [
     (tl.test_page_bytes_hand_derived, {}),
     (tl.test_write_read_tile_roundtrip, {}),
     (tl.test_plane_positions_hand_derived, {}),
+    (tl.test_mixed_width_page_bytes_hand_derived, dict(D=128, N=128, kb=8, vb=4, expected=3264)),
     (ta.test_softmax_attention_matches_scipy, {}),
     (ta.test_softmax_attention_two_tokens_by_hand, {}),
     (ta.test_decode_equals_rotated_space_computation, {}),
@@ -182,6 +183,18 @@ def _recent_ignored(orig):
     return lambda L, Q, N, sink, recent: orig(L, Q, N, sink, 0)
 
 
+def _v_region_at_key_width(orig):
+    # the V codes sized by the key width (separate widths mixed up)
+    class Mut(orig):
+        def __init__(self, D, N, k_bits=4, v_bits=2, scale_bytes=4):
+            super().__init__(D, N, k_bits, v_bits, scale_bytes)
+            self.v_a = self.v_codes + 2 * D * k_bits
+            self.v_b = self.v_a + scale_bytes * layout.P
+            self.v_col = self.v_b + scale_bytes * layout.P
+            self.page_bytes = layout._align16(self.v_col + scale_bytes * self.col_per_page)
+    return Mut
+
+
 MUTATIONS = [
     ("hadamard without 1/sqrt(D)", codec, "hadamard", _hadamard_unscaled),
     ("hadamard with a wrong sign", codec, "hadamard", _hadamard_wrong_sign),
@@ -201,6 +214,7 @@ MUTATIONS = [
     ("verify query sees one token too few", attention, "verify_visible", _visible_off_by_one),
     ("recent raw records ignored", attention, "window_committed", _recent_ignored),
     ("plane register halves swapped", layout, "k_plane_position", _plane_halves_swapped),
+    ("V codes sized by the key width", layout, "DenseLayout", _v_region_at_key_width),
 ]
 
 
