@@ -21,7 +21,13 @@
  *     current device; the caller owns every buffer. The library allocates
  *     nothing and keeps no state between calls, except the static scratch
  *     array of kvarn_decode_noalloc described with that call.
- *   - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and
+ *     keep stream order. The dense decode kernels are launched as
+ *     programmatic dependents of the kernel before them on the stream: they
+ *     may be scheduled while that kernel finishes, but read nothing before
+ *     it has completed, so inputs written by any earlier work on the stream
+ *     are seen. Every call takes host sizes and pointers and never
+ *     synchronises, so a sequence of calls can be captured in a CUDA graph.
  *   - Argument errors are found on the host and returned at once, before any
  *     launch. Faults found on the device (a block-table entry outside the
  *     cache, a missing tail, a copy that never completed) set bits in the
