@@ -62,6 +62,23 @@ def _tensor_peak():
         return 1900.0, "fallback"
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's own synthetic batch: every rank decodes a different
+    batch of the same shape (weak scaling, no exchange between ranks)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of the ranks' values (the slowest rank's time); the value
+    itself when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def decode_source_digest(kind="dense"):
     h = hashlib.sha256()
     for f in DECODE_SOURCES[kind]:
@@ -247,7 +264,7 @@ class DenseHarness:
     def __init__(self, kv, W, wl, dev, rank, widths=(4, 2, 4)):
         import torch
         self.kv, self.wl, self.dev = kv, wl, dev
-        self.case = case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
+        self.case = case = W.make_dense(wl, device=dev, seed=rank_seed(wl.seed, rank))
         B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
         self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters, k_bits=widths[0],
@@ -435,7 +452,7 @@ class VerifyHarness(DenseHarness):
     def __init__(self, kv, W, wl, dev, rank, Q, S=0, R=0):
         import torch
         self.kv, self.wl, self.dev, self.Q, self.S, self.R = kv, wl, dev, Q, S, R
-        self.case = case = W.make_dense(wl, device=dev, seed=wl.seed + 7919 * rank)
+        self.case = case = W.make_dense(wl, device=dev, seed=rank_seed(wl.seed, rank))
         B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
         self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters)
@@ -469,7 +486,7 @@ class VerifyHarness(DenseHarness):
         for b, (L, C) in enumerate(zip(lens, committed)):
             self.tail_k[b, :, :L - C] = case.k[b, :, C:L]
             self.tail_v[b, :, :L - C] = case.v[b, :, C:L]
-        self.qv = W.verify_queries(wl, Q, device=dev, seed=wl.seed + 7919 * rank)
+        self.qv = W.verify_queries(wl, Q, device=dev, seed=rank_seed(wl.seed, rank))
         self.out = torch.empty((B, Q, wl.num_q_heads, D), dtype=torch.float32, device=dev)
         self.ws = torch.empty(kv.decode_window_workspace_bytes(self.lay, B, wl.num_q_heads, Q, self.Lmax, S, R),
                               dtype=torch.uint8, device=dev)
@@ -521,7 +538,7 @@ class LatentHarness:
     def __init__(self, kv, W, wl, dev, rank):
         import torch
         self.kv, self.wl, self.dev = kv, wl, dev
-        self.case = case = W.make_latent(wl, device=dev, seed=wl.seed + 7919 * rank)
+        self.case = case = W.make_latent(wl, device=dev, seed=rank_seed(wl.seed, rank))
         B, L = wl.num_seqs, wl.context
         self.lay = kv.latent_layout(case.num_pages, kv.BF16, wl.norm_iters)
         self.cache = kv.alloc_cache(self.lay, dev)
@@ -687,10 +704,7 @@ def run_kvarn(args):
     total_ms = start.elapsed_time(stop)
     dec_ms = d0.elapsed_time(d1) / args.steps
     enc_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     assert kv.read_error_flags(H.err) == 0, "device error in the timed region"
 
     ms_step = total_ms / args.steps
