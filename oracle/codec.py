@@ -1,14 +1,16 @@
 """KVarN per-tile codec, restated in float64 (test infrastructure only).
 
 Sources. "KVarN ... vLLM KV cache quantization" review, paragraph on the
-four-stage quantisation: a raw tile, a Hadamard rotation across the channel
-dimension (orthonormal, so scores are preserved while per-channel outliers are
-spread), an iterative Sinkhorn-like alternation of column- and row-wise
-standard-deviation normalisation in log space, then asymmetric round-to-nearest
-with the scales folded back in when the cache is read. The gmlx "KV cache
-quantization" page, section "The two schemes", restates it: each head is
-rotated by a Hadamard transform and stored in 128-token records scaled so that
-no token or channel dominates.
+four-stage quantisation. Restated: a tile of raw keys or values is turned by
+an orthonormal Hadamard matrix acting on its channels (scores do not change,
+and the energy of an outlier channel is shared among all channels); its
+columns and rows are then rescaled in turn by their standard deviations, a
+Sinkhorn-style alternation whose scales are accumulated as logarithms;
+finally every row is rounded to the nearest level of an asymmetric grid, and
+the scales are multiplied back in when the cache is read. The gmlx "KV cache
+quantization" page, section "The two schemes", describes the same codec as a
+Hadamard rotation of each head followed by 128-token records whose scaling
+keeps any single token or channel from dominating.
 
 Readings where the pages leave a step open (each also listed in the design
 notes):
@@ -17,9 +19,10 @@ notes):
   * One normalisation iteration is a column pass then a row pass. A pass
     divides by the population standard deviation (ddof=0) about the mean and
     adds log(sigma) to the running log-scale; scales leave log space once, at
-    the end. A vector that is numerically constant - sigma <= 2^-20 |mean|,
-    which covers sigma = 0 and the rounding residue of an exactly constant
-    vector - or whose sigma is not finite keeps sigma = 1.
+    the end. A constant vector (all of its entries equal, so that its
+    standard deviation is zero by definition) or one whose sigma is not
+    finite keeps sigma = 1. The test is exact: a vector whose entries differ
+    at all is normalised, however small its spread.
   * Quantisation is per token row of the normalised tile: lo = min, hi = max,
     delta = (hi - lo) / (2^bits - 1), code = clamp(rint((z - lo) / delta)),
     rint being round-half-to-even. A row with hi == lo gets delta = 0 and all
@@ -35,9 +38,9 @@ import numpy as np
 def hadamard(D: int) -> np.ndarray:
     """Sylvester Hadamard matrix of order D (a power of two), scaled by 1/sqrt(D).
 
-    KVarN review, four-stage paragraph: "a Hadamard rotation across the channel
-    dimension (orthonormal ...)". Built by the doubling rule H_2n = [[H, H],
-    [H, -H]] from H_1 = [1].
+    KVarN review, four-stage paragraph (stage two, the orthonormal rotation of
+    the channels). Built by the doubling rule H_2n = [[H, H], [H, -H]] from
+    H_1 = [1].
     """
     if D < 1 or D & (D - 1):
         raise ValueError("Hadamard order must be a power of two")
@@ -54,15 +57,13 @@ def rotate(X: np.ndarray) -> np.ndarray:
     return X @ hadamard(X.shape[-1])
 
 
-CONSTANT_REL = 2.0 ** -20
-
-
 def pop_std(Z: np.ndarray, axis: int) -> np.ndarray:
-    """Population standard deviation along ``axis``; 1 for a numerically
-    constant vector (std <= 2^-20 |mean|) or a non-finite std."""
+    """Population standard deviation along ``axis``; 1 for a constant vector
+    (max == min: its standard deviation is zero by definition, whatever
+    rounding residue the float64 mean leaves) or a non-finite std."""
     s = np.std(Z, axis=axis, ddof=0)
-    mu = np.abs(np.mean(Z, axis=axis))
-    return np.where(np.isfinite(s) & (s > CONSTANT_REL * mu), s, 1.0)
+    constant = np.max(Z, axis=axis) == np.min(Z, axis=axis)
+    return np.where(np.isfinite(s) & ~constant & (s > 0), s, 1.0)
 
 
 def column_pass(Z: np.ndarray):

@@ -156,6 +156,26 @@ def test_normalize_constant_vectors_keep_unit_scale():
     np.testing.assert_array_equal(Zr, R)
 
 
+def test_normalize_tiny_spread_is_not_constant():
+    """Only an exactly constant vector keeps sigma = 1: a column or row whose
+    entries differ by a relative 1e-9 has a genuine (tiny) standard deviation
+    and is divided by it, so it leaves the pass with unit std like any other
+    (the std definition of the four-stage paragraph of the KVarN review has
+    no threshold)."""
+    base = 5.0
+    col = base * (1.0 + 1e-9 * np.array([-1.0, 1.0] * 8))  # population std 5e-9, mean 5
+    Y = np.random.default_rng(17).standard_normal((16, 8))
+    Y[:, 2] = col
+    Z, ls = codec.column_pass(Y)
+    s = np.std(col)
+    assert s > 0 and ls[2] == np.log(s)
+    np.testing.assert_allclose(np.std(Z[:, 2]), 1.0, rtol=1e-6)
+    R = np.tile(col, (3, 2))
+    Zr, lr = codec.row_pass(R)
+    np.testing.assert_allclose(lr, np.log(s), rtol=1e-12)
+    np.testing.assert_allclose(np.std(Zr, axis=1), 1.0, rtol=1e-6)
+
+
 def test_normalize_zero_column_stays_finite():
     Y = np.random.default_rng(9).standard_normal((16, 8))
     Y[:, 3] = 0.0

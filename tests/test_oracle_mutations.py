@@ -24,6 +24,8 @@ PINS = [
     (tc.test_normalize_rows_have_unit_std, dict(T=2)),
     (tc.test_column_pass_gives_unit_column_std, {}),
     (tc.test_normalize_columns_converge_toward_one, {}),
+    (tc.test_normalize_constant_vectors_keep_unit_scale, {}),
+    (tc.test_normalize_tiny_spread_is_not_constant, {}),
     (tc.test_rtn_hand_worked_rows, {}),
     (tc.test_rtn_range_endpoints_and_error_bound, dict(bits=4)),
     (tc.test_reconstruction_error_shrinks_with_bits, {}),
@@ -89,6 +91,24 @@ def _normalize_swap_scales(orig):
 def _std_sample(orig):
     def s(Z, axis):
         v = np.std(Z, axis=axis, ddof=1)
+        return np.where(np.isfinite(v) & (v > 0), v, 1.0)
+    return s
+
+
+def _std_relative_threshold(orig):
+    # a near-constant vector (std <= 2^-20 |mean|) treated as constant
+    def s(Z, axis):
+        v = np.std(Z, axis=axis, ddof=0)
+        mu = np.abs(np.mean(Z, axis=axis))
+        return np.where(np.isfinite(v) & (v > 2.0 ** -20 * mu), v, 1.0)
+    return s
+
+
+def _std_zero_only(orig):
+    # only sigma == 0 in float64 counts as constant: the rounding residue of
+    # the mean of an exactly constant vector is divided out as spread
+    def s(Z, axis):
+        v = np.std(Z, axis=axis, ddof=0)
         return np.where(np.isfinite(v) & (v > 0), v, 1.0)
     return s
 
@@ -201,6 +221,8 @@ MUTATIONS = [
     ("row pass before column pass", codec, "variance_normalize", _normalize_row_first),
     ("row and column scales swapped", codec, "variance_normalize", _normalize_swap_scales),
     ("sample std instead of population std", codec, "pop_std", _std_sample),
+    ("constant test with a relative threshold", codec, "pop_std", _std_relative_threshold),
+    ("constant test on the float64 std alone", codec, "pop_std", _std_zero_only),
     ("floor instead of round-to-nearest", codec, "rtn_rows", _rtn_floor),
     ("2^bits levels instead of 2^bits - 1", codec, "rtn_rows", _rtn_levels_off_by_one),
     ("offset term b dropped at dequantisation", codec, "dequantize_rotated", _dequant_drop_b),
