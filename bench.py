@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +40,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn packed-KV GB/s (% of HBM peak), tokens/s; encode tokens/s"
 WORKLOAD = "dense32b"
+# decode calls timed back to back for the roofline figure (about 25 ms of
+# work on the dense-32B workload, so that clock samples fall inside it)
+DECODE_CALLS = 200
+# workloads measured beside the main one in a default run (each its own
+# step, decode call and roofline)
+EXTRA_WORKLOADS = ("toy", "g64", "hybrid", "mla")
+L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = {"dense": ["kvarn_decode.cu", "kvarn_decode_kernel.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"],
                   "mla": ["kvarn_mla.cu", "kvarn_tcgen05.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"]}
 
@@ -105,7 +113,7 @@ class ClockSampler:
 
     def __init__(self):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"kvarn_clocks_{os.getpid()}.csv")
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -113,7 +121,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -601,6 +609,104 @@ class LatentHarness:
 
 
 # ---------------------------------------------------------------- main arm
+def roofline_of(H, wl, dec_ms, traffic=None, kernel=None):
+    """Roofline object of a decode call of `dec_ms` ms: HBM for the dense
+    workloads (packed bytes read), bf16 tensor peak for MLA (algorithmic
+    flops: 2 per multiply-add of the scores, latent + rope width, and of the
+    output, latent width, per sequence, head and token)."""
+    peak, peak_kind = _peaks()
+    gbs = H.packed / (dec_ms * 1e-3) / 1e9
+    if wl.rope_dim:
+        flops = 2.0 * sum(H.lens) * wl.num_q_heads * (2 * wl.head_dim + wl.rope_dim)
+        tpk, tpk_kind = _tensor_peak()
+        tf = flops / (dec_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s",
+                "frac": round(tf / tpk, 4), "traffic": traffic, "kernel": kernel, "peak_kind": tpk_kind,
+                "flops_per_launch": flops, "hbm_gbs": round(gbs, 2), "hbm_frac": round(gbs / peak, 4)}
+    return {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "traffic": traffic, "kernel": kernel, "peak_kind": peak_kind, "bytes_per_launch": H.packed}
+
+
+def measure_extra(kv, W, name, dev, rank, steps, warmup):
+    """One more workload in the same run: its step (commit + decode, K back
+    to back), its decode call (DECODE_CALLS back to back) and its commit,
+    with the roofline of the decode call. A workload whose packed reads fit
+    in L2 (toy) is timed one step at a time with L2 flushed between steps
+    (outside the timed events)."""
+    import torch
+    wl = W.WORKLOADS[name]
+    H = LatentHarness(kv, W, wl, dev, rank) if wl.rope_dim else DenseHarness(kv, W, wl, dev, rank)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(warmup):
+        H.encode()
+        H.decode()
+    torch.cuda.synchronize()
+    small = H.packed < L2_BYTES
+    if small:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        times, dtimes, ctimes = [], [], []
+        for _ in range(steps):
+            flush.fill_(1.0)
+            a, b_ = ev(), ev()
+            a.record(stream)
+            H.encode()
+            H.decode()
+            b_.record(stream)
+            flush.fill_(2.0)
+            c0, c1, c2 = ev(), ev(), ev()
+            c0.record(stream)
+            H.encode()
+            c1.record(stream)
+            flush.fill_(3.0)
+            c2.record(stream)
+            d0, d1 = ev(), ev()
+            d0.record(stream)
+            H.decode()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b_))
+            ctimes.append(c0.elapsed_time(c1))
+            dtimes.append(d0.elapsed_time(d1))
+        ms_step, dec_ms, com_ms = statistics.median(times), statistics.median(dtimes), statistics.median(ctimes)
+        del flush
+    else:
+        a, b_ = ev(), ev()
+        a.record(stream)
+        for _ in range(steps):
+            H.encode()
+            H.decode()
+        b_.record(stream)
+        d0, d1 = ev(), ev()
+        d0.record(stream)
+        for _ in range(DECODE_CALLS):
+            H.decode()
+        d1.record(stream)
+        cs = []
+        for _ in range(steps):
+            c0, c1 = ev(), ev()
+            c0.record(stream)
+            H.encode()
+            c1.record(stream)
+            H.decode()
+            cs.append((c0, c1))
+        torch.cuda.synchronize()
+        ms_step = a.elapsed_time(b_) / steps
+        dec_ms = d0.elapsed_time(d1) / DECODE_CALLS
+        com_ms = statistics.mean(x.elapsed_time(y) for x, y in cs)
+    assert kv.read_error_flags(H.err) == 0, f"device error in the {name} workload"
+    out = {"workload": _workload_desc(wl), "ms_per_step": round(ms_step, 5),
+           "value": round(H.packed / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "decode_ms": round(dec_ms, 5), "commit_ms": round(com_ms, 5), "commit_tokens": H.encode_tokens,
+           "decode_tokens_per_s": round(wl.num_seqs / (ms_step * 1e-3), 1),
+           "l2": ("packed reads fit in L2: one step per timing, L2 flushed between steps (median of K)" if small
+                  else f"inputs larger than L2 ({H.packed / 1e6:.0f} MB of packed KV read per step)"),
+           "roofline": roofline_of(H, wl, dec_ms, kernel=f"decode call, {'median of K single' if small else str(DECODE_CALLS) + ' back-to-back'} calls")}
+    del H
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_kvarn(args):
     import torch
     import torch.distributed as dist
@@ -661,6 +767,12 @@ def run_kvarn(args):
         torch.cuda.synchronize()
         assert kv.read_error_flags(H.err) == 0
         return
+    if args.only == "full-encode":
+        for _ in range(args.warmup + args.steps):
+            H.full_encode()
+        torch.cuda.synchronize()
+        assert kv.read_error_flags(H.err) == 0
+        return
 
     for _ in range(args.warmup):
         H.encode()
@@ -694,7 +806,7 @@ def run_kvarn(args):
         H.decode()
     d0, d1 = ev(), ev()
     d0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(DECODE_CALLS):
         H.decode()
     d1.record(stream)
     torch.cuda.synchronize()
@@ -702,7 +814,7 @@ def run_kvarn(args):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     total_ms = start.elapsed_time(stop)
-    dec_ms = d0.elapsed_time(d1) / args.steps
+    dec_ms = d0.elapsed_time(d1) / DECODE_CALLS
     enc_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
     total_ms = max_over_ranks(total_ms, dev)
     assert kv.read_error_flags(H.err) == 0, "device error in the timed region"
@@ -740,7 +852,7 @@ def run_kvarn(args):
         ms16 = a.elapsed_time(b_) / args.steps
         fp16 = {"tokens_per_s": round(B / (ms16 * 1e-3), 1), "ms": round(ms16, 5),
                 "gbs": round(bytes16 / (ms16 * 1e-3) / 1e9, 2), "kvarn_decode_speedup": round(ms16 / dec_ms, 3)}
-        del keep
+        del keep, run16
 
     # end to end through the public API with host buffers
     run_e2e, h2d, d2h = H.e2e_setup()
@@ -808,30 +920,32 @@ def run_kvarn(args):
         pool, cores = oracle_pool(len(work))
         with pool:
             wall = oracle_time(pool, cores, work)
+        # the same oracle on one core: two of the sampled units
+        one = work[:2]
+        pool1, _ = oracle_pool(1)
+        with pool1:
+            wall1 = oracle_time(pool1, 1, one)
+        frac1 = frac * len(one) / len(work)
         unit = "(sequence, 16-head group)" if wl.rope_dim else "(sequence, KV head)"
         cpu = {"value": round(frac * H.packed / wall / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{len(work)} {unit} units of one step ({frac:.4f} of it): commit and decode, "
                          f"float64 oracle on {cores} single-threaded host processes",
-               "decode_tokens_per_s": round(frac * B * args.queries / wall, 4)}
+               "decode_tokens_per_s": round(frac * B * args.queries / wall, 4),
+               "single_core": {"value": round(frac1 * H.packed / wall1 / 1e9, 6), "unit": "GB/s", "cores": 1,
+                               "sample": f"{len(one)} of the same units on one single-threaded process"}}
 
-    kernel_desc = ("decode call (split kernel + merge kernel): K calls back to back after the timed steps, "
-                   "CUDA events on its stream")
-    if wl.rope_dim:
-        # MLA: tensor-bound. Algorithmic flops = 2 per multiply-add of the
-        # scores (latent + rope width) and of the output (latent width) for
-        # every (sequence, head, token); the kernel issues twice that on the
-        # tensor cores (fp16 hi + lo operands).
-        flops = 2.0 * sum(H.lens) * wl.num_q_heads * (2 * wl.head_dim + wl.rope_dim)
-        tpk, tpk_kind = _tensor_peak()
-        tf = flops / (dec_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s",
-                    "frac": round(tf / tpk, 4), "traffic": traffic, "kernel": kernel_desc,
-                    "peak_kind": tpk_kind, "flops_per_launch": flops,
-                    "hbm_gbs": round(dec_gbs, 2), "hbm_frac": round(dec_gbs / peak, 4)}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                    "frac": round(dec_gbs / peak, 4), "traffic": traffic, "kernel": kernel_desc,
-                    "peak_kind": peak_kind, "bytes_per_launch": H.packed}
+    kernel_desc = (f"decode call (split kernel + merge kernel): {DECODE_CALLS} calls back to back after the timed "
+                   "steps, CUDA events on its stream")
+    roofline = roofline_of(H, wl, dec_ms, traffic, kernel_desc)
+    # the full-context encode against HBM: its fp16/bf16 K and V read once
+    # and its pages written once (algorithmic bytes)
+    enc_bytes = enc_tokens * wl.num_kv_heads * (2 * 2 * wl.head_dim if not wl.rope_dim else 2 * (wl.head_dim + wl.rope_dim))
+    enc_bytes += H.packed
+    enc_gbs = enc_bytes / (enc_full_ms * 1e-3) / 1e9
+    encode_roofline = {"bound": "hbm", "achieved": round(enc_gbs, 2), "peak": peak, "unit": "GB/s",
+                       "frac": round(enc_gbs / peak, 4), "bytes_per_launch": enc_bytes,
+                       "kernel": "full-context encode (encode_tiles over every committed tile), 3 calls",
+                       "note": "ALU- and latency-bound, not HBM-bound: issue-slot use from ncu in profiles/"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -856,6 +970,7 @@ def run_kvarn(args):
         "encode_tokens_per_s": round(encode_tok_s, 1), "encode_full_context_ms": round(enc_full_ms, 4),
         "fp16_kv_decode": fp16,
         "roofline": roofline,
+        "encode_roofline": encode_roofline,
         "e2e": {"value": round(world * H.packed / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": H.launches * args.steps,
@@ -865,6 +980,15 @@ def run_kvarn(args):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    plain = not (args.num_seqs or args.queries > 1 or args.sink or args.recent or args.append
+                 or widths != (4, 2, 4) or args.no_extra)
+    if plain and world == 1 and args.workload == WORKLOAD:
+        # the other workloads of the same family, each measured on its own
+        del H, run_e2e, f
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            line["workloads"][name] = measure_extra(kv, W, name, dev, rank, args.steps, args.warmup)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -927,7 +1051,10 @@ def main():
                     help="commit through kvarn_append of the newest token (fused append + commit)")
     ap.add_argument("--sink", type=int, default=0, help="raw sink tokens (a multiple of the tile)")
     ap.add_argument("--recent", type=int, default=0, help="newest accepted tokens kept raw")
-    ap.add_argument("--only", choices=["decode", "encode"], default=None,
+    ap.add_argument("--no-extra", action="store_true",
+                    help="measure only the named workload (a default run adds the toy, g64, hybrid and MLA "
+                         "workloads as extra keys)")
+    ap.add_argument("--only", choices=["decode", "encode", "full-encode"], default=None,
                     help="run only warm-up + timed launches of one call, print nothing (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -194,6 +194,41 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
                            kvarn_stream_t stream);
 
 /*
+ * kvarn_encode_tiles_staged - kvarn_encode_tiles that also writes the fp32
+ * intermediates of every tile it encodes, so that each stage of the codec
+ * (KVarN review, four-stage paragraph) can be checked on its own: the
+ * rotation, the normalisation, and the round-to-nearest of the normalised
+ * values on their row grids. The pages written are the same bytes as
+ * kvarn_encode_tiles writes. A diagnostic call: the stage records are large.
+ *
+ *   stages  device fp32, kvarn_encode_stage_floats(layout, num_seqs,
+ *           chunk_tokens) floats, 16-byte aligned. Record (b, h, u, s)
+ *           (s = 0 for K, 1 for V; u the tile within the chunk) starts at
+ *           float (((b*Hkv + h)*(chunk_tokens/N) + u)*2 + s) * R,
+ *           R = 2*N*D + 3*N + D, and holds, in order:
+ *             Y[N][D]   the rotated tile x H (token rows)
+ *             Z[N][D]   the tile after the T normalisation iterations
+ *             r[N]      row scales (products of the row standard deviations)
+ *             lo[N]     row minimum of Z
+ *             delta[N]  grid step (max - min) / (2^bits - 1) of the row
+ *             c[D]      column scales
+ *           The code of element (i, j) is the round-half-to-even of the
+ *           exact quotient (Z[i][j] - lo[i]) / delta[i] of these fp32
+ *           values (0 where delta is 0), and the stored row scales are the
+ *           fp32 products a = r * delta and b = r * lo.
+ * Records of sequences skipped by a negative tile_start are not written.
+ * Other arguments, results and errors as kvarn_encode_tiles; a NULL `stages`
+ * is KVARN_EINVAL.
+ */
+int64_t kvarn_encode_stage_floats(const kvarn_layout* layout, int32_t num_seqs, int32_t chunk_tokens);
+
+int32_t kvarn_encode_tiles_staged(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                                  int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const kvarn_layout* layout, void* cache, float* stages,
+                                  uint32_t* error_flags, kvarn_stream_t stream);
+
+/*
  * kvarn_append - fused append and commit: one launch per decode step for the
  * whole batch (turbo-attn page, "Compress-on-the-wire": the new token is
  * encoded and written to the packed cache in one kernel; KVarN review,
@@ -424,9 +459,10 @@ int32_t kvarn_decode_mla(const void* q_latent, const void* q_rope, int32_t num_h
  * of static device memory inside the library, which every GPU that loads
  * the library holds until the process exits. The call allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture on the device.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it for the later calls; make that
+ *     first call before any stream capture on the device. A lookup that
+ *     fails returns KVARN_ECUDA and is tried again by the next call.
  *   - Every call shares the one array per device and leaves its partials
  *     there; calls whose kernels overlap on the GPU (two streams, two host
  *     threads) race on it. Nothing in it needs to start at zero.

@@ -56,6 +56,8 @@ _SIGS = {
     "kvarn_layout_check": ([_LP], _I32),
     "kvarn_page_bytes": ([_LP], _I64),
     "kvarn_encode_tiles": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P, _I32, _LP, _P, _P, _P], _I32),
+    "kvarn_encode_stage_floats": ([_LP, _I32, _I32], _I64),
+    "kvarn_encode_tiles_staged": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P, _I32, _LP, _P, _P, _P, _P], _I32),
     "kvarn_append": ([_P, _P, _P, _I32, _P, _P, _I32, _P, _I32, _LP, _P, _P, _P], _I32),
     "kvarn_decode_workspace_bytes": ([_LP, _I32, _I32, _I32], _I64),
     "kvarn_decode": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _I64,
@@ -167,6 +169,27 @@ def encode_tiles(k, v, layout: Layout, tile_start, block_table, cache, err, chun
     _check(lib().kvarn_encode_tiles(_ptr(k), _ptr(v), k.stride(0), k.stride(1), B, C, _ptr(tile_start),
                                     _ptr(block_table), block_table.stride(0), ctypes.byref(layout),
                                     _ptr(cache), _ptr(err), _stream(stream)), "encode_tiles")
+
+
+def encode_stage_floats(layout: Layout, num_seqs: int, chunk_tokens: int) -> int:
+    n = lib().kvarn_encode_stage_floats(ctypes.byref(layout), num_seqs, chunk_tokens)
+    if n < 0:
+        raise KvarnError("invalid arguments for kvarn_encode_stage_floats")
+    return n
+
+
+def encode_tiles_staged(k, v, layout: Layout, tile_start, block_table, cache, stages, err, chunk_tokens=None,
+                        stream=None):
+    """encode_tiles that also fills `stages` (fp32, encode_stage_floats(...)
+    floats) with the fp32 intermediates of every encoded tile."""
+    B = k.shape[0]
+    C = k.shape[2] if chunk_tokens is None else chunk_tokens
+    assert k.stride() == v.stride() and k.stride(3) == 1 and k.stride(2) == k.shape[3]
+    assert stages.dtype == torch.float32 and stages.numel() >= encode_stage_floats(layout, B, C)
+    _check(lib().kvarn_encode_tiles_staged(_ptr(k), _ptr(v), k.stride(0), k.stride(1), B, C, _ptr(tile_start),
+                                           _ptr(block_table), block_table.stride(0), ctypes.byref(layout),
+                                           _ptr(cache), _ptr(stages), _ptr(err), _stream(stream)),
+           "encode_tiles_staged")
 
 
 def append(k, v, seq_lens, max_seq_len, tail_k, tail_v, block_table, layout: Layout, cache, err, stream=None):

@@ -79,11 +79,10 @@ static bool is_preset(const kvarn_layout* L) {
   return L->k_bits == 4 && L->v_bits == 2 && L->scale_dtype == 0;
 }
 
-int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
-                           int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
-                           const int32_t* block_table, int32_t bt_stride,
-                           const kvarn_layout* L, void* cache, uint32_t* error_flags,
-                           kvarn_stream_t stream) {
+static int32_t encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                            int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                            const int32_t* block_table, int32_t bt_stride, const kvarn_layout* L,
+                            void* cache, float* stages, uint32_t* error_flags, kvarn_stream_t stream) {
   int32_t s = check_dense(L);
   if (s != KVARN_OK) return s;
   if (num_seqs < 0 || chunk_tokens < 0 || chunk_tokens % L->tile_tokens) return KVARN_EINVAL;
@@ -113,7 +112,35 @@ int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int
   p.k_bits = L->k_bits;
   p.v_bits = L->v_bits;
   p.scale_bytes = L->scale_dtype == 1 ? 2 : 4;
+  p.stages = stages;
   return from_cuda(launch_encode_dense(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvarn_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                           int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                           const int32_t* block_table, int32_t bt_stride,
+                           const kvarn_layout* L, void* cache, uint32_t* error_flags,
+                           kvarn_stream_t stream) {
+  return encode_tiles(k, v, seq_stride, head_stride, num_seqs, chunk_tokens, tile_start, block_table,
+                      bt_stride, L, cache, nullptr, error_flags, stream);
+}
+
+int64_t kvarn_encode_stage_floats(const kvarn_layout* L, int32_t num_seqs, int32_t chunk_tokens) {
+  if (check_dense(L) != KVARN_OK || num_seqs < 0 || chunk_tokens < 0 || chunk_tokens % L->tile_tokens)
+    return -1;
+  return static_cast<int64_t>(num_seqs) * L->num_kv_heads * (chunk_tokens / L->tile_tokens) * 2 *
+         stage_floats(L->head_dim, L->tile_tokens);
+}
+
+int32_t kvarn_encode_tiles_staged(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                                  int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const kvarn_layout* L, void* cache, float* stages,
+                                  uint32_t* error_flags, kvarn_stream_t stream) {
+  if (!stages) return KVARN_EINVAL;
+  if (!aligned(stages, 16)) return KVARN_EALIGN;
+  return encode_tiles(k, v, seq_stride, head_stride, num_seqs, chunk_tokens, tile_start, block_table,
+                      bt_stride, L, cache, stages, error_flags, stream);
 }
 
 // max_seq_len here: the accepted length bound (sizes the tile splits); raw_max:

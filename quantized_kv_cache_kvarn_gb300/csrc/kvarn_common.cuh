@@ -39,6 +39,12 @@ struct DensePage {
   __host__ __device__ constexpr int bytes() const { return k_part() + v_part(); }
 };
 
+// Floats of one dense tile's stage record (the encoder's fp32 intermediates:
+// Y and Z, N x D each, then r, lo, delta per token and c per channel).
+__host__ __device__ constexpr int64_t stage_floats(int D, int N) {
+  return 2LL * N * D + 3LL * N + D;
+}
+
 // Dense decode shapes whose page parts are staged by TMA gathers of four
 // pages: a 2-D tensor map over the cache with 8-byte elements and one row per
 // (page, KV head), boxes one row high and at most 256 elements (2048 bytes)

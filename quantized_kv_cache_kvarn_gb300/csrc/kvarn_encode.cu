@@ -50,6 +50,7 @@ cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st) {
   A.norm_iters = p.norm_iters;
   A.err = p.err;
   A.num_seqs = p.num_seqs;
+  A.stages = p.stages;
   if (A.chunk_tiles == 0 || p.num_seqs == 0) return cudaSuccess;
   if (p.D == 128 && p.N == 128) return launch_dense_w<128, 128>(A, p, st);
   if (p.D == 128 && p.N == 64) return launch_dense_w<128, 64>(A, p, st);

@@ -69,7 +69,13 @@ struct EncodeArgs {
   int32_t norm_iters;
   int32_t rope_dim;
   uint32_t* err;
+  // optional fp32 intermediates of every encoded dense tile (null in normal
+  // use): per (sequence, KV head, chunk tile, K|V) the rotated tile Y, the
+  // normalised tile Z (both N x D, token rows), then r, lo, delta per token
+  // and c per channel
+  float* stages;
 };
+
 
 // Merge of two (mean, M2) summaries of n values each (Chan, Golub and
 // LeVeque's pairwise update of the sum of squared deviations): the mean of
@@ -150,12 +156,56 @@ __device__ __forceinline__ void read_segment(float (&v)[16], const float* colbuf
   }
 }
 
-// Population std; 1 for a numerically constant vector (std <= 2^-20 |mean|,
-// which covers the rounding residue of an exactly constant one) or a
-// non-finite std.
-__device__ __forceinline__ float safe_sigma(float var, float mean) {
+// Population std; 1 for a constant vector or a non-finite std. The sums
+// behind `var` are pairwise trees and pairwise (mean, M2) merges, so a vector
+// of equal entries gives var == 0 exactly (every partial mean is exact and
+// every deviation zero), and one whose entries differ gives var > 0 (some
+// deviation or merge difference is non-zero; only differences below ~1e-19
+// would square to zero in fp32): var == 0 is the test max == min.
+__device__ __forceinline__ float safe_sigma(float var) {
   const float s = sqrtf(var);
-  return (isfinite(s) && s > 9.5367431640625e-07f * fabsf(mean)) ? s : 1.f;
+  return (isfinite(s) && s > 0.f) ? s : 1.f;
+}
+
+// Round-to-nearest of normalised values on their row's grid (lo, delta).
+// Two codes at a time: x = (z - lo) * (1/delta) as the caller formed it; the
+// sum x + 1.5 * 2^23 rounds x to an integer, half to even, in the addition
+// itself (the integer is the low bits of the sum), and x minus that integer
+// says how near x lies to a half-way point. The product is within a few
+// units in the last place of the exact quotient (z - lo) / delta of the fp32
+// operands, so only where it lands within 2^-14 of a half-way point is the
+// side taken again, exactly, by grid_boundary_code. The result is the
+// round-half-to-even of the exact quotient, clamped to qmax (which only
+// non-finite input can exceed).
+static __device__ __noinline__ uint32_t grid_boundary_code(float z, float lo, float delta, float x);
+
+__device__ __forceinline__ void grid_codes2(float2 z, float lo, float delta, float2 x, uint32_t qmax, uint32_t& q0,
+                                            uint32_t& q1) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  const float2 t = f2add(x, f2(kRound));
+  const float2 d = f2fma(f2add(t, f2(-kRound)), f2(-1.f), x);
+  q0 = __float_as_uint(t.x) - 0x4B400000u;
+  q1 = __float_as_uint(t.y) - 0x4B400000u;
+  if (fabsf(d.x) > 0.5f - 0x1p-14f) q0 = grid_boundary_code(z.x, lo, delta, x.x);
+  if (fabsf(d.y) > 0.5f - 0x1p-14f) q1 = grid_boundary_code(z.y, lo, delta, x.y);
+  q0 = min(q0, qmax);
+  q1 = min(q1, qmax);
+}
+
+// The side of the half-way point k + 1/2 nearest x, decided exactly: z - lo
+// is the rounded sum s plus its rounding error e (the two-sum), and
+// s - (k + 1/2) delta, a small multiple of the finer of the two operands'
+// last-place units near the boundary, is formed exactly by the fused
+// multiply-add; the sign of that plus e is the sign of the exact
+// (z - lo) - (k + 1/2) delta. A tie goes to the even code.
+static __device__ __noinline__ uint32_t grid_boundary_code(float z, float lo, float delta, float x) {
+  const float s = __fadd_rn(z, -lo);
+  const float bb = __fsub_rn(s, z);
+  const float e = __fadd_rn(__fsub_rn(z, __fsub_rn(s, bb)), __fsub_rn(-lo, bb));
+  const float k = floorf(x);
+  const float w = __fadd_rn(__fmaf_rn(-(k + 0.5f), delta, s), e);
+  const uint32_t ki = static_cast<uint32_t>(k);
+  return ki + ((w > 0.f || (w == 0.f && (ki & 1u))) ? 1u : 0u);
 }
 
 // Latent page word order (before the 16-byte unit swizzle): the 32-bit word
@@ -240,6 +290,21 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     pages[tid] = pg;
   }
 
+  // ---- the optional stage record of this tile (dense tiles only)
+  float* rec = nullptr;
+  if constexpr (KIND == 0 && CS == 1) {
+    if (A.stages != nullptr)
+      rec = A.stages + ((static_cast<int64_t>(b) * A.num_kv_heads + head) * A.chunk_tiles + u) * 2 * stage_floats(D, N) +
+            (IS_V ? stage_floats(D, N) : 0);
+  }
+  auto record_tile = [&](float* dst) {  // this thread's values of the N x D tile, token rows
+#pragma unroll
+    for (int i = 0; i < S::RPT; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<float2*>(dst + static_cast<int64_t>(local_row(i)) * D + seg * 16 + 2 * e) = xp[i][e];
+  };
+
   // ---- Hadamard: 4 in-register stages, then lane butterflies, then 1/sqrt(D)
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
@@ -278,6 +343,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 #pragma unroll
       for (int e = 0; e < 8; ++e) xp[i][e] = f2mul(xp[i][e], rsd);
   }
+  if (rec != nullptr) record_tile(rec);
 
   // ---- variance normalisation, T iterations of (column pass, row pass)
   float cscale = 1.f;  // column scale of channel tid (tid < D)
@@ -293,9 +359,11 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     float2 mo[16];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      float2 t = xp[0][e];
+      // pairwise, so that equal entries sum exactly
+      float2 cs[S::RPT];
 #pragma unroll
-      for (int i = 1; i < S::RPT; ++i) t = f2add(t, xp[i][e]);
+      for (int i = 0; i < S::RPT; ++i) cs[i] = xp[i][e];
+      const float2 t = tree_reduce(cs, [](float2 u, float2 w) { return f2add(u, w); });
       const float2 m = f2mul(t, f2(1.f / S::RPT)), nm = f2mul(m, f2(-1.f));
       float2 v = f2(0.f);
 #pragma unroll
@@ -308,7 +376,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     }
     const float2 cm = column_moments<D, N, CS>(mo, red, colpart + (it & 1) * 2 * D);
     if (tid < D) {
-      const float sig = safe_sigma(cm.y, cm.x);
+      const float sig = safe_sigma(cm.y);
       cscale *= sig;
       colbuf[tid] = 1.f / sig;
     }
@@ -351,13 +419,17 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
         r = merge_moments(r, make_float2(__shfl_xor_sync(0xffffffffu, r.x, o), __shfl_xor_sync(0xffffffffu, r.y, o)), n);
         n *= 2.f;
       }
-      const float sig = safe_sigma(r.y * invD, r.x);
+      const float sig = safe_sigma(r.y * invD);
       rscale[i] *= sig;
       const float2 ri = f2(1.f / sig);
 #pragma unroll
       for (int e = 0; e < 8; ++e) xp[i][e] = f2mul(xp[i][e], ri);
     }
     // colbuf is rewritten next only after the next column reduction's barrier
+  }
+  if (rec != nullptr) {
+    record_tile(rec + static_cast<int64_t>(N) * D);
+    if (tid < D) rec[2 * N * D + 3 * N + tid] = cscale;
   }
 
   // ---- asymmetric RTN per row: codes as bytes, Pc[i][k] byte e = channel 4k + e
@@ -384,12 +456,12 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       uint32_t word = 0;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        // x - lo lies in [0, hi - lo], so the rounded quotient lies in
-        // [0, QMAX]; the unsigned conversion saturates and min() only
-        // guards non-finite input
-        const float2 z = f2mul(f2add(xp[i][2 * k + e], nlo), rv);
-        const uint32_t q0 = min(__float2uint_rn(z.x), static_cast<uint32_t>(QMAX));
-        const uint32_t q1 = min(__float2uint_rn(z.y), static_cast<uint32_t>(QMAX));
+        // x - lo lies in [0, hi - lo], so the code lies in [0, QMAX]; the
+        // unsigned conversion saturates and min() only guards non-finite
+        // input
+        const float2 zz = xp[i][2 * k + e];
+        uint32_t q0, q1;
+        grid_codes2(zz, lo, delta, f2mul(f2add(zz, nlo), rv), QMAX, q0, q1);
         word |= (q0 << (16 * e)) | (q1 << (16 * e + 8));
       }
       Pc[i][k] = word;
@@ -398,6 +470,11 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
       const int r = local_row(i);
       rowA[r] = rscale[i] * (delta > 0.f ? delta : 0.f);
       rowB[r] = rscale[i] * lo;
+      if (rec != nullptr) {
+        rec[2 * N * D + r] = rscale[i];
+        rec[2 * N * D + N + r] = lo;
+        rec[2 * N * D + 2 * N + r] = delta;
+      }
     }
   }
 

@@ -20,6 +20,7 @@ struct EncodeParams {
   bool bf16;
   uint32_t* err;
   int32_t k_bits, v_bits, scale_bytes;  // 4, 2, 4 for the k4v2 preset with fp32 scales
+  float* stages;  // optional fp32 stage records of the encoded tiles (null: none)
 };
 
 // Code widths and scale sizes with compiled kernels: (4, 2) with fp32 scales

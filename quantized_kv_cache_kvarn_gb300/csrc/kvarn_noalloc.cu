@@ -10,6 +10,7 @@
 // library holds until the process exits, and allocates nothing.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/kvarn.h"
@@ -21,23 +22,30 @@ constexpr int64_t kDecodeScratchBytes = KVARN_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_lookup;
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device. In host code
 // the array's name is only a host-side stand-in, so the address is asked of
-// the runtime once per device, with that device current.
+// the runtime, with that device current, on the first call that finds none
+// cached. Only a successful lookup is kept: a call that failed (during a
+// stream capture, say) leaves the next call to try again.
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_once[dev], [dev] {
-    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch);
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
-  *out = g_scratch_ptr[dev];
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_lookup);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_decode_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
   return cudaSuccess;
 }
 

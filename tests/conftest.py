@@ -26,3 +26,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Repeat the parity tests' count lines (code flips, stage errors) in the
+    summary, where a run without -s still shows them."""
+    parity = sys.modules.get("tests.parity")
+    lines = getattr(parity, "REPORT", None) if parity else None
+    if lines:
+        terminalreporter.section("parity counts")
+        for line in lines:
+            terminalreporter.write_line(line)

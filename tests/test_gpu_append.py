@@ -1,12 +1,17 @@
-"""kvarn_append (fused append + commit) against kvarn_encode_tiles and the
-raw tokens: sequences grow token by token; every tile a token completes is
-encoded in the same launch, byte for byte as a separate encode would, and
-the partial tile stays raw in the tail."""
+"""kvarn_append (fused append + commit) against kvarn_encode_tiles, the raw
+tokens and the oracle: sequences grow token by token; every tile a token
+completes is encoded in the same launch, byte for byte as a separate encode
+would, the partial tile stays raw in the tail, the pages agree with the
+oracle's encoding of the same tokens, and a decode over the appended cache
+and tail agrees with the oracle's decode."""
+import numpy as np
 import pytest
 import torch
 
 import quantized_kv_cache_kvarn_gb300 as kv
 from quantized_kv_cache_kvarn_gb300 import workloads as W
+from oracle import attention, layout
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -57,3 +62,25 @@ def test_token_by_token_appends_equal_bulk_encode(wname, D, N, dt):
     c = (L // N) * N
     assert torch.equal(tail_k[:, :, :L - c], k[:, :, c:L])
     assert torch.equal(tail_v[:, :, :L - c], v[:, :, c:L])
+
+    # the oracle: its encoding of the same tokens, and its decode over that
+    # cache plus the raw tail, against the GPU decode over the appended state
+    kf, vf = parity.f64(k), parity.f64(v)
+    lens_np = np.full(B, L, dtype=np.int32)
+    st_k, st_v = parity.check_dense_pages(cache.cpu().numpy(), kf, vf, bt.cpu().numpy(), lens_np, N, D)
+    parity.report(f"append {wname}: K codes {st_k['mismatch']}/{st_k['codes']} and V codes "
+                  f"{st_v['mismatch']}/{st_v['codes']} differ from the oracle's float64 chain")
+    ocache = parity.oracle_dense_cache(kf, vf, bt.cpu().numpy(), lens_np, N, D, case.num_pages)
+    sm = W.default_sm_scale(wl)
+    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(D, N), bt.cpu().numpy(), lens_np,
+                                    sm, parity.tails(kf, lens_np, N), parity.tails(vf, lens_np, N))
+    out = torch.empty((B, 2 * Hkv, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, 2 * Hkv), dtype=torch.float32, device=dev)
+    ws = torch.empty(kv.decode_workspace_bytes(lay, B, 2 * Hkv, L), dtype=torch.uint8, device=dev)
+    kv.decode(case.q, lay, cache, bt, lens, L, out, ws, err, sm, tail_k, tail_v, lse=lse)
+    torch.cuda.synchronize()
+    assert kv.read_error_flags(err) == 0
+    diff = np.abs(parity.f64(out) - ref).max()
+    parity.report(f"append {wname}: decode after {steps} appends, max |out - oracle| = {diff:.3e}")
+    assert diff <= parity.OUT_ATOL
+    assert np.abs(parity.f64(lse) - ref_lse).max() <= 1e-4

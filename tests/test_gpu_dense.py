@@ -138,8 +138,8 @@ def test_decode_on_oracle_pages_matches_oracle(name):
 @pytest.mark.parametrize("name", ["toy", "g64_small"])
 def test_end_to_end_close_to_oracle(name):
     """GPU encode then GPU decode against oracle encode then oracle decode. The
-    only difference allowed is the few near-boundary code flips, so the bound
-    is the output tolerance."""
+    only difference between the two caches is the few near-boundary code
+    flips, so the bound is the output tolerance itself."""
     wl, case = _case(name)
     lay, cache = _gpu_encode(wl, case)
     k, v = parity.f64(case.k), parity.f64(case.v)
@@ -161,7 +161,7 @@ def test_end_to_end_close_to_oracle(name):
     torch.cuda.synchronize()
     diff = np.abs(parity.f64(out) - ref).max()
     print(f"\n{name}: end-to-end max |out - oracle| = {diff:.3e}")
-    assert diff <= 5 * parity.OUT_ATOL
+    assert diff <= parity.OUT_ATOL
 
 
 def test_decode_edge_lengths():

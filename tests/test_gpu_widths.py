@@ -14,15 +14,17 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-WIDTHS = [(2, 2, 128), (3, 3, 128), (4, 4, 64), (5, 5, 128), (6, 6, 128), (6, 6, 64), (8, 8, 128), (4, 2, 128)]
-# separate key and value widths (gmlx page, GMLX_KVARN_BITS): every width on
-# each side at least once, both tile sizes
-WIDTHS += [(8, 4, 128), (6, 4, 64), (4, 6, 128), (3, 2, 128), (2, 5, 64), (5, 3, 128), (8, 6, 128), (2, 8, 64),
-           (6, 2, 128)]
-WIDTHS = [w + (128,) for w in WIDTHS]
-# head_dim 256 (warp pairs share a tile; 8-bit parts wider than one gather box)
-WIDTHS += [(2, 2, 64, 256), (3, 3, 128, 256), (4, 2, 128, 256), (4, 4, 64, 256), (5, 5, 128, 256), (6, 6, 128, 256),
-           (6, 6, 64, 256), (8, 8, 128, 256)]
+BITS = (2, 3, 4, 5, 6, 8)
+# every compiled (key width, value width) pair at head_dim 128 (the gmlx
+# page sets the two widths separately, GMLX_KVARN_BITS), the tile size
+# alternating so that each size meets every key and every value width
+WIDTHS = [(kb, vb, 128 if (i + j) % 2 == 0 else 64, 128) for i, kb in enumerate(BITS) for j, vb in enumerate(BITS)]
+# both tile sizes for the equal widths and the preset pair
+WIDTHS += [(b, b, 64 if (i % 2 == 0) else 128, 128) for i, b in enumerate(BITS)] + [(4, 2, 64, 128)]
+# every pair compiled at head_dim 256 (warp pairs share a tile; 8-bit parts
+# wider than one gather box), at both tile sizes
+WIDTHS += [(kb, vb, N, 256) for kb, vb in ((2, 2), (3, 3), (4, 2), (4, 4), (5, 5), (6, 6), (8, 8)) for N in (64, 128)]
+WIDTHS = list(dict.fromkeys(WIDTHS))
 
 
 @pytest.fixture(scope="module", autouse=True)

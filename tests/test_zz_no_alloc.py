@@ -1,7 +1,8 @@
 """kvarn_decode_noalloc, the decode entry point for callers that can not
 allocate device memory (its split-K scratch is a static device array inside
 the library), gives the same output as kvarn_decode with a caller workspace,
-on two calls in a row with different queries. Called through the C ABI.
+on two calls in a row with different queries, and both agree with the
+oracle's decode of the same pages. Called through the C ABI.
 
 This file is named to be collected last."""
 import ctypes
@@ -12,6 +13,7 @@ import torch
 
 import quantized_kv_cache_kvarn_gb300 as kv
 from quantized_kv_cache_kvarn_gb300 import workloads as W
+from oracle import attention, layout
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +62,11 @@ def test_noalloc_matches_workspace_decode_twice(built):
         assert kv.read_error_flags(err) == 0
         assert np.abs(parity.f64(out) - parity.f64(ref)).max() <= parity.OUT_ATOL
         assert np.abs(parity.f64(lse) - parity.f64(ref_lse)).max() <= 1e-4
+        # the oracle's decode of the same (GPU-written) pages and tails
+        oref, olse = attention.decode(parity.f64(q), cache.cpu().numpy(), layout.DenseLayout(128, 128),
+                                      case.block_table.numpy(), lens.numpy(), 0.088, parity.f64(tk), parity.f64(tv))
+        assert np.abs(parity.f64(out) - oref).max() <= parity.OUT_ATOL
+        assert np.abs(parity.f64(lse) - olse).max() <= 1e-4
 
 
 def test_noalloc_rejects_beyond_its_scratch(built):
