@@ -167,29 +167,31 @@ __device__ __forceinline__ float safe_sigma(float var) {
   return (isfinite(s) && s > 0.f) ? s : 1.f;
 }
 
-// Round-to-nearest of normalised values on their row's grid (lo, delta).
-// Two codes at a time: x = (z - lo) * (1/delta) as the caller formed it; the
-// sum x + 1.5 * 2^23 rounds x to an integer, half to even, in the addition
-// itself (the integer is the low bits of the sum), and x minus that integer
-// says how near x lies to a half-way point. The product is within a few
-// units in the last place of the exact quotient (z - lo) / delta of the fp32
-// operands, so only where it lands within 2^-14 of a half-way point is the
-// side taken again, exactly, by grid_boundary_code. The result is the
-// round-half-to-even of the exact quotient, clamped to qmax (which only
-// non-finite input can exceed).
-static __device__ __noinline__ uint32_t grid_boundary_code(float z, float lo, float delta, float x);
+// Round-to-nearest of normalised values on their row's grid (lo, delta),
+// four codes at a time as the bytes of one word (pair k, element e at byte
+// 2k + e). x = (z - lo) * (1/delta) as the caller formed it; the sum
+// x + 1.5 * 2^23 rounds x to an integer, half to even, in the addition
+// itself, and the integer is the sum's low byte (x lies in [0, 2^bits - 1]
+// up to rounding, so no clamp is needed; a non-finite input gives unspecified
+// codes in its own row). x minus that integer says how near x lies to a
+// half-way point. The product is within a few units in the last place of the
+// exact quotient (z - lo) / delta of the fp32 operands, so only where one of
+// the four lands within 2^-14 of a half-way point is the word redone,
+// exactly, out of line. The result is the round-half-to-even of the exact
+// quotient.
+static __device__ __noinline__ uint32_t grid_word_exact(float2 z0, float2 z1, float lo, float delta, float2 x0,
+                                                        float2 x1, uint32_t w);
 
-__device__ __forceinline__ void grid_codes2(float2 z, float lo, float delta, float2 x, uint32_t qmax, uint32_t& q0,
-                                            uint32_t& q1) {
+__device__ __forceinline__ uint32_t grid_codes4(float2 z0, float2 z1, float lo, float delta, float2 x0, float2 x1) {
   constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-  const float2 t = f2add(x, f2(kRound));
-  const float2 d = f2fma(f2add(t, f2(-kRound)), f2(-1.f), x);
-  q0 = __float_as_uint(t.x) - 0x4B400000u;
-  q1 = __float_as_uint(t.y) - 0x4B400000u;
-  if (fabsf(d.x) > 0.5f - 0x1p-14f) q0 = grid_boundary_code(z.x, lo, delta, x.x);
-  if (fabsf(d.y) > 0.5f - 0x1p-14f) q1 = grid_boundary_code(z.y, lo, delta, x.y);
-  q0 = min(q0, qmax);
-  q1 = min(q1, qmax);
+  const float2 t0 = f2add(x0, f2(kRound)), t1 = f2add(x1, f2(kRound));
+  const float2 d0 = f2fma(f2add(t0, f2(-kRound)), f2(-1.f), x0);
+  const float2 d1 = f2fma(f2add(t1, f2(-kRound)), f2(-1.f), x1);
+  uint32_t w = __byte_perm(__byte_perm(__float_as_uint(t0.x), __float_as_uint(t0.y), 0x0040),
+                           __byte_perm(__float_as_uint(t1.x), __float_as_uint(t1.y), 0x0040), 0x5410);
+  const float m = fmaxf(fmaxf(fabsf(d0.x), fabsf(d0.y)), fmaxf(fabsf(d1.x), fabsf(d1.y)));
+  if (m > 0.5f - 0x1p-14f) w = grid_word_exact(z0, z1, lo, delta, x0, x1, w);
+  return w;
 }
 
 // The side of the half-way point k + 1/2 nearest x, decided exactly: z - lo
@@ -198,7 +200,7 @@ __device__ __forceinline__ void grid_codes2(float2 z, float lo, float delta, flo
 // last-place units near the boundary, is formed exactly by the fused
 // multiply-add; the sign of that plus e is the sign of the exact
 // (z - lo) - (k + 1/2) delta. A tie goes to the even code.
-static __device__ __noinline__ uint32_t grid_boundary_code(float z, float lo, float delta, float x) {
+__device__ __forceinline__ uint32_t grid_boundary_code(float z, float lo, float delta, float x) {
   const float s = __fadd_rn(z, -lo);
   const float bb = __fsub_rn(s, z);
   const float e = __fadd_rn(__fsub_rn(z, __fsub_rn(s, bb)), __fsub_rn(-lo, bb));
@@ -206,6 +208,16 @@ static __device__ __noinline__ uint32_t grid_boundary_code(float z, float lo, fl
   const float w = __fadd_rn(__fmaf_rn(-(k + 0.5f), delta, s), e);
   const uint32_t ki = static_cast<uint32_t>(k);
   return ki + ((w > 0.f || (w == 0.f && (ki & 1u))) ? 1u : 0u);
+}
+
+static __device__ __noinline__ uint32_t grid_word_exact(float2 z0, float2 z1, float lo, float delta, float2 x0,
+                                                        float2 x1, uint32_t w) {
+  const float z[4] = {z0.x, z0.y, z1.x, z1.y}, x[4] = {x0.x, x0.y, x1.x, x1.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (fabsf(x[i] - rintf(x[i])) > 0.5f - 0x1p-14f)
+      w = (w & ~(0xFFu << (8 * i))) | ((grid_boundary_code(z[i], lo, delta, x[i]) & 0xFFu) << (8 * i));
+  return w;
 }
 
 // Latent page word order (before the 16-byte unit swizzle): the 32-bit word
@@ -453,18 +465,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     const float2 nlo = f2(-lo), rv = f2(rinv);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        // x - lo lies in [0, hi - lo], so the code lies in [0, QMAX]; the
-        // unsigned conversion saturates and min() only guards non-finite
-        // input
-        const float2 zz = xp[i][2 * k + e];
-        uint32_t q0, q1;
-        grid_codes2(zz, lo, delta, f2mul(f2add(zz, nlo), rv), QMAX, q0, q1);
-        word |= (q0 << (16 * e)) | (q1 << (16 * e + 8));
-      }
-      Pc[i][k] = word;
+      // z - lo lies in [0, hi - lo], so the codes lie in [0, QMAX]
+      const float2 z0 = xp[i][2 * k], z1 = xp[i][2 * k + 1];
+      Pc[i][k] = grid_codes4(z0, z1, lo, delta, f2mul(f2add(z0, nlo), rv), f2mul(f2add(z1, nlo), rv));
     }
     if (seg == 0) {
       const int r = local_row(i);
