@@ -46,6 +46,9 @@ DECODE_CALLS = 200
 # workloads measured beside the main one in a default run (each its own
 # step, decode call and roofline)
 EXTRA_WORKLOADS = ("toy", "g64", "hybrid", "mla")
+# the dense-32B workload through the affine comparison codec (gmlx page: an
+# fp16 scale and offset per group of 64; compared at 4 and 8 bits)
+EXTRA_AFFINE = (4, 8)
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = {"dense": ["kvarn_decode.cu", "kvarn_decode_kernel.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"],
                   "mla": ["kvarn_mla.cu", "kvarn_tcgen05.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"]}
@@ -267,17 +270,27 @@ def oracle_work(wl, case, n, queries=1, qv=None, widths=(4, 2, 4)):
 
 # -------------------------------------------------------------- harnesses
 class DenseHarness:
-    """Dense (GQA) workloads: the cache, the step's commit and the decode."""
+    """Dense (GQA) workloads: the cache, the step's commit and the decode.
+    codec "affine": the same workload through the affine comparison codec
+    (keys and values at widths[0] bits) on the same decode skeleton."""
 
-    def __init__(self, kv, W, wl, dev, rank, widths=(4, 2, 4)):
+    def __init__(self, kv, W, wl, dev, rank, widths=(4, 2, 4), codec="kvarn"):
         import torch
         self.kv, self.wl, self.dev = kv, wl, dev
         self.case = case = W.make_dense(wl, device=dev, seed=rank_seed(wl.seed, rank))
         B, Hkv, D, N = wl.num_seqs, wl.num_kv_heads, wl.head_dim, wl.tile_tokens
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
-        self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters, k_bits=widths[0],
-                                   v_bits=widths[1], fp16_scales=widths[2] == 2)
-        self.cache = kv.alloc_cache(self.lay, dev)
+        if codec == "affine":
+            self.lay = kv.affine_layout(Hkv, case.num_pages, widths[0], self.dt)
+            self.cache = kv.alloc_affine_cache(self.lay, dev)
+            self._enc, self._dec = kv.affine_encode_tiles, kv.affine_decode
+            self._wsb, self._pb = kv.affine_decode_workspace_bytes, kv.affine_page_bytes
+        else:
+            self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters, k_bits=widths[0],
+                                       v_bits=widths[1], fp16_scales=widths[2] == 2)
+            self.cache = kv.alloc_cache(self.lay, dev)
+            self._enc, self._dec = kv.encode_tiles, kv.decode
+            self._wsb, self._pb = kv.decode_workspace_bytes, kv.page_bytes
         self.err = kv.new_error_word(dev)
         lens = case.seq_lens.cpu().tolist()
         self.lens = lens
@@ -289,7 +302,7 @@ class DenseHarness:
         if wl.encode_chunk:
             C = wl.encode_chunk
             start = self.Lmax - C
-            kv.encode_tiles(case.k, case.v, self.lay, torch.zeros(B, dtype=torch.int32, device=dev),
+            self._enc(case.k, case.v, self.lay, torch.zeros(B, dtype=torch.int32, device=dev),
                             case.block_table, self.cache, self.err, chunk_tokens=start)
             ts = torch.full((B,), start // N, dtype=torch.int32, device=dev)
             self.commit.append((case.k[:, :, start:], case.v[:, :, start:], ts, case.block_table, C))
@@ -297,7 +310,7 @@ class DenseHarness:
         elif len(set(lens)) == 1:
             T = lens[0] // N
             if T > 1:
-                kv.encode_tiles(case.k, case.v, self.lay, torch.zeros(B, dtype=torch.int32, device=dev),
+                self._enc(case.k, case.v, self.lay, torch.zeros(B, dtype=torch.int32, device=dev),
                                 case.block_table, self.cache, self.err, chunk_tokens=(T - 1) * N)
             ts = torch.full((B,), T - 1, dtype=torch.int32, device=dev)
             self.commit.append((case.k[:, :, (T - 1) * N:], case.v[:, :, (T - 1) * N:], ts, case.block_table, N))
@@ -311,7 +324,7 @@ class DenseHarness:
             for b, L in enumerate(lens):
                 T = L // N
                 if T > 1:
-                    kv.encode_tiles(case.k[b:b + 1], case.v[b:b + 1], self.lay, zeros1, case.block_table[b:b + 1],
+                    self._enc(case.k[b:b + 1], case.v[b:b + 1], self.lay, zeros1, case.block_table[b:b + 1],
                                     self.cache, self.err, chunk_tokens=(T - 1) * N)
                 ts.append(T - 1 if T else -1)
                 c0 = max(T - 1, 0) * N
@@ -331,10 +344,10 @@ class DenseHarness:
                     self.tail_k[b, :, :L - c] = case.k[b, :, c:L]
                     self.tail_v[b, :, :L - c] = case.v[b, :, c:L]
         self.out = torch.empty((B, wl.num_q_heads, D), dtype=torch.float32, device=dev)
-        self.ws = torch.empty(kv.decode_workspace_bytes(self.lay, B, wl.num_q_heads, self.Lmax),
+        self.ws = torch.empty(self._wsb(self.lay, B, wl.num_q_heads, self.Lmax),
                               dtype=torch.uint8, device=dev)
         self.sm = W.default_sm_scale(wl)
-        pb = kv.page_bytes(self.lay)
+        pb = self._pb(self.lay)
         self.packed = sum(Hkv * ((L // N) * N * pb // 16 + (L % N) * D * 2 * 2) for L in lens)
         self.launches = len(self.commit) + 2
 
@@ -365,11 +378,11 @@ class DenseHarness:
                            self.case.block_table, self.lay, self.cache, self.err)
             return
         for k, v, ts, bt, C in self.commit:
-            self.kv.encode_tiles(k, v, self.lay, ts, bt, self.cache, self.err, chunk_tokens=C)
+            self._enc(k, v, self.lay, ts, bt, self.cache, self.err, chunk_tokens=C)
 
     def decode(self, q=None, lens=None):
         c = self.case
-        self.kv.decode(c.q if q is None else q, self.lay, self.cache, c.block_table,
+        self._dec(c.q if q is None else q, self.lay, self.cache, c.block_table,
                        c.seq_lens if lens is None else lens, self.Lmax, self.out, self.ws, self.err, self.sm,
                        self.tail_k, self.tail_v)
 
@@ -378,14 +391,14 @@ class DenseHarness:
         import torch
         c, N = self.case, self.wl.tile_tokens
         if len(set(self.lens)) == 1:
-            self.kv.encode_tiles(c.k, c.v, self.lay,
+            self._enc(c.k, c.v, self.lay,
                                  torch.zeros(self.wl.num_seqs, dtype=torch.int32, device=self.dev),
                                  c.block_table, self.cache, self.err, chunk_tokens=(self.lens[0] // N) * N)
             return self.wl.num_seqs * (self.lens[0] // N) * N
         zeros1 = torch.zeros(1, dtype=torch.int32, device=self.dev)
         for b, L in enumerate(self.lens):
             if L // N:
-                self.kv.encode_tiles(c.k[b:b + 1], c.v[b:b + 1], self.lay, zeros1, c.block_table[b:b + 1],
+                self._enc(c.k[b:b + 1], c.v[b:b + 1], self.lay, zeros1, c.block_table[b:b + 1],
                                      self.cache, self.err, chunk_tokens=(L // N) * N)
         return sum((L // N) * N for L in self.lens)
 
@@ -627,7 +640,7 @@ def roofline_of(H, wl, dec_ms, traffic=None, kernel=None):
             "traffic": traffic, "kernel": kernel, "peak_kind": peak_kind, "bytes_per_launch": H.packed}
 
 
-def measure_extra(kv, W, name, dev, rank, steps, warmup):
+def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4):
     """One more workload in the same run: its step (commit + decode, K back
     to back), its decode call (DECODE_CALLS back to back) and its commit,
     with the roofline of the decode call. A workload whose packed reads fit
@@ -635,7 +648,10 @@ def measure_extra(kv, W, name, dev, rank, steps, warmup):
     (outside the timed events)."""
     import torch
     wl = W.WORKLOADS[name]
-    H = LatentHarness(kv, W, wl, dev, rank) if wl.rope_dim else DenseHarness(kv, W, wl, dev, rank)
+    if codec == "affine":
+        H = DenseHarness(kv, W, wl, dev, rank, widths=(bits, bits, 2), codec="affine")
+    else:
+        H = LatentHarness(kv, W, wl, dev, rank) if wl.rope_dim else DenseHarness(kv, W, wl, dev, rank)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(warmup):
@@ -695,7 +711,10 @@ def measure_extra(kv, W, name, dev, rank, steps, warmup):
         dec_ms = d0.elapsed_time(d1) / DECODE_CALLS
         com_ms = statistics.mean(x.elapsed_time(y) for x, y in cs)
     assert kv.read_error_flags(H.err) == 0, f"device error in the {name} workload"
-    out = {"workload": _workload_desc(wl), "ms_per_step": round(ms_step, 5),
+    desc = _workload_desc(wl)
+    if codec == "affine":
+        desc = desc.replace("K4V2", f"affine K{bits}V{bits} (groups of 64, fp16 scale and offset)")
+    out = {"workload": desc, "ms_per_step": round(ms_step, 5),
            "value": round(H.packed / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
            "decode_ms": round(dec_ms, 5), "commit_ms": round(com_ms, 5), "commit_tokens": H.encode_tokens,
            "decode_tokens_per_s": round(wl.num_seqs / (ms_step * 1e-3), 1),
@@ -742,6 +761,8 @@ def run_kvarn(args):
         H = VerifyHarness(kv, W, wl, dev, rank, args.queries, args.sink, args.recent)
     elif wl.rope_dim:
         H = LatentHarness(kv, W, wl, dev, rank)
+    elif args.codec == "affine":
+        H = DenseHarness(kv, W, wl, dev, rank, (args.kbits, args.kbits, 2), codec="affine")
     else:
         H = DenseHarness(kv, W, wl, dev, rank, widths)
     if args.append:
@@ -907,14 +928,14 @@ def run_kvarn(args):
         kind = "mla" if wl.rope_dim else "dense"
         # the capture is of the workload's own decode: the preset widths, one
         # query token, no raw records (the append step decodes the same pages)
-        same = widths == (4, 2, 4) and args.queries == 1 and not (args.sink or args.recent)
+        same = widths == (4, 2, 4) and args.queries == 1 and not (args.sink or args.recent) and args.codec == "kvarn"
         if entry and entry.get("source_digest") == decode_source_digest(kind) and not args.num_seqs and same:
             traffic = entry.get("bytes_per_launch")
     except Exception:
         pass
 
     cpu = None
-    if world == 1 and not args.no_cpu and not (args.sink or args.recent):
+    if world == 1 and not args.no_cpu and not (args.sink or args.recent) and args.codec == "kvarn":
         n = max(4, min(16, os.cpu_count() or 4))
         work, frac = oracle_work(wl, H.case, n, args.queries, getattr(H, "qv", None), widths)
         pool, cores = oracle_pool(len(work))
@@ -981,7 +1002,7 @@ def run_kvarn(args):
         "cpu_baseline": cpu,
     }
     plain = not (args.num_seqs or args.queries > 1 or args.sink or args.recent or args.append
-                 or widths != (4, 2, 4) or args.no_extra)
+                 or widths != (4, 2, 4) or args.no_extra or args.codec != "kvarn")
     if plain and world == 1 and args.workload == WORKLOAD:
         # the other workloads of the same family, each measured on its own
         del H, run_e2e, f
@@ -989,6 +1010,9 @@ def run_kvarn(args):
         line["workloads"] = {}
         for name in EXTRA_WORKLOADS:
             line["workloads"][name] = measure_extra(kv, W, name, dev, rank, args.steps, args.warmup)
+        for bits in EXTRA_AFFINE:
+            line["workloads"][f"affine{bits}"] = measure_extra(kv, W, WORKLOAD, dev, rank, args.steps, args.warmup,
+                                                               codec="affine", bits=bits)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -1047,6 +1071,8 @@ def main():
     ap.add_argument("--kbits", type=int, default=4, help="key code width (2, 3, 4, 5, 6, 8)")
     ap.add_argument("--vbits", type=int, default=2, help="value code width (2, 3, 4, 5, 6, 8)")
     ap.add_argument("--fp16-scales", action="store_true", help="fp16 scales in the page (else fp32)")
+    ap.add_argument("--codec", choices=["kvarn", "affine"], default="kvarn",
+                    help="affine: the comparison codec (keys and values at --kbits) on the same skeleton")
     ap.add_argument("--append", action="store_true",
                     help="commit through kvarn_append of the newest token (fused append + commit)")
     ap.add_argument("--sink", type=int, default=0, help="raw sink tokens (a multiple of the tile)")

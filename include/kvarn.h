@@ -479,6 +479,54 @@ int32_t kvarn_decode_noalloc(const void* q, int32_t num_q_heads, float sm_scale,
                              const void* tail_k, const void* tail_v, int32_t num_seqs, float* out,
                              float* lse, uint32_t* error_flags, kvarn_stream_t stream);
 
+/*
+ * The affine comparison codec (gmlx "KV cache quantization" page, "The two
+ * schemes": mlx-lm's affine quantization stores each token's K and V rows as
+ * groups of 64 values with N-bit codes and an fp16 scale and offset per
+ * group; widths 2, 3, 4, 6, 8). Built on this library's paged cache and
+ * decode kernel so that it can be compared with KVarN on the same skeleton,
+ * the codec being the only variable: no rotation, no normalisation.
+ *
+ * Quantisation of a group x[0..63] of one token: offset = fp16(min x), step
+ * = fp16((max x - min x) / (2^bits - 1)) (the quotient formed in double and
+ * rounded once), code = round-half-to-even of the exact quotient
+ * (x - offset) / step of the stored values, clamped to [0, 2^bits - 1]; a
+ * zero step gives code 0. A value is read back as offset + step * code.
+ *
+ * Layout: head_dim 128, tile_tokens 128, page_tokens 16, k_bits = v_bits in
+ * {2, 3, 4, 6, 8}; norm_iters and scale_dtype are ignored. The page of one KV
+ * head (16 tokens):
+ *   K part  K codes in the placement of the dense page's K codes at k_bits
+ *           (above), 2*D*k_bits bytes; then per token t, at 2*D*k_bits +
+ *           8t, its two group scales then its two group offsets, fp16;
+ *           padded to 16 bytes (KP = 2*D*k_bits + 128)
+ *   V part  at KP: V codes in the dense page's V placement at v_bits, then
+ *           the same token records; padded to 16 bytes
+ * (k_bits = 4: 2304 bytes a page, 144 bytes per token and head.)
+ *
+ * kvarn_affine_encode_tiles takes the arguments of kvarn_encode_tiles (the
+ * tiles are whole tiles of the layout, committed as the KVarN tiles are);
+ * kvarn_affine_decode those of kvarn_decode, with the raw tail rows scored
+ * as there, and a workspace of kvarn_affine_decode_workspace_bytes.
+ */
+int64_t kvarn_affine_page_bytes(const kvarn_layout* layout);
+
+int32_t kvarn_affine_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                                  int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                                  const int32_t* block_table, int32_t bt_stride,
+                                  const kvarn_layout* layout, void* cache, uint32_t* error_flags,
+                                  kvarn_stream_t stream);
+
+int64_t kvarn_affine_decode_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t max_seq_len);
+
+int32_t kvarn_affine_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                            const kvarn_layout* layout, const int32_t* block_table, int32_t bt_stride,
+                            const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
+                            const void* tail_v, int32_t num_seqs, float* out, float* lse,
+                            void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
+                            kvarn_stream_t stream);
+
 /* Copy the device error word to *host_out (synchronises `stream`). */
 int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,
                                kvarn_stream_t stream);

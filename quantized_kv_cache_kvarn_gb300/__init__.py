@@ -76,6 +76,11 @@ _SIGS = {
     "kvarn_decode_mla": ([_P, _P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P,
                           _I64, _P, _P], _I32),
     "kvarn_read_error_flags": ([_P, _P, _P], _I32),
+    "kvarn_affine_page_bytes": ([_LP], _I64),
+    "kvarn_affine_encode_tiles": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P, _I32, _LP, _P, _P, _P], _I32),
+    "kvarn_affine_decode_workspace_bytes": ([_LP, _I32, _I32, _I32], _I64),
+    "kvarn_affine_decode": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _I64,
+                             _P, _P], _I32),
     "kvarn_decode_noalloc": ([_P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P, _P],
                              _I32),
 }
@@ -311,3 +316,52 @@ def decode_noalloc(q, layout: Layout, cache, block_table, seq_lens, max_seq_len,
                                       _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
                                       max_seq_len, _ptr(tail_k), _ptr(tail_v), B, _ptr(out), _ptr(lse),
                                       _ptr(err), _stream(stream)), "decode_noalloc")
+
+
+# ------------------------------------------------------------------ affine
+# The affine comparison codec (per-token groups of 64 channels with an fp16
+# scale and offset each, no rotation) on the same paged decode skeleton.
+
+def affine_layout(num_kv_heads, num_pages, bits, kv_dtype=FP16) -> Layout:
+    """head_dim 128, 128-token tiles, keys and values at `bits` (2, 3, 4, 6, 8)."""
+    return Layout(128, 128, 16, num_kv_heads, bits, bits, 1, 0, kv_dtype, 1, num_pages)
+
+
+def affine_page_bytes(layout: Layout) -> int:
+    n = lib().kvarn_affine_page_bytes(ctypes.byref(layout))
+    if n < 0:
+        raise KvarnError("invalid affine layout")
+    return n
+
+
+def alloc_affine_cache(layout: Layout, device=None) -> torch.Tensor:
+    return torch.zeros((layout.num_pages, layout.num_kv_heads, affine_page_bytes(layout)), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def affine_encode_tiles(k, v, layout: Layout, tile_start, block_table, cache, err, chunk_tokens=None,
+                        stream=None):
+    """k, v: [B, Hkv, C, D] (any seq/head strides, contiguous rows)."""
+    B = k.shape[0]
+    C = k.shape[2] if chunk_tokens is None else chunk_tokens
+    assert k.stride() == v.stride() and k.stride(3) == 1 and k.stride(2) == k.shape[3]
+    _check(lib().kvarn_affine_encode_tiles(_ptr(k), _ptr(v), k.stride(0), k.stride(1), B, C, _ptr(tile_start),
+                                           _ptr(block_table), block_table.stride(0), ctypes.byref(layout),
+                                           _ptr(cache), _ptr(err), _stream(stream)), "affine_encode_tiles")
+
+
+def affine_decode_workspace_bytes(layout: Layout, num_seqs: int, num_q_heads: int, max_seq_len: int) -> int:
+    n = lib().kvarn_affine_decode_workspace_bytes(ctypes.byref(layout), num_seqs, num_q_heads, max_seq_len)
+    if n < 0:
+        raise KvarnError("invalid affine decode arguments")
+    return n
+
+
+def affine_decode(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, out, workspace, err,
+                  sm_scale, tail_k=None, tail_v=None, lse=None, stream=None):
+    B, Hq, _ = q.shape
+    _check(lib().kvarn_affine_decode(_ptr(q), Hq, sm_scale, _ptr(cache), ctypes.byref(layout),
+                                     _ptr(block_table), block_table.stride(0), _ptr(seq_lens), max_seq_len,
+                                     _ptr(tail_k), _ptr(tail_v), B, _ptr(out), _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(err),
+                                     _stream(stream)), "affine_decode")

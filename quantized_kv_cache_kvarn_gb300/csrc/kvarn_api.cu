@@ -45,6 +45,18 @@ int32_t check_latent(const kvarn_layout* L) {
 
 bool is_latent(const kvarn_layout* L) { return L && L->head_dim == 512 && L->rope_dim > 0; }
 
+// Layout of the affine comparison codec: head_dim 128, 128-token tiles of
+// 16-token pages, equal key and value widths from {2, 3, 4, 6, 8}.
+int32_t check_affine(const kvarn_layout* L) {
+  if (!L) return KVARN_EINVAL;
+  if (L->page_tokens != kPageTokens || L->head_dim != 128 || L->tile_tokens != 128 || L->rope_dim != 0)
+    return KVARN_EUNSUPPORTED;
+  if (L->k_bits != L->v_bits || !affine_width_compiled(L->k_bits)) return KVARN_EUNSUPPORTED;
+  if (L->kv_dtype != 0 && L->kv_dtype != 1) return KVARN_EUNSUPPORTED;
+  if (L->num_kv_heads < 1 || L->num_pages < 0) return KVARN_EINVAL;
+  return KVARN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -82,8 +94,9 @@ static bool is_preset(const kvarn_layout* L) {
 static int32_t encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
                             int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
                             const int32_t* block_table, int32_t bt_stride, const kvarn_layout* L,
-                            void* cache, float* stages, uint32_t* error_flags, kvarn_stream_t stream) {
-  int32_t s = check_dense(L);
+                            void* cache, float* stages, uint32_t* error_flags, kvarn_stream_t stream,
+                            bool affine = false) {
+  int32_t s = affine ? check_affine(L) : check_dense(L);
   if (s != KVARN_OK) return s;
   if (num_seqs < 0 || chunk_tokens < 0 || chunk_tokens % L->tile_tokens) return KVARN_EINVAL;
   if (num_seqs == 0 || chunk_tokens == 0) return KVARN_OK;
@@ -113,6 +126,7 @@ static int32_t encode_tiles(const void* k, const void* v, int64_t seq_stride, in
   p.v_bits = L->v_bits;
   p.scale_bytes = L->scale_dtype == 1 ? 2 : 4;
   p.stages = stages;
+  if (affine) return from_cuda(launch_encode_affine(p, reinterpret_cast<cudaStream_t>(stream)));
   return from_cuda(launch_encode_dense(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -146,8 +160,12 @@ int32_t kvarn_encode_tiles_staged(const void* k, const void* v, int64_t seq_stri
 // max_seq_len here: the accepted length bound (sizes the tile splits); raw_max:
 // raw (sink + tail) tokens a row may see (sizes the raw splits).
 static DensePlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
-                            int32_t num_queries, int32_t max_seq_len, int32_t raw_max) {
+                            int32_t num_queries, int32_t max_seq_len, int32_t raw_max, bool affine = false) {
   const int32_t G = num_q_heads / L->num_kv_heads;
+  if (affine)
+    return plan_dense_stream(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len / L->tile_tokens,
+                             L->head_dim, L->tile_tokens, raw_max, L->k_bits, L->v_bits, 2,
+                             affine_decode_ctas_per_sm(L->k_bits));
   return plan_dense_stream(num_seqs, L->num_kv_heads * row_groups(G, num_queries), max_seq_len / L->tile_tokens,
                            L->head_dim, L->tile_tokens, raw_max, L->k_bits ? L->k_bits : 4, L->v_bits ? L->v_bits : 2,
                            L->scale_dtype == 1 ? 2 : 4);
@@ -251,8 +269,8 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
                                    int32_t sink_tokens, const void* sink_k, const void* sink_v,
                                    int32_t recent_tokens, int32_t num_seqs, float* out, float* lse,
                                    void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
-                                   kvarn_stream_t stream) {
-  int32_t s = check_dense(L);
+                                   kvarn_stream_t stream, bool affine = false) {
+  int32_t s = affine ? check_affine(L) : check_dense(L);
   if (s != KVARN_OK) return s;
   s = check_decode_common(L, num_q_heads, block_table, bt_stride, seq_lens, max_seq_len, num_seqs,
                           out, workspace, error_flags);
@@ -270,7 +288,7 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   if ((tail_k && !aligned(tail_k, 16)) || (tail_v && !aligned(tail_v, 16))) return KVARN_EALIGN;
   if ((sink_k && !aligned(sink_k, 16)) || (sink_v && !aligned(sink_v, 16))) return KVARN_EALIGN;
   const DensePlan plan = dense_plan(L, num_seqs, num_q_heads, num_queries, accepted,
-                                    raw_bound(L, max_seq_len, num_queries, sink_tokens, recent_tokens));
+                                    raw_bound(L, max_seq_len, num_queries, sink_tokens, recent_tokens), affine);
   if (workspace_bytes < dense_ws(L, num_seqs, num_q_heads, num_queries, plan)) return KVARN_EWORKSPACE;
   DecodeParams p{};
   p.q = q;
@@ -301,7 +319,8 @@ static int32_t decode_dense_common(const void* q, int32_t num_q_heads, int32_t n
   p.recent_tokens = recent_tokens;
   p.k_bits = L->k_bits;
   p.v_bits = L->v_bits;
-  p.scale_bytes = L->scale_dtype == 1 ? 2 : 4;
+  p.scale_bytes = affine ? 2 : (L->scale_dtype == 1 ? 2 : 4);
+  p.codec = affine ? 1 : 0;
   return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -503,6 +522,40 @@ int32_t kvarn_decode_mla(const void* q_latent, const void* q_rope, int32_t num_h
   p.err = error_flags;
   p.bf16 = L->kv_dtype == 1;
   return from_cuda(launch_decode_mla(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t kvarn_affine_page_bytes(const kvarn_layout* L) {
+  if (check_affine(L) != KVARN_OK) return -1;
+  return AffinePage(L->head_dim, L->k_bits, L->v_bits).bytes();
+}
+
+int32_t kvarn_affine_encode_tiles(const void* k, const void* v, int64_t seq_stride, int64_t head_stride,
+                                  int32_t num_seqs, int32_t chunk_tokens, const int32_t* tile_start,
+                                  const int32_t* block_table, int32_t bt_stride, const kvarn_layout* L,
+                                  void* cache, uint32_t* error_flags, kvarn_stream_t stream) {
+  return encode_tiles(k, v, seq_stride, head_stride, num_seqs, chunk_tokens, tile_start, block_table, bt_stride, L,
+                      cache, nullptr, error_flags, stream, true);
+}
+
+int64_t kvarn_affine_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t max_seq_len) {
+  if (check_affine(L) != KVARN_OK || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0 ||
+      num_q_heads % L->num_kv_heads)
+    return -1;
+  const DensePlan plan =
+      dense_plan(L, num_seqs, num_q_heads, 1, max_seq_len, raw_bound(L, max_seq_len, 1, 0, 0), true);
+  return dense_ws(L, num_seqs, num_q_heads, 1, plan);
+}
+
+int32_t kvarn_affine_decode(const void* q, int32_t num_q_heads, float sm_scale, const void* cache,
+                            const kvarn_layout* L, const int32_t* block_table, int32_t bt_stride,
+                            const int32_t* seq_lens, int32_t max_seq_len, const void* tail_k,
+                            const void* tail_v, int32_t num_seqs, float* out, float* lse, void* workspace,
+                            int64_t workspace_bytes, uint32_t* error_flags, kvarn_stream_t stream) {
+  if (!L) return KVARN_EINVAL;
+  return decode_dense_common(q, num_q_heads, 1, sm_scale, cache, L, block_table, bt_stride, seq_lens,
+                             max_seq_len, tail_k, tail_v, L->tile_tokens, 0, nullptr, nullptr, 0, num_seqs,
+                             out, lse, workspace, workspace_bytes, error_flags, stream, true);
 }
 
 int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,

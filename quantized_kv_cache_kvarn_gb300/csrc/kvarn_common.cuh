@@ -65,6 +65,30 @@ __host__ __device__ constexpr bool dense_gather(int D, int N, int KB, int VB, in
          gather_part_ok(DensePage(D, N, KB, VB, SB).v_part(), 2 * D * VB);
 }
 
+// Page of the affine comparison codec (per token, groups of 64 channels with
+// an fp16 scale and offset each, original basis): a K part (K codes in the
+// dense page's K plane placement at KB bits, then per token its G = D / 64
+// scales and G offsets, fp16: 4G bytes at k_sc() + 4G t) and a V part (V
+// codes in the V placement at VB bits, then the same records at v_sc()
+// within the part), each padded to 16 bytes.
+struct AffinePage {
+  int D, KB, VB;
+  __host__ __device__ constexpr AffinePage(int d, int kb, int vb) : D(d), KB(kb), VB(vb) {}
+  __host__ __device__ constexpr int groups() const { return D / 64; }
+  __host__ __device__ constexpr int k_sc() const { return 2 * D * KB; }
+  __host__ __device__ constexpr int k_part() const { return align16(k_sc() + 4 * groups() * kPageTokens); }
+  __host__ __device__ constexpr int v_sc() const { return 2 * D * VB; }  // within the V part
+  __host__ __device__ constexpr int v_part() const { return align16(v_sc() + 4 * groups() * kPageTokens); }
+  __host__ __device__ constexpr int bytes() const { return k_part() + v_part(); }
+};
+
+// Whether pages with these part sizes are staged by TMA gathers (see
+// dense_gather).
+__host__ __device__ constexpr bool parts_gather(int D, int N, int kp, int vp, int KB, int VB) {
+  return (D == 128 || D == 256) && (N / kPageTokens) % 4 == 0 && gather_part_ok(kp, 2 * D * KB) &&
+         gather_part_ok(vp, 2 * D * VB);
+}
+
 // Code planes of a b-bit code (low plane first): 2: [2], 3: [2, 1], 4: [4],
 // 5: [4, 1], 6: [4, 2], 8: [4, 4]; the code is plane0 + 2^w0 plane1.
 __host__ __device__ constexpr int plane_w0(int b) { return b == 2 || b == 3 ? 2 : 4; }

@@ -54,11 +54,12 @@ SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len
 int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
-                            int32_t raw_max, int32_t kb, int32_t vb, int32_t sb) {
+                            int32_t raw_max, int32_t kb, int32_t vb, int32_t sb, int32_t ctas_per_sm) {
   DensePlan p{};
   // tiles a CTA has in flight: one per warp, one per warp pair at head_dim 256
   const int in_flight = D == 256 ? dense_decode_warps(D) / 2 : dense_decode_warps(D);
-  const int64_t resident = static_cast<int64_t>(device_sm_count()) * dense_decode_ctas_per_sm(D, N, kb, vb, sb);
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) *
+                           (ctas_per_sm > 0 ? ctas_per_sm : dense_decode_ctas_per_sm(D, N, kb, vb, sb));
   const int64_t units = static_cast<int64_t>(num_seqs) * units_per_seq;
   const int64_t most = units * std::max(0, max_tiles);
   // four tiles in flight per CTA slot at least, fewer (down to one round)
@@ -162,18 +163,19 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   DecArgs A{};
   {
     const int kb = p.k_bits ? p.k_bits : 4, vb = p.v_bits ? p.v_bits : 2, sb = p.scale_bytes ? p.scale_bytes : 4;
-    if (dense_gather(p.D, p.N, kb, vb, sb)) {
-      const DensePage pg(p.D, p.N, kb, vb, sb);
+    const bool aff = p.codec == 1;
+    const int kpart = aff ? AffinePage(p.D, kb, vb).k_part() : DensePage(p.D, p.N, kb, vb, sb).k_part();
+    const int vpart = aff ? AffinePage(p.D, kb, vb).v_part() : DensePage(p.D, p.N, kb, vb, sb).v_part();
+    if (parts_gather(p.D, p.N, kpart, vpart, kb, vb)) {
+      const int page = kpart + vpart;
       const int64_t rows = static_cast<int64_t>(p.num_pages) * p.num_kv_heads;
       // a part wider than one box is gathered as two (split where its
       // codes' first half ends); the second map is unused otherwise
-      const int ks = gather_split(pg.k_part(), 2 * p.D * kb), vs = gather_split(pg.v_part(), 2 * p.D * vb);
-      cudaError_t e = cache_tensor_map(&A.tmk, p.cache, rows, pg.bytes(), ks);
-      if (e == cudaSuccess) e = cache_tensor_map(&A.tmv, p.cache, rows, pg.bytes(), vs);
-      if (e == cudaSuccess && ks < pg.k_part())
-        e = cache_tensor_map(&A.tmk2, p.cache, rows, pg.bytes(), pg.k_part() - ks);
-      if (e == cudaSuccess && vs < pg.v_part())
-        e = cache_tensor_map(&A.tmv2, p.cache, rows, pg.bytes(), pg.v_part() - vs);
+      const int ks = gather_split(kpart, 2 * p.D * kb), vs = gather_split(vpart, 2 * p.D * vb);
+      cudaError_t e = cache_tensor_map(&A.tmk, p.cache, rows, page, ks);
+      if (e == cudaSuccess) e = cache_tensor_map(&A.tmv, p.cache, rows, page, vs);
+      if (e == cudaSuccess && ks < kpart) e = cache_tensor_map(&A.tmk2, p.cache, rows, page, kpart - ks);
+      if (e == cudaSuccess && vs < vpart) e = cache_tensor_map(&A.tmv2, p.cache, rows, page, vpart - vs);
       if (e != cudaSuccess) return e;
     }
   }
@@ -208,6 +210,18 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   A.err = p.err;
   cudaError_t e = cudaErrorInvalidValue;
   const int kb = p.k_bits ? p.k_bits : 4, vb = p.v_bits ? p.v_bits : 2, sb = p.scale_bytes ? p.scale_bytes : 4;
+  if (p.codec == 1) {
+    if (p.D != 128 || p.N != 128 || kb != vb) return cudaErrorInvalidValue;
+    switch (kb) {
+#define KVARN_AFF_CASE(K) \
+  case K: e = run_affine_widths<K>(A, p.bf16, plan.ctas, st); break;
+      KVARN_AFFINE_WIDTHS(KVARN_AFF_CASE)
+#undef KVARN_AFF_CASE
+      default: break;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_merge<128, false>(A.ws, A.slots, rows, A.counts, 0, A.tile_slots, p.out, p.lse, st);
+  }
   if (kb == 4 && vb == 2 && sb == 4) {
 #define KV_DISPATCH(DD, NN, WW)                                                              \
   if (p.D == DD && p.N == NN)                                                                \

@@ -59,15 +59,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 // channels of Q K and of P V, and the pair adds its partial scores).
 template <int D> constexpr int halves_for() { return D == 256 ? 2 : 1; }
 
-template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4>
+// Codecs of the decode skeleton: the KVarN pages, or the affine comparison
+// codec (per-token groups of 64 channels with an fp16 scale and offset each,
+// original basis).
+constexpr int kCodecKvarn = 0, kCodecAffine = 1;
+
+template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4, int CD = kCodecKvarn>
 struct DecShape {
   static constexpr int HV = halves_for<D>();
   static constexpr int UNITS = W / HV;  // tiles in flight per CTA
   static constexpr DensePage PG{D, N, KB, VB, SB};
+  static constexpr AffinePage AG{D, KB, VB};
+  static constexpr bool AFF = CD == kCodecAffine;
   static constexpr int PPT = N / kPageTokens;
-  static constexpr int PB = PG.bytes();
-  static constexpr int KP = PG.k_part();
-  static constexpr int VP = PG.v_part();
+  static constexpr int PB = AFF ? AG.bytes() : PG.bytes();
+  static constexpr int KP = AFF ? AG.k_part() : PG.k_part();
+  static constexpr int VP = AFF ? AG.v_part() : PG.v_part();
+  static constexpr int GR = D / 64;  // affine groups per token
   static constexpr int KSLOT = PPT * KP;
   static constexpr int VSLOT = PPT * VP;
   static constexpr int WARP_SMEM = KSLOT + VSLOT;
@@ -94,7 +102,8 @@ struct DecShape {
   static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
-  static constexpr bool GATHER = dense_gather(D, N, KB, VB, SB);
+  static constexpr bool GATHER = parts_gather(D, N, KP, VP, KB, VB);
+  static_assert(!AFF || HV == 1, "the affine codec is compiled at head_dim 128");
   // first-box widths of the K and V parts (the whole part unless split)
   static constexpr int KS = GATHER ? gather_split(KP, 2 * D * KB) : KP;
   static constexpr int VS = GATHER ? gather_split(VP, 2 * D * VB) : VP;
@@ -295,8 +304,11 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
 #ifndef KVARN_DECODE_MIN_CTAS_256
 #define KVARN_DECODE_MIN_CTAS_256 4
 #endif
-template <int D, int W> constexpr int decode_min_ctas() {
-  return W == 4 ? KVARN_DECODE_MIN_CTAS : D == 256 ? KVARN_DECODE_MIN_CTAS_256 : 1;
+// The affine codec keeps a score accumulator per channel group and builds
+// its value weights per group: 2 CTAs of 4 warps (up to 255 registers; at 3
+// CTAs it spills).
+template <int D, int W, int CD = 0> constexpr int decode_min_ctas() {
+  return W == 4 ? (CD == 1 ? 2 : KVARN_DECODE_MIN_CTAS) : D == 256 ? KVARN_DECODE_MIN_CTAS_256 : 1;
 }
 
 // ---------------------------------------------------------- work mapping
@@ -406,11 +418,12 @@ __device__ __forceinline__ int cta_of_tile(int64_t t, int C, int64_t total, int 
 // 24), each counted mod 256 (only parities are read). `dead`: a copy timed
 // out earlier; the segment then only writes empty partials. Returns false
 // when a copy timed out (in this segment or before).
-template <int D, int N, typename T, int W, int KB, int VB, int SB>
+template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD>
 __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* smem, int b, int x, int t0, int t1,
                                               int slot, uint32_t& ph,
                                               bool dead) {
-  using S = DecShape<D, N, W, KB, VB, SB>;
+  using S = DecShape<D, N, W, KB, VB, SB, CD>;
+  constexpr bool AFF = S::AFF;
   constexpr DensePage PG = S::PG;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -521,8 +534,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     if (h < R.n) {
       const int hq = kvh * A.G + R.head(A, h), j = R.query(A, h);
       load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, v);
-      warp_fwht<E>(v);
-      const float sc = A.kappa / sqrtf(static_cast<float>(D));
+      if constexpr (!AFF) warp_fwht<E>(v);  // the affine pages are in the original basis
+      const float sc = AFF ? A.kappa : A.kappa / sqrtf(static_cast<float>(D));
 #pragma unroll
       for (int e = 0; e < E; ++e) v[e] *= sc;
     } else {
@@ -559,7 +572,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         break;
       }
     }
-    // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels)
+    // -- q~ = q' * c_K as fp16 hi/lo A fragments (this warp's channels);
+    //    the affine pages take q' as it is
     uint32_t Aq[KCW][4];
     float2 qs2[KCW];
 #pragma unroll
@@ -567,28 +581,48 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const int kc = half * KCW + kcl;
       const int ch0 = 16 * kc + 2 * t;
       const float4 qv = *reinterpret_cast<const float4*>(qrot + q_frag(kc, g, t));
-      const unsigned char* cp = kp(ch0 / S::CPP, PG.k_col() + (ch0 % S::CPP) * SB);
-      const float2 x01 = f2mul(make_float2(qv.x, qv.y), load_scale2<SB>(cp));
-      const float2 x89 = f2mul(make_float2(qv.z, qv.w), load_scale2<SB>(cp + 8 * SB));
+      float2 x01 = make_float2(qv.x, qv.y), x89 = make_float2(qv.z, qv.w);
+      if constexpr (!AFF) {
+        const unsigned char* cp = kp(ch0 / S::CPP, PG.k_col() + (ch0 % S::CPP) * SB);
+        x01 = f2mul(x01, load_scale2<SB>(cp));
+        x89 = f2mul(x89, load_scale2<SB>(cp + 8 * SB));
+      }
       qs2[kcl] = f2add(x01, x89);
       split_hi_lo2(x01, Aq[kcl][0], Aq[kcl][1]);
       split_hi_lo2(x89, Aq[kcl][2], Aq[kcl][3]);
     }
-    const float2 q2 = tree_reduce(qs2, [](float2 a, float2 b) { return f2add(a, b); });
-    const float2 qsum = f2(warp_sum_xor(q2.x + q2.y, 1, 4));
+    float2 qsum = f2(0.f);
+    float qg[S::GR];  // affine: sum of the query over each 64-channel group
+    if constexpr (AFF) {
+#pragma unroll
+      for (int gr = 0; gr < S::GR; ++gr) {
+        float2 a = qs2[4 * gr];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) a = f2add(a, qs2[4 * gr + k]);
+        qg[gr] = warp_sum_xor(a.x + a.y, 1, 4);
+      }
+    } else {
+      const float2 q2 = tree_reduce(qs2, [](float2 a, float2 b) { return f2add(a, b); });
+      qsum = f2(warp_sum_xor(q2.x + q2.y, 1, 4));
+    }
 
     // -- S = q~ . (kappa_K codes)^T, two pages (four 8-token blocks) at a
     //    time so that four independent accumulator chains hide the mma
     //    latency. Per group of four k-chunks a lane's fragments (2 kc + e,
     //    e the token block) are KW consecutive words of each code plane.
     float2 s[S::NB];
+    // the affine scores keep one accumulator per 64-channel group (one group
+    // of four k-chunks), each scaled by its own per-token scale
+    constexpr int DG = AFF ? S::KCH : 1;
 #pragma unroll
     for (int p0 = 0; p0 < S::PPT; p0 += 2) {
-      float d[2][2][4];
+      float d[DG][2][2][4];
 #pragma unroll
-      for (int pi = 0; pi < 2; ++pi)
+      for (int dg = 0; dg < DG; ++dg)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) d[pi][e][0] = d[pi][e][1] = d[pi][e][2] = d[pi][e][3] = 0.f;
+        for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) d[dg][pi][e][0] = d[dg][pi][e][1] = d[dg][pi][e][2] = d[dg][pi][e][3] = 0.f;
 #pragma unroll
       for (int chl = 0; chl < S::KCH / HV; ++chl) {
         const int ch = half * (S::KCH / HV) + chl;
@@ -610,28 +644,56 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
             uint32_t b0, b1;
             code_pair<KB, fg % S::KF0, fg % S::KF1>(x0[pi][fg / S::KF0], x1[pi][(fg / S::KF1) % (S::KW1 ? S::KW1 : 1)],
                                                     b0, b1);
-            mma_f16(d[pi][fg % 2], Aq[kc][0], Aq[kc][1], Aq[kc][2], Aq[kc][3], b0, b1);
+            mma_f16(d[AFF ? chl : 0][pi][fg % 2], Aq[kc][0], Aq[kc][1], Aq[kc][2], Aq[kc][3], b0, b1);
           }
         });
       }
+      if constexpr (AFF) {
+        // s = sum over groups of kappa_K sc_g S_g + (of_g + center sc_g) Q_g,
+        // the records of tokens 8 e + 2 t and + 1 (scales, then offsets)
+        static_assert(S::GR == 2, "two groups per token record");
 #pragma unroll
-      for (int pi = 0; pi < 2; ++pi)
+        for (int pi = 0; pi < 2; ++pi)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          s[2 * (p0 + pi) + e] = f2add(make_float2(d[pi][e][0], d[pi][e][1]), make_float2(d[pi][e][2], d[pi][e][3]));
+          for (int e = 0; e < 2; ++e) {
+            const uint4 rec = *reinterpret_cast<const uint4*>(kp(p0 + pi, S::AG.k_sc() + 8 * (8 * e + 2 * t)));
+            const float2 sa = __half22float2(u32_as_h2(rec.x)), oa = __half22float2(u32_as_h2(rec.y));
+            const float2 sb = __half22float2(u32_as_h2(rec.z)), ob = __half22float2(u32_as_h2(rec.w));
+            float2 v = f2(0.f);
+#pragma unroll
+            for (int gr = 0; gr < 2; ++gr) {
+              const float2 sc = gr ? make_float2(sa.y, sb.y) : make_float2(sa.x, sb.x);
+              const float2 of = gr ? make_float2(oa.y, ob.y) : make_float2(oa.x, ob.x);
+              const float2 Sg = f2add(make_float2(d[gr][pi][e][0], d[gr][pi][e][1]),
+                                      make_float2(d[gr][pi][e][2], d[gr][pi][e][3]));
+              v = f2fma(f2mul(sc, f2(S::KINV)), Sg, v);
+              v = f2fma(f2fma(f2(S::KCENTER), sc, of), f2(qg[gr]), v);
+            }
+            s[2 * (p0 + pi) + e] = v;
+          }
+      } else {
+#pragma unroll
+        for (int pi = 0; pi < 2; ++pi)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            s[2 * (p0 + pi) + e] =
+                f2add(make_float2(d[0][pi][e][0], d[0][pi][e][1]), make_float2(d[0][pi][e][2], d[0][pi][e][3]));
+      }
     }
 
     // -- row-scale fold (linear, so a warp of a pair folds its partial
     //    scores with its own sum of q~ and the pair adds them in a fixed
     //    order, leaving both with the same scores), then the online softmax
     //    in base 2. The K slot is read for the last time here.
+    if constexpr (!AFF) {
 #pragma unroll
-    for (int nb = 0; nb < S::NB; ++nb) {
-      const int idx = (nb & 1) * 8 + 2 * t;
-      const float2 ka = load_scale2<SB>(kp(nb >> 1, PG.k_a() + idx * SB));
-      const float2 kb = load_scale2<SB>(kp(nb >> 1, PG.k_b() + idx * SB));
-      const float2 kb_c = S::KCENTER != 0.f ? f2fma(f2(S::KCENTER), ka, kb) : kb;
-      s[nb] = f2fma(f2mul(ka, f2(S::KINV)), s[nb], f2mul(kb_c, qsum));
+      for (int nb = 0; nb < S::NB; ++nb) {
+        const int idx = (nb & 1) * 8 + 2 * t;
+        const float2 ka = load_scale2<SB>(kp(nb >> 1, PG.k_a() + idx * SB));
+        const float2 kb = load_scale2<SB>(kp(nb >> 1, PG.k_b() + idx * SB));
+        const float2 kb_c = S::KCENTER != 0.f ? f2fma(f2(S::KCENTER), ka, kb) : kb;
+        s[nb] = f2fma(f2mul(ka, f2(S::KINV)), s[nb], f2mul(kb_c, qsum));
+      }
     }
     if constexpr (HV == 2) {
 #pragma unroll
@@ -687,8 +749,11 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     }
 
     // -- P V: weights p * a_V as hi/lo A fragments, one k16 chunk per page
+    //    (affine: p * the group's scale, built per group below)
     uint32_t Ap[S::PPT][4];
     float2 be2[S::PPT];
+    float2 beta = f2(0.f);
+    if constexpr (!AFF) {
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
       const float2 va0 = load_scale2<SB>(vp(pp, PG.v_a() - S::KP + (2 * t) * SB));
@@ -700,8 +765,9 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       split_hi_lo2(f2mul(s[2 * pp], va0), Ap[pp][0], Ap[pp][1]);
       split_hi_lo2(f2mul(s[2 * pp + 1], va1), Ap[pp][2], Ap[pp][3]);
     }
-    const float2 bt2 = tree_reduce(be2, [](float2 a, float2 b) { return f2add(a, b); });
-    const float2 beta = f2(warp_sum_xor(bt2.x + bt2.y, 1, 4));
+      const float2 bt2 = tree_reduce(be2, [](float2 a, float2 b) { return f2add(a, b); });
+      beta = f2(warp_sum_xor(bt2.x + bt2.y, 1, 4));
+    }
 
 #pragma unroll
     for (int nc = 0; nc < NCW; ++nc) acc[nc] = f2mul(acc[nc], f2(alpha));
@@ -710,6 +776,28 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 #pragma unroll
     for (int hql = 0; hql < S::VHC / HV; ++hql) {
       const int hq = half * (S::VHC / HV) + hql;
+      if constexpr (AFF) {
+        // group hq (channels [64 hq, +64)): weights p * sc_hq and the offset
+        // term sum p (of_hq + center sc_hq), records of tokens 2t, 2t + 1
+        // and 8 + 2t, 9 + 2t of each page
+#pragma unroll
+        for (int pp = 0; pp < S::PPT; ++pp) {
+          const uint4 r0 = *reinterpret_cast<const uint4*>(vp(pp, S::AG.v_sc() + 8 * (2 * t)));
+          const uint4 r1 = *reinterpret_cast<const uint4*>(vp(pp, S::AG.v_sc() + 8 * (8 + 2 * t)));
+          auto pick = [&](uint32_t a, uint32_t b2) {
+            const float2 fa = __half22float2(u32_as_h2(a)), fb = __half22float2(u32_as_h2(b2));
+            return hq ? make_float2(fa.y, fb.y) : make_float2(fa.x, fb.x);
+          };
+          const float2 sc0 = pick(r0.x, r0.z), of0 = pick(r0.y, r0.w);
+          const float2 sc1 = pick(r1.x, r1.z), of1 = pick(r1.y, r1.w);
+          be2[pp] = f2fma(s[2 * pp], f2fma(f2(S::VCENTER), sc0, of0),
+                          f2mul(s[2 * pp + 1], f2fma(f2(S::VCENTER), sc1, of1)));
+          split_hi_lo2(f2mul(s[2 * pp], sc0), Ap[pp][0], Ap[pp][1]);
+          split_hi_lo2(f2mul(s[2 * pp + 1], sc1), Ap[pp][2], Ap[pp][3]);
+        }
+        const float2 bt2 = tree_reduce(be2, [](float2 a, float2 b) { return f2add(a, b); });
+        beta = f2(warp_sum_xor(bt2.x + bt2.y, 1, 4));
+      }
       float u[8][4];
 #pragma unroll
       for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
@@ -729,9 +817,13 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       for (int k = 0; k < 8; ++k) {
         const int nc = 8 * hq + k, ncl = 8 * hql + k;
         const int ch = 8 * nc + 2 * t;
-        const float2 cv = load_scale2<SB>(vp(ch / S::CPP, PG.v_col() - S::KP + (ch % S::CPP) * SB));
         const float2 uk = f2add(make_float2(u[k][0], u[k][1]), make_float2(u[k][2], u[k][3]));
-        acc[ncl] = f2fma(cv, f2fma(uk, f2(S::VINV), beta), acc[ncl]);
+        if constexpr (AFF) {
+          acc[ncl] = f2add(f2fma(uk, f2(S::VINV), beta), acc[ncl]);
+        } else {
+          const float2 cv = load_scale2<SB>(vp(ch / S::CPP, PG.v_col() - S::KP + (ch % S::CPP) * SB));
+          acc[ncl] = f2fma(cv, f2fma(uk, f2(S::VINV), beta), acc[ncl]);
+        }
       }
     }
     if constexpr (HV == 2) {  // both warps are done with the V slot
@@ -798,9 +890,9 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   return !any_late;
 }
 
-template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4>
-__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dense_kernel(const __grid_constant__ DecArgs A) {
-  using S = DecShape<D, N, W, KB, VB, SB>;
+template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4, int CD = kCodecKvarn>
+__global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_dense_kernel(const __grid_constant__ DecArgs A) {
+  using S = DecShape<D, N, W, KB, VB, SB, CD>;
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -874,14 +966,14 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W>())) decode_dens
     const int t0 = A.sink_tiles + P.tile;
     const int t1 = t0 + static_cast<int>(seg_end - cur);
     if (threadIdx.x == 0) pos[k ^ 1] = seg_end;
-    dead = !dense_segment<D, N, T, W, KB, VB, SB>(A, smem, P.b, P.x, t0, t1, slot, ph, dead) || dead;
+    dead = !dense_segment<D, N, T, W, KB, VB, SB, CD>(A, smem, P.b, P.x, t0, t1, slot, ph, dead) || dead;
   }
 }
 
-template <int D, int N, typename T, int W, int KB, int VB, int SB>
+template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
 cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
-  using S = DecShape<D, N, W, KB, VB, SB>;
-  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
+  using S = DecShape<D, N, W, KB, VB, SB, CD>;
+  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB, CD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the kernel before it on the stream: the
@@ -901,10 +993,10 @@ cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
 }
 
 // CTAs of one decode kernel resident per SM (registers and shared memory).
-template <int D, int N, typename T, int W, int KB, int VB, int SB>
+template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
 int resident_dense() {
-  using S = DecShape<D, N, W, KB, VB, SB>;
-  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB>;
+  using S = DecShape<D, N, W, KB, VB, SB, CD>;
+  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB, CD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM) != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, S::SMEM) != cudaSuccess || n < 1) return 1;
@@ -915,9 +1007,9 @@ int resident_dense() {
 // 4-warp CTA's page slots would take more than half an SM's shared memory
 // (8-bit codes at 128-token tiles: 137 KB, one CTA of 4 warps per SM; 2-warp
 // CTAs fit three to an SM).
-template <int D, int N, int KB, int VB, int SB>
+template <int D, int N, int KB, int VB, int SB, int CD = kCodecKvarn>
 constexpr int width_warps() {
-  return DecShape<D, N, 4, KB, VB, SB>::SMEM > 116 * 1024 ? 2 : 4;
+  return DecShape<D, N, 4, KB, VB, SB, CD>::SMEM > 116 * 1024 ? 2 : 4;
 }
 
 // The decode kernels of one (K width, V width, scale bytes) combination and
@@ -951,6 +1043,21 @@ int resident_widths256(int N);
   int resident_widths256<KB, VB, 2>(int N);
 KVARN_WIDTH_PAIRS_256(KVARN_DECLARE_WIDTHS_256)
 #undef KVARN_DECLARE_WIDTHS_256
+
+// The affine comparison decode of one code width (keys and values alike,
+// head_dim 128, 128-token tiles), compiled in kvarn_affine_dec.cu.
+#define KVARN_AFFINE_WIDTHS(X) X(2) X(3) X(4) X(6) X(8)
+template <int KB>
+cudaError_t run_affine_widths(const DecArgs& A, bool bf16, int ctas, cudaStream_t st);
+template <int KB>
+int resident_affine();
+#define KVARN_DECLARE_AFFINE(K)                                                                  \
+  template <>                                                                                   \
+  cudaError_t run_affine_widths<K>(const DecArgs& A, bool bf16, int ctas, cudaStream_t st);     \
+  template <>                                                                                   \
+  int resident_affine<K>();
+KVARN_AFFINE_WIDTHS(KVARN_DECLARE_AFFINE)
+#undef KVARN_DECLARE_AFFINE
 
 #define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \
   template <>                                                                                           \

@@ -231,6 +231,38 @@ __device__ __forceinline__ uint32_t k_word_part(const uint32_t (&P)[4], int t, i
   return ((v | (v >> 4)) & 0x00FF00FFu) << (8 * s);
 }
 
+// The plane words of `pages` pages of codes staged as bytes cb [16 pages][D]
+// (one byte per code, token-major), in the dense page's K (IS_V false) or V
+// placement at BITS bits: img[p * D * BITS / 2 + w] is word w of page p's
+// code region. Threads tid, tid + nt, ... build one word each.
+template <int D, int BITS, bool IS_V>
+__device__ __forceinline__ void pack_plane_words(const unsigned char* cb, uint32_t* img, int pages, int tid, int nt) {
+  constexpr int W0 = plane_w0(BITS), W1 = plane_w1(BITS);
+  constexpr int WPP = D * BITS / 2;  // 32-bit words of codes per page
+  for (int ws = tid; ws < pages * WPP; ws += nt) {
+    const int pg = ws / WPP, rem = ws % WPP;
+    const bool p1 = rem >= D * W0 / 2;
+    const int w = p1 ? W1 : W0, shift = p1 ? W0 : 0, wi = p1 ? rem - D * W0 / 2 : rem;
+    const int U = IS_V ? w : min(4, D * w / 64);
+    const int L = (wi % (32 * U)) / U, i = (wi / (32 * U)) * U + wi % U;
+    const int g = L >> 2, t = L & 3, F = 8 / w;
+    uint32_t word = 0;
+    for (int f = 0; f < F; ++f) {
+      const int fg = i * F + f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int ep = 0; ep < 2; ++ep) {
+          const int ch = IS_V ? 8 * fg + g : 16 * (fg >> 1) + 2 * t + ep + 8 * h;
+          const int tok = IS_V ? 2 * t + ep + 8 * h : 8 * (fg & 1) + g;
+          const uint32_t field = (cb[(pg * kPageTokens + tok) * D + ch] >> shift) & ((1u << w) - 1u);
+          word |= field << plane_bit(w, f, h, ep);
+        }
+    }
+    img[ws] = word;
+  }
+}
+
 // Encodes rows [0, N) of `src` as logical tile `tile` of sequence b (u: the
 // tile's index in the chunk, for the latent rope rows). With last_row set,
 // row N - 1 comes from last_row instead of src (the newest token, appended
@@ -507,31 +539,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
     for (int i = 0; i < S::RPT; ++i)
       *reinterpret_cast<uint4*>(cb + local_row(i) * D + seg * 16) = make_uint4(Pc[i][0], Pc[i][1], Pc[i][2], Pc[i][3]);
     __syncthreads();
-    constexpr int W0 = plane_w0(BITS), W1 = plane_w1(BITS);
-    constexpr int WPP = D * BITS / 2;  // 32-bit words of codes per page
-    uint32_t* img = reinterpret_cast<uint32_t*>(stage + S::ROWS * D);
-    for (int ws = tid; ws < S::PPC * WPP; ws += S::NT) {
-      const int pg = ws / WPP, rem = ws % WPP;
-      const bool p1 = rem >= D * W0 / 2;
-      const int w = p1 ? W1 : W0, shift = p1 ? W0 : 0, wi = p1 ? rem - D * W0 / 2 : rem;
-      const int U = IS_V ? w : min(4, D * w / 64);
-      const int L = (wi % (32 * U)) / U, i = (wi / (32 * U)) * U + wi % U;
-      const int g = L >> 2, t = L & 3, F = 8 / w;
-      uint32_t word = 0;
-      for (int f = 0; f < F; ++f) {
-        const int fg = i * F + f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int ep = 0; ep < 2; ++ep) {
-            const int ch = IS_V ? 8 * fg + g : 16 * (fg >> 1) + 2 * t + ep + 8 * h;
-            const int tok = IS_V ? 2 * t + ep + 8 * h : 8 * (fg & 1) + g;
-            const uint32_t field = (cb[(pg * kPageTokens + tok) * D + ch] >> shift) & ((1u << w) - 1u);
-            word |= field << plane_bit(w, f, h, ep);
-          }
-      }
-      img[ws] = word;
-    }
+    pack_plane_words<D, BITS, IS_V>(cb, reinterpret_cast<uint32_t*>(stage + S::ROWS * D), S::PPC, tid, S::NT);
   } else {
     const int j = warp * S::RPW + rsub, g = j & 7;
 #pragma unroll

@@ -105,6 +105,7 @@ struct DecodeParams {
   const void* sink_k;   // dense: [B][Hkv][sink_tokens][D]
   const void* sink_v;
   int32_t k_bits, v_bits, scale_bytes;  // dense code widths and scale size (0: the k4v2 preset, fp32)
+  int32_t codec;        // dense: 0 the KVarN pages, 1 the affine comparison pages
 };
 
 // (query head, query token) row groups of eight per KV head.
@@ -146,7 +147,8 @@ struct DensePlan {
 // units_per_seq: KV heads x row groups; max_tiles: compressed tiles a unit
 // can hold; raw_max: raw tokens a row can see.
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
-                            int32_t raw_max, int32_t kb = 4, int32_t vb = 2, int32_t sb = 4);
+                            int32_t raw_max, int32_t kb = 4, int32_t vb = 2, int32_t sb = 4,
+                            int32_t ctas_per_sm = 0);
 // Partials of `rows` output rows, then one int32 tile-partial count per row.
 int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& plan);
 int dense_decode_warps(int32_t D);
@@ -155,6 +157,15 @@ int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
                               const SplitPlan& plan);
 
 cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st);
+
+// The affine comparison codec (per-token groups of 64 channels, an fp16
+// scale and offset per group; head_dim 128, 128-token tiles, equal key and
+// value widths): whether a width is compiled, the encoder, and the decode
+// kernel's residency (the decode runs through launch_decode_dense with
+// DecodeParams::codec = 1).
+inline bool affine_width_compiled(int32_t b) { return b == 2 || b == 3 || b == 4 || b == 6 || b == 8; }
+cudaError_t launch_encode_affine(const EncodeParams& p, cudaStream_t st);
+int affine_decode_ctas_per_sm(int32_t bits);
 cudaError_t launch_encode_latent(const EncodeLatentParams& p, cudaStream_t st);
 cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cudaStream_t st);
 

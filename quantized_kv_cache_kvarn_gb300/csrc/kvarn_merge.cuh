@@ -65,7 +65,9 @@ __device__ __forceinline__ void accumulate_slots(const float* P, int stride, int
 // rotated ones (slots [0, counts[row]), or [0, rotated_slots) without
 // counts) through the inverse Hadamard transform, plus the raw ones (slots
 // [raw_begin, slots)). The lanes read the slot maxima and sums in parallel.
-template <int D>
+// ROT = false: the tile partials are in the original basis too (the affine
+// comparison codec) and are added without the transform.
+template <int D, bool ROT = true>
 __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws, int slots, int rows,
                                                     const int32_t* __restrict__ counts, int rotated_slots,
                                                     int raw_begin, float* out, float* lse) {
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws
   accumulate_slots<E>(P, kPStride(D), raw_begin, slots, M, tl);
   L = warp_sum_xor(L, 1, 32);
   const float invL = 1.f / L;
-  warp_fwht<E>(rot);
-  const float sc = invL / sqrtf(static_cast<float>(D));
+  if constexpr (ROT) warp_fwht<E>(rot);
+  const float sc = ROT ? invL / sqrtf(static_cast<float>(D)) : invL;
 #pragma unroll
   for (int e = 0; e < E; ++e) o[e] = fmaf(rot[e], sc, tl[e] * invL);
   if (lse && lane == 0) lse[row] = (M + log2f(L)) * kLn2;
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws
 
 // Launches the merge as a programmatic dependent of the kernel before it on
 // the stream.
-template <int D>
+template <int D, bool ROT = true>
 cudaError_t launch_merge(const float* ws, int slots, int rows, const int32_t* counts, int rotated_slots,
                          int raw_begin, float* out, float* lse, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
@@ -118,7 +120,7 @@ cudaError_t launch_merge(const float* ws, int slots, int rows, const int32_t* co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, ws, slots, rows, counts, rotated_slots, raw_begin, out, lse);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, ROT>, ws, slots, rows, counts, rotated_slots, raw_begin, out, lse);
 }
 
 }  // namespace kvarn

@@ -14,12 +14,25 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 CASES = {
-    # name: (workload, overrides, Q)
+    # name: (workload, overrides, Q[, (k_bits, v_bits, scale bytes)]). The
+    # (head, query) rows of a KV head come in row groups of eight (the mma
+    # row tile); the cases cover 1, 2, 3, 4 and 8 row groups, partial ones
+    # included, and code widths other than the preset
     "g8_q4": ("dense32b", dict(num_seqs=2, num_q_heads=16, num_kv_heads=2, context=700), 4),
     "g2_q4_one_row_tile": ("dense32b", dict(num_seqs=2, num_q_heads=4, num_kv_heads=2, context=517), 4),
     "g64_q3_ragged": ("g64", dict(num_seqs=3, num_q_heads=16, num_kv_heads=2, context=640, min_context=1), 3),
     "hybrid_q2_bf16": ("hybrid", dict(num_seqs=2, num_q_heads=12, num_kv_heads=2, context=400), 2),
+    "g8_q2": ("dense32b", dict(num_seqs=3, num_q_heads=16, num_kv_heads=2, context=900), 2),
+    "g8_q8_two_blocks": ("dense32b", dict(num_seqs=2, num_q_heads=8, num_kv_heads=1, context=1000), 8),
+    "g4_q5_idle_group": ("dense32b", dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, context=650), 5),
+    "k6v6_g8_q4": ("dense32b", dict(num_seqs=2, num_q_heads=16, num_kv_heads=2, context=700), 4, (6, 6, 2)),
+    "k8v8_g8_q4_two_warps": ("dense32b", dict(num_seqs=2, num_q_heads=8, num_kv_heads=1, context=600), 4, (8, 8, 2)),
 }
+
+
+def _widths(name):
+    c = CASES[name]
+    return c[3] if len(c) > 3 else (4, 2, 4)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,7 +43,7 @@ def built():
 
 
 def _setup(name, lens_override=None):
-    wname, over, Q = CASES[name]
+    wname, over, Q = CASES[name][:3]
     wl = W.WORKLOADS[wname].with_(**over)
     case = W.make_dense(wl, device="cpu")
     lens = case.seq_lens.numpy().copy() if lens_override is None else np.array(lens_override, np.int32)
@@ -47,7 +60,7 @@ def _setup(name, lens_override=None):
         for b, n in enumerate(per):
             bt[b, :n] = order[off:off + n]
             off += n
-    lay = layout.DenseLayout(D, N)
+    lay = layout.DenseLayout(D, N, *_widths(name))
     cache = np.zeros((num_pages, wl.num_kv_heads, lay.page_bytes), np.uint8)
     cap = N + Q - 2
     tk = np.zeros((wl.num_seqs, wl.num_kv_heads, cap, D))
@@ -62,11 +75,12 @@ def _setup(name, lens_override=None):
     return wl, case, Q, lens, cache, tk, tv, q, bt
 
 
-def _gpu(wl, case, Q, lens, cache, tk, tv, q, bt):
+def _gpu(wl, case, Q, lens, cache, tk, tv, q, bt, widths=(4, 2, 4)):
     dev = "cuda"
     dt = W.TORCH_DTYPE[wl.dtype]
     lay = kv.dense_layout(wl.head_dim, wl.tile_tokens, wl.num_kv_heads, cache.shape[0],
-                          kv.BF16 if wl.dtype == "bf16" else kv.FP16)
+                          kv.BF16 if wl.dtype == "bf16" else kv.FP16, k_bits=widths[0], v_bits=widths[1],
+                          fp16_scales=widths[2] == 2)
     B, Hq, D = wl.num_seqs, wl.num_q_heads, wl.head_dim
     Lmax = int(lens.max())
     out = torch.empty((B, Q, Hq, D), dtype=torch.float32, device=dev)
@@ -88,9 +102,10 @@ def test_verify_matches_oracle(name):
     # the tail goes to the GPU in the storage dtype; the oracle reads the same values
     tk64 = torch.from_numpy(tk).to(dt).double().numpy()
     tv64 = torch.from_numpy(tv).to(dt).double().numpy()
-    ref, rlse = attention.decode_verify(parity.f64(q), cache, layout.DenseLayout(wl.head_dim, wl.tile_tokens),
+    ref, rlse = attention.decode_verify(parity.f64(q), cache,
+                                        layout.DenseLayout(wl.head_dim, wl.tile_tokens, *_widths(name)),
                                         bt, lens, W.default_sm_scale(wl), tk64, tv64)
-    out, lse = _gpu(wl, case, Q, lens, cache, tk, tv, q, bt)
+    out, lse = _gpu(wl, case, Q, lens, cache, tk, tv, q, bt, _widths(name))
     diff = np.abs(out - ref).max()
     print(f"\n{name}: lens {lens.tolist()}, max |out - oracle| = {diff:.3e}, "
           f"max |lse - oracle| = {np.abs(lse - rlse).max():.3e}")
