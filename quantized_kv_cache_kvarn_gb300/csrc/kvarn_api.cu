@@ -171,6 +171,14 @@ static DensePlan dense_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num
                            L->scale_dtype == 1 ? 2 : 4);
 }
 
+// Plan of the decode over uncompressed fp16 pages: 32-token tiles, the last
+// one partial, no raw records.
+static DensePlan fp16_plan(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len) {
+  const int32_t G = num_q_heads / L->num_kv_heads;
+  return plan_dense_stream(num_seqs, L->num_kv_heads * row_groups(G, 1), (max_seq_len + 31) / 32, L->head_dim, 32, 0,
+                           4, 2, 4, raw_decode_ctas_per_sm(L->head_dim));
+}
+
 static int64_t dense_ws(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads, int32_t num_queries,
                         const DensePlan& plan) {
   return dense_stream_workspace_bytes(static_cast<int64_t>(num_seqs) * num_q_heads * num_queries, L->head_dim, plan);
@@ -226,9 +234,11 @@ int64_t kvarn_decode_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, in
   if (is_latent(L)) return mla_workspace_bytes(num_seqs, num_q_heads, plan_mla(num_seqs, max_seq_len));
   if (num_q_heads % L->num_kv_heads) return -1;
   const DensePlan plan = dense_plan(L, num_seqs, num_q_heads, 1, max_seq_len, raw_bound(L, max_seq_len, 1, 0, 0));
-  const SplitPlan plan16 = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
-  return std::max(dense_ws(L, num_seqs, num_q_heads, 1, plan),
-                  dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan16));
+  int64_t ws16 = 0;
+  if (L->head_dim == 128 || L->head_dim == 256)
+    ws16 = dense_stream_workspace_bytes(static_cast<int64_t>(num_seqs) * num_q_heads, L->head_dim,
+                                        fp16_plan(L, num_seqs, num_q_heads, max_seq_len));
+  return std::max(dense_ws(L, num_seqs, num_q_heads, 1, plan), ws16);
 }
 
 int64_t kvarn_decode_window_workspace_bytes(const kvarn_layout* L, int32_t num_seqs, int32_t num_q_heads,
@@ -420,8 +430,8 @@ int32_t kvarn_decode_fp16(const void* q, int32_t num_q_heads, float sm_scale, co
   if (num_q_heads / L->num_kv_heads > 8) return KVARN_EUNSUPPORTED;
   if (bt_stride < (max_seq_len + kPageTokens - 1) / kPageTokens) return KVARN_EINVAL;
   if (!aligned(q, 16) || !aligned(cache, 128)) return KVARN_EALIGN;
-  const SplitPlan plan = plan_dense(num_seqs, L->num_kv_heads, max_seq_len + 31, 32, 2, 3);
-  if (workspace_bytes < dense_workspace_bytes(num_seqs, num_q_heads, L->head_dim, plan))
+  const DensePlan plan = fp16_plan(L, num_seqs, num_q_heads, max_seq_len);
+  if (workspace_bytes < dense_stream_workspace_bytes(static_cast<int64_t>(num_seqs) * num_q_heads, L->head_dim, plan))
     return KVARN_EWORKSPACE;
   DecodeParams p{};
   p.q = q;
@@ -441,10 +451,10 @@ int32_t kvarn_decode_fp16(const void* q, int32_t num_q_heads, float sm_scale, co
   p.lse = lse;
   p.workspace = workspace;
   p.err = error_flags;
-  SplitPlan pl = plan;
-  pl.slots = plan.nsplit;  // no tail slot: partial pages are read directly
-  if (pl.slots == 0) pl.slots = pl.nsplit = 1;
-  return from_cuda(launch_decode_fp16(p, pl, reinterpret_cast<cudaStream_t>(stream)));
+  p.num_queries = 1;
+  p.tail_cap = 32;
+  p.codec = 2;
+  return from_cuda(launch_decode_dense(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int32_t kvarn_encode_latent(const void* latent, int64_t seq_stride, const void* rope,

@@ -19,38 +19,6 @@ int device_sm_count() {
   return n;
 }
 
-SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
-                     int32_t warps, int32_t ctas_per_sm) {
-  SplitPlan p{};
-  const int tiles = max_seq_len / N;
-  const int units = std::max(1, num_seqs * num_kv_heads);
-  if (tiles == 0) {
-    p.tiles_per_split = 1;
-    p.nsplit = 0;
-  } else {
-    // Split count whose CTA count fills whole waves best (resident CTAs per
-    // SM times the SM count), keeping at least 4 tiles per warp; ties go to
-    // fewer splits (fewer partials to merge).
-    const double slots = static_cast<double>(device_sm_count()) * ctas_per_sm;
-    const int max_split = std::max(1, tiles / (4 * warps));
-    int best = 1;
-    double best_eff = 0.0;
-    for (int n = 1; n <= max_split; ++n) {
-      const double waves = units * static_cast<double>(n) / slots;
-      const double eff = waves / std::ceil(waves);
-      if (eff > best_eff + 0.02) {
-        best_eff = eff;
-        best = n;
-      }
-    }
-    p.tiles_per_split = (tiles + best - 1) / best;
-    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  }
-  p.raw_splits = 1;
-  p.slots = p.nsplit + 1;
-  return p;
-}
-
 int dense_decode_warps(int32_t D) { return D == 256 ? 2 : 4; }
 
 DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max_tiles, int32_t D, int32_t N,
@@ -122,11 +90,6 @@ int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32
   return c;
 }
 
-int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
-                              const SplitPlan& plan) {
-  return static_cast<int64_t>(num_seqs) * num_q_heads * plan.slots * kPStride(D) * 4;
-}
-
 // cuTensorMapEncodeTiled of the driver, found once through the runtime.
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   // a function-local static: initialised once, thread-safe
@@ -166,7 +129,7 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
     const bool aff = p.codec == 1;
     const int kpart = aff ? AffinePage(p.D, kb, vb).k_part() : DensePage(p.D, p.N, kb, vb, sb).k_part();
     const int vpart = aff ? AffinePage(p.D, kb, vb).v_part() : DensePage(p.D, p.N, kb, vb, sb).v_part();
-    if (parts_gather(p.D, p.N, kpart, vpart, kb, vb)) {
+    if (p.codec != 2 && parts_gather(p.D, p.N, kpart, vpart, kb, vb)) {
       const int page = kpart + vpart;
       const int64_t rows = static_cast<int64_t>(p.num_pages) * p.num_kv_heads;
       // a part wider than one box is gathered as two (split where its
@@ -208,8 +171,16 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   A.raw_splits = plan.raw_splits;
   A.slots = plan.slots;
   A.err = p.err;
+  A.partial_tiles = p.codec == 2;
   cudaError_t e = cudaErrorInvalidValue;
   const int kb = p.k_bits ? p.k_bits : 4, vb = p.v_bits ? p.v_bits : 2, sb = p.scale_bytes ? p.scale_bytes : 4;
+  if (p.codec == 2) {  // the uncompressed fp16 pages (tiles of 32 tokens)
+    e = p.D == 128 ? run_raw<128>(A, plan.ctas, st) : p.D == 256 ? run_raw<256>(A, plan.ctas, st)
+                                                                  : cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    return p.D == 128 ? launch_merge<128, false>(A.ws, A.slots, rows, A.counts, 0, A.tile_slots, p.out, p.lse, st)
+                      : launch_merge<256, false>(A.ws, A.slots, rows, A.counts, 0, A.tile_slots, p.out, p.lse, st);
+  }
   if (p.codec == 1) {
     if (p.D != 128 || p.N != 128 || kb != vb) return cudaErrorInvalidValue;
     switch (kb) {

@@ -59,10 +59,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // channels of Q K and of P V, and the pair adds its partial scores).
 template <int D> constexpr int halves_for() { return D == 256 ? 2 : 1; }
 
-// Codecs of the decode skeleton: the KVarN pages, or the affine comparison
+// Codecs of the decode skeleton: the KVarN pages, the affine comparison
 // codec (per-token groups of 64 channels with an fp16 scale and offset each,
-// original basis).
-constexpr int kCodecKvarn = 0, kCodecAffine = 1;
+// original basis), or none: the uncompressed fp16 pages (K and V in fragment
+// order, original basis; tiles of 32 tokens, the last one partial).
+constexpr int kCodecKvarn = 0, kCodecAffine = 1, kCodecRaw = 2;
 
 template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4, int CD = kCodecKvarn>
 struct DecShape {
@@ -71,10 +72,12 @@ struct DecShape {
   static constexpr DensePage PG{D, N, KB, VB, SB};
   static constexpr AffinePage AG{D, KB, VB};
   static constexpr bool AFF = CD == kCodecAffine;
+  static constexpr bool RAW = CD == kCodecRaw;
   static constexpr int PPT = N / kPageTokens;
-  static constexpr int PB = AFF ? AG.bytes() : PG.bytes();
-  static constexpr int KP = AFF ? AG.k_part() : PG.k_part();
-  static constexpr int VP = AFF ? AG.v_part() : PG.v_part();
+  static constexpr int RAW_PART = 2 * kPageTokens * D;  // fp16 K (or V) of a page
+  static constexpr int PB = RAW ? 2 * RAW_PART : AFF ? AG.bytes() : PG.bytes();
+  static constexpr int KP = RAW ? RAW_PART : AFF ? AG.k_part() : PG.k_part();
+  static constexpr int VP = RAW ? RAW_PART : AFF ? AG.v_part() : PG.v_part();
   static constexpr int GR = D / 64;  // affine groups per token
   static constexpr int KSLOT = PPT * KP;
   static constexpr int VSLOT = PPT * VP;
@@ -104,6 +107,7 @@ struct DecShape {
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
   static constexpr bool GATHER = parts_gather(D, N, KP, VP, KB, VB);
   static_assert(!AFF || HV == 1, "the affine codec is compiled at head_dim 128");
+  static_assert(!RAW || (N == 32 && !GATHER), "fp16 pages: tiles of two pages, copied by cp.async");
   // first-box widths of the K and V parts (the whole part unless split)
   static constexpr int KS = GATHER ? gather_split(KP, 2 * D * KB) : KP;
   static constexpr int VS = GATHER ? gather_split(VP, 2 * D * VB) : VP;
@@ -141,6 +145,7 @@ struct DecArgs {
   int32_t raw_splits;  // raw slots (chunks of kRawChunk raw tokens)
   int32_t slots;       // tile_slots + raw_splits
   uint32_t* err;
+  int32_t partial_tiles;  // uncompressed pages: a sequence's last tile may be partial (tokens past len masked)
 };
 
 template <typename T, int E>
@@ -334,6 +339,7 @@ __device__ __forceinline__ int checked_len(const DecArgs& A, int b) {
 // the raw sink records come first and the newest `recent` accepted tokens
 // stay raw. Compressed tiles are [sink_tiles, committed / N).
 __device__ __forceinline__ int committed_end(const DecArgs& A, int N, int len) {
+  if (A.partial_tiles) return (len + N - 1) / N * N;  // every token is in the pages
   return max(A.sink_tiles * N, (max(0, visible_len(len, A.Q, 0) - A.recent) / N) * N);
 }
 
@@ -423,7 +429,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
                                               int slot, uint32_t& ph,
                                               bool dead) {
   using S = DecShape<D, N, W, KB, VB, SB, CD>;
-  constexpr bool AFF = S::AFF;
+  constexpr bool AFF = S::AFF, RAW = S::RAW;
+  constexpr bool PLAIN_Q = AFF || RAW;  // original basis, no column scale on the query
   constexpr DensePage PG = S::PG;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -452,8 +459,15 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   // physical page `lane` (lanes < PPT) of this unit's i-th tile; the load is
   // issued a tile ahead and checked only where the copy needs it, so that
   // no instruction waits on it early
-  auto page_load = [&](int i) -> int { return lane < S::PPT ? bt[(first + i * UNITS) * S::PPT + lane] : 0; };
+  // uncompressed pages: the sequence's tokens, the last tile partial
+  const int len_b = RAW ? checked_len(A, b) : 0;
+  auto tile_valid = [&](int i) -> int { return RAW ? len_b - (first + i * UNITS) * N : N; };
+  auto page_load = [&](int i) -> int {
+    if (RAW && lane * kPageTokens >= tile_valid(i)) return -1;  // past the sequence: not loaded
+    return lane < S::PPT ? bt[(first + i * UNITS) * S::PPT + lane] : 0;
+  };
   auto page_check = [&](int phys) -> int {
+    if (RAW && phys == -1) return -1;
     if (phys < 0 || phys >= A.num_pages) {
       set_error(A.err, KVARN_DEVERR_PAGE_RANGE);
       phys = 0;
@@ -504,7 +518,9 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const int tid = half * 32 + lane;
 #pragma unroll
       for (int p = 0; p < S::PPT; ++p) {
-        const unsigned char* src = page_at(__shfl_sync(0xffffffffu, phys, p)) + part_off;
+        const int pid = __shfl_sync(0xffffffffu, phys, p);
+        if (RAW && pid < 0) continue;  // a page past the sequence is not read
+        const unsigned char* src = page_at(pid) + part_off;
         unsigned char* dst = slot + p * part_bytes;
 #pragma unroll
         for (int c = tid; c < part_bytes / 16; c += 32 * HV) cp_async16(dst + 16 * c, src + 16 * c);
@@ -534,8 +550,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     if (h < R.n) {
       const int hq = kvh * A.G + R.head(A, h), j = R.query(A, h);
       load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, v);
-      if constexpr (!AFF) warp_fwht<E>(v);  // the affine pages are in the original basis
-      const float sc = AFF ? A.kappa : A.kappa / sqrtf(static_cast<float>(D));
+      if constexpr (!PLAIN_Q) warp_fwht<E>(v);  // the affine and fp16 pages are in the original basis
+      const float sc = PLAIN_Q ? A.kappa : A.kappa / sqrtf(static_cast<float>(D));
 #pragma unroll
       for (int e = 0; e < E; ++e) v[e] *= sc;
     } else {
@@ -582,7 +598,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       const int ch0 = 16 * kc + 2 * t;
       const float4 qv = *reinterpret_cast<const float4*>(qrot + q_frag(kc, g, t));
       float2 x01 = make_float2(qv.x, qv.y), x89 = make_float2(qv.z, qv.w);
-      if constexpr (!AFF) {
+      if constexpr (!PLAIN_Q) {
         const unsigned char* cp = kp(ch0 / S::CPP, PG.k_col() + (ch0 % S::CPP) * SB);
         x01 = f2mul(x01, load_scale2<SB>(cp));
         x89 = f2mul(x89, load_scale2<SB>(cp + 8 * SB));
@@ -601,10 +617,11 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         for (int k = 1; k < 4; ++k) a = f2add(a, qs2[4 * gr + k]);
         qg[gr] = warp_sum_xor(a.x + a.y, 1, 4);
       }
-    } else {
+    } else if constexpr (!RAW) {
       const float2 q2 = tree_reduce(qs2, [](float2 a, float2 b) { return f2add(a, b); });
       qsum = f2(warp_sum_xor(q2.x + q2.y, 1, 4));
     }
+    const int valid = tile_valid(i);  // tokens of this tile below the length (N but for fp16 pages)
 
     // -- S = q~ . (kappa_K codes)^T, two pages (four 8-token blocks) at a
     //    time so that four independent accumulator chains hide the mma
@@ -614,8 +631,28 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     // the affine scores keep one accumulator per 64-channel group (one group
     // of four k-chunks), each scaled by its own per-token scale
     constexpr int DG = AFF ? S::KCH : 1;
+    if constexpr (RAW) {
+      // the fp16 rows: row 8 e + g of a page, lane chunk t holding channels
+      // 16 kc + {2t, 2t + 1, 2t + 8, 2t + 9} in k-chunk order (8 bytes each)
 #pragma unroll
-    for (int p0 = 0; p0 < S::PPT; p0 += 2) {
+      for (int p = 0; p < S::PPT; ++p) {
+        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const unsigned char* kr = kp(p, (8 * e + g) * 2 * D + t * (D / 2) + 8 * half * KCW);
+#pragma unroll
+          for (int j = 0; j < KCW / 2; ++j) {
+            const uint4 kw = *reinterpret_cast<const uint4*>(kr + 16 * j);
+            mma_f16(d[e], Aq[2 * j][0], Aq[2 * j][1], Aq[2 * j][2], Aq[2 * j][3], kw.x, kw.y);
+            mma_f16(d[e], Aq[2 * j + 1][0], Aq[2 * j + 1][1], Aq[2 * j + 1][2], Aq[2 * j + 1][3], kw.z, kw.w);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) s[2 * p + e] = f2add(make_float2(d[e][0], d[e][1]), make_float2(d[e][2], d[e][3]));
+      }
+    }
+#pragma unroll
+    for (int p0 = 0; p0 < S::PPT && !RAW; p0 += 2) {
       float d[DG][2][2][4];
 #pragma unroll
       for (int dg = 0; dg < DG; ++dg)
@@ -685,7 +722,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     //    scores with its own sum of q~ and the pair adds them in a fixed
     //    order, leaving both with the same scores), then the online softmax
     //    in base 2. The K slot is read for the last time here.
-    if constexpr (!AFF) {
+    if constexpr (!PLAIN_Q) {
 #pragma unroll
       for (int nb = 0; nb < S::NB; ++nb) {
         const int idx = (nb & 1) * 8 + 2 * t;
@@ -713,6 +750,13 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       if (late) {
         timed_out = true;
         break;
+      }
+    }
+    if constexpr (RAW) {  // tokens past the length (a partial last tile) take no weight
+#pragma unroll
+      for (int nb = 0; nb < S::NB; ++nb) {
+        const int tok = 8 * nb + 2 * t;
+        s[nb] = make_float2(tok < valid ? s[nb].x : -INFINITY, tok + 1 < valid ? s[nb].y : -INFINITY);
       }
     }
     float mts[S::NB];
@@ -753,7 +797,13 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     uint32_t Ap[S::PPT][4];
     float2 be2[S::PPT];
     float2 beta = f2(0.f);
-    if constexpr (!AFF) {
+    if constexpr (RAW) {
+#pragma unroll
+      for (int pp = 0; pp < S::PPT; ++pp) {
+        split_hi_lo2(s[2 * pp], Ap[pp][0], Ap[pp][1]);
+        split_hi_lo2(s[2 * pp + 1], Ap[pp][2], Ap[pp][3]);
+      }
+    } else if constexpr (!AFF) {
 #pragma unroll
     for (int pp = 0; pp < S::PPT; ++pp) {
       const float2 va0 = load_scale2<SB>(vp(pp, PG.v_a() - S::KP + (2 * t) * SB));
@@ -801,8 +851,27 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       float u[8][4];
 #pragma unroll
       for (int k = 0; k < 8; ++k) u[k][0] = u[k][1] = u[k][2] = u[k][3] = 0.f;
+      if constexpr (RAW) {
+        // lane chunk 4 g + t of a page's V rows: per 8-channel block nc,
+        // channel 8 nc + g at tokens (2t, 2t + 1) then (2t + 8, 2t + 9);
+        // rows past the length may hold any bits and are cleared, so that
+        // their zero weight never meets an inf or nan
 #pragma unroll
-      for (int pp = 0; pp < S::PPT; ++pp) {
+        for (int pp = 0; pp < S::PPT; ++pp) {
+          const int tb = pp * kPageTokens + 2 * t;
+          const uint32_t m01 = (tb < valid ? 0x0000FFFFu : 0u) | (tb + 1 < valid ? 0xFFFF0000u : 0u);
+          const uint32_t m89 = (tb + 8 < valid ? 0x0000FFFFu : 0u) | (tb + 9 < valid ? 0xFFFF0000u : 0u);
+          const unsigned char* vr = vp(pp, (4 * g + t) * D + 64 * hq);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 vw = *reinterpret_cast<const uint4*>(vr + 16 * j);
+            mma_f16(u[2 * j], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], vw.x & m01, vw.y & m89);
+            mma_f16(u[2 * j + 1], Ap[pp][0], Ap[pp][1], Ap[pp][2], Ap[pp][3], vw.z & m01, vw.w & m89);
+          }
+        }
+      }
+#pragma unroll
+      for (int pp = 0; pp < S::PPT && !RAW; ++pp) {
         uint32_t x0[S::VW0], x1[S::VW1 ? S::VW1 : 1];
         load_words<S::VW0>(vp(pp, 4 * S::VW0 * (32 * hq + lane)), x0);
         if constexpr (S::VW1 != 0) load_words<S::VW1>(vp(pp, S::VR1 + 4 * S::VW1 * (32 * hq + lane)), x1);
@@ -818,7 +887,9 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
         const int nc = 8 * hq + k, ncl = 8 * hql + k;
         const int ch = 8 * nc + 2 * t;
         const float2 uk = f2add(make_float2(u[k][0], u[k][1]), make_float2(u[k][2], u[k][3]));
-        if constexpr (AFF) {
+        if constexpr (RAW) {
+          acc[ncl] = f2add(uk, acc[ncl]);
+        } else if constexpr (AFF) {
           acc[ncl] = f2add(f2fma(uk, f2(S::VINV), beta), acc[ncl]);
         } else {
           const float2 cv = load_scale2<SB>(vp(ch / S::CPP, PG.v_col() - S::KP + (ch % S::CPP) * SB));
@@ -1043,6 +1114,14 @@ int resident_widths256(int N);
   int resident_widths256<KB, VB, 2>(int N);
 KVARN_WIDTH_PAIRS_256(KVARN_DECLARE_WIDTHS_256)
 #undef KVARN_DECLARE_WIDTHS_256
+
+// The decode over uncompressed fp16 pages (the same kernel with no codec;
+// 32-token tiles, 4 warps at head_dim 128, warp pairs at 256), compiled in
+// kvarn_fp16.cu.
+template <int D>
+cudaError_t run_raw(const DecArgs& A, int ctas, cudaStream_t st);
+template <int D>
+int resident_raw();
 
 // The affine comparison decode of one code width (keys and values alike,
 // head_dim 128, 128-token tiles), compiled in kvarn_affine_dec.cu.

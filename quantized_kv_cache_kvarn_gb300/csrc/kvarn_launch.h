@@ -129,9 +129,6 @@ inline SplitPlan with_raw_chunks(SplitPlan p, int32_t raw_max) {
   return p;
 }
 
-SplitPlan plan_dense(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t N,
-                     int32_t warps, int32_t ctas_per_sm);
-
 // Plan of the compressed decode: `ctas` persistent CTAs share the flattened
 // list of compressed tiles (stream-K), each taking at least `min_tiles` of
 // them, so a unit of n tiles writes at most 1 + ceil((n - 1) / min_tiles)
@@ -153,9 +150,6 @@ DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max
 int64_t dense_stream_workspace_bytes(int64_t rows, int32_t D, const DensePlan& plan);
 int dense_decode_warps(int32_t D);
 int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb = 4, int32_t vb = 2, int32_t sb = 4);
-int64_t dense_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t D,
-                              const SplitPlan& plan);
-
 cudaError_t launch_encode_dense(const EncodeParams& p, cudaStream_t st);
 
 // The affine comparison codec (per-token groups of 64 channels, an fp16
@@ -182,7 +176,9 @@ struct StoreFp16Params {
   uint32_t* err;
 };
 cudaError_t launch_store_fp16(const StoreFp16Params& p, cudaStream_t st);
-cudaError_t launch_decode_fp16(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
+// Resident CTAs per SM of the decode over uncompressed fp16 pages (the dense
+// decode kernel with no codec: DecodeParams::codec = 2, N = 32).
+int raw_decode_ctas_per_sm(int32_t D);
 
 SplitPlan plan_mla(int32_t num_seqs, int32_t max_seq_len);
 int64_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const SplitPlan& plan);

@@ -252,32 +252,44 @@ def test_device_errors_are_flagged_not_faulted():
     assert flags & kv.DEVERR_PAGE_RANGE and flags & kv.DEVERR_NO_TAIL
 
 
-def test_fp16_bypass_matches_plain_attention():
-    """The uncompressed path on the same skeleton equals plain attention over
-    the raw tokens (ragged last page included)."""
-    wl = W.WORKLOADS["dense32b"].with_(num_seqs=3, num_q_heads=16, num_kv_heads=2, context=700)
+@pytest.mark.parametrize("D", [128, 256])
+def test_fp16_bypass_matches_plain_attention(D):
+    """The uncompressed path on the same skeleton (the decode kernel with no
+    codec, 32-token tiles) equals plain attention over the raw tokens: ragged
+    last pages and tiles, a one-page sequence, an empty one; the rows past a
+    length in its last page hold NaN and must take no weight."""
+    B = 4
+    wl = W.WORKLOADS["dense32b"].with_(num_seqs=B, num_q_heads=16, num_kv_heads=2, context=700, head_dim=D)
     case = W.make_dense(wl, device="cpu")
-    lens = np.array([700, 333, 16], dtype=np.int32)
+    lens = np.array([700, 333, 16, 0], dtype=np.int32)
     dev = "cuda"
-    num_pages = 3 * ((700 + 15) // 16)
-    bt = torch.arange(num_pages, dtype=torch.int32).flip(0).reshape(3, -1).contiguous()
-    lay = kv.dense_layout(128, 128, 2, num_pages)
+    num_pages = B * ((700 + 15) // 16)
+    bt = torch.arange(num_pages, dtype=torch.int32).flip(0).reshape(B, -1).contiguous()
+    lay = kv.dense_layout(D, 128, 2, num_pages)
     cache = kv.alloc_fp16_cache(lay, dev)
     err = kv.new_error_word(dev)
-    kpad = torch.zeros((3, 2, 704, 128), dtype=torch.float16)
-    vpad = torch.zeros_like(kpad)
-    kpad[:, :, :700] = case.k
-    vpad[:, :, :700] = case.v
+    kpad = torch.full((B, 2, 704, D), float("nan"), dtype=torch.float16)
+    vpad = torch.full_like(kpad, float("nan"))
+    for b in range(B):
+        kpad[b, :, :lens[b]] = case.k[b, :, :lens[b]]
+        vpad[b, :, :lens[b]] = case.v[b, :, :lens[b]]
     kv.store_fp16(kpad.to(dev), vpad.to(dev), lay, 0, 704, bt.to(dev), cache, err)
-    out = torch.empty((3, 16, 128), dtype=torch.float32, device=dev)
-    ws = torch.empty(kv.decode_workspace_bytes(lay, 3, 16, 700), dtype=torch.uint8, device=dev)
-    kv.decode_fp16(case.q.to(dev), lay, cache, bt.to(dev), torch.from_numpy(lens).to(dev), 700, out, ws, err,
-                   0.0883883)
+    out = torch.empty((B, 16, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, 16), dtype=torch.float32, device=dev)
+    ws = torch.empty(kv.decode_workspace_bytes(lay, B, 16, 700), dtype=torch.uint8, device=dev)
+    sm = 1 / np.sqrt(D)
+    kv.decode_fp16(case.q.to(dev), lay, cache, bt.to(dev), torch.from_numpy(lens).to(dev), 700, out, ws, err, sm,
+                   lse=lse)
     torch.cuda.synchronize()
     assert kv.read_error_flags(err) == 0
-    o = parity.f64(out)
+    o, l = parity.f64(out), parity.f64(lse)
+    assert (o[3] == 0).all() and np.isneginf(l[3]).all()
+    worst = 0.0
     for b in range(3):
         for h in range(16):
-            ref, _ = attention.softmax_attention(parity.f64(case.q[b, h]), parity.f64(case.k[b, h // 8, :lens[b]]),
-                                                 parity.f64(case.v[b, h // 8, :lens[b]]), 0.0883883)
-            assert np.abs(o[b, h] - ref).max() <= parity.OUT_ATOL
+            ref, rl = attention.softmax_attention(parity.f64(case.q[b, h]), parity.f64(case.k[b, h // 8, :lens[b]]),
+                                                  parity.f64(case.v[b, h // 8, :lens[b]]), sm)
+            worst = max(worst, float(np.abs(o[b, h] - ref).max()))
+            assert abs(l[b, h] - rl) <= 1e-4
+    parity.report(f"fp16 pages D{D}: max |out - plain attention| = {worst:.3e}")
+    assert worst <= parity.OUT_ATOL
