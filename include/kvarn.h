@@ -135,7 +135,7 @@ typedef enum {
 /* Bits of the device error word. */
 #define KVARN_DEVERR_PAGE_RANGE 0x1u  /* block-table entry outside [0, num_pages) */
 #define KVARN_DEVERR_NO_TAIL    0x2u  /* a raw record (tail or sink) is needed but its buffer is NULL */
-#define KVARN_DEVERR_TIMEOUT    0x4u  /* a bulk copy did not complete in time */
+#define KVARN_DEVERR_TIMEOUT    0x4u  /* a page copy did not complete in time (see kvarn_set_copy_wait_test) */
 #define KVARN_DEVERR_SEQ_LEN    0x8u  /* seq_len < 0 or above max_seq_len */
 
 typedef struct {
@@ -526,6 +526,27 @@ int32_t kvarn_affine_decode(const void* q, int32_t num_q_heads, float sm_scale, 
                             const void* tail_v, int32_t num_seqs, float* out, float* lse,
                             void* workspace, int64_t workspace_bytes, uint32_t* error_flags,
                             kvarn_stream_t stream);
+
+/*
+ * kvarn_set_copy_wait_test - diagnostic of the dense decode kernels'
+ * (kvarn_decode, _verify, _window, _fp16, _noalloc, kvarn_affine_decode)
+ * bounded waits for their page copies, so that a test can drive the time-out
+ * path without making a copy fail. `cycles`: how long a wait lasts before the
+ * kernel gives up (0 restores the default, 2e9 cycles, about a second; a limit
+ * below 1e5 cycles is kept by polling instead of the suspending wait).
+ * `withhold` = 1: every copy is announced 16 bytes larger than it is (or, for
+ * copies by the threads themselves, one thread's arrival is withheld), so
+ * that no copy's phase ever completes and every wait runs out, while the
+ * copies themselves land as usual. On giving up, a kernel sets
+ * KVARN_DEVERR_TIMEOUT in the call's error word, waits a bounded time (about
+ * 50 ms) for the copies it started, writes empty partials for the rest of its
+ * work and returns: the context stays usable; the call's outputs are
+ * unspecified. Process-wide; read when a call launches (a captured CUDA graph
+ * keeps the values of its capture). KVARN_EINVAL for a negative count or a
+ * withhold other than 0 and 1. The pages describing the method have no
+ * counterpart of this call.
+ */
+int32_t kvarn_set_copy_wait_test(int64_t cycles, int32_t withhold);
 
 /* Copy the device error word to *host_out (synchronises `stream`). */
 int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,

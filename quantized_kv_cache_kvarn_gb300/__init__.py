@@ -76,6 +76,7 @@ _SIGS = {
     "kvarn_decode_mla": ([_P, _P, _I32, _F32, _P, _LP, _P, _I32, _P, _I32, _P, _P, _I32, _P, _P, _P,
                           _I64, _P, _P], _I32),
     "kvarn_read_error_flags": ([_P, _P, _P], _I32),
+    "kvarn_set_copy_wait_test": ([_I64, _I32], _I32),
     "kvarn_affine_page_bytes": ([_LP], _I64),
     "kvarn_affine_encode_tiles": ([_P, _P, _I64, _I64, _I32, _I32, _P, _P, _I32, _LP, _P, _P, _P], _I32),
     "kvarn_affine_decode_workspace_bytes": ([_LP, _I32, _I32, _I32], _I64),
@@ -365,3 +366,10 @@ def affine_decode(q, layout: Layout, cache, block_table, seq_lens, max_seq_len, 
                                      _ptr(tail_k), _ptr(tail_v), B, _ptr(out), _ptr(lse), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _ptr(err),
                                      _stream(stream)), "affine_decode")
+
+
+def set_copy_wait_test(cycles: int, withhold: bool = False) -> None:
+    """Diagnostic: clock cycles the dense decode kernels wait for a page copy
+    before they flag DEVERR_TIMEOUT and return (0: the default), and whether
+    every copy is announced larger than it is so that every wait runs out."""
+    _check(lib().kvarn_set_copy_wait_test(cycles, 1 if withhold else 0), "set_copy_wait_test")

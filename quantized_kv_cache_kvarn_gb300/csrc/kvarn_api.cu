@@ -568,6 +568,12 @@ int32_t kvarn_affine_decode(const void* q, int32_t num_q_heads, float sm_scale, 
                              out, lse, workspace, workspace_bytes, error_flags, stream, true);
 }
 
+int32_t kvarn_set_copy_wait_test(int64_t cycles, int32_t withhold) {
+  if (cycles < 0 || (withhold != 0 && withhold != 1)) return KVARN_EINVAL;
+  set_copy_wait_test(cycles, withhold ? 16 : 0);
+  return KVARN_OK;
+}
+
 int32_t kvarn_read_error_flags(const uint32_t* error_flags, uint32_t* host_out,
                                kvarn_stream_t stream) {
   if (!error_flags || !host_out) return KVARN_EINVAL;

@@ -218,8 +218,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // Bounded wait: gives up after about `limit_cycles` SM clocks and returns
 // false, so that a copy that never lands can not hang the GPU.
+__device__ __forceinline__ bool mbar_test_phase(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits at most about limit_cycles for the phase. try_wait may suspend the
+// thread until the phase completes, so a limit below kPollWaitBelow (a
+// diagnostic setting) is kept by polling with the non-blocking test_wait.
+constexpr long long kPollWaitBelow = 100000;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   long long limit_cycles = 2000000000LL) {
+  if (limit_cycles < kPollWaitBelow) {
+    const long long t0 = clock64();
+    while (!mbar_test_phase(bar, parity))
+      if (clock64() - t0 > limit_cycles) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {

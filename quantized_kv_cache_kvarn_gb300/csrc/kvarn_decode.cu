@@ -10,6 +10,18 @@
 
 namespace kvarn {
 
+// Clock cycles the dense decode kernels wait for a page copy before they
+// give up (flag KVARN_DEVERR_TIMEOUT and return); 0: the default, about a
+// second. Read when a call launches.
+static std::atomic<long long> g_copy_wait_limit{0};
+static std::atomic<int> g_copy_withhold{0};
+constexpr long long kDefaultCopyWait = 2000000000LL;
+
+void set_copy_wait_test(long long cycles, int withhold) {
+  g_copy_wait_limit.store(cycles, std::memory_order_relaxed);
+  g_copy_withhold.store(withhold, std::memory_order_relaxed);
+}
+
 // ------------------------------------------------------------- planning
 int device_sm_count() {
   int dev = 0, n = 0;
@@ -172,6 +184,11 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   A.slots = plan.slots;
   A.err = p.err;
   A.partial_tiles = p.codec == 2;
+  {
+    const long long w = g_copy_wait_limit.load(std::memory_order_relaxed);
+    A.wait_limit = w > 0 ? w : kDefaultCopyWait;
+    A.withhold = g_copy_withhold.load(std::memory_order_relaxed);
+  }
   cudaError_t e = cudaErrorInvalidValue;
   const int kb = p.k_bits ? p.k_bits : 4, vb = p.v_bits ? p.v_bits : 2, sb = p.scale_bytes ? p.scale_bytes : 4;
   if (p.codec == 2) {  // the uncompressed fp16 pages (tiles of 32 tokens)

@@ -146,6 +146,8 @@ struct DecArgs {
   int32_t slots;       // tile_slots + raw_splits
   uint32_t* err;
   int32_t partial_tiles;  // uncompressed pages: a sequence's last tile may be partial (tokens past len masked)
+  long long wait_limit;   // clock cycles a page copy is waited for before the kernel gives up
+  int32_t withhold;       // diagnostic: every copy is announced this many bytes larger (its phase never completes)
 };
 
 template <typename T, int E>
@@ -503,7 +505,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       for (int p = 0; p < S::PPT; ++p) row[p] = __shfl_sync(0xffffffffu, phys, p) * A.Hkv + kvh;
       __syncwarp();
       if (leader && lane == 0) {
-        mbar_arrive_expect_tx(bar, S::PPT * part_bytes);
+        mbar_arrive_expect_tx(bar, S::PPT * part_bytes + A.withhold);
 #pragma unroll
         for (int q4 = 0; q4 < S::PPT / 4; ++q4) {
           unsigned char* dst = slot + 4 * q4 * part_bytes;
@@ -525,7 +527,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
 #pragma unroll
         for (int c = tid; c < part_bytes / 16; c += 32 * HV) cp_async16(dst + 16 * c, src + 16 * c);
       }
-      cp_async_arrive(bar);
+      if (A.withhold == 0 || tid != 0) cp_async_arrive(bar);  // a withheld arrival: the phase never completes
     }
   };
   auto issue_k = [&](int phys) {
@@ -580,7 +582,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     int phys_next = i + 1 < n_my ? page_load(i + 1) : 0;
     // a warp of a pair that gives up on a copy tells its partner at the next
     // pair barrier and both leave together
-    bool late = !mbar_wait_bounded(barK, ph & 1);
+    bool late = !mbar_wait_bounded(barK, ph & 1, A.wait_limit);
     ph += 1u;
     if constexpr (HV == 1) {
       if (late) {
@@ -783,7 +785,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
       issue_k(phys_next);
     }
 
-    late = !mbar_wait_bounded(barV, (ph >> 8) & 1);
+    late = !mbar_wait_bounded(barV, (ph >> 8) & 1, A.wait_limit);
     ph += 1u << 8;
     if constexpr (HV == 1) {
       if (late) {

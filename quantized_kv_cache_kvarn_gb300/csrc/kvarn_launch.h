@@ -185,5 +185,9 @@ int64_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const SplitPlan
 cudaError_t launch_decode_mla(const DecodeParams& p, const SplitPlan& plan, cudaStream_t st);
 
 int device_sm_count();
+// Diagnostic: clock cycles the dense decode kernels wait for a page copy (0:
+// default) and whether each copy is announced larger than it is (so that its
+// phase never completes and every wait runs out).
+void set_copy_wait_test(long long cycles, int withhold);
 
 }  // namespace kvarn

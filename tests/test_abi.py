@@ -123,3 +123,9 @@ def test_workspace_bytes(L):
 def test_status_strings(L):
     for code in (0, -1, -2, -3, -4, -5):
         assert L.kvarn_status_string(code)
+
+
+def test_copy_wait_test_rejects_bad_arguments(L):
+    assert L.kvarn_set_copy_wait_test(-5, 0) == -1
+    assert L.kvarn_set_copy_wait_test(0, 2) == -1
+    assert L.kvarn_set_copy_wait_test(0, 0) == 0
