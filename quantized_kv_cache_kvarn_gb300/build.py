@@ -67,6 +67,12 @@ def build(verbose: bool = False, force: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    # every build compiles all sources, so the objects are not kept
+    for o in objs:
+        try:
+            os.remove(o)
+        except OSError:
+            pass
     return LIB
 
 

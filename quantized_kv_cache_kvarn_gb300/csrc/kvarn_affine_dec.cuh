@@ -9,14 +9,13 @@
 #define KVARN_AFFINE_DECODE(K)                                                                              \
   namespace kvarn {                                                                                         \
   template <>                                                                                               \
-  cudaError_t run_affine_widths<K>(const DecArgs& A, bool bf16, int ctas, cudaStream_t st) {                \
+  cudaError_t run_affine_widths<K>(const DecArgs& A, bool /*bf16*/, int ctas, cudaStream_t st) {           \
     constexpr int W = width_warps<128, 128, K, K, 2, kCodecAffine>();                                       \
-    return bf16 ? run_dense<128, 128, __nv_bfloat16, W, K, K, 2, kCodecAffine>(A, ctas, st)                 \
-                : run_dense<128, 128, __half, W, K, K, 2, kCodecAffine>(A, ctas, st);                       \
+    return run_dense<128, 128, W, K, K, 2, kCodecAffine>(A, ctas, st);                       \
   }                                                                                                         \
   template <>                                                                                               \
   int resident_affine<K>() {                                                                                \
-    return resident_dense<128, 128, __half, width_warps<128, 128, K, K, 2, kCodecAffine>(), K, K, 2,       \
+    return resident_dense<128, 128, width_warps<128, 128, K, K, 2, kCodecAffine>(), K, K, 2,       \
                           kCodecAffine>();                                                                  \
   }                                                                                                         \
   }

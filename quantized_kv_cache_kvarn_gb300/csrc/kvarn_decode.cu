@@ -74,15 +74,23 @@ int dense_decode_ctas_per_sm(int32_t D, int32_t N, int32_t kb, int32_t vb, int32
   int c = 0;
   {
     if (kb == 4 && vb == 2 && sb == 4) {
-      if (D == 128 && N == 128) c = resident_dense<128, 128, __half, 4, 4, 2, 4>();
-      else if (D == 128) c = resident_dense<128, 64, __half, 4, 4, 2, 4>();
-      else if (N == 128) c = resident_dense<256, 128, __half, 2, 4, 2, 4>();
-      else c = resident_dense<256, 64, __half, 2, 4, 2, 4>();
+      if (D == 128 && N == 128) c = resident_dense<128, 128, 4, 4, 2, 4>();
+      else if (D == 128) c = resident_dense<128, 64, 4, 4, 2, 4>();
+      else if (N == 128) c = resident_dense<256, 128, 2, 4, 2, 4>();
+      else c = resident_dense<256, 64, 2, 4, 2, 4>();
     } else if (D == 128 && sb == 2) {
       switch (16 * kb + vb) {
 #define KVARN_RES_CASE(K, V) \
   case 16 * K + V: c = resident_widths<K, V, 2>(D, N); break;
         KVARN_WIDTH_PAIRS(KVARN_RES_CASE)
+#undef KVARN_RES_CASE
+        default: c = 1; break;
+      }
+    } else if (D == 128 && sb == 4) {
+      switch (16 * kb + vb) {
+#define KVARN_RES_CASE(K, V) \
+  case 16 * K + V: c = resident_widths<K, V, 4>(D, N); break;
+        KVARN_WIDTH_PAIRS_S32(KVARN_RES_CASE)
 #undef KVARN_RES_CASE
         default: c = 1; break;
       }
@@ -183,6 +191,7 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   A.raw_splits = plan.raw_splits;
   A.slots = plan.slots;
   A.err = p.err;
+  A.bf16 = p.bf16 ? 1 : 0;
   A.partial_tiles = p.codec == 2;
   {
     const long long w = g_copy_wait_limit.load(std::memory_order_relaxed);
@@ -213,8 +222,7 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   if (kb == 4 && vb == 2 && sb == 4) {
 #define KV_DISPATCH(DD, NN, WW)                                                              \
   if (p.D == DD && p.N == NN)                                                                \
-    e = p.bf16 ? run_dense<DD, NN, __nv_bfloat16, WW, 4, 2, 4>(A, plan.ctas, st)             \
-               : run_dense<DD, NN, __half, WW, 4, 2, 4>(A, plan.ctas, st);
+    e = run_dense<DD, NN, WW, 4, 2, 4>(A, plan.ctas, st);
     KV_DISPATCH(128, 128, 4)
     KV_DISPATCH(128, 64, 4)
     KV_DISPATCH(256, 128, 2)
@@ -233,6 +241,14 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
 #define KVARN_RUN_CASE(K, V) \
   case 16 * K + V: e = run_dense_widths<K, V, 2>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
       KVARN_WIDTH_PAIRS(KVARN_RUN_CASE)
+#undef KVARN_RUN_CASE
+      default: break;
+    }
+  } else if (sb == 4 && p.D == 128) {
+    switch (16 * kb + vb) {
+#define KVARN_RUN_CASE(K, V) \
+  case 16 * K + V: e = run_dense_widths<K, V, 4>(A, p.D, p.N, p.bf16, plan.ctas, st); break;
+      KVARN_WIDTH_PAIRS_S32(KVARN_RUN_CASE)
 #undef KVARN_RUN_CASE
       default: break;
     }

@@ -1,0 +1,11 @@
+// Decode kernels for key code width 5 with value widths 2, 3, 4
+// (fp32 scales, head_dim 128; the preset 4 / 2 has its own instantiation);
+// the pairs are split over translation units so that they compile in
+// parallel.
+#include "kvarn_decode_kernel.cuh"
+
+namespace kvarn {
+KVARN_DECODE_WIDTHS(5, 2, 4)
+KVARN_DECODE_WIDTHS(5, 3, 4)
+KVARN_DECODE_WIDTHS(5, 4, 4)
+}  // namespace kvarn

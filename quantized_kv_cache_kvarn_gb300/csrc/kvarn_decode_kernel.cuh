@@ -147,6 +147,7 @@ struct DecArgs {
   uint32_t* err;
   int32_t partial_tiles;  // uncompressed pages: a sequence's last tile may be partial (tokens past len masked)
   long long wait_limit;   // clock cycles a page copy is waited for before the kernel gives up
+  int32_t bf16;           // storage dtype of q and of the raw records: 0 fp16, 1 bf16
   int32_t withhold;       // diagnostic: every copy is announced this many bytes larger (its phase never completes)
 };
 
@@ -162,6 +163,16 @@ __device__ __forceinline__ void load_vec(const T* p, float* out) {
 #pragma unroll
     for (int k = 0; k < E; k += 8) load8<T>(p + k, out + k);
   }
+}
+
+// E consecutive fp16 or bf16 elements (the storage dtype chosen at run time:
+// the branch is uniform over the grid).
+template <int E>
+__device__ __forceinline__ void load_vec_rt(const void* p, bool bf16, float* out) {
+  if (bf16)
+    load_vec<__nv_bfloat16, E>(static_cast<const __nv_bfloat16*>(p), out);
+  else
+    load_vec<__half, E>(static_cast<const __half*>(p), out);
 }
 
 __device__ __forceinline__ void write_empty(float* part, int D, int lane) {
@@ -260,7 +271,7 @@ __device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count,
 
 // Raw split `chunk` covers raw tokens [chunk * kRawChunk, +kRawChunk) of the
 // row's raw list: its sink rows, then its tail rows.
-template <int D, int N, typename T, int W>
+template <int D, int N, int W>
 __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int sink,
                               int committed, int chunk) {
   constexpr int E = D / 32;
@@ -280,7 +291,8 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
       continue;
     }
     float qv[E];
-    load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, qv);
+    const int64_t qoff = (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E;
+    load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, qv);
 #pragma unroll
     for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
     float mx = -INFINITY, l = 0.f, acc[E];
@@ -288,13 +300,21 @@ __device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R,
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     if (s_cnt > 0) {
       const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N) + c0;
-      raw_segment<D, T>(static_cast<const T*>(A.sink_k) + row0 * D, static_cast<const T*>(A.sink_v) + row0 * D,
-                        s_cnt, qv, mx, l, acc);
+      if (A.bf16)
+        raw_segment<D>(static_cast<const __nv_bfloat16*>(A.sink_k) + row0 * D,
+                       static_cast<const __nv_bfloat16*>(A.sink_v) + row0 * D, s_cnt, qv, mx, l, acc);
+      else
+        raw_segment<D>(static_cast<const __half*>(A.sink_k) + row0 * D, static_cast<const __half*>(A.sink_v) + row0 * D,
+                       s_cnt, qv, mx, l, acc);
     }
     if (t_cnt > 0) {
       const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap + t0;
-      raw_segment<D, T>(static_cast<const T*>(A.tail_k) + row0 * D, static_cast<const T*>(A.tail_v) + row0 * D,
-                        t_cnt, qv, mx, l, acc);
+      if (A.bf16)
+        raw_segment<D>(static_cast<const __nv_bfloat16*>(A.tail_k) + row0 * D,
+                       static_cast<const __nv_bfloat16*>(A.tail_v) + row0 * D, t_cnt, qv, mx, l, acc);
+      else
+        raw_segment<D>(static_cast<const __half*>(A.tail_k) + row0 * D, static_cast<const __half*>(A.tail_v) + row0 * D,
+                       t_cnt, qv, mx, l, acc);
     }
     if (lane == 0) {
       part[0] = mx;
@@ -426,7 +446,7 @@ __device__ __forceinline__ int cta_of_tile(int64_t t, int C, int64_t total, int 
 // 24), each counted mod 256 (only parities are read). `dead`: a copy timed
 // out earlier; the segment then only writes empty partials. Returns false
 // when a copy timed out (in this segment or before).
-template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD>
+template <int D, int N, int W, int KB, int VB, int SB, int CD>
 __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* smem, int b, int x, int t0, int t1,
                                               int slot, uint32_t& ph,
                                               bool dead) {
@@ -551,7 +571,8 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
     float v[E];
     if (h < R.n) {
       const int hq = kvh * A.G + R.head(A, h), j = R.query(A, h);
-      load_vec<T, E>(static_cast<const T*>(A.q) + (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E, v);
+      const int64_t qoff = (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E;
+      load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, v);
       if constexpr (!PLAIN_Q) warp_fwht<E>(v);  // the affine and fp16 pages are in the original basis
       const float sc = PLAIN_Q ? A.kappa : A.kappa / sqrtf(static_cast<float>(D));
 #pragma unroll
@@ -963,7 +984,7 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   return !any_late;
 }
 
-template <int D, int N, typename T, int W, int KB = 4, int VB = 2, int SB = 4, int CD = kCodecKvarn>
+template <int D, int N, int W, int KB = 4, int VB = 2, int SB = 4, int CD = kCodecKvarn>
 __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_dense_kernel(const __grid_constant__ DecArgs A) {
   using S = DecShape<D, N, W, KB, VB, SB, CD>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -991,7 +1012,7 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_
     const int64_t u = r / A.raw_splits;
     const int b = static_cast<int>(u / A.X), x = static_cast<int>(u % A.X);
     const int len = checked_len(A, b);
-    tail_partials<D, N, T, W>(A, b, x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N,
+    tail_partials<D, N, W>(A, b, x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N,
                               committed_end(A, N, len), chunk);
   }
 
@@ -1039,14 +1060,14 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_
     const int t0 = A.sink_tiles + P.tile;
     const int t1 = t0 + static_cast<int>(seg_end - cur);
     if (threadIdx.x == 0) pos[k ^ 1] = seg_end;
-    dead = !dense_segment<D, N, T, W, KB, VB, SB, CD>(A, smem, P.b, P.x, t0, t1, slot, ph, dead) || dead;
+    dead = !dense_segment<D, N, W, KB, VB, SB, CD>(A, smem, P.b, P.x, t0, t1, slot, ph, dead) || dead;
   }
 }
 
-template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
+template <int D, int N, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
 cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
   using S = DecShape<D, N, W, KB, VB, SB, CD>;
-  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB, CD>;
+  auto kern = decode_dense_kernel<D, N, W, KB, VB, SB, CD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the kernel before it on the stream: the
@@ -1066,10 +1087,10 @@ cudaError_t run_dense(const DecArgs& A, int ctas, cudaStream_t st) {
 }
 
 // CTAs of one decode kernel resident per SM (registers and shared memory).
-template <int D, int N, typename T, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
+template <int D, int N, int W, int KB, int VB, int SB, int CD = kCodecKvarn>
 int resident_dense() {
   using S = DecShape<D, N, W, KB, VB, SB, CD>;
-  auto kern = decode_dense_kernel<D, N, T, W, KB, VB, SB, CD>;
+  auto kern = decode_dense_kernel<D, N, W, KB, VB, SB, CD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM) != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, W * 32, S::SMEM) != cudaSuccess || n < 1) return 1;
@@ -1094,13 +1115,18 @@ cudaError_t run_dense_widths(const DecArgs& A, int D, int N, bool bf16, int ctas
 template <int KB, int VB, int SB>
 int resident_widths(int D, int N);
 
-#define KVARN_DECLARE_WIDTHS(KB, VB)                                                                 \
+#define KVARN_DECLARE_WIDTHS(KB, VB, SB)                                                             \
   template <>                                                                                       \
-  cudaError_t run_dense_widths<KB, VB, 2>(const DecArgs& A, int D, int N, bool bf16, int ctas,     \
-                                          cudaStream_t st);                                         \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas,    \
+                                           cudaStream_t st);                                        \
   template <>                                                                                       \
-  int resident_widths<KB, VB, 2>(int D, int N);
-KVARN_WIDTH_PAIRS(KVARN_DECLARE_WIDTHS)
+  int resident_widths<KB, VB, SB>(int D, int N);
+#define KVARN_DECLARE_WIDTHS_S16(KB, VB) KVARN_DECLARE_WIDTHS(KB, VB, 2)
+#define KVARN_DECLARE_WIDTHS_S32(KB, VB) KVARN_DECLARE_WIDTHS(KB, VB, 4)
+KVARN_WIDTH_PAIRS(KVARN_DECLARE_WIDTHS_S16)
+KVARN_WIDTH_PAIRS_S32(KVARN_DECLARE_WIDTHS_S32)
+#undef KVARN_DECLARE_WIDTHS_S16
+#undef KVARN_DECLARE_WIDTHS_S32
 #undef KVARN_DECLARE_WIDTHS
 
 // The same at head_dim 256 (warp pairs share a tile).
@@ -1142,39 +1168,35 @@ KVARN_AFFINE_WIDTHS(KVARN_DECLARE_AFFINE)
 
 #define KVARN_DECODE_WIDTHS(KB, VB, SB)                                                                   \
   template <>                                                                                           \
-  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool bf16, int ctas,         \
+  cudaError_t run_dense_widths<KB, VB, SB>(const DecArgs& A, int D, int N, bool /*bf16*/, int ctas,    \
                                            cudaStream_t st) {                                           \
     constexpr int W1 = width_warps<128, 128, KB, VB, SB>(), W2 = width_warps<128, 64, KB, VB, SB>();    \
     if (D == 128 && N == 128)                                                                           \
-      return bf16 ? run_dense<128, 128, __nv_bfloat16, W1, KB, VB, SB>(A, ctas, st)                \
-                  : run_dense<128, 128, __half, W1, KB, VB, SB>(A, ctas, st);                       \
+      return run_dense<128, 128, W1, KB, VB, SB>(A, ctas, st);                       \
     if (D == 128 && N == 64)                                                                            \
-      return bf16 ? run_dense<128, 64, __nv_bfloat16, W2, KB, VB, SB>(A, ctas, st)                 \
-                  : run_dense<128, 64, __half, W2, KB, VB, SB>(A, ctas, st);                        \
+      return run_dense<128, 64, W2, KB, VB, SB>(A, ctas, st);                        \
     return cudaErrorInvalidValue;                                                                       \
   }                                                                                                     \
   template <>                                                                                           \
   int resident_widths<KB, VB, SB>(int D, int N) {                                                       \
-    if (D == 128 && N == 128) return resident_dense<128, 128, __half, width_warps<128, 128, KB, VB, SB>(), KB, VB, SB>(); \
-    if (D == 128 && N == 64) return resident_dense<128, 64, __half, width_warps<128, 64, KB, VB, SB>(), KB, VB, SB>();   \
+    if (D == 128 && N == 128) return resident_dense<128, 128, width_warps<128, 128, KB, VB, SB>(), KB, VB, SB>(); \
+    if (D == 128 && N == 64) return resident_dense<128, 64, width_warps<128, 64, KB, VB, SB>(), KB, VB, SB>();   \
     return 1;                                                                                           \
   }
 
 #define KVARN_DECODE_WIDTHS_256(KB, VB)                                                                \
   template <>                                                                                          \
-  cudaError_t run_dense_widths256<KB, VB, 2>(const DecArgs& A, int N, bool bf16, int ctas, cudaStream_t st) { \
+  cudaError_t run_dense_widths256<KB, VB, 2>(const DecArgs& A, int N, bool /*bf16*/, int ctas, cudaStream_t st) { \
     if (N == 128)                                                                                      \
-      return bf16 ? run_dense<256, 128, __nv_bfloat16, 2, KB, VB, 2>(A, ctas, st)                     \
-                  : run_dense<256, 128, __half, 2, KB, VB, 2>(A, ctas, st);                            \
+      return run_dense<256, 128, 2, KB, VB, 2>(A, ctas, st);                            \
     if (N == 64)                                                                                       \
-      return bf16 ? run_dense<256, 64, __nv_bfloat16, 2, KB, VB, 2>(A, ctas, st)                      \
-                  : run_dense<256, 64, __half, 2, KB, VB, 2>(A, ctas, st);                             \
+      return run_dense<256, 64, 2, KB, VB, 2>(A, ctas, st);                             \
     return cudaErrorInvalidValue;                                                                      \
   }                                                                                                    \
   template <>                                                                                          \
   int resident_widths256<KB, VB, 2>(int N) {                                                           \
-    return N == 128 ? resident_dense<256, 128, __half, 2, KB, VB, 2>()                                 \
-                    : resident_dense<256, 64, __half, 2, KB, VB, 2>();                                 \
+    return N == 128 ? resident_dense<256, 128, 2, KB, VB, 2>()                                 \
+                    : resident_dense<256, 64, 2, KB, VB, 2>();                                 \
   }
 
 }  // namespace kvarn

@@ -1,0 +1,13 @@
+// Encode kernels at head_dim 256 with fp16 scales for key code width 5 and
+// every value width; one translation unit per key width, so that the pairs
+// compile in parallel.
+#include "kvarn_encode_kernel.cuh"
+
+namespace kvarn {
+KVARN_ENCODE_WIDTHS_256(5, 2)
+KVARN_ENCODE_WIDTHS_256(5, 3)
+KVARN_ENCODE_WIDTHS_256(5, 4)
+KVARN_ENCODE_WIDTHS_256(5, 5)
+KVARN_ENCODE_WIDTHS_256(5, 6)
+KVARN_ENCODE_WIDTHS_256(5, 8)
+}  // namespace kvarn

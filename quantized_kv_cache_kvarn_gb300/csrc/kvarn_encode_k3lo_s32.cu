@@ -1,0 +1,11 @@
+// Encode kernels for key code width 3 with value widths 2, 3, 4
+// (fp32 scales, head_dim 128; the preset 4 / 2 has its own instantiation);
+// the pairs are split over translation units so that they compile in
+// parallel.
+#include "kvarn_encode_kernel.cuh"
+
+namespace kvarn {
+KVARN_ENCODE_WIDTHS(3, 2, 4)
+KVARN_ENCODE_WIDTHS(3, 3, 4)
+KVARN_ENCODE_WIDTHS(3, 4, 4)
+}  // namespace kvarn

@@ -69,6 +69,7 @@ struct EncodeArgs {
   int32_t norm_iters;
   int32_t rope_dim;
   uint32_t* err;
+  int32_t bf16;  // storage dtype of the dense and latent inputs: 0 fp16, 1 bf16
   // optional fp32 intermediates of every encoded dense tile (null in normal
   // use): per (sequence, KV head, chunk tile, K|V) the rotated tile Y, the
   // normalised tile Z (both N x D, token rows), then r, lo, delta per token
@@ -269,10 +270,10 @@ __device__ __forceinline__ void pack_plane_words(const unsigned char* cb, uint32
 // in the same launch).
 // KIND 0: a dense tile, SIDE_V selecting its V (else K) part of pages of code
 // widths KB, VB and SB-byte scales; KIND 1: a latent tile (4-bit, fp32).
-template <int D, int N, int CS, int BITS, int KIND, typename T, bool SIDE_V = false, int KB = 4, int VB = 2,
+template <int D, int N, int CS, int BITS, int KIND, bool SIDE_V = false, int KB = 4, int VB = 2,
           int SB = 4>
-__device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __restrict__ src,
-                                            int b, int head, int u, int64_t tile, const T* last_row,
+__device__ __forceinline__ void encode_tile(const EncodeArgs& A, const unsigned char* __restrict__ src,
+                                            int b, int head, int u, int64_t tile, const unsigned char* last_row,
                                             unsigned char* smem) {
   constexpr bool IS_V = KIND == 0 && SIDE_V;
   // the 4-bit K and 2-bit V placements pack in registers; other widths take
@@ -312,10 +313,18 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 #pragma unroll
   for (int i = 0; i < S::RPT; ++i) {
     const int r = crank * S::ROWS + local_row(i);
-    const T* p = (last_row != nullptr && r == N - 1) ? last_row + seg * 16 : src + static_cast<int64_t>(r) * D + seg * 16;
+    // 16-bit elements (fp16 or bf16 by A.bf16, uniform over the grid)
+    const unsigned char* p = (last_row != nullptr && r == N - 1)
+                                 ? last_row + 2 * (seg * 16)
+                                 : src + 2 * (static_cast<int64_t>(r) * D + seg * 16);
     float v[16];
-    load8<T>(p, v);
-    load8<T>(p + 8, v + 8);
+    if (A.bf16) {
+      load8<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(p), v);
+      load8<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(p) + 8, v + 8);
+    } else {
+      load8<__half>(reinterpret_cast<const __half*>(p), v);
+      load8<__half>(reinterpret_cast<const __half*>(p) + 8, v + 8);
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) xp[i][e] = make_float2(v[2 * e], v[2 * e + 1]);
   }
@@ -647,7 +656,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const T* __rest
 // K (4-bit) and V (2-bit) tiles share one launch: blockIdx.z < num_seqs
 // encodes K, the rest V, so that the K half of a large grid runs before the
 // V half and an SM mostly runs one of the two code paths.
-template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
+template <int D, int N, int KB = 4, int VB = 2, int SB = 4>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) encode_dense_kernel(EncodeArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   // the decode launched after a commit may be scheduled once every CTA here
@@ -659,23 +668,13 @@ __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) encode_dense_kernel(E
   const int64_t off = static_cast<int64_t>(b) * A.seq_stride + static_cast<int64_t>(head) * A.head_stride +
                       static_cast<int64_t>(u) * N * D;
   if (is_v)
-    encode_tile<D, N, 1, VB, 0, T, true, KB, VB, SB>(A, static_cast<const T*>(A.x[1]) + off, b, head, u,
+    encode_tile<D, N, 1, VB, 0, true, KB, VB, SB>(A, static_cast<const unsigned char*>(A.x[1]) + 2 * off, b, head, u,
                                                      A.tile_start[b] + u, nullptr, smem);
   else
-    encode_tile<D, N, 1, KB, 0, T, false, KB, VB, SB>(A, static_cast<const T*>(A.x[0]) + off, b, head, u,
+    encode_tile<D, N, 1, KB, 0, false, KB, VB, SB>(A, static_cast<const unsigned char*>(A.x[0]) + 2 * off, b, head, u,
                                                       A.tile_start[b] + u, nullptr, smem);
 }
 
-template <typename T>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
-    encode_latent_kernel(EncodeArgs A) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int u = blockIdx.x >> 1, b = blockIdx.y;
-  if (A.tile_start[b] < 0) return;  // uniform over the cluster: both CTAs share b
-  const T* src = static_cast<const T*>(A.x[0]) + static_cast<int64_t>(b) * A.seq_stride +
-                 static_cast<int64_t>(u) * 128 * 512;
-  encode_tile<512, 128, 2, 4, 1, T>(A, src, b, 0, u, A.tile_start[b] + u, nullptr, smem);
-}
 
 // Fused append + commit (one launch per decode step): x[0] / x[1] hold each
 // (sequence, KV head)'s newest K / V token, at position seq_lens[b] - 1. A
@@ -683,9 +682,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
 // that does completes the tile in the tail's rows 0..N-2 and the tile is
 // encoded straight into its pages (the tail then holds nothing). The tail
 // rows read here were written by earlier launches.
-template <int D, int N, typename T>
+template <int D, int N>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
-                                                              int32_t max_seq_len, T* tail_k, T* tail_v) {
+                                                              int32_t max_seq_len, unsigned char* tail_k,
+                                                              unsigned char* tail_v) {
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_launch_dependents();
   const bool is_v = blockIdx.z == 1;
@@ -696,26 +696,27 @@ __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) append_commit_kernel(
     return;
   }
   const int64_t hs = static_cast<int64_t>(b) * A.num_kv_heads + head;
-  const T* tok = static_cast<const T*>(A.x[is_v]) + hs * D;
-  T* tail = (is_v ? tail_v : tail_k) + hs * N * D;
+  // 16-bit elements (fp16 or bf16)
+  const unsigned char* tok = static_cast<const unsigned char*>(A.x[is_v]) + 2 * hs * D;
+  unsigned char* tail = (is_v ? tail_v : tail_k) + 2 * hs * N * D;
   if (L % N != 0) {
     const int row = (L - 1) % N;
     for (int i = threadIdx.x; i < D / 8; i += blockDim.x)
-      reinterpret_cast<uint4*>(tail + static_cast<int64_t>(row) * D)[i] = reinterpret_cast<const uint4*>(tok)[i];
+      reinterpret_cast<uint4*>(tail + 2 * static_cast<int64_t>(row) * D)[i] = reinterpret_cast<const uint4*>(tok)[i];
     return;
   }
   if (is_v)
-    encode_tile<D, N, 1, 2, 0, T, true>(A, tail, b, head, 0, L / N - 1, tok, smem);
+    encode_tile<D, N, 1, 2, 0, true>(A, tail, b, head, 0, L / N - 1, tok, smem);
   else
-    encode_tile<D, N, 1, 4, 0, T, false>(A, tail, b, head, 0, L / N - 1, tok, smem);
+    encode_tile<D, N, 1, 4, 0, false>(A, tail, b, head, 0, L / N - 1, tok, smem);
 }
 
 // ------------------------------------------------------------- launchers
-template <int D, int N, typename T, int KB = 4, int VB = 2, int SB = 4>
+template <int D, int N, int KB = 4, int VB = 2, int SB = 4>
 cudaError_t launch_dense(const EncodeArgs& A, cudaStream_t st) {
   constexpr bool gen = !(KB == 4 && VB == 2);
   constexpr int smem = gen ? EncShape<D, N, 1, true>::SMEM : EncShape<D, N, 1>::SMEM;
-  auto kern = encode_dense_kernel<D, N, T, KB, VB, SB>;
+  auto kern = encode_dense_kernel<D, N, KB, VB, SB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(A.chunk_tiles, A.num_kv_heads, 2 * A.num_seqs);
@@ -733,6 +734,11 @@ cudaError_t launch_encode_widths(const EncodeArgs& A, int N, bool bf16, cudaStre
   template <>                            \
   cudaError_t launch_encode_widths<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
 KVARN_WIDTH_PAIRS(KVARN_DECLARE_ENC_WIDTHS)
+#define KVARN_DECLARE_ENC_WIDTHS_S32(KB, VB) \
+  template <>                                \
+  cudaError_t launch_encode_widths<KB, VB, 4>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
+KVARN_WIDTH_PAIRS_S32(KVARN_DECLARE_ENC_WIDTHS_S32)
+#undef KVARN_DECLARE_ENC_WIDTHS_S32
 template <int KB, int VB, int SB>
 cudaError_t launch_encode_widths256(const EncodeArgs& A, int N, bool bf16, cudaStream_t st);
 #define KVARN_DECLARE_ENC_WIDTHS_256(KB, VB) \
@@ -744,25 +750,21 @@ KVARN_WIDTH_PAIRS_256(KVARN_DECLARE_ENC_WIDTHS_256)
 
 #define KVARN_ENCODE_WIDTHS(KB, VB, SB)                                                                \
   template <>                                                                                          \
-  cudaError_t launch_encode_widths<KB, VB, SB>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st) { \
+  cudaError_t launch_encode_widths<KB, VB, SB>(const EncodeArgs& A, int N, bool /*bf16*/, cudaStream_t st) { \
     if (N == 128)                                                                                      \
-      return bf16 ? launch_dense<128, 128, __nv_bfloat16, KB, VB, SB>(A, st)                          \
-                  : launch_dense<128, 128, __half, KB, VB, SB>(A, st);                                 \
+      return launch_dense<128, 128, KB, VB, SB>(A, st);                                 \
     if (N == 64)                                                                                       \
-      return bf16 ? launch_dense<128, 64, __nv_bfloat16, KB, VB, SB>(A, st)                           \
-                  : launch_dense<128, 64, __half, KB, VB, SB>(A, st);                                  \
+      return launch_dense<128, 64, KB, VB, SB>(A, st);                                  \
     return cudaErrorInvalidValue;                                                                      \
   }
 
 #define KVARN_ENCODE_WIDTHS_256(KB, VB)                                                                 \
   template <>                                                                                         \
-  cudaError_t launch_encode_widths256<KB, VB, 2>(const EncodeArgs& A, int N, bool bf16, cudaStream_t st) { \
+  cudaError_t launch_encode_widths256<KB, VB, 2>(const EncodeArgs& A, int N, bool /*bf16*/, cudaStream_t st) { \
     if (N == 128)                                                                                     \
-      return bf16 ? launch_dense<256, 128, __nv_bfloat16, KB, VB, 2>(A, st)                          \
-                  : launch_dense<256, 128, __half, KB, VB, 2>(A, st);                                 \
+      return launch_dense<256, 128, KB, VB, 2>(A, st);                                 \
     if (N == 64)                                                                                      \
-      return bf16 ? launch_dense<256, 64, __nv_bfloat16, KB, VB, 2>(A, st)                           \
-                  : launch_dense<256, 64, __half, KB, VB, 2>(A, st);                                  \
+      return launch_dense<256, 64, KB, VB, 2>(A, st);                                  \
     return cudaErrorInvalidValue;                                                                     \
   }
 

@@ -83,11 +83,11 @@ cudaError_t launch_store_fp16(const StoreFp16Params& p, cudaStream_t st) {
 template <int D>
 cudaError_t run_raw(const DecArgs& A, int ctas, cudaStream_t st) {
   constexpr int W = D == 256 ? 2 : 4;
-  return run_dense<D, 32, __half, W, 4, 2, 4, kCodecRaw>(A, ctas, st);
+  return run_dense<D, 32, W, 4, 2, 4, kCodecRaw>(A, ctas, st);
 }
 template <int D>
 int resident_raw() {
-  return resident_dense<D, 32, __half, D == 256 ? 2 : 4, 4, 2, 4, kCodecRaw>();
+  return resident_dense<D, 32, D == 256 ? 2 : 4, 4, 2, 4, kCodecRaw>();
 }
 template cudaError_t run_raw<128>(const DecArgs&, int, cudaStream_t);
 template cudaError_t run_raw<256>(const DecArgs&, int, cudaStream_t);

@@ -23,16 +23,16 @@ struct EncodeParams {
   float* stages;  // optional fp32 stage records of the encoded tiles (null: none)
 };
 
-// Code widths and scale sizes with compiled kernels: (4, 2) with fp32 scales
-// for every head_dim and tile; with fp16 scales, every pair of a key width
-// and a value width from {2, 3, 4, 5, 6, 8} for head_dim 128 (the gmlx page
-// sets the two widths separately), and equal widths plus (4, 2) for head_dim
-// 256.
+// Code widths and scale sizes with compiled kernels: every pair of a key
+// width and a value width from {2, 3, 4, 5, 6, 8} (the gmlx page sets the
+// two widths separately), with fp16 or fp32 scales at head_dim 128 and with
+// fp16 scales at head_dim 256, where (4, 2) also takes fp32 scales.
 inline bool width_compiled(int32_t b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 inline bool widths_supported(int32_t D, int32_t kb, int32_t vb, int32_t sb) {
   if (kb == 4 && vb == 2 && sb == 4) return true;
-  if (D == 256) return sb == 2 && width_compiled(kb) && (kb == vb || (kb == 4 && vb == 2));
-  return D == 128 && sb == 2 && width_compiled(kb) && width_compiled(vb);
+  if (!width_compiled(kb) || !width_compiled(vb)) return false;
+  if (D == 256) return sb == 2;
+  return D == 128 && (sb == 2 || sb == 4);
 }
 
 // X(KB, VB) for every compiled (key width, value width) pair with fp16
@@ -41,8 +41,14 @@ inline bool widths_supported(int32_t D, int32_t kb, int32_t vb, int32_t sb) {
 #define KVARN_WIDTH_PAIRS(X)                                                         \
   KVARN_WIDTH_ROW(X, 2) KVARN_WIDTH_ROW(X, 3) KVARN_WIDTH_ROW(X, 4) KVARN_WIDTH_ROW(X, 5) \
   KVARN_WIDTH_ROW(X, 6) KVARN_WIDTH_ROW(X, 8)
-// X(KB, VB) for the pairs compiled at head_dim 256 (fp16 scales).
-#define KVARN_WIDTH_PAIRS_256(X) X(2, 2) X(3, 3) X(4, 2) X(4, 4) X(5, 5) X(6, 6) X(8, 8)
+// X(KB, VB) for the pairs compiled at head_dim 256 (fp16 scales): all.
+#define KVARN_WIDTH_PAIRS_256(X) KVARN_WIDTH_PAIRS(X)
+// X(KB, VB) for the pairs compiled with fp32 scales at head_dim 128 besides
+// the preset (4, 2), which has its own instantiation.
+#define KVARN_WIDTH_ROW_NO42(X, K) X(K, 3) X(K, 4) X(K, 5) X(K, 6) X(K, 8)
+#define KVARN_WIDTH_PAIRS_S32(X)                                                              \
+  KVARN_WIDTH_ROW(X, 2) KVARN_WIDTH_ROW(X, 3) KVARN_WIDTH_ROW_NO42(X, 4) KVARN_WIDTH_ROW(X, 5) \
+  KVARN_WIDTH_ROW(X, 6) KVARN_WIDTH_ROW(X, 8)
 
 struct AppendParams {
   const void* k;  // newest token per (sequence, KV head): [B][Hkv][D]

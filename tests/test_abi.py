@@ -46,8 +46,8 @@ def test_page_bytes(L):
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("head_dim", 64, -2), ("head_dim", 96, -2), ("tile_tokens", 32, -2), ("k_bits", 3, -2),
-    ("v_bits", 4, -2), ("norm_iters", 0, -2), ("norm_iters", 9, -2), ("page_tokens", 32, -2),
+    ("head_dim", 64, -2), ("head_dim", 96, -2), ("tile_tokens", 32, -2), ("k_bits", 7, -2),
+    ("v_bits", 1, -2), ("norm_iters", 0, -2), ("norm_iters", 9, -2), ("page_tokens", 32, -2),
     ("kv_dtype", 2, -2), ("num_kv_heads", 0, -1)])
 def test_layout_rejections(L, field, value, code):
     lay = kv.dense_layout(128, 128, 8, 10)
@@ -60,16 +60,19 @@ def test_layout_rejections(L, field, value, code):
 @pytest.mark.parametrize("vb", [2, 3, 4, 5, 6, 8])
 def test_width_pairs_with_fp16_scales(L, kb, vb):
     """Keys and values take their widths separately (gmlx page, "The two
-    schemes"): every pair is accepted at head_dim 128 with fp16 scales (equal
-    widths and k4v2 at 256), and the page is the K part then the V part at
-    their own widths."""
-    lay = kv.dense_layout(128, 128, 8, 10, k_bits=kb, v_bits=vb, fp16_scales=True)
-    assert L.kvarn_layout_check(ctypes.byref(lay)) == 0
+    schemes"): every pair is accepted at head_dim 128 with fp16 or fp32
+    scales and at head_dim 256 with fp16 scales (fp32 there only for k4v2),
+    and the page is the K part then the V part at their own widths."""
     from oracle import layout
-    assert kv.page_bytes(lay) == layout.DenseLayout(128, 128, kb, vb, 2).page_bytes
+    for sb in (2, 4):
+        lay = kv.dense_layout(128, 128, 8, 10, k_bits=kb, v_bits=vb, fp16_scales=sb == 2)
+        assert L.kvarn_layout_check(ctypes.byref(lay)) == 0
+        assert kv.page_bytes(lay) == layout.DenseLayout(128, 128, kb, vb, sb).page_bytes
     wide = kv.dense_layout(256, 128, 4, 10, k_bits=kb, v_bits=vb, fp16_scales=True)
-    # head_dim 256 carries equal widths and the k4v2 pair
-    assert L.kvarn_layout_check(ctypes.byref(wide)) == (0 if kb == vb or (kb, vb) == (4, 2) else -2)
+    assert L.kvarn_layout_check(ctypes.byref(wide)) == 0
+    assert kv.page_bytes(wide) == layout.DenseLayout(256, 128, kb, vb, 2).page_bytes
+    wide32 = kv.dense_layout(256, 128, 4, 10, k_bits=kb, v_bits=vb, fp16_scales=False)
+    assert L.kvarn_layout_check(ctypes.byref(wide32)) == (0 if (kb, vb) == (4, 2) else -2)
 
 
 @pytest.mark.parametrize("kb,vb", [(7, 4), (4, 7), (1, 2), (6, 0)])

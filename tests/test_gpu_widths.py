@@ -1,8 +1,8 @@
 """GPU parity of the other code widths (gmlx page, "The two schemes": kvarn
-widths 2, 3, 4, 5, 6 and 8, set separately for keys and values) with fp16
-scales at head_dim 128 and 256, through the C ABI: the pages the
-GPU encoder writes against the oracle's encoding, and the GPU decode of pages
-the oracle wrote against the oracle's decode."""
+widths 2, 3, 4, 5, 6 and 8, set separately for keys and values), with fp16
+and fp32 scales at head_dim 128 and fp16 scales at 256, through the C ABI: the
+pages the GPU encoder writes against the oracle's encoding, and the GPU
+decode of pages the oracle wrote against the oracle's decode."""
 import numpy as np
 import pytest
 import torch
@@ -15,15 +15,15 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 BITS = (2, 3, 4, 5, 6, 8)
-# every compiled (key width, value width) pair at head_dim 128 (the gmlx
-# page sets the two widths separately, GMLX_KVARN_BITS), the tile size
-# alternating so that each size meets every key and every value width
-WIDTHS = [(kb, vb, 128 if (i + j) % 2 == 0 else 64, 128) for i, kb in enumerate(BITS) for j, vb in enumerate(BITS)]
-# both tile sizes for the equal widths and the preset pair
-WIDTHS += [(b, b, 64 if (i % 2 == 0) else 128, 128) for i, b in enumerate(BITS)] + [(4, 2, 64, 128)]
-# every pair compiled at head_dim 256 (warp pairs share a tile; 8-bit parts
-# wider than one gather box), at both tile sizes
-WIDTHS += [(kb, vb, N, 256) for kb, vb in ((2, 2), (3, 3), (4, 2), (4, 4), (5, 5), (6, 6), (8, 8)) for N in (64, 128)]
+# every compiled (key width, value width) pair (the gmlx page sets the two
+# widths separately, GMLX_KVARN_BITS), the tile size alternating so that each
+# size meets every key and every value width: head_dim 128 with fp16 scales
+# and with fp32 scales, head_dim 256 with fp16 scales; (k, v, N, D, scale bytes)
+WIDTHS = [(kb, vb, 128 if (i + j) % 2 == 0 else 64, 128, 2) for i, kb in enumerate(BITS) for j, vb in enumerate(BITS)]
+WIDTHS += [(b, b, 64 if (i % 2 == 0) else 128, 128, 2) for i, b in enumerate(BITS)] + [(4, 2, 64, 128, 2)]
+WIDTHS += [(kb, vb, 64 if (i + j) % 2 == 0 else 128, 128, 4) for i, kb in enumerate(BITS) for j, vb in enumerate(BITS)]
+WIDTHS += [(kb, vb, 128 if (i + j) % 2 == 0 else 64, 256, 2) for i, kb in enumerate(BITS) for j, vb in enumerate(BITS)]
+WIDTHS += [(b, b, 64 if (i % 2 == 0) else 128, 256, 2) for i, b in enumerate(BITS)]
 WIDTHS = list(dict.fromkeys(WIDTHS))
 
 
@@ -40,12 +40,12 @@ def _case(N, D=128):
     return wl, W.make_dense(wl, device="cpu")
 
 
-@pytest.mark.parametrize("kb,vb,N,D", WIDTHS)
-def test_encode_matches_oracle(kb, vb, N, D):
+@pytest.mark.parametrize("kb,vb,N,D,sb", WIDTHS)
+def test_encode_matches_oracle(kb, vb, N, D, sb):
     wl, case = _case(N, D)
     dev = "cuda"
-    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
-    assert kv.page_bytes(lay) == layout.DenseLayout(D, N, kb, vb, 2).page_bytes
+    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=sb == 2)
+    assert kv.page_bytes(lay) == layout.DenseLayout(D, N, kb, vb, sb).page_bytes
     cache = kv.alloc_cache(lay, dev)
     err = kv.new_error_word(dev)
     T = int(case.seq_lens[0]) // N
@@ -55,23 +55,23 @@ def test_encode_matches_oracle(kb, vb, N, D):
     assert kv.read_error_flags(err) == 0
     st_k, st_v = parity.check_dense_pages(cache.cpu().numpy(), parity.f64(case.k), parity.f64(case.v),
                                           case.block_table.numpy(), case.seq_lens.numpy(), N, D,
-                                          kb=kb, vb=vb, sb=2)
-    print(f"\nK{kb}V{vb} N{N} D{D}: K codes {st_k['mismatch']}/{st_k['codes']} differ, V {st_v['mismatch']}/"
+                                          kb=kb, vb=vb, sb=sb)
+    print(f"\nK{kb}V{vb} N{N} D{D} S{8 * sb}: K codes {st_k['mismatch']}/{st_k['codes']} differ, V {st_v['mismatch']}/"
           f"{st_v['codes']}")
 
 
-@pytest.mark.parametrize("kb,vb,N,D", WIDTHS)
-def test_decode_on_oracle_pages_matches_oracle(kb, vb, N, D):
+@pytest.mark.parametrize("kb,vb,N,D,sb", WIDTHS)
+def test_decode_on_oracle_pages_matches_oracle(kb, vb, N, D, sb):
     wl, case = _case(N, D)
     k, v = parity.f64(case.k), parity.f64(case.v)
     bt, lens = case.block_table.numpy(), case.seq_lens.numpy()
-    ocache = parity.oracle_dense_cache(k, v, bt, lens, N, D, case.num_pages, kb=kb, vb=vb, sb=2)
+    ocache = parity.oracle_dense_cache(k, v, bt, lens, N, D, case.num_pages, kb=kb, vb=vb, sb=sb)
     tk, tv = parity.tails(k, lens, N), parity.tails(v, lens, N)
     sm = W.default_sm_scale(wl)
-    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(D, N, kb, vb, 2), bt, lens,
+    ref, ref_lse = attention.decode(parity.f64(case.q), ocache, layout.DenseLayout(D, N, kb, vb, sb), bt, lens,
                                     sm, tk, tv)
     dev = "cuda"
-    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=True)
+    lay = kv.dense_layout(D, N, wl.num_kv_heads, case.num_pages, k_bits=kb, v_bits=vb, fp16_scales=sb == 2)
     Lmax = int(lens.max())
     out = torch.empty((wl.num_seqs, wl.num_q_heads, D), dtype=torch.float32, device=dev)
     lse = torch.empty((wl.num_seqs, wl.num_q_heads), dtype=torch.float32, device=dev)
@@ -84,6 +84,6 @@ def test_decode_on_oracle_pages_matches_oracle(kb, vb, N, D):
     torch.cuda.synchronize()
     assert kv.read_error_flags(err) == 0
     diff = np.abs(parity.f64(out) - ref).max()
-    print(f"\nK{kb}V{vb} N{N} D{D}: max |out - oracle| = {diff:.3e}")
+    print(f"\nK{kb}V{vb} N{N} D{D} S{8 * sb}: max |out - oracle| = {diff:.3e}")
     assert diff <= parity.OUT_ATOL
     np.testing.assert_allclose(parity.f64(lse), ref_lse, atol=1e-4, rtol=0)
