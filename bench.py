@@ -478,6 +478,8 @@ class VerifyHarness(DenseHarness):
         self.dt = kv.BF16 if wl.dtype == "bf16" else kv.FP16
         self.lay = kv.dense_layout(D, N, Hkv, case.num_pages, self.dt, wl.norm_iters)
         self.cache = kv.alloc_cache(self.lay, dev)
+        self._enc, self._dec = kv.encode_tiles, kv.decode
+        self._wsb, self._pb = kv.decode_workspace_bytes, kv.page_bytes
         self.err = kv.new_error_word(dev)
         lens = case.seq_lens.cpu().tolist()
         self.lens, self.Lmax = lens, max(lens)

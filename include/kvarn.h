@@ -386,7 +386,7 @@ int32_t kvarn_decode_window(const void* q, int32_t num_q_heads, int32_t num_quer
  * fp16 page format (P = 16 tokens of one KV head, kv_dtype elements):
  *   K: [16][D] placed per token as four lane chunks of D/4 elements, chunk t
  *      holding channels 16kc + {2t, 2t+1, 2t+8, 2t+9} in kc order;
- *   V: lane chunk L = 4g + t (D/4 elements) holding, for every 8-channel block
+ *   V: lane chunk L = 4g + t (D/2 elements) holding, for every 8-channel block
  *      nc, channel 8nc + g at tokens {2t, 2t+1, 2t+8, 2t+9}.
  *   page_bytes = 4 * 16 * D (K then V).
  * kvarn_store_fp16 writes tokens [token0, token0 + count) of every sequence

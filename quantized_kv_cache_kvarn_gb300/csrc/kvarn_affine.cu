@@ -120,7 +120,7 @@ __device__ __forceinline__ void affine_tile(const EncodeArgs& A, const T* __rest
 // K and V tiles of the chunk: blockIdx.z < num_seqs encodes K, the rest V.
 template <int D, int N, typename T, int KB, int VB>
 __global__ void __launch_bounds__(N) encode_affine_kernel(EncodeArgs A) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
   const bool is_v = static_cast<int>(blockIdx.z) >= A.num_seqs;
   const int u = blockIdx.x, head = blockIdx.y, b = blockIdx.z - (is_v ? A.num_seqs : 0);

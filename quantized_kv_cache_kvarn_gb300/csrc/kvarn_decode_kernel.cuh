@@ -101,8 +101,13 @@ struct DecShape {
   static constexpr int XS = 2 * (N / 8) + 2;  // exchanged per lane: partial scores, two timeout flags
   static constexpr int XBUF = HV == 2 ? UNITS * 2 * 32 * XS * 4 : 0;
   static constexpr int OFF_BARS = RING, OFF_QROT = RING + UNITS * 2 * 8, OFF_XBUF = OFF_QROT + 8 * D * 4;
-  static constexpr int SMEM = OFF_XBUF + XBUF;
-  static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "merge scratch must fit in the slots");
+  // the raw-record warps' partials: in the slots, or past the rest where the
+  // slots are smaller (head_dim 256, 64-token tiles)
+  static constexpr int RAW_MRG = W * 8 * (D + 2) * 4;
+  static constexpr int OFF_RAW_MRG = RAW_MRG <= RING ? 0 : OFF_XBUF + XBUF;
+  static constexpr int SMEM = OFF_XBUF + XBUF + (RAW_MRG <= RING ? 0 : RAW_MRG);
+  static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "tile merge scratch must fit in the slots");
+  static_assert(W * 40 <= 8 * D, "raw-record weight exchange must fit in the query rows");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
   static constexpr bool GATHER = parts_gather(D, N, KP, VP, KB, VB);
@@ -208,121 +213,230 @@ __device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j,
 // the Q tokens under verification), and the committed prefix shared by all.
 __device__ __forceinline__ int visible_len(int len, int Q, int j) { return max(0, len - Q + 1 + j); }
 
-// Raw records of a row: the sink rows [0, min(sink, visible)) and the tail rows
-// for tokens [committed, visible); dense attention in the original basis, one
-// warp per row, one pass with a running maximum (no per-token buffer, so the
-// record lengths are bounded only by their buffers).
-template <int D, typename T>
-__device__ __forceinline__ void raw_segment(const T* kp, const T* vp, int count, const float* qv, float& mx,
-                                            float& l, float* acc) {
-  constexpr int E = D / 32;
-  constexpr int U = D == 128 ? 8 : 4;  // tokens in flight per step
-  const int lane = threadIdx.x & 31;
-  int tau = 0;
-  for (; tau + U <= count; tau += U) {
-    float kv[U][E], vv[U][E], dot[U];
+// ------------------------------------------------------------- raw records
+// E consecutive fp16 or bf16 elements as raw bits (converted at use, so that a
+// prefetched row holds half the registers of its floats).
+template <int E>
+struct RawRow {
+  uint32_t w[E / 2];
+};
+template <int E>
+__device__ __forceinline__ RawRow<E> raw_load(const void* p) {
+  RawRow<E> r;
+  if constexpr (E == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    r.w[0] = u.x;
+    r.w[1] = u.y;
+  } else {
+    static_assert(E % 8 == 0, "vector width");
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      load_vec<T, E>(kp + static_cast<int64_t>(tau + u) * D + lane * E, kv[u]);
-      load_vec<T, E>(vp + static_cast<int64_t>(tau + u) * D + lane * E, vv[u]);
+    for (int k = 0; k < E / 8; ++k) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + k);
+      r.w[4 * k] = u.x;
+      r.w[4 * k + 1] = u.y;
+      r.w[4 * k + 2] = u.z;
+      r.w[4 * k + 3] = u.w;
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      dot[u] = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) dot[u] = fmaf(qv[e], kv[u][e], dot[u]);
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1)
-#pragma unroll
-      for (int u = 0; u < U; ++u) dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], o);  // same in every lane
-    float mn = mx;
-#pragma unroll
-    for (int u = 0; u < U; ++u) mn = fmaxf(mn, dot[u]);
-    const float sc = exp2f(mx - mn);
-    l *= sc;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] *= sc;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float p = exp2f(dot[u] - mn);
-      l += p;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vv[u][e], acc[e]);
-    }
-    mx = mn;
   }
-  for (; tau < count; ++tau) {
-    float kv[E], vv[E];
-    load_vec<T, E>(kp + static_cast<int64_t>(tau) * D + lane * E, kv);
-    load_vec<T, E>(vp + static_cast<int64_t>(tau) * D + lane * E, vv);
-    float dot = 0.f;
+  return r;
+}
+template <int E>
+__device__ __forceinline__ void raw_floats(const RawRow<E>& r, bool bf16, float* out) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kv[e], dot);
-    dot = warp_sum_xor(dot, 1, 32);
-    const float mn = fmaxf(mx, dot);
-    const float sc = exp2f(mx - mn), p = exp2f(dot - mn);
-    l = fmaf(l, sc, p);
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], sc, p * vv[e]);
-    mx = mn;
+  for (int k = 0; k < E / 2; ++k) {
+    float2 f;
+    if (bf16)
+      f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.w[k]));
+    else
+      f = __half22float2(*reinterpret_cast<const __half2*>(&r.w[k]));
+    out[2 * k] = f.x;
+    out[2 * k + 1] = f.y;
   }
 }
 
-// Raw split `chunk` covers raw tokens [chunk * kRawChunk, +kRawChunk) of the
-// row's raw list: its sink rows, then its tail rows.
+// Raw (sink and tail) records of a unit: dense attention in the original
+// basis, in fp32 on the CUDA cores. Row r of the unit (a (head, query token)
+// pair) attends to the raw tokens at positions below its visible length: the
+// sink rows [0, min(sink, visible)) and the tail rows for tokens [committed,
+// visible). All rows of the unit share one raw list, the sink rows of the
+// longest row then its tail rows, masked per row by position; raw split
+// `chunk` covers list entries [chunk * kRawChunk, +kRawChunk). The CTA's W
+// warps take consecutive pieces of the chunk, each warp scoring every row of
+// the unit against each record row it loads (one load per record row, not
+// one per query row): per step of four records a lane forms its channels'
+// products for the 8 x 4 (row, record) pairs, and a reduce-scatter over the
+// warp leaves lane l with the whole score of pair l (row l / 4, record
+// l % 4). Online softmax per row in base 2, the weights exchanged through
+// shared memory, the warps' partials merged at the end (`mrg`: scratch that
+// aliases the page slots where they are large enough, which no copy touches
+// before the tile loop starts).
 template <int D, int N, int W>
-__device__ void tail_partials(const DecArgs& A, int b, int kvh, const RowMap& R, int len, int sink,
-                              int committed, int chunk) {
-  constexpr int E = D / 32;
+__device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* pxbuf, int b, int kvh, const RowMap& R,
+                              int len, int sink, int committed, int chunk) {
+  constexpr int E = D / 32, U = 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int r = warp; r < R.n; r += W) {
-    const int j = R.query(A, r), hq = kvh * A.G + R.head(A, r);
-    const int vis = visible_len(len, A.Q, j);
-    const int n_sink = min(sink, vis), n_tail = max(0, vis - committed);
-    const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
-    const int s_cnt = max(0, min(c1, n_sink) - c0), t0 = max(c0, n_sink) - n_sink, t_cnt = max(0, c1 - max(c0, n_sink));
-    float* part = part_of(A, D, b, j, hq, A.tile_slots + chunk);
-    const bool miss = (t_cnt > 0 && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
-                      (s_cnt > 0 && (A.sink_k == nullptr || A.sink_v == nullptr));
-    if ((t_cnt <= 0 && s_cnt <= 0) || miss) {
-      if (miss && lane == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
-      write_empty(part, D, lane);
-      continue;
-    }
-    float qv[E];
-    const int64_t qoff = (static_cast<int64_t>(b * A.Q + j) * A.Hq + hq) * D + lane * E;
-    load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, qv);
-#pragma unroll
-    for (int e = 0; e < E; ++e) qv[e] *= A.kappa;
-    float mx = -INFINITY, l = 0.f, acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    if (s_cnt > 0) {
-      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N) + c0;
-      if (A.bf16)
-        raw_segment<D>(static_cast<const __nv_bfloat16*>(A.sink_k) + row0 * D,
-                       static_cast<const __nv_bfloat16*>(A.sink_v) + row0 * D, s_cnt, qv, mx, l, acc);
-      else
-        raw_segment<D>(static_cast<const __half*>(A.sink_k) + row0 * D, static_cast<const __half*>(A.sink_v) + row0 * D,
-                       s_cnt, qv, mx, l, acc);
-    }
-    if (t_cnt > 0) {
-      const int64_t row0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap + t0;
-      if (A.bf16)
-        raw_segment<D>(static_cast<const __nv_bfloat16*>(A.tail_k) + row0 * D,
-                       static_cast<const __nv_bfloat16*>(A.tail_v) + row0 * D, t_cnt, qv, mx, l, acc);
-      else
-        raw_segment<D>(static_cast<const __half*>(A.tail_k) + row0 * D, static_cast<const __half*>(A.tail_v) + row0 * D,
-                       t_cnt, qv, mx, l, acc);
-    }
-    if (lane == 0) {
-      part[0] = mx;
-      part[1] = l;
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) part[4 + lane * E + e] = acc[e];
+  const int my_r = lane >> 2, my_u = lane & 3;
+  // the longest row's list bounds everything read
+  int vis_max = 0;
+  for (int r = 0; r < R.n; ++r) vis_max = max(vis_max, visible_len(len, A.Q, R.query(A, r)));
+  const int n_sink = min(sink, vis_max), n_tail = max(0, vis_max - committed);
+  const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
+  const bool miss = (c1 > max(c0, n_sink) && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
+                    (min(c1, n_sink) > c0 && (A.sink_k == nullptr || A.sink_v == nullptr));
+  if (c1 <= c0 || miss) {
+    if (miss && threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
+    for (int r = warp; r < R.n; r += W)
+      write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), A.tile_slots + chunk), D, lane);
+    return;
   }
+  // this lane's channels of every row's query, kappa-scaled (zero past R.n)
+  float q[8][E];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (r < R.n) {
+      const int64_t qoff =
+          (static_cast<int64_t>(b * A.Q + R.query(A, r)) * A.Hq + kvh * A.G + R.head(A, r)) * D + lane * E;
+      load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, q[r]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) q[r][e] *= A.kappa;
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) q[r][e] = 0.f;
+    }
+  }
+  const int my_vis = my_r < R.n ? visible_len(len, A.Q, R.query(A, my_r)) : 0;
+  // list entry i: its token position and record row
+  const int64_t sink0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
+  const int64_t tail0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
+  auto row_ptr = [&](int i, bool v) -> const char* {
+    const void* base = i < n_sink ? (v ? A.sink_v : A.sink_k) : (v ? A.tail_v : A.tail_k);
+    const int64_t row = i < n_sink ? sink0 + i : tail0 + (i - n_sink);
+    return static_cast<const char*>(base) + 2 * (row * D + lane * E);
+  };
+  auto position = [&](int i) { return i < n_sink ? i : committed + (i - n_sink); };
+  // this warp's piece of the chunk, a multiple of U records
+  const int per = (c1 - c0 + W * U - 1) / (W * U) * U;
+  const int w0 = c0 + warp * per, w1 = min(c1, w0 + per);
+
+  float acc[8][E];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+  float m = -INFINITY, l = 0.f;  // row my_r (same in its four lanes)
+  RawRow<E> kb[U], vb[U];
+  auto fetch = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (i0 + u < w1) {
+        kb[u] = raw_load<E>(row_ptr(i0 + u, false));
+        vb[u] = raw_load<E>(row_ptr(i0 + u, true));
+      } else {
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k) kb[u].w[k] = vb[u].w[k] = 0u;
+      }
+    }
+  };
+  if (w0 < w1) fetch(w0);
+  for (int i0 = w0; i0 < w1; i0 += U) {
+    RawRow<E> kc[U], vc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      kc[u] = kb[u];
+      vc[u] = vb[u];
+    }
+    if (i0 + U < w1) fetch(i0 + U);  // the next step's records load during this one
+    // partial products of pair (r, u) over this lane's channels
+    float v[32];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float kf[E];
+      raw_floats<E>(kc[u], A.bf16, kf);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) d = fmaf(q[r][e], kf[e], d);
+        v[4 * r + u] = d;
+      }
+    }
+    // reduce-scatter: at the stage of offset o a lane keeps the half of its
+    // values that its bit o selects and adds its partner's copy of that half
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float keep = up ? v[i + o] : v[i], give = up ? v[i] : v[i + o];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+      }
+    }
+    const int i = i0 + my_u;
+    const float s = (i < w1 && position(i) < my_vis) ? v[0] : -INFINITY;
+    const float mx = fmaxf(fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1)),
+                           fmaxf(__shfl_xor_sync(0xffffffffu, s, 2), __shfl_xor_sync(0xffffffffu, s, 3)));
+    const float m_new = fmaxf(m, mx);
+    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+    const float p = s == -INFINITY ? 0.f : exp2f(s - m_new);
+    l = fmaf(l, alpha, warp_sum_xor(p, 1, 4));
+    m = m_new;
+    // weights and rescales of every row to every lane
+    pxbuf[lane] = p;
+    if (my_u == 0) pxbuf[32 + my_r] = alpha;
+    __syncwarp();
+    float vf[U][E];
+#pragma unroll
+    for (int u = 0; u < U; ++u) raw_floats<E>(vc[u], A.bf16, vf[u]);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float4 pr = *reinterpret_cast<const float4*>(pxbuf + 4 * r);
+      const float al = pxbuf[32 + r];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        float a = acc[r][e] * al;
+        a = fmaf(pr.x, vf[0][e], a);
+        a = fmaf(pr.y, vf[1][e], a);
+        a = fmaf(pr.z, vf[2][e], a);
+        acc[r][e] = fmaf(pr.w, vf[3][e], a);
+      }
+    }
+    __syncwarp();
+  }
+  // ---- merge the warps' pieces per row
+  float* mrg = reinterpret_cast<float*>(mrg_smem);
+  float* mw = mrg + warp * 8 * (D + 2);
+  if (my_u == 0) {
+    mw[my_r * (D + 2)] = m;
+    mw[my_r * (D + 2) + 1] = l;
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int e = 0; e < E; ++e) mw[r * (D + 2) + 2 + lane * E + e] = acc[r][e];
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
+    const int r = idx / D, j = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + r) * (D + 2)]);
+    float a = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* x = mrg + (w * 8 + r) * (D + 2);
+        const float sc = exp2f(x[0] - M);
+        a = fmaf(x[2 + j], sc, a);
+        L = fmaf(x[1], sc, L);
+      }
+    }
+    float* part = part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), A.tile_slots + chunk);
+    part[4 + j] = a;
+    if (j == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+  }
+  __syncthreads();  // the scratch is read before the next item writes it
 }
 
 // Resident CTAs per SM the kernel is compiled for: 3 x 4 warps at head_dim
@@ -1012,8 +1126,8 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_
     const int64_t u = r / A.raw_splits;
     const int b = static_cast<int>(u / A.X), x = static_cast<int>(u % A.X);
     const int len = checked_len(A, b);
-    tail_partials<D, N, W>(A, b, x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N,
-                              committed_end(A, N, len), chunk);
+    tail_partials<D, N, W>(A, smem + S::OFF_RAW_MRG, reinterpret_cast<float*>(smem + S::OFF_QROT) + warp * 40, b, x % A.Hkv,
+                           RowMap(A, x / A.Hkv), len, A.sink_tiles * N, committed_end(A, N, len), chunk);
   }
 
   const int64_t total = tiles_before(A, N, A.num_seqs);

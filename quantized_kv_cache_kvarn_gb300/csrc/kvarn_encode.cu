@@ -112,7 +112,7 @@ cudaError_t launch_append_commit(const AppendParams& p, cudaStream_t st) {
 // rows (4-bit codes, one code set for keys and values).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(512)
     encode_latent_kernel(EncodeArgs A) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int u = blockIdx.x >> 1, b = blockIdx.y;
   if (A.tile_start[b] < 0) return;  // uniform over the cluster: both CTAs share b
   const unsigned char* src = static_cast<const unsigned char*>(A.x[0]) +

@@ -658,7 +658,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const unsigned 
 // V half and an SM mostly runs one of the two code paths.
 template <int D, int N, int KB = 4, int VB = 2, int SB = 4>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) encode_dense_kernel(EncodeArgs A) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   // the decode launched after a commit may be scheduled once every CTA here
   // has started; it waits for this grid's completion before it reads
   pdl_launch_dependents();
@@ -686,7 +686,7 @@ template <int D, int N>
 __global__ void __launch_bounds__(2 * D, D == 128 ? 2 : 1) append_commit_kernel(EncodeArgs A, const int32_t* seq_lens,
                                                               int32_t max_seq_len, unsigned char* tail_k,
                                                               unsigned char* tail_v) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
   const bool is_v = blockIdx.z == 1;
   const int head = blockIdx.x, b = blockIdx.y;
