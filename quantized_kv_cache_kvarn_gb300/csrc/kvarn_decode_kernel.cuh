@@ -261,21 +261,25 @@ __device__ __forceinline__ void raw_floats(const RawRow<E>& r, bool bf16, float*
 // visible). All rows of the unit share one raw list, the sink rows of the
 // longest row then its tail rows, masked per row by position; raw split
 // `chunk` covers list entries [chunk * kRawChunk, +kRawChunk). The CTA's W
-// warps take consecutive pieces of the chunk, each warp scoring every row of
-// the unit against each record row it loads (one load per record row, not
-// one per query row): per step of four records a lane forms its channels'
-// products for the 8 x 4 (row, record) pairs, and a reduce-scatter over the
-// warp leaves lane l with the whole score of pair l (row l / 4, record
-// l % 4). Online softmax per row in base 2, the weights exchanged through
+// warps take consecutive pieces of the chunk, each warp scoring the rows of
+// the unit against each record row it loads (one load per record row and
+// pass, not one per query row; one pass of eight rows at head_dim 128, two of
+// four at 256): per step of four records a lane forms its channels'
+// products for the rows x 4 (row, record) pairs, and a reduce-scatter over
+// the warp leaves lane l with the whole score of pair l mod (4 x rows) (row
+// of the pass (l mod (4 x rows)) / 4, record l % 4). Online softmax per row in base 2, the weights exchanged through
 // shared memory, the warps' partials merged at the end (`mrg`: scratch that
 // aliases the page slots where they are large enough, which no copy touches
 // before the tile loop starts).
 template <int D, int N, int W>
 __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* pxbuf, int b, int kvh, const RowMap& R,
                               int len, int sink, int committed, int chunk) {
-  constexpr int E = D / 32, U = 4;
+  // rows per pass (the query and accumulator rows a lane holds): all eight
+  // at head_dim 128, four at 256 (two passes over the records, which keeps
+  // the kernel's register budget of the tile loop)
+  constexpr int E = D / 32, U = 4, RP = D == 256 ? 4 : 8, PAIRS = RP * U;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int my_r = lane >> 2, my_u = lane & 3;
+  const int my_r = (lane & (PAIRS - 1)) >> 2, my_u = lane & 3;  // pair of the lane after the reduce-scatter
   // the longest row's list bounds everything read
   int vis_max = 0;
   for (int r = 0; r < R.n; ++r) vis_max = max(vis_max, visible_len(len, A.Q, R.query(A, r)));
@@ -289,22 +293,6 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
       write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), A.tile_slots + chunk), D, lane);
     return;
   }
-  // this lane's channels of every row's query, kappa-scaled (zero past R.n)
-  float q[8][E];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (r < R.n) {
-      const int64_t qoff =
-          (static_cast<int64_t>(b * A.Q + R.query(A, r)) * A.Hq + kvh * A.G + R.head(A, r)) * D + lane * E;
-      load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, q[r]);
-#pragma unroll
-      for (int e = 0; e < E; ++e) q[r][e] *= A.kappa;
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) q[r][e] = 0.f;
-    }
-  }
-  const int my_vis = my_r < R.n ? visible_len(len, A.Q, R.query(A, my_r)) : 0;
   // list entry i: its token position and record row
   const int64_t sink0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
   const int64_t tail0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
@@ -317,102 +305,128 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
   // this warp's piece of the chunk, a multiple of U records
   const int per = (c1 - c0 + W * U - 1) / (W * U) * U;
   const int w0 = c0 + warp * per, w1 = min(c1, w0 + per);
-
-  float acc[8][E];
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
-  float m = -INFINITY, l = 0.f;  // row my_r (same in its four lanes)
-  RawRow<E> kb[U], vb[U];
-  auto fetch = [&](int i0) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (i0 + u < w1) {
-        kb[u] = raw_load<E>(row_ptr(i0 + u, false));
-        vb[u] = raw_load<E>(row_ptr(i0 + u, true));
-      } else {
-#pragma unroll
-        for (int k = 0; k < E / 2; ++k) kb[u].w[k] = vb[u].w[k] = 0u;
-      }
-    }
-  };
-  if (w0 < w1) fetch(w0);
-  for (int i0 = w0; i0 < w1; i0 += U) {
-    RawRow<E> kc[U], vc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      kc[u] = kb[u];
-      vc[u] = vb[u];
-    }
-    if (i0 + U < w1) fetch(i0 + U);  // the next step's records load during this one
-    // partial products of pair (r, u) over this lane's channels
-    float v[32];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float kf[E];
-      raw_floats<E>(kc[u], A.bf16, kf);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        float d = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) d = fmaf(q[r][e], kf[e], d);
-        v[4 * r + u] = d;
-      }
-    }
-    // reduce-scatter: at the stage of offset o a lane keeps the half of its
-    // values that its bit o selects and adds its partner's copy of that half
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < o; ++i) {
-        const float keep = up ? v[i + o] : v[i], give = up ? v[i] : v[i + o];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
-      }
-    }
-    const int i = i0 + my_u;
-    const float s = (i < w1 && position(i) < my_vis) ? v[0] : -INFINITY;
-    const float mx = fmaxf(fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1)),
-                           fmaxf(__shfl_xor_sync(0xffffffffu, s, 2), __shfl_xor_sync(0xffffffffu, s, 3)));
-    const float m_new = fmaxf(m, mx);
-    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
-    const float p = s == -INFINITY ? 0.f : exp2f(s - m_new);
-    l = fmaf(l, alpha, warp_sum_xor(p, 1, 4));
-    m = m_new;
-    // weights and rescales of every row to every lane
-    pxbuf[lane] = p;
-    if (my_u == 0) pxbuf[32 + my_r] = alpha;
-    __syncwarp();
-    float vf[U][E];
-#pragma unroll
-    for (int u = 0; u < U; ++u) raw_floats<E>(vc[u], A.bf16, vf[u]);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float4 pr = *reinterpret_cast<const float4*>(pxbuf + 4 * r);
-      const float al = pxbuf[32 + r];
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        float a = acc[r][e] * al;
-        a = fmaf(pr.x, vf[0][e], a);
-        a = fmaf(pr.y, vf[1][e], a);
-        a = fmaf(pr.z, vf[2][e], a);
-        acc[r][e] = fmaf(pr.w, vf[3][e], a);
-      }
-    }
-    __syncwarp();
-  }
-  // ---- merge the warps' pieces per row
   float* mrg = reinterpret_cast<float*>(mrg_smem);
   float* mw = mrg + warp * 8 * (D + 2);
-  if (my_u == 0) {
-    mw[my_r * (D + 2)] = m;
-    mw[my_r * (D + 2) + 1] = l;
+
+  for (int r0 = 0; r0 < R.n; r0 += RP) {
+    // this lane's channels of the pass's query rows, kappa-scaled (zero past R.n)
+    float q[RP][E];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      if (r0 + r < R.n) {
+        const int64_t qoff = (static_cast<int64_t>(b * A.Q + R.query(A, r0 + r)) * A.Hq + kvh * A.G +
+                              R.head(A, r0 + r)) * D + lane * E;
+        load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, q[r]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) q[r][e] *= A.kappa;
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) q[r][e] = 0.f;
+      }
+    }
+    const int my_vis = r0 + my_r < R.n ? visible_len(len, A.Q, R.query(A, r0 + my_r)) : 0;
+    float acc[RP][E];
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+    float m = -INFINITY, l = 0.f;  // row r0 + my_r (the same in every lane of the row)
+    RawRow<E> kb[U], vb[U];
+    auto fetch = [&](int i0) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (i0 + u < w1) {
+          kb[u] = raw_load<E>(row_ptr(i0 + u, false));
+          vb[u] = raw_load<E>(row_ptr(i0 + u, true));
+        } else {
+#pragma unroll
+          for (int k = 0; k < E / 2; ++k) kb[u].w[k] = vb[u].w[k] = 0u;
+        }
+      }
+    };
+    if (w0 < w1) fetch(w0);
+    for (int i0 = w0; i0 < w1; i0 += U) {
+      RawRow<E> kc[U], vc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        kc[u] = kb[u];
+        vc[u] = vb[u];
+      }
+      if (i0 + U < w1) fetch(i0 + U);  // the next step's records load during this one
+      // partial products of pair (r, u) over this lane's channels
+      float v[PAIRS];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float kf[E];
+        raw_floats<E>(kc[u], A.bf16, kf);
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) d = fmaf(q[r][e], kf[e], d);
+          v[4 * r + u] = d;
+        }
+      }
+      // whole sums over the lanes above the pair count, then a
+      // reduce-scatter: at the stage of offset o a lane keeps the half of
+      // its values that its bit o selects and adds its partner's copy of it
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        if (o >= PAIRS) {
+#pragma unroll
+          for (int i = 0; i < PAIRS; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+        } else {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float keep = up ? v[i + o] : v[i], give = up ? v[i] : v[i + o];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+          }
+        }
+      }
+      const int i = i0 + my_u;
+      const float s = (i < w1 && position(i) < my_vis) ? v[0] : -INFINITY;
+      const float mx = fmaxf(fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1)),
+                             fmaxf(__shfl_xor_sync(0xffffffffu, s, 2), __shfl_xor_sync(0xffffffffu, s, 3)));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+      const float p = s == -INFINITY ? 0.f : exp2f(s - m_new);
+      l = fmaf(l, alpha, warp_sum_xor(p, 1, 4));
+      m = m_new;
+      // weights and rescales of every row to every lane (lanes holding the
+      // same pair store the same value)
+      pxbuf[lane & (PAIRS - 1)] = p;
+      if (my_u == 0) pxbuf[32 + my_r] = alpha;
+      __syncwarp();
+      float vf[U][E];
+#pragma unroll
+      for (int u = 0; u < U; ++u) raw_floats<E>(vc[u], A.bf16, vf[u]);
+#pragma unroll
+      for (int r = 0; r < RP; ++r) {
+        const float4 pr = *reinterpret_cast<const float4*>(pxbuf + 4 * r);
+        const float al = pxbuf[32 + r];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          float a = acc[r][e] * al;
+          a = fmaf(pr.x, vf[0][e], a);
+          a = fmaf(pr.y, vf[1][e], a);
+          a = fmaf(pr.z, vf[2][e], a);
+          acc[r][e] = fmaf(pr.w, vf[3][e], a);
+        }
+      }
+      __syncwarp();
+    }
+    // this warp's piece of the pass's rows into the merge scratch
+    if (my_u == 0 && lane < PAIRS) {
+      mw[(r0 + my_r) * (D + 2)] = m;
+      mw[(r0 + my_r) * (D + 2) + 1] = l;
+    }
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+#pragma unroll
+      for (int e = 0; e < E; ++e) mw[(r0 + r) * (D + 2) + 2 + lane * E + e] = acc[r][e];
   }
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int e = 0; e < E; ++e) mw[r * (D + 2) + 2 + lane * E + e] = acc[r][e];
+  // ---- merge the warps' pieces per row
   __syncthreads();
   for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
     const int r = idx / D, j = idx % D;
