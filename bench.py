@@ -797,6 +797,11 @@ def run_kvarn(args):
         assert kv.read_error_flags(H.err) == 0
         return
 
+    # the clock sampler starts first, so that the warm-up steps run right
+    # before the timed region (an idle GPU lowers its clocks within a few
+    # hundred milliseconds)
+    clocks = ClockSampler() if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
     for _ in range(args.warmup):
         H.encode()
         H.decode()
@@ -807,8 +812,6 @@ def run_kvarn(args):
     # event recorded between two kernels holds the second one back by a few
     # microseconds, about 12 us per step with three of them)
     evs = [(ev(), ev(), None) for _ in range(args.steps)]
-    clocks = ClockSampler() if rank == 0 else None
-    time.sleep(0.3 if clocks else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
