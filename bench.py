@@ -49,6 +49,9 @@ EXTRA_WORKLOADS = ("toy", "g64", "hybrid", "mla")
 # the dense-32B workload through the affine comparison codec (gmlx page: an
 # fp16 scale and offset per group of 64; compared at 4 and 8 bits)
 EXTRA_AFFINE = (4, 8)
+# speculative verification (query tokens per sequence) and the raw-record
+# window (sink, recent) on the default workload
+EXTRA_VERIFY = (("verify4", 4, 0, 0), ("window", 1, 128, 1024))
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = {"dense": ["kvarn_decode.cu", "kvarn_decode_kernel.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"],
                   "mla": ["kvarn_mla.cu", "kvarn_tcgen05.cuh", "kvarn_common.cuh", "kvarn_merge.cuh"]}
@@ -642,7 +645,7 @@ def roofline_of(H, wl, dec_ms, traffic=None, kernel=None):
             "traffic": traffic, "kernel": kernel, "peak_kind": peak_kind, "bytes_per_launch": H.packed}
 
 
-def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4):
+def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4, queries=1, sink=0, recent=0):
     """One more workload in the same run: its step (commit + decode, K back
     to back), its decode call (DECODE_CALLS back to back) and its commit,
     with the roofline of the decode call. A workload whose packed reads fit
@@ -652,6 +655,8 @@ def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4):
     wl = W.WORKLOADS[name]
     if codec == "affine":
         H = DenseHarness(kv, W, wl, dev, rank, widths=(bits, bits, 2), codec="affine")
+    elif queries > 1 or sink or recent:
+        H = VerifyHarness(kv, W, wl, dev, rank, queries, sink, recent)
     else:
         H = LatentHarness(kv, W, wl, dev, rank) if wl.rope_dim else DenseHarness(kv, W, wl, dev, rank)
     stream = torch.cuda.current_stream()
@@ -716,10 +721,14 @@ def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4):
     desc = _workload_desc(wl)
     if codec == "affine":
         desc = desc.replace("K4V2", f"affine K{bits}V{bits} (groups of 64, fp16 scale and offset)")
+    if queries > 1:
+        desc += f", {queries} query tokens per sequence (kvarn_decode_verify)"
+    if sink or recent:
+        desc += f", raw sink {sink} + recent {recent} (kvarn_decode_window)"
     out = {"workload": desc, "ms_per_step": round(ms_step, 5),
            "value": round(H.packed / (ms_step * 1e-3) / 1e9, 2), "unit": "GB/s",
            "decode_ms": round(dec_ms, 5), "commit_ms": round(com_ms, 5), "commit_tokens": H.encode_tokens,
-           "decode_tokens_per_s": round(wl.num_seqs / (ms_step * 1e-3), 1),
+           "decode_tokens_per_s": round(wl.num_seqs * queries / (ms_step * 1e-3), 1),
            "l2": ("packed reads fit in L2: one step per timing, L2 flushed between steps (median of K)" if small
                   else f"inputs larger than L2 ({H.packed / 1e6:.0f} MB of packed KV read per step)"),
            "roofline": roofline_of(H, wl, dec_ms, kernel=f"decode call, {'median of K single' if small else str(DECODE_CALLS) + ' back-to-back'} calls")}
@@ -1018,6 +1027,9 @@ def run_kvarn(args):
         for bits in EXTRA_AFFINE:
             line["workloads"][f"affine{bits}"] = measure_extra(kv, W, WORKLOAD, dev, rank, args.steps, args.warmup,
                                                                codec="affine", bits=bits)
+        for key, q, sk, rc in EXTRA_VERIFY:
+            line["workloads"][key] = measure_extra(kv, W, WORKLOAD, dev, rank, args.steps, args.warmup,
+                                                   queries=q, sink=sk, recent=rc)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
