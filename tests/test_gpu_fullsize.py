@@ -54,9 +54,12 @@ def _encode_dense(case, wl, lay, cache, err, chunk_from=None):
 
 
 @pytest.mark.parametrize("name,pairs,chunk", [
-    ("dense32b", [(3, 5), (30, 0)], None),
-    ("g64", [(1, 2), (17, 7)], None),
-    ("hybrid", [(5, 3)], (61440, 4096)),
+    # pairs spread over the batch (first, middle and last sequences, several
+    # KV heads), so that the sampled units sit in different CTA ranges of
+    # the full-size split plan
+    ("dense32b", [(0, 0), (3, 5), (17, 3), (30, 0), (31, 7)], None),
+    ("g64", [(0, 0), (1, 2), (17, 7), (31, 4)], None),
+    ("hybrid", [(0, 0), (5, 3), (7, 1)], (61440, 4096)),
 ])
 def test_dense_fullsize(name, pairs, chunk):
     wl = W.WORKLOADS[name]
