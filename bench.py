@@ -645,6 +645,21 @@ def roofline_of(H, wl, dec_ms, traffic=None, kernel=None):
             "traffic": traffic, "kernel": kernel, "peak_kind": peak_kind, "bytes_per_launch": H.packed}
 
 
+def captured_traffic(wl):
+    """DRAM bytes per decode launch of workload `wl` at its preset widths, one
+    query token and no raw records, from the committed ncu capture, while
+    the decode kernel's sources hash to the captured digest; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as fh:
+            entry = json.load(fh).get(wl.name)
+        kind = "mla" if wl.rope_dim else "dense"
+        if entry and entry.get("source_digest") == decode_source_digest(kind):
+            return entry.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
 def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4, queries=1, sink=0, recent=0):
     """One more workload in the same run: its step (commit + decode, K back
     to back), its decode call (DECODE_CALLS back to back) and its commit,
@@ -731,7 +746,10 @@ def measure_extra(kv, W, name, dev, rank, steps, warmup, codec="kvarn", bits=4, 
            "decode_tokens_per_s": round(wl.num_seqs * queries / (ms_step * 1e-3), 1),
            "l2": ("packed reads fit in L2: one step per timing, L2 flushed between steps (median of K)" if small
                   else f"inputs larger than L2 ({H.packed / 1e6:.0f} MB of packed KV read per step)"),
-           "roofline": roofline_of(H, wl, dec_ms, kernel=f"decode call, {'median of K single' if small else str(DECODE_CALLS) + ' back-to-back'} calls")}
+           "roofline": roofline_of(H, wl, dec_ms,
+                                   traffic=(captured_traffic(wl) if codec == "kvarn" and queries == 1
+                                            and not (sink or recent) else None),
+                                   kernel=f"decode call, {'median of K single' if small else str(DECODE_CALLS) + ' back-to-back'} calls")}
     del H
     torch.cuda.empty_cache()
     return out
@@ -934,19 +952,10 @@ def run_kvarn(args):
         dist.destroy_process_group()
         return
 
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as fh:
-            tr = json.load(fh)
-        entry = tr.get(wl.name)
-        kind = "mla" if wl.rope_dim else "dense"
-        # the capture is of the workload's own decode: the preset widths, one
-        # query token, no raw records (the append step decodes the same pages)
-        same = widths == (4, 2, 4) and args.queries == 1 and not (args.sink or args.recent) and args.codec == "kvarn"
-        if entry and entry.get("source_digest") == decode_source_digest(kind) and not args.num_seqs and same:
-            traffic = entry.get("bytes_per_launch")
-    except Exception:
-        pass
+    # the capture is of the workload's own decode: the preset widths, one
+    # query token, no raw records (the append step decodes the same pages)
+    same = widths == (4, 2, 4) and args.queries == 1 and not (args.sink or args.recent) and args.codec == "kvarn"
+    traffic = captured_traffic(wl) if same and not args.num_seqs else None
 
     cpu = None
     if world == 1 and not args.no_cpu and not (args.sink or args.recent) and args.codec == "kvarn":
