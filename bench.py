@@ -113,6 +113,71 @@ def _workload_desc(wl):
 
 
 # ----------------------------------------------------------------- clocks
+class E2E:
+    """One step end to end: its inputs copied from pinned host memory, the
+    step through the public API, its output copied back. The copies run on
+    their own streams, double-buffered on the device, so that a step's input
+    copy overlaps the step before and its output copy the step after; every
+    step still moves its own bytes both ways.
+
+    ins: (pinned host tensor, [device buffer of slot 0, of slot 1]);
+    outs: ([device buffer of slot 0, of slot 1], [pinned host buffers]);
+    step(slot): the step on the current stream, reading ins[...][1][slot],
+    writing outs[...][0][slot]."""
+
+    def __init__(self, ins, outs, step):
+        import torch
+        self.ins, self.outs, self.step = ins, outs, step
+        self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in ins)
+        self.d2h_bytes = sum(d[0].numel() * d[0].element_size() for d, _ in outs)
+        self.up, self.down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = torch.cuda.Event
+        self.ev_in, self.ev_done, self.ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    @staticmethod
+    def inp(src, dev=None):
+        import torch
+        dev = src.device if dev is None else dev
+        host = src.detach().cpu().contiguous().pin_memory()
+        return host, [torch.empty(host.shape, dtype=host.dtype, device=dev) for _ in range(2)]
+
+    @staticmethod
+    def outp(like):
+        import torch
+        return ([like, torch.empty_like(like)],
+                [torch.empty(like.shape, dtype=like.dtype).pin_memory() for _ in range(2)])
+
+    def run(self, steps, stream):
+        """`steps` steps; everything they issue is ordered before the next
+        work recorded on `stream`."""
+        import torch
+        start = torch.cuda.Event()
+        start.record(stream)
+        self.up.wait_event(start)
+        self.down.wait_event(start)
+        for t in range(steps):
+            s = t % 2
+            with torch.cuda.stream(self.up):
+                if t >= 2:
+                    self.up.wait_event(self.ev_done[s])  # step t - 2 has read slot s
+                for h, d in self.ins:
+                    d[s].copy_(h, non_blocking=True)
+                self.ev_in[s].record(self.up)
+            stream.wait_event(self.ev_in[s])
+            if t >= 2:
+                stream.wait_event(self.ev_out[s])  # slot s's output of step t - 2 has left
+            with torch.cuda.stream(stream):
+                self.step(s)
+            self.ev_done[s].record(stream)
+            with torch.cuda.stream(self.down):
+                self.down.wait_event(self.ev_done[s])
+                for d, h in self.outs:
+                    h[s].copy_(d[s], non_blocking=True)
+                self.ev_out[s].record(self.down)
+        for s in range(min(2, steps)):
+            stream.wait_event(self.ev_out[s])
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed
     region (read-only queries)."""
@@ -430,39 +495,31 @@ class DenseHarness:
 
     def e2e_setup(self):
         """Per step from pinned host memory: the queries, the newest token's K
-        and V (written into its slot) and the lengths; the output goes back."""
+        and V (written into its slot) and the lengths; the output goes back.
+        Device copies of the inputs and outputs are double-buffered (E2E)."""
         import torch
         c = self.case
-        q_h = c.q.cpu().pin_memory()
         pos = [L - 1 for L in self.lens]
         tok_k = torch.stack([c.k[b, :, p] for b, p in enumerate(pos)]).cpu().pin_memory()
         tok_v = torch.stack([c.v[b, :, p] for b, p in enumerate(pos)]).cpu().pin_memory()
-        lens_h = c.seq_lens.cpu().pin_memory()
-        out_h = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        q_d = torch.empty_like(c.q)
-        lens_d = torch.empty_like(c.seq_lens)
-        tok_d = torch.empty((2,) + tuple(tok_k.shape), dtype=tok_k.dtype, device=self.dev)
+        ins = [E2E.inp(c.q), E2E.inp(c.seq_lens), E2E.inp(tok_k, self.dev), E2E.inp(tok_v, self.dev)]
+        outs = [E2E.outp(self.out)]
         same = len(set(pos)) == 1
         bidx = torch.arange(len(pos), device=self.dev)
         pidx = torch.tensor(pos, device=self.dev)
 
-        def run():
-            q_d.copy_(q_h, non_blocking=True)
-            lens_d.copy_(lens_h, non_blocking=True)
-            tok_d[0].copy_(tok_k, non_blocking=True)
-            tok_d[1].copy_(tok_v, non_blocking=True)
+        def step(slot):
+            q_d, lens_d, tk, tv = (x[1][slot] for x in ins)
             if same:
-                c.k[:, :, pos[0]] = tok_d[0]
-                c.v[:, :, pos[0]] = tok_d[1]
+                c.k[:, :, pos[0]] = tk
+                c.v[:, :, pos[0]] = tv
             else:
-                c.k[bidx, :, pidx] = tok_d[0]
-                c.v[bidx, :, pidx] = tok_d[1]
+                c.k[bidx, :, pidx] = tk
+                c.v[bidx, :, pidx] = tv
             self.encode()
+            self.out = outs[0][0][slot]
             self.decode(q_d, lens_d)
-            out_h.copy_(self.out, non_blocking=True)
-        h2d = q_h.numel() * q_h.element_size() + lens_h.numel() * 4 + 2 * tok_k.numel() * tok_k.element_size()
-        d2h = out_h.numel() * 4
-        return run, h2d, d2h
+        return E2E(ins, outs, step)
 
 
 class VerifyHarness(DenseHarness):
@@ -542,20 +599,14 @@ class VerifyHarness(DenseHarness):
     def e2e_setup(self):
         """Per step from pinned host memory: the Q query rows and the lengths;
         the Q outputs go back."""
-        import torch
-        q_h = self.qv.cpu().pin_memory()
-        lens_h = self.case.seq_lens.cpu().pin_memory()
-        out_h = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        q_d = torch.empty_like(self.qv)
-        lens_d = torch.empty_like(self.case.seq_lens)
+        ins = [E2E.inp(self.qv), E2E.inp(self.case.seq_lens)]
+        outs = [E2E.outp(self.out)]
 
-        def run():
-            q_d.copy_(q_h, non_blocking=True)
-            lens_d.copy_(lens_h, non_blocking=True)
+        def step(slot):
             self.encode()
-            self.decode(q_d, lens_d)
-            out_h.copy_(self.out, non_blocking=True)
-        return run, q_h.numel() * q_h.element_size() + lens_h.numel() * 4, out_h.numel() * 4
+            self.out = outs[0][0][slot]
+            self.decode(ins[0][1][slot], ins[1][1][slot])
+        return E2E(ins, outs, step)
 
 
 class LatentHarness:
@@ -606,24 +657,20 @@ class LatentHarness:
         return None
 
     def e2e_setup(self):
-        import torch
+        """Per step from pinned host memory: the latent queries, the newest
+        token's latent (written into its slot) and the lengths; the output
+        goes back."""
         c = self.case
-        q_h = c.q_latent.cpu().pin_memory()
-        tok_h = c.latent[:, self.Lmax - 1].cpu().pin_memory()
-        lens_h = c.seq_lens.cpu().pin_memory()
-        out_h = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        q_d = torch.empty_like(c.q_latent)
-        lens_d = torch.empty_like(c.seq_lens)
+        ins = [E2E.inp(c.q_latent), E2E.inp(c.seq_lens), E2E.inp(c.latent[:, self.Lmax - 1].contiguous())]
+        outs = [E2E.outp(self.out)]
 
-        def run():
-            q_d.copy_(q_h, non_blocking=True)
-            lens_d.copy_(lens_h, non_blocking=True)
-            c.latent[:, self.Lmax - 1].copy_(tok_h, non_blocking=True)
+        def step(slot):
+            q_d, lens_d, tok_d = (x[1][slot] for x in ins)
+            c.latent[:, self.Lmax - 1].copy_(tok_d)
             self.encode()
+            self.out = outs[0][0][slot]
             self.decode(q_d, lens_d)
-            out_h.copy_(self.out, non_blocking=True)
-        h2d = q_h.numel() * 2 + lens_h.numel() * 4 + tok_h.numel() * 2
-        return run, h2d, out_h.numel() * 4
+        return E2E(ins, outs, step)
 
 
 # ---------------------------------------------------------------- main arm
@@ -908,16 +955,15 @@ def run_kvarn(args):
         del keep, run16
 
     # end to end through the public API with host buffers
-    run_e2e, h2d, d2h = H.e2e_setup()
-    for _ in range(3):
-        run_e2e()
+    e2e = H.e2e_setup()
+    e2e.run(3, stream)
     torch.cuda.synchronize()
     a.record(stream)
-    for _ in range(args.steps):
-        run_e2e()
+    e2e.run(args.steps, stream)
     b_.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b_) / args.steps
+    h2d, d2h = e2e.h2d_bytes, e2e.d2h_bytes
 
     # the same K steps captured once in a CUDA graph and replayed (every
     # launch takes host sizes and pointers, so the graph replays the step as
@@ -1016,7 +1062,9 @@ def run_kvarn(args):
         "roofline": roofline,
         "encode_roofline": encode_roofline,
         "e2e": {"value": round(world * H.packed / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "from and to pinned host memory every step, on their own streams, double-buffered on "
+                          "the device: a step's input copy overlaps the step before, its output copy the step after"},
         "gpu_launches": H.launches * args.steps,
         "graph": None if graph_ms is None else {
             "ms_per_step": round(graph_ms, 5),
@@ -1028,7 +1076,7 @@ def run_kvarn(args):
                  or widths != (4, 2, 4) or args.no_extra or args.codec != "kvarn")
     if plain and world == 1 and args.workload == WORKLOAD:
         # the other workloads of the same family, each measured on its own
-        del H, run_e2e, f
+        del H, e2e, f
         torch.cuda.empty_cache()
         line["workloads"] = {}
         for name in EXTRA_WORKLOADS:

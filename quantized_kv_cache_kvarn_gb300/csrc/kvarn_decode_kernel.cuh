@@ -1140,8 +1140,16 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_
     const int64_t u = r / A.raw_splits;
     const int b = static_cast<int>(u / A.X), x = static_cast<int>(u % A.X);
     const int len = checked_len(A, b);
-    tail_partials<D, N, W>(A, smem + S::OFF_RAW_MRG, reinterpret_cast<float*>(smem + S::OFF_QROT) + warp * 40, b, x % A.Hkv,
-                           RowMap(A, x / A.Hkv), len, A.sink_tiles * N, committed_end(A, N, len), chunk);
+    if constexpr (S::RAW) {
+      // the uncompressed pages hold every token: the raw splits stay empty
+      const RowMap R(A, x / A.Hkv);
+      for (int rr = warp; rr < R.n; rr += W)
+        write_empty(part_of(A, D, b, R.query(A, rr), (x % A.Hkv) * A.G + R.head(A, rr), A.tile_slots + chunk), D,
+                    lane);
+    } else {
+      tail_partials<D, N, W>(A, smem + S::OFF_RAW_MRG, reinterpret_cast<float*>(smem + S::OFF_QROT) + warp * 40, b,
+                             x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N, committed_end(A, N, len), chunk);
+    }
   }
 
   const int64_t total = tiles_before(A, N, A.num_seqs);
