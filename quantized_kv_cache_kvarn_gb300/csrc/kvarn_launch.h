@@ -121,19 +121,11 @@ inline int32_t row_groups(int32_t G, int32_t Q) { return (G * Q + 7) / 8; }
 // tail partial). Depends only on the arguments and the device's SM count.
 struct SplitPlan {
   int32_t tiles_per_split;
-  int32_t nsplit;      // splits over committed tiles
-  int32_t raw_splits;  // splits over the raw records (chunks of kRawChunk tokens; at least 1)
-  int32_t slots;       // nsplit + raw_splits
+  int32_t nsplit;  // splits over committed tiles
+  int32_t slots;   // nsplit + 1 (the tail)
 };
 
-constexpr int32_t kRawChunk = 128;  // raw (sink and tail) tokens per split
-
-// The plan with enough raw splits for up to raw_max raw tokens per row.
-inline SplitPlan with_raw_chunks(SplitPlan p, int32_t raw_max) {
-  p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
-  p.slots = p.nsplit + p.raw_splits;
-  return p;
-}
+constexpr int32_t kRawChunk = 128;  // raw (sink and tail) tokens per split of the dense decode
 
 // Plan of the compressed decode: `ctas` persistent CTAs share the flattened
 // list of compressed tiles (stream-K), each taking at least `min_tiles` of
