@@ -61,9 +61,9 @@
  *   as the low 2 bits of nibbles, which the e2m1 -> fp16 conversion turns
  *   into exact operands (code / 2), two per instruction.
  * Other widths (gmlx page, "The two schemes": kvarn widths 2, 3, 4, 5, 6, 8,
- * with separate widths for keys and values): with head_dim 128 and fp16
- * scales, k_bits and v_bits are each any of {2, 3, 4, 5, 6, 8}; with head_dim
- * 256 and fp16 scales, k_bits = v_bits in that set, or 4 and 2. A
+ * with separate widths for keys and values): k_bits and v_bits are each any
+ * of {2, 3, 4, 5, 6, 8} with head_dim 128 (fp16 or fp32 scales) and with
+ * head_dim 256 (fp16 scales; fp32 scales only for k_bits 4, v_bits 2). A
  * b-bit code is stored as planes, 2: [2], 3: [2, 1], 4: [4], 5: [4, 1],
  * 6: [4, 2], 8: [4, 4] (code = plane0 + 2^w0 plane1), each plane region
  * (2*D*w bytes per page, in order) placed by one rule for width w in
