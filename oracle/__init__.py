@@ -10,5 +10,7 @@ Modules:
   layout     byte layout of a cache page (the library's documented format)
   attention  decode attention over a paged cache, fp16 tail, fp16 bypass
   mla        the MLA latent-cache codec and decode
+  affine     the per-token affine comparison codec (groups of 64 channels,
+             fp16 scale and offset), its page layout and decode
 """
-from . import codec, layout, attention, mla  # noqa: F401
+from . import codec, layout, attention, mla, affine  # noqa: F401
