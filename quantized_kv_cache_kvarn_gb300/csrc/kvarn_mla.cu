@@ -369,10 +369,24 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
           // k (nibbles k, k + 4) is channels 32 w + 8 k + 2 t + {0, 1}
           const int tau = p >> 1, wp = p & 1, w = 2 * c + wp;
           const unsigned char* row = raw + (tau / 16) * kPB + (tau % 16) * (kDl / 2);
+          // token rows are 256 bytes apart (one bank set): the lanes of a
+          // warp read the four words in an order rotated by (tau / 2) % 4,
+          // so that one load instruction touches 16 banks instead of 4
+          const int rot = (tau >> 1) & 3;
+          uint32_t y[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int t = (j + rot) & 3;
+            y[j] = *reinterpret_cast<const uint32_t*>(row + 16 * ((4 * (w >> 2) + t) ^ (4 * (tau & 1))) + 4 * (w & 3));
+          }
+          // x[t] = y[(t - rot) mod 4], in two conditional rotations
           uint32_t x[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            x[t] = *reinterpret_cast<const uint32_t*>(row + 16 * ((4 * (w >> 2) + t) ^ (4 * (tau & 1))) + 4 * (w & 3));
+          for (int t = 0; t < 4; ++t) x[t] = (rot & 1) ? y[(t + 3) & 3] : y[t];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) y[t] = x[t];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) x[t] = (rot & 2) ? y[(t + 2) & 3] : y[t];
           unsigned char* bdst = (c / 4 == half) ? sm + kOffOwn + (c % 4) * kBlk : st + 2 * kBlk;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
