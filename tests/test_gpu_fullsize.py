@@ -205,3 +205,63 @@ def test_degenerate_tiles():
             assert st["mismatch"] <= 4 and st["scale_rel"] <= parity.SCALE_RTOL, (t, bits, st)
             rec = codec.dequantize(got["codes"], got["a"], got["b"], got["c"])
             assert np.isfinite(rec).all()
+
+
+@pytest.mark.parametrize("Q,S,R,pairs", [(1, 128, 1024, [(0, 0), (13, 6), (31, 7)]),
+                                         (4, 128, 256, [(2, 1), (29, 4)])])
+def test_window_fullsize(Q, S, R, pairs):
+    """The raw-record decode (sink S + recent R raw tokens, Q query tokens)
+    on the full dense32b batch: every (sequence, KV head) unit has S + R or
+    more raw tokens, so the raw records span several splits of the full-size
+    plan. Sampled pairs get the oracle's pages; their rows are checked
+    against the oracle's window decode."""
+    wl = W.WORKLOADS["dense32b"]
+    case = W.make_dense(wl, device=DEV)
+    N, D, B, Hkv = wl.tile_tokens, wl.head_dim, wl.num_seqs, wl.num_kv_heads
+    lay = kv.dense_layout(D, N, Hkv, case.num_pages, kv.FP16, wl.norm_iters)
+    cache = kv.alloc_cache(lay, DEV)
+    err = kv.new_error_word(DEV)
+    _encode_dense(case, wl, lay, cache, err)
+    torch.cuda.synchronize()
+    lens = case.seq_lens.cpu().numpy()
+    bt = case.block_table.cpu().numpy()
+    olay = layout.DenseLayout(D, N)
+    ppt = N // 16
+    host = np.zeros((case.num_pages, Hkv, olay.page_bytes), np.uint8)
+    for b, h in pairs:
+        L = int(lens[b])
+        C = attention.window_committed(L, Q, N, S, R)
+        kbh, vbh = parity.f64(case.k[b, h, :L]), parity.f64(case.v[b, h, :L])
+        for t in range(S // N, C // N):
+            pg = [int(x) for x in bt[b, t * ppt:(t + 1) * ppt]]
+            layout.write_tile(host, olay, pg, h, codec.encode_tile(kbh[t * N:(t + 1) * N], 4, wl.norm_iters),
+                              codec.encode_tile(vbh[t * N:(t + 1) * N], 2, wl.norm_iters))
+        pages = torch.from_numpy(bt[b, (S // N) * ppt:(C // N) * ppt]).long().to(DEV)
+        cache[pages, h] = torch.from_numpy(host[bt[b, (S // N) * ppt:(C // N) * ppt], h]).to(DEV)
+    sink_k, sink_v = case.k[:, :, :S].contiguous(), case.v[:, :, :S].contiguous()
+    cap = R + N + Q - 2
+    tail_k = torch.zeros((B, Hkv, cap, D), dtype=case.k.dtype, device=DEV)
+    tail_v = torch.zeros_like(tail_k)
+    for b in range(B):
+        L = int(lens[b])
+        C = attention.window_committed(L, Q, N, S, R)
+        tail_k[b, :, :L - C] = case.k[b, :, C:L]
+        tail_v[b, :, :L - C] = case.v[b, :, C:L]
+    q = W.verify_queries(wl, Q, device=DEV)
+    Lmax = int(lens.max())
+    out = torch.empty((B, Q, wl.num_q_heads, D), dtype=torch.float32, device=DEV)
+    ws = torch.empty(kv.decode_window_workspace_bytes(lay, B, wl.num_q_heads, Q, Lmax, S, R), dtype=torch.uint8,
+                     device=DEV)
+    sm = W.default_sm_scale(wl)
+    kv.decode_window(q, lay, cache, case.block_table, case.seq_lens, Lmax, out, ws, err, sm, sink_k=sink_k,
+                     sink_v=sink_v, recent_tokens=R, tail_k=tail_k, tail_v=tail_v)
+    torch.cuda.synchronize()
+    assert kv.read_error_flags(err) == 0
+    G = wl.group
+    rows = [(b, j, h * G + g) for b, h in pairs for j in range(Q) for g in range(G)]
+    ref, _ = attention.decode_window(parity.f64(q), host, olay, bt, lens, sm, S, R, parity.f64(sink_k),
+                                     parity.f64(sink_v), parity.f64(tail_k), parity.f64(tail_v), rows=rows)
+    o = parity.f64(out)
+    diff = max(np.abs(o[b, j, hq] - ref[b, j, hq]).max() for b, j, hq in rows)
+    print(f"window Q{Q} S{S} R{R}: max |out - oracle| over {len(rows)} sampled rows = {diff:.3e}")
+    assert diff <= parity.OUT_ATOL
