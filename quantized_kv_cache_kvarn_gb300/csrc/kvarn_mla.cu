@@ -147,7 +147,8 @@ constexpr int kSmem = kOffBar + 128 + 1024;  // + room to align the base to 1024
 constexpr int kConsumers = 128, kProducers = 256;
 constexpr int kThreads = kConsumers + kProducers + 32;
 constexpr int kMmaWarp = kThreads / 32 - 1;
-enum { BAR_AFULL = 0, BAR_AEMPTY = 2, BAR_SFULL = 4, BAR_PFULL, BAR_OFULL, BAR_TFREE, BAR_RAW, BAR_META, BAR_PSYNC,
+// BAR_OFULL: P V of the tile complete; BAR_OFULL_A: its first 128 channels
+enum { BAR_AFULL = 0, BAR_AEMPTY = 2, BAR_SFULL = 4, BAR_PFULL, BAR_OFULL, BAR_OFULL_A, BAR_TFREE, BAR_RAW, BAR_META, BAR_PSYNC,
        BAR_FIN, NBARS };
 static_assert(kOffRaw % 16 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0 && NBARS * 8 + 8 <= 128, "layout");
 static_assert(kSmem <= 232448, "one CTA per SM");
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
     mbar_init(bars + BAR_SFULL, 1);
     mbar_init(bars + BAR_PFULL, kConsumers);
     mbar_init(bars + BAR_OFULL, 1);
+    mbar_init(bars + BAR_OFULL_A, 1);
     mbar_init(bars + BAR_TFREE, kConsumers);
     mbar_init(bars + BAR_RAW, 1);
     mbar_init(bars + BAR_META, kProducers);
@@ -531,14 +533,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_plain(bars + BAR_PFULL);
-      if (!wait(BAR_OFULL, par)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // acc = alpha acc + c (u + beta), own channel 32 q + e
+      // acc = alpha acc + c (u + beta), own channel 32 q + e: the first 128
+      // channels as soon as their P V completes, while the rest still runs
 #pragma unroll 1
       for (int q = 0; q < 8; ++q) {
+        if ((q & 3) == 0) {
+          if (!wait(q == 0 ? BAR_OFULL_A : BAR_OFULL, par)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         uint32_t ot[32], oa[32];
         tc_ld32(tl + 32 * q, ot);
         if (i > 0) tc_ld32(tl + 256 + 32 * q, oa);
@@ -551,6 +556,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
         }
         tc_st32(tl + 256 + 32 * q, oa);
       }
+      if (!ok) break;
       tc_wait_st();
       tc_fence_before();
       mbar_arrive_plain(bars + BAR_TFREE);
@@ -616,14 +622,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1) mla_tc_kernel(MlaArgs A) {
         // read MN-major (64-channel atoms one block apart, 8-token groups
         // 1024 bytes apart); P K-major in two 64-token blocks
 #pragma unroll 1
-        for (int r = 0; r < 2; ++r)
+        for (int r = 0; r < 2; ++r) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
             for (int pl = 0; pl < 2; ++pl)
               tc_mma_f16(tmem + 128 * r, tc_desc_sw128(pa + pl * 2 * kBlk + (ks / 4) * kBlk + 32 * (ks % 4), 16, 1024),
                          tc_desc_sw128(own + 2 * r * kBlk + ks * 2048, kBlk, 1024), kIdPV, ks > 0 || pl > 0);
-        tc_commit(bars + BAR_OFULL);
+          tc_commit(bars + (r == 0 ? BAR_OFULL_A : BAR_OFULL));
+        }
       }
       __syncwarp();
     }
