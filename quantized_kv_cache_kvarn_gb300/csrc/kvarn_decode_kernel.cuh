@@ -55,6 +55,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 #define KVARN_DECODE_MIN_CTAS 3
 #endif
 
+// Floats per k-chunk block of the rotated query rows in shared memory: the
+// block's 128 (8 rows x 4 lane columns x 4 channels) plus 4 of padding, so
+// that the scalar stores that build the rows (one lane per k-chunk, a block
+// apart) fall in different banks.
+constexpr int kQFragStride = 132;
+
+// Floats per row of the merge scratch: m, l, two pads, then D values; a
+// stride of 8 modulo the 32 banks keeps the row-wise float2 / float4 stores
+// of a warp on distinct banks.
+template <int D> constexpr int merge_stride() { return D + 8; }
+
 // HV warps share a tile (HV = 2 at head_dim 256: each warp owns half of the
 // channels of Q K and of P V, and the pair adds its partial scores).
 template <int D> constexpr int halves_for() { return D == 256 ? 2 : 1; }
@@ -100,13 +111,14 @@ struct DecShape {
   static constexpr int RING = UNITS * WARP_SMEM;
   static constexpr int XS = 2 * (N / 8) + 2;  // exchanged per lane: partial scores, two timeout flags
   static constexpr int XBUF = HV == 2 ? UNITS * 2 * 32 * XS * 4 : 0;
-  static constexpr int OFF_BARS = RING, OFF_QROT = RING + UNITS * 2 * 8, OFF_XBUF = OFF_QROT + 8 * D * 4;
+  static constexpr int OFF_BARS = RING, OFF_QROT = RING + UNITS * 2 * 8;
+  static constexpr int OFF_XBUF = OFF_QROT + (D / 16) * kQFragStride * 4;
   // the raw-record warps' partials: in the slots, or past the rest where the
   // slots are smaller (head_dim 256, 64-token tiles)
-  static constexpr int RAW_MRG = W * 8 * (D + 2) * 4;
+  static constexpr int RAW_MRG = W * 8 * merge_stride<D>() * 4;
   static constexpr int OFF_RAW_MRG = RAW_MRG <= RING ? 0 : OFF_XBUF + XBUF;
   static constexpr int SMEM = OFF_XBUF + XBUF + (RAW_MRG <= RING ? 0 : RAW_MRG);
-  static_assert(UNITS * 8 * (D + 2) * 4 <= RING, "tile merge scratch must fit in the slots");
+  static_assert(UNITS * 8 * merge_stride<D>() * 4 <= RING, "tile merge scratch must fit in the slots");
   static_assert(W * 40 <= 8 * D, "raw-record weight exchange must fit in the query rows");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
@@ -201,8 +213,9 @@ struct RowMap {
 // The rotated, scaled query rows in shared memory, in mma fragment order:
 // for k-chunk kc, row g and lane column t the four channels 16 kc + 2 t,
 // +1, +8, +9 are one 16-byte word, and a warp's 32 words for one k-chunk are
-// contiguous (one conflict-free 128-bit load per lane).
-__device__ __forceinline__ int q_frag(int kc, int g, int t) { return ((kc * 8 + g) * 4 + t) * 4; }
+// contiguous (one conflict-free 128-bit load per lane); k-chunk blocks are
+// kQFragStride floats apart.
+__device__ __forceinline__ int q_frag(int kc, int g, int t) { return kc * kQFragStride + (g * 4 + t) * 4; }
 
 // Partial slot of (sequence b, query token j, query head hq).
 __device__ __forceinline__ float* part_of(const DecArgs& A, int D, int b, int j, int hq, int slot) {
@@ -306,7 +319,8 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
   const int per = (c1 - c0 + W * U - 1) / (W * U) * U;
   const int w0 = c0 + warp * per, w1 = min(c1, w0 + per);
   float* mrg = reinterpret_cast<float*>(mrg_smem);
-  float* mw = mrg + warp * 8 * (D + 2);
+  constexpr int MS = merge_stride<D>();
+  float* mw = mrg + warp * 8 * MS;
 
   for (int r0 = 0; r0 < R.n; r0 += RP) {
     // this lane's channels of the pass's query rows, kappa-scaled (zero past R.n)
@@ -418,13 +432,15 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
     }
     // this warp's piece of the pass's rows into the merge scratch
     if (my_u == 0 && lane < PAIRS) {
-      mw[(r0 + my_r) * (D + 2)] = m;
-      mw[(r0 + my_r) * (D + 2) + 1] = l;
+      mw[(r0 + my_r) * MS] = m;
+      mw[(r0 + my_r) * MS + 1] = l;
     }
 #pragma unroll
     for (int r = 0; r < RP; ++r)
 #pragma unroll
-      for (int e = 0; e < E; ++e) mw[(r0 + r) * (D + 2) + 2 + lane * E + e] = acc[r][e];
+      for (int e = 0; e < E; e += 4)
+        *reinterpret_cast<float4*>(mw + (r0 + r) * MS + 4 + lane * E + e) =
+            make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
   }
   // ---- merge the warps' pieces per row
   __syncthreads();
@@ -432,14 +448,14 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
     const int r = idx / D, j = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + r) * (D + 2)]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + r) * MS]);
     float a = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
-        const float* x = mrg + (w * 8 + r) * (D + 2);
+        const float* x = mrg + (w * 8 + r) * MS;
         const float sc = exp2f(x[0] - M);
-        a = fmaf(x[2 + j], sc, a);
+        a = fmaf(x[4 + j], sc, a);
         L = fmaf(x[1], sc, L);
       }
     }
@@ -1073,30 +1089,30 @@ __device__ __forceinline__ bool dense_segment(const DecArgs& A, unsigned char* s
   // ---- merge the units of the CTA (scratch aliases the slots)
   const bool any_late = __syncthreads_or(timed_out);
   float* mrg = reinterpret_cast<float*>(smem);
-  float* mw = mrg + unit * 8 * (D + 2);
+  constexpr int MS = merge_stride<D>();
+  float* mw = mrg + unit * 8 * MS;
   if (t == 0 && leader) {
-    mw[g * (D + 2)] = n_my > 0 ? m : -INFINITY;
-    mw[g * (D + 2) + 1] = n_my > 0 ? lsum : 0.f;
+    mw[g * MS] = n_my > 0 ? m : -INFINITY;
+    mw[g * MS + 1] = n_my > 0 ? lsum : 0.f;
   }
 #pragma unroll
   for (int ncl = 0; ncl < NCW; ++ncl) {
     const int nc = half * NCW + ncl;
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t] = acc[ncl].x;
-    mw[g * (D + 2) + 2 + 8 * nc + 2 * t + 1] = acc[ncl].y;
+    *reinterpret_cast<float2*>(mw + g * MS + 4 + 8 * nc + 2 * t) = acc[ncl];
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
     const int gg = idx / D, j = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < UNITS; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * (D + 2)]);
+    for (int w = 0; w < UNITS; ++w) M = fmaxf(M, mrg[(w * 8 + gg) * MS]);
     float a = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < UNITS; ++w) {
-        const float* r = mrg + (w * 8 + gg) * (D + 2);
+        const float* r = mrg + (w * 8 + gg) * MS;
         const float sc = exp2f(r[0] - M);
-        a = fmaf(r[2 + j], sc, a);
+        a = fmaf(r[4 + j], sc, a);
         L = fmaf(r[1], sc, L);
       }
     }
