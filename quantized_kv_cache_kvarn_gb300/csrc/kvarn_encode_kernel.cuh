@@ -78,6 +78,15 @@ struct EncodeArgs {
 };
 
 
+// Position of channel c in a per-channel shared buffer written a 16-byte
+// chunk per lane: chunk e (channels 4e..4e+3) of every segment, then chunk
+// e + 1, so that the segments' stores (and reads) of one chunk fill
+// consecutive banks.
+template <int D>
+__device__ __forceinline__ int chunk_pos(int c) {
+  return (((c & 15) >> 2) * (D / 16) + (c >> 4)) * 4 + (c & 3);
+}
+
 // Merge of two (mean, M2) summaries of n values each (Chan, Golub and
 // LeVeque's pairwise update of the sum of squared deviations): the mean of
 // 2n values and their M2. Written symmetrically in a and b, so that the two
@@ -108,12 +117,12 @@ __device__ __forceinline__ float2 column_moments(float2 (&mo)[16], float* red, f
     n *= 2.f;
   }
   if (lane < S::TPR) {
-    float4* dm = reinterpret_cast<float4*>(red + warp * D + seg * 16);
-    float4* dv = reinterpret_cast<float4*>(red + (S::NW + warp) * D + seg * 16);
+    float4* dm = reinterpret_cast<float4*>(red + warp * D);
+    float4* dv = reinterpret_cast<float4*>(red + (S::NW + warp) * D);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      dm[e] = make_float4(mo[4 * e].x, mo[4 * e + 1].x, mo[4 * e + 2].x, mo[4 * e + 3].x);
-      dv[e] = make_float4(mo[4 * e].y, mo[4 * e + 1].y, mo[4 * e + 2].y, mo[4 * e + 3].y);
+      dm[e * S::TPR + seg] = make_float4(mo[4 * e].x, mo[4 * e + 1].x, mo[4 * e + 2].x, mo[4 * e + 3].x);
+      dv[e * S::TPR + seg] = make_float4(mo[4 * e].y, mo[4 * e + 1].y, mo[4 * e + 2].y, mo[4 * e + 3].y);
     }
   }
   __syncthreads();
@@ -121,7 +130,10 @@ __device__ __forceinline__ float2 column_moments(float2 (&mo)[16], float* red, f
   if (threadIdx.x < D) {
     float2 w[S::NW];
 #pragma unroll
-    for (int i = 0; i < S::NW; ++i) w[i] = make_float2(red[i * D + threadIdx.x], red[(S::NW + i) * D + threadIdx.x]);
+    for (int i = 0; i < S::NW; ++i) {
+      const int pos = chunk_pos<D>(threadIdx.x);
+      w[i] = make_float2(red[i * D + pos], red[(S::NW + i) * D + pos]);
+    }
     float nw = static_cast<float>(S::RPT * S::RPW);  // rows per warp
 #pragma unroll
     for (int st = 1; st < S::NW; st *= 2) {
@@ -144,17 +156,6 @@ __device__ __forceinline__ float2 column_moments(float2 (&mo)[16], float* red, f
     }
   }
   return make_float2(t.x, t.y * (1.f / N));
-}
-
-// Reads the 16 broadcast per-channel values of this thread's segment.
-template <int D>
-__device__ __forceinline__ void read_segment(float (&v)[16], const float* colbuf, int seg) {
-  const float4* src = reinterpret_cast<const float4*>(colbuf + seg * 16);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float4 f = src[e];
-    v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
-  }
 }
 
 // Population std; 1 for a constant vector or a non-finite std. The sums
@@ -431,15 +432,15 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const unsigned 
     if (tid < D) {
       const float sig = safe_sigma(cm.y);
       cscale *= sig;
-      colbuf[tid] = 1.f / sig;
+      colbuf[chunk_pos<D>(tid)] = 1.f / sig;
     }
     __syncthreads();
     float2 inv[8];
     {
-      const float4* src = reinterpret_cast<const float4*>(colbuf + seg * 16);
+      const float4* src = reinterpret_cast<const float4*>(colbuf);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float4 f = src[e];
+        const float4 f = src[e * S::TPR + seg];
         inv[2 * e] = make_float2(f.x, f.y);
         inv[2 * e + 1] = make_float2(f.z, f.w);
       }
