@@ -113,13 +113,30 @@ struct DecShape {
   static constexpr int XBUF = HV == 2 ? UNITS * 2 * 32 * XS * 4 : 0;
   static constexpr int OFF_BARS = RING, OFF_QROT = RING + UNITS * 2 * 8;
   static constexpr int OFF_XBUF = OFF_QROT + (D / 16) * kQFragStride * 4;
-  // the raw-record warps' partials: in the slots, or past the rest where the
-  // slots are smaller (head_dim 256, 64-token tiles)
+  // raw-record scratch, taken from the page slots (which no copy touches
+  // before the tile loop starts) where it fits. While a CTA scores its raw
+  // records: each warp's weight block (32 records x 8 rows) and, at head_dim
+  // 128 where they fit in the slots, its staged key rows (32 rows, each padded
+  // by 16 bytes so that the lanes' reads of their own rows do not collide);
+  // elsewhere a lane reads its key row from global memory. Afterwards, at
+  // the same place, the warps' partials for the merge (a barrier between).
+  // The channel-major query rows (8 x D floats) take the query-row region.
   static constexpr int RAW_MRG = W * 8 * merge_stride<D>() * 4;
-  static constexpr int OFF_RAW_MRG = RAW_MRG <= RING ? 0 : OFF_XBUF + XBUF;
-  static constexpr int SMEM = OFF_XBUF + XBUF + (RAW_MRG <= RING ? 0 : RAW_MRG);
+  static constexpr int RAW_PB = W * 32 * 8 * 4;
+  static constexpr int RAW_KROW = 2 * D + 16;
+  static constexpr int RAW_KST = HV == 1 && !RAW && RAW_PB + W * 32 * RAW_KROW <= RING ? W * 32 * RAW_KROW : 0;
+  static constexpr int RAW_P1 = RAW_PB + RAW_KST;
+  static constexpr bool MRG_IN = RAW_MRG <= RING;
+  static constexpr int END0 = OFF_XBUF + XBUF;
+  static constexpr int OFF_RAW_MRG = MRG_IN ? 0 : END0;
+  static constexpr int OFF_RAW_PB = RAW_P1 <= RING ? 0 : XBUF >= RAW_P1 ? OFF_XBUF : END0;
+  static constexpr int OFF_RAW_KST = OFF_RAW_PB + RAW_PB;
+  static constexpr int SMEM = END0 + (MRG_IN ? 0 : RAW_MRG) > OFF_RAW_PB + RAW_P1 ? END0 + (MRG_IN ? 0 : RAW_MRG)
+                                                                                    : OFF_RAW_PB + RAW_P1;
   static_assert(UNITS * 8 * merge_stride<D>() * 4 <= RING, "tile merge scratch must fit in the slots");
-  static_assert(W * 40 <= 8 * D, "raw-record weight exchange must fit in the query rows");
+  static_assert(8 * D * 4 <= (D / 16) * kQFragStride * 4 && W * 40 * 4 <= (D / 16) * kQFragStride * 4,
+                "raw-record query rows and weight exchange must fit in the query-row region");
+  static_assert(OFF_RAW_PB % 16 == 0 && OFF_RAW_KST % 16 == 0 && RAW_KROW % 16 == 0, "raw scratch alignment");
   static_assert(W % HV == 0, "whole warp pairs");
   static_assert(KP % 16 == 0 && VP % 16 == 0, "page parts must keep 16-byte alignment");
   static constexpr bool GATHER = parts_gather(D, N, KP, VP, KB, VB);
@@ -273,63 +290,77 @@ __device__ __forceinline__ void raw_floats(const RawRow<E>& r, bool bf16, float*
 // sink rows [0, min(sink, visible)) and the tail rows for tokens [committed,
 // visible). All rows of the unit share one raw list, the sink rows of the
 // longest row then its tail rows, masked per row by position; raw split
-// `chunk` covers list entries [chunk * kRawChunk, +kRawChunk). The CTA's W
-// warps take consecutive pieces of the chunk, each warp scoring the rows of
-// the unit against each record row it loads (one load per record row and
-// pass, not one per query row; one pass of eight rows at head_dim 128, two of
-// four at 256): per step of four records a lane forms its channels'
-// products for the rows x 4 (row, record) pairs, and a reduce-scatter over
-// the warp leaves lane l with the whole score of pair l mod (4 x rows) (row
-// of the pass (l mod (4 x rows)) / 4, record l % 4). Online softmax per row in base 2, the weights exchanged through
-// shared memory, the warps' partials merged at the end (`mrg`: scratch that
-// aliases the page slots where they are large enough, which no copy touches
-// before the tile loop starts).
-template <int D, int N, int W>
-__device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* pxbuf, int b, int kvh, const RowMap& R,
-                              int len, int sink, int committed, int chunk) {
-  // rows per pass (the query and accumulator rows a lane holds): all eight
-  // at head_dim 128, four at 256 (two passes over the records, which keeps
-  // the kernel's register budget of the tile loop)
-  constexpr int E = D / 32, U = 4, RP = D == 256 ? 4 : 8, PAIRS = RP * U;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int my_r = (lane & (PAIRS - 1)) >> 2, my_u = lane & 3;  // pair of the lane after the reduce-scatter
-  // the longest row's list bounds everything read
-  int vis_max = 0;
-  for (int r = 0; r < R.n; ++r) vis_max = max(vis_max, visible_len(len, A.Q, R.query(A, r)));
-  const int n_sink = min(sink, vis_max), n_tail = max(0, vis_max - committed);
-  const int c0 = chunk * kRawChunk, c1 = min(n_sink + n_tail, c0 + kRawChunk);
-  const bool miss = (c1 > max(c0, n_sink) && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
-                    (min(c1, n_sink) > c0 && (A.sink_k == nullptr || A.sink_v == nullptr));
-  if (c1 <= c0 || miss) {
-    if (miss && threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
-    for (int r = warp; r < R.n; r += W)
-      write_empty(part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), A.tile_slots + chunk), D, lane);
-    return;
+// `chunk` covers list entries [chunk * kRawChunk, +kRawChunk), cut into W
+// consecutive pieces, one per warp. Each warp leaves the (max, sum,
+// unnormalised output) of its piece per row in the merge scratch `mrg`
+// (8 rows of merge_stride<D>() floats per warp), and the pieces are merged
+// per row into the split's partial.
+//
+// The list of a split: row r's query token, query head and visible length in
+// lane r (r < R.n), the list bounds, and where its records start.
+struct RawSplit {
+  int qj_l = 0, hq_l = 0, vis_l = 0;
+  int n_sink, c0, c1, committed, slot;
+  int64_t sink0, tail0;
+  bool miss;
+  __device__ RawSplit(const DecArgs& A, const RowMap& R, int N, int b, int kvh, int len, int sink, int committed_,
+                      int chunk) {
+    const int lane = threadIdx.x & 31;
+    if (lane < R.n) {
+      qj_l = R.query(A, lane);
+      hq_l = kvh * A.G + R.head(A, lane);
+      vis_l = visible_len(len, A.Q, qj_l);
+    }
+    // the longest row's list bounds everything read
+    int vis_max = vis_l;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) vis_max = max(vis_max, __shfl_xor_sync(0xffffffffu, vis_max, o));
+    committed = committed_;
+    n_sink = min(sink, vis_max);
+    const int n_tail = max(0, vis_max - committed);
+    c0 = chunk * kRawChunk;
+    c1 = min(n_sink + n_tail, c0 + kRawChunk);
+    miss = (c1 > max(c0, n_sink) && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
+           (min(c1, n_sink) > c0 && (A.sink_k == nullptr || A.sink_v == nullptr));
+    slot = A.tile_slots + chunk;
+    sink0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
+    tail0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
   }
-  // list entry i: its token position and record row
-  const int64_t sink0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * (A.sink_tiles * N);
-  const int64_t tail0 = (static_cast<int64_t>(b) * A.Hkv + kvh) * A.tail_cap;
-  auto row_ptr = [&](int i, bool v) -> const char* {
+  __device__ int qj(int r) const { return __shfl_sync(0xffffffffu, qj_l, r); }
+  __device__ int hq(int r) const { return __shfl_sync(0xffffffffu, hq_l, r); }
+  __device__ int position(int i) const { return i < n_sink ? i : committed + (i - n_sink); }
+  // record row of list entry i (keys or values)
+  __device__ const char* row(const DecArgs& A, int D, int i, bool v) const {
     const void* base = i < n_sink ? (v ? A.sink_v : A.sink_k) : (v ? A.tail_v : A.tail_k);
-    const int64_t row = i < n_sink ? sink0 + i : tail0 + (i - n_sink);
-    return static_cast<const char*>(base) + 2 * (row * D + lane * E);
-  };
-  auto position = [&](int i) { return i < n_sink ? i : committed + (i - n_sink); };
-  // this warp's piece of the chunk, a multiple of U records
-  const int per = (c1 - c0 + W * U - 1) / (W * U) * U;
-  const int w0 = c0 + warp * per, w1 = min(c1, w0 + per);
-  float* mrg = reinterpret_cast<float*>(mrg_smem);
-  constexpr int MS = merge_stride<D>();
-  float* mw = mrg + warp * 8 * MS;
+    return static_cast<const char*>(base) + 2 * D * (i < n_sink ? sink0 + i : tail0 + (i - n_sink));
+  }
+};
 
+// Scoring with the channels split over the lanes (head_dim 256, and where the
+// key rows of a block cannot be staged): a lane holds D / 32 channels of the
+// rows of a pass (all eight at head_dim 128, four at 256: two passes over
+// the records, which keeps the kernel's register budget of the tile loop).
+// Per step of four records a lane forms its channels' products for the
+// rows x 4 (row, record) pairs, and a reduce-scatter over the warp leaves
+// lane l with the whole score of pair l mod (4 x rows); online softmax per
+// row over groups of four lanes, the weights and rescales to every lane
+// through 160 bytes of shared memory (`pxbuf`); the next four records load
+// while the current ones are scored.
+template <int D, int N, int W>
+__device__ void raw_pieces_by_channel(const DecArgs& A, const RawSplit& L, float* mw, float* pxbuf, int b,
+                                      const RowMap& R, int w0, int w1) {
+  constexpr int E = D / 32, U = 4, RP = D == 256 ? 4 : 8, PAIRS = RP * U;
+  constexpr int MS = merge_stride<D>();
+  const int lane = threadIdx.x & 31;
+  const int my_r = (lane & (PAIRS - 1)) >> 2, my_u = lane & 3;  // pair of the lane after the reduce-scatter
   for (int r0 = 0; r0 < R.n; r0 += RP) {
     // this lane's channels of the pass's query rows, kappa-scaled (zero past R.n)
     float q[RP][E];
 #pragma unroll
     for (int r = 0; r < RP; ++r) {
+      const int qj = L.qj(r0 + r), hq = L.hq(r0 + r);
       if (r0 + r < R.n) {
-        const int64_t qoff = (static_cast<int64_t>(b * A.Q + R.query(A, r0 + r)) * A.Hq + kvh * A.G +
-                              R.head(A, r0 + r)) * D + lane * E;
+        const int64_t qoff = (static_cast<int64_t>(b * A.Q + qj) * A.Hq + hq) * D + lane * E;
         load_vec_rt<E>(static_cast<const char*>(A.q) + 2 * qoff, A.bf16, q[r]);
 #pragma unroll
         for (int e = 0; e < E; ++e) q[r][e] *= A.kappa;
@@ -338,7 +369,7 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
         for (int e = 0; e < E; ++e) q[r][e] = 0.f;
       }
     }
-    const int my_vis = r0 + my_r < R.n ? visible_len(len, A.Q, R.query(A, r0 + my_r)) : 0;
+    const int my_vis = __shfl_sync(0xffffffffu, L.vis_l, r0 + my_r);
     float acc[RP][E];
 #pragma unroll
     for (int r = 0; r < RP; ++r)
@@ -350,8 +381,8 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (i0 + u < w1) {
-          kb[u] = raw_load<E>(row_ptr(i0 + u, false));
-          vb[u] = raw_load<E>(row_ptr(i0 + u, true));
+          kb[u] = raw_load<E>(L.row(A, D, i0 + u, false) + 2 * lane * E);
+          vb[u] = raw_load<E>(L.row(A, D, i0 + u, true) + 2 * lane * E);
         } else {
 #pragma unroll
           for (int k = 0; k < E / 2; ++k) kb[u].w[k] = vb[u].w[k] = 0u;
@@ -399,7 +430,7 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
         }
       }
       const int i = i0 + my_u;
-      const float s = (i < w1 && position(i) < my_vis) ? v[0] : -INFINITY;
+      const float s = (i < w1 && L.position(i) < my_vis) ? v[0] : -INFINITY;
       const float mx = fmaxf(fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1)),
                              fmaxf(__shfl_xor_sync(0xffffffffu, s, 2), __shfl_xor_sync(0xffffffffu, s, 3)));
       const float m_new = fmaxf(m, mx);
@@ -442,31 +473,212 @@ __device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* 
         *reinterpret_cast<float4*>(mw + (r0 + r) * MS + 4 + lane * E + e) =
             make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
   }
-  // ---- merge the warps' pieces per row
+}
+
+// Scoring with one record per lane (head_dim 128 where a block's key rows fit
+// in the page slots). A warp takes its piece in blocks of 32 records:
+//  - the block's key rows are copied into shared memory coalesced (`kst`,
+//    rows padded by 16 bytes) and each lane reads its own record's row back;
+//    it forms the dot products with all eight rows, whose kappa-scaled query
+//    channels come channel-major from shared memory (`qs`: qs[8 d + r], one
+//    broadcast load per four rows), so no score needs a cross-lane sum;
+//  - softmax: per row, the block maximum over the lanes, the rescale of the
+//    running state, base-2 weights; each lane keeps its own partial of the
+//    row sums (one warp sum per row at the end);
+//  - P.V: the weights go through shared memory (`pw`, 1 KB per warp); the
+//    lane owns D / 32 channels of every row's accumulator and walks the
+//    block's records, one coalesced read of each value row.
+template <int D, int N, int W>
+__device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float* mw, const float* qs, float* pw,
+                                     unsigned char* kw, int w0, int w1) {
+  constexpr int E = D / 32, KROW = 2 * D + 16, MS = merge_stride<D>();
+  const int lane = threadIdx.x & 31;
+  int vis[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) vis[r] = __shfl_sync(0xffffffffu, L.vis_l, r);
+  float acc[8][E], m[8], l[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+  }
+  // P.V of record j of the block from its value row vr
+  auto pv = [&](const char* vr, int j) {
+    float vf[E];
+    raw_floats<E>(raw_load<E>(vr + 2 * lane * E), A.bf16, vf);
+    const float4 pa = *reinterpret_cast<const float4*>(pw + j * 8);
+    const float4 pb = *reinterpret_cast<const float4*>(pw + j * 8 + 4);
+    const float p8[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[r][e] = fmaf(p8[r], vf[e], acc[r][e]);
+  };
+  for (int blk = w0; blk < w1; blk += 32) {
+    const int nrec = min(32, w1 - blk);
+    // the block's key rows, coalesced: 16-byte piece lane + 32 t is piece
+    // (lane + 32 t) % (D / 8) of row (lane + 32 t) / (D / 8)
+#pragma unroll 4
+    for (int t = 0; t < D / 8; ++t) {
+      const int q = lane + 32 * t, row = q / (D / 8), col = q % (D / 8);
+      if (row < nrec) cp_async16(kw + row * KROW + 16 * col, L.row(A, D, blk + row, false) + 16 * col);
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    const int i = blk + lane;
+    const bool valid = i < w1;
+    float s[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) s[r] = 0.f;
+    if (valid) {
+#pragma unroll 8
+      for (int c = 0; c < D / 8; ++c) {
+        RawRow<8> k8;
+        const uint4 u = *reinterpret_cast<const uint4*>(kw + lane * KROW + 16 * c);
+        k8.w[0] = u.x;
+        k8.w[1] = u.y;
+        k8.w[2] = u.z;
+        k8.w[3] = u.w;
+        float kf[8];
+        raw_floats<8>(k8, A.bf16, kf);
+#pragma unroll
+        for (int dd = 0; dd < 8; ++dd) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + (8 * c + dd) * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + (8 * c + dd) * 8 + 4);
+          s[0] = fmaf(qa.x, kf[dd], s[0]);
+          s[1] = fmaf(qa.y, kf[dd], s[1]);
+          s[2] = fmaf(qa.z, kf[dd], s[2]);
+          s[3] = fmaf(qa.w, kf[dd], s[3]);
+          s[4] = fmaf(qb.x, kf[dd], s[4]);
+          s[5] = fmaf(qb.y, kf[dd], s[5]);
+          s[6] = fmaf(qb.z, kf[dd], s[6]);
+          s[7] = fmaf(qb.w, kf[dd], s[7]);
+        }
+      }
+    }
+    const int pos = L.position(i);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float sr = valid && pos < vis[r] ? s[r] : -INFINITY;
+      float bm = sr;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      const float mn = fmaxf(m[r], bm);
+      const float al = mn == -INFINITY ? 1.f : exp2f(m[r] - mn);
+      const float p = sr == -INFINITY ? 0.f : exp2f(sr - mn);
+      l[r] = fmaf(l[r], al, p);
+      m[r] = mn;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[r][e] *= al;
+      s[r] = p;
+    }
+    // the block's weights to every lane
+    *reinterpret_cast<float4*>(pw + lane * 8) = make_float4(s[0], s[1], s[2], s[3]);
+    *reinterpret_cast<float4*>(pw + lane * 8 + 4) = make_float4(s[4], s[5], s[6], s[7]);
+    __syncwarp();
+    // the block's value rows: its sink records, then its tail records, each
+    // region contiguous
+    const int ns = min(nrec, max(0, L.n_sink - blk));
+    if (ns > 0) {
+      const char* vr = L.row(A, D, blk, true);
+#pragma unroll 4
+      for (int j = 0; j < ns; ++j) pv(vr + 2 * D * j, j);
+    }
+    if (ns < nrec) {
+      const char* vr = L.row(A, D, blk + ns, true);
+#pragma unroll 4
+      for (int j = ns; j < nrec; ++j) pv(vr + 2 * D * (j - ns), j);
+    }
+    __syncwarp();  // pw and the staged key rows are rewritten by the next block
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) l[r] = warp_sum_xor(l[r], 1, 32);
+  // this warp's piece into the merge scratch, which the other warps' weight
+  // blocks and key rows may occupy until they are done
   __syncthreads();
-  for (int idx = threadIdx.x; idx < R.n * D; idx += W * 32) {
-    const int r = idx / D, j = idx % D;
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      mw[r * MS] = m[r];
+      mw[r * MS + 1] = l[r];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int e = 0; e < E; e += 4)
+      *reinterpret_cast<float4*>(mw + r * MS + 4 + lane * E + e) =
+          make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
+}
+
+// The raw partials of split `chunk` of a unit. KST: scoring by record with
+// the key rows staged in shared memory (`kst`, `pbuf` the weight blocks, `qs`
+// the channel-major query rows), else by channel (`pxbuf`).
+template <int D, int N, int W, bool KST>
+__device__ void tail_partials(const DecArgs& A, unsigned char* mrg_smem, float* qrows, float* pbuf, unsigned char* kst,
+                              int b, int kvh, const RowMap& R, int len, int sink, int committed, int chunk) {
+  constexpr int MS = merge_stride<D>();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RawSplit L(A, R, N, b, kvh, len, sink, committed, chunk);
+  if (L.c1 <= L.c0 || L.miss) {
+    if (L.miss && threadIdx.x == 0) set_error(A.err, KVARN_DEVERR_NO_TAIL);
+    for (int r = warp; r < R.n; r += W) write_empty(part_of(A, D, b, L.qj(r), L.hq(r), L.slot), D, lane);
+    return;
+  }
+  // this warp's piece of the split
+  const int per = KST ? (L.c1 - L.c0 + W - 1) / W : (L.c1 - L.c0 + W * 4 - 1) / (W * 4) * 4;
+  const int w0 = L.c0 + warp * per, w1 = min(L.c1, w0 + per);
+  float* mrg = reinterpret_cast<float*>(mrg_smem);
+  float* mw = mrg + warp * 8 * MS;
+  if constexpr (KST) {
+    // query rows, kappa-scaled, channel-major (zero past R.n): row r by warp r % W
+    for (int r = warp; r < 8; r += W) {
+      const int qj = L.qj(r), hq = L.hq(r);
+      const unsigned short* qrow =
+          static_cast<const unsigned short*>(A.q) + (static_cast<int64_t>(b * A.Q + qj) * A.Hq + hq) * D;
+#pragma unroll
+      for (int d = lane; d < D; d += 32) {
+        float v = 0.f;
+        if (r < R.n) {
+          const unsigned short h = __ldg(qrow + d);
+          v = (A.bf16 ? __bfloat162float(__ushort_as_bfloat16(h)) : __half2float(__ushort_as_half(h))) * A.kappa;
+        }
+        qrows[d * 8 + r] = v;
+      }
+    }
+    __syncthreads();
+    raw_pieces_by_record<D, N, W>(A, L, mw, qrows, pbuf + warp * 256, kst + warp * 32 * (2 * D + 16), w0, w1);
+  } else {
+    raw_pieces_by_channel<D, N, W>(A, L, mw, qrows + warp * 40, b, R, w0, w1);
+  }
+  // ---- merge the warps' pieces, row r by warp r % W
+  __syncthreads();
+  for (int r = warp; r < R.n; r += W) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) M = fmaxf(M, mrg[(w * 8 + r) * MS]);
-    float a = 0.f, L = 0.f;
-    if (M != -INFINITY) {
+    float sc[W], Lr = 0.f;
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float* x = mrg + (w * 8 + r) * MS;
-        const float sc = exp2f(x[0] - M);
-        a = fmaf(x[4 + j], sc, a);
-        L = fmaf(x[1], sc, L);
-      }
+    for (int w = 0; w < W; ++w) {
+      sc[w] = M == -INFINITY ? 0.f : exp2f(mrg[(w * 8 + r) * MS] - M);
+      Lr = fmaf(mrg[(w * 8 + r) * MS + 1], sc[w], Lr);
     }
-    float* part = part_of(A, D, b, R.query(A, r), kvh * A.G + R.head(A, r), A.tile_slots + chunk);
-    part[4 + j] = a;
-    if (j == 0) {
+    float* part = part_of(A, D, b, L.qj(r), L.hq(r), L.slot);
+#pragma unroll
+    for (int j = lane; j < D; j += 32) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) a = fmaf(mrg[(w * 8 + r) * MS + 4 + j], sc[w], a);
+      part[4 + j] = a;
+    }
+    if (lane == 0) {
       part[0] = M;
-      part[1] = L;
+      part[1] = Lr;
     }
   }
-  __syncthreads();  // the scratch is read before the next item writes it
+  __syncthreads();  // the scratch and the query rows are read before the next item writes them
 }
 
 // Resident CTAs per SM the kernel is compiled for: 3 x 4 warps at head_dim
@@ -1163,8 +1375,10 @@ __global__ void __launch_bounds__(W * 32, (decode_min_ctas<D, W, CD>())) decode_
         write_empty(part_of(A, D, b, R.query(A, rr), (x % A.Hkv) * A.G + R.head(A, rr), A.tile_slots + chunk), D,
                     lane);
     } else {
-      tail_partials<D, N, W>(A, smem + S::OFF_RAW_MRG, reinterpret_cast<float*>(smem + S::OFF_QROT) + warp * 40, b,
-                             x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N, committed_end(A, N, len), chunk);
+      tail_partials<D, N, W, (S::RAW_KST > 0)>(A, smem + S::OFF_RAW_MRG, reinterpret_cast<float*>(smem + S::OFF_QROT),
+                                               reinterpret_cast<float*>(smem + S::OFF_RAW_PB), smem + S::OFF_RAW_KST, b,
+                                               x % A.Hkv, RowMap(A, x / A.Hkv), len, A.sink_tiles * N,
+                                               committed_end(A, N, len), chunk);
     }
   }
 
