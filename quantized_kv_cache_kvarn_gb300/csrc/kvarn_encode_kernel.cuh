@@ -652,6 +652,9 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const unsigned 
       reinterpret_cast<uint4*>(pg + L.rope())[k] = __ldg(reinterpret_cast<const uint4*>(s) + k);
     }
   }
+  // a CTA of a cluster exits only after its peer has read its last column
+  // statistics from this CTA's shared memory
+  if constexpr (CS > 1) cg::this_cluster().sync();
 }
 
 // K (4-bit) and V (2-bit) tiles share one launch: blockIdx.z < num_seqs
