@@ -270,6 +270,27 @@ __device__ __forceinline__ RawRow<E> raw_load(const void* p) {
   }
   return r;
 }
+// The same from shared memory.
+template <int E>
+__device__ __forceinline__ RawRow<E> raw_shared(const unsigned char* p) {
+  RawRow<E> r;
+  if constexpr (E == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    r.w[0] = u.x;
+    r.w[1] = u.y;
+  } else {
+    static_assert(E % 8 == 0, "vector width");
+#pragma unroll
+    for (int k = 0; k < E / 8; ++k) {
+      const uint4 u = reinterpret_cast<const uint4*>(p)[k];
+      r.w[4 * k] = u.x;
+      r.w[4 * k + 1] = u.y;
+      r.w[4 * k + 2] = u.z;
+      r.w[4 * k + 3] = u.w;
+    }
+  }
+  return r;
+}
 template <int E>
 __device__ __forceinline__ void raw_floats(const RawRow<E>& r, bool bf16, float* out) {
 #pragma unroll
@@ -485,9 +506,10 @@ __device__ void raw_pieces_by_channel(const DecArgs& A, const RawSplit& L, float
 //  - softmax: per row, the block maximum over the lanes, the rescale of the
 //    running state, base-2 weights; each lane keeps its own partial of the
 //    row sums (one warp sum per row at the end);
-//  - P.V: the weights go through shared memory (`pw`, 1 KB per warp); the
-//    lane owns D / 32 channels of every row's accumulator and walks the
-//    block's records, one coalesced read of each value row.
+//  - P.V: the block's value rows are copied into the staging rows once the
+//    keys are read (the copy runs while the weights are formed), the weights
+//    go through shared memory (`pw`, 1 KB per warp), and the lane owns D / 32
+//    channels of every row's accumulator and walks the block's records.
 template <int D, int N, int W>
 __device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float* mw, const float* qs, float* pw,
                                      unsigned char* kw, int w0, int w1) {
@@ -504,10 +526,10 @@ __device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float*
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
   }
-  // P.V of record j of the block from its value row vr
-  auto pv = [&](const char* vr, int j) {
+  // P.V of record j of the block from its value row, staged in shared memory
+  auto pv = [&](int j) {
     float vf[E];
-    raw_floats<E>(raw_load<E>(vr + 2 * lane * E), A.bf16, vf);
+    raw_floats<E>(raw_shared<E>(kw + j * KROW + 2 * lane * E), A.bf16, vf);
     const float4 pa = *reinterpret_cast<const float4*>(pw + j * 8);
     const float4 pb = *reinterpret_cast<const float4*>(pw + j * 8 + 4);
     const float p8[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
@@ -518,13 +540,16 @@ __device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float*
   };
   for (int blk = w0; blk < w1; blk += 32) {
     const int nrec = min(32, w1 - blk);
-    // the block's key rows, coalesced: 16-byte piece lane + 32 t is piece
-    // (lane + 32 t) % (D / 8) of row (lane + 32 t) / (D / 8)
+    // the block's key (then value) rows, coalesced: 16-byte piece lane + 32 t
+    // is piece (lane + 32 t) % (D / 8) of row (lane + 32 t) / (D / 8)
+    auto stage_rows = [&](bool v) {
 #pragma unroll 4
-    for (int t = 0; t < D / 8; ++t) {
-      const int q = lane + 32 * t, row = q / (D / 8), col = q % (D / 8);
-      if (row < nrec) cp_async16(kw + row * KROW + 16 * col, L.row(A, D, blk + row, false) + 16 * col);
-    }
+      for (int t = 0; t < D / 8; ++t) {
+        const int q = lane + 32 * t, row = q / (D / 8), col = q % (D / 8);
+        if (row < nrec) cp_async16(kw + row * KROW + 16 * col, L.row(A, D, blk + row, v) + 16 * col);
+      }
+    };
+    stage_rows(false);
     cp_async_wait_all();
     __syncwarp();
     const int i = blk + lane;
@@ -558,6 +583,10 @@ __device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float*
         }
       }
     }
+    // every lane is done with its key row: the value rows take their place
+    // while the weights are formed
+    __syncwarp();
+    stage_rows(true);
     const int pos = L.position(i);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -577,21 +606,11 @@ __device__ void raw_pieces_by_record(const DecArgs& A, const RawSplit& L, float*
     // the block's weights to every lane
     *reinterpret_cast<float4*>(pw + lane * 8) = make_float4(s[0], s[1], s[2], s[3]);
     *reinterpret_cast<float4*>(pw + lane * 8 + 4) = make_float4(s[4], s[5], s[6], s[7]);
+    cp_async_wait_all();
     __syncwarp();
-    // the block's value rows: its sink records, then its tail records, each
-    // region contiguous
-    const int ns = min(nrec, max(0, L.n_sink - blk));
-    if (ns > 0) {
-      const char* vr = L.row(A, D, blk, true);
 #pragma unroll 4
-      for (int j = 0; j < ns; ++j) pv(vr + 2 * D * j, j);
-    }
-    if (ns < nrec) {
-      const char* vr = L.row(A, D, blk + ns, true);
-#pragma unroll 4
-      for (int j = ns; j < nrec; ++j) pv(vr + 2 * D * (j - ns), j);
-    }
-    __syncwarp();  // pw and the staged key rows are rewritten by the next block
+    for (int j = 0; j < nrec; ++j) pv(j);
+    __syncwarp();  // pw and the staged rows are rewritten by the next block
   }
 #pragma unroll
   for (int r = 0; r < 8; ++r) l[r] = warp_sum_xor(l[r], 1, 32);
