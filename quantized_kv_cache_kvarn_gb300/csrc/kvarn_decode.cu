@@ -48,7 +48,25 @@ DensePlan plan_dense_stream(int32_t num_seqs, int32_t units_per_seq, int32_t max
   const int64_t want = std::max<int64_t>(in_flight, std::min<int64_t>(4 * in_flight, most / resident));
   p.min_tiles = static_cast<int32_t>((want + in_flight - 1) / in_flight * in_flight);
   p.tile_slots = max_tiles > 0 ? 1 + (max_tiles - 1 + p.min_tiles - 1) / p.min_tiles : 0;
-  p.raw_splits = raw_max > kRawChunk ? (raw_max + kRawChunk - 1) / kRawChunk : 1;
+  // raw tokens per split: the size with the shortest estimated raw phase,
+  // (splits per CTA slot, rounded up) x (tokens of a split + about 96 tokens'
+  // worth of fixed cost per split: its query rows, barriers and merge).
+  // Larger splits cost less each but can leave a few CTAs with two of them.
+  p.raw_chunk = kRawChunk;
+  {
+    int64_t best = -1;
+    for (int32_t ch = kRawChunk; ch <= 16 * kRawChunk; ch *= 2) {
+      const int64_t splits = raw_max > ch ? (raw_max + ch - 1) / ch : 1;
+      const int64_t rounds = (units * splits + resident - 1) / resident;
+      const int64_t cost = rounds * (std::min<int64_t>(ch, std::max(0, raw_max)) + 96);
+      if (best < 0 || cost < best) {
+        best = cost;
+        p.raw_chunk = ch;
+      }
+      if (splits == 1) break;
+    }
+  }
+  p.raw_splits = raw_max > p.raw_chunk ? (raw_max + p.raw_chunk - 1) / p.raw_chunk : 1;
   p.slots = p.tile_slots + p.raw_splits;
   const int64_t tile_ctas = (most + p.min_tiles - 1) / p.min_tiles;
   const int64_t raw_items = units * p.raw_splits;
@@ -189,6 +207,7 @@ cudaError_t launch_decode_dense(const DecodeParams& p, const DensePlan& plan, cu
   A.min_tiles = plan.min_tiles;
   A.tile_slots = plan.tile_slots;
   A.raw_splits = plan.raw_splits;
+  A.raw_chunk = plan.raw_chunk;
   A.slots = plan.slots;
   A.err = p.err;
   A.bf16 = p.bf16 ? 1 : 0;

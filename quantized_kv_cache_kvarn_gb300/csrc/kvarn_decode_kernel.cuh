@@ -176,7 +176,8 @@ struct DecArgs {
   int32_t X;           // work units per sequence: KV heads x row groups
   int32_t min_tiles;   // fewest compressed tiles a CTA takes (bounds the slots a unit needs)
   int32_t tile_slots;  // partial slots reserved for compressed tiles; raw slots follow them
-  int32_t raw_splits;  // raw slots (chunks of kRawChunk raw tokens)
+  int32_t raw_splits;  // raw slots (chunks of raw_chunk raw tokens)
+  int32_t raw_chunk;   // raw tokens per raw split
   int32_t slots;       // tile_slots + raw_splits
   uint32_t* err;
   int32_t partial_tiles;  // uncompressed pages: a sequence's last tile may be partial (tokens past len masked)
@@ -311,7 +312,7 @@ __device__ __forceinline__ void raw_floats(const RawRow<E>& r, bool bf16, float*
 // sink rows [0, min(sink, visible)) and the tail rows for tokens [committed,
 // visible). All rows of the unit share one raw list, the sink rows of the
 // longest row then its tail rows, masked per row by position; raw split
-// `chunk` covers list entries [chunk * kRawChunk, +kRawChunk), cut into W
+// `chunk` covers list entries [chunk * raw_chunk, +raw_chunk), cut into W
 // consecutive pieces, one per warp. Each warp leaves the (max, sum,
 // unnormalised output) of its piece per row in the merge scratch `mrg`
 // (8 rows of merge_stride<D>() floats per warp), and the pieces are merged
@@ -339,8 +340,8 @@ struct RawSplit {
     committed = committed_;
     n_sink = min(sink, vis_max);
     const int n_tail = max(0, vis_max - committed);
-    c0 = chunk * kRawChunk;
-    c1 = min(n_sink + n_tail, c0 + kRawChunk);
+    c0 = chunk * A.raw_chunk;
+    c1 = min(n_sink + n_tail, c0 + A.raw_chunk);
     miss = (c1 > max(c0, n_sink) && (A.tail_k == nullptr || A.tail_v == nullptr)) ||
            (min(c1, n_sink) > c0 && (A.sink_k == nullptr || A.sink_v == nullptr));
     slot = A.tile_slots + chunk;

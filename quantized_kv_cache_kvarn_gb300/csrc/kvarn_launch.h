@@ -125,17 +125,18 @@ struct SplitPlan {
   int32_t slots;   // nsplit + 1 (the tail)
 };
 
-constexpr int32_t kRawChunk = 128;  // raw (sink and tail) tokens per split of the dense decode
+constexpr int32_t kRawChunk = 128;  // smallest split of the raw (sink and tail) records of the dense decode
 
 // Plan of the compressed decode: `ctas` persistent CTAs share the flattened
 // list of compressed tiles (stream-K), each taking at least `min_tiles` of
 // them, so a unit of n tiles writes at most 1 + ceil((n - 1) / min_tiles)
-// tile partials; raw partials (kRawChunk raw tokens each) follow them.
+// tile partials; raw partials (raw_chunk raw tokens each) follow them.
 struct DensePlan {
   int32_t ctas;
   int32_t min_tiles;
   int32_t tile_slots;  // partial slots per row reserved for tiles
   int32_t raw_splits;
+  int32_t raw_chunk;   // raw tokens per raw split (kRawChunk times a power of two)
   int32_t slots;       // tile_slots + raw_splits
 };
 
