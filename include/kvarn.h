@@ -361,7 +361,8 @@ int32_t kvarn_decode_verify(const void* q, int32_t num_q_heads, int32_t num_quer
  *                  sink_tokens and recent_tokens
  * Other arguments as for kvarn_decode_verify. A missing sink or tail buffer
  * that a row needs sets KVARN_DEVERR_NO_TAIL. The raw records are read in
- * splits of 128 tokens, in parallel with the splits over the pages.
+ * splits of 128 to 2048 tokens (chosen from the batch size and the raw
+ * length), in parallel with the splits over the pages.
  */
 int64_t kvarn_decode_window_workspace_bytes(const kvarn_layout* layout, int32_t num_seqs,
                                             int32_t num_q_heads, int32_t num_queries,
