@@ -78,13 +78,20 @@ struct EncodeArgs {
 };
 
 
-// Position of channel c in a per-channel shared buffer written a 16-byte
-// chunk per lane: chunk e (channels 4e..4e+3) of every segment, then chunk
-// e + 1, so that the segments' stores (and reads) of one chunk fill
-// consecutive banks.
+// Per-channel shared buffers are written a 16-byte chunk per lane: lane seg
+// holds channels 16 seg .. 16 seg + 15, its chunk e channels 16 seg + 4e ..
+// + 3. Chunk (e, seg) goes to slot e * (D / 16) + (seg ^ 2e): for one e the
+// lanes' chunks fill consecutive slots (a permutation of them), and the 32
+// consecutive channels a warp reads one per thread fall in 32 different
+// banks (the XOR spreads the four chunks e of one lane over the 128-byte
+// rows). chunk_slot is that slot, chunk_pos the float position of channel c.
+template <int D>
+__device__ __forceinline__ int chunk_slot(int e, int seg) {
+  return e * (D / 16) + (seg ^ (2 * e));
+}
 template <int D>
 __device__ __forceinline__ int chunk_pos(int c) {
-  return (((c & 15) >> 2) * (D / 16) + (c >> 4)) * 4 + (c & 3);
+  return chunk_slot<D>((c & 15) >> 2, c >> 4) * 4 + (c & 3);
 }
 
 // Merge of two (mean, M2) summaries of n values each (Chan, Golub and
@@ -121,8 +128,8 @@ __device__ __forceinline__ float2 column_moments(float2 (&mo)[16], float* red, f
     float4* dv = reinterpret_cast<float4*>(red + (S::NW + warp) * D);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      dm[e * S::TPR + seg] = make_float4(mo[4 * e].x, mo[4 * e + 1].x, mo[4 * e + 2].x, mo[4 * e + 3].x);
-      dv[e * S::TPR + seg] = make_float4(mo[4 * e].y, mo[4 * e + 1].y, mo[4 * e + 2].y, mo[4 * e + 3].y);
+      dm[chunk_slot<D>(e, seg)] = make_float4(mo[4 * e].x, mo[4 * e + 1].x, mo[4 * e + 2].x, mo[4 * e + 3].x);
+      dv[chunk_slot<D>(e, seg)] = make_float4(mo[4 * e].y, mo[4 * e + 1].y, mo[4 * e + 2].y, mo[4 * e + 3].y);
     }
   }
   __syncthreads();
@@ -440,7 +447,7 @@ __device__ __forceinline__ void encode_tile(const EncodeArgs& A, const unsigned 
       const float4* src = reinterpret_cast<const float4*>(colbuf);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float4 f = src[e * S::TPR + seg];
+        const float4 f = src[chunk_slot<D>(e, seg)];
         inv[2 * e] = make_float2(f.x, f.y);
         inv[2 * e + 1] = make_float2(f.z, f.w);
       }
